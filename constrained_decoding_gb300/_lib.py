@@ -1,0 +1,44 @@
+"""ctypes loader of the in-tree PCD library (lib/libpcd.so).
+
+There is no fallback: if the library is missing the import of the package
+raises, and every computation goes through the library's CUDA kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "lib", "libpcd.so")
+
+_lib = None
+
+c_int, c_int64, c_float, c_void_p, c_char_p = ctypes.c_int, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_char_p
+c_int32_p = ctypes.POINTER(ctypes.c_int32)
+c_float_p = ctypes.POINTER(ctypes.c_float)
+
+
+def load() -> ctypes.CDLL:
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"PCD CUDA library not built ({LIB_PATH} missing); "
+                          "run `python -m constrained_decoding_gb300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    _declare(lib)
+    _lib = lib
+    return lib
+
+
+def _sig(lib, name, res, args):
+    f = getattr(lib, name)
+    f.restype = res
+    f.argtypes = args
+
+
+def _declare(lib):
+    _sig(lib, "pcd_k_gemm", c_int, [c_void_p, c_int, c_int, c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_int,
+                                    c_int, c_int, c_int, c_void_p, c_void_p])
+    from . import _decls
+    _decls.declare(lib, _sig)

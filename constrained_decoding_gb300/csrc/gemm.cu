@@ -1,0 +1,451 @@
+// tcgen05 GEMM for sm_103a: D[M][N] = A[M][K] . B[N][K]^T, bf16 in, fp32
+// accumulation in tensor memory (TMEM).
+//
+// One persistent CTA per SM, 6 warps:
+//   warp 0     TMA producer: fills a ring of shared-memory stages, each holding
+//              MT A tiles (128 x 64) and one B tile (BN x 64), 128-byte swizzled;
+//   warp 1     allocates TMEM; one thread issues tcgen05.mma (M=128, N=BN,
+//              K=16) for every A tile against the shared B tile, so one B tile
+//              (the weights) read from HBM feeds MT*128 rows of A;
+//   warps 2-5  epilogue: read the accumulator from TMEM (each warp owns one
+//              32-lane quarter) and apply the fused epilogue.
+// Accumulators are double-buffered in TMEM when MT*BN <= 256, so the epilogue
+// of one work unit overlaps the main loop of the next.
+// A work unit is (N tile, K split, group of MT M tiles), ordered so that the
+// units sharing a B tile run on neighbouring CTAs at the same time and read
+// it from L2.
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "gemm.h"
+#include "ptx.cuh"
+
+namespace pcd {
+
+struct GemmParams {
+  int M, N, K;
+  int n_mgroups, n_ntiles, k_splits, n_units, nkb;
+  uint64_t wait_ns;
+  int* err;
+  int b_evict_first;  // B is read by one M group only: stream it past L2
+};
+
+template <int MT, int BN>
+struct GemmCfg {
+  static constexpr int A_BYTES = 128 * 128;  // 128 rows x 64 bf16
+  static constexpr int B_BYTES = BN * 128;
+  static constexpr int STAGE_BYTES = MT * A_BYTES + B_BYTES;
+  static constexpr int SMEM_BUDGET = 227 * 1024 - 2048;
+  static constexpr int STAGES_RAW = SMEM_BUDGET / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  static constexpr int ACC_COLS = MT * BN;
+  static constexpr int ACC_STAGES = (2 * ACC_COLS <= 512) ? 2 : 1;
+  static constexpr int TMEM_COLS_RAW = ACC_STAGES * ACC_COLS;
+  static constexpr int TMEM_COLS = TMEM_COLS_RAW <= 32    ? 32
+                                   : TMEM_COLS_RAW <= 64  ? 64
+                                   : TMEM_COLS_RAW <= 128 ? 128
+                                   : TMEM_COLS_RAW <= 256 ? 256
+                                                          : 512;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align slack*/ + 256 /*barriers*/;
+  static_assert(ACC_STAGES * ACC_COLS <= 512, "accumulator does not fit in TMEM");
+  static_assert(STAGES >= 2, "need at least two pipeline stages");
+};
+
+__device__ __forceinline__ void decode_unit(const GemmParams& p, int u, int& nt, int& mg, int& ks) {
+  mg = u % p.n_mgroups;
+  const int rest = u / p.n_mgroups;
+  ks = rest % p.k_splits;
+  nt = rest / p.k_splits;
+}
+
+template <int EPI>
+__device__ __forceinline__ void epi_chunk(const GemmParams& p, const EpiArgs& e, int row, int col0, const float* v,
+                                          float& run_m, float& run_s) {
+  if constexpr (EPI == EPI_READOUT) {
+    // online max / sum-exp over the valid vocabulary columns of this chunk
+    float cm = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (col0 + i < p.N) cm = fmaxf(cm, v[i]);
+    const float nm = fmaxf(run_m, cm);
+    float acc = (run_m == -INFINITY) ? 0.f : run_s * __expf(run_m - nm);
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (col0 + i < p.N) acc += __expf(v[i] - nm);
+    run_m = nm;
+    run_s = acc;
+  } else {
+    if (row >= p.M) return;
+    if constexpr (EPI == EPI_BF16) {
+      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(e.out) + static_cast<size_t>(row) * e.ldo + col0;
+      uint4* o4 = reinterpret_cast<uint4*>(o);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        uint4 w;
+        w.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
+        w.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
+        w.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
+        w.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+        o4[j] = w;
+      }
+    } else if constexpr (EPI == EPI_F32_ADD) {
+      float4* o4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(e.out) + static_cast<size_t>(row) * e.ldo + col0);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float4 a = o4[j];
+        a.x += v[4 * j + 0];
+        a.y += v[4 * j + 1];
+        a.z += v[4 * j + 2];
+        a.w += v[4 * j + 3];
+        o4[j] = a;
+      }
+    } else if constexpr (EPI == EPI_F32_ATOMIC) {
+      float4* o4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(e.out) + static_cast<size_t>(row) * e.ldo + col0);
+#pragma unroll
+      for (int j = 0; j < 8; ++j)
+        atomicAdd(o4 + j, make_float4(v[4 * j + 0], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+    } else if constexpr (EPI == EPI_SWIGLU) {
+      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(e.out) + static_cast<size_t>(row) * e.ldo + col0 / 2;
+      uint4* o4 = reinterpret_cast<uint4*>(o);
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float h[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) h[i] = silu_f(v[16 * j + 2 * i]) * v[16 * j + 2 * i + 1];
+        uint4 w;
+        w.x = pack_bf16x2(h[0], h[1]);
+        w.y = pack_bf16x2(h[2], h[3]);
+        w.z = pack_bf16x2(h[4], h[5]);
+        w.w = pack_bf16x2(h[6], h[7]);
+        o4[j] = w;
+      }
+    }
+  }
+}
+
+template <int MT, int BN, int EPI>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p, const EpiArgs e) {
+  using C = GemmCfg<MT, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + C::ACC_STAGES;
+  uint64_t* drain = tempty + C::ACC_STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < C::ACC_STAGES; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tbase = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      const uint64_t pol_b = p.b_evict_first ? l2_policy_evict_first() : l2_policy_evict_last();
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t last_phase[8];
+      bool issued[8];
+      for (int s = 0; s < 8; ++s) issued[s] = false, last_phase[s] = 0;
+      for (int u = blockIdx.x; u < p.n_units && !*abort_flag; u += gridDim.x) {
+        int nt, mg, ks;
+        decode_unit(p, u, nt, mg, ks);
+        const int kb0 = ks * p.nkb / p.k_splits, kb1 = (ks + 1) * p.nkb / p.k_splits;
+        const int mt_valid = min(MT, (p.M - mg * MT * 128 + 127) / 128);
+        const uint32_t bytes = mt_valid * C::A_BYTES + C::B_BYTES;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns)) {
+            record_error(p.err, DEV_WAIT_TIMEOUT_PRODUCER);
+            *abort_flag = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          uint8_t* base = smem + stage * C::STAGE_BYTES;
+          for (int mt = 0; mt < mt_valid; ++mt)
+            tma_load_2d(base + mt * C::A_BYTES, &tmA, &full[stage], kb * 64, (mg * MT + mt) * 128);
+          tma_load_2d_hint(base + MT * C::A_BYTES, &tmB, &full[stage], kb * 64, nt * BN, pol_b);
+          issued[stage] = true;
+          last_phase[stage] = phase;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+      if (*abort_flag) {
+        // let every copy still in flight land before the CTA exits
+        for (int s = 0; s < C::STAGES; ++s)
+          if (issued[s]) mbar_wait(&full[s], last_phase[s], p.wait_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      constexpr uint32_t IDESC = idesc_bf16_f32(128, BN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool any = false;
+      for (int u = blockIdx.x; u < p.n_units && !*abort_flag; u += gridDim.x) {
+        int nt, mg, ks;
+        decode_unit(p, u, nt, mg, ks);
+        const int kb0 = ks * p.nkb / p.k_splits, kb1 = (ks + 1) * p.nkb / p.k_splits;
+        const int mt_valid = min(MT, (p.M - mg * MT * 128 + 127) / 128);
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, p.wait_ns)) {
+          record_error(p.err, DEV_WAIT_TIMEOUT_MMA);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_base = tbase + acc * C::ACC_COLS;
+        bool ok = true;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&full[stage], phase, p.wait_ns)) {
+            record_error(p.err, DEV_WAIT_TIMEOUT_MMA);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a_base = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint32_t b_base = a_base + MT * C::A_BYTES;
+          for (int mt = 0; mt < mt_valid; ++mt) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              umma_bf16(d_base + mt * BN, sdesc_kmajor_sw128(a_base + mt * C::A_BYTES + k * 32),
+                        sdesc_kmajor_sw128(b_base + k * 32), IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+            }
+          }
+          umma_commit(&empty[stage]);
+          any = true;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        if (++acc == C::ACC_STAGES) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      // every MMA must be finished before TMEM is released
+      if (any) {
+        umma_commit(drain);
+        if (!mbar_wait(drain, 0, p.wait_ns)) record_error(p.err, DEV_WAIT_TIMEOUT_DRAIN);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = blockIdx.x; u < p.n_units && !*abort_flag; u += gridDim.x) {
+      int nt, mg, ks;
+      decode_unit(p, u, nt, mg, ks);
+      const int mt_valid = min(MT, (p.M - mg * MT * 128 + 127) / 128);
+      if (!mbar_wait(&tfull[acc], acc_phase, p.wait_ns)) {
+        record_error(p.err, DEV_WAIT_TIMEOUT_EPILOGUE);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after_sync();
+      for (int mt = 0; mt < mt_valid; ++mt) {
+        const int row = (mg * MT + mt) * 128 + q * 32 + lane;
+        const uint32_t t_row = tbase + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS + mt * BN;
+        float run_m = -INFINITY, run_s = 0.f;
+        for (int c = 0; c < BN / 32; ++c) {
+          const int col0 = nt * BN + c * 32;
+          if (col0 >= p.N) break;  // uniform across the warp
+          float v[32];
+          tmem_ld_32cols(t_row + c * 32, v);
+          epi_chunk<EPI>(p, e, row, col0, v, run_m, run_s);
+        }
+        if constexpr (EPI == EPI_READOUT) {
+          if (row < p.M) e.part[static_cast<size_t>(nt) * p.M + row] = make_float2(run_m, run_s);
+          // gathered logits: entries are sorted by N tile; the loop is uniform per warp
+          const int g0 = e.gather_off[nt], g1 = e.gather_off[nt + 1];
+          for (int g = g0; g < g1; ++g) {
+            const int4 en = e.gather[g];
+            const int r = en.y;
+            if (r / 128 != mg * MT + mt || ((r & 127) >> 5) != q) continue;
+            const float z = tmem_ld_1col(t_row + en.x);
+            if (lane == (r & 31)) e.z_out[en.z] = z;
+          }
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive(&tempty[acc]);
+      if (++acc == C::ACC_STAGES) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tbase, C::TMEM_COLS);
+  }
+}
+
+// ====================================================================== host
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static std::once_flag g_encode_once;
+
+bool tma_init() {
+  std::call_once(g_encode_once, [] {
+    cudaDriverEntryPointQueryResult q;
+    void* fn = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// bf16 matrix [rows][>= cols], row stride ld elements; box 64 (K) x box_rows.
+static bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int ld, int box_rows) {
+  if (!tma_init()) return false;
+  if ((reinterpret_cast<uintptr_t>(ptr) & 15) || (ld * 2) % 16) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
+  cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int MT, int BN, int EPI>
+static int launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p, const EpiArgs& e,
+                    cudaStream_t st, int sms) {
+  using C = GemmCfg<MT, BN>;
+  auto kern = gemm_tc_kernel<MT, BN, EPI>;
+  static bool attr_set = false;  // per instantiation
+  if (!attr_set) {
+    cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (r != cudaSuccess) return r;
+    attr_set = true;
+  }
+  const int grid = std::min(p.n_units, sms);
+  kern<<<grid, 192, C::SMEM_BYTES, st>>>(ma, mb, p, e);
+  return cudaGetLastError();
+}
+
+template <int EPI>
+static int dispatch_tiling(const GemmTiling& t, const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p,
+                           const EpiArgs& e, cudaStream_t st, int sms) {
+  if (t.mt == 1 && t.bn == 128) return launch_t<1, 128, EPI>(ma, mb, p, e, st, sms);
+  if (t.mt == 1 && t.bn == 256) return launch_t<1, 256, EPI>(ma, mb, p, e, st, sms);
+  if (t.mt == 2 && t.bn == 128) return launch_t<2, 128, EPI>(ma, mb, p, e, st, sms);
+  if (t.mt == 2 && t.bn == 256) return launch_t<2, 256, EPI>(ma, mb, p, e, st, sms);
+  if (t.mt == 4 && t.bn == 128) return launch_t<4, 128, EPI>(ma, mb, p, e, st, sms);
+  return -1;
+}
+
+int launch_gemm(const GemmShape& s, int epi, const EpiArgs& e, const GemmTiling& t, cudaStream_t stream, int* dev_err,
+                uint64_t wait_ns, int sms) {
+  const int M = s.a_rows, N = s.b_rows, K = s.K;
+  if (M <= 0 || N <= 0) return 0;
+  if (K <= 0 || K % 64 || N % 32) return -1;
+  if (t.splits > 1 && epi != EPI_F32_ATOMIC) return -1;
+  GemmParams p;
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.nkb = K / 64;
+  p.n_mgroups = ceil_div(M, 128 * t.mt);
+  p.n_ntiles = ceil_div(N, t.bn);
+  p.k_splits = std::max(1, std::min(t.splits, p.nkb));
+  p.n_units = p.n_mgroups * p.n_ntiles * p.k_splits;
+  p.wait_ns = wait_ns;
+  p.err = dev_err;
+  p.b_evict_first = p.n_mgroups == 1 ? 1 : 0;
+  CUtensorMap ma, mb;
+  if (!make_map(&ma, s.a, M, K, s.a_ld, 128)) return -1;
+  if (!make_map(&mb, s.b, N, K, s.b_ld, t.bn)) return -1;
+  switch (epi) {
+    case EPI_BF16: return dispatch_tiling<EPI_BF16>(t, ma, mb, p, e, stream, sms);
+    case EPI_F32_ADD: return dispatch_tiling<EPI_F32_ADD>(t, ma, mb, p, e, stream, sms);
+    case EPI_F32_ATOMIC: return dispatch_tiling<EPI_F32_ATOMIC>(t, ma, mb, p, e, stream, sms);
+    case EPI_SWIGLU: return dispatch_tiling<EPI_SWIGLU>(t, ma, mb, p, e, stream, sms);
+    case EPI_READOUT: return dispatch_tiling<EPI_READOUT>(t, ma, mb, p, e, stream, sms);
+  }
+  return -1;
+}
+
+// Tiling heuristic.  Work units are (N tile, K split, M group); every unit
+// streams its B tile slice once and reuses it for MT*128 rows of A.  The
+// estimate charges each wave of units the larger of its tensor time and its
+// shared-memory fill time, plus a fixed pipeline fill / epilogue cost.
+GemmTiling choose_tiling(int M, int N, int K, int epi, int sms) {
+  static const int cand[5][2] = {{1, 128}, {1, 256}, {2, 128}, {2, 256}, {4, 128}};
+  const int nkb = K / 64;
+  GemmTiling best;
+  double best_t = 1e30;
+  for (auto& c : cand) {
+    const int mt = c[0], bn = c[1];
+    const int mg = ceil_div(M, 128 * mt);
+    const int nt = ceil_div(N, bn);
+    const int max_split = (epi == EPI_F32_ATOMIC) ? std::max(1, nkb / 4) : 1;
+    for (int sp = 1; sp <= max_split; sp *= 2) {
+      const int units = mg * nt * sp;
+      const int waves = ceil_div(units, sms);
+      const int kbs = ceil_div(nkb, sp);
+      const int rows = std::min(mt * 128, ceil_div(M, 128) * 128);
+      // tensor cycles per k-block: rows x bn x 64 x 2 flop at ~8192 flop/clk/SM
+      const double mma = static_cast<double>(rows) * bn * 128.0 / 8192.0;
+      // bytes per k-block into smem at ~128 B/clk/SM
+      const double fill = (rows * 128.0 + bn * 128.0) / 128.0;
+      const double per_unit = kbs * std::max(mma, fill) + 1500.0 + (sp > 1 ? 300.0 : 0.0);
+      const double tt = waves * per_unit;
+      if (tt < best_t) {
+        best_t = tt;
+        best.mt = mt;
+        best.bn = bn;
+        best.splits = sp;
+      }
+    }
+  }
+  return best;
+}
+
+}  // namespace pcd

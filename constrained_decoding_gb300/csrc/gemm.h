@@ -1,0 +1,53 @@
+// Host interface of the tcgen05 GEMM: D = A . B^T with A [M][K] and B [N][K]
+// bf16, both K-contiguous, fp32 accumulation in tensor memory, and one of a
+// few fused epilogues.
+#pragma once
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace pcd {
+
+enum EpiKind : int {
+  EPI_BF16 = 0,        // out bf16 [M][ldo] = D
+  EPI_F32_ADD = 1,     // out f32 [M][ldo] += D (one K split: plain read-modify-write)
+  EPI_F32_ATOMIC = 2,  // out f32 [M][ldo] += D with atomics (any number of K splits)
+  EPI_SWIGLU = 3,      // D columns (2f, 2f+1) = (gate_f, up_f); out bf16 [M][ldo]: silu(gate) * up
+  EPI_READOUT = 4,     // vocabulary readout: per (row, N tile) max and sum-exp, plus gathered logits
+};
+
+struct GemmShape {
+  const void* a; int a_rows; int a_ld;   // A: a_rows x K, leading dim in elements
+  const void* b; int b_rows; int b_ld;   // B: b_rows x K
+  int K;
+};
+
+struct EpiArgs {
+  void* out = nullptr;            // output base (bf16 or f32)
+  int ldo = 0;                    // leading dimension of out, in elements
+  float2* part = nullptr;         // EPI_READOUT: [n_tiles_n][M] (max, sum exp(z - max))
+  const int* gather_off = nullptr;  // EPI_READOUT: [n_tiles_n + 1] CSR over gather entries
+  const int4* gather = nullptr;   // EPI_READOUT: (column in tile, row, output index, 0)
+  float* z_out = nullptr;         // EPI_READOUT: gathered logits
+};
+
+struct GemmTiling {
+  int mt = 1;       // 128-row M tiles per CTA work unit (1, 2 or 4)
+  int bn = 256;     // N tile (128 or 256)
+  int splits = 1;   // K splits (EPI_F32_ATOMIC only when > 1)
+};
+
+// Picks a tiling for the shape and epilogue on an `sms`-SM device.
+GemmTiling choose_tiling(int M, int N, int K, int epi, int sms);
+
+// Number of N tiles for a tiling (the readout partial array's first dimension).
+inline int gemm_n_tiles(int N, const GemmTiling& t) { return (N + t.bn - 1) / t.bn; }
+
+// Launches D = A . B^T with the epilogue on `stream`.  Returns a cudaError_t
+// value (0 on success); -1 for an invalid shape or tiling.
+int launch_gemm(const GemmShape& s, int epi, const EpiArgs& e, const GemmTiling& t, cudaStream_t stream,
+                int* dev_err, uint64_t wait_ns, int sms);
+
+// Loads cuTensorMapEncodeTiled from the driver; false if it is unavailable.
+bool tma_init();
+
+}  // namespace pcd

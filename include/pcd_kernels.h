@@ -1,0 +1,38 @@
+/* Kernel-level entry points of the PCD library, for testing one device step
+ * in isolation against the CPU oracle.  Every pointer is a DEVICE pointer the
+ * caller owns; nothing is allocated or freed here.  Each call is enqueued on
+ * `stream` (a cudaStream_t, NULL = legacy default stream) and returns without
+ * synchronising.  Return value: 0 on success, a negative PCD_ERR_* code
+ * (pcd.h) for invalid arguments, or PCD_ERR_CUDA when the launch fails.
+ */
+#ifndef PCD_KERNELS_H
+#define PCD_KERNELS_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Epilogue kinds of pcd_k_gemm. */
+#define PCD_EPI_BF16 0       /* out bf16 [M][ldo] = A.B^T                                   */
+#define PCD_EPI_F32_ADD 1    /* out f32 [M][ldo] += A.B^T (splits must be 1)                */
+#define PCD_EPI_F32_ATOMIC 2 /* out f32 [M][ldo] += A.B^T with atomics (any splits)         */
+#define PCD_EPI_SWIGLU 3     /* out bf16 [M][ldo]: col f = silu(D[:,2f]) * D[:,2f+1]        */
+
+/* Dense projection on the tensor cores: D[M][N] = A[M][K] . B[N][K]^T with
+ * bf16 A and B (row-major, K contiguous, leading dimensions lda/ldb in
+ * elements, multiples of 8), fp32 accumulation and a fused epilogue.  This is
+ * the contraction of every QKV, output and SwiGLU projection of the decoder
+ * (configs: nn.Linear weights [out][in] as B, activations [tokens][in] as A).
+ * K must be a multiple of 64, N a multiple of 32.  mt/bn/splits force a
+ * tiling (mt in {1,2,4}, bn in {128,256}); mt = 0 lets the library choose.
+ * `dev_err` (device int, may be NULL) receives a nonzero code if a pipeline
+ * wait times out. */
+int pcd_k_gemm(const void* a, int M, int lda, const void* b, int N, int ldb, int K, int epi, void* out, int ldo,
+               int mt, int bn, int splits, int* dev_err, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

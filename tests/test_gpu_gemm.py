@@ -1,0 +1,75 @@
+"""The tcgen05 GEMM against a plain fp32 matmul of the same bf16 operands."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+
+def _lib():
+    import constrained_decoding_gb300 as pcd
+    return pcd.load()
+
+
+def _ref(a, b):
+    return a.float().cpu() @ b.float().cpu().T
+
+
+def _run(M, N, K, epi, mt, bn, splits, seed=0):
+    lib = _lib()
+    g = torch.Generator().manual_seed(seed)
+    a = (torch.randn(M, K, generator=g) * 0.5).to(torch.bfloat16).cuda()
+    b = (torch.randn(N, K, generator=g) * 0.05).to(torch.bfloat16).cuda()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    if epi == 0:
+        out = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
+    elif epi == 3:
+        out = torch.zeros(M, N // 2, dtype=torch.bfloat16, device="cuda")
+    else:
+        out = torch.full((M, N), 0.25, dtype=torch.float32, device="cuda")
+    rc = lib.pcd_k_gemm(a.data_ptr(), M, K, b.data_ptr(), N, K, K, epi, out.data_ptr(), out.shape[1],
+                        mt, bn, splits, err.data_ptr(), s)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    ref = _ref(a, b)
+    if epi == 0:
+        return out.float().cpu(), ref, 1e-2
+    if epi == 3:
+        g_, u_ = ref[:, 0::2], ref[:, 1::2]
+        return out.float().cpu(), torch.nn.functional.silu(g_) * u_, 2e-2
+    return out.cpu(), ref + 0.25, 1e-3
+
+
+@pytest.mark.parametrize("M,N,K,mt,bn", [
+    (128, 128, 64, 1, 128),      # one tile, one k-block
+    (128, 256, 128, 1, 256),
+    (200, 384, 320, 1, 128),     # ragged M, several tiles
+    (333, 512, 1536, 2, 256),    # the branch-pass shape class
+    (512, 640, 256, 4, 128),
+    (77, 256, 192, 2, 128),      # M smaller than one group
+])
+def test_gemm_bf16_store(M, N, K, mt, bn):
+    out, ref, tol = _run(M, N, K, 0, mt, bn, 1)
+    err = (out - ref).abs().max().item()
+    assert err < tol * max(1.0, ref.abs().max().item()), err
+
+
+@pytest.mark.parametrize("splits", [1, 3, 8])
+def test_gemm_f32_accumulate(splits):
+    epi = 1 if splits == 1 else 2
+    out, ref, tol = _run(300, 256, 1024, epi, 1, 128, splits, seed=1)
+    assert (out - ref).abs().max().item() < tol
+
+
+def test_gemm_swiglu():
+    out, ref, tol = _run(150, 512, 256, 3, 2, 256, 1, seed=2)
+    assert (out - ref).abs().max().item() < tol
+
+
+def test_gemm_auto_tiling_large():
+    out, ref, tol = _run(332, 2048, 1536, 2, 0, 0, 0, seed=3)
+    assert (out - ref).abs().max().item() < 1e-3
