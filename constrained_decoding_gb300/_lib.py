@@ -38,7 +38,5 @@ def _sig(lib, name, res, args):
 
 
 def _declare(lib):
-    _sig(lib, "pcd_k_gemm", c_int, [c_void_p, c_int, c_int, c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_int,
-                                    c_int, c_int, c_int, c_void_p, c_void_p])
     from . import _decls
     _decls.declare(lib, _sig)

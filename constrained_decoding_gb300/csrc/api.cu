@@ -1,0 +1,1168 @@
+// The PCD library: model loading, the prefill and branch-pass executors, and
+// the C ABI of include/pcd.h.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <chrono>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <map>
+#include <string>
+#include <tuple>
+#include <vector>
+
+#include "common.cuh"
+#include "gemm.h"
+#include "kernels.h"
+#include "pcd.h"
+#include "plan.h"
+
+using pcd::bf16;
+
+// ============================================================ error reporting
+namespace {
+thread_local std::string g_last_error;
+
+int fail(int code, const std::string& msg) {
+  g_last_error = msg;
+  return code;
+}
+}  // namespace
+
+#define PCD_CUDA(x)                                                                                   \
+  do {                                                                                                \
+    cudaError_t e_ = (x);                                                                             \
+    if (e_ != cudaSuccess) return fail(PCD_ERR_CUDA, std::string(#x) + ": " + cudaGetErrorString(e_)); \
+  } while (0)
+
+#define PCD_LAUNCH(x)                                                                                          \
+  do {                                                                                                         \
+    int e_ = (x);                                                                                              \
+    if (e_ != 0)                                                                                               \
+      return fail(e_ < 0 ? PCD_ERR_SHAPE_MISMATCH : PCD_ERR_CUDA,                                              \
+                  std::string(#x) + ": " + (e_ > 0 ? cudaGetErrorString(static_cast<cudaError_t>(e_)) : "bad shape")); \
+  } while (0)
+
+#define PCD_TRY(x)          \
+  do {                      \
+    int e_ = (x);           \
+    if (e_ != PCD_OK) return e_; \
+  } while (0)
+
+// ================================================================ structures
+namespace {
+
+struct DevBuf {
+  void* p = nullptr;
+  size_t n = 0;
+};
+
+int ensure(DevBuf& b, size_t bytes) {
+  if (bytes <= b.n) return PCD_OK;
+  if (b.p) cudaFree(b.p);
+  b.p = nullptr;
+  b.n = 0;
+  bytes = std::max<size_t>(bytes, 256);
+  if (cudaMalloc(&b.p, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    return fail(PCD_ERR_OOM, "device allocation of " + std::to_string(bytes) + " bytes failed");
+  }
+  b.n = bytes;
+  return PCD_OK;
+}
+
+struct Layer {
+  bf16 *wqkv, *wo, *wgu, *wd;
+  float *attn_norm, *mlp_norm;
+};
+
+// Device view of a compiled branch batch (all pointers into one int32 blob).
+struct PlanView {
+  int n_fields = 0, T = 0, R = 0, n_children = 0, n_labels = 0, max_rel = 0;
+  int n_vtiles = 0;
+  pcd::GemmTiling ro_tiling;
+  const int32_t *tok, *rel, *anc_off, *anc_idx, *ro_tok, *row_ch, *child_row, *lab_off, *path, *fld_lab, *fld_root,
+      *gather_off;
+  const float* temp;
+  const int4* gather;
+  int result_floats() const { return n_fields * 8 + 2 * n_labels; }
+};
+
+enum ProfClass { PROF_GEMM_PREFILL = 0, PROF_GEMM_BRANCH = 1, PROF_ATTN_PREFILL = 2, PROF_ATTN_BRANCH = 3,
+                 PROF_READOUT = 4, PROF_OTHER = 5 };
+
+}  // namespace
+
+struct pcd_model {
+  pcd_model_config cfg{};
+  int L = 0, d = 0, Hq = 0, Hkv = 0, dh = 0, G = 0, F = 0, Fp = 0, V = 0, Nqkv = 0, qdim = 0, kvdim = 0;
+  int max_pos = 0;
+  cudaStream_t stream = nullptr;
+  int sms = 1;
+  void* wblob = nullptr;
+  float* fblob = nullptr;
+  std::vector<Layer> layers;
+  bf16* embed = nullptr;
+  bf16* lm = nullptr;
+  float* final_norm = nullptr;
+  float2* rope = nullptr;
+  int* d_err = nullptr;
+  uint64_t wait_ns = 2000000000ull;
+  DevBuf x32, xn, qkv, q, kb, vb, att, hb, part_o, part_ml, hr, ro_part, z, lse, plan_buf, result, ids;
+  // pinned staging: `up` feeds host->device copies (reused only once the last
+  // copy from it has completed: up_ev), `down` receives results
+  void* up = nullptr;
+  size_t up_n = 0;
+  void* down = nullptr;
+  size_t down_n = 0;
+  cudaEvent_t up_ev = nullptr;
+  bool up_pending = false;
+  std::map<std::tuple<int, int, int, int>, pcd::GemmTiling> tilings;
+  std::vector<std::pair<size_t, void*>> cache_pool;
+  bool prof = false;
+  std::vector<cudaEvent_t> ev_pool;
+  size_t ev_next = 0;
+  std::vector<std::tuple<int, cudaEvent_t, cudaEvent_t>> prof_rec;
+  cudaEvent_t ev_a = nullptr, ev_b = nullptr, ev_c = nullptr;
+};
+
+struct pcd_cache {
+  pcd_model* m = nullptr;
+  void* mem = nullptr;
+  size_t bytes = 0;
+  int len = 0, cap = 0;
+  bf16* k = nullptr;  // [L][Hkv][cap][dh]
+  bf16* v = nullptr;
+};
+
+struct pcd_plan {
+  pcd_model* m = nullptr;
+  void* mem = nullptr;
+  PlanView view;
+};
+
+namespace {
+
+// ----------------------------------------------------------------- helpers
+int ensure_pinned(void*& buf, size_t& cap, size_t bytes) {
+  if (bytes <= cap) return PCD_OK;
+  if (buf) cudaFreeHost(buf);
+  buf = nullptr;
+  cap = 0;
+  if (cudaMallocHost(&buf, bytes) != cudaSuccess) {
+    cudaGetLastError();
+    buf = nullptr;
+    return fail(PCD_ERR_OOM, "pinned host allocation failed");
+  }
+  cap = bytes;
+  return PCD_OK;
+}
+
+// Copies `bytes` of host data to `dst` on the model stream through the pinned
+// upload buffer.
+int upload_async(pcd_model* m, void* dst, const void* src, size_t bytes) {
+  if (m->up_pending) {
+    cudaEventSynchronize(m->up_ev);
+    m->up_pending = false;
+  }
+  PCD_TRY(ensure_pinned(m->up, m->up_n, bytes));
+  std::memcpy(m->up, src, bytes);
+  PCD_CUDA(cudaMemcpyAsync(dst, m->up, bytes, cudaMemcpyHostToDevice, m->stream));
+  cudaEventRecord(m->up_ev, m->stream);
+  m->up_pending = true;
+  return PCD_OK;
+}
+
+cudaEvent_t next_event(pcd_model* m) {
+  if (m->ev_next == m->ev_pool.size()) {
+    cudaEvent_t e;
+    cudaEventCreate(&e);
+    m->ev_pool.push_back(e);
+  }
+  return m->ev_pool[m->ev_next++];
+}
+
+// Runs `launch` on the model stream, bracketed by events when profiling.
+template <class Fn>
+int timed(pcd_model* m, int cls, Fn&& launch) {
+  cudaEvent_t a = nullptr, b = nullptr;
+  if (m->prof) {
+    a = next_event(m);
+    b = next_event(m);
+    cudaEventRecord(a, m->stream);
+  }
+  const int r = launch();
+  if (m->prof) {
+    cudaEventRecord(b, m->stream);
+    m->prof_rec.emplace_back(cls, a, b);
+  }
+  return r;
+}
+
+// D = A . B^T into `out` with the epilogue family `epi`:
+//   EPI_F32_ADD    residual += (split-K with atomics when the tiling splits K)
+//   EPI_F32_STORE  out = (zeroed + atomics when split)
+//   EPI_SWIGLU / EPI_BF16: one K split
+int gemm(pcd_model* m, int cls, const void* A, int M, int lda, const bf16* B, int N, int ldb, int K, int epi, void* out,
+         int ldo) {
+  if (M <= 0) return PCD_OK;
+  const bool splittable = (epi == pcd::EPI_F32_ADD || epi == pcd::EPI_F32_STORE);
+  const int key_epi = splittable ? pcd::EPI_F32_ATOMIC : epi;
+  auto key = std::make_tuple(M, N, K, key_epi);
+  auto it = m->tilings.find(key);
+  pcd::GemmTiling t;
+  if (it == m->tilings.end()) {
+    t = pcd::choose_tiling(M, N, K, key_epi, m->sms);
+    m->tilings[key] = t;
+  } else {
+    t = it->second;
+  }
+  int run_epi = epi;
+  if (splittable && t.splits > 1) {
+    if (epi == pcd::EPI_F32_STORE)
+      PCD_CUDA(cudaMemsetAsync(out, 0, static_cast<size_t>(M) * ldo * sizeof(float), m->stream));
+    run_epi = pcd::EPI_F32_ATOMIC;
+  }
+  pcd::GemmShape s{A, M, lda, B, N, ldb, K};
+  pcd::EpiArgs e;
+  e.out = out;
+  e.ldo = ldo;
+  PCD_LAUNCH(timed(m, cls, [&] { return pcd::launch_gemm(s, run_epi, e, t, m->stream, m->d_err, m->wait_ns, m->sms); }));
+  return PCD_OK;
+}
+
+int ensure_workspace(pcd_model* m, int T) {
+  const size_t t = static_cast<size_t>(std::max(T, 1));
+  PCD_TRY(ensure(m->x32, t * m->d * 4));
+  PCD_TRY(ensure(m->xn, t * m->d * 2));
+  PCD_TRY(ensure(m->qkv, t * m->Nqkv * 4));
+  PCD_TRY(ensure(m->q, t * m->qdim * 2));
+  PCD_TRY(ensure(m->att, t * m->qdim * 2));
+  PCD_TRY(ensure(m->hb, t * m->Fp * 2));
+  return PCD_OK;
+}
+
+// -------------------------------------------------------------- prefill pass
+// Tokens ids[0..n) at positions p0..p0+n-1 of cache c (rows p0.. are written).
+int run_prefill(pcd_model* m, const int32_t* d_ids, int n, pcd_cache* c, int p0) {
+  PCD_TRY(ensure_workspace(m, n));
+  float* x = static_cast<float*>(m->x32.p);
+  bf16* xn = static_cast<bf16*>(m->xn.p);
+  float* qkv = static_cast<float*>(m->qkv.p);
+  bf16* q = static_cast<bf16*>(m->q.p);
+  bf16* att = static_cast<bf16*>(m->att.p);
+  bf16* hb = static_cast<bf16*>(m->hb.p);
+  const size_t layer_kv = static_cast<size_t>(m->Hkv) * c->cap * m->dh;
+  PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_embed(d_ids, n, m->embed, m->d, m->V, x, m->d_err, m->stream); }));
+  for (int l = 0; l < m->L; ++l) {
+    const Layer& W = m->layers[l];
+    PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
+      return pcd::launch_rmsnorm(x, m->d, nullptr, n, m->d, W.attn_norm, m->cfg.rms_eps, xn, m->d, m->stream);
+    }));
+    PCD_TRY(gemm(m, PROF_GEMM_PREFILL, xn, n, m->d, W.wqkv, m->Nqkv, m->d, m->d, pcd::EPI_F32_STORE, qkv, m->Nqkv));
+    pcd::RopeArgs ra;
+    ra.qkv = qkv;
+    ra.ldqkv = m->Nqkv;
+    ra.n = n;
+    ra.Hq = m->Hq;
+    ra.Hkv = m->Hkv;
+    ra.DH = m->dh;
+    ra.cs = m->rope;
+    ra.max_pos = m->max_pos;
+    ra.rel = nullptr;
+    ra.base = p0;
+    ra.q = q;
+    ra.k_dst = c->k + l * layer_kv;
+    ra.v_dst = c->v + l * layer_kv;
+    ra.kv_head_stride = c->cap;
+    ra.kv_row0 = p0;
+    ra.err = m->d_err;
+    PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_rope_kv(ra, m->stream); }));
+    // The last layer's attention output and MLP change no cached key or value.
+    if (l == m->L - 1) break;
+    pcd::AttnArgs aa{};
+    aa.q = q;
+    aa.n_tok = n;
+    aa.Hq = m->Hq;
+    aa.Hkv = m->Hkv;
+    aa.DH = m->dh;
+    aa.tok0 = 0;
+    aa.part_rows = n * m->G;
+    aa.k = c->k + l * layer_kv;
+    aa.v = c->v + l * layer_kv;
+    aa.kv_head_stride = c->cap;
+    aa.n_keys = p0 + n;
+    aa.rel = nullptr;
+    aa.base = p0;
+    aa.n_splits = 1;
+    aa.split_len = ((p0 + n + 63) / 64) * 64;
+    aa.scale_log2 = 1.4426950408889634f / std::sqrt(static_cast<float>(m->dh));
+    aa.out = att;
+    aa.ld_out = m->qdim;
+    aa.partial = 0;
+    aa.causal_heavy_first = 1;
+    PCD_LAUNCH(timed(m, PROF_ATTN_PREFILL, [&] { return pcd::launch_attention(aa, m->stream); }));
+    PCD_TRY(gemm(m, PROF_GEMM_PREFILL, att, n, m->qdim, W.wo, m->d, m->qdim, m->qdim, pcd::EPI_F32_ADD, x, m->d));
+    PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
+      return pcd::launch_rmsnorm(x, m->d, nullptr, n, m->d, W.mlp_norm, m->cfg.rms_eps, xn, m->d, m->stream);
+    }));
+    PCD_TRY(gemm(m, PROF_GEMM_PREFILL, xn, n, m->d, W.wgu, 2 * m->Fp, m->d, m->d, pcd::EPI_SWIGLU, hb, m->Fp));
+    PCD_TRY(gemm(m, PROF_GEMM_PREFILL, hb, n, m->Fp, W.wd, m->d, m->Fp, m->Fp, pcd::EPI_F32_ADD, x, m->d));
+  }
+  return PCD_OK;
+}
+
+// --------------------------------------------------------------- branch pass
+struct Segment {
+  const pcd_cache* c;
+  int t0, t1;  // branch tokens of this request
+};
+
+int run_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_seg, float* d_result,
+               cudaEvent_t ev_mid = nullptr) {
+  const int T = p.T, R = p.R, G = m->G;
+  PCD_TRY(ensure_workspace(m, T));
+  PCD_TRY(ensure(m->kb, static_cast<size_t>(m->Hkv) * T * m->dh * 2));
+  PCD_TRY(ensure(m->vb, static_cast<size_t>(m->Hkv) * T * m->dh * 2));
+  int max_lp = 0;
+  for (int s = 0; s < n_seg; ++s) max_lp = std::max(max_lp, segs[s].c->len);
+  // key splits of the prefix attention: enough CTAs to cover the SMs twice
+  const int blocks = ((T * G + 63) / 64) * m->Hkv;
+  int splits = std::max(1, std::min((2 * m->sms + blocks - 1) / blocks, (max_lp + 255) / 256));
+  PCD_TRY(ensure(m->part_o, static_cast<size_t>(splits) * m->Hkv * T * G * m->dh * 4));
+  PCD_TRY(ensure(m->part_ml, static_cast<size_t>(splits) * m->Hkv * T * G * 8));
+  PCD_TRY(ensure(m->hr, static_cast<size_t>(std::max(R, 1)) * m->d * 2));
+  PCD_TRY(ensure(m->ro_part, static_cast<size_t>(p.n_vtiles) * std::max(R, 1) * 8));
+  PCD_TRY(ensure(m->z, static_cast<size_t>(std::max(p.n_children, 1)) * 4));
+  PCD_TRY(ensure(m->lse, static_cast<size_t>(std::max(R, 1)) * 4));
+
+  float* x = static_cast<float*>(m->x32.p);
+  bf16* xn = static_cast<bf16*>(m->xn.p);
+  float* qkv = static_cast<float*>(m->qkv.p);
+  bf16* q = static_cast<bf16*>(m->q.p);
+  bf16* att = static_cast<bf16*>(m->att.p);
+  bf16* hb = static_cast<bf16*>(m->hb.p);
+  bf16* kb = static_cast<bf16*>(m->kb.p);
+  bf16* vb = static_cast<bf16*>(m->vb.p);
+  float* part_o = static_cast<float*>(m->part_o.p);
+  float2* part_ml = static_cast<float2*>(m->part_ml.p);
+  const float scale_log2 = 1.4426950408889634f / std::sqrt(static_cast<float>(m->dh));
+
+  PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_embed(p.tok, T, m->embed, m->d, m->V, x, m->d_err, m->stream); }));
+  for (int l = 0; l < m->L; ++l) {
+    const Layer& W = m->layers[l];
+    PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
+      return pcd::launch_rmsnorm(x, m->d, nullptr, T, m->d, W.attn_norm, m->cfg.rms_eps, xn, m->d, m->stream);
+    }));
+    PCD_TRY(gemm(m, PROF_GEMM_BRANCH, xn, T, m->d, W.wqkv, m->Nqkv, m->d, m->d, pcd::EPI_F32_STORE, qkv, m->Nqkv));
+    for (int s = 0; s < n_seg; ++s) {
+      const Segment& sg = segs[s];
+      const int n = sg.t1 - sg.t0;
+      if (n <= 0) continue;
+      pcd::RopeArgs ra;
+      ra.qkv = qkv + static_cast<size_t>(sg.t0) * m->Nqkv;
+      ra.ldqkv = m->Nqkv;
+      ra.n = n;
+      ra.Hq = m->Hq;
+      ra.Hkv = m->Hkv;
+      ra.DH = m->dh;
+      ra.cs = m->rope;
+      ra.max_pos = m->max_pos;
+      ra.rel = p.rel + sg.t0;
+      ra.base = sg.c->len;
+      ra.q = q + static_cast<size_t>(sg.t0) * m->qdim;
+      ra.k_dst = kb;
+      ra.v_dst = vb;
+      ra.kv_head_stride = T;
+      ra.kv_row0 = sg.t0;
+      ra.err = m->d_err;
+      PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_rope_kv(ra, m->stream); }));
+    }
+    for (int s = 0; s < n_seg; ++s) {
+      const Segment& sg = segs[s];
+      const int n = sg.t1 - sg.t0;
+      if (n <= 0) continue;
+      const size_t layer_kv = static_cast<size_t>(m->Hkv) * sg.c->cap * m->dh;
+      pcd::AttnArgs aa{};
+      aa.q = q;
+      aa.n_tok = n;
+      aa.Hq = m->Hq;
+      aa.Hkv = m->Hkv;
+      aa.DH = m->dh;
+      aa.tok0 = sg.t0;
+      aa.part_rows = T * G;
+      aa.k = sg.c->k + l * layer_kv;
+      aa.v = sg.c->v + l * layer_kv;
+      aa.kv_head_stride = sg.c->cap;
+      aa.n_keys = sg.c->len;
+      aa.rel = p.rel;
+      aa.base = sg.c->len;
+      aa.n_splits = splits;
+      aa.split_len = ((sg.c->len + splits - 1) / splits + 63) / 64 * 64;
+      aa.scale_log2 = scale_log2;
+      aa.part_o = part_o;
+      aa.part_ml = part_ml;
+      aa.partial = 1;
+      aa.causal_heavy_first = 0;
+      PCD_LAUNCH(timed(m, PROF_ATTN_BRANCH, [&] { return pcd::launch_attention(aa, m->stream); }));
+    }
+    pcd::MergeArgs ma{};
+    ma.q = q;
+    ma.n_tok = T;
+    ma.Hq = m->Hq;
+    ma.Hkv = m->Hkv;
+    ma.DH = m->dh;
+    ma.part_o = part_o;
+    ma.part_ml = part_ml;
+    ma.n_splits = splits;
+    ma.kb = kb;
+    ma.vb = vb;
+    ma.anc_off = p.anc_off;
+    ma.anc_idx = p.anc_idx;
+    ma.scale_log2 = scale_log2;
+    ma.out = att;
+    ma.ld_out = m->qdim;
+    PCD_LAUNCH(timed(m, PROF_ATTN_BRANCH, [&] { return pcd::launch_branch_merge(ma, m->stream); }));
+    PCD_TRY(gemm(m, PROF_GEMM_BRANCH, att, T, m->qdim, W.wo, m->d, m->qdim, m->qdim, pcd::EPI_F32_ADD, x, m->d));
+    PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
+      return pcd::launch_rmsnorm(x, m->d, nullptr, T, m->d, W.mlp_norm, m->cfg.rms_eps, xn, m->d, m->stream);
+    }));
+    PCD_TRY(gemm(m, PROF_GEMM_BRANCH, xn, T, m->d, W.wgu, 2 * m->Fp, m->d, m->d, pcd::EPI_SWIGLU, hb, m->Fp));
+    PCD_TRY(gemm(m, PROF_GEMM_BRANCH, hb, T, m->Fp, W.wd, m->d, m->Fp, m->Fp, pcd::EPI_F32_ADD, x, m->d));
+  }
+  if (ev_mid) cudaEventRecord(ev_mid, m->stream);
+
+  // final norm on the readout rows only, then the fused vocabulary readout
+  bf16* hr = static_cast<bf16*>(m->hr.p);
+  PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
+    return pcd::launch_rmsnorm(x, m->d, p.ro_tok, R, m->d, m->final_norm, m->cfg.rms_eps, hr, m->d, m->stream);
+  }));
+  pcd::GemmShape rs{hr, R, m->d, m->lm, m->V, m->d, m->d};
+  pcd::EpiArgs re;
+  re.part = static_cast<float2*>(m->ro_part.p);
+  re.gather_off = p.gather_off;
+  re.gather = p.gather;
+  re.z_out = static_cast<float*>(m->z.p);
+  PCD_LAUNCH(timed(m, PROF_READOUT, [&] {
+    return pcd::launch_gemm(rs, pcd::EPI_READOUT, re, p.ro_tiling, m->stream, m->d_err, m->wait_ns, m->sms);
+  }));
+  PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
+    return pcd::launch_lse_combine(static_cast<float2*>(m->ro_part.p), p.n_vtiles, R, static_cast<float*>(m->lse.p),
+                                   m->stream);
+  }));
+  pcd::ScoreArgs sa;
+  sa.z = static_cast<float*>(m->z.p);
+  sa.lse = static_cast<float*>(m->lse.p);
+  sa.child_row = p.child_row;
+  sa.lab_off = p.lab_off;
+  sa.path = p.path;
+  sa.fld_lab = p.fld_lab;
+  sa.fld_root = p.fld_root;
+  sa.row_ch = p.row_ch;
+  sa.temp = p.temp;
+  sa.n_fields = p.n_fields;
+  sa.out_field = d_result;
+  sa.out_probs = d_result + p.n_fields * 8;
+  sa.out_logprobs = d_result + p.n_fields * 8 + p.n_labels;
+  PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_score(sa, m->stream); }));
+  return PCD_OK;
+}
+
+// ------------------------------------------------------------ plan upload
+// Serialises a host plan into an int32 blob; `view` gets pointers relative to
+// `dev` (the blob's device address).
+size_t plan_blob(const pcd_model* m, const pcd::HostPlan& hp, std::vector<int32_t>& blob, PlanView& v,
+                 const int32_t* dev) {
+  v.n_fields = hp.n_fields;
+  v.T = hp.T;
+  v.R = hp.R;
+  v.n_children = hp.n_children;
+  v.n_labels = hp.n_labels;
+  v.max_rel = hp.max_rel;
+  v.ro_tiling = pcd::choose_tiling(hp.R, m->V, m->d, pcd::EPI_READOUT, m->sms);
+  v.ro_tiling.splits = 1;
+  v.n_vtiles = pcd::gemm_n_tiles(m->V, v.ro_tiling);
+  const int bn = v.ro_tiling.bn;
+  // gather entries sorted by vocabulary tile
+  std::vector<int> order(hp.n_children);
+  for (int e = 0; e < hp.n_children; ++e) order[e] = e;
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return hp.ch_tok[a] / bn < hp.ch_tok[b] / bn; });
+  std::vector<int32_t> goff(v.n_vtiles + 1, 0), g4;
+  for (int e : order) {
+    goff[hp.ch_tok[e] / bn + 1]++;
+    g4.push_back(hp.ch_tok[e] % bn);
+    g4.push_back(hp.child_row[e]);
+    g4.push_back(e);
+    g4.push_back(0);
+  }
+  for (int i = 0; i < v.n_vtiles; ++i) goff[i + 1] += goff[i];
+
+  blob.clear();
+  auto put = [&](const int32_t* src, size_t n) {
+    while (blob.size() % 4) blob.push_back(0);
+    const size_t off = blob.size();
+    blob.insert(blob.end(), src, src + n);
+    return dev + off;
+  };
+  v.tok = put(hp.tok.data(), hp.tok.size());
+  v.rel = put(hp.rel.data(), hp.rel.size());
+  v.anc_off = put(hp.anc_off.data(), hp.anc_off.size());
+  v.anc_idx = put(hp.anc_idx.data(), hp.anc_idx.size());
+  v.ro_tok = put(hp.ro_tok.data(), hp.ro_tok.size());
+  v.row_ch = put(hp.row_ch.data(), hp.row_ch.size());
+  v.child_row = put(hp.child_row.data(), hp.child_row.size());
+  v.lab_off = put(hp.lab_off.data(), hp.lab_off.size());
+  v.path = put(hp.path.data(), hp.path.size());
+  v.fld_lab = put(hp.fld_lab.data(), hp.fld_lab.size());
+  v.fld_root = put(hp.fld_root.data(), hp.fld_root.size());
+  v.temp = reinterpret_cast<const float*>(put(reinterpret_cast<const int32_t*>(hp.temp.data()), hp.temp.size()));
+  v.gather_off = put(goff.data(), goff.size());
+  v.gather = reinterpret_cast<const int4*>(put(g4.data(), g4.size()));
+  return blob.size() * sizeof(int32_t);
+}
+
+int check_positions(const pcd_model* m, int prefix_len, int max_rel) {
+  if (prefix_len + max_rel >= m->max_pos)
+    return fail(PCD_ERR_TOO_LONG, "position " + std::to_string(prefix_len + max_rel) + " beyond max_positions " +
+                                      std::to_string(m->max_pos));
+  return PCD_OK;
+}
+
+int read_device_error(pcd_model* m) {
+  int h = 0;
+  PCD_CUDA(cudaMemcpy(&h, m->d_err, sizeof(int), cudaMemcpyDeviceToHost));
+  if (h != 0) {
+    cudaMemset(m->d_err, 0, sizeof(int));
+    if (h == pcd::DEV_BAD_INDEX) return fail(PCD_ERR_TOKEN_RANGE, "a device kernel met a token id or position out of range");
+    return fail(PCD_ERR_DEVICE_TIMEOUT, "a kernel pipeline wait timed out (code " + std::to_string(h) + ")");
+  }
+  return PCD_OK;
+}
+
+// ----------------------------------------------------------- weight loading
+uint16_t f32_to_bf16_rne(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  if ((u & 0x7f800000u) == 0x7f800000u) return static_cast<uint16_t>((u >> 16) | ((u & 0xffffu) ? 0x40u : 0u));
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return static_cast<uint16_t>(u >> 16);
+}
+
+// Writes rows x cols of a host matrix (f32 or bf16 bits) into dst (bf16 bits,
+// row stride dst_ld, row r of the source at dst row r * row_step + row_off).
+void put_matrix(uint16_t* dst, int dst_ld, int row_step, int row_off, const void* src, int rows, int cols, int dtype) {
+  for (int r = 0; r < rows; ++r) {
+    uint16_t* d = dst + static_cast<size_t>(r * row_step + row_off) * dst_ld;
+    if (dtype == PCD_DTYPE_BF16) {
+      std::memcpy(d, static_cast<const uint16_t*>(src) + static_cast<size_t>(r) * cols, cols * 2);
+    } else {
+      const float* s = static_cast<const float*>(src) + static_cast<size_t>(r) * cols;
+      for (int c = 0; c < cols; ++c) d[c] = f32_to_bf16_rne(s[c]);
+    }
+  }
+}
+
+int validate_cfg(const pcd_model_config& c) {
+  if (c.n_layers < 1 || c.d_model < 64 || c.n_q_heads < 1 || c.n_kv_heads < 1 || c.head_dim < 16 || c.d_ff < 1 ||
+      c.vocab < 2)
+    return fail(PCD_ERR_SHAPE_MISMATCH, "model shape out of range");
+  if (c.d_model % 64) return fail(PCD_ERR_SHAPE_MISMATCH, "d_model must be a multiple of 64");
+  if (c.n_q_heads % c.n_kv_heads) return fail(PCD_ERR_SHAPE_MISMATCH, "n_q_heads must be a multiple of n_kv_heads");
+  if (c.head_dim != 16 && c.head_dim != 64 && c.head_dim != 128)
+    return fail(PCD_ERR_SHAPE_MISMATCH, "head_dim must be 16, 64 or 128");
+  if ((c.n_q_heads * c.head_dim) % 64) return fail(PCD_ERR_SHAPE_MISMATCH, "n_q_heads * head_dim must be a multiple of 64");
+  if (((c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim) % 32)
+    return fail(PCD_ERR_SHAPE_MISMATCH, "q/k/v width must be a multiple of 32");
+  if (c.vocab % 32) return fail(PCD_ERR_SHAPE_MISMATCH, "vocab must be a multiple of 32");
+  if (!(c.rms_eps > 0.f) || !(c.rope_theta > 1.f)) return fail(PCD_ERR_SHAPE_MISMATCH, "rms_eps / rope_theta invalid");
+  return PCD_OK;
+}
+
+// Tensor i of the fixed order (see pcd.h); returns host data or nullptr.
+using TensorFn = const void* (*)(void* ctx, int index, size_t bytes);
+
+int build_model(const pcd_model_config& cfg, TensorFn get, void* ctx, int dtype, void* stream, pcd_model** out) {
+  PCD_TRY(validate_cfg(cfg));
+  int dev = 0;
+  PCD_CUDA(cudaGetDevice(&dev));
+  cudaDeviceProp prop;
+  PCD_CUDA(cudaGetDeviceProperties(&prop, dev));
+  if (prop.major != 10 || prop.minor != 3)
+    return fail(PCD_ERR_CUDA, std::string("this library is built for sm_103a; device is ") + prop.name + " (sm_" +
+                                  std::to_string(prop.major) + std::to_string(prop.minor) + ")");
+  if (!pcd::tma_init()) return fail(PCD_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+
+  pcd_model* m = new pcd_model();
+  m->cfg = cfg;
+  m->L = cfg.n_layers;
+  m->d = cfg.d_model;
+  m->Hq = cfg.n_q_heads;
+  m->Hkv = cfg.n_kv_heads;
+  m->dh = cfg.head_dim;
+  m->G = m->Hq / m->Hkv;
+  m->F = cfg.d_ff;
+  m->Fp = (cfg.d_ff + 63) / 64 * 64;
+  m->V = cfg.vocab;
+  m->qdim = m->Hq * m->dh;
+  m->kvdim = m->Hkv * m->dh;
+  m->Nqkv = m->qdim + 2 * m->kvdim;
+  m->max_pos = cfg.max_positions > 0 ? cfg.max_positions : 32768;
+  m->stream = static_cast<cudaStream_t>(stream);
+  m->sms = prop.multiProcessorCount;
+  if (const char* w = std::getenv("PCD_WAIT_LIMIT_MS")) m->wait_ns = static_cast<uint64_t>(std::atof(w) * 1e6);
+
+  auto cleanup = [&](int code) {
+    pcd_model_free(m);
+    return code;
+  };
+
+  const int L = m->L, d = m->d, V = m->V;
+  const size_t n_embed = static_cast<size_t>(V) * d;
+  const size_t n_qkv = static_cast<size_t>(m->Nqkv) * d, n_o = static_cast<size_t>(d) * m->qdim;
+  const size_t n_gu = static_cast<size_t>(2) * m->Fp * d, n_dn = static_cast<size_t>(d) * m->Fp;
+  const size_t per_layer = n_qkv + n_o + n_gu + n_dn;
+  const size_t n_bf16 = n_embed + per_layer * L + (cfg.tied_embedding ? 0 : n_embed);
+  if (cudaMalloc(&m->wblob, n_bf16 * 2) != cudaSuccess) {
+    cudaGetLastError();
+    m->wblob = nullptr;
+    return cleanup(fail(PCD_ERR_OOM, "weights do not fit on the device"));
+  }
+  if (cudaMalloc(&m->fblob, (static_cast<size_t>(2) * L + 1) * d * 4) != cudaSuccess) {
+    cudaGetLastError();
+    m->fblob = nullptr;
+    return cleanup(fail(PCD_ERR_OOM, "norm gains do not fit on the device"));
+  }
+  bf16* w = static_cast<bf16*>(m->wblob);
+  m->embed = w;
+  w += n_embed;
+  m->layers.resize(L);
+  for (int l = 0; l < L; ++l) {
+    Layer& Y = m->layers[l];
+    Y.wqkv = w;
+    w += n_qkv;
+    Y.wo = w;
+    w += n_o;
+    Y.wgu = w;
+    w += n_gu;
+    Y.wd = w;
+    w += n_dn;
+    Y.attn_norm = m->fblob + (2 * l) * d;
+    Y.mlp_norm = m->fblob + (2 * l + 1) * d;
+  }
+  m->final_norm = m->fblob + 2 * L * d;
+  m->lm = cfg.tied_embedding ? m->embed : w;
+
+  const size_t esz = dtype == PCD_DTYPE_BF16 ? 2 : 4;
+  std::vector<uint16_t> stage;
+  auto fetch = [&](int idx, size_t elems) -> const void* { return get(ctx, idx, elems * esz); };
+  auto fetch_f32 = [&](int idx, size_t elems) -> const float* {
+    return static_cast<const float*>(get(ctx, idx, elems * 4));
+  };
+  auto upload = [&](bf16* dst, size_t elems) { return cudaMemcpy(dst, stage.data(), elems * 2, cudaMemcpyHostToDevice); };
+
+  // embedding
+  const void* src = fetch(0, n_embed);
+  if (!src) return cleanup(fail(PCD_ERR_BAD_WEIGHTS, "embedding tensor missing or truncated"));
+  stage.assign(n_embed, 0);
+  put_matrix(stage.data(), d, 1, 0, src, V, d, dtype);
+  if (upload(m->embed, n_embed) != cudaSuccess) return cleanup(fail(PCD_ERR_CUDA, "embedding upload failed"));
+  for (int l = 0; l < L; ++l) {
+    const int b = 1 + 9 * l;
+    Layer& Y = m->layers[l];
+    const float* an = fetch_f32(b + 0, d);
+    if (!an || cudaMemcpy(Y.attn_norm, an, d * 4, cudaMemcpyHostToDevice) != cudaSuccess)
+      return cleanup(fail(PCD_ERR_BAD_WEIGHTS, "attn_norm of layer " + std::to_string(l)));
+    // q, k, v rows stacked into one [Nqkv][d] matrix
+    stage.assign(n_qkv, 0);
+    const int rows_of[3] = {m->qdim, m->kvdim, m->kvdim};
+    int row0 = 0;
+    for (int j = 0; j < 3; ++j) {
+      const void* t = fetch(b + 1 + j, static_cast<size_t>(rows_of[j]) * d);
+      if (!t) return cleanup(fail(PCD_ERR_BAD_WEIGHTS, "q/k/v of layer " + std::to_string(l)));
+      put_matrix(stage.data(), d, 1, row0, t, rows_of[j], d, dtype);
+      row0 += rows_of[j];
+    }
+    if (upload(Y.wqkv, n_qkv) != cudaSuccess) return cleanup(fail(PCD_ERR_CUDA, "upload failed"));
+    stage.assign(n_o, 0);
+    const void* to = fetch(b + 4, n_o);
+    if (!to) return cleanup(fail(PCD_ERR_BAD_WEIGHTS, "o of layer " + std::to_string(l)));
+    put_matrix(stage.data(), m->qdim, 1, 0, to, d, m->qdim, dtype);
+    if (upload(Y.wo, n_o) != cudaSuccess) return cleanup(fail(PCD_ERR_CUDA, "upload failed"));
+    const float* mn = fetch_f32(b + 5, d);
+    if (!mn || cudaMemcpy(Y.mlp_norm, mn, d * 4, cudaMemcpyHostToDevice) != cudaSuccess)
+      return cleanup(fail(PCD_ERR_BAD_WEIGHTS, "mlp_norm of layer " + std::to_string(l)));
+    // gate / up interleaved by row: row 2f = gate f, row 2f + 1 = up f; padded rows stay zero
+    stage.assign(n_gu, 0);
+    for (int j = 0; j < 2; ++j) {
+      const void* t = fetch(b + 6 + j, static_cast<size_t>(m->F) * d);
+      if (!t) return cleanup(fail(PCD_ERR_BAD_WEIGHTS, "gate/up of layer " + std::to_string(l)));
+      put_matrix(stage.data(), d, 2, j, t, m->F, d, dtype);
+    }
+    if (upload(Y.wgu, n_gu) != cudaSuccess) return cleanup(fail(PCD_ERR_CUDA, "upload failed"));
+    // down [d][F] padded to [d][Fp] with zero columns
+    stage.assign(n_dn, 0);
+    const void* td = fetch(b + 8, static_cast<size_t>(d) * m->F);
+    if (!td) return cleanup(fail(PCD_ERR_BAD_WEIGHTS, "down of layer " + std::to_string(l)));
+    put_matrix(stage.data(), m->Fp, 1, 0, td, d, m->F, dtype);
+    if (upload(Y.wd, n_dn) != cudaSuccess) return cleanup(fail(PCD_ERR_CUDA, "upload failed"));
+  }
+  const float* fn = fetch_f32(1 + 9 * L, d);
+  if (!fn || cudaMemcpy(m->final_norm, fn, d * 4, cudaMemcpyHostToDevice) != cudaSuccess)
+    return cleanup(fail(PCD_ERR_BAD_WEIGHTS, "final_norm missing"));
+  if (!cfg.tied_embedding) {
+    const void* lm = fetch(2 + 9 * L, n_embed);
+    if (!lm) return cleanup(fail(PCD_ERR_BAD_WEIGHTS, "lm_head missing"));
+    stage.assign(n_embed, 0);
+    put_matrix(stage.data(), d, 1, 0, lm, V, d, dtype);
+    if (upload(m->lm, n_embed) != cudaSuccess) return cleanup(fail(PCD_ERR_CUDA, "lm_head upload failed"));
+  }
+  stage.clear();
+  stage.shrink_to_fit();
+
+  // RoPE table: angle pos * theta^(-2i/dh) in double precision, stored as fp32 (cos, sin)
+  {
+    const int half = m->dh / 2;
+    std::vector<float2> cs(static_cast<size_t>(m->max_pos) * half);
+    for (int i = 0; i < half; ++i) {
+      const double inv = std::pow(static_cast<double>(cfg.rope_theta), -2.0 * i / m->dh);
+      for (int pos = 0; pos < m->max_pos; ++pos) {
+        const double a = pos * inv;
+        cs[static_cast<size_t>(pos) * half + i] = make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
+      }
+    }
+    if (cudaMalloc(&m->rope, cs.size() * sizeof(float2)) != cudaSuccess) {
+      cudaGetLastError();
+      m->rope = nullptr;
+      return cleanup(fail(PCD_ERR_OOM, "RoPE table"));
+    }
+    if (cudaMemcpy(m->rope, cs.data(), cs.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess)
+      return cleanup(fail(PCD_ERR_CUDA, "RoPE upload"));
+  }
+  if (cudaMalloc(&m->d_err, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    m->d_err = nullptr;
+    return cleanup(fail(PCD_ERR_OOM, "error word"));
+  }
+  cudaMemset(m->d_err, 0, sizeof(int));
+  cudaEventCreateWithFlags(&m->up_ev, cudaEventDisableTiming);
+  cudaEventCreate(&m->ev_a);
+  cudaEventCreate(&m->ev_b);
+  cudaEventCreate(&m->ev_c);
+  if (cudaDeviceSynchronize() != cudaSuccess) return cleanup(fail(PCD_ERR_CUDA, "device error during load"));
+  *out = m;
+  return PCD_OK;
+}
+
+struct HostTensors {
+  const void* const* t;
+  int n;
+};
+const void* host_tensor(void* ctx, int i, size_t) {
+  auto* h = static_cast<HostTensors*>(ctx);
+  return i < h->n ? h->t[i] : nullptr;
+}
+
+struct FileTensors {
+  FILE* f;
+  std::vector<uint8_t> buf;
+};
+const void* file_tensor(void* ctx, int, size_t bytes) {
+  auto* h = static_cast<FileTensors*>(ctx);
+  h->buf.resize(bytes);
+  if (bytes && std::fread(h->buf.data(), 1, bytes, h->f) != bytes) return nullptr;
+  return h->buf.data();
+}
+
+// ------------------------------------------------------------ caches
+int new_cache(pcd_model* m, int cap, pcd_cache** out) {
+  const size_t bytes = static_cast<size_t>(m->L) * m->Hkv * cap * m->dh * 2 * 2;
+  void* mem = nullptr;
+  size_t got = 0;
+  for (size_t i = 0; i < m->cache_pool.size(); ++i) {
+    const auto& e = m->cache_pool[i];
+    if (e.first >= bytes && e.first <= 2 * bytes + (1u << 20)) {
+      mem = e.second;
+      got = e.first;
+      m->cache_pool.erase(m->cache_pool.begin() + i);
+      break;
+    }
+  }
+  if (!mem) {
+    if (cudaMalloc(&mem, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      return fail(PCD_ERR_OOM, "KV cache allocation failed");
+    }
+    got = bytes;
+  }
+  pcd_cache* c = new pcd_cache();
+  c->m = m;
+  c->mem = mem;
+  c->bytes = got;
+  c->cap = cap;
+  c->len = 0;
+  c->k = static_cast<bf16*>(mem);
+  c->v = c->k + static_cast<size_t>(m->L) * m->Hkv * cap * m->dh;
+  *out = c;
+  return PCD_OK;
+}
+
+int upload_ids(pcd_model* m, const int32_t* ids, int n, const int32_t** d_ids) {
+  for (int i = 0; i < n; ++i)
+    if (ids[i] < 0 || ids[i] >= m->V) return fail(PCD_ERR_TOKEN_RANGE, "prefix token id out of range");
+  PCD_TRY(ensure(m->ids, static_cast<size_t>(n) * 4));
+  PCD_TRY(upload_async(m, m->ids.p, ids, static_cast<size_t>(n) * 4));
+  *d_ids = static_cast<const int32_t*>(m->ids.p);
+  return PCD_OK;
+}
+
+// Uploads a host plan into the model's plan buffer; fills `v`.
+int upload_plan(pcd_model* m, const pcd::HostPlan& hp, PlanView& v) {
+  std::vector<int32_t> blob;
+  // first pass for the size, second with the real device base
+  plan_blob(m, hp, blob, v, nullptr);
+  const size_t bytes = blob.size() * 4;
+  PCD_TRY(ensure(m->plan_buf, bytes));
+  plan_blob(m, hp, blob, v, static_cast<const int32_t*>(m->plan_buf.p));
+  return upload_async(m, m->plan_buf.p, blob.data(), bytes);
+}
+
+void unpack_results(const float* res, const PlanView& v, int f0, int l0, int n_fields, pcd_field_result* out) {
+  const float* fl = res;
+  const float* probs = res + v.n_fields * 8;
+  const float* lps = probs + v.n_labels;
+  int lab = l0;
+  for (int f = 0; f < n_fields; ++f) {
+    const float* o = fl + (f0 + f) * 8;
+    const int nl = static_cast<int>(o[5]);
+    pcd_field_result& r = out[f];
+    r.label = static_cast<int32_t>(o[0]);
+    r.mass = o[1];
+    r.log_mass = o[2];
+    r.margin = o[3];
+    r.first_mass = o[4];
+    if (r.probs) std::memcpy(r.probs, probs + lab, nl * sizeof(float));
+    if (r.logprobs) std::memcpy(r.logprobs, lps + lab, nl * sizeof(float));
+    lab += nl;
+  }
+}
+
+int score_impl(pcd_model* m, const pcd_cache* const* caches, const pcd_field* const* fields, const int* n_fields,
+               int n_req, pcd_field_result* const* out, pcd_stats* stats) {
+  if (!m || !caches || !fields || !n_fields || !out || n_req < 1) return fail(PCD_ERR_INVALID_ARG, "NULL argument");
+  const auto t_start = std::chrono::steady_clock::now();
+  pcd::HostPlan hp;
+  std::string msg;
+  std::vector<Segment> segs(n_req);
+  std::vector<int> field0(n_req), label0(n_req);
+  for (int r = 0; r < n_req; ++r) {
+    if (!caches[r] || caches[r]->m != m) return fail(PCD_ERR_SHAPE_MISMATCH, "cache belongs to another model");
+    if (n_fields[r] < 1 || !fields[r] || !out[r]) return fail(PCD_ERR_INVALID_ARG, "request without fields");
+    field0[r] = hp.n_fields;
+    label0[r] = hp.n_labels;
+    const int t0 = hp.T;
+    const int rel0 = hp.max_rel;
+    hp.max_rel = 0;
+    int rc = pcd::compile_fields(fields[r], n_fields[r], m->V, &hp, &msg);
+    if (rc != PCD_OK) return fail(rc, "request " + std::to_string(r) + ", " + msg);
+    PCD_TRY(check_positions(m, caches[r]->len, hp.max_rel));
+    hp.max_rel = std::max(hp.max_rel, rel0);
+    segs[r] = Segment{caches[r], t0, hp.T};
+  }
+  const auto t_comp = std::chrono::steady_clock::now();
+  PlanView v;
+  PCD_TRY(upload_plan(m, hp, v));
+  PCD_TRY(ensure(m->result, static_cast<size_t>(v.result_floats()) * 4));
+  if (stats) cudaEventRecord(m->ev_a, m->stream);
+  PCD_TRY(run_branch(m, v, segs.data(), n_req, static_cast<float*>(m->result.p), stats ? m->ev_b : nullptr));
+  if (stats) cudaEventRecord(m->ev_c, m->stream);
+  const size_t rbytes = static_cast<size_t>(v.result_floats()) * 4;
+  PCD_TRY(ensure_pinned(m->down, m->down_n, rbytes));
+  PCD_CUDA(cudaMemcpyAsync(m->down, m->result.p, rbytes, cudaMemcpyDeviceToHost, m->stream));
+  PCD_CUDA(cudaStreamSynchronize(m->stream));
+  m->up_pending = false;
+  PCD_TRY(read_device_error(m));
+  for (int r = 0; r < n_req; ++r)
+    unpack_results(static_cast<const float*>(m->down), v, field0[r], label0[r], n_fields[r], out[r]);
+  if (stats) {
+    const auto t_end = std::chrono::steady_clock::now();
+    std::memset(stats, 0, sizeof(*stats));
+    stats->compile_ms = std::chrono::duration<float, std::milli>(t_comp - t_start).count();
+    cudaEventElapsedTime(&stats->branch_ms, m->ev_a, m->ev_b);
+    cudaEventElapsedTime(&stats->readout_ms, m->ev_b, m->ev_c);
+    stats->total_ms = std::chrono::duration<float, std::milli>(t_end - t_start).count();
+    stats->forward_passes = 1;
+    stats->branch_tokens = v.T;
+    stats->readout_rows = v.R;
+  }
+  return PCD_OK;
+}
+
+}  // namespace
+
+// ===================================================================== C ABI
+extern "C" {
+
+int pcd_load_weights_host(const pcd_model_config* cfg, const void* const* tensors, int dtype, void* stream,
+                          pcd_model** out) {
+  if (!cfg || !tensors || !out) return fail(PCD_ERR_INVALID_ARG, "NULL argument");
+  if (dtype != PCD_DTYPE_F32 && dtype != PCD_DTYPE_BF16) return fail(PCD_ERR_INVALID_ARG, "dtype");
+  HostTensors h{tensors, 3 + 9 * cfg->n_layers};
+  return build_model(*cfg, host_tensor, &h, dtype, stream, out);
+}
+
+int pcd_load_weights(const pcd_model_config* cfg, const char* path, void* stream, pcd_model** out) {
+  if (!path || !out) return fail(PCD_ERR_INVALID_ARG, "NULL argument");
+  FILE* f = std::fopen(path, "rb");
+  if (!f) return fail(PCD_ERR_BAD_WEIGHTS, std::string("cannot open ") + path);
+  unsigned char hdr[64];
+  if (std::fread(hdr, 1, 64, f) != 64 || std::memcmp(hdr, "PCDW", 4) != 0) {
+    std::fclose(f);
+    return fail(PCD_ERR_BAD_WEIGHTS, "not a .pcdw file");
+  }
+  uint32_t u[11];
+  float fl[2];
+  std::memcpy(u, hdr + 4, sizeof(u));
+  std::memcpy(fl, hdr + 48, sizeof(fl));
+  if (u[0] != 1 || (u[1] != 1 && u[1] != 2)) {
+    std::fclose(f);
+    return fail(PCD_ERR_BAD_WEIGHTS, "unsupported .pcdw version or dtype");
+  }
+  pcd_model_config c{};
+  c.n_layers = static_cast<int>(u[2]);
+  c.d_model = static_cast<int>(u[3]);
+  c.n_q_heads = static_cast<int>(u[4]);
+  c.n_kv_heads = static_cast<int>(u[5]);
+  c.head_dim = static_cast<int>(u[6]);
+  c.d_ff = static_cast<int>(u[7]);
+  c.vocab = static_cast<int>(u[8]);
+  c.tied_embedding = static_cast<int>(u[9]);
+  c.rms_eps = fl[0];
+  c.rope_theta = fl[1];
+  c.max_positions = cfg ? cfg->max_positions : 0;
+  if (cfg && (cfg->n_layers != c.n_layers || cfg->d_model != c.d_model || cfg->n_q_heads != c.n_q_heads ||
+              cfg->n_kv_heads != c.n_kv_heads || cfg->head_dim != c.head_dim || cfg->d_ff != c.d_ff ||
+              cfg->vocab != c.vocab || (cfg->tied_embedding != 0) != (c.tied_embedding != 0))) {
+    std::fclose(f);
+    return fail(PCD_ERR_SHAPE_MISMATCH, "config does not match the file header");
+  }
+  // expected size
+  const int dtype = static_cast<int>(u[1]);
+  const size_t es = dtype == 2 ? 2 : 4;
+  const size_t d = c.d_model, V = c.vocab, F = c.d_ff, qd = static_cast<size_t>(c.n_q_heads) * c.head_dim,
+               kd = static_cast<size_t>(c.n_kv_heads) * c.head_dim;
+  const size_t per_layer = 2 * d * 4 + (qd * d + 2 * kd * d + d * qd + 3 * F * d) * es;
+  const size_t expect = 64 + V * d * es + per_layer * c.n_layers + d * 4 + (c.tied_embedding ? 0 : V * d * es);
+  std::fseek(f, 0, SEEK_END);
+  const long size = std::ftell(f);
+  std::fseek(f, 64, SEEK_SET);
+  if (size < 0 || static_cast<size_t>(size) != expect) {
+    std::fclose(f);
+    return fail(PCD_ERR_BAD_WEIGHTS, "file size " + std::to_string(size) + " != expected " + std::to_string(expect));
+  }
+  FileTensors ft{f, {}};
+  const int rc = build_model(c, file_tensor, &ft, dtype, stream, out);
+  std::fclose(f);
+  return rc;
+}
+
+void pcd_model_free(pcd_model* m) {
+  if (!m) return;
+  if (m->stream) cudaStreamSynchronize(m->stream);
+  cudaDeviceSynchronize();
+  for (DevBuf* b : {&m->x32, &m->xn, &m->qkv, &m->q, &m->kb, &m->vb, &m->att, &m->hb, &m->part_o, &m->part_ml, &m->hr,
+                    &m->ro_part, &m->z, &m->lse, &m->plan_buf, &m->result, &m->ids})
+    if (b->p) cudaFree(b->p);
+  for (auto& e : m->cache_pool) cudaFree(e.second);
+  if (m->wblob) cudaFree(m->wblob);
+  if (m->fblob) cudaFree(m->fblob);
+  if (m->rope) cudaFree(m->rope);
+  if (m->d_err) cudaFree(m->d_err);
+  if (m->up) cudaFreeHost(m->up);
+  if (m->down) cudaFreeHost(m->down);
+  if (m->up_ev) cudaEventDestroy(m->up_ev);
+  for (cudaEvent_t e : m->ev_pool) cudaEventDestroy(e);
+  for (cudaEvent_t e : {m->ev_a, m->ev_b, m->ev_c})
+    if (e) cudaEventDestroy(e);
+  delete m;
+}
+
+int64_t pcd_kv_bytes_per_token(const pcd_model* m) {
+  if (!m) return 0;
+  return static_cast<int64_t>(m->L) * 2 * m->Hkv * m->dh * 2;
+}
+
+int pcd_prefill_device(pcd_model* m, const int32_t* ids_device, int n, pcd_cache** out) {
+  if (!m || !ids_device || !out) return fail(PCD_ERR_INVALID_ARG, "NULL argument");
+  if (n < 1) return fail(PCD_ERR_INVALID_ARG, "empty prefix");
+  if (n > m->max_pos) return fail(PCD_ERR_TOO_LONG, "prefix longer than max_positions");
+  pcd_cache* c = nullptr;
+  PCD_TRY(new_cache(m, n, &c));
+  const int rc = run_prefill(m, ids_device, n, c, 0);
+  if (rc != PCD_OK) {
+    pcd_cache_free(c);
+    return rc;
+  }
+  c->len = n;
+  *out = c;
+  return PCD_OK;
+}
+
+int pcd_prefill(pcd_model* m, const int32_t* ids, int n, pcd_cache** out) {
+  if (!m || !ids || !out) return fail(PCD_ERR_INVALID_ARG, "NULL argument");
+  if (n < 1) return fail(PCD_ERR_INVALID_ARG, "empty prefix");
+  if (n > m->max_pos) return fail(PCD_ERR_TOO_LONG, "prefix longer than max_positions");
+  const int32_t* d_ids = nullptr;
+  PCD_TRY(upload_ids(m, ids, n, &d_ids));
+  return pcd_prefill_device(m, d_ids, n, out);
+}
+
+int pcd_prefill_extend(pcd_model* m, const pcd_cache* head, const int32_t* ids, int n, pcd_cache** out) {
+  if (!m || !head || !ids || !out) return fail(PCD_ERR_INVALID_ARG, "NULL argument");
+  if (head->m != m) return fail(PCD_ERR_SHAPE_MISMATCH, "cache belongs to another model");
+  if (n < 1) return fail(PCD_ERR_INVALID_ARG, "empty extension");
+  const int total = head->len + n;
+  if (total > m->max_pos) return fail(PCD_ERR_TOO_LONG, "prefix longer than max_positions");
+  const int32_t* d_ids = nullptr;
+  PCD_TRY(upload_ids(m, ids, n, &d_ids));
+  pcd_cache* c = nullptr;
+  PCD_TRY(new_cache(m, total, &c));
+  // copy the head's keys and values: per (layer, KV head) a block of head->len rows
+  const size_t row = static_cast<size_t>(m->dh) * 2;
+  for (bf16* const* pair : {&c->k, &c->v}) {
+    const bf16* src = (pair == &c->k) ? head->k : head->v;
+    const cudaError_t e = cudaMemcpy2DAsync(*pair, static_cast<size_t>(c->cap) * row, src,
+                                            static_cast<size_t>(head->cap) * row, head->len * row,
+                                            static_cast<size_t>(m->L) * m->Hkv, cudaMemcpyDeviceToDevice, m->stream);
+    if (e != cudaSuccess) {
+      pcd_cache_free(c);
+      return fail(PCD_ERR_CUDA, std::string("KV copy: ") + cudaGetErrorString(e));
+    }
+  }
+  const int rc = run_prefill(m, d_ids, n, c, head->len);
+  if (rc != PCD_OK) {
+    pcd_cache_free(c);
+    return rc;
+  }
+  c->len = total;
+  *out = c;
+  return PCD_OK;
+}
+
+int pcd_cache_length(const pcd_cache* c) { return c ? c->len : 0; }
+
+void pcd_cache_free(pcd_cache* c) {
+  if (!c) return;
+  if (c->m && c->mem) c->m->cache_pool.emplace_back(c->bytes, c->mem);
+  delete c;
+}
+
+int pcd_score(pcd_model* m, const pcd_cache* cache, const pcd_field* fields, int n_fields, pcd_field_result* out,
+              pcd_stats* stats) {
+  const pcd_cache* cs[1] = {cache};
+  const pcd_field* fs[1] = {fields};
+  int nf[1] = {n_fields};
+  pcd_field_result* os[1] = {out};
+  return score_impl(m, cs, fs, nf, 1, os, stats);
+}
+
+int pcd_score_batch(pcd_model* m, const pcd_cache* const* caches, const pcd_field* const* fields, const int* n_fields,
+                    int n_requests, pcd_field_result* const* out, pcd_stats* stats) {
+  return score_impl(m, caches, fields, n_fields, n_requests, out, stats);
+}
+
+int pcd_plan_create(pcd_model* m, const pcd_field* fields, int n_fields, pcd_plan** out) {
+  if (!m || !fields || !out || n_fields < 1) return fail(PCD_ERR_INVALID_ARG, "NULL argument or no fields");
+  pcd::HostPlan hp;
+  std::string msg;
+  const int rc = pcd::compile_fields(fields, n_fields, m->V, &hp, &msg);
+  if (rc != PCD_OK) return fail(rc, msg);
+  pcd_plan* p = new pcd_plan();
+  p->m = m;
+  std::vector<int32_t> blob;
+  plan_blob(m, hp, blob, p->view, nullptr);
+  if (cudaMalloc(&p->mem, blob.size() * 4) != cudaSuccess) {
+    cudaGetLastError();
+    delete p;
+    return fail(PCD_ERR_OOM, "plan allocation");
+  }
+  plan_blob(m, hp, blob, p->view, static_cast<const int32_t*>(p->mem));
+  if (cudaMemcpy(p->mem, blob.data(), blob.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess) {
+    cudaFree(p->mem);
+    delete p;
+    return fail(PCD_ERR_CUDA, "plan upload");
+  }
+  *out = p;
+  return PCD_OK;
+}
+
+void pcd_plan_free(pcd_plan* p) {
+  if (!p) return;
+  if (p->m && p->m->stream) cudaStreamSynchronize(p->m->stream);
+  if (p->mem) cudaFree(p->mem);
+  delete p;
+}
+
+int pcd_plan_result_floats(const pcd_plan* p) { return p ? p->view.result_floats() : 0; }
+
+int pcd_score_plan_device(pcd_model* m, const pcd_cache* cache, const pcd_plan* p, float* result_device) {
+  if (!m || !cache || !p || !result_device) return fail(PCD_ERR_INVALID_ARG, "NULL argument");
+  if (cache->m != m || p->m != m) return fail(PCD_ERR_SHAPE_MISMATCH, "cache or plan belongs to another model");
+  PCD_TRY(check_positions(m, cache->len, p->view.max_rel));
+  Segment s{cache, 0, p->view.T};
+  return run_branch(m, p->view, &s, 1, result_device);
+}
+
+int pcd_sync(pcd_model* m) {
+  if (!m) return fail(PCD_ERR_INVALID_ARG, "NULL model");
+  PCD_CUDA(cudaStreamSynchronize(m->stream));
+  return read_device_error(m);
+}
+
+int pcd_profile_enable(pcd_model* m, int on) {
+  if (!m) return fail(PCD_ERR_INVALID_ARG, "NULL model");
+  m->prof = on != 0;
+  m->prof_rec.clear();
+  m->ev_next = 0;
+  return PCD_OK;
+}
+
+int pcd_profile_read(pcd_model* m, int* launches, float* ms) {
+  if (!m || !launches || !ms) return fail(PCD_ERR_INVALID_ARG, "NULL argument");
+  PCD_CUDA(cudaStreamSynchronize(m->stream));
+  for (int i = 0; i < PCD_PROF_CLASSES; ++i) launches[i] = 0, ms[i] = 0.f;
+  for (auto& r : m->prof_rec) {
+    float t = 0.f;
+    cudaEventElapsedTime(&t, std::get<1>(r), std::get<2>(r));
+    launches[std::get<0>(r)]++;
+    ms[std::get<0>(r)] += t;
+  }
+  m->prof_rec.clear();
+  m->ev_next = 0;
+  return PCD_OK;
+}
+
+const char* pcd_strerror(int code) {
+  switch (code) {
+    case PCD_OK: return "ok";
+    case PCD_ERR_INVALID_ARG: return "invalid argument";
+    case PCD_ERR_TOO_MANY_CANDIDATES: return "more than 255 candidates in a field";
+    case PCD_ERR_TOO_FEW_CANDIDATES: return "fewer than 2 candidates in a field";
+    case PCD_ERR_EMPTY_LABEL: return "empty label";
+    case PCD_ERR_DUPLICATE_LABEL: return "duplicate label";
+    case PCD_ERR_PREFIX_LABEL: return "a label is a strict prefix of another";
+    case PCD_ERR_TOKEN_RANGE: return "token id out of range";
+    case PCD_ERR_SHAPE_MISMATCH: return "shape mismatch";
+    case PCD_ERR_OOM: return "out of memory";
+    case PCD_ERR_CUDA: return "CUDA error";
+    case PCD_ERR_DEVICE_TIMEOUT: return "device pipeline wait timed out";
+    case PCD_ERR_BAD_WEIGHTS: return "bad weights";
+    case PCD_ERR_TOO_LONG: return "position beyond max_positions";
+  }
+  return "unknown error";
+}
+
+const char* pcd_last_error(void) { return g_last_error.c_str(); }
+
+}  // extern "C"

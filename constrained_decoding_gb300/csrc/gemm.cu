@@ -103,6 +103,10 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, const EpiArgs& e,
         a.w += v[4 * j + 3];
         o4[j] = a;
       }
+    } else if constexpr (EPI == EPI_F32_STORE) {
+      float4* o4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(e.out) + static_cast<size_t>(row) * e.ldo + col0);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) o4[j] = make_float4(v[4 * j + 0], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
     } else if constexpr (EPI == EPI_F32_ATOMIC) {
       float4* o4 = reinterpret_cast<float4*>(reinterpret_cast<float*>(e.out) + static_cast<size_t>(row) * e.ldo + col0);
 #pragma unroll
@@ -408,6 +412,7 @@ int launch_gemm(const GemmShape& s, int epi, const EpiArgs& e, const GemmTiling&
     case EPI_F32_ATOMIC: return dispatch_tiling<EPI_F32_ATOMIC>(t, ma, mb, p, e, stream, sms);
     case EPI_SWIGLU: return dispatch_tiling<EPI_SWIGLU>(t, ma, mb, p, e, stream, sms);
     case EPI_READOUT: return dispatch_tiling<EPI_READOUT>(t, ma, mb, p, e, stream, sms);
+    case EPI_F32_STORE: return dispatch_tiling<EPI_F32_STORE>(t, ma, mb, p, e, stream, sms);
   }
   return -1;
 }

@@ -13,6 +13,7 @@ enum EpiKind : int {
   EPI_F32_ATOMIC = 2,  // out f32 [M][ldo] += D with atomics (any number of K splits)
   EPI_SWIGLU = 3,      // D columns (2f, 2f+1) = (gate_f, up_f); out bf16 [M][ldo]: silu(gate) * up
   EPI_READOUT = 4,     // vocabulary readout: per (row, N tile) max and sum-exp, plus gathered logits
+  EPI_F32_STORE = 5,   // out f32 [M][ldo] = D (one K split)
 };
 
 struct GemmShape {

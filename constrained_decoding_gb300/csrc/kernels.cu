@@ -1,0 +1,620 @@
+// Non-GEMM device steps of the PCD hot path: embedding gather, RMSNorm,
+// RoPE + KV write, prefill / prefix attention, branch-ancestor merge,
+// vocabulary log-sum-exp combine and field scoring.
+#include <cfloat>
+#include <cstdint>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace pcd {
+
+// ======================================================================= embed
+__global__ void embed_kernel(const int32_t* __restrict__ ids, int n, const bf16* __restrict__ E, int d, int vocab,
+                             float* __restrict__ x, int* err) {
+  const int t = blockIdx.x;
+  if (t >= n) return;
+  int id = ids[t];
+  if (id < 0 || id >= vocab) {
+    if (threadIdx.x == 0) record_error(err, DEV_BAD_INDEX);
+    id = 0;
+  }
+  const uint4* src = reinterpret_cast<const uint4*>(E + static_cast<size_t>(id) * d);
+  float4* dst = reinterpret_cast<float4*>(x + static_cast<size_t>(t) * d);
+  for (int i = threadIdx.x; i < d / 8; i += blockDim.x) {
+    uint4 w = src[i];
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
+    float2 a = __bfloat1622float2(h[0]), b = __bfloat1622float2(h[1]), c = __bfloat1622float2(h[2]),
+           e = __bfloat1622float2(h[3]);
+    dst[2 * i] = make_float4(a.x, a.y, b.x, b.y);
+    dst[2 * i + 1] = make_float4(c.x, c.y, e.x, e.y);
+  }
+}
+
+int launch_embed(const int32_t* ids, int n, const bf16* E, int d, int vocab, float* x, int* err, cudaStream_t s) {
+  if (n <= 0) return 0;
+  embed_kernel<<<n, 128, 0, s>>>(ids, n, E, d, vocab, x, err);
+  return cudaGetLastError();
+}
+
+// ===================================================================== rmsnorm
+// One warp per row; fp32 statistics.
+__global__ void rmsnorm_kernel(const float* __restrict__ x, int ldx, const int32_t* __restrict__ rows, int n, int d,
+                               const float* __restrict__ gain, float eps, bf16* __restrict__ out, int ldo) {
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= n) return;
+  const int src = rows ? rows[r] : r;
+  const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(src) * ldx);
+  float ss = 0.f;
+  for (int i = lane; i < d / 4; i += 32) {
+    float4 v = xr[i];
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  const float inv = rsqrtf(ss / static_cast<float>(d) + eps);
+  const float4* g4 = reinterpret_cast<const float4*>(gain);
+  uint2* o2 = reinterpret_cast<uint2*>(out + static_cast<size_t>(r) * ldo);
+  for (int i = lane; i < d / 4; i += 32) {
+    float4 v = xr[i], g = g4[i];
+    uint2 w;
+    w.x = pack_bf16x2(v.x * inv * g.x, v.y * inv * g.y);
+    w.y = pack_bf16x2(v.z * inv * g.z, v.w * inv * g.w);
+    o2[i] = w;
+  }
+}
+
+int launch_rmsnorm(const float* x, int ldx, const int32_t* rows, int n, int d, const float* gain, float eps, bf16* out,
+                   int ldo, cudaStream_t s) {
+  if (n <= 0) return 0;
+  const int wpb = 8;
+  rmsnorm_kernel<<<(n + wpb - 1) / wpb, wpb * 32, 0, s>>>(x, ldx, rows, n, d, gain, eps, out, ldo);
+  return cudaGetLastError();
+}
+
+// ====================================================================== rope_kv
+// Thread per (token, head, rotation pair).  Rotate-half pairing (i, i + DH/2),
+// angle pos * theta^(-2i/DH) from a (cos, sin) table built in double precision.
+__global__ void rope_kv_kernel(RopeArgs a) {
+  const int half = a.DH / 2;
+  const int heads = a.Hq + 2 * a.Hkv;
+  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const long long total = static_cast<long long>(a.n) * heads * half;
+  if (idx >= total) return;
+  const int i = static_cast<int>(idx % half);
+  const int h = static_cast<int>((idx / half) % heads);
+  const int t = static_cast<int>(idx / (static_cast<long long>(half) * heads));
+  int pos = a.base + (a.rel ? a.rel[t] : t);
+  if (pos < 0 || pos >= a.max_pos) {
+    record_error(a.err, DEV_BAD_INDEX);
+    pos = 0;
+  }
+  const float* src = a.qkv + static_cast<size_t>(t) * a.ldqkv + h * a.DH;
+  const float x1 = src[i], x2 = src[i + half];
+  if (h < a.Hq + a.Hkv) {
+    const float2 cs = a.cs[static_cast<size_t>(pos) * half + i];
+    const float y1 = x1 * cs.x - x2 * cs.y;
+    const float y2 = x2 * cs.x + x1 * cs.y;
+    bf16* dst;
+    if (h < a.Hq) {
+      dst = a.q + (static_cast<size_t>(t) * a.Hq + h) * a.DH;
+    } else {
+      dst = a.k_dst + (static_cast<size_t>(h - a.Hq) * a.kv_head_stride + a.kv_row0 + t) * a.DH;
+    }
+    dst[i] = f2bf(y1);
+    dst[i + half] = f2bf(y2);
+  } else {
+    bf16* dst = a.v_dst + (static_cast<size_t>(h - a.Hq - a.Hkv) * a.kv_head_stride + a.kv_row0 + t) * a.DH;
+    dst[i] = f2bf(x1);
+    dst[i + half] = f2bf(x2);
+  }
+}
+
+int launch_rope_kv(const RopeArgs& a, cudaStream_t s) {
+  if (a.n <= 0) return 0;
+  const long long total = static_cast<long long>(a.n) * (a.Hq + 2 * a.Hkv) * (a.DH / 2);
+  rope_kv_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+// ==================================================================== attention
+// Flash attention (online softmax, fp32 statistics) with mma.sync bf16
+// tensor-core tiles.  A CTA owns 64 query rows of one KV head; the rows are
+// (token, query head of the group) pairs, so every key tile loaded into
+// shared memory serves all query heads that share it.  Key j is visible to a
+// query at position p iff j <= p (causal prefill; branch queries sit after
+// the whole prefix and see all of it).
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem, bool valid) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  const int n = valid ? 16 : 0;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem), "r"(n) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(s));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(p));
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(s));
+}
+__device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "{%0, %1, %2, %3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+template <int DH>
+struct AttnSmem {
+  static constexpr int LDS = DH + 8;  // padded row: conflict-free ldmatrix
+  static constexpr int BYTES = (64 + 4 * 64) * LDS * 2 + 64 * 4;
+};
+
+template <int DH>
+__global__ void __launch_bounds__(128) attn_kernel(AttnArgs a) {
+  constexpr int LDS = AttnSmem<DH>::LDS;
+  constexpr int KS = DH / 16;  // k-steps over the head dim
+  constexpr int ND = DH / 8;   // 8-wide output column blocks
+  extern __shared__ __align__(16) uint8_t attn_smem[];
+  bf16* sQ = reinterpret_cast<bf16*>(attn_smem);
+  bf16* sK = sQ + 64 * LDS;          // [2][64][LDS]
+  bf16* sV = sK + 2 * 64 * LDS;      // [2][64][LDS]
+  int* sPos = reinterpret_cast<int*>(sV + 2 * 64 * LDS);
+
+  const int G = a.Hq / a.Hkv;
+  const int rows = a.n_tok * G;
+  const int nrb = gridDim.x;
+  const int rb = a.causal_heavy_first ? (nrb - 1 - blockIdx.x) : blockIdx.x;
+  const int hk = blockIdx.y;
+  const int split = blockIdx.z;
+  const int r0 = rb * 64;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int gid = lane >> 2, tq = lane & 3;
+
+  // query rows: positions, and the Q tile
+  if (tid < 64) {
+    const int r = r0 + tid;
+    int p = -1;
+    if (r < rows) {
+      const int t = a.tok0 + r / G;
+      p = a.base + (a.rel ? a.rel[t] : t);
+    }
+    sPos[tid] = p;
+  }
+  constexpr int QCH = DH / 8;  // 16-byte chunks per row
+  for (int c = tid; c < 64 * QCH; c += 128) {
+    const int rr = c / QCH, ch = c % QCH;
+    const int r = r0 + rr;
+    const bool ok = r < rows;
+    const int t = a.tok0 + (ok ? r / G : 0), g = ok ? r % G : 0;
+    const bf16* src = a.q + (static_cast<size_t>(t) * a.Hq + hk * G + g) * DH + ch * 8;
+    cp_async16(sQ + rr * LDS + ch * 8, src, ok);
+  }
+  cp_async_commit();
+  __syncthreads();
+  int pmax = -1;
+  for (int i = 0; i < 64; ++i) pmax = max(pmax, sPos[i]);
+  const int k_lo = split * a.split_len;
+  const int k_hi = min(min(a.n_keys, (split + 1) * a.split_len), pmax + 1);
+  const int n_tiles = k_hi > k_lo ? (k_hi - k_lo + 63) / 64 : 0;
+
+  const bf16* kbase = a.k + static_cast<size_t>(hk) * a.kv_head_stride * DH;
+  const bf16* vbase = a.v + static_cast<size_t>(hk) * a.kv_head_stride * DH;
+  auto load_kv = [&](int tile, int buf) {
+    const int j0 = k_lo + tile * 64;
+    for (int c = tid; c < 64 * QCH; c += 128) {
+      const int kr = c / QCH, ch = c % QCH;
+      const int j = j0 + kr;
+      const bool ok = j < k_hi;
+      const size_t off = static_cast<size_t>(ok ? j : 0) * DH + ch * 8;
+      cp_async16(sK + (buf * 64 + kr) * LDS + ch * 8, kbase + off, ok);
+      cp_async16(sV + (buf * 64 + kr) * LDS + ch * 8, vbase + off, ok);
+    }
+    cp_async_commit();
+  };
+  // Q fragments (the Q group was committed first)
+  if (n_tiles > 0) {
+    load_kv(0, 0);
+    cp_async_wait<1>();
+  } else {
+    cp_async_wait<0>();
+  }
+  __syncthreads();
+  uint32_t qf[KS][4];
+#pragma unroll
+  for (int kk = 0; kk < KS; ++kk)
+    ldsm_x4(qf[kk], sQ + (warp * 16 + (lane & 15)) * LDS + kk * 16 + (lane >> 4) * 8);
+
+  const int pos_lo = sPos[warp * 16 + gid], pos_hi = sPos[warp * 16 + gid + 8];
+  float o[ND][4];
+#pragma unroll
+  for (int i = 0; i < ND; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
+
+  for (int tile = 0; tile < n_tiles; ++tile) {
+    const int buf = tile & 1;
+    if (tile + 1 < n_tiles) {
+      load_kv(tile + 1, buf ^ 1);
+      cp_async_wait<1>();
+    } else {
+      cp_async_wait<0>();
+    }
+    __syncthreads();
+    const bf16* K = sK + buf * 64 * LDS;
+    const bf16* V = sV + buf * 64 * LDS;
+    const int j0 = k_lo + tile * 64;
+
+    float s[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
+#pragma unroll
+    for (int nb2 = 0; nb2 < 4; ++nb2) {
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        uint32_t b[4];
+        ldsm_x4(b, K + (nb2 * 16 + (lane >> 4) * 8 + (lane & 7)) * LDS + kk * 16 + ((lane >> 3) & 1) * 8);
+        mma16816(s[2 * nb2], qf[kk], b[0], b[1]);
+        mma16816(s[2 * nb2 + 1], qf[kk], b[2], b[3]);
+      }
+    }
+    // scale, mask, online softmax (log2 units)
+    float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+    for (int nb = 0; nb < 8; ++nb) {
+      const int j = j0 + nb * 8 + tq * 2;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const bool in = (j + e) < k_hi;
+        float v0 = s[nb][e] * a.scale_log2, v1 = s[nb][2 + e] * a.scale_log2;
+        if (!in || j + e > pos_lo) v0 = -INFINITY;
+        if (!in || j + e > pos_hi) v1 = -INFINITY;
+        s[nb][e] = v0;
+        s[nb][2 + e] = v1;
+        mx_lo = fmaxf(mx_lo, v0);
+        mx_hi = fmaxf(mx_hi, v1);
+      }
+    }
+#pragma unroll
+    for (int off = 1; off <= 2; off <<= 1) {
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, off));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, off));
+    }
+    const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+    const float c_lo = (mn_lo == -INFINITY) ? 1.f : exp2f(m_lo - mn_lo);
+    const float c_hi = (mn_hi == -INFINITY) ? 1.f : exp2f(m_hi - mn_hi);
+    m_lo = mn_lo;
+    m_hi = mn_hi;
+    float rs_lo = 0.f, rs_hi = 0.f;
+#pragma unroll
+    for (int nb = 0; nb < 8; ++nb) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const float p0 = (mn_lo == -INFINITY) ? 0.f : exp2f(s[nb][e] - mn_lo);
+        const float p1 = (mn_hi == -INFINITY) ? 0.f : exp2f(s[nb][2 + e] - mn_hi);
+        s[nb][e] = p0;
+        s[nb][2 + e] = p1;
+        rs_lo += p0;
+        rs_hi += p1;
+      }
+    }
+    l_lo = l_lo * c_lo + rs_lo;
+    l_hi = l_hi * c_hi + rs_hi;
+#pragma unroll
+    for (int i = 0; i < ND; ++i) {
+      o[i][0] *= c_lo;
+      o[i][1] *= c_lo;
+      o[i][2] *= c_hi;
+      o[i][3] *= c_hi;
+    }
+    // O += P V
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) {
+      uint32_t pa[4];
+      pa[0] = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
+      pa[1] = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
+      pa[2] = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+      pa[3] = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+#pragma unroll
+      for (int nd2 = 0; nd2 < DH / 16; ++nd2) {
+        uint32_t b[4];
+        ldsm_x4_t(b, V + (kk * 16 + ((lane >> 3) & 1) * 8 + (lane & 7)) * LDS + nd2 * 16 + (lane >> 4) * 8);
+        mma16816(o[2 * nd2], pa, b[0], b[1]);
+        mma16816(o[2 * nd2 + 1], pa, b[2], b[3]);
+      }
+    }
+    __syncthreads();  // the buffer is refilled next iteration
+  }
+
+  // finalise: full row sums across the quad
+#pragma unroll
+  for (int off = 1; off <= 2; off <<= 1) {
+    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, off);
+    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, off);
+  }
+  const float il_lo = l_lo > 0.f ? 1.f / l_lo : 0.f;
+  const float il_hi = l_hi > 0.f ? 1.f / l_hi : 0.f;
+  const int rlo = r0 + warp * 16 + gid, rhi = rlo + 8;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    const int r = half ? rhi : rlo;
+    if (r >= rows) continue;
+    const float il = half ? il_hi : il_lo;
+    const int t = a.tok0 + r / G, g = r % G;
+    if (!a.partial) {
+      bf16* dst = a.out + static_cast<size_t>(t) * a.ld_out + (hk * G + g) * DH;
+#pragma unroll
+      for (int nd = 0; nd < ND; ++nd) {
+        const int d = nd * 8 + tq * 2;
+        *reinterpret_cast<uint32_t*>(dst + d) = pack_bf16x2(o[nd][2 * half] * il, o[nd][2 * half + 1] * il);
+      }
+    } else {
+      const size_t prow = (static_cast<size_t>(split) * a.Hkv + hk) * a.part_rows + static_cast<size_t>(t) * G + g;
+      float* dst = a.part_o + prow * DH;
+#pragma unroll
+      for (int nd = 0; nd < ND; ++nd) {
+        const int d = nd * 8 + tq * 2;
+        *reinterpret_cast<float2*>(dst + d) = make_float2(o[nd][2 * half] * il, o[nd][2 * half + 1] * il);
+      }
+      if (tq == 0) a.part_ml[prow] = make_float2(half ? m_hi : m_lo, half ? l_hi : l_lo);
+    }
+  }
+}
+
+template <int DH>
+static int launch_attn_t(const AttnArgs& a, cudaStream_t s) {
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t r = cudaFuncSetAttribute(attn_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         AttnSmem<DH>::BYTES);
+    if (r != cudaSuccess) return r;
+    attr = true;
+  }
+  const int G = a.Hq / a.Hkv;
+  const int rows = a.n_tok * G;
+  dim3 grid((rows + 63) / 64, a.Hkv, a.n_splits);
+  attn_kernel<DH><<<grid, 128, AttnSmem<DH>::BYTES, s>>>(a);
+  return cudaGetLastError();
+}
+
+int launch_attention(const AttnArgs& a, cudaStream_t s) {
+  if (a.n_tok <= 0) return 0;
+  switch (a.DH) {
+    case 16: return launch_attn_t<16>(a, s);
+    case 64: return launch_attn_t<64>(a, s);
+    case 128: return launch_attn_t<128>(a, s);
+  }
+  return -1;
+}
+
+// ================================================================ branch merge
+// One warp per (branch token, query head): merges the prefix partials of all
+// key splits with the token's own ancestors in the branch (scaffold chain and
+// trie path, the token itself included).
+template <int DH>
+__global__ void branch_merge_kernel(MergeArgs a) {
+  constexpr int EPT = DH >= 32 ? DH / 32 : 1;
+  const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (w >= a.n_tok * a.Hq) return;
+  const int t = w / a.Hq, h = w % a.Hq;
+  const int G = a.Hq / a.Hkv;
+  const int hk = h / G, g = h % G;
+  const int rows = a.n_tok * G;
+  const int r = t * G + g;
+  float q[EPT], acc[EPT];
+  const bf16* qp = a.q + (static_cast<size_t>(t) * a.Hq + h) * DH;
+#pragma unroll
+  for (int i = 0; i < EPT; ++i) {
+    const int d = lane + 32 * i;
+    q[i] = d < DH ? bf2f(qp[d]) : 0.f;
+    acc[i] = 0.f;
+  }
+  float m = -INFINITY, l = 0.f;
+  for (int sp = 0; sp < a.n_splits; ++sp) {
+    const size_t prow = (static_cast<size_t>(sp) * a.Hkv + hk) * rows + r;
+    const float2 ml = a.part_ml[prow];
+    if (!(ml.y > 0.f)) continue;
+    const float mn = fmaxf(m, ml.x);
+    const float co = exp2f(m - mn), cs = exp2f(ml.x - mn);
+    const float* po = a.part_o + prow * DH;
+#pragma unroll
+    for (int i = 0; i < EPT; ++i) {
+      const int d = lane + 32 * i;
+      const float ov = d < DH ? po[d] : 0.f;
+      acc[i] = acc[i] * co + ov * ml.y * cs;
+    }
+    l = l * co + ml.y * cs;
+    m = mn;
+  }
+  for (int ai = a.anc_off[t]; ai < a.anc_off[t + 1]; ++ai) {
+    const int j = a.anc_idx[ai];
+    const bf16* kp = a.kb + (static_cast<size_t>(hk) * a.n_tok + j) * DH;
+    const bf16* vp = a.vb + (static_cast<size_t>(hk) * a.n_tok + j) * DH;
+    float dot = 0.f;
+#pragma unroll
+    for (int i = 0; i < EPT; ++i) {
+      const int d = lane + 32 * i;
+      if (d < DH) dot += q[i] * bf2f(kp[d]);
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    const float sc = dot * a.scale_log2;
+    const float mn = fmaxf(m, sc);
+    const float co = exp2f(m - mn), p = exp2f(sc - mn);
+#pragma unroll
+    for (int i = 0; i < EPT; ++i) {
+      const int d = lane + 32 * i;
+      acc[i] = acc[i] * co + (d < DH ? p * bf2f(vp[d]) : 0.f);
+    }
+    l = l * co + p;
+    m = mn;
+  }
+  const float il = l > 0.f ? 1.f / l : 0.f;
+  bf16* dst = a.out + static_cast<size_t>(t) * a.ld_out + h * DH;
+#pragma unroll
+  for (int i = 0; i < EPT; ++i) {
+    const int d = lane + 32 * i;
+    if (d < DH) dst[d] = f2bf(acc[i] * il);
+  }
+}
+
+int launch_branch_merge(const MergeArgs& a, cudaStream_t s) {
+  const int warps = a.n_tok * a.Hq;
+  if (warps <= 0) return 0;
+  const int blocks = (warps + 7) / 8;
+  switch (a.DH) {
+    case 16: branch_merge_kernel<16><<<blocks, 256, 0, s>>>(a); break;
+    case 64: branch_merge_kernel<64><<<blocks, 256, 0, s>>>(a); break;
+    case 128: branch_merge_kernel<128><<<blocks, 256, 0, s>>>(a); break;
+    default: return -1;
+  }
+  return cudaGetLastError();
+}
+
+// ================================================================ lse combine
+__global__ void lse_combine_kernel(const float2* __restrict__ part, int n_tiles, int R, float* __restrict__ lse) {
+  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= R) return;
+  float m = -INFINITY;
+  for (int i = lane; i < n_tiles; i += 32) m = fmaxf(m, part[static_cast<size_t>(i) * R + r].x);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float sum = 0.f;
+  for (int i = lane; i < n_tiles; i += 32) {
+    const float2 p = part[static_cast<size_t>(i) * R + r];
+    sum += p.y * __expf(p.x - m);
+  }
+#pragma unroll
+  for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  if (lane == 0) lse[r] = m + __logf(sum);
+}
+
+int launch_lse_combine(const float2* part, int n_tiles, int R, float* lse, cudaStream_t s) {
+  if (R <= 0) return 0;
+  lse_combine_kernel<<<(R + 7) / 8, 256, 0, s>>>(part, n_tiles, R, lse);
+  return cudaGetLastError();
+}
+
+// ====================================================================== score
+// One CTA per field.  Label score s_c = sum over its path of (z - lse); then
+// the candidate-only softmax at temperature T, the argmax (lowest index on
+// ties), the candidate mass sum_c exp(s_c), the top-2 margin of s and the
+// first-decision mass (distinct first tokens at the root readout row).
+__global__ void __launch_bounds__(256) score_kernel(ScoreArgs a) {
+  const int f = blockIdx.x;
+  const int c0 = a.fld_lab[f], c1 = a.fld_lab[f + 1];
+  const int nl = c1 - c0;
+  const float T = a.temp[f];
+  __shared__ float s_sc[256];
+  __shared__ float red[32];
+  __shared__ int redi[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+
+  // scores (labels beyond 256 per field are rejected by the host)
+  float sc = -INFINITY;
+  if (tid < nl) {
+    const int c = c0 + tid;
+    float acc = 0.f;
+    for (int i = a.lab_off[c]; i < a.lab_off[c + 1]; ++i) {
+      const int e = a.path[i];
+      acc += a.z[e] - a.lse[a.child_row[e]];
+    }
+    sc = acc;
+    s_sc[tid] = acc;
+  }
+  // block max of s (and its first index), block max of s/T
+  auto block_max_idx = [&](float v, int idx, float& out_v, int& out_i) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+      if (ov > v || (ov == v && oi < idx)) v = ov, idx = oi;
+    }
+    if (lane == 0) red[warp] = v, redi[warp] = idx;
+    __syncthreads();
+    if (warp == 0) {
+      v = lane < nw ? red[lane] : -INFINITY;
+      idx = lane < nw ? redi[lane] : 0x7fffffff;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, idx, o);
+        if (ov > v || (ov == v && oi < idx)) v = ov, idx = oi;
+      }
+      if (lane == 0) red[0] = v, redi[0] = idx;
+    }
+    __syncthreads();
+    out_v = red[0];
+    out_i = redi[0];
+    __syncthreads();
+  };
+  auto block_sum = [&](float v) {
+#pragma unroll
+    for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+      v = lane < nw ? red[lane] : 0.f;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) red[0] = v;
+    }
+    __syncthreads();
+    const float r = red[0];
+    __syncthreads();
+    return r;
+  };
+  float smax;
+  int top;
+  block_max_idx(sc, tid < nl ? tid : 0x7fffffff, smax, top);
+  // second best score: max over everything but the argmax
+  float s2;
+  int i2;
+  block_max_idx((tid < nl && tid != top) ? sc : -INFINITY, tid, s2, i2);
+  const float es = tid < nl ? __expf(sc - smax) : 0.f;
+  const float sum_es = block_sum(es);
+  const float ea = tid < nl ? __expf((sc - smax) / T) : 0.f;
+  const float sum_ea = block_sum(ea);
+  // first-decision mass at the field's root readout row
+  const int root = a.fld_root[f];
+  float fm = 0.f;
+  for (int e = a.row_ch[root] + tid; e < a.row_ch[root + 1]; e += blockDim.x) fm += __expf(a.z[e] - a.lse[root]);
+  fm = block_sum(fm);
+
+  if (tid < nl) {
+    a.out_probs[c0 + tid] = ea / sum_ea;
+    a.out_logprobs[c0 + tid] = sc;
+  }
+  if (tid == 0) {
+    const float lm = smax + __logf(sum_es);
+    float* o = a.out_field + static_cast<size_t>(f) * 8;
+    o[0] = static_cast<float>(top);
+    o[1] = __expf(lm);
+    o[2] = lm;
+    o[3] = nl > 1 ? smax - s2 : INFINITY;
+    o[4] = fm;
+    o[5] = static_cast<float>(nl);
+    o[6] = 0.f;
+    o[7] = 0.f;
+  }
+}
+
+int launch_score(const ScoreArgs& a, cudaStream_t s) {
+  if (a.n_fields <= 0) return 0;
+  score_kernel<<<a.n_fields, 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace pcd

@@ -1,0 +1,92 @@
+// Host launchers of the non-GEMM device steps of the PCD hot path.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace pcd {
+
+using bf16 = __nv_bfloat16;
+
+// x[t][0..d) = E[ids[t]][0..d) as fp32 (the residual stream starts here).
+int launch_embed(const int32_t* ids, int n, const bf16* E, int d, int vocab, float* x, int* err, cudaStream_t s);
+
+// out[r] = bf16( x[src] / sqrt(mean(x[src]^2) + eps) * gain ), src = rows ? rows[r] : r.
+int launch_rmsnorm(const float* x, int ldx, const int32_t* rows, int n, int d, const float* gain, float eps, bf16* out,
+                   int ldo, cudaStream_t s);
+
+struct RopeArgs {
+  const float* qkv;       // [n][ldqkv] fp32: q heads, then k heads, then v heads
+  int ldqkv, n, Hq, Hkv, DH;
+  const float2* cs;       // [max_pos][DH/2] (cos, sin)
+  int max_pos;
+  const int32_t* rel;     // position of token t = base + (rel ? rel[t] : t)
+  int base;
+  bf16* q;                // [n][Hq][DH]
+  bf16* k_dst;            // K row of token t: k_dst + (h * kv_head_stride + kv_row0 + t) * DH
+  bf16* v_dst;
+  int64_t kv_head_stride; // elements between KV heads
+  int kv_row0;
+  int* err;
+};
+int launch_rope_kv(const RopeArgs& a, cudaStream_t s);
+
+struct AttnArgs {
+  const bf16* q;            // [tok0 + n_tok][Hq][DH]: this launch's query tokens are tok0 .. tok0+n_tok-1
+  int n_tok, Hq, Hkv, DH;
+  int tok0;                 // first token (also offsets rel, out and the partial rows)
+  int part_rows;            // rows of the partial arrays per (split, KV head): all tokens x G
+  const bf16* k;            // this layer's keys: k + (h * kv_head_stride + j) * DH, j < n_keys
+  const bf16* v;
+  int64_t kv_head_stride;
+  int n_keys;
+  const int32_t* rel;       // query position = base + (rel ? rel[t] : t); key j is visible iff j <= position
+  int base;
+  int n_splits, split_len;  // keys are cut into n_splits ranges of split_len (a multiple of 64)
+  float scale_log2;         // log2(e) / sqrt(DH)
+  bf16* out;                // n_splits == 1 and !partial: out[t][h * DH + d] (normalised)
+  int ld_out;
+  float* part_o;            // partial: [split][Hkv][part_rows][DH] normalised by the split's own l
+  float2* part_ml;          // partial: [split][Hkv][part_rows] (max, sum) in log2 units
+  int partial;
+  int causal_heavy_first;   // schedule the row blocks with the most keys first
+};
+int launch_attention(const AttnArgs& a, cudaStream_t s);
+
+struct MergeArgs {
+  const bf16* q;            // [n_tok][Hq][DH]
+  int n_tok, Hq, Hkv, DH;
+  const float* part_o;      // prefix partials from launch_attention (partial = 1)
+  const float2* part_ml;
+  int n_splits;
+  const bf16* kb;           // branch keys/values [Hkv][n_tok][DH]
+  const bf16* vb;
+  const int32_t* anc_off;   // [n_tok + 1]: ancestors (incl. itself) of token t in the branch batch
+  const int32_t* anc_idx;
+  float scale_log2;
+  bf16* out;                // out[t][h * DH + d]
+  int ld_out;
+};
+int launch_branch_merge(const MergeArgs& a, cudaStream_t s);
+
+// lse[r] = log sum_tiles sum exp(z) from per-tile (max, sum exp(z - max)).
+int launch_lse_combine(const float2* part, int n_tiles, int R, float* lse, cudaStream_t s);
+
+struct ScoreArgs {
+  const float* z;           // gathered candidate logits, one per child entry
+  const float* lse;         // [R]
+  const int32_t* child_row; // readout row of each child entry
+  const int32_t* lab_off;   // [n_labels_total + 1] CSR into path_entries
+  const int32_t* path;      // child entry of every step of every label path
+  const int32_t* fld_lab;   // [n_fields + 1] labels of each field
+  const int32_t* fld_root;  // root readout row of each field
+  const int32_t* row_ch;    // [R + 1] child entries of each readout row
+  const float* temp;        // [n_fields]
+  int n_fields;
+  float* out_field;         // [n_fields][8]: label, mass, log_mass, margin, first_mass, n_labels, 0, 0
+  float* out_probs;         // [n_labels_total]
+  float* out_logprobs;      // [n_labels_total]
+};
+int launch_score(const ScoreArgs& a, cudaStream_t s);
+
+}  // namespace pcd

@@ -1,0 +1,42 @@
+// Branch compiler: a closed schema's fields -> one packed branch batch.
+//
+// Each field contributes its scaffold tokens and the internal nodes of the
+// trie of its label token paths (a label's last token is only predicted,
+// never fed).  Readout rows are the scaffold's last token and every internal
+// trie node; each readout row's children are the candidate next tokens.  A
+// label's score is the sum, along its path, of (logit - log-sum-exp) at the
+// readout rows ("When one token is not enough", How TypeSafe's Jev Might
+// Work: follow shared prefixes and multiply the per-token probabilities).
+#pragma once
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include "pcd.h"
+
+namespace pcd {
+
+struct HostPlan {
+  int n_fields = 0, T = 0, R = 0, n_children = 0, n_labels = 0, n_path = 0;
+  int max_rel = 0;                 // largest relative position
+  std::vector<int32_t> tok;        // [T] token id of each branch token
+  std::vector<int32_t> rel;        // [T] position after the prefix end: k for scaffold token k,
+                                   //     S + depth - 1 for a trie node at depth >= 1
+  std::vector<int32_t> anc_off;    // [T + 1] ancestors of each token (same field, itself included)
+  std::vector<int32_t> anc_idx;
+  std::vector<int32_t> ro_tok;     // [R] branch token whose output is read
+  std::vector<int32_t> row_ch;     // [R + 1] child entries of each readout row
+  std::vector<int32_t> ch_tok;     // [n_children] candidate token id of each child entry
+  std::vector<int32_t> child_row;  // [n_children] its readout row
+  std::vector<int32_t> lab_off;    // [n_labels + 1] path steps of each label
+  std::vector<int32_t> path;       // [n_path] child entry of each step
+  std::vector<int32_t> fld_lab;    // [n_fields + 1] labels of each field
+  std::vector<int32_t> fld_root;   // [n_fields] readout row of the field's scaffold end
+  std::vector<float> temp;         // [n_fields]
+};
+
+// Appends `fields` to `p` (so several requests can share one batch).  On
+// error returns a PCD_ERR_* code and sets *msg; `p` is then unspecified.
+int compile_fields(const pcd_field* fields, int n_fields, int vocab, HostPlan* p, std::string* msg);
+
+}  // namespace pcd

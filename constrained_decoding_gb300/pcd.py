@@ -1,0 +1,305 @@
+"""Python binding of the PCD C ABI (include/pcd.h), same names as the C
+entry points.  Argument marshalling only: numpy arrays and torch tensors are
+turned into pointers, results are copied into Python objects; every step of
+the hot path runs in the library's CUDA kernels.
+"""
+from __future__ import annotations
+
+import ctypes
+import weakref
+from dataclasses import dataclass
+from typing import List, Optional, Sequence
+
+import numpy as np
+
+from . import _decls as D
+from ._lib import load
+
+
+class PCDError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        lib = load()
+        msg = lib.pcd_strerror(code).decode()
+        detail = lib.pcd_last_error().decode()
+        super().__init__(f"{where}: {msg} ({code}): {detail}")
+        self.code = code
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != 0:
+        raise PCDError(rc, where)
+
+
+def _i32(a) -> np.ndarray:
+    return np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+
+
+def _ptr_i32(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_int32))
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        return None
+    return int(getattr(stream, "cuda_stream", stream))
+
+
+@dataclass
+class FieldResult:
+    probs: np.ndarray
+    logprobs: np.ndarray
+    label: int
+    mass: float
+    log_mass: float
+    margin: float
+    first_mass: float
+
+
+# ----------------------------------------------------------------- handles
+class Model:
+    def __init__(self, handle: int, cfg: D.pcd_model_config):
+        self.handle = handle
+        self.cfg = cfg
+        self._children = weakref.WeakSet()
+
+    def free(self) -> None:
+        if self.handle:
+            for ch in list(self._children):
+                ch.free()
+            load().pcd_model_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+class Cache:
+    def __init__(self, model: Model, handle: int):
+        self.model = model
+        self.handle = handle
+        model._children.add(self)
+
+    @property
+    def length(self) -> int:
+        return load().pcd_cache_length(self.handle)
+
+    def free(self) -> None:
+        if self.handle:
+            load().pcd_cache_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+class Plan:
+    def __init__(self, model: Model, handle: int):
+        self.model = model
+        self.handle = handle
+        model._children.add(self)
+
+    @property
+    def result_floats(self) -> int:
+        return load().pcd_plan_result_floats(self.handle)
+
+    def free(self) -> None:
+        if self.handle:
+            load().pcd_plan_free(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass
+
+
+# ------------------------------------------------------------------ models
+def model_config(cfg, max_positions: int = 0) -> D.pcd_model_config:
+    """A pcd_model_config from any object with the decoder-shape attributes."""
+    return D.pcd_model_config(cfg.n_layers, cfg.d_model, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.d_ff,
+                              cfg.vocab, float(cfg.rms_eps), float(cfg.rope_theta), 1 if cfg.tied_embedding else 0,
+                              max_positions)
+
+
+def pcd_load_weights(path: str, cfg=None, stream=None, max_positions: int = 0) -> Model:
+    lib = load()
+    c = model_config(cfg, max_positions) if cfg is not None else None
+    out = ctypes.c_void_p()
+    _check(lib.pcd_load_weights(ctypes.byref(c) if c is not None else None, path.encode(),
+                                _stream_handle(stream), ctypes.byref(out)), "pcd_load_weights")
+    return Model(out.value, c)
+
+
+def pcd_load_weights_host(weights, stream=None, max_positions: int = 0) -> Model:
+    """`weights` has cfg, embed, layers[i][attn_norm, wq, wk, wv, wo, mlp_norm,
+    w_gate, w_up, w_down], final_norm, lm_head (None when tied); matrices are
+    float32 or bf16 bit patterns (uint16)."""
+    lib = load()
+    c = model_config(weights.cfg, max_positions)
+    arrays = [weights.embed]
+    for lw in weights.layers:
+        arrays += [np.asarray(lw["attn_norm"], np.float32), lw["wq"], lw["wk"], lw["wv"], lw["wo"],
+                   np.asarray(lw["mlp_norm"], np.float32), lw["w_gate"], lw["w_up"], lw["w_down"]]
+    arrays.append(np.asarray(weights.final_norm, np.float32))
+    if weights.lm_head is not None:
+        arrays.append(weights.lm_head)
+    arrays = [np.ascontiguousarray(a) for a in arrays]
+    dtype = 2 if weights.embed.dtype == np.uint16 else 1
+    ptrs = (ctypes.c_void_p * len(arrays))(*[a.ctypes.data for a in arrays])
+    out = ctypes.c_void_p()
+    _check(lib.pcd_load_weights_host(ctypes.byref(c), ptrs, dtype, _stream_handle(stream), ctypes.byref(out)),
+           "pcd_load_weights_host")
+    return Model(out.value, c)
+
+
+def pcd_model_free(model: Model) -> None:
+    model.free()
+
+
+def pcd_kv_bytes_per_token(model: Model) -> int:
+    return int(load().pcd_kv_bytes_per_token(model.handle))
+
+
+# ----------------------------------------------------------------- prefill
+def pcd_prefill(model: Model, ids) -> Cache:
+    ids = _i32(ids)
+    out = ctypes.c_void_p()
+    _check(load().pcd_prefill(model.handle, _ptr_i32(ids), len(ids), ctypes.byref(out)), "pcd_prefill")
+    return Cache(model, out.value)
+
+
+def pcd_prefill_device(model: Model, ids_device) -> Cache:
+    """ids_device: a CUDA int32 tensor (torch) or (pointer, length)."""
+    if isinstance(ids_device, tuple):
+        ptr, n = ids_device
+    else:
+        ptr, n = ids_device.data_ptr(), ids_device.numel()
+    out = ctypes.c_void_p()
+    _check(load().pcd_prefill_device(model.handle, ptr, int(n), ctypes.byref(out)), "pcd_prefill_device")
+    return Cache(model, out.value)
+
+
+def pcd_prefill_extend(model: Model, head: Cache, ids) -> Cache:
+    ids = _i32(ids)
+    out = ctypes.c_void_p()
+    _check(load().pcd_prefill_extend(model.handle, head.handle, _ptr_i32(ids), len(ids), ctypes.byref(out)),
+           "pcd_prefill_extend")
+    return Cache(model, out.value)
+
+
+def pcd_cache_free(cache: Cache) -> None:
+    cache.free()
+
+
+# ------------------------------------------------------------------- score
+class _Fields:
+    """Keeps the int32 arrays of a list of fields alive for one call."""
+
+    def __init__(self, fields: Sequence):
+        self.keep = []
+        self.arr = (D.pcd_field * len(fields))()
+        self.n_cands = []
+        for i, f in enumerate(fields):
+            sc = _i32(f.scaffold)
+            labels = [_i32(l) for l in f.labels]
+            toks = _i32(np.concatenate(labels)) if labels else _i32([])
+            offs = _i32(np.concatenate([[0], np.cumsum([len(l) for l in labels])]))
+            self.keep += [sc, toks, offs]
+            self.arr[i] = D.pcd_field(_ptr_i32(sc), len(sc), _ptr_i32(toks), _ptr_i32(offs), len(labels),
+                                      float(getattr(f, "temperature", 1.0) or 0.0))
+            self.n_cands.append(len(labels))
+
+
+class _Results:
+    def __init__(self, n_cands: List[int]):
+        self.arr = (D.pcd_field_result * len(n_cands))()
+        self.buf = []
+        for i, n in enumerate(n_cands):
+            p = np.zeros(n, np.float32)
+            lp = np.zeros(n, np.float32)
+            self.buf.append((p, lp))
+            self.arr[i].probs = p.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+            self.arr[i].logprobs = lp.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+
+    def results(self) -> List[FieldResult]:
+        return [FieldResult(p, lp, int(r.label), float(r.mass), float(r.log_mass), float(r.margin),
+                            float(r.first_mass)) for r, (p, lp) in zip(self.arr, self.buf)]
+
+
+def _stats_dict(s: D.pcd_stats) -> dict:
+    return {k: getattr(s, k) for k, _ in D.pcd_stats._fields_}
+
+
+def pcd_score(model: Model, cache: Cache, fields: Sequence, with_stats: bool = False):
+    f = _Fields(fields)
+    r = _Results(f.n_cands)
+    st = D.pcd_stats()
+    _check(load().pcd_score(model.handle, cache.handle, f.arr, len(fields), r.arr, ctypes.byref(st)), "pcd_score")
+    return (r.results(), _stats_dict(st)) if with_stats else r.results()
+
+
+def pcd_score_batch(model: Model, caches: Sequence[Cache], fields: Sequence[Sequence], with_stats: bool = False):
+    n = len(caches)
+    fs = [_Fields(fl) for fl in fields]
+    rs = [_Results(x.n_cands) for x in fs]
+    c_arr = (ctypes.c_void_p * n)(*[c.handle for c in caches])
+    f_arr = (ctypes.POINTER(D.pcd_field) * n)(*[ctypes.cast(x.arr, ctypes.POINTER(D.pcd_field)) for x in fs])
+    r_arr = (ctypes.POINTER(D.pcd_field_result) * n)(
+        *[ctypes.cast(x.arr, ctypes.POINTER(D.pcd_field_result)) for x in rs])
+    nf = (ctypes.c_int * n)(*[len(fl) for fl in fields])
+    st = D.pcd_stats()
+    _check(load().pcd_score_batch(model.handle, c_arr, f_arr, nf, n, r_arr, ctypes.byref(st)), "pcd_score_batch")
+    out = [x.results() for x in rs]
+    return (out, _stats_dict(st)) if with_stats else out
+
+
+def pcd_plan_create(model: Model, fields: Sequence) -> Plan:
+    f = _Fields(fields)
+    out = ctypes.c_void_p()
+    _check(load().pcd_plan_create(model.handle, f.arr, len(fields), ctypes.byref(out)), "pcd_plan_create")
+    return Plan(model, out.value)
+
+
+def pcd_score_plan_device(model: Model, cache: Cache, plan: Plan, result_device) -> None:
+    """result_device: CUDA float32 tensor of plan.result_floats elements (or a pointer)."""
+    ptr = result_device if isinstance(result_device, int) else result_device.data_ptr()
+    _check(load().pcd_score_plan_device(model.handle, cache.handle, plan.handle, ptr), "pcd_score_plan_device")
+
+
+def unpack_plan_result(blob: np.ndarray, n_cands: Sequence[int]) -> List[FieldResult]:
+    """Splits a plan's result blob (layout in include/pcd.h) into per-field results."""
+    nf = len(n_cands)
+    nl = int(sum(n_cands))
+    probs, lps = blob[nf * 8:nf * 8 + nl], blob[nf * 8 + nl:nf * 8 + 2 * nl]
+    out, o = [], 0
+    for f, n in enumerate(n_cands):
+        h = blob[f * 8:(f + 1) * 8]
+        out.append(FieldResult(probs[o:o + n].copy(), lps[o:o + n].copy(), int(h[0]), float(h[1]), float(h[2]),
+                               float(h[3]), float(h[4])))
+        o += n
+    return out
+
+
+def pcd_sync(model: Model) -> None:
+    _check(load().pcd_sync(model.handle), "pcd_sync")
+
+
+def pcd_profile_enable(model: Model, on: bool = True) -> None:
+    _check(load().pcd_profile_enable(model.handle, 1 if on else 0), "pcd_profile_enable")
+
+
+PROFILE_CLASSES = ("gemm_prefill", "gemm_branch", "attn_prefill", "attn_branch", "readout", "other")
+
+
+def pcd_profile_read(model: Model) -> dict:
+    n = (ctypes.c_int * 6)()
+    ms = (ctypes.c_float * 6)()
+    _check(load().pcd_profile_read(model.handle, n, ms), "pcd_profile_read")
+    return {k: (int(n[i]), float(ms[i])) for i, k in enumerate(PROFILE_CLASSES)}

@@ -1,0 +1,48 @@
+"""Shared parity check of the CUDA path against the oracle.
+
+Tolerances of the PCD hot path (bf16 weights and activations, fp32
+accumulation, against the fp32 oracle):
+  * label: bit-exact wherever the oracle's top-2 log-prob margin > 0.05
+    (a closer call may flip under bf16, as batch-shape drift does);
+  * probabilities within 2e-3 absolute;
+  * label log-probs (summed), log mass within 3e-2 absolute;
+  * first-decision mass within 2e-3 absolute (a probability).
+"""
+import numpy as np
+
+PROB_TOL = 2e-3
+LOGP_TOL = 3e-2
+MARGIN_EXACT = 0.05
+
+
+def compare_field(gpu, ref, where=""):
+    """gpu: constrained_decoding_gb300.pcd.FieldResult; ref: oracle FieldResult."""
+    n = len(ref.scores)
+    assert len(gpu.probs) == n, where
+    errs = {
+        "probs": float(np.max(np.abs(gpu.probs - ref.probs))),
+        "logprobs": float(np.max(np.abs(gpu.logprobs - ref.scores))),
+        "log_mass": abs(gpu.log_mass - ref.log_mass),
+        "first_mass": abs(gpu.first_mass - ref.first_mass),
+    }
+    assert errs["probs"] <= PROB_TOL, (where, errs)
+    assert errs["logprobs"] <= LOGP_TOL, (where, errs)
+    assert errs["log_mass"] <= LOGP_TOL, (where, errs)
+    assert errs["first_mass"] <= PROB_TOL, (where, errs)
+    assert abs(gpu.mass - ref.mass) <= max(PROB_TOL, 3e-2 * ref.mass), (where, gpu.mass, ref.mass)
+    if ref.margin > MARGIN_EXACT:
+        assert gpu.label == ref.label, (where, gpu.label, ref.label, ref.margin)
+    else:
+        # a near tie: the GPU's label must be one of the near-best
+        assert ref.scores[gpu.label] >= ref.scores.max() - MARGIN_EXACT - LOGP_TOL, where
+    assert abs(float(np.sum(gpu.probs)) - 1.0) < 1e-4, where
+    return errs
+
+
+def compare_request(gpu_results, ref_results, where=""):
+    worst = {}
+    for i, (g, r) in enumerate(zip(gpu_results, ref_results)):
+        e = compare_field(g, r, f"{where} field {i}")
+        for k, v in e.items():
+            worst[k] = max(worst.get(k, 0.0), v)
+    return worst
