@@ -1,0 +1,415 @@
+#!/usr/bin/env python
+"""Benchmark of the parallel constrained decoding (PCD) hot path on GB300.
+
+One step = one request of the 28-field triage workload: a Qwen2.5-1.5B-shaped
+random decoder (bf16), a 512-token prefix (uniform ids), 28 fields (10
+booleans, 18 four-way enums of 1-4 token labels, 8 scaffold tokens each):
+prefill the prefix into a KV cache, then one batched branch pass scores every
+field.  Inputs are seeded and synthetic; the weights (3.1 GB) are larger than
+L2, so every step streams them from HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+`value` is requests/s with the prefix ids and the compiled schema resident in
+HBM; `e2e` is the same metric through the host-pointer C ABI (ids and fields
+from host memory, results back to host memory, copies inside the timed
+region).  With N > 1 (torchrun) every rank runs an independent replica on
+its own GPU (requests are independent: weak scaling, no collective on the
+data path).  `--impl reference` times the CPU oracle on the host cores on a
+bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "28-field requests/sec & p50 latency (ms); branch-pass HBM GB/s vs peak"
+WORKLOAD = "28-field triage request: Qwen2.5-1.5B-shaped decoder (bf16, random init), prefix 512, 28 fields"
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=2, help="workload number (2: 28-field triage)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- helpers
+def dist_info():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_init(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+        return dist
+    return None
+
+
+def barrier(dist):
+    if dist is not None:
+        dist.barrier()
+
+
+def max_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(dist, x: float) -> float:
+    if dist is None:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def read_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return {"hbm_gbs": j["hbm_gbs"], "bf16_tflops": j["bf16_tflops"],
+                "bf16_tflops_sustained": j.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            self.proc.wait()
+
+    def summary(self):
+        self.f.flush()
+        self.f.seek(0)
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        os.unlink(self.f.name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def work_model(cfg, Lp: int, T: int, R: int):
+    """Algorithmic work of one request (units counted once, no padding)."""
+    d, L, F, V = cfg.d_model, cfg.n_layers, cfg.d_ff, cfg.vocab
+    qd, kd = cfg.q_dim, cfg.kv_dim
+    w_qkv, w_o, w_mlp = d * (qd + 2 * kd), qd * d, 3 * F * d
+    layer_params = w_qkv + w_o + w_mlp
+    # prefill GEMMs: the last layer only needs its keys and values (QKV)
+    prefill_gemm_flops = 2.0 * Lp * (L * w_qkv + (L - 1) * (w_o + w_mlp))
+    prefill_attn_flops = 2.0 * 2 * (Lp * (Lp + 1) / 2) * qd * (L - 1)
+    branch_weight_bytes = 2.0 * L * layer_params
+    branch_gemm_flops = 2.0 * T * L * layer_params
+    branch_attn_bytes = 2.0 * Lp * L * 2 * kd           # prefix K and V, read once per request
+    readout_bytes = 2.0 * V * d
+    readout_flops = 2.0 * R * V * d
+    return dict(prefill_gemm_flops=prefill_gemm_flops, prefill_attn_flops=prefill_attn_flops,
+                branch_weight_bytes=branch_weight_bytes, branch_gemm_flops=branch_gemm_flops,
+                branch_attn_bytes=branch_attn_bytes, readout_bytes=readout_bytes, readout_flops=readout_flops)
+
+
+# --------------------------------------------------------- CPU oracle timing
+def time_oracle(weights, req, n_field_steps: int, warm_prefill: bool = True):
+    """The oracle as it stands on the host cores.  Sample: one prefill of the
+    request's prefix plus `n_field_steps` fields (cycling through the schema);
+    a request's time = prefill + sum over its fields of the measured mean time
+    of a field of the same kind."""
+    from oracle import Oracle
+    orc = Oracle(weights, np.float32)
+    t0 = time.perf_counter()
+    cache = orc.prefill(req.prefix)
+    t_prefill = time.perf_counter() - t0
+    per_kind = {}
+    order = list(range(len(req.fields)))
+    for i in range(n_field_steps):
+        f = req.fields[order[i % len(order)]]
+        t0 = time.perf_counter()
+        orc.score_field(f, cache=cache)
+        per_kind.setdefault(f.kind, []).append(time.perf_counter() - t0)
+    mean_kind = {k: float(np.mean(v)) for k, v in per_kind.items()}
+    fallback = float(np.mean([x for v in per_kind.values() for x in v]))
+    t_req = t_prefill + sum(mean_kind.get(f.kind, fallback) for f in req.fields)
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    return t_req, t_prefill, per_kind, cores
+
+
+# ------------------------------------------------------------------- ours
+def run_ours(args):
+    import torch
+    import synth
+    import constrained_decoding_gb300.pcd as pcd
+
+    ws, rank, local = dist_info()
+    dist = dist_init(ws)
+    torch.cuda.set_device(local)
+    from synth.shapes import CONFIG_MODEL
+    cfg = synth.model_config(CONFIG_MODEL[args.config])
+    weights = synth.make_weights(cfg, seed=0)
+    req = synth.make_request(args.config)
+    stream = torch.cuda.current_stream()
+    model = pcd.pcd_load_weights_host(weights, stream=stream)
+    plan = pcd.pcd_plan_create(model, req.fields)
+    # distinct prefixes per step: same shape, different ids
+    rng = np.random.default_rng(7 + rank)
+    n_pref = 8
+    prefixes = [req.prefix] + [rng.integers(0, cfg.vocab, len(req.prefix)).astype(np.int32) for _ in range(n_pref - 1)]
+    ids_dev = [torch.tensor(p, dtype=torch.int32, device="cuda") for p in prefixes]
+    out = torch.zeros(plan.result_floats, dtype=torch.float32, device="cuda")
+
+    def step(i):
+        cache = pcd.pcd_prefill_device(model, ids_dev[i % n_pref])
+        pcd.pcd_score_plan_device(model, cache, plan, out)
+        cache.free()
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    pcd.pcd_sync(model)
+
+    # ---- timed region: device-resident inputs
+    K = args.steps
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(K + 1)]
+    barrier(dist)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        evs[0].record(stream)
+        for i in range(K):
+            step(i)
+            evs[i + 1].record(stream)
+        torch.cuda.synchronize()
+    pcd.pcd_sync(model)
+    barrier(dist)
+    step_ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(K)]
+    total_s = evs[0].elapsed_time(evs[K]) / 1e3
+    total_s = max_over_ranks(dist, total_s)
+    clocks = clk.summary()
+
+    # ---- per-kernel-class times over the same workload (profiled pass)
+    pcd.pcd_profile_enable(model, True)
+    for i in range(K):
+        step(i)
+    prof = pcd.pcd_profile_read(model)
+    pcd.pcd_profile_enable(model, False)
+    launches_per_step = sum(n for n, _ in prof.values()) / K
+
+    # ---- end to end through the host-pointer C ABI
+    fields = req.fields
+    for i in range(2):
+        c = pcd.pcd_prefill(model, prefixes[i % n_pref])
+        pcd.pcd_score(model, c, fields)
+        c.free()
+    barrier(dist)
+    torch.cuda.synchronize()
+    e2e_ms = []
+    h2d = d2h = 0
+    t_e2e0 = time.perf_counter()
+    for i in range(K):
+        t0 = time.perf_counter()
+        c = pcd.pcd_prefill(model, prefixes[i % n_pref])
+        res, st = pcd.pcd_score(model, c, fields, with_stats=True)
+        c.free()
+        e2e_ms.append((time.perf_counter() - t0) * 1e3)
+        h2d = 4 * len(prefixes[i % n_pref]) + st["h2d_bytes"]
+        d2h = st["d2h_bytes"]
+    e2e_s = max_over_ranks(dist, time.perf_counter() - t_e2e0)
+    barrier(dist)
+
+    # ---- roofline of the dominant kernel class
+    T, R = st["branch_tokens"], st["readout_rows"]
+    wm = work_model(cfg, len(req.prefix), T, R)
+    peaks = read_peaks()
+    cls_ms = {k: v[1] / K for k, v in prof.items()}       # per request
+    dominant = max(("gemm_prefill", "gemm_branch", "attn_prefill", "attn_branch", "readout"), key=lambda k: cls_ms[k])
+
+    def roof(cls):
+        ms = cls_ms[cls]
+        n_launch = prof[cls][0] / K
+        if cls == "gemm_prefill":
+            work, bound = wm["prefill_gemm_flops"], "tensor"
+        elif cls == "gemm_branch":
+            # at the ridge: report the bound with the larger roofline time
+            t_hbm = wm["branch_weight_bytes"] / (peaks["hbm_gbs"] * 1e9)
+            t_tc = wm["branch_gemm_flops"] / (peaks["bf16_tflops"] * 1e12)
+            work, bound = (wm["branch_weight_bytes"], "hbm") if t_hbm >= t_tc else (wm["branch_gemm_flops"], "tensor")
+        elif cls == "attn_prefill":
+            work, bound = wm["prefill_attn_flops"], "tensor"
+        elif cls == "attn_branch":
+            work, bound = wm["branch_attn_bytes"], "hbm"
+        else:
+            work, bound = wm["readout_bytes"], "hbm"
+        if bound == "hbm":
+            achieved = work / (ms / 1e3) / 1e9
+            peak, unit = peaks["hbm_gbs"], "GB/s"
+        else:
+            achieved = work / (ms / 1e3) / 1e12
+            peak, unit = peaks["bf16_tflops"], "TFLOP/s"
+        return {"kernel": cls, "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
+                "frac": round(achieved / peak, 4), "traffic": None, "launches_per_step": n_launch,
+                "ms_per_step": round(ms, 4), "algorithmic_per_step": work,
+                "peak_source": peaks["source"] + (" (burst)" if unit == "TFLOP/s" else "")}
+
+    roofline = roof(dominant)
+    # branch pass HBM GB/s (the metric's second half): weights + prefix KV + E over the branch kernels
+    branch_ms = cls_ms["gemm_branch"] + cls_ms["attn_branch"] + cls_ms["readout"]
+    branch_bytes = wm["branch_weight_bytes"] + wm["branch_attn_bytes"] + wm["readout_bytes"]
+    branch_gbs = branch_bytes / (branch_ms / 1e3) / 1e9
+
+    n_total = sum_over_ranks(dist, K)
+    value = n_total / total_s
+    line = {
+        "metric": METRIC,
+        "value": round(value, 3),
+        "unit": "req/s",
+        "n_gpus": ws,
+        "steps": K,
+        "warmup": max(args.warmup, 3),
+        "ms_per_step": round(total_s * 1e3 / K, 4),
+        "p50_latency_ms": round(statistics.median(step_ms), 4),
+        "fields_per_s": round(value * len(req.fields), 1),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded random-init weights and token ids)",
+        "config": {"workload": WORKLOAD, "prefix_len": len(req.prefix), "fields": len(req.fields),
+                   "branch_tokens": T, "readout_rows": R, "requests_per_step": 1,
+                   "l2": "inputs larger than L2 (3.1 GB of weights streamed every step)",
+                   "parallelism": f"replicas x{ws}"},
+        "roofline": roofline,
+        "branch_pass": {"hbm_gbs": round(branch_gbs, 1), "frac_of_measured": round(branch_gbs / peaks["hbm_gbs"], 4),
+                        "frac_of_8tbs_spec": round(branch_gbs / 8000.0, 4), "ms_per_request": round(branch_ms, 4),
+                        "algorithmic_bytes": branch_bytes},
+        "kernel_ms_per_step": {k: round(v, 4) for k, v in cls_ms.items()},
+        "e2e": {"value": round(n_total / e2e_s, 3), "unit": "req/s", "p50_latency_ms": round(statistics.median(e2e_ms), 4),
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": int(round(launches_per_step * K)),
+        "clocks": clocks,
+    }
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        t_req, t_pf, per_kind, cores = time_oracle(weights, req, n_field_steps=2)
+        line["cpu_baseline"] = {"value": round(1.0 / t_req, 5), "unit": "req/s", "cores": cores, "kind": "oracle",
+                                "sample": f"oracle (numpy fp32) prefill of the 512-token prefix ({t_pf:.2f} s) + "
+                                          f"2 fields ({', '.join(f'{k}: {np.mean(v):.2f} s' for k, v in per_kind.items())}); "
+                                          "request time = prefill + 28 fields at the measured per-kind mean"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    for x in (plan, model):
+        x.free()
+
+
+# -------------------------------------------------------------- reference
+def run_reference(args):
+    ws, rank, _ = dist_info()
+    if rank != 0:
+        return
+    import synth
+    from synth.shapes import CONFIG_MODEL
+    cfg = synth.model_config(CONFIG_MODEL[args.config])
+    weights = synth.make_weights(cfg, seed=0)
+    req = synth.make_request(args.config)
+    from oracle import Oracle
+    orc = Oracle(weights, np.float32)
+    t0 = time.perf_counter()
+    cache = orc.prefill(req.prefix)
+    t_prefill = time.perf_counter() - t0
+    fields = req.fields
+    for i in range(args.warmup):
+        orc.score_field(fields[i % len(fields)], cache=cache)
+    per_kind, step_s = {}, []
+    t_all = time.perf_counter()
+    for i in range(args.steps):
+        f = fields[i % len(fields)]
+        t0 = time.perf_counter()
+        orc.score_field(f, cache=cache)
+        dt = time.perf_counter() - t0
+        step_s.append(dt)
+        per_kind.setdefault(f.kind, []).append(dt)
+    wall = time.perf_counter() - t_all
+    mean_kind = {k: float(np.mean(v)) for k, v in per_kind.items()}
+    fb = float(np.mean(step_s))
+    t_req = t_prefill + sum(mean_kind.get(f.kind, fb) for f in fields)
+    value = 1.0 / t_req
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    sample = (f"each step scores one field of the request with the oracle (numpy fp32) on the prefix cache; the "
+              f"prefix prefill ({t_prefill:.2f} s) is timed once; request time = prefill + 28 fields at the "
+              f"measured per-kind mean")
+    line = {
+        "metric": METRIC, "value": round(value, 5), "unit": "req/s", "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(wall * 1e3 / args.steps, 3),
+        "p50_latency_ms": round(t_req * 1e3, 1), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f32", "data": "synthetic (seeded random-init weights and token ids)",
+        "config": {"workload": WORKLOAD, "prefix_len": len(req.prefix), "fields": len(fields)},
+        "impl": "reference",
+        "cpu_baseline": {"value": round(value, 5), "unit": "req/s", "kind": "oracle", "cores": cores, "sample": sample},
+        "e2e": {"value": round(value, 5), "unit": "req/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -24,7 +24,8 @@ class pcd_field_result(ctypes.Structure):
 
 class pcd_stats(ctypes.Structure):
     _fields_ = [("prefill_ms", c_float), ("compile_ms", c_float), ("branch_ms", c_float), ("readout_ms", c_float),
-                ("total_ms", c_float), ("forward_passes", c_int), ("branch_tokens", c_int), ("readout_rows", c_int)]
+                ("total_ms", c_float), ("forward_passes", c_int), ("branch_tokens", c_int), ("readout_rows", c_int),
+                ("h2d_bytes", c_int64), ("d2h_bytes", c_int64)]
 
 
 # (name, restype, argtypes) of every entry point declared in include/*.h

@@ -19,7 +19,7 @@
 #include "pcd.h"
 #include "plan.h"
 
-using pcd::bf16;
+using pcd::act_t;
 
 // ============================================================ error reporting
 namespace {
@@ -74,7 +74,7 @@ int ensure(DevBuf& b, size_t bytes) {
 }
 
 struct Layer {
-  bf16 *wqkv, *wo, *wgu, *wd;
+  act_t *wqkv, *wo, *wgu, *wd;
   float *attn_norm, *mlp_norm;
 };
 
@@ -104,8 +104,8 @@ struct pcd_model {
   void* wblob = nullptr;
   float* fblob = nullptr;
   std::vector<Layer> layers;
-  bf16* embed = nullptr;
-  bf16* lm = nullptr;
+  act_t* embed = nullptr;
+  act_t* lm = nullptr;
   float* final_norm = nullptr;
   float2* rope = nullptr;
   int* d_err = nullptr;
@@ -133,8 +133,8 @@ struct pcd_cache {
   void* mem = nullptr;
   size_t bytes = 0;
   int len = 0, cap = 0;
-  bf16* k = nullptr;  // [L][Hkv][cap][dh]
-  bf16* v = nullptr;
+  act_t* k = nullptr;  // [L][Hkv][cap][dh]
+  act_t* v = nullptr;
 };
 
 struct pcd_plan {
@@ -205,7 +205,7 @@ int timed(pcd_model* m, int cls, Fn&& launch) {
 //   EPI_F32_ADD    residual += (split-K with atomics when the tiling splits K)
 //   EPI_F32_STORE  out = (zeroed + atomics when split)
 //   EPI_SWIGLU / EPI_BF16: one K split
-int gemm(pcd_model* m, int cls, const void* A, int M, int lda, const bf16* B, int N, int ldb, int K, int epi, void* out,
+int gemm(pcd_model* m, int cls, const void* A, int M, int lda, const act_t* B, int N, int ldb, int K, int epi, void* out,
          int ldo) {
   if (M <= 0) return PCD_OK;
   const bool splittable = (epi == pcd::EPI_F32_ADD || epi == pcd::EPI_F32_STORE);
@@ -249,11 +249,11 @@ int ensure_workspace(pcd_model* m, int T) {
 int run_prefill(pcd_model* m, const int32_t* d_ids, int n, pcd_cache* c, int p0) {
   PCD_TRY(ensure_workspace(m, n));
   float* x = static_cast<float*>(m->x32.p);
-  bf16* xn = static_cast<bf16*>(m->xn.p);
+  act_t* xn = static_cast<act_t*>(m->xn.p);
   float* qkv = static_cast<float*>(m->qkv.p);
-  bf16* q = static_cast<bf16*>(m->q.p);
-  bf16* att = static_cast<bf16*>(m->att.p);
-  bf16* hb = static_cast<bf16*>(m->hb.p);
+  act_t* q = static_cast<act_t*>(m->q.p);
+  act_t* att = static_cast<act_t*>(m->att.p);
+  act_t* hb = static_cast<act_t*>(m->hb.p);
   const size_t layer_kv = static_cast<size_t>(m->Hkv) * c->cap * m->dh;
   PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_embed(d_ids, n, m->embed, m->d, m->V, x, m->d_err, m->stream); }));
   for (int l = 0; l < m->L; ++l) {
@@ -339,13 +339,13 @@ int run_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_seg, 
   PCD_TRY(ensure(m->lse, static_cast<size_t>(std::max(R, 1)) * 4));
 
   float* x = static_cast<float*>(m->x32.p);
-  bf16* xn = static_cast<bf16*>(m->xn.p);
+  act_t* xn = static_cast<act_t*>(m->xn.p);
   float* qkv = static_cast<float*>(m->qkv.p);
-  bf16* q = static_cast<bf16*>(m->q.p);
-  bf16* att = static_cast<bf16*>(m->att.p);
-  bf16* hb = static_cast<bf16*>(m->hb.p);
-  bf16* kb = static_cast<bf16*>(m->kb.p);
-  bf16* vb = static_cast<bf16*>(m->vb.p);
+  act_t* q = static_cast<act_t*>(m->q.p);
+  act_t* att = static_cast<act_t*>(m->att.p);
+  act_t* hb = static_cast<act_t*>(m->hb.p);
+  act_t* kb = static_cast<act_t*>(m->kb.p);
+  act_t* vb = static_cast<act_t*>(m->vb.p);
   float* part_o = static_cast<float*>(m->part_o.p);
   float2* part_ml = static_cast<float2*>(m->part_ml.p);
   const float scale_log2 = 1.4426950408889634f / std::sqrt(static_cast<float>(m->dh));
@@ -435,7 +435,7 @@ int run_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_seg, 
   if (ev_mid) cudaEventRecord(ev_mid, m->stream);
 
   // final norm on the readout rows only, then the fused vocabulary readout
-  bf16* hr = static_cast<bf16*>(m->hr.p);
+  act_t* hr = static_cast<act_t*>(m->hr.p);
   PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
     return pcd::launch_rmsnorm(x, m->d, p.ro_tok, R, m->d, m->final_norm, m->cfg.rms_eps, hr, m->d, m->stream);
   }));
@@ -542,24 +542,31 @@ int read_device_error(pcd_model* m) {
 }
 
 // ----------------------------------------------------------- weight loading
-uint16_t f32_to_bf16_rne(float f) {
-  uint32_t u;
-  std::memcpy(&u, &f, 4);
-  if ((u & 0x7f800000u) == 0x7f800000u) return static_cast<uint16_t>((u >> 16) | ((u & 0xffffu) ? 0x40u : 0u));
-  u += 0x7fffu + ((u >> 16) & 1u);
-  return static_cast<uint16_t>(u >> 16);
+// Host conversions to the device operand format (fp16 bits, round to nearest even).
+uint16_t f32_to_f16_bits(float f) {
+  const __half h = __float2half_rn(f);
+  uint16_t u;
+  std::memcpy(&u, &h, 2);
+  return u;
+}
+float bf16_bits_to_f32(uint16_t b) {
+  const uint32_t u = static_cast<uint32_t>(b) << 16;
+  float f;
+  std::memcpy(&f, &u, 4);
+  return f;
 }
 
-// Writes rows x cols of a host matrix (f32 or bf16 bits) into dst (bf16 bits,
-// row stride dst_ld, row r of the source at dst row r * row_step + row_off).
+// Writes rows x cols of a host matrix (f32, or bf16 bit patterns) into dst as
+// fp16 bits (row stride dst_ld; source row r goes to dst row r * row_step + row_off).
 void put_matrix(uint16_t* dst, int dst_ld, int row_step, int row_off, const void* src, int rows, int cols, int dtype) {
   for (int r = 0; r < rows; ++r) {
     uint16_t* d = dst + static_cast<size_t>(r * row_step + row_off) * dst_ld;
     if (dtype == PCD_DTYPE_BF16) {
-      std::memcpy(d, static_cast<const uint16_t*>(src) + static_cast<size_t>(r) * cols, cols * 2);
+      const uint16_t* s = static_cast<const uint16_t*>(src) + static_cast<size_t>(r) * cols;
+      for (int c = 0; c < cols; ++c) d[c] = f32_to_f16_bits(bf16_bits_to_f32(s[c]));
     } else {
       const float* s = static_cast<const float*>(src) + static_cast<size_t>(r) * cols;
-      for (int c = 0; c < cols; ++c) d[c] = f32_to_bf16_rne(s[c]);
+      for (int c = 0; c < cols; ++c) d[c] = f32_to_f16_bits(s[c]);
     }
   }
 }
@@ -623,8 +630,8 @@ int build_model(const pcd_model_config& cfg, TensorFn get, void* ctx, int dtype,
   const size_t n_qkv = static_cast<size_t>(m->Nqkv) * d, n_o = static_cast<size_t>(d) * m->qdim;
   const size_t n_gu = static_cast<size_t>(2) * m->Fp * d, n_dn = static_cast<size_t>(d) * m->Fp;
   const size_t per_layer = n_qkv + n_o + n_gu + n_dn;
-  const size_t n_bf16 = n_embed + per_layer * L + (cfg.tied_embedding ? 0 : n_embed);
-  if (cudaMalloc(&m->wblob, n_bf16 * 2) != cudaSuccess) {
+  const size_t n_w16 = n_embed + per_layer * L + (cfg.tied_embedding ? 0 : n_embed);
+  if (cudaMalloc(&m->wblob, n_w16 * 2) != cudaSuccess) {
     cudaGetLastError();
     m->wblob = nullptr;
     return cleanup(fail(PCD_ERR_OOM, "weights do not fit on the device"));
@@ -634,7 +641,7 @@ int build_model(const pcd_model_config& cfg, TensorFn get, void* ctx, int dtype,
     m->fblob = nullptr;
     return cleanup(fail(PCD_ERR_OOM, "norm gains do not fit on the device"));
   }
-  bf16* w = static_cast<bf16*>(m->wblob);
+  act_t* w = static_cast<act_t*>(m->wblob);
   m->embed = w;
   w += n_embed;
   m->layers.resize(L);
@@ -660,7 +667,7 @@ int build_model(const pcd_model_config& cfg, TensorFn get, void* ctx, int dtype,
   auto fetch_f32 = [&](int idx, size_t elems) -> const float* {
     return static_cast<const float*>(get(ctx, idx, elems * 4));
   };
-  auto upload = [&](bf16* dst, size_t elems) { return cudaMemcpy(dst, stage.data(), elems * 2, cudaMemcpyHostToDevice); };
+  auto upload = [&](act_t* dst, size_t elems) { return cudaMemcpy(dst, stage.data(), elems * 2, cudaMemcpyHostToDevice); };
 
   // embedding
   const void* src = fetch(0, n_embed);
@@ -802,7 +809,7 @@ int new_cache(pcd_model* m, int cap, pcd_cache** out) {
   c->bytes = got;
   c->cap = cap;
   c->len = 0;
-  c->k = static_cast<bf16*>(mem);
+  c->k = static_cast<act_t*>(mem);
   c->v = c->k + static_cast<size_t>(m->L) * m->Hkv * cap * m->dh;
   *out = c;
   return PCD_OK;
@@ -818,13 +825,14 @@ int upload_ids(pcd_model* m, const int32_t* ids, int n, const int32_t** d_ids) {
 }
 
 // Uploads a host plan into the model's plan buffer; fills `v`.
-int upload_plan(pcd_model* m, const pcd::HostPlan& hp, PlanView& v) {
+int upload_plan(pcd_model* m, const pcd::HostPlan& hp, PlanView& v, size_t* bytes_out) {
   std::vector<int32_t> blob;
   // first pass for the size, second with the real device base
   plan_blob(m, hp, blob, v, nullptr);
   const size_t bytes = blob.size() * 4;
   PCD_TRY(ensure(m->plan_buf, bytes));
   plan_blob(m, hp, blob, v, static_cast<const int32_t*>(m->plan_buf.p));
+  *bytes_out = bytes;
   return upload_async(m, m->plan_buf.p, blob.data(), bytes);
 }
 
@@ -872,7 +880,8 @@ int score_impl(pcd_model* m, const pcd_cache* const* caches, const pcd_field* co
   }
   const auto t_comp = std::chrono::steady_clock::now();
   PlanView v;
-  PCD_TRY(upload_plan(m, hp, v));
+  size_t plan_bytes = 0;
+  PCD_TRY(upload_plan(m, hp, v, &plan_bytes));
   PCD_TRY(ensure(m->result, static_cast<size_t>(v.result_floats()) * 4));
   if (stats) cudaEventRecord(m->ev_a, m->stream);
   PCD_TRY(run_branch(m, v, segs.data(), n_req, static_cast<float*>(m->result.p), stats ? m->ev_b : nullptr));
@@ -895,6 +904,8 @@ int score_impl(pcd_model* m, const pcd_cache* const* caches, const pcd_field* co
     stats->forward_passes = 1;
     stats->branch_tokens = v.T;
     stats->readout_rows = v.R;
+    stats->h2d_bytes = static_cast<int64_t>(plan_bytes);
+    stats->d2h_bytes = static_cast<int64_t>(rbytes);
   }
   return PCD_OK;
 }
@@ -1030,8 +1041,8 @@ int pcd_prefill_extend(pcd_model* m, const pcd_cache* head, const int32_t* ids, 
   PCD_TRY(new_cache(m, total, &c));
   // copy the head's keys and values: per (layer, KV head) a block of head->len rows
   const size_t row = static_cast<size_t>(m->dh) * 2;
-  for (bf16* const* pair : {&c->k, &c->v}) {
-    const bf16* src = (pair == &c->k) ? head->k : head->v;
+  for (act_t* const* pair : {&c->k, &c->v}) {
+    const act_t* src = (pair == &c->k) ? head->k : head->v;
     const cudaError_t e = cudaMemcpy2DAsync(*pair, static_cast<size_t>(c->cap) * row, src,
                                             static_cast<size_t>(head->cap) * row, head->len * row,
                                             static_cast<size_t>(m->L) * m->Hkv, cudaMemcpyDeviceToDevice, m->stream);

@@ -1,7 +1,7 @@
-// Shared definitions of the PCD CUDA library: error words, bf16 helpers and
-// the host-side launch helpers every kernel file uses.
+// Shared definitions of the PCD CUDA library: error words, the operand
+// element type and its conversions.
 #pragma once
-#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
@@ -22,11 +22,19 @@ __device__ __forceinline__ void record_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
-__device__ __forceinline__ float bf2f(__nv_bfloat16 x) { return __bfloat162float(x); }
-__device__ __forceinline__ __nv_bfloat16 f2bf(float x) { return __float2bfloat16_rn(x); }
+// Element type of every tensor-core operand and stored activation: fp16.
+// The model's weights are bf16 numbers; they are carried as fp16 (every bf16
+// value of magnitude >= 2^-17 is exact in fp16, smaller ones land on the
+// fp16 subnormal grid, error <= 2^-25).  fp16 rounds activations 8x finer
+// than bf16, which the 28-layer decoders need to stay within the parity
+// tolerance of the fp32 reference.
+using act_t = __half;
 
-__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
-  __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+__device__ __forceinline__ float a2f(act_t x) { return __half2float(x); }
+__device__ __forceinline__ act_t f2a(float x) { return __float2half_rn(x); }
+
+__device__ __forceinline__ uint32_t pack2(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
 }
 

@@ -1,4 +1,4 @@
-// tcgen05 GEMM for sm_103a: D[M][N] = A[M][K] . B[N][K]^T, bf16 in, fp32
+// tcgen05 GEMM for sm_103a: D[M][N] = A[M][K] . B[N][K]^T, fp16 in, fp32
 // accumulation in tensor memory (TMEM).
 //
 // One persistent CTA per SM, 6 warps:
@@ -36,7 +36,7 @@ struct GemmParams {
 
 template <int MT, int BN>
 struct GemmCfg {
-  static constexpr int A_BYTES = 128 * 128;  // 128 rows x 64 bf16
+  static constexpr int A_BYTES = 128 * 128;  // 128 rows x 64 fp16
   static constexpr int B_BYTES = BN * 128;
   static constexpr int STAGE_BYTES = MT * A_BYTES + B_BYTES;
   static constexpr int SMEM_BUDGET = 227 * 1024 - 2048;
@@ -81,15 +81,15 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, const EpiArgs& e,
   } else {
     if (row >= p.M) return;
     if constexpr (EPI == EPI_BF16) {
-      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(e.out) + static_cast<size_t>(row) * e.ldo + col0;
+      act_t* o = reinterpret_cast<act_t*>(e.out) + static_cast<size_t>(row) * e.ldo + col0;
       uint4* o4 = reinterpret_cast<uint4*>(o);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
         uint4 w;
-        w.x = pack_bf16x2(v[8 * j + 0], v[8 * j + 1]);
-        w.y = pack_bf16x2(v[8 * j + 2], v[8 * j + 3]);
-        w.z = pack_bf16x2(v[8 * j + 4], v[8 * j + 5]);
-        w.w = pack_bf16x2(v[8 * j + 6], v[8 * j + 7]);
+        w.x = pack2(v[8 * j + 0], v[8 * j + 1]);
+        w.y = pack2(v[8 * j + 2], v[8 * j + 3]);
+        w.z = pack2(v[8 * j + 4], v[8 * j + 5]);
+        w.w = pack2(v[8 * j + 6], v[8 * j + 7]);
         o4[j] = w;
       }
     } else if constexpr (EPI == EPI_F32_ADD) {
@@ -113,7 +113,7 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, const EpiArgs& e,
       for (int j = 0; j < 8; ++j)
         atomicAdd(o4 + j, make_float4(v[4 * j + 0], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
     } else if constexpr (EPI == EPI_SWIGLU) {
-      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(e.out) + static_cast<size_t>(row) * e.ldo + col0 / 2;
+      act_t* o = reinterpret_cast<act_t*>(e.out) + static_cast<size_t>(row) * e.ldo + col0 / 2;
       uint4* o4 = reinterpret_cast<uint4*>(o);
 #pragma unroll
       for (int j = 0; j < 2; ++j) {
@@ -121,10 +121,10 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, const EpiArgs& e,
 #pragma unroll
         for (int i = 0; i < 8; ++i) h[i] = silu_f(v[16 * j + 2 * i]) * v[16 * j + 2 * i + 1];
         uint4 w;
-        w.x = pack_bf16x2(h[0], h[1]);
-        w.y = pack_bf16x2(h[2], h[3]);
-        w.z = pack_bf16x2(h[4], h[5]);
-        w.w = pack_bf16x2(h[6], h[7]);
+        w.x = pack2(h[0], h[1]);
+        w.y = pack2(h[2], h[3]);
+        w.z = pack2(h[4], h[5]);
+        w.w = pack2(h[6], h[7]);
         o4[j] = w;
       }
     }
@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t IDESC = idesc_bf16_f32(128, BN);
+      constexpr uint32_t IDESC = idesc_f16_f32(128, BN);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool any = false;
@@ -248,7 +248,7 @@ __global__ void __launch_bounds__(192, 1)
           for (int mt = 0; mt < mt_valid; ++mt) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-              umma_bf16(d_base + mt * BN, sdesc_kmajor_sw128(a_base + mt * C::A_BYTES + k * 32),
+              umma_f16(d_base + mt * BN, sdesc_kmajor_sw128(a_base + mt * C::A_BYTES + k * 32),
                         sdesc_kmajor_sw128(b_base + k * 32), IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
             }
           }
@@ -344,7 +344,7 @@ bool tma_init() {
   return g_encode != nullptr;
 }
 
-// bf16 matrix [rows][>= cols], row stride ld elements; box 64 (K) x box_rows.
+// 16-bit matrix [rows][>= cols], row stride ld elements; box 64 (K) x box_rows.
 static bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int ld, int box_rows) {
   if (!tma_init()) return false;
   if ((reinterpret_cast<uintptr_t>(ptr) & 15) || (ld * 2) % 16) return false;
@@ -352,7 +352,7 @@ static bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int ld
   cuuint64_t strides[1] = {static_cast<cuuint64_t>(ld) * 2};
   cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;

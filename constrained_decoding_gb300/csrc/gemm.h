@@ -1,5 +1,5 @@
 // Host interface of the tcgen05 GEMM: D = A . B^T with A [M][K] and B [N][K]
-// bf16, both K-contiguous, fp32 accumulation in tensor memory, and one of a
+// 16-bit, both K-contiguous, fp32 accumulation in tensor memory, and one of a
 // few fused epilogues.
 #pragma once
 #include <cuda_runtime.h>
@@ -8,10 +8,10 @@
 namespace pcd {
 
 enum EpiKind : int {
-  EPI_BF16 = 0,        // out bf16 [M][ldo] = D
+  EPI_BF16 = 0,        // out 16-bit [M][ldo] = D
   EPI_F32_ADD = 1,     // out f32 [M][ldo] += D (one K split: plain read-modify-write)
   EPI_F32_ATOMIC = 2,  // out f32 [M][ldo] += D with atomics (any number of K splits)
-  EPI_SWIGLU = 3,      // D columns (2f, 2f+1) = (gate_f, up_f); out bf16 [M][ldo]: silu(gate) * up
+  EPI_SWIGLU = 3,      // D columns (2f, 2f+1) = (gate_f, up_f); out 16-bit [M][ldo]: silu(gate) * up
   EPI_READOUT = 4,     // vocabulary readout: per (row, N tile) max and sum-exp, plus gathered logits
   EPI_F32_STORE = 5,   // out f32 [M][ldo] = D (one K split)
 };

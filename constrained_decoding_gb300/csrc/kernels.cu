@@ -10,7 +10,7 @@
 namespace pcd {
 
 // ======================================================================= embed
-__global__ void embed_kernel(const int32_t* __restrict__ ids, int n, const bf16* __restrict__ E, int d, int vocab,
+__global__ void embed_kernel(const int32_t* __restrict__ ids, int n, const act_t* __restrict__ E, int d, int vocab,
                              float* __restrict__ x, int* err) {
   const int t = blockIdx.x;
   if (t >= n) return;
@@ -23,15 +23,15 @@ __global__ void embed_kernel(const int32_t* __restrict__ ids, int n, const bf16*
   float4* dst = reinterpret_cast<float4*>(x + static_cast<size_t>(t) * d);
   for (int i = threadIdx.x; i < d / 8; i += blockDim.x) {
     uint4 w = src[i];
-    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&w);
-    float2 a = __bfloat1622float2(h[0]), b = __bfloat1622float2(h[1]), c = __bfloat1622float2(h[2]),
-           e = __bfloat1622float2(h[3]);
+    const __half2* h = reinterpret_cast<const __half2*>(&w);
+    float2 a = __half22float2(h[0]), b = __half22float2(h[1]), c = __half22float2(h[2]),
+           e = __half22float2(h[3]);
     dst[2 * i] = make_float4(a.x, a.y, b.x, b.y);
     dst[2 * i + 1] = make_float4(c.x, c.y, e.x, e.y);
   }
 }
 
-int launch_embed(const int32_t* ids, int n, const bf16* E, int d, int vocab, float* x, int* err, cudaStream_t s) {
+int launch_embed(const int32_t* ids, int n, const act_t* E, int d, int vocab, float* x, int* err, cudaStream_t s) {
   if (n <= 0) return 0;
   embed_kernel<<<n, 128, 0, s>>>(ids, n, E, d, vocab, x, err);
   return cudaGetLastError();
@@ -40,7 +40,7 @@ int launch_embed(const int32_t* ids, int n, const bf16* E, int d, int vocab, flo
 // ===================================================================== rmsnorm
 // One warp per row; fp32 statistics.
 __global__ void rmsnorm_kernel(const float* __restrict__ x, int ldx, const int32_t* __restrict__ rows, int n, int d,
-                               const float* __restrict__ gain, float eps, bf16* __restrict__ out, int ldo) {
+                               const float* __restrict__ gain, float eps, act_t* __restrict__ out, int ldo) {
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= n) return;
@@ -59,13 +59,13 @@ __global__ void rmsnorm_kernel(const float* __restrict__ x, int ldx, const int32
   for (int i = lane; i < d / 4; i += 32) {
     float4 v = xr[i], g = g4[i];
     uint2 w;
-    w.x = pack_bf16x2(v.x * inv * g.x, v.y * inv * g.y);
-    w.y = pack_bf16x2(v.z * inv * g.z, v.w * inv * g.w);
+    w.x = pack2(v.x * inv * g.x, v.y * inv * g.y);
+    w.y = pack2(v.z * inv * g.z, v.w * inv * g.w);
     o2[i] = w;
   }
 }
 
-int launch_rmsnorm(const float* x, int ldx, const int32_t* rows, int n, int d, const float* gain, float eps, bf16* out,
+int launch_rmsnorm(const float* x, int ldx, const int32_t* rows, int n, int d, const float* gain, float eps, act_t* out,
                    int ldo, cudaStream_t s) {
   if (n <= 0) return 0;
   const int wpb = 8;
@@ -96,18 +96,18 @@ __global__ void rope_kv_kernel(RopeArgs a) {
     const float2 cs = a.cs[static_cast<size_t>(pos) * half + i];
     const float y1 = x1 * cs.x - x2 * cs.y;
     const float y2 = x2 * cs.x + x1 * cs.y;
-    bf16* dst;
+    act_t* dst;
     if (h < a.Hq) {
       dst = a.q + (static_cast<size_t>(t) * a.Hq + h) * a.DH;
     } else {
       dst = a.k_dst + (static_cast<size_t>(h - a.Hq) * a.kv_head_stride + a.kv_row0 + t) * a.DH;
     }
-    dst[i] = f2bf(y1);
-    dst[i + half] = f2bf(y2);
+    dst[i] = f2a(y1);
+    dst[i + half] = f2a(y2);
   } else {
-    bf16* dst = a.v_dst + (static_cast<size_t>(h - a.Hq - a.Hkv) * a.kv_head_stride + a.kv_row0 + t) * a.DH;
-    dst[i] = f2bf(x1);
-    dst[i + half] = f2bf(x2);
+    act_t* dst = a.v_dst + (static_cast<size_t>(h - a.Hq - a.Hkv) * a.kv_head_stride + a.kv_row0 + t) * a.DH;
+    dst[i] = f2a(x1);
+    dst[i + half] = f2a(x2);
   }
 }
 
@@ -119,7 +119,7 @@ int launch_rope_kv(const RopeArgs& a, cudaStream_t s) {
 }
 
 // ==================================================================== attention
-// Flash attention (online softmax, fp32 statistics) with mma.sync bf16
+// Flash attention (online softmax, fp32 statistics) with mma.sync fp16
 // tensor-core tiles.  A CTA owns 64 query rows of one KV head; the rows are
 // (token, query head of the group) pairs, so every key tile loaded into
 // shared memory serves all query heads that share it.  Key j is visible to a
@@ -149,7 +149,7 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], const void* p) {
 }
 __device__ __forceinline__ void mma16816(float (&c)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
       "{%0, %1, %2, %3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
@@ -167,9 +167,9 @@ __global__ void __launch_bounds__(128) attn_kernel(AttnArgs a) {
   constexpr int KS = DH / 16;  // k-steps over the head dim
   constexpr int ND = DH / 8;   // 8-wide output column blocks
   extern __shared__ __align__(16) uint8_t attn_smem[];
-  bf16* sQ = reinterpret_cast<bf16*>(attn_smem);
-  bf16* sK = sQ + 64 * LDS;          // [2][64][LDS]
-  bf16* sV = sK + 2 * 64 * LDS;      // [2][64][LDS]
+  act_t* sQ = reinterpret_cast<act_t*>(attn_smem);
+  act_t* sK = sQ + 64 * LDS;          // [2][64][LDS]
+  act_t* sV = sK + 2 * 64 * LDS;      // [2][64][LDS]
   int* sPos = reinterpret_cast<int*>(sV + 2 * 64 * LDS);
 
   const int G = a.Hq / a.Hkv;
@@ -198,7 +198,7 @@ __global__ void __launch_bounds__(128) attn_kernel(AttnArgs a) {
     const int r = r0 + rr;
     const bool ok = r < rows;
     const int t = a.tok0 + (ok ? r / G : 0), g = ok ? r % G : 0;
-    const bf16* src = a.q + (static_cast<size_t>(t) * a.Hq + hk * G + g) * DH + ch * 8;
+    const act_t* src = a.q + (static_cast<size_t>(t) * a.Hq + hk * G + g) * DH + ch * 8;
     cp_async16(sQ + rr * LDS + ch * 8, src, ok);
   }
   cp_async_commit();
@@ -209,8 +209,8 @@ __global__ void __launch_bounds__(128) attn_kernel(AttnArgs a) {
   const int k_hi = min(min(a.n_keys, (split + 1) * a.split_len), pmax + 1);
   const int n_tiles = k_hi > k_lo ? (k_hi - k_lo + 63) / 64 : 0;
 
-  const bf16* kbase = a.k + static_cast<size_t>(hk) * a.kv_head_stride * DH;
-  const bf16* vbase = a.v + static_cast<size_t>(hk) * a.kv_head_stride * DH;
+  const act_t* kbase = a.k + static_cast<size_t>(hk) * a.kv_head_stride * DH;
+  const act_t* vbase = a.v + static_cast<size_t>(hk) * a.kv_head_stride * DH;
   auto load_kv = [&](int tile, int buf) {
     const int j0 = k_lo + tile * 64;
     for (int c = tid; c < 64 * QCH; c += 128) {
@@ -251,8 +251,8 @@ __global__ void __launch_bounds__(128) attn_kernel(AttnArgs a) {
       cp_async_wait<0>();
     }
     __syncthreads();
-    const bf16* K = sK + buf * 64 * LDS;
-    const bf16* V = sV + buf * 64 * LDS;
+    const act_t* K = sK + buf * 64 * LDS;
+    const act_t* V = sV + buf * 64 * LDS;
     const int j0 = k_lo + tile * 64;
 
     float s[8][4];
@@ -321,10 +321,10 @@ __global__ void __launch_bounds__(128) attn_kernel(AttnArgs a) {
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) {
       uint32_t pa[4];
-      pa[0] = pack_bf16x2(s[2 * kk][0], s[2 * kk][1]);
-      pa[1] = pack_bf16x2(s[2 * kk][2], s[2 * kk][3]);
-      pa[2] = pack_bf16x2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-      pa[3] = pack_bf16x2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+      pa[0] = pack2(s[2 * kk][0], s[2 * kk][1]);
+      pa[1] = pack2(s[2 * kk][2], s[2 * kk][3]);
+      pa[2] = pack2(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+      pa[3] = pack2(s[2 * kk + 1][2], s[2 * kk + 1][3]);
 #pragma unroll
       for (int nd2 = 0; nd2 < DH / 16; ++nd2) {
         uint32_t b[4];
@@ -352,11 +352,11 @@ __global__ void __launch_bounds__(128) attn_kernel(AttnArgs a) {
     const float il = half ? il_hi : il_lo;
     const int t = a.tok0 + r / G, g = r % G;
     if (!a.partial) {
-      bf16* dst = a.out + static_cast<size_t>(t) * a.ld_out + (hk * G + g) * DH;
+      act_t* dst = a.out + static_cast<size_t>(t) * a.ld_out + (hk * G + g) * DH;
 #pragma unroll
       for (int nd = 0; nd < ND; ++nd) {
         const int d = nd * 8 + tq * 2;
-        *reinterpret_cast<uint32_t*>(dst + d) = pack_bf16x2(o[nd][2 * half] * il, o[nd][2 * half + 1] * il);
+        *reinterpret_cast<uint32_t*>(dst + d) = pack2(o[nd][2 * half] * il, o[nd][2 * half + 1] * il);
       }
     } else {
       const size_t prow = (static_cast<size_t>(split) * a.Hkv + hk) * a.part_rows + static_cast<size_t>(t) * G + g;
@@ -413,11 +413,11 @@ __global__ void branch_merge_kernel(MergeArgs a) {
   const int rows = a.n_tok * G;
   const int r = t * G + g;
   float q[EPT], acc[EPT];
-  const bf16* qp = a.q + (static_cast<size_t>(t) * a.Hq + h) * DH;
+  const act_t* qp = a.q + (static_cast<size_t>(t) * a.Hq + h) * DH;
 #pragma unroll
   for (int i = 0; i < EPT; ++i) {
     const int d = lane + 32 * i;
-    q[i] = d < DH ? bf2f(qp[d]) : 0.f;
+    q[i] = d < DH ? a2f(qp[d]) : 0.f;
     acc[i] = 0.f;
   }
   float m = -INFINITY, l = 0.f;
@@ -439,13 +439,13 @@ __global__ void branch_merge_kernel(MergeArgs a) {
   }
   for (int ai = a.anc_off[t]; ai < a.anc_off[t + 1]; ++ai) {
     const int j = a.anc_idx[ai];
-    const bf16* kp = a.kb + (static_cast<size_t>(hk) * a.n_tok + j) * DH;
-    const bf16* vp = a.vb + (static_cast<size_t>(hk) * a.n_tok + j) * DH;
+    const act_t* kp = a.kb + (static_cast<size_t>(hk) * a.n_tok + j) * DH;
+    const act_t* vp = a.vb + (static_cast<size_t>(hk) * a.n_tok + j) * DH;
     float dot = 0.f;
 #pragma unroll
     for (int i = 0; i < EPT; ++i) {
       const int d = lane + 32 * i;
-      if (d < DH) dot += q[i] * bf2f(kp[d]);
+      if (d < DH) dot += q[i] * a2f(kp[d]);
     }
 #pragma unroll
     for (int o = 16; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
@@ -455,17 +455,17 @@ __global__ void branch_merge_kernel(MergeArgs a) {
 #pragma unroll
     for (int i = 0; i < EPT; ++i) {
       const int d = lane + 32 * i;
-      acc[i] = acc[i] * co + (d < DH ? p * bf2f(vp[d]) : 0.f);
+      acc[i] = acc[i] * co + (d < DH ? p * a2f(vp[d]) : 0.f);
     }
     l = l * co + p;
     m = mn;
   }
   const float il = l > 0.f ? 1.f / l : 0.f;
-  bf16* dst = a.out + static_cast<size_t>(t) * a.ld_out + h * DH;
+  act_t* dst = a.out + static_cast<size_t>(t) * a.ld_out + h * DH;
 #pragma unroll
   for (int i = 0; i < EPT; ++i) {
     const int d = lane + 32 * i;
-    if (d < DH) dst[d] = f2bf(acc[i] * il);
+    if (d < DH) dst[d] = f2a(acc[i] * il);
   }
 }
 

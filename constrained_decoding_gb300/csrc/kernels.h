@@ -1,18 +1,18 @@
 // Host launchers of the non-GEMM device steps of the PCD hot path.
 #pragma once
-#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
 namespace pcd {
 
-using bf16 = __nv_bfloat16;
+using act_t = __half;  // same as common.cuh
 
 // x[t][0..d) = E[ids[t]][0..d) as fp32 (the residual stream starts here).
-int launch_embed(const int32_t* ids, int n, const bf16* E, int d, int vocab, float* x, int* err, cudaStream_t s);
+int launch_embed(const int32_t* ids, int n, const act_t* E, int d, int vocab, float* x, int* err, cudaStream_t s);
 
-// out[r] = bf16( x[src] / sqrt(mean(x[src]^2) + eps) * gain ), src = rows ? rows[r] : r.
-int launch_rmsnorm(const float* x, int ldx, const int32_t* rows, int n, int d, const float* gain, float eps, bf16* out,
+// out[r] = act_t( x[src] / sqrt(mean(x[src]^2) + eps) * gain ), src = rows ? rows[r] : r.
+int launch_rmsnorm(const float* x, int ldx, const int32_t* rows, int n, int d, const float* gain, float eps, act_t* out,
                    int ldo, cudaStream_t s);
 
 struct RopeArgs {
@@ -22,9 +22,9 @@ struct RopeArgs {
   int max_pos;
   const int32_t* rel;     // position of token t = base + (rel ? rel[t] : t)
   int base;
-  bf16* q;                // [n][Hq][DH]
-  bf16* k_dst;            // K row of token t: k_dst + (h * kv_head_stride + kv_row0 + t) * DH
-  bf16* v_dst;
+  act_t* q;                // [n][Hq][DH]
+  act_t* k_dst;            // K row of token t: k_dst + (h * kv_head_stride + kv_row0 + t) * DH
+  act_t* v_dst;
   int64_t kv_head_stride; // elements between KV heads
   int kv_row0;
   int* err;
@@ -32,19 +32,19 @@ struct RopeArgs {
 int launch_rope_kv(const RopeArgs& a, cudaStream_t s);
 
 struct AttnArgs {
-  const bf16* q;            // [tok0 + n_tok][Hq][DH]: this launch's query tokens are tok0 .. tok0+n_tok-1
+  const act_t* q;            // [tok0 + n_tok][Hq][DH]: this launch's query tokens are tok0 .. tok0+n_tok-1
   int n_tok, Hq, Hkv, DH;
   int tok0;                 // first token (also offsets rel, out and the partial rows)
   int part_rows;            // rows of the partial arrays per (split, KV head): all tokens x G
-  const bf16* k;            // this layer's keys: k + (h * kv_head_stride + j) * DH, j < n_keys
-  const bf16* v;
+  const act_t* k;            // this layer's keys: k + (h * kv_head_stride + j) * DH, j < n_keys
+  const act_t* v;
   int64_t kv_head_stride;
   int n_keys;
   const int32_t* rel;       // query position = base + (rel ? rel[t] : t); key j is visible iff j <= position
   int base;
   int n_splits, split_len;  // keys are cut into n_splits ranges of split_len (a multiple of 64)
   float scale_log2;         // log2(e) / sqrt(DH)
-  bf16* out;                // n_splits == 1 and !partial: out[t][h * DH + d] (normalised)
+  act_t* out;                // n_splits == 1 and !partial: out[t][h * DH + d] (normalised)
   int ld_out;
   float* part_o;            // partial: [split][Hkv][part_rows][DH] normalised by the split's own l
   float2* part_ml;          // partial: [split][Hkv][part_rows] (max, sum) in log2 units
@@ -54,17 +54,17 @@ struct AttnArgs {
 int launch_attention(const AttnArgs& a, cudaStream_t s);
 
 struct MergeArgs {
-  const bf16* q;            // [n_tok][Hq][DH]
+  const act_t* q;            // [n_tok][Hq][DH]
   int n_tok, Hq, Hkv, DH;
   const float* part_o;      // prefix partials from launch_attention (partial = 1)
   const float2* part_ml;
   int n_splits;
-  const bf16* kb;           // branch keys/values [Hkv][n_tok][DH]
-  const bf16* vb;
+  const act_t* kb;           // branch keys/values [Hkv][n_tok][DH]
+  const act_t* vb;
   const int32_t* anc_off;   // [n_tok + 1]: ancestors (incl. itself) of token t in the branch batch
   const int32_t* anc_idx;
   float scale_log2;
-  bf16* out;                // out[t][h * DH + d]
+  act_t* out;                // out[t][h * DH + d]
   int ld_out;
 };
 int launch_branch_merge(const MergeArgs& a, cudaStream_t s);

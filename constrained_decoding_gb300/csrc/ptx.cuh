@@ -5,7 +5,7 @@
 // arrives returns an error instead of hanging the GPU.
 #pragma once
 #include <cuda.h>
-#include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cstdint>
 
 namespace pcd {
@@ -114,7 +114,7 @@ __device__ __forceinline__ void tc_fence_after_sync() {
 }
 
 // Shared-memory matrix descriptor for a K-major operand tile written by TMA
-// with 128-byte swizzling: 128-byte rows (64 bf16 of K), 8-row groups 1024 B
+// with 128-byte swizzling: 128-byte rows (64 16-bit elements of K), 8-row groups 1024 B
 // apart.  Advancing along K inside the 128-byte row is done by adding the
 // byte offset to the start address.
 __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
@@ -127,17 +127,17 @@ __device__ __forceinline__ uint64_t sdesc_kmajor_sw128(uint32_t saddr) {
   return d;
 }
 
-// Instruction descriptor, kind::f16: bf16 x bf16 -> fp32, A and B K-major.
-__host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
+// Instruction descriptor, kind::f16: f16 x f16 -> fp32, A and B K-major.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
   return (1u << 4)                                   // D format f32
-         | (1u << 7)                                 // A format bf16
-         | (1u << 10)                                // B format bf16
+         | (0u << 7)                                 // A format f16
+         | (0u << 10)                                // B format f16
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                           uint32_t accumulate) {
   asm volatile(
       "{\n\t.reg .pred p;\n\t"

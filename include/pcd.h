@@ -56,8 +56,11 @@ extern "C" {
 #define PCD_ERR_BAD_WEIGHTS -12        /* weight file missing, truncated or inconsistent                 */
 #define PCD_ERR_TOO_LONG -13           /* a position beyond the model's max_positions                    */
 
-/* dtypes of pcd_load_weights_host matrices */
-#define PCD_DTYPE_F32 1 /* converted to bf16 (round to nearest even) on load */
+/* dtypes of pcd_load_weights_host matrices.  On the device every matrix is
+ * carried as fp16 (round to nearest even): bf16 values of magnitude >= 2^-17
+ * convert exactly, smaller ones within 2^-25.  Activations and the KV cache
+ * are fp16 too; accumulation and the residual stream are fp32. */
+#define PCD_DTYPE_F32 1
 #define PCD_DTYPE_BF16 2
 
 typedef struct pcd_model pcd_model; /* opaque, library-owned */
@@ -114,6 +117,7 @@ typedef struct {
   float prefill_ms, compile_ms, branch_ms, readout_ms, total_ms;
   int forward_passes;
   int branch_tokens, readout_rows;
+  int64_t h2d_bytes, d2h_bytes; /* host<->device bytes this call copied */
 } pcd_stats;
 
 /* ------------------------------------------------------------------ models */

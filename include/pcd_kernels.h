@@ -15,13 +15,13 @@ extern "C" {
 #endif
 
 /* Epilogue kinds of pcd_k_gemm. */
-#define PCD_EPI_BF16 0       /* out bf16 [M][ldo] = A.B^T                                   */
+#define PCD_EPI_BF16 0       /* out fp16 [M][ldo] = A.B^T (16-bit store)                    */
 #define PCD_EPI_F32_ADD 1    /* out f32 [M][ldo] += A.B^T (splits must be 1)                */
 #define PCD_EPI_F32_ATOMIC 2 /* out f32 [M][ldo] += A.B^T with atomics (any splits)         */
-#define PCD_EPI_SWIGLU 3     /* out bf16 [M][ldo]: col f = silu(D[:,2f]) * D[:,2f+1]        */
+#define PCD_EPI_SWIGLU 3     /* out fp16 [M][ldo]: col f = silu(D[:,2f]) * D[:,2f+1]        */
 
 /* Dense projection on the tensor cores: D[M][N] = A[M][K] . B[N][K]^T with
- * bf16 A and B (row-major, K contiguous, leading dimensions lda/ldb in
+ * fp16 A and B (row-major, K contiguous, leading dimensions lda/ldb in
  * elements, multiples of 8), fp32 accumulation and a fused epilogue.  This is
  * the contraction of every QKV, output and SwiGLU projection of the decoder
  * (configs: nn.Linear weights [out][in] as B, activations [tokens][in] as A).

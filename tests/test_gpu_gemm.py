@@ -20,14 +20,14 @@ def _ref(a, b):
 def _run(M, N, K, epi, mt, bn, splits, seed=0):
     lib = _lib()
     g = torch.Generator().manual_seed(seed)
-    a = (torch.randn(M, K, generator=g) * 0.5).to(torch.bfloat16).cuda()
-    b = (torch.randn(N, K, generator=g) * 0.05).to(torch.bfloat16).cuda()
+    a = (torch.randn(M, K, generator=g) * 0.5).to(torch.float16).cuda()
+    b = (torch.randn(N, K, generator=g) * 0.05).to(torch.float16).cuda()
     err = torch.zeros(1, dtype=torch.int32, device="cuda")
     s = torch.cuda.current_stream().cuda_stream
     if epi == 0:
-        out = torch.zeros(M, N, dtype=torch.bfloat16, device="cuda")
+        out = torch.zeros(M, N, dtype=torch.float16, device="cuda")
     elif epi == 3:
-        out = torch.zeros(M, N // 2, dtype=torch.bfloat16, device="cuda")
+        out = torch.zeros(M, N // 2, dtype=torch.float16, device="cuda")
     else:
         out = torch.full((M, N), 0.25, dtype=torch.float32, device="cuda")
     rc = lib.pcd_k_gemm(a.data_ptr(), M, K, b.data_ptr(), N, K, K, epi, out.data_ptr(), out.shape[1],
