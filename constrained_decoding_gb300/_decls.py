@@ -51,6 +51,7 @@ SIGNATURES = [
     ("pcd_profile_read", c_int, [c_void_p, P(c_int), P(c_float)]),
     ("pcd_strerror", c_char_p, [c_int]),
     ("pcd_last_error", c_char_p, []),
+    ("pcd_plan_inspect", c_int, [c_void_p, c_int, c_int, P(c_int32), P(P(c_int32))]),
     ("pcd_k_gemm", c_int, [c_void_p, c_int, c_int, c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_int,
                            c_int, c_int, c_int, c_void_p, c_void_p]),
 ]

@@ -1,8 +1,12 @@
 // extern "C" kernel-level entry points (include/pcd_kernels.h).
 #include <cuda_runtime.h>
 
+#include <cstring>
+#include <string>
+
 #include "gemm.h"
 #include "pcd_kernels.h"
+#include "plan.h"
 
 namespace {
 int device_sms() {
@@ -32,4 +36,26 @@ extern "C" int pcd_k_gemm(const void* a, int M, int lda, const void* b, int N, i
   e.ldo = ldo;
   const int r = pcd::launch_gemm(s, epi, e, t, static_cast<cudaStream_t>(stream), dev_err, 2000000000ull, sms);
   return r == 0 ? 0 : (r < 0 ? -1 : -10);
+}
+
+extern "C" int pcd_plan_inspect(const void* fields, int n_fields, int vocab, int32_t* sizes, int32_t* const* arrays) {
+  if (!sizes || vocab < 1) return PCD_ERR_INVALID_ARG;
+  pcd::HostPlan p;
+  std::string msg;
+  const int rc = pcd::compile_fields(static_cast<const pcd_field*>(fields), n_fields, vocab, &p, &msg);
+  if (rc != PCD_OK) return rc;
+  sizes[0] = p.T;
+  sizes[1] = p.R;
+  sizes[2] = p.n_children;
+  sizes[3] = p.n_labels;
+  sizes[4] = p.n_path;
+  sizes[5] = static_cast<int32_t>(p.anc_idx.size());
+  sizes[6] = p.n_fields;
+  if (arrays) {
+    const std::vector<int32_t>* src[12] = {&p.tok,     &p.rel,       &p.anc_off, &p.anc_idx, &p.ro_tok,  &p.row_ch,
+                                          &p.ch_tok,  &p.child_row, &p.lab_off, &p.path,    &p.fld_lab, &p.fld_root};
+    for (int i = 0; i < 12; ++i)
+      if (arrays[i] && !src[i]->empty()) std::memcpy(arrays[i], src[i]->data(), src[i]->size() * sizeof(int32_t));
+  }
+  return PCD_OK;
 }

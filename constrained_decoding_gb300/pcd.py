@@ -303,3 +303,25 @@ def pcd_profile_read(model: Model) -> dict:
     ms = (ctypes.c_float * 6)()
     _check(load().pcd_profile_read(model.handle, n, ms), "pcd_profile_read")
     return {k: (int(n[i]), float(ms[i])) for i, k in enumerate(PROFILE_CLASSES)}
+
+
+PLAN_ARRAYS = ("tok", "rel", "anc_off", "anc_idx", "ro_tok", "row_ch", "ch_tok", "child_row", "lab_off", "path",
+               "fld_lab", "fld_root")
+
+
+def pcd_plan_inspect(fields: Sequence, vocab: int) -> dict:
+    """Host-only compile of `fields` (no GPU): the packed branch batch as numpy arrays."""
+    lib = load()
+    f = _Fields(fields)
+    sizes = np.zeros(7, np.int32)
+    _check(lib.pcd_plan_inspect(ctypes.cast(f.arr, ctypes.c_void_p), len(fields), vocab, _ptr_i32(sizes), None),
+           "pcd_plan_inspect")
+    T, R, C, NL, NP, NA, NF = (int(x) for x in sizes)
+    lens = [T, T, T + 1, NA, R, R + 1, C, C, NL + 1, NP, NF + 1, NF]
+    bufs = [np.zeros(max(n, 1), np.int32) for n in lens]
+    ptrs = (ctypes.POINTER(ctypes.c_int32) * 12)(*[_ptr_i32(b) for b in bufs])
+    _check(lib.pcd_plan_inspect(ctypes.cast(f.arr, ctypes.c_void_p), len(fields), vocab, _ptr_i32(sizes), ptrs),
+           "pcd_plan_inspect")
+    out = {k: b[:n] for k, b, n in zip(PLAN_ARRAYS, bufs, lens)}
+    out.update(T=T, R=R, C=C, NL=NL, NP=NP, NA=NA, NF=NF)
+    return out

@@ -1,0 +1,170 @@
+"""Host-side checks that need no GPU: the C ABI library loads and exports every
+symbol include/*.h declares, the branch compiler's packed batch is a correct
+trie of every field's labels, validation codes, and the replica path of the
+benchmark on two gloo ranks."""
+import os
+import re
+import subprocess
+import sys
+
+import numpy as np
+import pytest
+
+import synth
+from synth.requests import make_custom
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from constrained_decoding_gb300.build import build
+    build()
+    import constrained_decoding_gb300 as pkg
+    return pkg.load()
+
+
+def declared_symbols():
+    names = set()
+    for h in ("pcd.h", "pcd_kernels.h"):
+        text = open(os.path.join(ROOT, "include", h)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(pcd_\w+)\s*\(", text))
+    return names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_symbols()
+    assert {"pcd_load_weights", "pcd_prefill", "pcd_score", "pcd_prefill_extend", "pcd_score_batch"} <= names
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+    from constrained_decoding_gb300._decls import SIGNATURES
+    assert {s[0] for s in SIGNATURES} == names
+
+
+def _check_plan(plan, fields):
+    T, R = plan["T"], plan["R"]
+    # sizes
+    internal = []
+    for f in fields:
+        prefixes = {tuple(l[:j]) for l in f.labels for j in range(1, len(l))}
+        internal.append(len(prefixes))
+    assert T == sum(len(f.scaffold) + n for f, n in zip(fields, internal))
+    assert R == sum(1 + n for n in internal)
+    assert plan["NL"] == sum(len(f.labels) for f in fields)
+    tok, rel, ao, ai = plan["tok"], plan["rel"], plan["anc_off"], plan["anc_idx"]
+    # ancestors: positions 0..rel of the token's own row, ending with itself
+    for t in range(T):
+        anc = ai[ao[t]:ao[t + 1]]
+        assert anc[-1] == t
+        np.testing.assert_array_equal(rel[anc], np.arange(rel[t] + 1))
+    # every label's path spells its tokens; step j is read at the node of its first j tokens
+    lab = 0
+    for fi, f in enumerate(fields):
+        S = len(f.scaffold)
+        root = plan["fld_root"][fi]
+        rt = plan["ro_tok"][root]
+        assert tok[rt] == f.scaffold[-1] and rel[rt] == S - 1
+        for l in f.labels:
+            steps = plan["path"][plan["lab_off"][lab]:plan["lab_off"][lab + 1]]
+            np.testing.assert_array_equal(plan["ch_tok"][steps], l)
+            for j, e in enumerate(steps):
+                row = plan["child_row"][e]
+                b = plan["ro_tok"][row]
+                if j == 0:
+                    assert row == root
+                else:
+                    assert tok[b] == l[j - 1] and rel[b] == S + j - 1
+                    # the node's ancestors spell the scaffold then the label prefix
+                    anc = ai[ao[b]:ao[b + 1]]
+                    np.testing.assert_array_equal(tok[anc], np.concatenate([f.scaffold, l[:j]]))
+            lab += 1
+    # the children of a readout row are distinct tokens
+    rc = plan["row_ch"]
+    for r in range(R):
+        ch = plan["ch_tok"][rc[r]:rc[r + 1]]
+        assert len(np.unique(ch)) == len(ch) >= 1
+
+
+@pytest.mark.parametrize("which", [1, 2, 3, 4])
+def test_branch_compiler_workloads(lib, which):
+    import constrained_decoding_gb300.pcd as pcd
+    req = synth.make_request(which)
+    V = synth.model_config(synth.CONFIG_MODEL[which]).vocab
+    plan = pcd.pcd_plan_inspect(req.fields, V)
+    _check_plan(plan, req.fields)
+    if which == 3:
+        # one shared first token: the root has one child, 255 leaves below 2nd-level nodes
+        assert plan["row_ch"][1] - plan["row_ch"][0] == 1
+
+
+def test_branch_compiler_random_shapes(lib):
+    import constrained_decoding_gb300.pcd as pcd
+    for seed in range(20):
+        rng = np.random.default_rng(seed)
+        specs = []
+        for _ in range(int(rng.integers(1, 6))):
+            specs.append(("scaffold", int(rng.integers(1, 12))))
+            k = rng.integers(0, 3)
+            specs.append([("bool",), ("enum", int(rng.integers(2, 9)), 1, 5), ("shared", int(rng.integers(2, 9)), 2, 6)][k])
+        req = make_custom(seed, 512, 10, specs)
+        _check_plan(pcd.pcd_plan_inspect(req.fields, 512), req.fields)
+
+
+def test_branch_compiler_validation(lib):
+    import constrained_decoding_gb300.pcd as pcd
+    F = synth.Field
+    cases = {
+        -3: [F(np.array([1]), [np.array([5])])],
+        -4: [F(np.array([1]), [np.array([5]), np.array([], np.int32)])],
+        -5: [F(np.array([1]), [np.array([5, 6]), np.array([5, 6])])],
+        -6: [F(np.array([1]), [np.array([5]), np.array([5, 6])])],
+        -7: [F(np.array([1]), [np.array([5]), np.array([512])])],
+        -1: [F(np.array([], np.int32), [np.array([5]), np.array([6])])],
+        -2: [F(np.array([1]), [np.array([i]) for i in range(256)])],
+    }
+    for code, fields in cases.items():
+        with pytest.raises(pcd.PCDError) as ei:
+            pcd.pcd_plan_inspect(fields, 512)
+        assert ei.value.code == code
+    bad_T = F(np.array([1]), [np.array([5]), np.array([6])], temperature=-1.0)
+    with pytest.raises(pcd.PCDError):
+        pcd.pcd_plan_inspect([bad_T], 512)
+
+
+def _replica_worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
+                      LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import bench
+    ws, r, _ = bench.dist_info()
+    dist = bench.dist_init(ws)
+    bench.barrier(dist)
+    mx = bench.max_over_ranks(dist, 1.0 + r)
+    sm = bench.sum_over_ranks(dist, 10.0)
+    out.put((r, mx, sm))
+    dist.destroy_process_group()
+
+
+def test_replica_timing_helpers_two_gloo_ranks():
+    """The N>1 benchmark path: every rank times its own replica; rank 0 reports
+    the max time over ranks and the sum of the units all ranks processed."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = 29500 + os.getpid() % 1000
+    ps = [ctx.Process(target=_replica_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in ps:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in ps)
+    for p in ps:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert res == [(0, 2.0, 20.0), (1, 2.0, 20.0)]
+
+
+def test_reference_arm_other_ranks_exit_without_work():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
+                        "--warmup", "0"], env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == ""
