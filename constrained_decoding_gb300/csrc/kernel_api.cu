@@ -4,7 +4,12 @@
 #include <cstring>
 #include <string>
 
+#include <algorithm>
+#include <vector>
+
 #include "gemm.h"
+#include "kernels.h"
+#include "pcd.h"
 #include "pcd_kernels.h"
 #include "plan.h"
 
@@ -36,6 +41,76 @@ extern "C" int pcd_k_gemm(const void* a, int M, int lda, const void* b, int N, i
   e.ldo = ldo;
   const int r = pcd::launch_gemm(s, epi, e, t, static_cast<cudaStream_t>(stream), dev_err, 2000000000ull, sms);
   return r == 0 ? 0 : (r < 0 ? -1 : -10);
+}
+
+namespace {
+// Scratch layout of the readout: partials [n_tiles][R] float2, then the gather
+// CSR [n_tiles + 1] int32, then the gather entries [n_cand] int4.  Sized for
+// the smallest N tile (the most tiles) so any tiling fits.
+int64_t readout_scratch_bytes(int R, int V, int n_cand) {
+  const int64_t tiles = (V + 127) / 128;
+  const int64_t part = tiles * R * 8;
+  const int64_t off = ((tiles + 1) * 4 + 15) / 16 * 16;
+  return (part + 255) / 256 * 256 + off + static_cast<int64_t>(n_cand) * 16 + 256;
+}
+
+int readout_into(const void* h, int R, const void* w, int V, int d, const int32_t* cand_row, const int32_t* cand_tok,
+                 int n_cand, float* lse, float* z_out, void* scratch, int64_t scratch_bytes, int* dev_err,
+                 cudaStream_t st) {
+  if (!h || !w || !lse || R < 1 || V < 32 || V % 32 || d < 64 || d % 64 || n_cand < 0) return PCD_ERR_INVALID_ARG;
+  if (n_cand > 0 && (!cand_row || !cand_tok || !z_out)) return PCD_ERR_INVALID_ARG;
+  if (!scratch || scratch_bytes < readout_scratch_bytes(R, V, n_cand)) return PCD_ERR_INVALID_ARG;
+  for (int i = 0; i < n_cand; ++i)
+    if (cand_row[i] < 0 || cand_row[i] >= R || cand_tok[i] < 0 || cand_tok[i] >= V) return PCD_ERR_TOKEN_RANGE;
+  const int sms = device_sms();
+  pcd::GemmTiling t = pcd::choose_tiling(R, V, d, pcd::EPI_READOUT, sms);
+  t.splits = 1;
+  const int tiles = pcd::gemm_n_tiles(V, t);
+  // host: gather entries sorted by vocabulary tile
+  std::vector<int> order(n_cand);
+  for (int i = 0; i < n_cand; ++i) order[i] = i;
+  std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return cand_tok[a] / t.bn < cand_tok[b] / t.bn; });
+  const int64_t part_bytes = (static_cast<int64_t>(tiles) * R * 8 + 255) / 256 * 256;
+  const int64_t off_bytes = ((static_cast<int64_t>(tiles) + 1) * 4 + 15) / 16 * 16;
+  std::vector<int32_t> host(static_cast<size_t>(off_bytes / 4 + 4 * n_cand), 0);
+  for (int i : order) host[cand_tok[i] / t.bn + 1]++;
+  for (int i = 0; i < tiles; ++i) host[i + 1] += host[i];
+  int32_t* g = host.data() + off_bytes / 4;
+  for (size_t k = 0; k < order.size(); ++k) {
+    const int i = order[k];
+    g[4 * k + 0] = cand_tok[i] % t.bn;
+    g[4 * k + 1] = cand_row[i];
+    g[4 * k + 2] = i;
+    g[4 * k + 3] = 0;
+  }
+  uint8_t* base = static_cast<uint8_t*>(scratch);
+  float2* part = reinterpret_cast<float2*>(base);
+  int32_t* dev_lists = reinterpret_cast<int32_t*>(base + part_bytes);
+  if (cudaMemcpyAsync(dev_lists, host.data(), host.size() * 4, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return PCD_ERR_CUDA;
+  pcd::GemmShape s{h, R, d, w, V, d, d};
+  pcd::EpiArgs e;
+  e.part = part;
+  e.gather_off = dev_lists;
+  e.gather = reinterpret_cast<const int4*>(dev_lists + off_bytes / 4);
+  e.z_out = z_out;
+  int r = pcd::launch_gemm(s, pcd::EPI_READOUT, e, t, st, dev_err, 2000000000ull, sms);
+  if (r != 0) return r < 0 ? PCD_ERR_INVALID_ARG : PCD_ERR_CUDA;
+  r = pcd::launch_lse_combine(part, tiles, R, lse, st);
+  return r == 0 ? PCD_OK : PCD_ERR_CUDA;
+}
+}  // namespace
+
+extern "C" int64_t pcd_k_readout_scratch_bytes(int R, int V, int n_cand) {
+  if (R < 1 || V < 1 || n_cand < 0) return 0;
+  return readout_scratch_bytes(R, V, n_cand);
+}
+
+extern "C" int pcd_k_readout(const void* h, int R, const void* w, int V, int d, const int32_t* cand_row,
+                             const int32_t* cand_tok, int n_cand, float* lse, float* z_out, void* scratch,
+                             int64_t scratch_bytes, int* dev_err, void* stream) {
+  return readout_into(h, R, w, V, d, cand_row, cand_tok, n_cand, lse, z_out, scratch, scratch_bytes, dev_err,
+                      static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int pcd_plan_inspect(const void* fields, int n_fields, int vocab, int32_t* sizes, int32_t* const* arrays) {

@@ -32,6 +32,24 @@ extern "C" {
 int pcd_k_gemm(const void* a, int M, int lda, const void* b, int N, int ldb, int K, int epi, void* out, int ldo,
                int mt, int bn, int splits, int* dev_err, void* stream);
 
+/* Fused vocabulary readout: the LM-head contraction z = h . W^T run tile by
+ * tile on the tensor cores with an online log-sum-exp over the whole
+ * vocabulary and a gather of selected logits, so the [R][V] logits are never
+ * written (PCD: A Technical Reference, section 4, stages 3-4: read only the
+ * candidate logits; the log-sum-exp turns them into full-vocabulary
+ * log-probs).  h [R][d] and w [V][d] are fp16 device matrices (K
+ * contiguous, d a multiple of 64, V a multiple of 32).  The gathered pairs are
+ * HOST arrays cand_row/cand_tok[n_cand] (row < R, token < V).  Outputs
+ * (device): lse[R] = log sum_v exp(z[r][v]) and z_out[n_cand] =
+ * z[cand_row][cand_tok], fp32.  `scratch` is a device buffer of at least
+ * pcd_k_readout_scratch_bytes(R, V, n_cand) bytes that the call overwrites
+ * (per-tile partial maxima and sums, the tile-sorted gather list).  Enqueued
+ * on `stream`; the gather list is copied from host memory first. */
+int64_t pcd_k_readout_scratch_bytes(int R, int V, int n_cand);
+int pcd_k_readout(const void* h, int R, const void* w, int V, int d, const int32_t* cand_row, const int32_t* cand_tok,
+                  int n_cand, float* lse, float* z_out, void* scratch, int64_t scratch_bytes, int* dev_err,
+                  void* stream);
+
 /* Host-only view of the branch compiler (no GPU needed): compiles `fields`
  * (pcd.h) for a vocabulary of `vocab` tokens into the packed branch batch the
  * branch pass runs (How TypeSafe's Jev Might Work, "When one token is not
