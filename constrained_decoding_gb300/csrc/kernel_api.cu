@@ -5,6 +5,7 @@
 #include <string>
 
 #include <algorithm>
+#include <mutex>
 #include <vector>
 
 #include "gemm.h"
@@ -111,6 +112,50 @@ extern "C" int pcd_k_readout(const void* h, int R, const void* w, int V, int d, 
                              int64_t scratch_bytes, int* dev_err, void* stream) {
   return readout_into(h, R, w, V, d, cand_row, cand_tok, n_cand, lse, z_out, scratch, scratch_bytes, dev_err,
                       static_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------ allocation-free readout
+// The readout's scratch for callers that cannot allocate: a fixed array in
+// device global memory, shared by every call on a device.  Host code may not
+// use the symbol's address directly (in host code it names a host-side
+// stand-in), so its device address is looked up once per device.
+static __device__ __align__(256) unsigned char g_readout_scratch[PCD_K_READOUT_NOALLOC_MAX_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of g_readout_scratch on the current device (looked up on the
+// first call per device, with that device current).
+int noalloc_scratch(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PCD_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_readout_scratch) != cudaSuccess || !p) {
+      cudaGetLastError();
+      return PCD_ERR_CUDA;
+    }
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return PCD_OK;
+}
+}  // namespace
+
+extern "C" int pcd_k_readout_noalloc(const void* h, int R, const void* w, int V, int d, const int32_t* cand_row,
+                                     const int32_t* cand_tok, int n_cand, float* lse, float* z_out, int* dev_err,
+                                     void* stream) {
+  if (R < 1 || V < 1 || n_cand < 0) return PCD_ERR_INVALID_ARG;
+  const int64_t need = readout_scratch_bytes(R, V, n_cand);
+  if (need > static_cast<int64_t>(PCD_K_READOUT_NOALLOC_MAX_BYTES)) return PCD_ERR_OOM;
+  void* scratch = nullptr;
+  const int rc = noalloc_scratch(&scratch);
+  if (rc != PCD_OK) return rc;
+  return readout_into(h, R, w, V, d, cand_row, cand_tok, n_cand, lse, z_out, scratch,
+                      static_cast<int64_t>(PCD_K_READOUT_NOALLOC_MAX_BYTES), dev_err, static_cast<cudaStream_t>(stream));
 }
 
 extern "C" int pcd_plan_inspect(const void* fields, int n_fields, int vocab, int32_t* sizes, int32_t* const* arrays) {

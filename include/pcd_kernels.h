@@ -50,6 +50,28 @@ int pcd_k_readout(const void* h, int R, const void* w, int V, int d, const int32
                   int n_cand, float* lse, float* z_out, void* scratch, int64_t scratch_bytes, int* dev_err,
                   void* stream);
 
+/* pcd_k_readout without a scratch argument, for callers that cannot allocate
+ * device memory: a serving loop whose GPU memory is already reserved by its
+ * own pool (a fresh cudaMalloc would fail or fragment it), or code on a
+ * latency-critical stream where cudaMalloc / cudaFree would synchronise the
+ * device and stall every other stream.  (The pages have no counterpart: it is
+ * a property of this library's interface, not of the method.)
+ * The scratch is one file-scope __device__ array of
+ * PCD_K_READOUT_NOALLOC_MAX_BYTES bytes that every GPU loading the library
+ * holds until the process exits.  Inputs, outputs and errors are those of
+ * pcd_k_readout; a problem whose pcd_k_readout_scratch_bytes(R, V, n_cand)
+ * exceeds the array returns PCD_ERR_OOM without launching anything.  The
+ * first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current; make that first call
+ * before any stream capture.  No call allocates or frees memory.  Every call
+ * shares the one array and leaves its contents behind; each call writes every
+ * scratch element it reads before reading it, so nothing needs clearing, but
+ * calls that overlap on the GPU (other streams, other threads) race on the
+ * array and must be serialised by the caller. */
+#define PCD_K_READOUT_NOALLOC_MAX_BYTES (8 * 1024 * 1024)
+int pcd_k_readout_noalloc(const void* h, int R, const void* w, int V, int d, const int32_t* cand_row,
+                          const int32_t* cand_tok, int n_cand, float* lse, float* z_out, int* dev_err, void* stream);
+
 /* Host-only view of the branch compiler (no GPU needed): compiles `fields`
  * (pcd.h) for a vocabulary of `vocab` tokens into the packed branch batch the
  * branch pass runs (How TypeSafe's Jev Might Work, "When one token is not
