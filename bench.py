@@ -204,7 +204,8 @@ def run_ours(args):
     cfg = synth.model_config(CONFIG_MODEL[args.config])
     weights = synth.make_weights(cfg, seed=0)
     req = synth.make_request(args.config)
-    stream = torch.cuda.current_stream()
+    stream = torch.cuda.Stream()          # a non-default stream: passes run as CUDA graphs
+    torch.cuda.set_stream(stream)
     model = pcd.pcd_load_weights_host(weights, stream=stream)
     plan = pcd.pcd_plan_create(model, req.fields)
     # distinct prefixes per step: same shape, different ids

@@ -59,8 +59,13 @@ struct DevBuf {
   size_t n = 0;
 };
 
+// Bumped whenever a workspace buffer moves: captured graphs of an older epoch
+// point at freed memory and are re-captured.
+uint64_t g_alloc_epoch = 1;
+
 int ensure(DevBuf& b, size_t bytes) {
   if (bytes <= b.n) return PCD_OK;
+  ++g_alloc_epoch;
   if (b.p) cudaFree(b.p);
   b.p = nullptr;
   b.n = 0;
@@ -126,6 +131,10 @@ struct pcd_model {
   size_t ev_next = 0;
   std::vector<std::tuple<int, cudaEvent_t, cudaEvent_t>> prof_rec;
   cudaEvent_t ev_a = nullptr, ev_b = nullptr, ev_c = nullptr;
+  // CUDA graphs of whole passes, keyed by everything a pass's launches bake in
+  bool graphs = true;
+  bool own_stream = false;
+  std::map<std::vector<int64_t>, std::pair<uint64_t, cudaGraphExec_t>> graph_cache;
 };
 
 struct pcd_cache {
@@ -201,6 +210,46 @@ int timed(pcd_model* m, int cls, Fn&& launch) {
   return r;
 }
 
+void drop_graphs(pcd_model* m) {
+  for (auto& kv : m->graph_cache) cudaGraphExecDestroy(kv.second.second);
+  m->graph_cache.clear();
+}
+
+// Runs `record` (a sequence of launches on the model stream) as a CUDA graph:
+// captured on first use of `key`, replayed afterwards.  `record` must not
+// allocate.  Without graphs (disabled, or profiling) the launches run directly.
+template <class Fn>
+int with_graph(pcd_model* m, const std::vector<int64_t>& key, Fn&& record) {
+  if (!m->graphs || m->prof) return record();
+  auto it = m->graph_cache.find(key);
+  if (it != m->graph_cache.end()) {
+    if (it->second.first == g_alloc_epoch) {
+      PCD_CUDA(cudaGraphLaunch(it->second.second, m->stream));
+      return PCD_OK;
+    }
+    cudaGraphExecDestroy(it->second.second);
+    m->graph_cache.erase(it);
+  }
+  if (m->graph_cache.size() >= 64) drop_graphs(m);
+  PCD_CUDA(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal));
+  const int rc = record();
+  cudaGraph_t graph = nullptr;
+  const cudaError_t ec = cudaStreamEndCapture(m->stream, &graph);
+  if (rc != PCD_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    cudaGetLastError();
+    return rc;
+  }
+  if (ec != cudaSuccess || !graph) return fail(PCD_ERR_CUDA, std::string("graph capture: ") + cudaGetErrorString(ec));
+  cudaGraphExec_t exec = nullptr;
+  const cudaError_t ei = cudaGraphInstantiate(&exec, graph, 0);
+  cudaGraphDestroy(graph);
+  if (ei != cudaSuccess) return fail(PCD_ERR_CUDA, std::string("graph instantiate: ") + cudaGetErrorString(ei));
+  m->graph_cache[key] = {g_alloc_epoch, exec};
+  PCD_CUDA(cudaGraphLaunch(exec, m->stream));
+  return PCD_OK;
+}
+
 // D = A . B^T into `out` with the epilogue family `epi`:
 //   EPI_F32_ADD    residual += (split-K with atomics when the tiling splits K)
 //   EPI_F32_STORE  out = (zeroed + atomics when split)
@@ -246,8 +295,33 @@ int ensure_workspace(pcd_model* m, int T) {
 
 // -------------------------------------------------------------- prefill pass
 // Tokens ids[0..n) at positions p0..p0+n-1 of cache c (rows p0.. are written).
+int record_prefill(pcd_model* m, const int32_t* d_ids, int n, pcd_cache* c, int p0, int splits);
+
+// Key splits of the causal prefill attention: when the (row block, KV head)
+// CTAs would not cover the SMs twice, cut the keys into 256-key ranges and
+// combine the ranges' partial results (empty ranges of early blocks exit).
+int prefill_splits(const pcd_model* m, int n, int p0) {
+  const int blocks = ((n * m->G + 63) / 64) * m->Hkv;
+  if (blocks >= 2 * m->sms) return 1;
+  return std::max(1, std::min((2 * m->sms + blocks - 1) / blocks, (p0 + n + 255) / 256));
+}
+
 int run_prefill(pcd_model* m, const int32_t* d_ids, int n, pcd_cache* c, int p0) {
   PCD_TRY(ensure_workspace(m, n));
+  const int splits = prefill_splits(m, n, p0);
+  if (splits > 1) {
+    PCD_TRY(ensure(m->part_o, static_cast<size_t>(splits) * m->Hkv * n * m->G * m->dh * 4));
+    PCD_TRY(ensure(m->part_ml, static_cast<size_t>(splits) * m->Hkv * n * m->G * 8));
+  }
+  PCD_TRY(ensure(m->ids, static_cast<size_t>(n) * 4));
+  if (d_ids != m->ids.p)
+    PCD_CUDA(cudaMemcpyAsync(m->ids.p, d_ids, static_cast<size_t>(n) * 4, cudaMemcpyDeviceToDevice, m->stream));
+  const std::vector<int64_t> key{1, n, p0, reinterpret_cast<int64_t>(c->k), reinterpret_cast<int64_t>(c->v), c->cap};
+  const int32_t* ids = static_cast<const int32_t*>(m->ids.p);
+  return with_graph(m, key, [&] { return record_prefill(m, ids, n, c, p0, splits); });
+}
+
+int record_prefill(pcd_model* m, const int32_t* d_ids, int n, pcd_cache* c, int p0, int splits) {
   float* x = static_cast<float*>(m->x32.p);
   act_t* xn = static_cast<act_t*>(m->xn.p);
   float* qkv = static_cast<float*>(m->qkv.p);
@@ -296,14 +370,33 @@ int run_prefill(pcd_model* m, const int32_t* d_ids, int n, pcd_cache* c, int p0)
     aa.n_keys = p0 + n;
     aa.rel = nullptr;
     aa.base = p0;
-    aa.n_splits = 1;
-    aa.split_len = ((p0 + n + 63) / 64) * 64;
+    aa.n_splits = splits;
+    aa.split_len = ((p0 + n + splits - 1) / splits + 63) / 64 * 64;  // the splits cover every key
     aa.scale_log2 = 1.4426950408889634f / std::sqrt(static_cast<float>(m->dh));
     aa.out = att;
     aa.ld_out = m->qdim;
-    aa.partial = 0;
+    aa.partial = splits > 1;
+    aa.part_o = static_cast<float*>(m->part_o.p);
+    aa.part_ml = static_cast<float2*>(m->part_ml.p);
     aa.causal_heavy_first = 1;
     PCD_LAUNCH(timed(m, PROF_ATTN_PREFILL, [&] { return pcd::launch_attention(aa, m->stream); }));
+    if (splits > 1) {
+      pcd::MergeArgs ma{};
+      ma.q = q;
+      ma.n_tok = n;
+      ma.Hq = m->Hq;
+      ma.Hkv = m->Hkv;
+      ma.DH = m->dh;
+      ma.part_o = aa.part_o;
+      ma.part_ml = aa.part_ml;
+      ma.n_splits = splits;
+      ma.anc_off = nullptr;
+      ma.anc_idx = nullptr;
+      ma.scale_log2 = aa.scale_log2;
+      ma.out = att;
+      ma.ld_out = m->qdim;
+      PCD_LAUNCH(timed(m, PROF_ATTN_PREFILL, [&] { return pcd::launch_branch_merge(ma, m->stream); }));
+    }
     PCD_TRY(gemm(m, PROF_GEMM_PREFILL, att, n, m->qdim, W.wo, m->d, m->qdim, m->qdim, pcd::EPI_F32_ADD, x, m->d));
     PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
       return pcd::launch_rmsnorm(x, m->d, nullptr, n, m->d, W.mlp_norm, m->cfg.rms_eps, xn, m->d, m->stream);
@@ -319,6 +412,9 @@ struct Segment {
   const pcd_cache* c;
   int t0, t1;  // branch tokens of this request
 };
+
+int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_seg, float* d_result, int splits,
+                  cudaEvent_t ev_mid);
 
 int run_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_seg, float* d_result,
                cudaEvent_t ev_mid = nullptr) {
@@ -337,6 +433,22 @@ int run_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_seg, 
   PCD_TRY(ensure(m->ro_part, static_cast<size_t>(p.n_vtiles) * std::max(R, 1) * 8));
   PCD_TRY(ensure(m->z, static_cast<size_t>(std::max(p.n_children, 1)) * 4));
   PCD_TRY(ensure(m->lse, static_cast<size_t>(std::max(R, 1)) * 4));
+  if (ev_mid) return record_branch(m, p, segs, n_seg, d_result, splits, ev_mid);
+  std::vector<int64_t> key{2, reinterpret_cast<int64_t>(p.tok), T, R, p.n_children, p.n_labels, p.n_fields,
+                           reinterpret_cast<int64_t>(d_result), splits, n_seg};
+  for (int s = 0; s < n_seg; ++s) {
+    key.push_back(reinterpret_cast<int64_t>(segs[s].c->k));
+    key.push_back(segs[s].c->cap);
+    key.push_back(segs[s].c->len);
+    key.push_back(segs[s].t0);
+    key.push_back(segs[s].t1);
+  }
+  return with_graph(m, key, [&] { return record_branch(m, p, segs, n_seg, d_result, splits, nullptr); });
+}
+
+int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_seg, float* d_result, int splits,
+                  cudaEvent_t ev_mid) {
+  const int T = p.T, R = p.R, G = m->G;
 
   float* x = static_cast<float*>(m->x32.p);
   act_t* xn = static_cast<act_t*>(m->xn.p);
@@ -617,6 +729,16 @@ int build_model(const pcd_model_config& cfg, TensorFn get, void* ctx, int dtype,
   m->Nqkv = m->qdim + 2 * m->kvdim;
   m->max_pos = cfg.max_positions > 0 ? cfg.max_positions : 32768;
   m->stream = static_cast<cudaStream_t>(stream);
+  if (!m->stream) {
+    // a blocking stream of our own: ordered with the legacy default stream,
+    // and capturable into graphs
+    if (cudaStreamCreate(&m->stream) != cudaSuccess) {
+      delete m;
+      return fail(PCD_ERR_CUDA, "stream creation failed");
+    }
+    m->own_stream = true;
+  }
+  if (const char* g = std::getenv("PCD_GRAPHS")) m->graphs = std::atoi(g) != 0;
   m->sms = prop.multiProcessorCount;
   if (const char* w = std::getenv("PCD_WAIT_LIMIT_MS")) m->wait_ns = static_cast<uint64_t>(std::atof(w) * 1e6);
 
@@ -884,7 +1006,10 @@ int score_impl(pcd_model* m, const pcd_cache* const* caches, const pcd_field* co
   PCD_TRY(upload_plan(m, hp, v, &plan_bytes));
   PCD_TRY(ensure(m->result, static_cast<size_t>(v.result_floats()) * 4));
   if (stats) cudaEventRecord(m->ev_a, m->stream);
-  PCD_TRY(run_branch(m, v, segs.data(), n_req, static_cast<float*>(m->result.p), stats ? m->ev_b : nullptr));
+  // the mid-pass event splits branch and readout time; it forces direct
+  // launches, so it is only used when graphs are off
+  cudaEvent_t mid = (stats && !m->graphs) ? m->ev_b : nullptr;
+  PCD_TRY(run_branch(m, v, segs.data(), n_req, static_cast<float*>(m->result.p), mid));
   if (stats) cudaEventRecord(m->ev_c, m->stream);
   const size_t rbytes = static_cast<size_t>(v.result_floats()) * 4;
   PCD_TRY(ensure_pinned(m->down, m->down_n, rbytes));
@@ -898,8 +1023,12 @@ int score_impl(pcd_model* m, const pcd_cache* const* caches, const pcd_field* co
     const auto t_end = std::chrono::steady_clock::now();
     std::memset(stats, 0, sizeof(*stats));
     stats->compile_ms = std::chrono::duration<float, std::milli>(t_comp - t_start).count();
-    cudaEventElapsedTime(&stats->branch_ms, m->ev_a, m->ev_b);
-    cudaEventElapsedTime(&stats->readout_ms, m->ev_b, m->ev_c);
+    if (mid) {
+      cudaEventElapsedTime(&stats->branch_ms, m->ev_a, m->ev_b);
+      cudaEventElapsedTime(&stats->readout_ms, m->ev_b, m->ev_c);
+    } else {
+      cudaEventElapsedTime(&stats->branch_ms, m->ev_a, m->ev_c);
+    }
     stats->total_ms = std::chrono::duration<float, std::milli>(t_end - t_start).count();
     stats->forward_passes = 1;
     stats->branch_tokens = v.T;
@@ -993,6 +1122,8 @@ void pcd_model_free(pcd_model* m) {
   if (m->up) cudaFreeHost(m->up);
   if (m->down) cudaFreeHost(m->down);
   if (m->up_ev) cudaEventDestroy(m->up_ev);
+  drop_graphs(m);
+  if (m->own_stream && m->stream) cudaStreamDestroy(m->stream);
   for (cudaEvent_t e : m->ev_pool) cudaEventDestroy(e);
   for (cudaEvent_t e : {m->ev_a, m->ev_b, m->ev_c})
     if (e) cudaEventDestroy(e);

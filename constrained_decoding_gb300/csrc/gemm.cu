@@ -18,7 +18,10 @@
 
 #include <algorithm>
 #include <cstdio>
+#include <cstdlib>
 #include <mutex>
+#include <tuple>
+#include <unordered_map>
 
 #include "common.cuh"
 #include "gemm.h"
@@ -131,11 +134,14 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, const EpiArgs& e,
   }
 }
 
-template <int MT, int BN, int EPI>
+template <int MT, int BN, int EPI, int CS>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p, const EpiArgs e) {
   using C = GemmCfg<MT, BN>;
+  static_assert(CS == 1 || MT == 1, "clusters share B across single-tile CTAs");
+  constexpr uint16_t MASK = static_cast<uint16_t>((1u << CS) - 1u);
+  constexpr int B_SLICE = BN / CS;  // B rows each CTA of a cluster loads and multicasts
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
@@ -148,11 +154,18 @@ __global__ void __launch_bounds__(192, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  // work distribution: a CTA (CS = 1) or a cluster (CS > 1) takes units slot,
+  // slot + stride, ...; in a cluster every CTA runs the same units, on its own
+  // M tile, and they share the B tile
+  const int rank = CS > 1 ? static_cast<int>(cluster_ctarank()) : 0;
+  const int slot = CS > 1 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
+  const int stride = CS > 1 ? static_cast<int>(n_clusters_x()) : static_cast<int>(gridDim.x);
+  const int mtiles = (p.M + 127) / 128;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], CS);
     }
     for (int a = 0; a < C::ACC_STAGES; ++a) {
       mbar_init(&tfull[a], 1);
@@ -171,9 +184,16 @@ __global__ void __launch_bounds__(192, 1)
     tmem_relinquish();
   }
   tc_fence_before_sync();
-  __syncthreads();
+  if constexpr (CS > 1) {
+    cluster_sync_all();  // peers multicast into this CTA only once its barriers exist
+  } else {
+    __syncthreads();
+  }
   tc_fence_after_sync();
   const uint32_t tbase = *tmem_slot;
+
+  auto tile0 = [&](int mg) { return mg * MT * CS + rank * MT; };  // this CTA's first M tile of group mg
+  auto valid_tiles = [&](int mg) { return max(0, min(MT, mtiles - tile0(mg))); };
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -184,11 +204,11 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t last_phase[8];
       bool issued[8];
       for (int s = 0; s < 8; ++s) issued[s] = false, last_phase[s] = 0;
-      for (int u = blockIdx.x; u < p.n_units && !*abort_flag; u += gridDim.x) {
+      for (int u = slot; u < p.n_units && !*abort_flag; u += stride) {
         int nt, mg, ks;
         decode_unit(p, u, nt, mg, ks);
         const int kb0 = ks * p.nkb / p.k_splits, kb1 = (ks + 1) * p.nkb / p.k_splits;
-        const int mt_valid = min(MT, (p.M - mg * MT * 128 + 127) / 128);
+        const int mt_valid = valid_tiles(mg);
         const uint32_t bytes = mt_valid * C::A_BYTES + C::B_BYTES;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns)) {
@@ -199,8 +219,13 @@ __global__ void __launch_bounds__(192, 1)
           mbar_arrive_expect_tx(&full[stage], bytes);
           uint8_t* base = smem + stage * C::STAGE_BYTES;
           for (int mt = 0; mt < mt_valid; ++mt)
-            tma_load_2d(base + mt * C::A_BYTES, &tmA, &full[stage], kb * 64, (mg * MT + mt) * 128);
-          tma_load_2d_hint(base + MT * C::A_BYTES, &tmB, &full[stage], kb * 64, nt * BN, pol_b);
+            tma_load_2d(base + mt * C::A_BYTES, &tmA, &full[stage], kb * 64, (tile0(mg) + mt) * 128);
+          if constexpr (CS == 1) {
+            tma_load_2d_hint(base + MT * C::A_BYTES, &tmB, &full[stage], kb * 64, nt * BN, pol_b);
+          } else {
+            tma_load_2d_mc(base + MT * C::A_BYTES + rank * B_SLICE * 128, &tmB, &full[stage], kb * 64,
+                           nt * BN + rank * B_SLICE, MASK, pol_b);
+          }
           issued[stage] = true;
           last_phase[stage] = phase;
           if (++stage == C::STAGES) {
@@ -214,6 +239,11 @@ __global__ void __launch_bounds__(192, 1)
         for (int s = 0; s < C::STAGES; ++s)
           if (issued[s]) mbar_wait(&full[s], last_phase[s], p.wait_ns);
       }
+      if constexpr (CS > 1) {
+        // every peer's release of the last fill of each stage has arrived here
+        for (int s = 0; s < C::STAGES; ++s)
+          if (issued[s] && !mbar_wait(&empty[s], last_phase[s], p.wait_ns)) record_error(p.err, DEV_WAIT_TIMEOUT_PRODUCER);
+      }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -222,11 +252,11 @@ __global__ void __launch_bounds__(192, 1)
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool any = false;
-      for (int u = blockIdx.x; u < p.n_units && !*abort_flag; u += gridDim.x) {
+      for (int u = slot; u < p.n_units && !*abort_flag; u += stride) {
         int nt, mg, ks;
         decode_unit(p, u, nt, mg, ks);
         const int kb0 = ks * p.nkb / p.k_splits, kb1 = (ks + 1) * p.nkb / p.k_splits;
-        const int mt_valid = min(MT, (p.M - mg * MT * 128 + 127) / 128);
+        const int mt_valid = valid_tiles(mg);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, p.wait_ns)) {
           record_error(p.err, DEV_WAIT_TIMEOUT_MMA);
           *abort_flag = 1;
@@ -249,10 +279,14 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               umma_f16(d_base + mt * BN, sdesc_kmajor_sw128(a_base + mt * C::A_BYTES + k * 32),
-                        sdesc_kmajor_sw128(b_base + k * 32), IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+                       sdesc_kmajor_sw128(b_base + k * 32), IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
             }
           }
-          umma_commit(&empty[stage]);
+          if constexpr (CS == 1) {
+            umma_commit(&empty[stage]);
+          } else {
+            umma_commit_mc(&empty[stage], MASK);  // the stage is free once every CTA of the cluster is done
+          }
           any = true;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -277,10 +311,10 @@ __global__ void __launch_bounds__(192, 1)
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = blockIdx.x; u < p.n_units && !*abort_flag; u += gridDim.x) {
+    for (int u = slot; u < p.n_units && !*abort_flag; u += stride) {
       int nt, mg, ks;
       decode_unit(p, u, nt, mg, ks);
-      const int mt_valid = min(MT, (p.M - mg * MT * 128 + 127) / 128);
+      const int mt_valid = valid_tiles(mg);
       if (!mbar_wait(&tfull[acc], acc_phase, p.wait_ns)) {
         record_error(p.err, DEV_WAIT_TIMEOUT_EPILOGUE);
         *abort_flag = 1;
@@ -288,7 +322,8 @@ __global__ void __launch_bounds__(192, 1)
       }
       tc_fence_after_sync();
       for (int mt = 0; mt < mt_valid; ++mt) {
-        const int row = (mg * MT + mt) * 128 + q * 32 + lane;
+        const int tile = tile0(mg) + mt;
+        const int row = tile * 128 + q * 32 + lane;
         const uint32_t t_row = tbase + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS + mt * BN;
         float run_m = -INFINITY, run_s = 0.f;
         for (int c = 0; c < BN / 32; ++c) {
@@ -305,7 +340,7 @@ __global__ void __launch_bounds__(192, 1)
           for (int g = g0; g < g1; ++g) {
             const int4 en = e.gather[g];
             const int r = en.y;
-            if (r / 128 != mg * MT + mt || ((r & 127) >> 5) != q) continue;
+            if (r / 128 != tile || ((r & 127) >> 5) != q) continue;
             const float z = tmem_ld_1col(t_row + en.x);
             if (lane == (r & 31)) e.z_out[en.z] = z;
           }
@@ -321,7 +356,11 @@ __global__ void __launch_bounds__(192, 1)
   }
 
   tc_fence_before_sync();
-  __syncthreads();
+  if constexpr (CS > 1) {
+    cluster_sync_all();  // no peer touches this CTA's shared memory after this point
+  } else {
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tbase, C::TMEM_COLS);
@@ -345,7 +384,42 @@ bool tma_init() {
 }
 
 // 16-bit matrix [rows][>= cols], row stride ld elements; box 64 (K) x box_rows.
+// Encoded maps are cached by (pointer, shape, box): the executor reuses the
+// same weight and workspace matrices every call.
+struct MapKey {
+  uintptr_t p;
+  int rows, cols, ld, box;
+  bool operator==(const MapKey& o) const {
+    return p == o.p && rows == o.rows && cols == o.cols && ld == o.ld && box == o.box;
+  }
+};
+struct MapKeyHash {
+  size_t operator()(const MapKey& k) const {
+    size_t h = std::hash<uintptr_t>()(k.p);
+    for (int v : {k.rows, k.cols, k.ld, k.box}) h = h * 1000003u ^ static_cast<size_t>(v);
+    return h;
+  }
+};
+static std::mutex g_map_mu;
+static std::unordered_map<MapKey, CUtensorMap, MapKeyHash> g_maps;
+
+static bool encode_map(CUtensorMap* m, const void* ptr, int rows, int cols, int ld, int box_rows);
+
 static bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int ld, int box_rows) {
+  const MapKey k{reinterpret_cast<uintptr_t>(ptr), rows, cols, ld, box_rows};
+  std::lock_guard<std::mutex> lock(g_map_mu);
+  auto it = g_maps.find(k);
+  if (it != g_maps.end()) {
+    *m = it->second;
+    return true;
+  }
+  if (!encode_map(m, ptr, rows, cols, ld, box_rows)) return false;
+  if (g_maps.size() > 4096) g_maps.clear();
+  g_maps.emplace(k, *m);
+  return true;
+}
+
+static bool encode_map(CUtensorMap* m, const void* ptr, int rows, int cols, int ld, int box_rows) {
   if (!tma_init()) return false;
   if ((reinterpret_cast<uintptr_t>(ptr) & 15) || (ld * 2) % 16) return false;
   cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
@@ -358,30 +432,72 @@ static bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int ld
   return r == CUDA_SUCCESS;
 }
 
-template <int MT, int BN, int EPI>
+template <int MT, int BN, int EPI, int CS>
 static int launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p, const EpiArgs& e,
                     cudaStream_t st, int sms) {
   using C = GemmCfg<MT, BN>;
-  auto kern = gemm_tc_kernel<MT, BN, EPI>;
+  auto kern = gemm_tc_kernel<MT, BN, EPI, CS>;
   static bool attr_set = false;  // per instantiation
+  static int max_clusters = 0;
   if (!attr_set) {
     cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (r != cudaSuccess) return r;
+    if (CS > 1) {
+      // how many clusters can be resident at once: the kernel is persistent
+      cudaLaunchConfig_t q = {};
+      q.gridDim = dim3(CS * (sms / CS), 1, 1);
+      q.blockDim = dim3(192, 1, 1);
+      q.dynamicSmemBytes = C::SMEM_BYTES;
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = CS;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      q.attrs = at;
+      q.numAttrs = 1;
+      int n = 0;
+      r = cudaOccupancyMaxActiveClusters(&n, kern, &q);
+      if (r != cudaSuccess) return r;
+      max_clusters = n > 0 ? n : 1;
+    }
     attr_set = true;
   }
-  const int grid = std::min(p.n_units, sms);
-  kern<<<grid, 192, C::SMEM_BYTES, st>>>(ma, mb, p, e);
-  return cudaGetLastError();
+  if (CS == 1) {
+    const int grid = std::min(p.n_units, sms);
+    kern<<<grid, 192, C::SMEM_BYTES, st>>>(ma, mb, p, e);
+    return cudaGetLastError();
+  }
+  const int clusters = std::min(p.n_units, max_clusters);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(clusters * CS, 1, 1);
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = CS;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, ma, mb, p, e);
 }
 
 template <int EPI>
 static int dispatch_tiling(const GemmTiling& t, const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p,
                            const EpiArgs& e, cudaStream_t st, int sms) {
-  if (t.mt == 1 && t.bn == 128) return launch_t<1, 128, EPI>(ma, mb, p, e, st, sms);
-  if (t.mt == 1 && t.bn == 256) return launch_t<1, 256, EPI>(ma, mb, p, e, st, sms);
-  if (t.mt == 2 && t.bn == 128) return launch_t<2, 128, EPI>(ma, mb, p, e, st, sms);
-  if (t.mt == 2 && t.bn == 256) return launch_t<2, 256, EPI>(ma, mb, p, e, st, sms);
-  if (t.mt == 4 && t.bn == 128) return launch_t<4, 128, EPI>(ma, mb, p, e, st, sms);
+  if (t.cs == 1) {
+    if (t.mt == 1 && t.bn == 128) return launch_t<1, 128, EPI, 1>(ma, mb, p, e, st, sms);
+    if (t.mt == 1 && t.bn == 256) return launch_t<1, 256, EPI, 1>(ma, mb, p, e, st, sms);
+    if (t.mt == 2 && t.bn == 128) return launch_t<2, 128, EPI, 1>(ma, mb, p, e, st, sms);
+    if (t.mt == 2 && t.bn == 256) return launch_t<2, 256, EPI, 1>(ma, mb, p, e, st, sms);
+    if (t.mt == 4 && t.bn == 128) return launch_t<4, 128, EPI, 1>(ma, mb, p, e, st, sms);
+  } else if (t.mt == 1) {
+    if (t.cs == 2 && t.bn == 128) return launch_t<1, 128, EPI, 2>(ma, mb, p, e, st, sms);
+    if (t.cs == 2 && t.bn == 256) return launch_t<1, 256, EPI, 2>(ma, mb, p, e, st, sms);
+    if (t.cs == 4 && t.bn == 128) return launch_t<1, 128, EPI, 4>(ma, mb, p, e, st, sms);
+    if (t.cs == 4 && t.bn == 256) return launch_t<1, 256, EPI, 4>(ma, mb, p, e, st, sms);
+  }
   return -1;
 }
 
@@ -396,16 +512,18 @@ int launch_gemm(const GemmShape& s, int epi, const EpiArgs& e, const GemmTiling&
   p.N = N;
   p.K = K;
   p.nkb = K / 64;
-  p.n_mgroups = ceil_div(M, 128 * t.mt);
+  if (t.cs != 1 && t.cs != 2 && t.cs != 4) return -1;
+  if (t.cs > 1 && t.mt != 1) return -1;
+  p.n_mgroups = ceil_div(M, 128 * t.mt * t.cs);
   p.n_ntiles = ceil_div(N, t.bn);
   p.k_splits = std::max(1, std::min(t.splits, p.nkb));
   p.n_units = p.n_mgroups * p.n_ntiles * p.k_splits;
   p.wait_ns = wait_ns;
   p.err = dev_err;
-  p.b_evict_first = p.n_mgroups == 1 ? 1 : 0;
+  p.b_evict_first = (p.n_mgroups == 1 && t.mt * t.cs * 128 >= M) ? 1 : 0;
   CUtensorMap ma, mb;
   if (!make_map(&ma, s.a, M, K, s.a_ld, 128)) return -1;
-  if (!make_map(&mb, s.b, N, K, s.b_ld, t.bn)) return -1;
+  if (!make_map(&mb, s.b, N, K, s.b_ld, t.bn / t.cs)) return -1;
   switch (epi) {
     case EPI_BF16: return dispatch_tiling<EPI_BF16>(t, ma, mb, p, e, stream, sms);
     case EPI_F32_ADD: return dispatch_tiling<EPI_F32_ADD>(t, ma, mb, p, e, stream, sms);
@@ -417,36 +535,44 @@ int launch_gemm(const GemmShape& s, int epi, const EpiArgs& e, const GemmTiling&
   return -1;
 }
 
-// Tiling heuristic.  Work units are (N tile, K split, M group); every unit
-// streams its B tile slice once and reuses it for MT*128 rows of A.  The
-// estimate charges each wave of units the larger of its tensor time and its
-// shared-memory fill time, plus a fixed pipeline fill / epilogue cost.
+// Tiling heuristic (calibrated on GB300).  One 128-row M tile per work unit:
+// it leaves room for the deepest stage ring, and the units that share a B
+// tile run on neighbouring CTAs and share it through L2.  A k-block costs the
+// larger of its MMA time (128 x BN x 64 x 2 flop at ~8192 flop/clk/SM) and its
+// shared-memory fill ((128 + BN) x 128 bytes at ~60 B/clk/SM, the rate a
+// 128x256 tile sustains at 82% of peak); a unit adds a fixed pipeline fill and
+// epilogue cost; waves of `sms` units run back to back.
 GemmTiling choose_tiling(int M, int N, int K, int epi, int sms) {
-  static const int cand[5][2] = {{1, 128}, {1, 256}, {2, 128}, {2, 256}, {4, 128}};
   const int nkb = K / 64;
+  const int mtiles = ceil_div(M, 128);
+  static const int max_cs = [] {
+    const char* e = std::getenv("PCD_GEMM_MAX_CS");
+    return e ? std::max(1, std::atoi(e)) : 4;
+  }();
   GemmTiling best;
+  best.mt = 1;
   double best_t = 1e30;
-  for (auto& c : cand) {
-    const int mt = c[0], bn = c[1];
-    const int mg = ceil_div(M, 128 * mt);
-    const int nt = ceil_div(N, bn);
-    const int max_split = (epi == EPI_F32_ATOMIC) ? std::max(1, nkb / 4) : 1;
-    for (int sp = 1; sp <= max_split; sp *= 2) {
-      const int units = mg * nt * sp;
-      const int waves = ceil_div(units, sms);
-      const int kbs = ceil_div(nkb, sp);
-      const int rows = std::min(mt * 128, ceil_div(M, 128) * 128);
-      // tensor cycles per k-block: rows x bn x 64 x 2 flop at ~8192 flop/clk/SM
-      const double mma = static_cast<double>(rows) * bn * 128.0 / 8192.0;
-      // bytes per k-block into smem at ~128 B/clk/SM
-      const double fill = (rows * 128.0 + bn * 128.0) / 128.0;
-      const double per_unit = kbs * std::max(mma, fill) + 1500.0 + (sp > 1 ? 300.0 : 0.0);
-      const double tt = waves * per_unit;
-      if (tt < best_t) {
-        best_t = tt;
-        best.mt = mt;
-        best.bn = bn;
-        best.splits = sp;
+  for (int cs : {1, 2, 4}) {
+    if (cs > max_cs) continue;
+    if (cs > 1 && mtiles < cs) continue;  // a cluster needs that many M tiles to share B
+    for (int bn : {128, 256}) {
+      const int nt = ceil_div(N, bn);
+      const int groups = ceil_div(mtiles, cs);
+      const int max_split = (epi == EPI_F32_ATOMIC) ? std::max(1, nkb / 3) : 1;
+      for (int sp = 1; sp <= max_split; sp *= 2) {
+        const int units = groups * nt * sp;         // each unit occupies cs SMs
+        const int slots = std::max(1, sms / cs);    // units running at once
+        const int kbs = ceil_div(nkb, sp);
+        const double mma = 128.0 * bn * 128.0 / 8192.0;
+        const double fill = (128.0 + static_cast<double>(bn) / cs) * 128.0 / 60.0;
+        const double per_unit = kbs * std::max(mma, fill) + 2500.0 + (cs > 1 ? 500.0 : 0.0);
+        const double tt = ceil_div(units, slots) * per_unit + (sp > 1 ? 400.0 : 0.0);
+        if (tt < best_t * 0.97) {
+          best_t = tt;
+          best.bn = bn;
+          best.splits = sp;
+          best.cs = cs;
+        }
       }
     }
   }

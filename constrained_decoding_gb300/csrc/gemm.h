@@ -35,6 +35,8 @@ struct GemmTiling {
   int mt = 1;       // 128-row M tiles per CTA work unit (1, 2 or 4)
   int bn = 256;     // N tile (128 or 256)
   int splits = 1;   // K splits (EPI_F32_ATOMIC only when > 1)
+  int cs = 1;       // cluster size along M (1, 2 or 4; mt must be 1): the CTAs of a
+                    // cluster share each B tile through TMA multicast
 };
 
 // Picks a tiling for the shape and epilogue on an `sms`-SM device.

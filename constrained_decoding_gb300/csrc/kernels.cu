@@ -38,38 +38,58 @@ int launch_embed(const int32_t* ids, int n, const act_t* E, int d, int vocab, fl
 }
 
 // ===================================================================== rmsnorm
-// One warp per row; fp32 statistics.
-__global__ void rmsnorm_kernel(const float* __restrict__ x, int ldx, const int32_t* __restrict__ rows, int n, int d,
-                               const float* __restrict__ gain, float eps, act_t* __restrict__ out, int ldo) {
-  const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (r >= n) return;
+// One CTA per row; the row stays in registers between the sum of squares and
+// the scaling (fp32 statistics).
+constexpr int kNormThreads = 256;
+constexpr int kNormMaxVec = 8;  // float4 per thread: d <= 8192
+
+__global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float* __restrict__ x, int ldx,
+                                                               const int32_t* __restrict__ rows, int n, int d,
+                                                               const float* __restrict__ gain, float eps,
+                                                               act_t* __restrict__ out, int ldo) {
+  const int r = blockIdx.x;
   const int src = rows ? rows[r] : r;
   const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(src) * ldx);
+  const int nv = d / 4;
+  float4 v[kNormMaxVec];
   float ss = 0.f;
-  for (int i = lane; i < d / 4; i += 32) {
-    float4 v = xr[i];
-    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+#pragma unroll
+  for (int j = 0; j < kNormMaxVec; ++j) {
+    const int i = threadIdx.x + j * kNormThreads;
+    if (i < nv) {
+      v[j] = xr[i];
+      ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
+    }
   }
 #pragma unroll
   for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  const float inv = rsqrtf(ss / static_cast<float>(d) + eps);
+  __shared__ float red[kNormThreads / 32];
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+#pragma unroll
+  for (int w = 0; w < kNormThreads / 32; ++w) tot += red[w];
+  const float inv = rsqrtf(tot / static_cast<float>(d) + eps);
   const float4* g4 = reinterpret_cast<const float4*>(gain);
   uint2* o2 = reinterpret_cast<uint2*>(out + static_cast<size_t>(r) * ldo);
-  for (int i = lane; i < d / 4; i += 32) {
-    float4 v = xr[i], g = g4[i];
-    uint2 w;
-    w.x = pack2(v.x * inv * g.x, v.y * inv * g.y);
-    w.y = pack2(v.z * inv * g.z, v.w * inv * g.w);
-    o2[i] = w;
+#pragma unroll
+  for (int j = 0; j < kNormMaxVec; ++j) {
+    const int i = threadIdx.x + j * kNormThreads;
+    if (i < nv) {
+      const float4 g = g4[i];
+      uint2 w;
+      w.x = pack2(v[j].x * inv * g.x, v[j].y * inv * g.y);
+      w.y = pack2(v[j].z * inv * g.z, v[j].w * inv * g.w);
+      o2[i] = w;
+    }
   }
 }
 
 int launch_rmsnorm(const float* x, int ldx, const int32_t* rows, int n, int d, const float* gain, float eps, act_t* out,
                    int ldo, cudaStream_t s) {
   if (n <= 0) return 0;
-  const int wpb = 8;
-  rmsnorm_kernel<<<(n + wpb - 1) / wpb, wpb * 32, 0, s>>>(x, ldx, rows, n, d, gain, eps, out, ldo);
+  if (d % 4 || d > 4 * kNormThreads * kNormMaxVec) return -1;
+  rmsnorm_kernel<<<n, kNormThreads, 0, s>>>(x, ldx, rows, n, d, gain, eps, out, ldo);
   return cudaGetLastError();
 }
 
@@ -400,11 +420,16 @@ int launch_attention(const AttnArgs& a, cudaStream_t s) {
 // ================================================================ branch merge
 // One warp per (branch token, query head): merges the prefix partials of all
 // key splits with the token's own ancestors in the branch (scaffold chain and
-// trie path, the token itself included).
+// trie path, the token itself included).  The ancestors' scores are computed
+// by the lanes in parallel (lane j scores ancestor j), then each lane
+// accumulates its DH/32 output dimensions over the weighted values.  With no
+// ancestor list (anc_off == nullptr) it only combines the key splits.
 template <int DH>
-__global__ void branch_merge_kernel(MergeArgs a) {
+__global__ void __launch_bounds__(256) branch_merge_kernel(MergeArgs a) {
   constexpr int EPT = DH >= 32 ? DH / 32 : 1;
-  const int w = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  __shared__ __align__(16) float sq[8][DH];
+  const int wl = threadIdx.x >> 5;
+  const int w = blockIdx.x * (blockDim.x >> 5) + wl;
   const int lane = threadIdx.x & 31;
   if (w >= a.n_tok * a.Hq) return;
   const int t = w / a.Hq, h = w % a.Hq;
@@ -412,15 +437,14 @@ __global__ void branch_merge_kernel(MergeArgs a) {
   const int hk = h / G, g = h % G;
   const int rows = a.n_tok * G;
   const int r = t * G + g;
-  float q[EPT], acc[EPT];
   const act_t* qp = a.q + (static_cast<size_t>(t) * a.Hq + h) * DH;
+  for (int d = lane; d < DH; d += 32) sq[wl][d] = a2f(qp[d]);
+  __syncwarp();
+
+  // prefix partials
+  float m = -INFINITY, l = 0.f, acc[EPT];
 #pragma unroll
-  for (int i = 0; i < EPT; ++i) {
-    const int d = lane + 32 * i;
-    q[i] = d < DH ? a2f(qp[d]) : 0.f;
-    acc[i] = 0.f;
-  }
-  float m = -INFINITY, l = 0.f;
+  for (int i = 0; i < EPT; ++i) acc[i] = 0.f;
   for (int sp = 0; sp < a.n_splits; ++sp) {
     const size_t prow = (static_cast<size_t>(sp) * a.Hkv + hk) * rows + r;
     const float2 ml = a.part_ml[prow];
@@ -431,34 +455,58 @@ __global__ void branch_merge_kernel(MergeArgs a) {
 #pragma unroll
     for (int i = 0; i < EPT; ++i) {
       const int d = lane + 32 * i;
-      const float ov = d < DH ? po[d] : 0.f;
-      acc[i] = acc[i] * co + ov * ml.y * cs;
+      acc[i] = acc[i] * co + (d < DH ? po[d] : 0.f) * ml.y * cs;
     }
     l = l * co + ml.y * cs;
     m = mn;
   }
-  for (int ai = a.anc_off[t]; ai < a.anc_off[t + 1]; ++ai) {
-    const int j = a.anc_idx[ai];
-    const act_t* kp = a.kb + (static_cast<size_t>(hk) * a.n_tok + j) * DH;
-    const act_t* vp = a.vb + (static_cast<size_t>(hk) * a.n_tok + j) * DH;
-    float dot = 0.f;
+  if (a.anc_off) {
+    const int a0 = a.anc_off[t], a1 = a.anc_off[t + 1];
+    for (int base = a0; base < a1; base += 32) {
+      const int na = min(32, a1 - base);
+      // lane j: score of ancestor base + j
+      float sc = -INFINITY;
+      int j = 0;
+      if (lane < na) {
+        j = a.anc_idx[base + lane];
+        const uint4* kp = reinterpret_cast<const uint4*>(a.kb + (static_cast<size_t>(hk) * a.n_tok + j) * DH);
+        float dot = 0.f;
 #pragma unroll
-    for (int i = 0; i < EPT; ++i) {
-      const int d = lane + 32 * i;
-      if (d < DH) dot += q[i] * a2f(kp[d]);
+        for (int c = 0; c < DH / 8; ++c) {
+          const uint4 kv = kp[c];
+          const __half2* k2 = reinterpret_cast<const __half2*>(&kv);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 kf = __half22float2(k2[e]);
+            dot += sq[wl][c * 8 + 2 * e] * kf.x + sq[wl][c * 8 + 2 * e + 1] * kf.y;
+          }
+        }
+        sc = dot * a.scale_log2;
+      }
+      float cm = sc;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) cm = fmaxf(cm, __shfl_xor_sync(0xffffffffu, cm, o));
+      const float mn = fmaxf(m, cm);
+      const float co = exp2f(m - mn);
+      const float p = lane < na ? exp2f(sc - mn) : 0.f;
+      float ps = p;
+#pragma unroll
+      for (int o = 16; o; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+#pragma unroll
+      for (int i = 0; i < EPT; ++i) acc[i] *= co;
+      l = l * co + ps;
+      m = mn;
+      for (int jj = 0; jj < na; ++jj) {
+        const float pj = __shfl_sync(0xffffffffu, p, jj);
+        const int aj = __shfl_sync(0xffffffffu, j, jj);
+        const act_t* vp = a.vb + (static_cast<size_t>(hk) * a.n_tok + aj) * DH;
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) {
+          const int d = lane + 32 * i;
+          if (d < DH) acc[i] += pj * a2f(vp[d]);
+        }
+      }
     }
-#pragma unroll
-    for (int o = 16; o; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-    const float sc = dot * a.scale_log2;
-    const float mn = fmaxf(m, sc);
-    const float co = exp2f(m - mn), p = exp2f(sc - mn);
-#pragma unroll
-    for (int i = 0; i < EPT; ++i) {
-      const int d = lane + 32 * i;
-      acc[i] = acc[i] * co + (d < DH ? p * a2f(vp[d]) : 0.f);
-    }
-    l = l * co + p;
-    m = mn;
   }
   const float il = l > 0.f ? 1.f / l : 0.f;
   act_t* dst = a.out + static_cast<size_t>(t) * a.ld_out + h * DH;

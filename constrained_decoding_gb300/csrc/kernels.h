@@ -61,7 +61,8 @@ struct MergeArgs {
   int n_splits;
   const act_t* kb;           // branch keys/values [Hkv][n_tok][DH]
   const act_t* vb;
-  const int32_t* anc_off;   // [n_tok + 1]: ancestors (incl. itself) of token t in the branch batch
+  const int32_t* anc_off;   // [n_tok + 1]: ancestors (incl. itself) of token t in the branch batch;
+                            // nullptr: only combine the key splits (split prefill attention)
   const int32_t* anc_idx;
   float scale_log2;
   act_t* out;                // out[t][h * DH + d]

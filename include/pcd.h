@@ -22,8 +22,10 @@
  *  - Host pointers unless a name ends in _device.  Inputs are borrowed for the
  *    duration of the call only (copied).  Result arrays are caller-allocated.
  *    Handles are freed only by pcd_*_free.
- *  - A model owns one CUDA stream (the one given at load, NULL = legacy
- *    default stream); every call is ordered on it.  Calls that return host
+ *  - A model owns one CUDA stream (the one given at load; for NULL the
+ *    library creates a blocking stream, which is ordered with the legacy
+ *    default stream); every call is ordered on it.  Passes run as CUDA
+ *    graphs captured on first use (environment PCD_GRAPHS=0 disables them).  Calls that return host
  *    results synchronise that stream; *_device calls only enqueue.
  *  - A cache is immutable once created: it may be scored many times and
  *    extended into new caches.
@@ -110,8 +112,9 @@ typedef struct {
   float mass, log_mass, margin, first_mass;
 } pcd_field_result;
 
-/* Phase timings (CUDA events on the model stream) and the true number of
- * sequential forward passes (PCD From First Principles, "Where the two real
+/* Phase timings (CUDA events on the model stream; when the branch pass runs
+ * as a CUDA graph, branch_ms covers the readout too and readout_ms is 0) and
+ * the true number of sequential forward passes (PCD From First Principles, "Where the two real
  * implementations disagree": count what ran, do not hard-code it). */
 typedef struct {
   float prefill_ms, compile_ms, branch_ms, readout_ms, total_ms;

@@ -26,7 +26,9 @@ extern "C" {
  * the contraction of every QKV, output and SwiGLU projection of the decoder
  * (configs: nn.Linear weights [out][in] as B, activations [tokens][in] as A).
  * K must be a multiple of 64, N a multiple of 32.  mt/bn/splits force a
- * tiling (mt in {1,2,4}, bn in {128,256}); mt = 0 lets the library choose.
+ * tiling (mt in {1,2,4}, bn in {128,256}); mt = 0 lets the library choose;
+ * mt = 21 or 41 runs clusters of 2 or 4 CTAs along M (one 128-row tile each)
+ * that share every B tile through TMA multicast.
  * `dev_err` (device int, may be NULL) receives a nonzero code if a pipeline
  * wait times out. */
 int pcd_k_gemm(const void* a, int M, int lda, const void* b, int N, int ldb, int K, int epi, void* out, int ldo,

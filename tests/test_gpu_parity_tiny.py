@@ -144,3 +144,13 @@ def test_validation_errors(pcd, model, request1):
 def test_kv_bytes(pcd, model, tiny_weights):
     c = tiny_weights.cfg
     assert pcd.pcd_kv_bytes_per_token(model) == c.n_layers * 2 * c.n_kv_heads * c.head_dim * 2
+
+
+@pytest.mark.parametrize("prefix_len", [300, 700, 1500])
+def test_long_prefix_split_attention(pcd, model, tiny_oracle, prefix_len):
+    """Prefixes long enough that the prefill attention cuts its keys into
+    several ranges (and the branch pass does too) still match the oracle."""
+    req = make_custom(40 + prefix_len, 512, prefix_len, [("bool",), ("enum", 4, 1, 3), ("shared", 5, 2, 3)])
+    cache = pcd.pcd_prefill(model, req.prefix)
+    got = pcd.pcd_score(model, cache, req.fields)
+    compare_request(got, _oracle_results(tiny_oracle, req), f"prefix {prefix_len}")
