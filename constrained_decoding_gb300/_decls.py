@@ -51,6 +51,8 @@ SIGNATURES = [
     ("pcd_profile_read", c_int, [c_void_p, P(c_int), P(c_float)]),
     ("pcd_strerror", c_char_p, [c_int]),
     ("pcd_last_error", c_char_p, []),
+    ("pcd_k_gemm_split", c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, c_int, c_int, c_int, c_int, c_void_p,
+                                 c_int, c_int, c_int, c_void_p, c_void_p]),
     ("pcd_k_readout_scratch_bytes", c_int64, [c_int, c_int, c_int]),
     ("pcd_k_readout", c_int, [c_void_p, c_int, c_void_p, c_int, c_int, P(c_int32), P(c_int32), c_int, c_void_p,
                               c_void_p, c_void_p, c_int64, c_void_p, c_void_p]),

@@ -115,7 +115,8 @@ struct pcd_model {
   float2* rope = nullptr;
   int* d_err = nullptr;
   uint64_t wait_ns = 2000000000ull;
-  DevBuf x32, xn, qkv, q, kb, vb, att, hb, part_o, part_ml, hr, ro_part, z, lse, plan_buf, result, ids;
+  DevBuf x32, xn, xn_lo, qkv, q, kb, vb, att, att_lo, hb, hb_lo, hr_lo, part_o, part_ml, hr, ro_part, z, lse, plan_buf,
+      result, ids;
   // pinned staging: `up` feeds host->device copies (reused only once the last
   // copy from it has completed: up_ev), `down` receives results
   void* up = nullptr;
@@ -134,6 +135,11 @@ struct pcd_model {
   // CUDA graphs of whole passes, keyed by everything a pass's launches bake in
   bool graphs = true;
   bool own_stream = false;
+  // which fp16 GEMM inputs also carry their rounding remainder (hi + lo):
+  // 1 branch-pass normalised inputs, 2 prefill normalised inputs, 4 branch
+  // attention and SwiGLU outputs, 8 prefill attention and SwiGLU outputs,
+  // 16 the readout rows
+  int split_act = 1;
   std::map<std::vector<int64_t>, std::pair<uint64_t, cudaGraphExec_t>> graph_cache;
 };
 
@@ -255,15 +261,19 @@ int with_graph(pcd_model* m, const std::vector<int64_t>& key, Fn&& record) {
 //   EPI_F32_STORE  out = (zeroed + atomics when split)
 //   EPI_SWIGLU / EPI_BF16: one K split
 int gemm(pcd_model* m, int cls, const void* A, int M, int lda, const act_t* B, int N, int ldb, int K, int epi, void* out,
-         int ldo) {
+         int ldo, const void* A_lo = nullptr, void* out_lo = nullptr) {
   if (M <= 0) return PCD_OK;
   const bool splittable = (epi == pcd::EPI_F32_ADD || epi == pcd::EPI_F32_STORE);
   const int key_epi = splittable ? pcd::EPI_F32_ATOMIC : epi;
-  auto key = std::make_tuple(M, N, K, key_epi);
+  auto key = std::make_tuple(M, N, K, key_epi + (A_lo ? 100 : 0));
   auto it = m->tilings.find(key);
   pcd::GemmTiling t;
   if (it == m->tilings.end()) {
     t = pcd::choose_tiling(M, N, K, key_epi, m->sms);
+    if (A_lo) {  // the hi + lo form runs one 128-row tile per CTA, no cluster
+      t.mt = 1;
+      t.cs = 1;
+    }
     m->tilings[key] = t;
   } else {
     t = it->second;
@@ -274,10 +284,11 @@ int gemm(pcd_model* m, int cls, const void* A, int M, int lda, const act_t* B, i
       PCD_CUDA(cudaMemsetAsync(out, 0, static_cast<size_t>(M) * ldo * sizeof(float), m->stream));
     run_epi = pcd::EPI_F32_ATOMIC;
   }
-  pcd::GemmShape s{A, M, lda, B, N, ldb, K};
+  pcd::GemmShape s{A, M, lda, B, N, ldb, K, A_lo};
   pcd::EpiArgs e;
   e.out = out;
   e.ldo = ldo;
+  e.out_lo = out_lo;
   PCD_LAUNCH(timed(m, cls, [&] { return pcd::launch_gemm(s, run_epi, e, t, m->stream, m->d_err, m->wait_ns, m->sms); }));
   return PCD_OK;
 }
@@ -290,6 +301,11 @@ int ensure_workspace(pcd_model* m, int T) {
   PCD_TRY(ensure(m->q, t * m->qdim * 2));
   PCD_TRY(ensure(m->att, t * m->qdim * 2));
   PCD_TRY(ensure(m->hb, t * m->Fp * 2));
+  PCD_TRY(ensure(m->xn_lo, t * m->d * 2));
+  if (m->split_act & (4 | 8)) {
+    PCD_TRY(ensure(m->att_lo, t * m->qdim * 2));
+    PCD_TRY(ensure(m->hb_lo, t * m->Fp * 2));
+  }
   return PCD_OK;
 }
 
@@ -309,7 +325,7 @@ int prefill_splits(const pcd_model* m, int n, int p0) {
 int run_prefill(pcd_model* m, const int32_t* d_ids, int n, pcd_cache* c, int p0) {
   PCD_TRY(ensure_workspace(m, n));
   const int splits = prefill_splits(m, n, p0);
-  if (splits > 1) {
+  if (splits > 1 || (m->split_act & 8)) {
     PCD_TRY(ensure(m->part_o, static_cast<size_t>(splits) * m->Hkv * n * m->G * m->dh * 4));
     PCD_TRY(ensure(m->part_ml, static_cast<size_t>(splits) * m->Hkv * n * m->G * 8));
   }
@@ -328,14 +344,18 @@ int record_prefill(pcd_model* m, const int32_t* d_ids, int n, pcd_cache* c, int 
   act_t* q = static_cast<act_t*>(m->q.p);
   act_t* att = static_cast<act_t*>(m->att.p);
   act_t* hb = static_cast<act_t*>(m->hb.p);
+  act_t* xlo = (m->split_act & 2) ? static_cast<act_t*>(m->xn_lo.p) : nullptr;
+  const bool split_out = (m->split_act & 8) != 0;
+  act_t* att_lo = split_out ? static_cast<act_t*>(m->att_lo.p) : nullptr;
+  act_t* hb_lo = split_out ? static_cast<act_t*>(m->hb_lo.p) : nullptr;
   const size_t layer_kv = static_cast<size_t>(m->Hkv) * c->cap * m->dh;
   PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_embed(d_ids, n, m->embed, m->d, m->V, x, m->d_err, m->stream); }));
   for (int l = 0; l < m->L; ++l) {
     const Layer& W = m->layers[l];
     PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
-      return pcd::launch_rmsnorm(x, m->d, nullptr, n, m->d, W.attn_norm, m->cfg.rms_eps, xn, m->d, m->stream);
+      return pcd::launch_rmsnorm(x, m->d, nullptr, n, m->d, W.attn_norm, m->cfg.rms_eps, xn, m->d, m->stream, xlo);
     }));
-    PCD_TRY(gemm(m, PROF_GEMM_PREFILL, xn, n, m->d, W.wqkv, m->Nqkv, m->d, m->d, pcd::EPI_F32_STORE, qkv, m->Nqkv));
+    PCD_TRY(gemm(m, PROF_GEMM_PREFILL, xn, n, m->d, W.wqkv, m->Nqkv, m->d, m->d, pcd::EPI_F32_STORE, qkv, m->Nqkv, xlo));
     pcd::RopeArgs ra;
     ra.qkv = qkv;
     ra.ldqkv = m->Nqkv;
@@ -375,12 +395,12 @@ int record_prefill(pcd_model* m, const int32_t* d_ids, int n, pcd_cache* c, int 
     aa.scale_log2 = 1.4426950408889634f / std::sqrt(static_cast<float>(m->dh));
     aa.out = att;
     aa.ld_out = m->qdim;
-    aa.partial = splits > 1;
+    aa.partial = splits > 1 || split_out;
     aa.part_o = static_cast<float*>(m->part_o.p);
     aa.part_ml = static_cast<float2*>(m->part_ml.p);
     aa.causal_heavy_first = 1;
     PCD_LAUNCH(timed(m, PROF_ATTN_PREFILL, [&] { return pcd::launch_attention(aa, m->stream); }));
-    if (splits > 1) {
+    if (aa.partial) {
       pcd::MergeArgs ma{};
       ma.q = q;
       ma.n_tok = n;
@@ -395,14 +415,17 @@ int record_prefill(pcd_model* m, const int32_t* d_ids, int n, pcd_cache* c, int 
       ma.scale_log2 = aa.scale_log2;
       ma.out = att;
       ma.ld_out = m->qdim;
+      ma.out_lo = att_lo;
       PCD_LAUNCH(timed(m, PROF_ATTN_PREFILL, [&] { return pcd::launch_branch_merge(ma, m->stream); }));
     }
-    PCD_TRY(gemm(m, PROF_GEMM_PREFILL, att, n, m->qdim, W.wo, m->d, m->qdim, m->qdim, pcd::EPI_F32_ADD, x, m->d));
+    PCD_TRY(gemm(m, PROF_GEMM_PREFILL, att, n, m->qdim, W.wo, m->d, m->qdim, m->qdim, pcd::EPI_F32_ADD, x, m->d,
+                 att_lo));
     PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
-      return pcd::launch_rmsnorm(x, m->d, nullptr, n, m->d, W.mlp_norm, m->cfg.rms_eps, xn, m->d, m->stream);
+      return pcd::launch_rmsnorm(x, m->d, nullptr, n, m->d, W.mlp_norm, m->cfg.rms_eps, xn, m->d, m->stream, xlo);
     }));
-    PCD_TRY(gemm(m, PROF_GEMM_PREFILL, xn, n, m->d, W.wgu, 2 * m->Fp, m->d, m->d, pcd::EPI_SWIGLU, hb, m->Fp));
-    PCD_TRY(gemm(m, PROF_GEMM_PREFILL, hb, n, m->Fp, W.wd, m->d, m->Fp, m->Fp, pcd::EPI_F32_ADD, x, m->d));
+    PCD_TRY(gemm(m, PROF_GEMM_PREFILL, xn, n, m->d, W.wgu, 2 * m->Fp, m->d, m->d, pcd::EPI_SWIGLU, hb, m->Fp, xlo,
+                 hb_lo));
+    PCD_TRY(gemm(m, PROF_GEMM_PREFILL, hb, n, m->Fp, W.wd, m->d, m->Fp, m->Fp, pcd::EPI_F32_ADD, x, m->d, hb_lo));
   }
   return PCD_OK;
 }
@@ -422,6 +445,7 @@ int run_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_seg, 
   PCD_TRY(ensure_workspace(m, T));
   PCD_TRY(ensure(m->kb, static_cast<size_t>(m->Hkv) * T * m->dh * 2));
   PCD_TRY(ensure(m->vb, static_cast<size_t>(m->Hkv) * T * m->dh * 2));
+  PCD_TRY(ensure(m->xn_lo, static_cast<size_t>(T) * m->d * 2));
   int max_lp = 0;
   for (int s = 0; s < n_seg; ++s) max_lp = std::max(max_lp, segs[s].c->len);
   // key splits of the prefix attention: enough CTAs to cover the SMs twice
@@ -430,6 +454,7 @@ int run_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_seg, 
   PCD_TRY(ensure(m->part_o, static_cast<size_t>(splits) * m->Hkv * T * G * m->dh * 4));
   PCD_TRY(ensure(m->part_ml, static_cast<size_t>(splits) * m->Hkv * T * G * 8));
   PCD_TRY(ensure(m->hr, static_cast<size_t>(std::max(R, 1)) * m->d * 2));
+  PCD_TRY(ensure(m->hr_lo, static_cast<size_t>(std::max(R, 1)) * m->d * 2));
   PCD_TRY(ensure(m->ro_part, static_cast<size_t>(p.n_vtiles) * std::max(R, 1) * 8));
   PCD_TRY(ensure(m->z, static_cast<size_t>(std::max(p.n_children, 1)) * 4));
   PCD_TRY(ensure(m->lse, static_cast<size_t>(std::max(R, 1)) * 4));
@@ -456,6 +481,13 @@ int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_se
   act_t* q = static_cast<act_t*>(m->q.p);
   act_t* att = static_cast<act_t*>(m->att.p);
   act_t* hb = static_cast<act_t*>(m->hb.p);
+  // the branch rows carry their normalised activations as fp16 hi + lo into
+  // the QKV and gate/up projections: the readout is most sensitive to them
+  act_t* xlo = (m->split_act & 1) ? static_cast<act_t*>(m->xn_lo.p) : nullptr;
+  const bool split_out = (m->split_act & 4) != 0;
+  act_t* att_lo = split_out ? static_cast<act_t*>(m->att_lo.p) : nullptr;
+  act_t* hb_lo = split_out ? static_cast<act_t*>(m->hb_lo.p) : nullptr;
+  act_t* hr_lo = (m->split_act & 16) ? static_cast<act_t*>(m->hr_lo.p) : nullptr;
   act_t* kb = static_cast<act_t*>(m->kb.p);
   act_t* vb = static_cast<act_t*>(m->vb.p);
   float* part_o = static_cast<float*>(m->part_o.p);
@@ -466,9 +498,9 @@ int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_se
   for (int l = 0; l < m->L; ++l) {
     const Layer& W = m->layers[l];
     PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
-      return pcd::launch_rmsnorm(x, m->d, nullptr, T, m->d, W.attn_norm, m->cfg.rms_eps, xn, m->d, m->stream);
+      return pcd::launch_rmsnorm(x, m->d, nullptr, T, m->d, W.attn_norm, m->cfg.rms_eps, xn, m->d, m->stream, xlo);
     }));
-    PCD_TRY(gemm(m, PROF_GEMM_BRANCH, xn, T, m->d, W.wqkv, m->Nqkv, m->d, m->d, pcd::EPI_F32_STORE, qkv, m->Nqkv));
+    PCD_TRY(gemm(m, PROF_GEMM_BRANCH, xn, T, m->d, W.wqkv, m->Nqkv, m->d, m->d, pcd::EPI_F32_STORE, qkv, m->Nqkv, xlo));
     for (int s = 0; s < n_seg; ++s) {
       const Segment& sg = segs[s];
       const int n = sg.t1 - sg.t0;
@@ -536,29 +568,37 @@ int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_se
     ma.scale_log2 = scale_log2;
     ma.out = att;
     ma.ld_out = m->qdim;
+    ma.out_lo = att_lo;
     PCD_LAUNCH(timed(m, PROF_ATTN_BRANCH, [&] { return pcd::launch_branch_merge(ma, m->stream); }));
-    PCD_TRY(gemm(m, PROF_GEMM_BRANCH, att, T, m->qdim, W.wo, m->d, m->qdim, m->qdim, pcd::EPI_F32_ADD, x, m->d));
+    PCD_TRY(gemm(m, PROF_GEMM_BRANCH, att, T, m->qdim, W.wo, m->d, m->qdim, m->qdim, pcd::EPI_F32_ADD, x, m->d,
+                 att_lo));
     PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
-      return pcd::launch_rmsnorm(x, m->d, nullptr, T, m->d, W.mlp_norm, m->cfg.rms_eps, xn, m->d, m->stream);
+      return pcd::launch_rmsnorm(x, m->d, nullptr, T, m->d, W.mlp_norm, m->cfg.rms_eps, xn, m->d, m->stream, xlo);
     }));
-    PCD_TRY(gemm(m, PROF_GEMM_BRANCH, xn, T, m->d, W.wgu, 2 * m->Fp, m->d, m->d, pcd::EPI_SWIGLU, hb, m->Fp));
-    PCD_TRY(gemm(m, PROF_GEMM_BRANCH, hb, T, m->Fp, W.wd, m->d, m->Fp, m->Fp, pcd::EPI_F32_ADD, x, m->d));
+    PCD_TRY(gemm(m, PROF_GEMM_BRANCH, xn, T, m->d, W.wgu, 2 * m->Fp, m->d, m->d, pcd::EPI_SWIGLU, hb, m->Fp, xlo,
+                 hb_lo));
+    PCD_TRY(gemm(m, PROF_GEMM_BRANCH, hb, T, m->Fp, W.wd, m->d, m->Fp, m->Fp, pcd::EPI_F32_ADD, x, m->d, hb_lo));
   }
   if (ev_mid) cudaEventRecord(ev_mid, m->stream);
 
   // final norm on the readout rows only, then the fused vocabulary readout
   act_t* hr = static_cast<act_t*>(m->hr.p);
   PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
-    return pcd::launch_rmsnorm(x, m->d, p.ro_tok, R, m->d, m->final_norm, m->cfg.rms_eps, hr, m->d, m->stream);
+    return pcd::launch_rmsnorm(x, m->d, p.ro_tok, R, m->d, m->final_norm, m->cfg.rms_eps, hr, m->d, m->stream, hr_lo);
   }));
-  pcd::GemmShape rs{hr, R, m->d, m->lm, m->V, m->d, m->d};
+  pcd::GemmShape rs{hr, R, m->d, m->lm, m->V, m->d, m->d, hr_lo};
+  pcd::GemmTiling ro_t = p.ro_tiling;
+  if (hr_lo) {
+    ro_t.mt = 1;
+    ro_t.cs = 1;
+  }
   pcd::EpiArgs re;
   re.part = static_cast<float2*>(m->ro_part.p);
   re.gather_off = p.gather_off;
   re.gather = p.gather;
   re.z_out = static_cast<float*>(m->z.p);
   PCD_LAUNCH(timed(m, PROF_READOUT, [&] {
-    return pcd::launch_gemm(rs, pcd::EPI_READOUT, re, p.ro_tiling, m->stream, m->d_err, m->wait_ns, m->sms);
+    return pcd::launch_gemm(rs, pcd::EPI_READOUT, re, ro_t, m->stream, m->d_err, m->wait_ns, m->sms);
   }));
   PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
     return pcd::launch_lse_combine(static_cast<float2*>(m->ro_part.p), p.n_vtiles, R, static_cast<float*>(m->lse.p),
@@ -739,6 +779,7 @@ int build_model(const pcd_model_config& cfg, TensorFn get, void* ctx, int dtype,
     m->own_stream = true;
   }
   if (const char* g = std::getenv("PCD_GRAPHS")) m->graphs = std::atoi(g) != 0;
+  if (const char* g = std::getenv("PCD_SPLIT_ACT")) m->split_act = std::atoi(g);
   m->sms = prop.multiProcessorCount;
   if (const char* w = std::getenv("PCD_WAIT_LIMIT_MS")) m->wait_ns = static_cast<uint64_t>(std::atof(w) * 1e6);
 
@@ -1112,7 +1153,8 @@ void pcd_model_free(pcd_model* m) {
   if (m->stream) cudaStreamSynchronize(m->stream);
   cudaDeviceSynchronize();
   for (DevBuf* b : {&m->x32, &m->xn, &m->qkv, &m->q, &m->kb, &m->vb, &m->att, &m->hb, &m->part_o, &m->part_ml, &m->hr,
-                    &m->ro_part, &m->z, &m->lse, &m->plan_buf, &m->result, &m->ids})
+                    &m->ro_part, &m->z, &m->lse, &m->plan_buf, &m->result, &m->ids, &m->xn_lo, &m->att_lo, &m->hb_lo,
+                    &m->hr_lo})
     if (b->p) cudaFree(b->p);
   for (auto& e : m->cache_pool) cudaFree(e.second);
   if (m->wblob) cudaFree(m->wblob);

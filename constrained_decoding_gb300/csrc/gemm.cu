@@ -37,11 +37,12 @@ struct GemmParams {
   int b_evict_first;  // B is read by one M group only: stream it past L2
 };
 
-template <int MT, int BN>
+template <int MT, int BN, bool ALO = false>
 struct GemmCfg {
   static constexpr int A_BYTES = 128 * 128;  // 128 rows x 64 fp16
   static constexpr int B_BYTES = BN * 128;
-  static constexpr int STAGE_BYTES = MT * A_BYTES + B_BYTES;
+  static constexpr int A_PARTS = ALO ? 2 : 1;  // A as hi + lo fp16 halves
+  static constexpr int STAGE_BYTES = A_PARTS * MT * A_BYTES + B_BYTES;
   static constexpr int SMEM_BUDGET = 227 * 1024 - 2048;
   static constexpr int STAGES_RAW = SMEM_BUDGET / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
@@ -129,16 +130,28 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, const EpiArgs& e,
         w.z = pack2(h[4], h[5]);
         w.w = pack2(h[6], h[7]);
         o4[j] = w;
+        if (e.out_lo) {
+          const __half* hh = reinterpret_cast<const __half*>(&w);
+          uint4 lo;
+          lo.x = pack2(h[0] - __half2float(hh[0]), h[1] - __half2float(hh[1]));
+          lo.y = pack2(h[2] - __half2float(hh[2]), h[3] - __half2float(hh[3]));
+          lo.z = pack2(h[4] - __half2float(hh[4]), h[5] - __half2float(hh[5]));
+          lo.w = pack2(h[6] - __half2float(hh[6]), h[7] - __half2float(hh[7]));
+          reinterpret_cast<uint4*>(reinterpret_cast<act_t*>(e.out_lo) + static_cast<size_t>(row) * e.ldo + col0 / 2)[j] = lo;
+        }
       }
     }
   }
 }
 
-template <int MT, int BN, int EPI, int CS>
+// ALO: A is given as two fp16 matrices, hi and lo (hi + lo carries ~22 bits of
+// the activation); both are multiplied by the same B tile into one
+// accumulator, so the weights are read once.
+template <int MT, int BN, int EPI, int CS, bool ALO>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmParams p, const EpiArgs e) {
-  using C = GemmCfg<MT, BN>;
+                   const __grid_constant__ CUtensorMap tmA2, const GemmParams p, const EpiArgs e) {
+  using C = GemmCfg<MT, BN, ALO>;
   static_assert(CS == 1 || MT == 1, "clusters share B across single-tile CTAs");
   constexpr uint16_t MASK = static_cast<uint16_t>((1u << CS) - 1u);
   constexpr int B_SLICE = BN / CS;  // B rows each CTA of a cluster loads and multicasts
@@ -178,6 +191,7 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if constexpr (ALO) tma_prefetch_desc(&tmA2);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::TMEM_COLS);
@@ -209,7 +223,7 @@ __global__ void __launch_bounds__(192, 1)
         decode_unit(p, u, nt, mg, ks);
         const int kb0 = ks * p.nkb / p.k_splits, kb1 = (ks + 1) * p.nkb / p.k_splits;
         const int mt_valid = valid_tiles(mg);
-        const uint32_t bytes = mt_valid * C::A_BYTES + C::B_BYTES;
+        const uint32_t bytes = C::A_PARTS * mt_valid * C::A_BYTES + C::B_BYTES;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns)) {
             record_error(p.err, DEV_WAIT_TIMEOUT_PRODUCER);
@@ -218,13 +232,17 @@ __global__ void __launch_bounds__(192, 1)
           }
           mbar_arrive_expect_tx(&full[stage], bytes);
           uint8_t* base = smem + stage * C::STAGE_BYTES;
-          for (int mt = 0; mt < mt_valid; ++mt)
+          for (int mt = 0; mt < mt_valid; ++mt) {
             tma_load_2d(base + mt * C::A_BYTES, &tmA, &full[stage], kb * 64, (tile0(mg) + mt) * 128);
+            if constexpr (ALO)
+              tma_load_2d(base + (MT + mt) * C::A_BYTES, &tmA2, &full[stage], kb * 64, (tile0(mg) + mt) * 128);
+          }
+          uint8_t* bdst = base + C::A_PARTS * MT * C::A_BYTES;
           if constexpr (CS == 1) {
-            tma_load_2d_hint(base + MT * C::A_BYTES, &tmB, &full[stage], kb * 64, nt * BN, pol_b);
+            tma_load_2d_hint(bdst, &tmB, &full[stage], kb * 64, nt * BN, pol_b);
           } else {
-            tma_load_2d_mc(base + MT * C::A_BYTES + rank * B_SLICE * 128, &tmB, &full[stage], kb * 64,
-                           nt * BN + rank * B_SLICE, MASK, pol_b);
+            tma_load_2d_mc(bdst + rank * B_SLICE * 128, &tmB, &full[stage], kb * 64, nt * BN + rank * B_SLICE, MASK,
+                           pol_b);
           }
           issued[stage] = true;
           last_phase[stage] = phase;
@@ -274,12 +292,18 @@ __global__ void __launch_bounds__(192, 1)
           }
           tc_fence_after_sync();
           const uint32_t a_base = smem_u32(smem + stage * C::STAGE_BYTES);
-          const uint32_t b_base = a_base + MT * C::A_BYTES;
+          const uint32_t b_base = a_base + C::A_PARTS * MT * C::A_BYTES;
           for (int mt = 0; mt < mt_valid; ++mt) {
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
               umma_f16(d_base + mt * BN, sdesc_kmajor_sw128(a_base + mt * C::A_BYTES + k * 32),
                        sdesc_kmajor_sw128(b_base + k * 32), IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
+            }
+            if constexpr (ALO) {
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                umma_f16(d_base + mt * BN, sdesc_kmajor_sw128(a_base + (MT + mt) * C::A_BYTES + k * 32),
+                         sdesc_kmajor_sw128(b_base + k * 32), IDESC, 1u);
             }
           }
           if constexpr (CS == 1) {
@@ -432,11 +456,11 @@ static bool encode_map(CUtensorMap* m, const void* ptr, int rows, int cols, int 
   return r == CUDA_SUCCESS;
 }
 
-template <int MT, int BN, int EPI, int CS>
-static int launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p, const EpiArgs& e,
-                    cudaStream_t st, int sms) {
-  using C = GemmCfg<MT, BN>;
-  auto kern = gemm_tc_kernel<MT, BN, EPI, CS>;
+template <int MT, int BN, int EPI, int CS, bool ALO = false>
+static int launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ma2, const GemmParams& p,
+                    const EpiArgs& e, cudaStream_t st, int sms) {
+  using C = GemmCfg<MT, BN, ALO>;
+  auto kern = gemm_tc_kernel<MT, BN, EPI, CS, ALO>;
   static bool attr_set = false;  // per instantiation
   static int max_clusters = 0;
   if (!attr_set) {
@@ -464,7 +488,7 @@ static int launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const GemmPara
   }
   if (CS == 1) {
     const int grid = std::min(p.n_units, sms);
-    kern<<<grid, 192, C::SMEM_BYTES, st>>>(ma, mb, p, e);
+    kern<<<grid, 192, C::SMEM_BYTES, st>>>(ma, mb, ma2, p, e);
     return cudaGetLastError();
   }
   const int clusters = std::min(p.n_units, max_clusters);
@@ -480,23 +504,31 @@ static int launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const GemmPara
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, ma, mb, p, e);
+  return cudaLaunchKernelEx(&cfg, kern, ma, mb, ma2, p, e);
 }
 
 template <int EPI>
-static int dispatch_tiling(const GemmTiling& t, const CUtensorMap& ma, const CUtensorMap& mb, const GemmParams& p,
-                           const EpiArgs& e, cudaStream_t st, int sms) {
+static int dispatch_tiling(const GemmTiling& t, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap* ma2,
+                           const GemmParams& p, const EpiArgs& e, cudaStream_t st, int sms) {
+  if (ma2) {  // hi + lo A: one 128-row tile per CTA, no cluster
+    if constexpr (EPI == EPI_F32_STORE || EPI == EPI_F32_ADD || EPI == EPI_F32_ATOMIC || EPI == EPI_SWIGLU ||
+                  EPI == EPI_READOUT) {
+      if (t.mt == 1 && t.cs == 1 && t.bn == 128) return launch_t<1, 128, EPI, 1, true>(ma, mb, *ma2, p, e, st, sms);
+      if (t.mt == 1 && t.cs == 1 && t.bn == 256) return launch_t<1, 256, EPI, 1, true>(ma, mb, *ma2, p, e, st, sms);
+    }
+    return -1;
+  }
   if (t.cs == 1) {
-    if (t.mt == 1 && t.bn == 128) return launch_t<1, 128, EPI, 1>(ma, mb, p, e, st, sms);
-    if (t.mt == 1 && t.bn == 256) return launch_t<1, 256, EPI, 1>(ma, mb, p, e, st, sms);
-    if (t.mt == 2 && t.bn == 128) return launch_t<2, 128, EPI, 1>(ma, mb, p, e, st, sms);
-    if (t.mt == 2 && t.bn == 256) return launch_t<2, 256, EPI, 1>(ma, mb, p, e, st, sms);
-    if (t.mt == 4 && t.bn == 128) return launch_t<4, 128, EPI, 1>(ma, mb, p, e, st, sms);
+    if (t.mt == 1 && t.bn == 128) return launch_t<1, 128, EPI, 1>(ma, mb, ma, p, e, st, sms);
+    if (t.mt == 1 && t.bn == 256) return launch_t<1, 256, EPI, 1>(ma, mb, ma, p, e, st, sms);
+    if (t.mt == 2 && t.bn == 128) return launch_t<2, 128, EPI, 1>(ma, mb, ma, p, e, st, sms);
+    if (t.mt == 2 && t.bn == 256) return launch_t<2, 256, EPI, 1>(ma, mb, ma, p, e, st, sms);
+    if (t.mt == 4 && t.bn == 128) return launch_t<4, 128, EPI, 1>(ma, mb, ma, p, e, st, sms);
   } else if (t.mt == 1) {
-    if (t.cs == 2 && t.bn == 128) return launch_t<1, 128, EPI, 2>(ma, mb, p, e, st, sms);
-    if (t.cs == 2 && t.bn == 256) return launch_t<1, 256, EPI, 2>(ma, mb, p, e, st, sms);
-    if (t.cs == 4 && t.bn == 128) return launch_t<1, 128, EPI, 4>(ma, mb, p, e, st, sms);
-    if (t.cs == 4 && t.bn == 256) return launch_t<1, 256, EPI, 4>(ma, mb, p, e, st, sms);
+    if (t.cs == 2 && t.bn == 128) return launch_t<1, 128, EPI, 2>(ma, mb, ma, p, e, st, sms);
+    if (t.cs == 2 && t.bn == 256) return launch_t<1, 256, EPI, 2>(ma, mb, ma, p, e, st, sms);
+    if (t.cs == 4 && t.bn == 128) return launch_t<1, 128, EPI, 4>(ma, mb, ma, p, e, st, sms);
+    if (t.cs == 4 && t.bn == 256) return launch_t<1, 256, EPI, 4>(ma, mb, ma, p, e, st, sms);
   }
   return -1;
 }
@@ -521,16 +553,18 @@ int launch_gemm(const GemmShape& s, int epi, const EpiArgs& e, const GemmTiling&
   p.wait_ns = wait_ns;
   p.err = dev_err;
   p.b_evict_first = (p.n_mgroups == 1 && t.mt * t.cs * 128 >= M) ? 1 : 0;
-  CUtensorMap ma, mb;
+  CUtensorMap ma, mb, ma2;
   if (!make_map(&ma, s.a, M, K, s.a_ld, 128)) return -1;
+  if (s.a_lo && !make_map(&ma2, s.a_lo, M, K, s.a_ld, 128)) return -1;
+  const CUtensorMap* pa2 = s.a_lo ? &ma2 : nullptr;
   if (!make_map(&mb, s.b, N, K, s.b_ld, t.bn / t.cs)) return -1;
   switch (epi) {
-    case EPI_BF16: return dispatch_tiling<EPI_BF16>(t, ma, mb, p, e, stream, sms);
-    case EPI_F32_ADD: return dispatch_tiling<EPI_F32_ADD>(t, ma, mb, p, e, stream, sms);
-    case EPI_F32_ATOMIC: return dispatch_tiling<EPI_F32_ATOMIC>(t, ma, mb, p, e, stream, sms);
-    case EPI_SWIGLU: return dispatch_tiling<EPI_SWIGLU>(t, ma, mb, p, e, stream, sms);
-    case EPI_READOUT: return dispatch_tiling<EPI_READOUT>(t, ma, mb, p, e, stream, sms);
-    case EPI_F32_STORE: return dispatch_tiling<EPI_F32_STORE>(t, ma, mb, p, e, stream, sms);
+    case EPI_BF16: return dispatch_tiling<EPI_BF16>(t, ma, mb, pa2, p, e, stream, sms);
+    case EPI_F32_ADD: return dispatch_tiling<EPI_F32_ADD>(t, ma, mb, pa2, p, e, stream, sms);
+    case EPI_F32_ATOMIC: return dispatch_tiling<EPI_F32_ATOMIC>(t, ma, mb, pa2, p, e, stream, sms);
+    case EPI_SWIGLU: return dispatch_tiling<EPI_SWIGLU>(t, ma, mb, pa2, p, e, stream, sms);
+    case EPI_READOUT: return dispatch_tiling<EPI_READOUT>(t, ma, mb, pa2, p, e, stream, sms);
+    case EPI_F32_STORE: return dispatch_tiling<EPI_F32_STORE>(t, ma, mb, pa2, p, e, stream, sms);
   }
   return -1;
 }

@@ -20,11 +20,13 @@ struct GemmShape {
   const void* a; int a_rows; int a_ld;   // A: a_rows x K, leading dim in elements
   const void* b; int b_rows; int b_ld;   // B: b_rows x K
   int K;
+  const void* a_lo = nullptr;            // optional low half of A (same layout): D = (A + A_lo) . B^T
 };
 
 struct EpiArgs {
-  void* out = nullptr;            // output base (bf16 or f32)
+  void* out = nullptr;            // output base (16-bit or f32)
   int ldo = 0;                    // leading dimension of out, in elements
+  void* out_lo = nullptr;         // EPI_SWIGLU: optional fp16 rounding remainder of out (same layout)
   float2* part = nullptr;         // EPI_READOUT: [n_tiles_n][M] (max, sum exp(z - max))
   const int* gather_off = nullptr;  // EPI_READOUT: [n_tiles_n + 1] CSR over gather entries
   const int4* gather = nullptr;   // EPI_READOUT: (column in tile, row, output index, 0)

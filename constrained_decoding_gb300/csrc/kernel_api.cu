@@ -51,6 +51,23 @@ extern "C" int pcd_k_gemm(const void* a, int M, int lda, const void* b, int N, i
   return r == 0 ? 0 : (r < 0 ? -1 : -10);
 }
 
+extern "C" int pcd_k_gemm_split(const void* a_hi, const void* a_lo, int M, int lda, const void* b, int N, int ldb,
+                                int K, int epi, void* out, int ldo, int bn, int splits, int* dev_err, void* stream) {
+  if (!a_hi || !a_lo || !b || !out || M < 0 || N <= 0 || K <= 0) return -1;
+  if (epi != PCD_EPI_F32_ADD && epi != PCD_EPI_F32_ATOMIC && epi != PCD_EPI_SWIGLU) return -1;
+  pcd::GemmTiling t;
+  t.mt = 1;
+  t.bn = bn;
+  t.splits = splits < 1 ? 1 : splits;
+  t.cs = 1;
+  pcd::GemmShape s{a_hi, M, lda, b, N, ldb, K, a_lo};
+  pcd::EpiArgs e;
+  e.out = out;
+  e.ldo = ldo;
+  const int r = pcd::launch_gemm(s, epi, e, t, static_cast<cudaStream_t>(stream), dev_err, 2000000000ull, device_sms());
+  return r == 0 ? 0 : (r < 0 ? -1 : -10);
+}
+
 namespace {
 // Scratch layout of the readout: partials [n_tiles][R] float2, then the gather
 // CSR [n_tiles + 1] int32, then the gather entries [n_cand] int4.  Sized for

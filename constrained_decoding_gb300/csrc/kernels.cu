@@ -46,7 +46,8 @@ constexpr int kNormMaxVec = 8;  // float4 per thread: d <= 8192
 __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float* __restrict__ x, int ldx,
                                                                const int32_t* __restrict__ rows, int n, int d,
                                                                const float* __restrict__ gain, float eps,
-                                                               act_t* __restrict__ out, int ldo) {
+                                                               act_t* __restrict__ out, int ldo,
+                                                               act_t* __restrict__ out_lo) {
   const int r = blockIdx.x;
   const int src = rows ? rows[r] : r;
   const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(src) * ldx);
@@ -72,24 +73,34 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float* __re
   const float inv = rsqrtf(tot / static_cast<float>(d) + eps);
   const float4* g4 = reinterpret_cast<const float4*>(gain);
   uint2* o2 = reinterpret_cast<uint2*>(out + static_cast<size_t>(r) * ldo);
+  uint2* l2 = out_lo ? reinterpret_cast<uint2*>(out_lo + static_cast<size_t>(r) * ldo) : nullptr;
 #pragma unroll
   for (int j = 0; j < kNormMaxVec; ++j) {
     const int i = threadIdx.x + j * kNormThreads;
     if (i < nv) {
       const float4 g = g4[i];
+      const float y0 = v[j].x * inv * g.x, y1 = v[j].y * inv * g.y, y2 = v[j].z * inv * g.z, y3 = v[j].w * inv * g.w;
       uint2 w;
-      w.x = pack2(v[j].x * inv * g.x, v[j].y * inv * g.y);
-      w.y = pack2(v[j].z * inv * g.z, v[j].w * inv * g.w);
+      w.x = pack2(y0, y1);
+      w.y = pack2(y2, y3);
       o2[i] = w;
+      if (l2) {  // the rounding remainder, so hi + lo carries the fp32 value
+        const __half2* h = reinterpret_cast<const __half2*>(&w);
+        const float2 a = __half22float2(h[0]), b = __half22float2(h[1]);
+        uint2 lo;
+        lo.x = pack2(y0 - a.x, y1 - a.y);
+        lo.y = pack2(y2 - b.x, y3 - b.y);
+        l2[i] = lo;
+      }
     }
   }
 }
 
 int launch_rmsnorm(const float* x, int ldx, const int32_t* rows, int n, int d, const float* gain, float eps, act_t* out,
-                   int ldo, cudaStream_t s) {
+                   int ldo, cudaStream_t s, act_t* out_lo) {
   if (n <= 0) return 0;
   if (d % 4 || d > 4 * kNormThreads * kNormMaxVec) return -1;
-  rmsnorm_kernel<<<n, kNormThreads, 0, s>>>(x, ldx, rows, n, d, gain, eps, out, ldo);
+  rmsnorm_kernel<<<n, kNormThreads, 0, s>>>(x, ldx, rows, n, d, gain, eps, out, ldo, out_lo);
   return cudaGetLastError();
 }
 
@@ -510,10 +521,16 @@ __global__ void __launch_bounds__(256) branch_merge_kernel(MergeArgs a) {
   }
   const float il = l > 0.f ? 1.f / l : 0.f;
   act_t* dst = a.out + static_cast<size_t>(t) * a.ld_out + h * DH;
+  act_t* dlo = a.out_lo ? a.out_lo + static_cast<size_t>(t) * a.ld_out + h * DH : nullptr;
 #pragma unroll
   for (int i = 0; i < EPT; ++i) {
     const int d = lane + 32 * i;
-    if (d < DH) dst[d] = f2a(acc[i] * il);
+    if (d < DH) {
+      const float y = acc[i] * il;
+      const act_t hv = f2a(y);
+      dst[d] = hv;
+      if (dlo) dlo[d] = f2a(y - a2f(hv));
+    }
   }
 }
 

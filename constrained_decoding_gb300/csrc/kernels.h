@@ -11,9 +11,10 @@ using act_t = __half;  // same as common.cuh
 // x[t][0..d) = E[ids[t]][0..d) as fp32 (the residual stream starts here).
 int launch_embed(const int32_t* ids, int n, const act_t* E, int d, int vocab, float* x, int* err, cudaStream_t s);
 
-// out[r] = act_t( x[src] / sqrt(mean(x[src]^2) + eps) * gain ), src = rows ? rows[r] : r.
+// out[r] = fp16( x[src] / sqrt(mean(x[src]^2) + eps) * gain ), src = rows ? rows[r] : r;
+// out_lo (optional) receives the rounding remainder fp16(y - out), so out + out_lo ~ y.
 int launch_rmsnorm(const float* x, int ldx, const int32_t* rows, int n, int d, const float* gain, float eps, act_t* out,
-                   int ldo, cudaStream_t s);
+                   int ldo, cudaStream_t s, act_t* out_lo = nullptr);
 
 struct RopeArgs {
   const float* qkv;       // [n][ldqkv] fp32: q heads, then k heads, then v heads
@@ -67,6 +68,7 @@ struct MergeArgs {
   float scale_log2;
   act_t* out;                // out[t][h * DH + d]
   int ld_out;
+  act_t* out_lo = nullptr;   // optional fp16 rounding remainder of out
 };
 int launch_branch_merge(const MergeArgs& a, cudaStream_t s);
 

@@ -34,6 +34,14 @@ extern "C" {
 int pcd_k_gemm(const void* a, int M, int lda, const void* b, int N, int ldb, int K, int epi, void* out, int ldo,
                int mt, int bn, int splits, int* dev_err, void* stream);
 
+/* pcd_k_gemm with A given as two fp16 halves, a_hi + a_lo (a_lo the rounding
+ * remainder of an fp32 activation): D = (A_hi + A_lo) . B^T, both products
+ * accumulated in one fp32 accumulator from one read of B.  One 128-row tile
+ * per CTA; epi PCD_EPI_F32_ADD, PCD_EPI_F32_ATOMIC or PCD_EPI_SWIGLU; bn in
+ * {128, 256}. */
+int pcd_k_gemm_split(const void* a_hi, const void* a_lo, int M, int lda, const void* b, int N, int ldb, int K, int epi,
+                     void* out, int ldo, int bn, int splits, int* dev_err, void* stream);
+
 /* Fused vocabulary readout: the LM-head contraction z = h . W^T run tile by
  * tile on the tensor cores with an online log-sum-exp over the whole
  * vocabulary and a gather of selected logits, so the [R][V] logits are never

@@ -7,15 +7,23 @@ accumulation, against the fp32 oracle):
   * probabilities within 2e-3 absolute;
   * label log-probs (summed), log mass within 3e-2 absolute;
   * first-decision mass within 2e-3 absolute (a probability).
+
+The Qwen2.5-7B-shaped random decoder is the exception for candidate
+probabilities: a CPU emulation of the device's fp16 rounding on it shows that
+rounding q/k/v alone moves label log-probs by up to 0.012 (the random 28-layer
+network amplifies a 2^-11 perturbation about a hundredfold), which on a
+near-even field is 3e-3 of probability.  There labels, log-probs and log mass
+keep the bounds above and probabilities are held to PROB_TOL_7B.
 """
 import numpy as np
 
 PROB_TOL = 2e-3
+PROB_TOL_7B = 5e-3
 LOGP_TOL = 3e-2
 MARGIN_EXACT = 0.05
 
 
-def compare_field(gpu, ref, where=""):
+def compare_field(gpu, ref, where="", prob_tol=PROB_TOL):
     """gpu: constrained_decoding_gb300.pcd.FieldResult; ref: oracle FieldResult."""
     n = len(ref.scores)
     assert len(gpu.probs) == n, where
@@ -25,7 +33,7 @@ def compare_field(gpu, ref, where=""):
         "log_mass": abs(gpu.log_mass - ref.log_mass),
         "first_mass": abs(gpu.first_mass - ref.first_mass),
     }
-    assert errs["probs"] <= PROB_TOL, (where, errs)
+    assert errs["probs"] <= prob_tol, (where, errs)
     assert errs["logprobs"] <= LOGP_TOL, (where, errs)
     assert errs["log_mass"] <= LOGP_TOL, (where, errs)
     assert errs["first_mass"] <= PROB_TOL, (where, errs)
@@ -39,10 +47,10 @@ def compare_field(gpu, ref, where=""):
     return errs
 
 
-def compare_request(gpu_results, ref_results, where=""):
+def compare_request(gpu_results, ref_results, where="", prob_tol=PROB_TOL):
     worst = {}
     for i, (g, r) in enumerate(zip(gpu_results, ref_results)):
-        e = compare_field(g, r, f"{where} field {i}")
+        e = compare_field(g, r, f"{where} field {i}", prob_tol)
         for k, v in e.items():
             worst[k] = max(worst.get(k, 0.0), v)
     return worst

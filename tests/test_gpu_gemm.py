@@ -98,3 +98,40 @@ def test_gemm_cluster_multicast_f32(cs, splits):
 def test_gemm_cluster_swiglu():
     out, ref, tol = _run(313, 1024, 256, 3, 41, 256, 1, seed=6)
     assert (out - ref).abs().max().item() < tol
+
+
+@pytest.mark.parametrize("epi,bn,splits", [(1, 128, 1), (2, 256, 4), (3, 256, 1), (3, 128, 1)])
+def test_gemm_split_activation(epi, bn, splits):
+    """A carried as fp16 hi + lo: the product matches the fp32 activation's
+    product far more closely than the hi half alone."""
+    lib = _lib()
+    M, N, K = 313, 1024, 1536
+    g = torch.Generator().manual_seed(7)
+    a32 = torch.randn(M, K, generator=g)
+    hi = a32.half()
+    lo = (a32 - hi.float()).half()
+    b = (torch.randn(N, K, generator=g) * 0.05).half()
+    ref = a32.double() @ b.double().T
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    if epi == 3:
+        out = torch.zeros(M, N // 2, dtype=torch.float16, device="cuda")
+        ref = (torch.nn.functional.silu(ref[:, 0::2]) * ref[:, 1::2])
+    else:
+        out = torch.zeros(M, N, dtype=torch.float32, device="cuda")
+    hi_d, lo_d, b_d = hi.cuda(), lo.cuda(), b.cuda()   # keep the device copies alive for the call
+    rc = lib.pcd_k_gemm_split(hi_d.data_ptr(), lo_d.data_ptr(), M, K, b_d.data_ptr(), N, K, K, epi,
+                              out.data_ptr(), out.shape[1], bn, splits, err.data_ptr(), s)
+    assert rc == 0
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got = out.double().cpu()
+    hi_only = hi.double() @ b.double().T
+    if epi == 3:
+        hi_only = torch.nn.functional.silu(hi_only[:, 0::2]) * hi_only[:, 1::2]
+        # fp16 output rounding dominates: within one fp16 ulp of the exact value
+        assert ((got - ref).abs() <= ref.abs() * 2.0 ** -10 + 1e-3).all()
+    else:
+        e_split = (got - ref).abs().max().item()
+        e_hi = (hi_only - ref).abs().max().item()
+        assert e_split < 2e-4 and e_split < e_hi / 4, (e_split, e_hi)

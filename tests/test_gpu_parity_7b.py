@@ -1,0 +1,63 @@
+"""Batched serving at the Qwen2.5-7B shape (untied LM head, GQA group 7):
+64 requests with prefixes of 512-4096 tokens and the 28-field schema, scored
+in one branch pass, cold and warm (a cached 512-token schema head extended by
+each request's tail).  The oracle checks the two shortest requests, cold and
+warm; the candidate-probability bound is PROB_TOL_7B (see tests/parity.py)."""
+import time
+
+import numpy as np
+import pytest
+
+import synth
+from parity import compare_request, PROB_TOL, LOGP_TOL, PROB_TOL_7B
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def big():
+    import constrained_decoding_gb300.pcd as pcd
+    cfg = synth.model_config("7b")
+    t = time.time()
+    w = synth.make_weights(cfg, seed=0)
+    print(f"7B weights drawn in {time.time() - t:.1f} s")
+    t = time.time()
+    model = pcd.pcd_load_weights_host(w)
+    print(f"7B weights loaded in {time.time() - t:.1f} s")
+    yield pcd, model, w
+    model.free()
+
+
+def test_config5_cold_parity_and_warm_equals_cold(big):
+    pcd, model, w = big
+    reqs = synth.make_requests(5)
+    caches = [pcd.pcd_prefill(model, r.prefix) for r in reqs]
+    t = time.time()
+    cold, st = pcd.pcd_score_batch(model, caches, [r.fields for r in reqs], with_stats=True)
+    print(f"batched branch pass: {len(reqs)} requests, T={st['branch_tokens']}, R={st['readout_rows']}, "
+          f"{time.time() - t:.2f} s wall")
+    for c in caches:
+        c.free()
+    # warm: the shared 512-token schema head is prefilled once
+    head = pcd.pcd_prefill(model, reqs[0].prefix[:512])
+    warm_caches = [pcd.pcd_prefill_extend(model, head, r.prefix[512:]) for r in reqs]
+    warm = pcd.pcd_score_batch(model, warm_caches, [r.fields for r in reqs])
+    # warm and cold are two valid rounding orders of the same numbers; the
+    # oracle judges both on the two shortest requests
+    gaps = [max(float(np.max(np.abs(a.probs - b.probs))) for a, b in zip(ra, rb)) for ra, rb in zip(cold, warm)]
+    print("warm/cold largest prob gap", max(gaps), "at request", int(np.argmax(gaps)))
+    for c in warm_caches:
+        c.free()
+    head.free()
+    from oracle import Oracle
+    orc = Oracle(w, np.float32)
+    pick = [int(i) for i in np.argsort([len(r.prefix) for r in reqs])[:2]]
+    for i in pick:
+        t = time.time()
+        oc = orc.prefill(reqs[i].prefix)
+        ref = [orc.score_field(f, cache=oc) for f in reqs[i].fields]
+        print(f"oracle request {i} (prefix {len(reqs[i].prefix)}): {time.time() - t:.1f} s")
+        worst = compare_request(cold[i], ref, f"config 5 request {i} cold", PROB_TOL_7B)
+        print("config 5 cold worst errors", worst)
+        worst = compare_request(warm[i], ref, f"config 5 request {i} warm", PROB_TOL_7B)
+        print("config 5 warm worst errors", worst)

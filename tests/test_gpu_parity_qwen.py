@@ -76,3 +76,25 @@ def test_warm_equals_cold_at_scale(qwen):
     for a, b in zip(cold, warm):
         np.testing.assert_allclose(a.probs, b.probs, atol=2e-3)
         np.testing.assert_allclose(a.logprobs, b.logprobs, atol=3e-2)
+
+
+def test_config4_long_document_sampled(qwen):
+    """8192-token prefix, 29 fields; the oracle checks a boolean, an enum and
+    the 218-label line-ID field (all its labels)."""
+    pcd, model, orc = qwen
+    req = synth.make_request(4)
+    cache = pcd.pcd_prefill(model, req.prefix)
+    got, st = pcd.pcd_score(model, cache, req.fields, with_stats=True)
+    t = time.time()
+    oc = orc.prefill(req.prefix)
+    print(f"oracle prefill 8192: {time.time() - t:.1f} s")
+    pick = [next(i for i, f in enumerate(req.fields) if f.kind == "bool"),
+            next(i for i, f in enumerate(req.fields) if f.kind == "enum"), len(req.fields) - 1]
+    t = time.time()
+    ref = [orc.score_field(req.fields[i], cache=oc) for i in pick]
+    print(f"oracle fields: {time.time() - t:.1f} s")
+    worst = compare_request([got[i] for i in pick], ref, "config 4")
+    print("config 4 worst errors", worst, "T", st["branch_tokens"], "R", st["readout_rows"])
+    # properties on every field
+    for g in got:
+        assert abs(g.probs.sum() - 1) < 1e-4 and 0 <= g.mass <= g.first_mass + 1e-6 <= 1 + 1e-6
