@@ -46,6 +46,8 @@ def parse_args():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", type=int, default=2, help="workload number (2: 28-field triage)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--mode", default="single", choices=["single", "two-pass"],
+                    help="single: prefix and branches in one forward pass; two-pass: prefill, then the branch pass")
     return ap.parse_args()
 
 
@@ -161,9 +163,13 @@ def work_model(cfg, Lp: int, T: int, R: int):
     branch_attn_bytes = 2.0 * Lp * L * 2 * kd           # prefix K and V, read once per request
     readout_bytes = 2.0 * V * d
     readout_flops = 2.0 * R * V * d
+    # single pass: every row through every layer, except the prefix rows of
+    # the last layer, which only need their keys and values
+    single_gemm_flops = 2.0 * (Lp + T) * L * layer_params - 2.0 * Lp * (w_o + w_mlp)
     return dict(prefill_gemm_flops=prefill_gemm_flops, prefill_attn_flops=prefill_attn_flops,
                 branch_weight_bytes=branch_weight_bytes, branch_gemm_flops=branch_gemm_flops,
-                branch_attn_bytes=branch_attn_bytes, readout_bytes=readout_bytes, readout_flops=readout_flops)
+                branch_attn_bytes=branch_attn_bytes, readout_bytes=readout_bytes, readout_flops=readout_flops,
+                single_gemm_flops=single_gemm_flops)
 
 
 # --------------------------------------------------------- CPU oracle timing
@@ -215,10 +221,15 @@ def run_ours(args):
     ids_dev = [torch.tensor(p, dtype=torch.int32, device="cuda") for p in prefixes]
     out = torch.zeros(plan.result_floats, dtype=torch.float32, device="cuda")
 
-    def step(i):
+    def step_two_pass(i):
         cache = pcd.pcd_prefill_device(model, ids_dev[i % n_pref])
         pcd.pcd_score_plan_device(model, cache, plan, out)
         cache.free()
+
+    def step_single(i):
+        pcd.pcd_prefill_score_plan_device(model, ids_dev[i % n_pref], plan, out)
+
+    step = step_single if args.mode == "single" else step_two_pass
 
     for i in range(max(args.warmup, 3)):
         step(i)
@@ -241,6 +252,18 @@ def run_ours(args):
     total_s = evs[0].elapsed_time(evs[K]) / 1e3
     total_s = max_over_ranks(dist, total_s)
     clocks = clk.summary()
+    # the other execution mode, same workload, for context
+    other = step_two_pass if step is step_single else step_single
+    for i in range(3):
+        other(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        other(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    other_ms = e0.elapsed_time(e1) / K
 
     # ---- per-kernel-class times over the same workload (profiled pass)
     pcd.pcd_profile_enable(model, True)
@@ -252,10 +275,17 @@ def run_ours(args):
 
     # ---- end to end through the host-pointer C ABI
     fields = req.fields
-    for i in range(2):
+    def e2e_step(i):
+        if args.mode == "single":
+            res, st = pcd.pcd_prefill_score(model, prefixes[i % n_pref], fields, with_stats=True)
+            return st, st["h2d_bytes"]
         c = pcd.pcd_prefill(model, prefixes[i % n_pref])
-        pcd.pcd_score(model, c, fields)
+        res, st = pcd.pcd_score(model, c, fields, with_stats=True)
         c.free()
+        return st, 4 * len(prefixes[i % n_pref]) + st["h2d_bytes"]
+
+    for i in range(2):
+        e2e_step(i)
     barrier(dist)
     torch.cuda.synchronize()
     e2e_ms = []
@@ -263,11 +293,8 @@ def run_ours(args):
     t_e2e0 = time.perf_counter()
     for i in range(K):
         t0 = time.perf_counter()
-        c = pcd.pcd_prefill(model, prefixes[i % n_pref])
-        res, st = pcd.pcd_score(model, c, fields, with_stats=True)
-        c.free()
+        st, h2d = e2e_step(i)
         e2e_ms.append((time.perf_counter() - t0) * 1e3)
-        h2d = 4 * len(prefixes[i % n_pref]) + st["h2d_bytes"]
         d2h = st["d2h_bytes"]
     e2e_s = max_over_ranks(dist, time.perf_counter() - t_e2e0)
     barrier(dist)
@@ -277,13 +304,18 @@ def run_ours(args):
     wm = work_model(cfg, len(req.prefix), T, R)
     peaks = read_peaks()
     cls_ms = {k: v[1] / K for k, v in prof.items()}       # per request
-    dominant = max(("gemm_prefill", "gemm_branch", "attn_prefill", "attn_branch", "readout"), key=lambda k: cls_ms[k])
+    dominant = max(("gemm_prefill", "gemm_branch", "gemm_single", "attn_prefill", "attn_branch", "readout"),
+                   key=lambda k: cls_ms[k])
 
     def roof(cls):
         ms = cls_ms[cls]
         n_launch = prof[cls][0] / K
         if cls == "gemm_prefill":
             work, bound = wm["prefill_gemm_flops"], "tensor"
+        elif cls == "gemm_single":
+            t_hbm = wm["branch_weight_bytes"] / (peaks["hbm_gbs"] * 1e9)
+            t_tc = wm["single_gemm_flops"] / (peaks["bf16_tflops"] * 1e12)
+            work, bound = (wm["branch_weight_bytes"], "hbm") if t_hbm >= t_tc else (wm["single_gemm_flops"], "tensor")
         elif cls == "gemm_branch":
             # at the ridge: report the bound with the larger roofline time
             t_hbm = wm["branch_weight_bytes"] / (peaks["hbm_gbs"] * 1e9)
@@ -307,8 +339,12 @@ def run_ours(args):
                 "peak_source": peaks["source"] + (" (burst)" if unit == "TFLOP/s" else "")}
 
     roofline = roof(dominant)
-    # branch pass HBM GB/s (the metric's second half): weights + prefix KV + E over the branch kernels
-    branch_ms = cls_ms["gemm_branch"] + cls_ms["attn_branch"] + cls_ms["readout"]
+    # HBM GB/s of the pass that streams the weights for the branch rows (the
+    # metric's second half): weights + prefix KV + E over that pass's kernels
+    # (in single-pass mode the prefix rows share the same weight stream)
+    branch_ms = cls_ms["gemm_branch"] + cls_ms["gemm_single"] + cls_ms["attn_branch"] + cls_ms["readout"]
+    if args.mode == "single":
+        branch_ms += cls_ms["attn_prefill"]
     branch_bytes = wm["branch_weight_bytes"] + wm["branch_attn_bytes"] + wm["readout_bytes"]
     branch_gbs = branch_bytes / (branch_ms / 1e3) / 1e9
 
@@ -330,7 +366,7 @@ def run_ours(args):
         "dtype": "bf16",
         "data": "synthetic (seeded random-init weights and token ids)",
         "config": {"workload": WORKLOAD, "prefix_len": len(req.prefix), "fields": len(req.fields),
-                   "branch_tokens": T, "readout_rows": R, "requests_per_step": 1,
+                   "branch_tokens": T, "readout_rows": R, "requests_per_step": 1, "mode": args.mode,
                    "l2": "inputs larger than L2 (3.1 GB of weights streamed every step)",
                    "parallelism": f"replicas x{ws}"},
         "roofline": roofline,
@@ -338,6 +374,8 @@ def run_ours(args):
                         "frac_of_8tbs_spec": round(branch_gbs / 8000.0, 4), "ms_per_request": round(branch_ms, 4),
                         "algorithmic_bytes": branch_bytes},
         "kernel_ms_per_step": {k: round(v, 4) for k, v in cls_ms.items()},
+        "other_mode": {"mode": "two-pass" if args.mode == "single" else "single", "ms_per_step": round(other_ms, 4),
+                       "req_per_s": round(1e3 / other_ms, 3)},
         "e2e": {"value": round(n_total / e2e_s, 3), "unit": "req/s", "p50_latency_ms": round(statistics.median(e2e_ms), 4),
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": int(round(launches_per_step * K)),

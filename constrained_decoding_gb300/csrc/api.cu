@@ -96,7 +96,7 @@ struct PlanView {
 };
 
 enum ProfClass { PROF_GEMM_PREFILL = 0, PROF_GEMM_BRANCH = 1, PROF_ATTN_PREFILL = 2, PROF_ATTN_BRANCH = 3,
-                 PROF_READOUT = 4, PROF_OTHER = 5 };
+                 PROF_READOUT = 4, PROF_OTHER = 5, PROF_GEMM_SINGLE = 6 };
 
 }  // namespace
 
@@ -280,8 +280,8 @@ int gemm(pcd_model* m, int cls, const void* A, int M, int lda, const act_t* B, i
   }
   int run_epi = epi;
   if (splittable && t.splits > 1) {
-    if (epi == pcd::EPI_F32_STORE)
-      PCD_CUDA(cudaMemsetAsync(out, 0, static_cast<size_t>(M) * ldo * sizeof(float), m->stream));
+    // EPI_F32_STORE outputs (the q/k/v accumulator) are kept zeroed by their
+    // consumer, so split-K partial sums can be added with atomics
     run_epi = pcd::EPI_F32_ATOMIC;
   }
   pcd::GemmShape s{A, M, lda, B, N, ldb, K, A_lo};
@@ -297,7 +297,9 @@ int ensure_workspace(pcd_model* m, int T) {
   const size_t t = static_cast<size_t>(std::max(T, 1));
   PCD_TRY(ensure(m->x32, t * m->d * 4));
   PCD_TRY(ensure(m->xn, t * m->d * 2));
+  const void* old_qkv = m->qkv.p;
   PCD_TRY(ensure(m->qkv, t * m->Nqkv * 4));
+  if (m->qkv.p != old_qkv) PCD_CUDA(cudaMemsetAsync(m->qkv.p, 0, m->qkv.n, m->stream));
   PCD_TRY(ensure(m->q, t * m->qdim * 2));
   PCD_TRY(ensure(m->att, t * m->qdim * 2));
   PCD_TRY(ensure(m->hb, t * m->Fp * 2));
@@ -373,6 +375,7 @@ int record_prefill(pcd_model* m, const int32_t* d_ids, int n, pcd_cache* c, int 
     ra.kv_head_stride = c->cap;
     ra.kv_row0 = p0;
     ra.err = m->d_err;
+    ra.clear_qkv = 1;
     PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_rope_kv(ra, m->stream); }));
     // The last layer's attention output and MLP change no cached key or value.
     if (l == m->L - 1) break;
@@ -522,6 +525,7 @@ int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_se
       ra.kv_head_stride = T;
       ra.kv_row0 = sg.t0;
       ra.err = m->d_err;
+      ra.clear_qkv = 1;
       PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_rope_kv(ra, m->stream); }));
     }
     for (int s = 0; s < n_seg; ++s) {
@@ -585,6 +589,246 @@ int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_se
   act_t* hr = static_cast<act_t*>(m->hr.p);
   PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
     return pcd::launch_rmsnorm(x, m->d, p.ro_tok, R, m->d, m->final_norm, m->cfg.rms_eps, hr, m->d, m->stream, hr_lo);
+  }));
+  pcd::GemmShape rs{hr, R, m->d, m->lm, m->V, m->d, m->d, hr_lo};
+  pcd::GemmTiling ro_t = p.ro_tiling;
+  if (hr_lo) {
+    ro_t.mt = 1;
+    ro_t.cs = 1;
+  }
+  pcd::EpiArgs re;
+  re.part = static_cast<float2*>(m->ro_part.p);
+  re.gather_off = p.gather_off;
+  re.gather = p.gather;
+  re.z_out = static_cast<float*>(m->z.p);
+  PCD_LAUNCH(timed(m, PROF_READOUT, [&] {
+    return pcd::launch_gemm(rs, pcd::EPI_READOUT, re, ro_t, m->stream, m->d_err, m->wait_ns, m->sms);
+  }));
+  PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
+    return pcd::launch_lse_combine(static_cast<float2*>(m->ro_part.p), p.n_vtiles, R, static_cast<float*>(m->lse.p),
+                                   m->stream);
+  }));
+  pcd::ScoreArgs sa;
+  sa.z = static_cast<float*>(m->z.p);
+  sa.lse = static_cast<float*>(m->lse.p);
+  sa.child_row = p.child_row;
+  sa.lab_off = p.lab_off;
+  sa.path = p.path;
+  sa.fld_lab = p.fld_lab;
+  sa.fld_root = p.fld_root;
+  sa.row_ch = p.row_ch;
+  sa.temp = p.temp;
+  sa.n_fields = p.n_fields;
+  sa.out_field = d_result;
+  sa.out_probs = d_result + p.n_fields * 8;
+  sa.out_logprobs = d_result + p.n_fields * 8 + p.n_labels;
+  PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_score(sa, m->stream); }));
+  return PCD_OK;
+}
+
+// ------------------------------------------------------------- single pass
+// The prefix and every branch row in ONE forward pass (the stephanj README's
+// single-pass mode): rows [0, n) are the prefix at positions 0..n-1, rows
+// [n, n + T) the branch tokens at n + rel.  In each layer the prefix rows
+// write their keys/values into the cache and attend causally; the branch rows
+// attend to that layer's prefix keys plus their own ancestors.  The weights
+// stream once per request.  In the last layer the prefix rows only need their
+// keys and values.
+int record_single(pcd_model* m, const PlanView& p, const int32_t* ids, int n, pcd_cache* c, float* d_result,
+                  int pf_splits, int br_splits);
+
+int run_single(pcd_model* m, const PlanView& p, const int32_t* d_ids, int n, pcd_cache* c, float* d_result) {
+  const int T = p.T, R = p.R, G = m->G, N = n + T;
+  PCD_TRY(ensure_workspace(m, N));
+  PCD_TRY(ensure(m->kb, static_cast<size_t>(m->Hkv) * T * m->dh * 2));
+  PCD_TRY(ensure(m->vb, static_cast<size_t>(m->Hkv) * T * m->dh * 2));
+  PCD_TRY(ensure(m->ids, static_cast<size_t>(n) * 4));
+  if (d_ids != m->ids.p)
+    PCD_CUDA(cudaMemcpyAsync(m->ids.p, d_ids, static_cast<size_t>(n) * 4, cudaMemcpyDeviceToDevice, m->stream));
+  const int pf_splits = prefill_splits(m, n, 0);
+  const int blocks = ((T * G + 63) / 64) * m->Hkv;
+  const int br_splits = std::max(1, std::min((2 * m->sms + blocks - 1) / blocks, (n + 255) / 256));
+  const size_t part_rows = std::max(static_cast<size_t>(pf_splits) * n, static_cast<size_t>(br_splits) * T);
+  PCD_TRY(ensure(m->part_o, part_rows * m->Hkv * G * m->dh * 4));
+  PCD_TRY(ensure(m->part_ml, part_rows * m->Hkv * G * 8));
+  PCD_TRY(ensure(m->hr, static_cast<size_t>(std::max(R, 1)) * m->d * 2));
+  PCD_TRY(ensure(m->hr_lo, static_cast<size_t>(std::max(R, 1)) * m->d * 2));
+  PCD_TRY(ensure(m->ro_part, static_cast<size_t>(p.n_vtiles) * std::max(R, 1) * 8));
+  PCD_TRY(ensure(m->z, static_cast<size_t>(std::max(p.n_children, 1)) * 4));
+  PCD_TRY(ensure(m->lse, static_cast<size_t>(std::max(R, 1)) * 4));
+  const int32_t* ids = static_cast<const int32_t*>(m->ids.p);
+  const std::vector<int64_t> key{3, n, reinterpret_cast<int64_t>(p.tok), T, R, p.n_children, p.n_labels, p.n_fields,
+                                 reinterpret_cast<int64_t>(d_result), reinterpret_cast<int64_t>(c->k), c->cap,
+                                 pf_splits, br_splits};
+  return with_graph(m, key, [&] { return record_single(m, p, ids, n, c, d_result, pf_splits, br_splits); });
+}
+
+int record_single(pcd_model* m, const PlanView& p, const int32_t* ids, int n, pcd_cache* c, float* d_result,
+                  int pf_splits, int br_splits) {
+  const int T = p.T, R = p.R, G = m->G, N = n + T;
+  float* x = static_cast<float*>(m->x32.p);
+  act_t* xn = static_cast<act_t*>(m->xn.p);
+  float* qkv = static_cast<float*>(m->qkv.p);
+  act_t* q = static_cast<act_t*>(m->q.p);
+  act_t* att = static_cast<act_t*>(m->att.p);
+  act_t* hb = static_cast<act_t*>(m->hb.p);
+  act_t* xlo = (m->split_act & 1) ? static_cast<act_t*>(m->xn_lo.p) : nullptr;
+  const bool split_out = (m->split_act & 4) != 0;
+  act_t* att_lo = split_out ? static_cast<act_t*>(m->att_lo.p) : nullptr;
+  act_t* hb_lo = split_out ? static_cast<act_t*>(m->hb_lo.p) : nullptr;
+  act_t* hr_lo = (m->split_act & 16) ? static_cast<act_t*>(m->hr_lo.p) : nullptr;
+  act_t* kb = static_cast<act_t*>(m->kb.p);
+  act_t* vb = static_cast<act_t*>(m->vb.p);
+  float* part_o = static_cast<float*>(m->part_o.p);
+  float2* part_ml = static_cast<float2*>(m->part_ml.p);
+  const float scale_log2 = 1.4426950408889634f / std::sqrt(static_cast<float>(m->dh));
+  const size_t layer_kv = static_cast<size_t>(m->Hkv) * c->cap * m->dh;
+  auto off = [](auto* ptr, size_t rows, size_t ld) { return ptr + rows * ld; };
+
+  PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_embed(ids, n, m->embed, m->d, m->V, x, m->d_err, m->stream); }));
+  PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
+    return pcd::launch_embed(p.tok, T, m->embed, m->d, m->V, off(x, n, m->d), m->d_err, m->stream);
+  }));
+  for (int l = 0; l < m->L; ++l) {
+    const Layer& W = m->layers[l];
+    const bool last = l == m->L - 1;
+    PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
+      return pcd::launch_rmsnorm(x, m->d, nullptr, N, m->d, W.attn_norm, m->cfg.rms_eps, xn, m->d, m->stream, xlo);
+    }));
+    PCD_TRY(gemm(m, PROF_GEMM_SINGLE, xn, N, m->d, W.wqkv, m->Nqkv, m->d, m->d, pcd::EPI_F32_STORE, qkv, m->Nqkv, xlo));
+    // RoPE: prefix rows -> the cache; branch rows -> the branch scratch
+    pcd::RopeArgs ra;
+    ra.ldqkv = m->Nqkv;
+    ra.Hq = m->Hq;
+    ra.Hkv = m->Hkv;
+    ra.DH = m->dh;
+    ra.cs = m->rope;
+    ra.max_pos = m->max_pos;
+    ra.err = m->d_err;
+    ra.clear_qkv = 1;
+    ra.qkv = qkv;
+    ra.n = n;
+    ra.rel = nullptr;
+    ra.base = 0;
+    ra.q = q;
+    ra.k_dst = c->k + l * layer_kv;
+    ra.v_dst = c->v + l * layer_kv;
+    ra.kv_head_stride = c->cap;
+    ra.kv_row0 = 0;
+    PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_rope_kv(ra, m->stream); }));
+    ra.qkv = off(qkv, n, m->Nqkv);
+    ra.n = T;
+    ra.rel = p.rel;
+    ra.base = n;
+    ra.q = off(q, n, m->qdim);
+    ra.k_dst = kb;
+    ra.v_dst = vb;
+    ra.kv_head_stride = T;
+    ra.kv_row0 = 0;
+    PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_rope_kv(ra, m->stream); }));
+    // prefix attention (causal); not needed in the last layer
+    if (!last) {
+      pcd::AttnArgs aa{};
+      aa.q = q;
+      aa.n_tok = n;
+      aa.Hq = m->Hq;
+      aa.Hkv = m->Hkv;
+      aa.DH = m->dh;
+      aa.tok0 = 0;
+      aa.part_rows = n * G;
+      aa.k = c->k + l * layer_kv;
+      aa.v = c->v + l * layer_kv;
+      aa.kv_head_stride = c->cap;
+      aa.n_keys = n;
+      aa.rel = nullptr;
+      aa.base = 0;
+      aa.n_splits = pf_splits;
+      aa.split_len = ((n + pf_splits - 1) / pf_splits + 63) / 64 * 64;
+      aa.scale_log2 = scale_log2;
+      aa.out = att;
+      aa.ld_out = m->qdim;
+      aa.partial = pf_splits > 1 || split_out;
+      aa.part_o = part_o;
+      aa.part_ml = part_ml;
+      aa.causal_heavy_first = 1;
+      PCD_LAUNCH(timed(m, PROF_ATTN_PREFILL, [&] { return pcd::launch_attention(aa, m->stream); }));
+      if (aa.partial) {
+        pcd::MergeArgs ma{};
+        ma.q = q;
+        ma.n_tok = n;
+        ma.Hq = m->Hq;
+        ma.Hkv = m->Hkv;
+        ma.DH = m->dh;
+        ma.part_o = part_o;
+        ma.part_ml = part_ml;
+        ma.n_splits = pf_splits;
+        ma.scale_log2 = scale_log2;
+        ma.out = att;
+        ma.ld_out = m->qdim;
+        ma.out_lo = att_lo;
+        PCD_LAUNCH(timed(m, PROF_ATTN_PREFILL, [&] { return pcd::launch_branch_merge(ma, m->stream); }));
+      }
+    }
+    // branch attention: this layer's prefix keys (split) + ancestors
+    {
+      pcd::AttnArgs aa{};
+      aa.q = off(q, n, m->qdim);
+      aa.n_tok = T;
+      aa.Hq = m->Hq;
+      aa.Hkv = m->Hkv;
+      aa.DH = m->dh;
+      aa.tok0 = 0;
+      aa.part_rows = T * G;
+      aa.k = c->k + l * layer_kv;
+      aa.v = c->v + l * layer_kv;
+      aa.kv_head_stride = c->cap;
+      aa.n_keys = n;
+      aa.rel = p.rel;
+      aa.base = n;
+      aa.n_splits = br_splits;
+      aa.split_len = ((n + br_splits - 1) / br_splits + 63) / 64 * 64;
+      aa.scale_log2 = scale_log2;
+      aa.part_o = part_o;
+      aa.part_ml = part_ml;
+      aa.partial = 1;
+      aa.causal_heavy_first = 0;
+      PCD_LAUNCH(timed(m, PROF_ATTN_BRANCH, [&] { return pcd::launch_attention(aa, m->stream); }));
+      pcd::MergeArgs ma{};
+      ma.q = off(q, n, m->qdim);
+      ma.n_tok = T;
+      ma.Hq = m->Hq;
+      ma.Hkv = m->Hkv;
+      ma.DH = m->dh;
+      ma.part_o = part_o;
+      ma.part_ml = part_ml;
+      ma.n_splits = br_splits;
+      ma.kb = kb;
+      ma.vb = vb;
+      ma.anc_off = p.anc_off;
+      ma.anc_idx = p.anc_idx;
+      ma.scale_log2 = scale_log2;
+      ma.out = off(att, n, m->qdim);
+      ma.ld_out = m->qdim;
+      ma.out_lo = att_lo ? off(att_lo, n, m->qdim) : nullptr;
+      PCD_LAUNCH(timed(m, PROF_ATTN_BRANCH, [&] { return pcd::launch_branch_merge(ma, m->stream); }));
+    }
+    // O-proj and MLP over every row, or only the branch rows in the last layer
+    const int r0 = last ? n : 0, M = N - r0;
+    PCD_TRY(gemm(m, PROF_GEMM_SINGLE, off(att, r0, m->qdim), M, m->qdim, W.wo, m->d, m->qdim, m->qdim,
+                 pcd::EPI_F32_ADD, off(x, r0, m->d), m->d, att_lo ? off(att_lo, r0, m->qdim) : nullptr));
+    PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
+      return pcd::launch_rmsnorm(off(x, r0, m->d), m->d, nullptr, M, m->d, W.mlp_norm, m->cfg.rms_eps, xn, m->d,
+                                 m->stream, xlo);
+    }));
+    PCD_TRY(gemm(m, PROF_GEMM_SINGLE, xn, M, m->d, W.wgu, 2 * m->Fp, m->d, m->d, pcd::EPI_SWIGLU, hb, m->Fp, xlo, hb_lo));
+    PCD_TRY(gemm(m, PROF_GEMM_SINGLE, hb, M, m->Fp, W.wd, m->d, m->Fp, m->Fp, pcd::EPI_F32_ADD, off(x, r0, m->d), m->d,
+                 hb_lo));
+  }
+
+  act_t* hr = static_cast<act_t*>(m->hr.p);
+  PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
+    return pcd::launch_rmsnorm(off(x, n, m->d), m->d, p.ro_tok, R, m->d, m->final_norm, m->cfg.rms_eps, hr, m->d,
+                               m->stream, hr_lo);
   }));
   pcd::GemmShape rs{hr, R, m->d, m->lm, m->V, m->d, m->d, hr_lo};
   pcd::GemmTiling ro_t = p.ro_tiling;
@@ -1296,6 +1540,83 @@ int pcd_score_plan_device(pcd_model* m, const pcd_cache* cache, const pcd_plan* 
   PCD_TRY(check_positions(m, cache->len, p->view.max_rel));
   Segment s{cache, 0, p->view.T};
   return run_branch(m, p->view, &s, 1, result_device);
+}
+
+int pcd_prefill_score(pcd_model* m, const int32_t* ids, int n, const pcd_field* fields, int n_fields,
+                      pcd_field_result* out, pcd_stats* stats, pcd_cache** cache_out) {
+  if (!m || !ids || !fields || !out || n < 1 || n_fields < 1) return fail(PCD_ERR_INVALID_ARG, "NULL argument or empty input");
+  const auto t_start = std::chrono::steady_clock::now();
+  pcd::HostPlan hp;
+  std::string msg;
+  const int rc = pcd::compile_fields(fields, n_fields, m->V, &hp, &msg);
+  if (rc != PCD_OK) return fail(rc, msg);
+  PCD_TRY(check_positions(m, n, hp.max_rel));
+  const auto t_comp = std::chrono::steady_clock::now();
+  const int32_t* d_ids = nullptr;
+  PCD_TRY(upload_ids(m, ids, n, &d_ids));
+  PlanView v;
+  size_t plan_bytes = 0;
+  PCD_TRY(upload_plan(m, hp, v, &plan_bytes));
+  PCD_TRY(ensure(m->result, static_cast<size_t>(v.result_floats()) * 4));
+  pcd_cache* c = nullptr;
+  PCD_TRY(new_cache(m, n, &c));
+  if (stats) cudaEventRecord(m->ev_a, m->stream);
+  int r = run_single(m, v, d_ids, n, c, static_cast<float*>(m->result.p));
+  if (r != PCD_OK) {
+    pcd_cache_free(c);
+    return r;
+  }
+  c->len = n;
+  if (stats) cudaEventRecord(m->ev_c, m->stream);
+  const size_t rbytes = static_cast<size_t>(v.result_floats()) * 4;
+  r = ensure_pinned(m->down, m->down_n, rbytes);
+  if (r == PCD_OK && cudaMemcpyAsync(m->down, m->result.p, rbytes, cudaMemcpyDeviceToHost, m->stream) != cudaSuccess)
+    r = fail(PCD_ERR_CUDA, "result copy");
+  if (r == PCD_OK && cudaStreamSynchronize(m->stream) != cudaSuccess) r = fail(PCD_ERR_CUDA, "stream sync");
+  m->up_pending = false;
+  if (r == PCD_OK) r = read_device_error(m);
+  if (r != PCD_OK) {
+    pcd_cache_free(c);
+    return r;
+  }
+  unpack_results(static_cast<const float*>(m->down), v, 0, 0, n_fields, out);
+  if (stats) {
+    const auto t_end = std::chrono::steady_clock::now();
+    std::memset(stats, 0, sizeof(*stats));
+    stats->compile_ms = std::chrono::duration<float, std::milli>(t_comp - t_start).count();
+    cudaEventElapsedTime(&stats->branch_ms, m->ev_a, m->ev_c);
+    stats->total_ms = std::chrono::duration<float, std::milli>(t_end - t_start).count();
+    stats->forward_passes = 1;
+    stats->branch_tokens = v.T;
+    stats->readout_rows = v.R;
+    stats->h2d_bytes = static_cast<int64_t>(plan_bytes) + static_cast<int64_t>(n) * 4;
+    stats->d2h_bytes = static_cast<int64_t>(rbytes);
+  }
+  if (cache_out)
+    *cache_out = c;
+  else
+    pcd_cache_free(c);
+  return PCD_OK;
+}
+
+int pcd_prefill_score_plan_device(pcd_model* m, const int32_t* ids_device, int n, const pcd_plan* plan,
+                                  float* result_device, pcd_cache** cache_out) {
+  if (!m || !ids_device || !plan || !result_device || n < 1) return fail(PCD_ERR_INVALID_ARG, "NULL argument");
+  if (plan->m != m) return fail(PCD_ERR_SHAPE_MISMATCH, "plan belongs to another model");
+  PCD_TRY(check_positions(m, n, plan->view.max_rel));
+  pcd_cache* c = nullptr;
+  PCD_TRY(new_cache(m, n, &c));
+  const int r = run_single(m, plan->view, ids_device, n, c, result_device);
+  if (r != PCD_OK) {
+    pcd_cache_free(c);
+    return r;
+  }
+  c->len = n;
+  if (cache_out)
+    *cache_out = c;
+  else
+    pcd_cache_free(c);
+  return PCD_OK;
 }
 
 int pcd_sync(pcd_model* m) {

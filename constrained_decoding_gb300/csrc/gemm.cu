@@ -205,6 +205,9 @@ __global__ void __launch_bounds__(192, 1)
   }
   tc_fence_after_sync();
   const uint32_t tbase = *tmem_slot;
+  // the prologue above overlapped the previous kernel's tail; its results are needed from here on
+  griddep_launch_dependents();
+  griddep_wait();
 
   auto tile0 = [&](int mg) { return mg * MT * CS + rank * MT; };  // this CTA's first M tile of group mg
   auto valid_tiles = [&](int mg) { return max(0, min(MT, mtiles - tile0(mg))); };
@@ -488,8 +491,7 @@ static int launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensor
   }
   if (CS == 1) {
     const int grid = std::min(p.n_units, sms);
-    kern<<<grid, 192, C::SMEM_BYTES, st>>>(ma, mb, ma2, p, e);
-    return cudaGetLastError();
+    return launch_k(kern, dim3(grid), dim3(192), C::SMEM_BYTES, st, ma, mb, ma2, p, e);
   }
   const int clusters = std::min(p.n_units, max_clusters);
   cudaLaunchConfig_t cfg = {};

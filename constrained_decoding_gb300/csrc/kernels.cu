@@ -9,9 +9,19 @@
 
 namespace pcd {
 
+bool pdl_enabled() {
+  static const bool on = [] {
+    const char* e = std::getenv("PCD_PDL");
+    return !e || std::atoi(e) != 0;
+  }();
+  return on;
+}
+
 // ======================================================================= embed
 __global__ void embed_kernel(const int32_t* __restrict__ ids, int n, const act_t* __restrict__ E, int d, int vocab,
                              float* __restrict__ x, int* err) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int t = blockIdx.x;
   if (t >= n) return;
   int id = ids[t];
@@ -33,8 +43,7 @@ __global__ void embed_kernel(const int32_t* __restrict__ ids, int n, const act_t
 
 int launch_embed(const int32_t* ids, int n, const act_t* E, int d, int vocab, float* x, int* err, cudaStream_t s) {
   if (n <= 0) return 0;
-  embed_kernel<<<n, 128, 0, s>>>(ids, n, E, d, vocab, x, err);
-  return cudaGetLastError();
+  return launch_k(embed_kernel, dim3(n), dim3(128), 0, s, ids, n, E, d, vocab, x, err);
 }
 
 // ===================================================================== rmsnorm
@@ -48,6 +57,8 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float* __re
                                                                const float* __restrict__ gain, float eps,
                                                                act_t* __restrict__ out, int ldo,
                                                                act_t* __restrict__ out_lo) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int r = blockIdx.x;
   const int src = rows ? rows[r] : r;
   const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(src) * ldx);
@@ -100,14 +111,15 @@ int launch_rmsnorm(const float* x, int ldx, const int32_t* rows, int n, int d, c
                    int ldo, cudaStream_t s, act_t* out_lo) {
   if (n <= 0) return 0;
   if (d % 4 || d > 4 * kNormThreads * kNormMaxVec) return -1;
-  rmsnorm_kernel<<<n, kNormThreads, 0, s>>>(x, ldx, rows, n, d, gain, eps, out, ldo, out_lo);
-  return cudaGetLastError();
+  return launch_k(rmsnorm_kernel, dim3(n), dim3(kNormThreads), 0, s, x, ldx, rows, n, d, gain, eps, out, ldo, out_lo);
 }
 
 // ====================================================================== rope_kv
 // Thread per (token, head, rotation pair).  Rotate-half pairing (i, i + DH/2),
 // angle pos * theta^(-2i/DH) from a (cos, sin) table built in double precision.
 __global__ void rope_kv_kernel(RopeArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int half = a.DH / 2;
   const int heads = a.Hq + 2 * a.Hkv;
   const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
@@ -121,8 +133,12 @@ __global__ void rope_kv_kernel(RopeArgs a) {
     record_error(a.err, DEV_BAD_INDEX);
     pos = 0;
   }
-  const float* src = a.qkv + static_cast<size_t>(t) * a.ldqkv + h * a.DH;
+  float* src = const_cast<float*>(a.qkv) + static_cast<size_t>(t) * a.ldqkv + h * a.DH;
   const float x1 = src[i], x2 = src[i + half];
+  if (a.clear_qkv) {  // leave the accumulation buffer zeroed for the next split-K projection
+    src[i] = 0.f;
+    src[i + half] = 0.f;
+  }
   if (h < a.Hq + a.Hkv) {
     const float2 cs = a.cs[static_cast<size_t>(pos) * half + i];
     const float y1 = x1 * cs.x - x2 * cs.y;
@@ -145,8 +161,7 @@ __global__ void rope_kv_kernel(RopeArgs a) {
 int launch_rope_kv(const RopeArgs& a, cudaStream_t s) {
   if (a.n <= 0) return 0;
   const long long total = static_cast<long long>(a.n) * (a.Hq + 2 * a.Hkv) * (a.DH / 2);
-  rope_kv_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_k(rope_kv_kernel, dim3(static_cast<unsigned>((total + 255) / 256)), dim3(256), 0, s, a);
 }
 
 // ==================================================================== attention
@@ -203,6 +218,8 @@ __global__ void __launch_bounds__(128) attn_kernel(AttnArgs a) {
   act_t* sV = sK + 2 * 64 * LDS;      // [2][64][LDS]
   int* sPos = reinterpret_cast<int*>(sV + 2 * 64 * LDS);
 
+  griddep_launch_dependents();
+  griddep_wait();
   const int G = a.Hq / a.Hkv;
   const int rows = a.n_tok * G;
   const int nrb = gridDim.x;
@@ -414,8 +431,7 @@ static int launch_attn_t(const AttnArgs& a, cudaStream_t s) {
   const int G = a.Hq / a.Hkv;
   const int rows = a.n_tok * G;
   dim3 grid((rows + 63) / 64, a.Hkv, a.n_splits);
-  attn_kernel<DH><<<grid, 128, AttnSmem<DH>::BYTES, s>>>(a);
-  return cudaGetLastError();
+  return launch_k(attn_kernel<DH>, grid, dim3(128), AttnSmem<DH>::BYTES, s, a);
 }
 
 int launch_attention(const AttnArgs& a, cudaStream_t s) {
@@ -439,6 +455,8 @@ template <int DH>
 __global__ void __launch_bounds__(256) branch_merge_kernel(MergeArgs a) {
   constexpr int EPT = DH >= 32 ? DH / 32 : 1;
   __shared__ __align__(16) float sq[8][DH];
+  griddep_launch_dependents();
+  griddep_wait();
   const int wl = threadIdx.x >> 5;
   const int w = blockIdx.x * (blockDim.x >> 5) + wl;
   const int lane = threadIdx.x & 31;
@@ -539,16 +557,17 @@ int launch_branch_merge(const MergeArgs& a, cudaStream_t s) {
   if (warps <= 0) return 0;
   const int blocks = (warps + 7) / 8;
   switch (a.DH) {
-    case 16: branch_merge_kernel<16><<<blocks, 256, 0, s>>>(a); break;
-    case 64: branch_merge_kernel<64><<<blocks, 256, 0, s>>>(a); break;
-    case 128: branch_merge_kernel<128><<<blocks, 256, 0, s>>>(a); break;
-    default: return -1;
+    case 16: return launch_k(branch_merge_kernel<16>, dim3(blocks), dim3(256), 0, s, a);
+    case 64: return launch_k(branch_merge_kernel<64>, dim3(blocks), dim3(256), 0, s, a);
+    case 128: return launch_k(branch_merge_kernel<128>, dim3(blocks), dim3(256), 0, s, a);
   }
-  return cudaGetLastError();
+  return -1;
 }
 
 // ================================================================ lse combine
 __global__ void lse_combine_kernel(const float2* __restrict__ part, int n_tiles, int R, float* __restrict__ lse) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= R) return;
@@ -568,8 +587,7 @@ __global__ void lse_combine_kernel(const float2* __restrict__ part, int n_tiles,
 
 int launch_lse_combine(const float2* part, int n_tiles, int R, float* lse, cudaStream_t s) {
   if (R <= 0) return 0;
-  lse_combine_kernel<<<(R + 7) / 8, 256, 0, s>>>(part, n_tiles, R, lse);
-  return cudaGetLastError();
+  return launch_k(lse_combine_kernel, dim3((R + 7) / 8), dim3(256), 0, s, part, n_tiles, R, lse);
 }
 
 // ====================================================================== score
@@ -578,6 +596,8 @@ int launch_lse_combine(const float2* part, int n_tiles, int R, float* lse, cudaS
 // ties), the candidate mass sum_c exp(s_c), the top-2 margin of s and the
 // first-decision mass (distinct first tokens at the root readout row).
 __global__ void __launch_bounds__(256) score_kernel(ScoreArgs a) {
+  griddep_launch_dependents();
+  griddep_wait();
   const int f = blockIdx.x;
   const int c0 = a.fld_lab[f], c1 = a.fld_lab[f + 1];
   const int nl = c1 - c0;
@@ -678,8 +698,7 @@ __global__ void __launch_bounds__(256) score_kernel(ScoreArgs a) {
 
 int launch_score(const ScoreArgs& a, cudaStream_t s) {
   if (a.n_fields <= 0) return 0;
-  score_kernel<<<a.n_fields, 256, 0, s>>>(a);
-  return cudaGetLastError();
+  return launch_k(score_kernel, dim3(a.n_fields), dim3(256), 0, s, a);
 }
 
 }  // namespace pcd

@@ -29,6 +29,7 @@ struct RopeArgs {
   int64_t kv_head_stride; // elements between KV heads
   int kv_row0;
   int* err;
+  int clear_qkv = 0;      // zero the consumed qkv values (the next split-K projection accumulates into them)
 };
 int launch_rope_kv(const RopeArgs& a, cudaStream_t s);
 

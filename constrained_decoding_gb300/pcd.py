@@ -260,6 +260,34 @@ def pcd_score_batch(model: Model, caches: Sequence[Cache], fields: Sequence[Sequ
     return (out, _stats_dict(st)) if with_stats else out
 
 
+def pcd_prefill_score(model: Model, ids, fields: Sequence, with_stats: bool = False, keep_cache: bool = False):
+    """Single-pass request: prefix + every field in one forward pass.
+    Returns results (and stats, and the prefix Cache when keep_cache)."""
+    ids = _i32(ids)
+    f = _Fields(fields)
+    r = _Results(f.n_cands)
+    st = D.pcd_stats()
+    cache = ctypes.c_void_p()
+    _check(load().pcd_prefill_score(model.handle, _ptr_i32(ids), len(ids), f.arr, len(fields), r.arr, ctypes.byref(st),
+                                    ctypes.byref(cache) if keep_cache else None), "pcd_prefill_score")
+    out = [r.results()]
+    if with_stats:
+        out.append(_stats_dict(st))
+    if keep_cache:
+        out.append(Cache(model, cache.value))
+    return out[0] if len(out) == 1 else tuple(out)
+
+
+def pcd_prefill_score_plan_device(model: Model, ids_device, plan: Plan, result_device, keep_cache: bool = False):
+    """Single-pass request from device-resident ids (CUDA int32 tensor) and a plan; only enqueues."""
+    cache = ctypes.c_void_p()
+    ptr = result_device if isinstance(result_device, int) else result_device.data_ptr()
+    _check(load().pcd_prefill_score_plan_device(model.handle, ids_device.data_ptr(), ids_device.numel(), plan.handle,
+                                                ptr, ctypes.byref(cache) if keep_cache else None),
+           "pcd_prefill_score_plan_device")
+    return Cache(model, cache.value) if keep_cache else None
+
+
 def pcd_plan_create(model: Model, fields: Sequence) -> Plan:
     f = _Fields(fields)
     out = ctypes.c_void_p()
@@ -295,12 +323,12 @@ def pcd_profile_enable(model: Model, on: bool = True) -> None:
     _check(load().pcd_profile_enable(model.handle, 1 if on else 0), "pcd_profile_enable")
 
 
-PROFILE_CLASSES = ("gemm_prefill", "gemm_branch", "attn_prefill", "attn_branch", "readout", "other")
+PROFILE_CLASSES = ("gemm_prefill", "gemm_branch", "attn_prefill", "attn_branch", "readout", "other", "gemm_single")
 
 
 def pcd_profile_read(model: Model) -> dict:
-    n = (ctypes.c_int * 6)()
-    ms = (ctypes.c_float * 6)()
+    n = (ctypes.c_int * 7)()
+    ms = (ctypes.c_float * 7)()
     _check(load().pcd_profile_read(model.handle, n, ms), "pcd_profile_read")
     return {k: (int(n[i]), float(ms[i])) for i, k in enumerate(PROFILE_CLASSES)}
 

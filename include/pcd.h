@@ -197,17 +197,32 @@ int pcd_plan_result_floats(const pcd_plan* p);
  * pcd_plan_result_floats(p) floats.  Only enqueues (no synchronisation). */
 int pcd_score_plan_device(pcd_model* m, const pcd_cache* cache, const pcd_plan* p, float* result_device);
 
+/* Single-pass request (the stephanj README's single-pass mode): the prefix
+ * ids[0..n) and every field's branch rows run in ONE forward pass -- each
+ * layer writes the prefix keys/values and the branch rows attend to them in
+ * the same layer -- so the weights stream once per request instead of twice.
+ * The results equal pcd_prefill + pcd_score's (same arithmetic, rows
+ * batched differently).  `cache_out` (nullable) receives the prefix cache for
+ * later pcd_score / pcd_prefill_extend calls.  Synchronises the model
+ * stream. */
+int pcd_prefill_score(pcd_model* m, const int32_t* ids, int n, const pcd_field* fields, int n_fields,
+                      pcd_field_result* out, pcd_stats* stats, pcd_cache** cache_out);
+/* Same with device-resident ids and a compiled plan; only enqueues. */
+int pcd_prefill_score_plan_device(pcd_model* m, const int32_t* ids_device, int n, const pcd_plan* plan,
+                                  float* result_device, pcd_cache** cache_out);
+
 /* Waits for the model stream; reports a device-side failure recorded since
  * the last pcd_sync (PCD_ERR_DEVICE_TIMEOUT, PCD_ERR_TOKEN_RANGE). */
 int pcd_sync(pcd_model* m);
 
 /* ---------------------------------------------------------- instrumentation */
 /* Per-kernel-class timing: when enabled, every launch is bracketed by CUDA
- * events on the model stream.  Classes: 0 prefill GEMMs, 1 branch GEMMs,
- * 2 prefill attention, 3 branch attention, 4 fused readout, 5 other.
+ * events on the model stream (and passes run as direct launches, not
+ * graphs).  Classes: 0 prefill GEMMs, 1 branch GEMMs, 2 prefill attention,
+ * 3 branch attention, 4 fused readout, 5 other, 6 single-pass GEMMs.
  * pcd_profile_read synchronises, returns per class the launch count and the
  * summed milliseconds, and resets the counters. */
-#define PCD_PROF_CLASSES 6
+#define PCD_PROF_CLASSES 7
 int pcd_profile_enable(pcd_model* m, int on);
 int pcd_profile_read(pcd_model* m, int* launches, float* ms);
 

@@ -50,6 +50,15 @@ def test_config2_triage_full(qwen):
     # split-K partial sums land in a run-dependent order, so the two runs agree
     # to rounding amplified through the layers, and each agrees with the oracle
     compare_request(dev, ref, "config 2, device plan path")
+    # the single-pass request (prefix and branches in one forward pass)
+    sp = pcd.pcd_prefill_score(model, req.prefix, req.fields)
+    print("config 2 single pass worst errors", compare_request(sp, ref, "config 2, single pass"))
+    c3 = pcd.pcd_prefill_score_plan_device(model, torch.tensor(req.prefix, dtype=torch.int32, device="cuda"), plan,
+                                           out, keep_cache=True)
+    pcd.pcd_sync(model)
+    assert c3.length == len(req.prefix)
+    compare_request(pcd.unpack_plan_result(out.cpu().numpy(), [len(f.labels) for f in req.fields]), ref,
+                    "config 2, single pass device plan")
 
 
 def test_config3_router(qwen):

@@ -154,3 +154,22 @@ def test_long_prefix_split_attention(pcd, model, tiny_oracle, prefix_len):
     cache = pcd.pcd_prefill(model, req.prefix)
     got = pcd.pcd_score(model, cache, req.fields)
     compare_request(got, _oracle_results(tiny_oracle, req), f"prefix {prefix_len}")
+
+
+@pytest.mark.parametrize("seed,prefix_len,specs", [
+    (1, None, None),                                                         # the reference workload
+    (12, 200, [("enum", 7, 1, 5), ("shared", 9, 2, 6), ("bool",)]),
+    (13, 77, [("router", 255)]),
+    (16, 700, [("bool",), ("line_id", 30), ("scaffold", 2), ("enum", 4, 1, 4)]),   # split prefix attention
+    (17, 1, [("scaffold", 1), ("bool",)]),
+])
+def test_single_pass_matches_oracle(pcd, model, tiny_oracle, request1, seed, prefix_len, specs):
+    """Prefix and branches in one forward pass (README single-pass mode)."""
+    req = request1 if specs is None else make_custom(seed, 512, prefix_len, specs)
+    got, cache = pcd.pcd_prefill_score(model, req.prefix, req.fields, keep_cache=True)
+    compare_request(got, _oracle_results(tiny_oracle, req), f"single pass {seed}")
+    # the prefix cache it leaves behind is the prefill's
+    again = pcd.pcd_score(model, cache, req.fields)
+    for a, b in zip(got, again):
+        assert a.label == b.label
+        np.testing.assert_allclose(a.logprobs, b.logprobs, atol=2e-3)
