@@ -261,7 +261,7 @@ int with_graph(pcd_model* m, const std::vector<int64_t>& key, Fn&& record) {
 //   EPI_F32_STORE  out = (zeroed + atomics when split)
 //   EPI_SWIGLU / EPI_BF16: one K split
 int gemm(pcd_model* m, int cls, const void* A, int M, int lda, const act_t* B, int N, int ldb, int K, int epi, void* out,
-         int ldo, const void* A_lo = nullptr, void* out_lo = nullptr) {
+         int ldo, const void* A_lo = nullptr, void* out_lo = nullptr, int lo_row0 = 0) {
   if (M <= 0) return PCD_OK;
   const bool splittable = (epi == pcd::EPI_F32_ADD || epi == pcd::EPI_F32_STORE);
   const int key_epi = splittable ? pcd::EPI_F32_ATOMIC : epi;
@@ -284,12 +284,64 @@ int gemm(pcd_model* m, int cls, const void* A, int M, int lda, const act_t* B, i
     // consumer, so split-K partial sums can be added with atomics
     run_epi = pcd::EPI_F32_ATOMIC;
   }
-  pcd::GemmShape s{A, M, lda, B, N, ldb, K, A_lo};
+  pcd::GemmShape s{A, M, lda, B, N, ldb, K, A_lo, lo_row0};
   pcd::EpiArgs e;
   e.out = out;
   e.ldo = ldo;
   e.out_lo = out_lo;
   PCD_LAUNCH(timed(m, cls, [&] { return pcd::launch_gemm(s, run_epi, e, t, m->stream, m->d_err, m->wait_ns, m->sms); }));
+  return PCD_OK;
+}
+
+// The q/k/v projection with the rotary embedding applied in its epilogue
+// (head dim 128): q to `q`, keys/values of rows < split_row to destination 0
+// and of the rest to destination 1 (see EpiArgs).
+struct KVDest {
+  act_t* k;
+  act_t* v;
+  int64_t stride;
+  int row0;
+  int pos_base;
+  const int32_t* rel;
+};
+int gemm_qkv_rope(pcd_model* m, int cls, const act_t* A, int M, const act_t* W, const act_t* A_lo, int lo_row0,
+                  act_t* q, int split_row, const KVDest& d0, const KVDest& d1) {
+  if (M <= 0) return PCD_OK;
+  auto key = std::make_tuple(M, m->Nqkv, m->d, pcd::EPI_QKV_ROPE + (A_lo ? 100 : 0));
+  auto it = m->tilings.find(key);
+  pcd::GemmTiling t;
+  if (it == m->tilings.end()) {
+    t = pcd::choose_tiling(M, m->Nqkv, m->d, pcd::EPI_QKV_ROPE, m->sms);
+    t.splits = 1;
+    if (A_lo) {
+      t.mt = 1;
+      t.cs = 1;
+    }
+    m->tilings[key] = t;
+  } else {
+    t = it->second;
+  }
+  pcd::GemmShape s{A, M, m->d, W, m->Nqkv, m->d, m->d, A_lo, lo_row0};
+  pcd::EpiArgs e;
+  e.q_out = q;
+  e.n_q_heads = m->Hq;
+  e.n_kv_heads = m->Hkv;
+  e.rope_cs = m->rope;
+  e.max_pos = m->max_pos;
+  e.split_row = split_row;
+  const KVDest* ds[2] = {&d0, &d1};
+  for (int i = 0; i < 2; ++i) {
+    e.kv_k[i] = ds[i]->k;
+    e.kv_v[i] = ds[i]->v;
+    e.kv_stride[i] = ds[i]->stride;
+    e.kv_row0[i] = ds[i]->row0;
+    e.pos_base[i] = ds[i]->pos_base;
+    e.pos_rel[i] = ds[i]->rel;
+  }
+  e.err = m->d_err;
+  PCD_LAUNCH(timed(m, cls, [&] {
+    return pcd::launch_gemm(s, pcd::EPI_QKV_ROPE, e, t, m->stream, m->d_err, m->wait_ns, m->sms);
+  }));
   return PCD_OK;
 }
 
@@ -357,6 +409,10 @@ int record_prefill(pcd_model* m, const int32_t* d_ids, int n, pcd_cache* c, int 
     PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
       return pcd::launch_rmsnorm(x, m->d, nullptr, n, m->d, W.attn_norm, m->cfg.rms_eps, xn, m->d, m->stream, xlo);
     }));
+    if (m->dh == 128) {
+      const KVDest d0{c->k + l * layer_kv, c->v + l * layer_kv, c->cap, p0, p0, nullptr};
+      PCD_TRY(gemm_qkv_rope(m, PROF_GEMM_PREFILL, xn, n, W.wqkv, xlo, 0, q, n, d0, d0));
+    } else {
     PCD_TRY(gemm(m, PROF_GEMM_PREFILL, xn, n, m->d, W.wqkv, m->Nqkv, m->d, m->d, pcd::EPI_F32_STORE, qkv, m->Nqkv, xlo));
     pcd::RopeArgs ra;
     ra.qkv = qkv;
@@ -377,6 +433,7 @@ int record_prefill(pcd_model* m, const int32_t* d_ids, int n, pcd_cache* c, int 
     ra.err = m->d_err;
     ra.clear_qkv = 1;
     PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_rope_kv(ra, m->stream); }));
+    }
     // The last layer's attention output and MLP change no cached key or value.
     if (l == m->L - 1) break;
     pcd::AttnArgs aa{};
@@ -503,6 +560,10 @@ int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_se
     PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
       return pcd::launch_rmsnorm(x, m->d, nullptr, T, m->d, W.attn_norm, m->cfg.rms_eps, xn, m->d, m->stream, xlo);
     }));
+    if (m->dh == 128 && n_seg == 1) {
+      const KVDest d1{kb, vb, T, 0, segs[0].c->len, p.rel};
+      PCD_TRY(gemm_qkv_rope(m, PROF_GEMM_BRANCH, xn, T, W.wqkv, xlo, 0, q, 0, d1, d1));
+    } else {
     PCD_TRY(gemm(m, PROF_GEMM_BRANCH, xn, T, m->d, W.wqkv, m->Nqkv, m->d, m->d, pcd::EPI_F32_STORE, qkv, m->Nqkv, xlo));
     for (int s = 0; s < n_seg; ++s) {
       const Segment& sg = segs[s];
@@ -527,6 +588,7 @@ int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_se
       ra.err = m->d_err;
       ra.clear_qkv = 1;
       PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_rope_kv(ra, m->stream); }));
+    }
     }
     for (int s = 0; s < n_seg; ++s) {
       const Segment& sg = segs[s];
@@ -695,7 +757,13 @@ int record_single(pcd_model* m, const PlanView& p, const int32_t* ids, int n, pc
     PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
       return pcd::launch_rmsnorm(x, m->d, nullptr, N, m->d, W.attn_norm, m->cfg.rms_eps, xn, m->d, m->stream, xlo);
     }));
-    PCD_TRY(gemm(m, PROF_GEMM_SINGLE, xn, N, m->d, W.wqkv, m->Nqkv, m->d, m->d, pcd::EPI_F32_STORE, qkv, m->Nqkv, xlo));
+    if (m->dh == 128) {
+      // RoPE in the projection's epilogue: prefix rows -> the cache, branch rows -> the branch scratch
+      const KVDest d0{c->k + l * layer_kv, c->v + l * layer_kv, c->cap, 0, 0, nullptr};
+      const KVDest d1{kb, vb, T, 0, n, p.rel};
+      PCD_TRY(gemm_qkv_rope(m, PROF_GEMM_SINGLE, xn, N, W.wqkv, xlo, n, q, n, d0, d1));
+    } else {
+    PCD_TRY(gemm(m, PROF_GEMM_SINGLE, xn, N, m->d, W.wqkv, m->Nqkv, m->d, m->d, pcd::EPI_F32_STORE, qkv, m->Nqkv, xlo, nullptr, n));
     // RoPE: prefix rows -> the cache; branch rows -> the branch scratch
     pcd::RopeArgs ra;
     ra.ldqkv = m->Nqkv;
@@ -726,6 +794,7 @@ int record_single(pcd_model* m, const PlanView& p, const int32_t* ids, int n, pc
     ra.kv_head_stride = T;
     ra.kv_row0 = 0;
     PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_rope_kv(ra, m->stream); }));
+    }
     // prefix attention (causal); not needed in the last layer
     if (!last) {
       pcd::AttnArgs aa{};
@@ -820,7 +889,8 @@ int record_single(pcd_model* m, const PlanView& p, const int32_t* ids, int n, pc
       return pcd::launch_rmsnorm(off(x, r0, m->d), m->d, nullptr, M, m->d, W.mlp_norm, m->cfg.rms_eps, xn, m->d,
                                  m->stream, xlo);
     }));
-    PCD_TRY(gemm(m, PROF_GEMM_SINGLE, xn, M, m->d, W.wgu, 2 * m->Fp, m->d, m->d, pcd::EPI_SWIGLU, hb, m->Fp, xlo, hb_lo));
+    PCD_TRY(gemm(m, PROF_GEMM_SINGLE, xn, M, m->d, W.wgu, 2 * m->Fp, m->d, m->d, pcd::EPI_SWIGLU, hb, m->Fp, xlo, hb_lo,
+                 n - r0));
     PCD_TRY(gemm(m, PROF_GEMM_SINGLE, hb, M, m->Fp, W.wd, m->d, m->Fp, m->Fp, pcd::EPI_F32_ADD, off(x, r0, m->d), m->d,
                  hb_lo));
   }

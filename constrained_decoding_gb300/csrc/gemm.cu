@@ -35,6 +35,7 @@ struct GemmParams {
   uint64_t wait_ns;
   int* err;
   int b_evict_first;  // B is read by one M group only: stream it past L2
+  int lo_row0;        // ALO: tiles entirely below this row have no low half
 };
 
 template <int MT, int BN, bool ALO = false>
@@ -144,6 +145,65 @@ __device__ __forceinline__ void epi_chunk(const GemmParams& p, const EpiArgs& e,
   }
 }
 
+// Fused q/k/v epilogue: for each 128-wide head of the tile, the thread (one
+// token row) rotates the pairs (i, i + 64) by the row's rotary angle
+// (rotate-half pairing; cos/sin from a double-precision table) and writes q,
+// or k and v, in fp16 straight to their destinations.
+template <int BN>
+__device__ __forceinline__ void epi_qkv_rope(const GemmParams& p, const EpiArgs& e, int row, int nt, uint32_t t_row) {
+  const bool valid = row < p.M;
+  const int dst = row >= e.split_row ? 1 : 0;
+  const int r2 = row - (dst ? e.split_row : 0);
+  int pos = 0;
+  if (valid) {
+    pos = e.pos_base[dst] + (e.pos_rel[dst] ? e.pos_rel[dst][r2] : r2);
+    if (pos < 0 || pos >= e.max_pos) {
+      record_error(e.err, DEV_BAD_INDEX);
+      pos = 0;
+    }
+  }
+  const float2* cs = e.rope_cs + static_cast<size_t>(pos) * 64;
+#pragma unroll 1
+  for (int hh = 0; hh < BN / 128; ++hh) {
+    const int head = (nt * BN) / 128 + hh;
+    if (head * 128 >= p.N) break;  // uniform across the warp
+    const bool is_v = head >= e.n_q_heads + e.n_kv_heads;
+    act_t* out;
+    if (head < e.n_q_heads) {
+      out = e.q_out + static_cast<size_t>(row) * e.n_q_heads * 128 + head * 128;
+    } else {
+      const int kh = is_v ? head - e.n_q_heads - e.n_kv_heads : head - e.n_q_heads;
+      act_t* base = is_v ? e.kv_v[dst] : e.kv_k[dst];
+      out = base + (static_cast<size_t>(kh) * e.kv_stride[dst] + e.kv_row0[dst] + r2) * 128;
+    }
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+      float a[32], b[32];
+      tmem_ld_32cols(t_row + hh * 128 + half * 32, a);
+      tmem_ld_32cols(t_row + hh * 128 + 64 + half * 32, b);
+      if (!valid) continue;
+      if (!is_v) {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float2 c = cs[half * 32 + j];
+          const float x1 = a[j], x2 = b[j];
+          a[j] = x1 * c.x - x2 * c.y;
+          b[j] = x2 * c.x + x1 * c.y;
+        }
+      }
+      uint4* o1 = reinterpret_cast<uint4*>(out + half * 32);
+      uint4* o2 = reinterpret_cast<uint4*>(out + 64 + half * 32);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        o1[j] = make_uint4(pack2(a[8 * j], a[8 * j + 1]), pack2(a[8 * j + 2], a[8 * j + 3]), pack2(a[8 * j + 4], a[8 * j + 5]),
+                           pack2(a[8 * j + 6], a[8 * j + 7]));
+        o2[j] = make_uint4(pack2(b[8 * j], b[8 * j + 1]), pack2(b[8 * j + 2], b[8 * j + 3]), pack2(b[8 * j + 4], b[8 * j + 5]),
+                           pack2(b[8 * j + 6], b[8 * j + 7]));
+      }
+    }
+  }
+}
+
 // ALO: A is given as two fp16 matrices, hi and lo (hi + lo carries ~22 bits of
 // the activation); both are multiplied by the same B tile into one
 // accumulator, so the weights are read once.
@@ -226,7 +286,10 @@ __global__ void __launch_bounds__(192, 1)
         decode_unit(p, u, nt, mg, ks);
         const int kb0 = ks * p.nkb / p.k_splits, kb1 = (ks + 1) * p.nkb / p.k_splits;
         const int mt_valid = valid_tiles(mg);
-        const uint32_t bytes = C::A_PARTS * mt_valid * C::A_BYTES + C::B_BYTES;
+        int lo_tiles = 0;
+        if constexpr (ALO)
+          for (int mt = 0; mt < mt_valid; ++mt) lo_tiles += ((tile0(mg) + mt + 1) * 128 > p.lo_row0) ? 1 : 0;
+        const uint32_t bytes = (mt_valid + lo_tiles) * C::A_BYTES + C::B_BYTES;
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns)) {
             record_error(p.err, DEV_WAIT_TIMEOUT_PRODUCER);
@@ -238,7 +301,8 @@ __global__ void __launch_bounds__(192, 1)
           for (int mt = 0; mt < mt_valid; ++mt) {
             tma_load_2d(base + mt * C::A_BYTES, &tmA, &full[stage], kb * 64, (tile0(mg) + mt) * 128);
             if constexpr (ALO)
-              tma_load_2d(base + (MT + mt) * C::A_BYTES, &tmA2, &full[stage], kb * 64, (tile0(mg) + mt) * 128);
+              if ((tile0(mg) + mt + 1) * 128 > p.lo_row0)
+                tma_load_2d(base + (MT + mt) * C::A_BYTES, &tmA2, &full[stage], kb * 64, (tile0(mg) + mt) * 128);
           }
           uint8_t* bdst = base + C::A_PARTS * MT * C::A_BYTES;
           if constexpr (CS == 1) {
@@ -303,6 +367,7 @@ __global__ void __launch_bounds__(192, 1)
                        sdesc_kmajor_sw128(b_base + k * 32), IDESC, (kb > kb0 || k > 0) ? 1u : 0u);
             }
             if constexpr (ALO) {
+              if ((tile0(mg) + mt + 1) * 128 > p.lo_row0)
 #pragma unroll
               for (int k = 0; k < 4; ++k)
                 umma_f16(d_base + mt * BN, sdesc_kmajor_sw128(a_base + (MT + mt) * C::A_BYTES + k * 32),
@@ -353,12 +418,16 @@ __global__ void __launch_bounds__(192, 1)
         const int row = tile * 128 + q * 32 + lane;
         const uint32_t t_row = tbase + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS + mt * BN;
         float run_m = -INFINITY, run_s = 0.f;
-        for (int c = 0; c < BN / 32; ++c) {
-          const int col0 = nt * BN + c * 32;
-          if (col0 >= p.N) break;  // uniform across the warp
-          float v[32];
-          tmem_ld_32cols(t_row + c * 32, v);
-          epi_chunk<EPI>(p, e, row, col0, v, run_m, run_s);
+        if constexpr (EPI == EPI_QKV_ROPE) {
+          epi_qkv_rope<BN>(p, e, row, nt, t_row);
+        } else {
+          for (int c = 0; c < BN / 32; ++c) {
+            const int col0 = nt * BN + c * 32;
+            if (col0 >= p.N) break;  // uniform across the warp
+            float v[32];
+            tmem_ld_32cols(t_row + c * 32, v);
+            epi_chunk<EPI>(p, e, row, col0, v, run_m, run_s);
+          }
         }
         if constexpr (EPI == EPI_READOUT) {
           if (row < p.M) e.part[static_cast<size_t>(nt) * p.M + row] = make_float2(run_m, run_s);
@@ -514,7 +583,7 @@ static int dispatch_tiling(const GemmTiling& t, const CUtensorMap& ma, const CUt
                            const GemmParams& p, const EpiArgs& e, cudaStream_t st, int sms) {
   if (ma2) {  // hi + lo A: one 128-row tile per CTA, no cluster
     if constexpr (EPI == EPI_F32_STORE || EPI == EPI_F32_ADD || EPI == EPI_F32_ATOMIC || EPI == EPI_SWIGLU ||
-                  EPI == EPI_READOUT) {
+                  EPI == EPI_READOUT || EPI == EPI_QKV_ROPE) {
       if (t.mt == 1 && t.cs == 1 && t.bn == 128) return launch_t<1, 128, EPI, 1, true>(ma, mb, *ma2, p, e, st, sms);
       if (t.mt == 1 && t.cs == 1 && t.bn == 256) return launch_t<1, 256, EPI, 1, true>(ma, mb, *ma2, p, e, st, sms);
     }
@@ -555,6 +624,7 @@ int launch_gemm(const GemmShape& s, int epi, const EpiArgs& e, const GemmTiling&
   p.wait_ns = wait_ns;
   p.err = dev_err;
   p.b_evict_first = (p.n_mgroups == 1 && t.mt * t.cs * 128 >= M) ? 1 : 0;
+  p.lo_row0 = s.lo_row0;
   CUtensorMap ma, mb, ma2;
   if (!make_map(&ma, s.a, M, K, s.a_ld, 128)) return -1;
   if (s.a_lo && !make_map(&ma2, s.a_lo, M, K, s.a_ld, 128)) return -1;
@@ -567,6 +637,9 @@ int launch_gemm(const GemmShape& s, int epi, const EpiArgs& e, const GemmTiling&
     case EPI_SWIGLU: return dispatch_tiling<EPI_SWIGLU>(t, ma, mb, pa2, p, e, stream, sms);
     case EPI_READOUT: return dispatch_tiling<EPI_READOUT>(t, ma, mb, pa2, p, e, stream, sms);
     case EPI_F32_STORE: return dispatch_tiling<EPI_F32_STORE>(t, ma, mb, pa2, p, e, stream, sms);
+    case EPI_QKV_ROPE:
+      if (t.splits != 1 || t.bn % 128 || N % 128) return -1;
+      return dispatch_tiling<EPI_QKV_ROPE>(t, ma, mb, pa2, p, e, stream, sms);
   }
   return -1;
 }

@@ -2,10 +2,13 @@
 // 16-bit, both K-contiguous, fp32 accumulation in tensor memory, and one of a
 // few fused epilogues.
 #pragma once
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
 
 namespace pcd {
+
+using act_t_storage = __half;
 
 enum EpiKind : int {
   EPI_BF16 = 0,        // out 16-bit [M][ldo] = D
@@ -14,6 +17,8 @@ enum EpiKind : int {
   EPI_SWIGLU = 3,      // D columns (2f, 2f+1) = (gate_f, up_f); out 16-bit [M][ldo]: silu(gate) * up
   EPI_READOUT = 4,     // vocabulary readout: per (row, N tile) max and sum-exp, plus gathered logits
   EPI_F32_STORE = 5,   // out f32 [M][ldo] = D (one K split)
+  EPI_QKV_ROPE = 6,    // q/k/v projection (head dim 128): rotary embedding applied, q to q_out, k/v to
+                       // the cache (rows < split_row) or the branch scratch (rows >= split_row)
 };
 
 struct GemmShape {
@@ -21,6 +26,7 @@ struct GemmShape {
   const void* b; int b_rows; int b_ld;   // B: b_rows x K
   int K;
   const void* a_lo = nullptr;            // optional low half of A (same layout): D = (A + A_lo) . B^T
+  int lo_row0 = 0;                       // 128-row tiles entirely below this row skip the low half
 };
 
 struct EpiArgs {
@@ -31,6 +37,19 @@ struct EpiArgs {
   const int* gather_off = nullptr;  // EPI_READOUT: [n_tiles_n + 1] CSR over gather entries
   const int4* gather = nullptr;   // EPI_READOUT: (column in tile, row, output index, 0)
   float* z_out = nullptr;         // EPI_READOUT: gathered logits
+  // EPI_QKV_ROPE: D columns are Hq query heads, then Hkv key heads, then Hkv value heads of 128
+  act_t_storage* q_out = nullptr;  // [M][Hq * 128]
+  int n_q_heads = 0, n_kv_heads = 0;
+  const float2* rope_cs = nullptr;  // [max_pos][64] (cos, sin)
+  int max_pos = 0;
+  int split_row = 0;              // rows < split_row use destination 0, the rest destination 1
+  act_t_storage* kv_k[2] = {nullptr, nullptr};  // key of (head h, row r') at kv_k[d] + (h * kv_stride[d] + kv_row0[d] + r') * 128
+  act_t_storage* kv_v[2] = {nullptr, nullptr};
+  int64_t kv_stride[2] = {0, 0};
+  int kv_row0[2] = {0, 0};
+  int pos_base[2] = {0, 0};       // position = pos_base[d] + (pos_rel[d] ? pos_rel[d][r'] : r'), r' = row - (d ? split_row : 0)
+  const int32_t* pos_rel[2] = {nullptr, nullptr};
+  int* err = nullptr;
 };
 
 struct GemmTiling {
