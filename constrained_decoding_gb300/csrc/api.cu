@@ -136,9 +136,9 @@ struct pcd_model {
   bool graphs = true;
   bool own_stream = false;
   // which fp16 GEMM inputs also carry their rounding remainder (hi + lo):
-  // 1 branch-pass normalised inputs, 2 prefill normalised inputs, 4 branch
-  // attention and SwiGLU outputs, 8 prefill attention and SwiGLU outputs,
-  // 16 the readout rows
+  // 1 branch rows' QKV input, 32 branch rows' gate/up input, 2 prefill
+  // normalised inputs, 4 branch attention and SwiGLU outputs, 8 prefill
+  // attention and SwiGLU outputs, 16 the readout rows
   int split_act = 1;
   std::map<std::vector<int64_t>, std::pair<uint64_t, cudaGraphExec_t>> graph_cache;
 };
@@ -542,8 +542,10 @@ int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_se
   act_t* att = static_cast<act_t*>(m->att.p);
   act_t* hb = static_cast<act_t*>(m->hb.p);
   // the branch rows carry their normalised activations as fp16 hi + lo into
-  // the QKV and gate/up projections: the readout is most sensitive to them
+  // the QKV (and optionally gate/up) projections: the readout is most
+  // sensitive to them
   act_t* xlo = (m->split_act & 1) ? static_cast<act_t*>(m->xn_lo.p) : nullptr;
+  act_t* xlo_m = (m->split_act & 32) ? static_cast<act_t*>(m->xn_lo.p) : nullptr;
   const bool split_out = (m->split_act & 4) != 0;
   act_t* att_lo = split_out ? static_cast<act_t*>(m->att_lo.p) : nullptr;
   act_t* hb_lo = split_out ? static_cast<act_t*>(m->hb_lo.p) : nullptr;
@@ -639,9 +641,9 @@ int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_se
     PCD_TRY(gemm(m, PROF_GEMM_BRANCH, att, T, m->qdim, W.wo, m->d, m->qdim, m->qdim, pcd::EPI_F32_ADD, x, m->d,
                  att_lo));
     PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
-      return pcd::launch_rmsnorm(x, m->d, nullptr, T, m->d, W.mlp_norm, m->cfg.rms_eps, xn, m->d, m->stream, xlo);
+      return pcd::launch_rmsnorm(x, m->d, nullptr, T, m->d, W.mlp_norm, m->cfg.rms_eps, xn, m->d, m->stream, xlo_m);
     }));
-    PCD_TRY(gemm(m, PROF_GEMM_BRANCH, xn, T, m->d, W.wgu, 2 * m->Fp, m->d, m->d, pcd::EPI_SWIGLU, hb, m->Fp, xlo,
+    PCD_TRY(gemm(m, PROF_GEMM_BRANCH, xn, T, m->d, W.wgu, 2 * m->Fp, m->d, m->d, pcd::EPI_SWIGLU, hb, m->Fp, xlo_m,
                  hb_lo));
     PCD_TRY(gemm(m, PROF_GEMM_BRANCH, hb, T, m->Fp, W.wd, m->d, m->Fp, m->Fp, pcd::EPI_F32_ADD, x, m->d, hb_lo));
   }
@@ -735,6 +737,7 @@ int record_single(pcd_model* m, const PlanView& p, const int32_t* ids, int n, pc
   act_t* att = static_cast<act_t*>(m->att.p);
   act_t* hb = static_cast<act_t*>(m->hb.p);
   act_t* xlo = (m->split_act & 1) ? static_cast<act_t*>(m->xn_lo.p) : nullptr;
+  act_t* xlo_m = (m->split_act & 32) ? static_cast<act_t*>(m->xn_lo.p) : nullptr;
   const bool split_out = (m->split_act & 4) != 0;
   act_t* att_lo = split_out ? static_cast<act_t*>(m->att_lo.p) : nullptr;
   act_t* hb_lo = split_out ? static_cast<act_t*>(m->hb_lo.p) : nullptr;
@@ -887,9 +890,9 @@ int record_single(pcd_model* m, const PlanView& p, const int32_t* ids, int n, pc
                  pcd::EPI_F32_ADD, off(x, r0, m->d), m->d, att_lo ? off(att_lo, r0, m->qdim) : nullptr));
     PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
       return pcd::launch_rmsnorm(off(x, r0, m->d), m->d, nullptr, M, m->d, W.mlp_norm, m->cfg.rms_eps, xn, m->d,
-                                 m->stream, xlo);
+                                 m->stream, xlo_m);
     }));
-    PCD_TRY(gemm(m, PROF_GEMM_SINGLE, xn, M, m->d, W.wgu, 2 * m->Fp, m->d, m->d, pcd::EPI_SWIGLU, hb, m->Fp, xlo, hb_lo,
+    PCD_TRY(gemm(m, PROF_GEMM_SINGLE, xn, M, m->d, W.wgu, 2 * m->Fp, m->d, m->d, pcd::EPI_SWIGLU, hb, m->Fp, xlo_m, hb_lo,
                  n - r0));
     PCD_TRY(gemm(m, PROF_GEMM_SINGLE, hb, M, m->Fp, W.wd, m->d, m->Fp, m->Fp, pcd::EPI_F32_ADD, off(x, r0, m->d), m->d,
                  hb_lo));
