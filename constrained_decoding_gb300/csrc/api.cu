@@ -92,6 +92,11 @@ struct PlanView {
       *gather_off;
   const float* temp;
   const int4* gather;
+  // tree-attention tiles over the branch tokens (tpt whole tokens each)
+  int tpt = 1, n_br_tiles = 0, max_tile_chunks = 0;
+  const int32_t* tile_chunk_off;
+  const int32_t* tile_keys;
+  const unsigned long long* tile_mask;
   int result_floats() const { return n_fields * 8 + 2 * n_labels; }
 };
 
@@ -140,6 +145,8 @@ struct pcd_model {
   // normalised inputs, 4 branch attention and SwiGLU outputs, 8 prefill
   // attention and SwiGLU outputs, 16 the readout rows
   int split_act = 1;
+  // one tree-attention launch per layer (else split attention + merge launches)
+  bool tree_attn = true;
   std::map<std::vector<int64_t>, std::pair<uint64_t, cudaGraphExec_t>> graph_cache;
 };
 
@@ -531,6 +538,29 @@ int run_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_seg, 
   return with_graph(m, key, [&] { return record_branch(m, p, segs, n_seg, d_result, splits, nullptr); });
 }
 
+// Tree-attention arguments common to both passes: the branch queries of plan
+// `p` (at rows br_row0.. of q and out) and their ancestor tiles.
+pcd::TreeAttnArgs tree_args(const pcd_model* m, const PlanView& p, const act_t* q, act_t* out, act_t* out_lo,
+                            float scale_log2) {
+  pcd::TreeAttnArgs ta{};
+  ta.q = q;
+  ta.out = out;
+  ta.out_lo = out_lo;
+  ta.ld_out = m->qdim;
+  ta.Hq = m->Hq;
+  ta.Hkv = m->Hkv;
+  ta.DH = m->dh;
+  ta.tpt = p.tpt;
+  ta.n_br = p.T;
+  ta.n_br_tiles = p.n_br_tiles;
+  ta.tile_chunk_off = p.tile_chunk_off;
+  ta.tile_keys = p.tile_keys;
+  ta.tile_mask = p.tile_mask;
+  ta.scale_log2 = scale_log2;
+  ta.csk = 1;
+  return ta;
+}
+
 int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_seg, float* d_result, int splits,
                   cudaEvent_t ev_mid) {
   const int T = p.T, R = p.R, G = m->G;
@@ -592,6 +622,19 @@ int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_se
       PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_rope_kv(ra, m->stream); }));
     }
     }
+    if (m->tree_attn && n_seg == 1) {
+      const pcd_cache* c = segs[0].c;
+      const size_t layer_kv = static_cast<size_t>(m->Hkv) * c->cap * m->dh;
+      pcd::TreeAttnArgs ta = tree_args(m, p, q, att, att_lo, scale_log2);
+      ta.k = c->k + l * layer_kv;
+      ta.v = c->v + l * layer_kv;
+      ta.kv_head_stride = c->cap;
+      ta.n_keys = c->len;
+      ta.kb = kb;
+      ta.vb = vb;
+      ta.csk = pcd::tree_attention_csk(ta.n_br_tiles, m->Hkv, (c->len + 63) / 64 + p.max_tile_chunks, m->sms);
+      PCD_LAUNCH(timed(m, PROF_ATTN_BRANCH, [&] { return pcd::launch_tree_attention(ta, m->stream); }));
+    } else {
     for (int s = 0; s < n_seg; ++s) {
       const Segment& sg = segs[s];
       const int n = sg.t1 - sg.t0;
@@ -638,6 +681,7 @@ int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_se
     ma.ld_out = m->qdim;
     ma.out_lo = att_lo;
     PCD_LAUNCH(timed(m, PROF_ATTN_BRANCH, [&] { return pcd::launch_branch_merge(ma, m->stream); }));
+    }
     PCD_TRY(gemm(m, PROF_GEMM_BRANCH, att, T, m->qdim, W.wo, m->d, m->qdim, m->qdim, pcd::EPI_F32_ADD, x, m->d,
                  att_lo));
     PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
@@ -798,6 +842,23 @@ int record_single(pcd_model* m, const PlanView& p, const int32_t* ids, int n, pc
     ra.kv_row0 = 0;
     PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_rope_kv(ra, m->stream); }));
     }
+    if (m->tree_attn) {
+      // every query in one launch: prefix rows causal (not needed in the last
+      // layer), branch rows over the prefix and their ancestors
+      pcd::TreeAttnArgs ta = tree_args(m, p, q, att, att_lo, scale_log2);
+      ta.n_pf = last ? 0 : n;
+      ta.n_pf_tiles = (ta.n_pf + p.tpt - 1) / p.tpt;
+      ta.br_row0 = n;
+      ta.k = c->k + l * layer_kv;
+      ta.v = c->v + l * layer_kv;
+      ta.kv_head_stride = c->cap;
+      ta.n_keys = n;
+      ta.kb = kb;
+      ta.vb = vb;
+      ta.csk = pcd::tree_attention_csk(ta.n_br_tiles + ta.n_pf_tiles, m->Hkv, (n + 63) / 64 + p.max_tile_chunks,
+                                       m->sms);
+      PCD_LAUNCH(timed(m, PROF_ATTN_BRANCH, [&] { return pcd::launch_tree_attention(ta, m->stream); }));
+    } else {
     // prefix attention (causal); not needed in the last layer
     if (!last) {
       pcd::AttnArgs aa{};
@@ -884,6 +945,7 @@ int record_single(pcd_model* m, const PlanView& p, const int32_t* ids, int n, pc
       ma.out_lo = att_lo ? off(att_lo, n, m->qdim) : nullptr;
       PCD_LAUNCH(timed(m, PROF_ATTN_BRANCH, [&] { return pcd::launch_branch_merge(ma, m->stream); }));
     }
+    }
     // O-proj and MLP over every row, or only the branch rows in the last layer
     const int r0 = last ? n : 0, M = N - r0;
     PCD_TRY(gemm(m, PROF_GEMM_SINGLE, off(att, r0, m->qdim), M, m->qdim, W.wo, m->d, m->qdim, m->qdim,
@@ -968,6 +1030,40 @@ size_t plan_blob(const pcd_model* m, const pcd::HostPlan& hp, std::vector<int32_
   }
   for (int i = 0; i < v.n_vtiles; ++i) goff[i + 1] += goff[i];
 
+  // tree-attention tiles: tpt whole branch tokens (tpt x G <= 64 query rows);
+  // a tile's ancestor keys are the ascending union of its tokens' ancestor
+  // lists, in chunks of 64, with one visibility bit per (chunk key, token)
+  v.tpt = std::max(1, 64 / std::max(1, m->G));
+  v.n_br_tiles = (hp.T + v.tpt - 1) / v.tpt;
+  v.max_tile_chunks = 0;
+  std::vector<int32_t> tco(v.n_br_tiles + 1, 0), tkeys, tmask;
+  for (int ti = 0; ti < v.n_br_tiles; ++ti) {
+    const int a0 = ti * v.tpt, a1 = std::min(hp.T, a0 + v.tpt);
+    std::vector<int32_t> u;
+    for (int t = a0; t < a1; ++t)
+      u.insert(u.end(), hp.anc_idx.begin() + hp.anc_off[t], hp.anc_idx.begin() + hp.anc_off[t + 1]);
+    std::sort(u.begin(), u.end());
+    u.erase(std::unique(u.begin(), u.end()), u.end());
+    const int nch = (static_cast<int>(u.size()) + 63) / 64;
+    for (int c = 0; c < nch; ++c) {
+      const auto k0 = u.begin() + 64 * c, k1 = u.begin() + std::min<size_t>(u.size(), 64 * (c + 1));
+      for (int i = 0; i < 64; ++i) tkeys.push_back(k0 + i < k1 ? *(k0 + i) : -1);
+      for (int tt = 0; tt < v.tpt; ++tt) {
+        uint64_t mask = 0;
+        const int t = a0 + tt;
+        if (t < a1)
+          for (int x = hp.anc_off[t]; x < hp.anc_off[t + 1]; ++x) {
+            const auto it = std::lower_bound(k0, k1, hp.anc_idx[x]);
+            if (it != k1 && *it == hp.anc_idx[x]) mask |= 1ull << (it - k0);
+          }
+        tmask.push_back(static_cast<int32_t>(static_cast<uint32_t>(mask)));
+        tmask.push_back(static_cast<int32_t>(static_cast<uint32_t>(mask >> 32)));
+      }
+    }
+    tco[ti + 1] = tco[ti] + nch;
+    v.max_tile_chunks = std::max(v.max_tile_chunks, nch);
+  }
+
   blob.clear();
   auto put = [&](const int32_t* src, size_t n) {
     while (blob.size() % 4) blob.push_back(0);
@@ -989,6 +1085,9 @@ size_t plan_blob(const pcd_model* m, const pcd::HostPlan& hp, std::vector<int32_
   v.temp = reinterpret_cast<const float*>(put(reinterpret_cast<const int32_t*>(hp.temp.data()), hp.temp.size()));
   v.gather_off = put(goff.data(), goff.size());
   v.gather = reinterpret_cast<const int4*>(put(g4.data(), g4.size()));
+  v.tile_chunk_off = put(tco.data(), tco.size());
+  v.tile_keys = put(tkeys.data(), tkeys.size());
+  v.tile_mask = reinterpret_cast<const unsigned long long*>(put(tmask.data(), tmask.size()));
   return blob.size() * sizeof(int32_t);
 }
 
@@ -1097,6 +1196,7 @@ int build_model(const pcd_model_config& cfg, TensorFn get, void* ctx, int dtype,
   }
   if (const char* g = std::getenv("PCD_GRAPHS")) m->graphs = std::atoi(g) != 0;
   if (const char* g = std::getenv("PCD_SPLIT_ACT")) m->split_act = std::atoi(g);
+  if (const char* g = std::getenv("PCD_TREE_ATTN")) m->tree_attn = std::atoi(g) != 0;
   m->sms = prop.multiProcessorCount;
   if (const char* w = std::getenv("PCD_WAIT_LIMIT_MS")) m->wait_ns = static_cast<uint64_t>(std::atof(w) * 1e6);
 

@@ -73,6 +73,42 @@ struct MergeArgs {
 };
 int launch_branch_merge(const MergeArgs& a, cudaStream_t s);
 
+// Tree attention: every query of a pass in one launch, normalised output
+// written directly.  Prefix queries are causal (query t sees prefix keys
+// 0..t); branch queries see every prefix key plus their own ancestors in the
+// branch batch (scaffold chain and trie path, themselves included).  Queries
+// are tiled by whole tokens (tpt tokens x G query heads <= 64 rows per tile);
+// a branch tile's ancestor keys are the ascending union of its tokens'
+// ancestor lists, cut into 64-key chunks, with a 64-bit visibility mask per
+// (chunk, token of the tile).  csk CTAs (a thread-block cluster) share one
+// (tile, KV head) and split its key blocks; they combine their partial
+// softmax states through distributed shared memory.
+struct TreeAttnArgs {
+  const act_t* q;               // [rows][Hq][DH]: prefix queries at rows 0..n_pf-1, branch queries at br_row0..
+  act_t* out;                   // out[row][h * DH + d]
+  act_t* out_lo = nullptr;      // optional fp16 rounding remainder of out
+  int ld_out;
+  int Hq, Hkv, DH;
+  int tpt;                      // query tokens per tile
+  int n_pf, n_pf_tiles;         // causal prefix queries
+  int n_br, n_br_tiles, br_row0;
+  const act_t* k;               // this layer's prefix keys: k + (h * kv_head_stride + j) * DH, j < n_keys
+  const act_t* v;
+  int64_t kv_head_stride;
+  int n_keys;
+  const act_t* kb;              // branch keys/values [Hkv][n_br][DH]
+  const act_t* vb;
+  const int32_t* tile_chunk_off;            // [n_br_tiles + 1] ancestor chunks of each branch tile
+  const int32_t* tile_keys;                 // [chunks][64] branch key index, -1 past the union's end
+  const unsigned long long* tile_mask;      // [chunks][tpt] bit i: key i of the chunk is visible to the token
+  float scale_log2;                         // log2(e) / sqrt(DH)
+  int csk;                                  // CTAs (cluster size) per (tile, KV head): 1, 2, 4 or 8
+};
+int launch_tree_attention(const TreeAttnArgs& a, cudaStream_t s);
+// CTAs per (tile, KV head) so that a launch fills the GPU: key blocks of the
+// heaviest tile (max_blocks) bound it.
+int tree_attention_csk(int tiles, int Hkv, int max_blocks, int sms);
+
 // lse[r] = log sum_tiles sum exp(z) from per-tile (max, sum exp(z - max)).
 int launch_lse_combine(const float2* part, int n_tiles, int R, float* lse, cudaStream_t s);
 
