@@ -141,12 +141,15 @@ struct pcd_model {
   bool graphs = true;
   bool own_stream = false;
   // which fp16 GEMM inputs also carry their rounding remainder (hi + lo):
-  // 1 branch rows' QKV input, 32 branch rows' gate/up input, 2 prefill
-  // normalised inputs, 4 branch attention and SwiGLU outputs, 8 prefill
-  // attention and SwiGLU outputs, 16 the readout rows
-  int split_act = 1;
-  // one tree-attention launch per layer (else split attention + merge launches)
+  // 1 branch rows' QKV input, 64 prefix rows' QKV input, 128 every attention
+  // output (the O projection's input), 32 branch rows' gate/up input, 2
+  // prefill normalised inputs, 4 branch attention and SwiGLU outputs, 8
+  // prefill attention and SwiGLU outputs, 16 the readout rows
+  int split_act = 1 | 16 | 64 | 128;
+  // one tree-attention launch per layer (else split attention + merge launches),
+  // on the tcgen05 tensor cores at head dim 128 (else warp-level MMA)
   bool tree_attn = true;
+  bool attn_tc = true;
   std::map<std::vector<int64_t>, std::pair<uint64_t, cudaGraphExec_t>> graph_cache;
 };
 
@@ -291,7 +294,7 @@ int gemm(pcd_model* m, int cls, const void* A, int M, int lda, const act_t* B, i
     // consumer, so split-K partial sums can be added with atomics
     run_epi = pcd::EPI_F32_ATOMIC;
   }
-  pcd::GemmShape s{A, M, lda, B, N, ldb, K, A_lo, lo_row0};
+  pcd::GemmShape s{A, M, lda, B, N, ldb, K, A_lo, lo_row0, true};
   pcd::EpiArgs e;
   e.out = out;
   e.ldo = ldo;
@@ -328,12 +331,12 @@ int gemm_qkv_rope(pcd_model* m, int cls, const act_t* A, int M, const act_t* W, 
   } else {
     t = it->second;
   }
-  pcd::GemmShape s{A, M, m->d, W, m->Nqkv, m->d, m->d, A_lo, lo_row0};
+  pcd::GemmShape s{A, M, m->d, W, m->Nqkv, m->d, m->d, A_lo, lo_row0, true};
   pcd::EpiArgs e;
   e.q_out = q;
   e.n_q_heads = m->Hq;
   e.n_kv_heads = m->Hkv;
-  e.rope_cs = m->rope;
+  e.rope_cs = m->rope + static_cast<size_t>(m->max_pos) * (m->dh / 2);  // the [dh/2][max_pos] copy
   e.max_pos = m->max_pos;
   e.split_row = split_row;
   const KVDest* ds[2] = {&d0, &d1};
@@ -363,10 +366,8 @@ int ensure_workspace(pcd_model* m, int T) {
   PCD_TRY(ensure(m->att, t * m->qdim * 2));
   PCD_TRY(ensure(m->hb, t * m->Fp * 2));
   PCD_TRY(ensure(m->xn_lo, t * m->d * 2));
-  if (m->split_act & (4 | 8)) {
-    PCD_TRY(ensure(m->att_lo, t * m->qdim * 2));
-    PCD_TRY(ensure(m->hb_lo, t * m->Fp * 2));
-  }
+  if (m->split_act & (4 | 8 | 128)) PCD_TRY(ensure(m->att_lo, t * m->qdim * 2));
+  if (m->split_act & (4 | 8)) PCD_TRY(ensure(m->hb_lo, t * m->Fp * 2));
   return PCD_OK;
 }
 
@@ -386,7 +387,7 @@ int prefill_splits(const pcd_model* m, int n, int p0) {
 int run_prefill(pcd_model* m, const int32_t* d_ids, int n, pcd_cache* c, int p0) {
   PCD_TRY(ensure_workspace(m, n));
   const int splits = prefill_splits(m, n, p0);
-  if (splits > 1 || (m->split_act & 8)) {
+  if (splits > 1 || (m->split_act & (8 | 128))) {
     PCD_TRY(ensure(m->part_o, static_cast<size_t>(splits) * m->Hkv * n * m->G * m->dh * 4));
     PCD_TRY(ensure(m->part_ml, static_cast<size_t>(splits) * m->Hkv * n * m->G * 8));
   }
@@ -405,10 +406,11 @@ int record_prefill(pcd_model* m, const int32_t* d_ids, int n, pcd_cache* c, int 
   act_t* q = static_cast<act_t*>(m->q.p);
   act_t* att = static_cast<act_t*>(m->att.p);
   act_t* hb = static_cast<act_t*>(m->hb.p);
-  act_t* xlo = (m->split_act & 2) ? static_cast<act_t*>(m->xn_lo.p) : nullptr;
-  const bool split_out = (m->split_act & 8) != 0;
+  act_t* xlo = (m->split_act & (2 | 64)) ? static_cast<act_t*>(m->xn_lo.p) : nullptr;   // QKV input
+  act_t* xlo_m = (m->split_act & 2) ? static_cast<act_t*>(m->xn_lo.p) : nullptr;        // gate/up input
+  const bool split_out = (m->split_act & (8 | 128)) != 0;
   act_t* att_lo = split_out ? static_cast<act_t*>(m->att_lo.p) : nullptr;
-  act_t* hb_lo = split_out ? static_cast<act_t*>(m->hb_lo.p) : nullptr;
+  act_t* hb_lo = (m->split_act & 8) ? static_cast<act_t*>(m->hb_lo.p) : nullptr;
   const size_t layer_kv = static_cast<size_t>(m->Hkv) * c->cap * m->dh;
   PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_embed(d_ids, n, m->embed, m->d, m->V, x, m->d_err, m->stream); }));
   for (int l = 0; l < m->L; ++l) {
@@ -488,9 +490,9 @@ int record_prefill(pcd_model* m, const int32_t* d_ids, int n, pcd_cache* c, int 
     PCD_TRY(gemm(m, PROF_GEMM_PREFILL, att, n, m->qdim, W.wo, m->d, m->qdim, m->qdim, pcd::EPI_F32_ADD, x, m->d,
                  att_lo));
     PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
-      return pcd::launch_rmsnorm(x, m->d, nullptr, n, m->d, W.mlp_norm, m->cfg.rms_eps, xn, m->d, m->stream, xlo);
+      return pcd::launch_rmsnorm(x, m->d, nullptr, n, m->d, W.mlp_norm, m->cfg.rms_eps, xn, m->d, m->stream, xlo_m);
     }));
-    PCD_TRY(gemm(m, PROF_GEMM_PREFILL, xn, n, m->d, W.wgu, 2 * m->Fp, m->d, m->d, pcd::EPI_SWIGLU, hb, m->Fp, xlo,
+    PCD_TRY(gemm(m, PROF_GEMM_PREFILL, xn, n, m->d, W.wgu, 2 * m->Fp, m->d, m->d, pcd::EPI_SWIGLU, hb, m->Fp, xlo_m,
                  hb_lo));
     PCD_TRY(gemm(m, PROF_GEMM_PREFILL, hb, n, m->Fp, W.wd, m->d, m->Fp, m->Fp, pcd::EPI_F32_ADD, x, m->d, hb_lo));
   }
@@ -502,6 +504,9 @@ struct Segment {
   const pcd_cache* c;
   int t0, t1;  // branch tokens of this request
 };
+
+int tree_tile_rows(const pcd_model* m);
+int launch_tree(pcd_model* m, const pcd::TreeAttnArgs& ta, const pcd_cache* c, int l);
 
 int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_seg, float* d_result, int splits,
                   cudaEvent_t ev_mid);
@@ -576,9 +581,8 @@ int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_se
   // sensitive to them
   act_t* xlo = (m->split_act & 1) ? static_cast<act_t*>(m->xn_lo.p) : nullptr;
   act_t* xlo_m = (m->split_act & 32) ? static_cast<act_t*>(m->xn_lo.p) : nullptr;
-  const bool split_out = (m->split_act & 4) != 0;
-  act_t* att_lo = split_out ? static_cast<act_t*>(m->att_lo.p) : nullptr;
-  act_t* hb_lo = split_out ? static_cast<act_t*>(m->hb_lo.p) : nullptr;
+  act_t* att_lo = (m->split_act & (4 | 128)) ? static_cast<act_t*>(m->att_lo.p) : nullptr;
+  act_t* hb_lo = (m->split_act & 4) ? static_cast<act_t*>(m->hb_lo.p) : nullptr;
   act_t* hr_lo = (m->split_act & 16) ? static_cast<act_t*>(m->hr_lo.p) : nullptr;
   act_t* kb = static_cast<act_t*>(m->kb.p);
   act_t* vb = static_cast<act_t*>(m->vb.p);
@@ -632,8 +636,9 @@ int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_se
       ta.n_keys = c->len;
       ta.kb = kb;
       ta.vb = vb;
-      ta.csk = pcd::tree_attention_csk(ta.n_br_tiles, m->Hkv, (c->len + 63) / 64 + p.max_tile_chunks, m->sms);
-      PCD_LAUNCH(timed(m, PROF_ATTN_BRANCH, [&] { return pcd::launch_tree_attention(ta, m->stream); }));
+      ta.csk = pcd::tree_attention_csk(ta.n_br_tiles, m->Hkv, (c->len + 63) / 64 + p.max_tile_chunks, m->sms,
+                                       tree_tile_rows(m) == 128);
+      PCD_LAUNCH(timed(m, PROF_ATTN_BRANCH, [&] { return launch_tree(m, ta, c, l); }));
     } else {
     for (int s = 0; s < n_seg; ++s) {
       const Segment& sg = segs[s];
@@ -698,7 +703,7 @@ int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_se
   PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
     return pcd::launch_rmsnorm(x, m->d, p.ro_tok, R, m->d, m->final_norm, m->cfg.rms_eps, hr, m->d, m->stream, hr_lo);
   }));
-  pcd::GemmShape rs{hr, R, m->d, m->lm, m->V, m->d, m->d, hr_lo};
+  pcd::GemmShape rs{hr, R, m->d, m->lm, m->V, m->d, m->d, hr_lo, 0, true};
   pcd::GemmTiling ro_t = p.ro_tiling;
   if (hr_lo) {
     ro_t.mt = 1;
@@ -780,11 +785,12 @@ int record_single(pcd_model* m, const PlanView& p, const int32_t* ids, int n, pc
   act_t* q = static_cast<act_t*>(m->q.p);
   act_t* att = static_cast<act_t*>(m->att.p);
   act_t* hb = static_cast<act_t*>(m->hb.p);
-  act_t* xlo = (m->split_act & 1) ? static_cast<act_t*>(m->xn_lo.p) : nullptr;
+  // the QKV input's remainder: branch rows (1), and prefix rows too (64)
+  act_t* xlo = (m->split_act & (1 | 64)) ? static_cast<act_t*>(m->xn_lo.p) : nullptr;
+  const int qkv_lo_row0 = (m->split_act & 64) ? 0 : n;
   act_t* xlo_m = (m->split_act & 32) ? static_cast<act_t*>(m->xn_lo.p) : nullptr;
-  const bool split_out = (m->split_act & 4) != 0;
-  act_t* att_lo = split_out ? static_cast<act_t*>(m->att_lo.p) : nullptr;
-  act_t* hb_lo = split_out ? static_cast<act_t*>(m->hb_lo.p) : nullptr;
+  act_t* att_lo = (m->split_act & (4 | 128)) ? static_cast<act_t*>(m->att_lo.p) : nullptr;
+  act_t* hb_lo = (m->split_act & 4) ? static_cast<act_t*>(m->hb_lo.p) : nullptr;
   act_t* hr_lo = (m->split_act & 16) ? static_cast<act_t*>(m->hr_lo.p) : nullptr;
   act_t* kb = static_cast<act_t*>(m->kb.p);
   act_t* vb = static_cast<act_t*>(m->vb.p);
@@ -808,9 +814,10 @@ int record_single(pcd_model* m, const PlanView& p, const int32_t* ids, int n, pc
       // RoPE in the projection's epilogue: prefix rows -> the cache, branch rows -> the branch scratch
       const KVDest d0{c->k + l * layer_kv, c->v + l * layer_kv, c->cap, 0, 0, nullptr};
       const KVDest d1{kb, vb, T, 0, n, p.rel};
-      PCD_TRY(gemm_qkv_rope(m, PROF_GEMM_SINGLE, xn, N, W.wqkv, xlo, n, q, n, d0, d1));
+      PCD_TRY(gemm_qkv_rope(m, PROF_GEMM_SINGLE, xn, N, W.wqkv, xlo, qkv_lo_row0, q, n, d0, d1));
     } else {
-    PCD_TRY(gemm(m, PROF_GEMM_SINGLE, xn, N, m->d, W.wqkv, m->Nqkv, m->d, m->d, pcd::EPI_F32_STORE, qkv, m->Nqkv, xlo, nullptr, n));
+    PCD_TRY(gemm(m, PROF_GEMM_SINGLE, xn, N, m->d, W.wqkv, m->Nqkv, m->d, m->d, pcd::EPI_F32_STORE, qkv, m->Nqkv, xlo,
+                 nullptr, qkv_lo_row0));
     // RoPE: prefix rows -> the cache; branch rows -> the branch scratch
     pcd::RopeArgs ra;
     ra.ldqkv = m->Nqkv;
@@ -856,8 +863,8 @@ int record_single(pcd_model* m, const PlanView& p, const int32_t* ids, int n, pc
       ta.kb = kb;
       ta.vb = vb;
       ta.csk = pcd::tree_attention_csk(ta.n_br_tiles + ta.n_pf_tiles, m->Hkv, (n + 63) / 64 + p.max_tile_chunks,
-                                       m->sms);
-      PCD_LAUNCH(timed(m, PROF_ATTN_BRANCH, [&] { return pcd::launch_tree_attention(ta, m->stream); }));
+                                       m->sms, tree_tile_rows(m) == 128);
+      PCD_LAUNCH(timed(m, PROF_ATTN_BRANCH, [&] { return launch_tree(m, ta, c, l); }));
     } else {
     // prefix attention (causal); not needed in the last layer
     if (!last) {
@@ -880,7 +887,7 @@ int record_single(pcd_model* m, const PlanView& p, const int32_t* ids, int n, pc
       aa.scale_log2 = scale_log2;
       aa.out = att;
       aa.ld_out = m->qdim;
-      aa.partial = pf_splits > 1 || split_out;
+      aa.partial = pf_splits > 1 || att_lo != nullptr;
       aa.part_o = part_o;
       aa.part_ml = part_ml;
       aa.causal_heavy_first = 1;
@@ -965,7 +972,7 @@ int record_single(pcd_model* m, const PlanView& p, const int32_t* ids, int n, pc
     return pcd::launch_rmsnorm(off(x, n, m->d), m->d, p.ro_tok, R, m->d, m->final_norm, m->cfg.rms_eps, hr, m->d,
                                m->stream, hr_lo);
   }));
-  pcd::GemmShape rs{hr, R, m->d, m->lm, m->V, m->d, m->d, hr_lo};
+  pcd::GemmShape rs{hr, R, m->d, m->lm, m->V, m->d, m->d, hr_lo, 0, true};
   pcd::GemmTiling ro_t = p.ro_tiling;
   if (hr_lo) {
     ro_t.mt = 1;
@@ -1001,6 +1008,23 @@ int record_single(pcd_model* m, const PlanView& p, const int32_t* ids, int n, pc
   return PCD_OK;
 }
 
+// Query rows per tree-attention tile: 128 for the tensor-core kernel, 64 for
+// the warp-MMA one.
+int tree_tile_rows(const pcd_model* m) { return (m->tree_attn && m->attn_tc && m->dh == 128) ? 128 : 64; }
+
+// One tree-attention launch over the prefix cache `c` at layer l.
+int launch_tree(pcd_model* m, const pcd::TreeAttnArgs& ta, const pcd_cache* c, int l) {
+  if (tree_tile_rows(m) == 128) {
+    CUtensorMap mk, mv;
+    const int64_t layer_elems = static_cast<int64_t>(m->Hkv) * c->cap * m->dh;
+    if (!pcd::make_kv_map(&mk, c->k, m->dh, ta.n_keys, m->Hkv, c->cap, m->L, layer_elems) ||
+        !pcd::make_kv_map(&mv, c->v, m->dh, ta.n_keys, m->Hkv, c->cap, m->L, layer_elems))
+      return cudaErrorInvalidValue;
+    return pcd::launch_tree_attention_tc(ta, mk, mv, l, m->wait_ns, m->d_err, m->stream);
+  }
+  return pcd::launch_tree_attention(ta, m->stream);
+}
+
 // ------------------------------------------------------------ plan upload
 // Serialises a host plan into an int32 blob; `view` gets pointers relative to
 // `dev` (the blob's device address).
@@ -1033,7 +1057,7 @@ size_t plan_blob(const pcd_model* m, const pcd::HostPlan& hp, std::vector<int32_
   // tree-attention tiles: tpt whole branch tokens (tpt x G <= 64 query rows);
   // a tile's ancestor keys are the ascending union of its tokens' ancestor
   // lists, in chunks of 64, with one visibility bit per (chunk key, token)
-  v.tpt = std::max(1, 64 / std::max(1, m->G));
+  v.tpt = std::max(1, tree_tile_rows(m) / std::max(1, m->G));
   v.n_br_tiles = (hp.T + v.tpt - 1) / v.tpt;
   v.max_tile_chunks = 0;
   std::vector<int32_t> tco(v.n_br_tiles + 1, 0), tkeys, tmask;
@@ -1197,6 +1221,7 @@ int build_model(const pcd_model_config& cfg, TensorFn get, void* ctx, int dtype,
   if (const char* g = std::getenv("PCD_GRAPHS")) m->graphs = std::atoi(g) != 0;
   if (const char* g = std::getenv("PCD_SPLIT_ACT")) m->split_act = std::atoi(g);
   if (const char* g = std::getenv("PCD_TREE_ATTN")) m->tree_attn = std::atoi(g) != 0;
+  if (const char* g = std::getenv("PCD_ATTN_TC")) m->attn_tc = std::atoi(g) != 0;
   m->sms = prop.multiProcessorCount;
   if (const char* w = std::getenv("PCD_WAIT_LIMIT_MS")) m->wait_ns = static_cast<uint64_t>(std::atof(w) * 1e6);
 
@@ -1308,15 +1333,21 @@ int build_model(const pcd_model_config& cfg, TensorFn get, void* ctx, int dtype,
   stage.clear();
   stage.shrink_to_fit();
 
-  // RoPE table: angle pos * theta^(-2i/dh) in double precision, stored as fp32 (cos, sin)
+  // RoPE table: angle pos * theta^(-2i/dh) in double precision, stored as fp32
+  // (cos, sin) twice: [max_pos][dh/2] for the per-element RoPE kernel, then
+  // [dh/2][max_pos] for the projection epilogue (a thread per row: adjacent
+  // rows read adjacent positions)
   {
     const int half = m->dh / 2;
-    std::vector<float2> cs(static_cast<size_t>(m->max_pos) * half);
+    const size_t n_cs = static_cast<size_t>(m->max_pos) * half;
+    std::vector<float2> cs(2 * n_cs);
     for (int i = 0; i < half; ++i) {
       const double inv = std::pow(static_cast<double>(cfg.rope_theta), -2.0 * i / m->dh);
       for (int pos = 0; pos < m->max_pos; ++pos) {
         const double a = pos * inv;
-        cs[static_cast<size_t>(pos) * half + i] = make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
+        const float2 v = make_float2(static_cast<float>(std::cos(a)), static_cast<float>(std::sin(a)));
+        cs[static_cast<size_t>(pos) * half + i] = v;
+        cs[n_cs + static_cast<size_t>(i) * m->max_pos + pos] = v;
       }
     }
     if (cudaMalloc(&m->rope, cs.size() * sizeof(float2)) != cudaSuccess) {

@@ -19,6 +19,7 @@
 #include <algorithm>
 #include <cstdio>
 #include <cstdlib>
+#include <map>
 #include <mutex>
 #include <tuple>
 #include <unordered_map>
@@ -36,6 +37,7 @@ struct GemmParams {
   int* err;
   int b_evict_first;  // B is read by one M group only: stream it past L2
   int lo_row0;        // ALO: tiles entirely below this row have no low half
+  int b_const;        // B tiles may load before the programmatic dependency wait
 };
 
 template <int MT, int BN, bool ALO = false>
@@ -162,7 +164,7 @@ __device__ __forceinline__ void epi_qkv_rope(const GemmParams& p, const EpiArgs&
       pos = 0;
     }
   }
-  const float2* cs = e.rope_cs + static_cast<size_t>(pos) * 64;
+  const float2* cs = e.rope_cs + pos;  // pair i at cs[i * max_pos]
 #pragma unroll 1
   for (int hh = 0; hh < BN / 128; ++hh) {
     const int head = (nt * BN) / 128 + hh;
@@ -185,7 +187,7 @@ __device__ __forceinline__ void epi_qkv_rope(const GemmParams& p, const EpiArgs&
       if (!is_v) {
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const float2 c = cs[half * 32 + j];
+          const float2 c = cs[static_cast<size_t>(half * 32 + j) * e.max_pos];
           const float x1 = a[j], x2 = b[j];
           a[j] = x1 * c.x - x2 * c.y;
           b[j] = x2 * c.x + x1 * c.y;
@@ -265,38 +267,70 @@ __global__ void __launch_bounds__(192, 1)
   }
   tc_fence_after_sync();
   const uint32_t tbase = *tmem_slot;
+
+  auto tile0 = [&](int mg) { return mg * MT * CS + rank * MT; };  // this CTA's first M tile of group mg
+  auto valid_tiles = [&](int mg) { return max(0, min(MT, mtiles - tile0(mg))); };
+  // bytes one stage of unit (mg) receives: its A tiles (and lo halves), then B
+  auto stage_bytes = [&](int mg) {
+    const int mt_valid = valid_tiles(mg);
+    int lo_tiles = 0;
+    if constexpr (ALO)
+      for (int mt = 0; mt < mt_valid; ++mt) lo_tiles += ((tile0(mg) + mt + 1) * 128 > p.lo_row0) ? 1 : 0;
+    return static_cast<uint32_t>((mt_valid + lo_tiles) * C::A_BYTES + C::B_BYTES);
+  };
+  const uint64_t pol_b = p.b_evict_first ? l2_policy_evict_first() : l2_policy_evict_last();
+  auto load_b = [&](int stage, int kb, int nt) {
+    uint8_t* bdst = smem + stage * C::STAGE_BYTES + C::A_PARTS * MT * C::A_BYTES;
+    if constexpr (CS == 1) {
+      tma_load_2d_hint(bdst, &tmB, &full[stage], kb * 64, nt * BN, pol_b);
+    } else {
+      tma_load_2d_mc(bdst + rank * B_SLICE * 128, &tmB, &full[stage], kb * 64, nt * BN + rank * B_SLICE, MASK, pol_b);
+    }
+  };
+  // The weights do not depend on the previous kernel: the first STAGES
+  // stages (all empty now) get their B tiles before the wait below, in the
+  // producer's own (unit, k block) order; their A tiles follow after it.
+  int pre = 0;
+  if (p.b_const && warp == 0 && lane == 0) {
+    for (int u = slot; u < p.n_units && pre < C::STAGES; u += stride) {
+      int nt, mg, ks;
+      decode_unit(p, u, nt, mg, ks);
+      const int kb0 = ks * p.nkb / p.k_splits, kb1 = (ks + 1) * p.nkb / p.k_splits;
+      const uint32_t bytes = stage_bytes(mg);
+      for (int kb = kb0; kb < kb1 && pre < C::STAGES; ++kb, ++pre) {
+        mbar_arrive_expect_tx(&full[pre], bytes);
+        load_b(pre, kb, nt);
+      }
+    }
+  }
   // the prologue above overlapped the previous kernel's tail; its results are needed from here on
   griddep_launch_dependents();
   griddep_wait();
 
-  auto tile0 = [&](int mg) { return mg * MT * CS + rank * MT; };  // this CTA's first M tile of group mg
-  auto valid_tiles = [&](int mg) { return max(0, min(MT, mtiles - tile0(mg))); };
-
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol_b = p.b_evict_first ? l2_policy_evict_first() : l2_policy_evict_last();
-      int stage = 0;
+      int stage = 0, it = 0;
       uint32_t phase = 0;
       uint32_t last_phase[8];
       bool issued[8];
-      for (int s = 0; s < 8; ++s) issued[s] = false, last_phase[s] = 0;
+      for (int s = 0; s < 8; ++s) issued[s] = s < pre, last_phase[s] = 0;
       for (int u = slot; u < p.n_units && !*abort_flag; u += stride) {
         int nt, mg, ks;
         decode_unit(p, u, nt, mg, ks);
         const int kb0 = ks * p.nkb / p.k_splits, kb1 = (ks + 1) * p.nkb / p.k_splits;
         const int mt_valid = valid_tiles(mg);
-        int lo_tiles = 0;
-        if constexpr (ALO)
-          for (int mt = 0; mt < mt_valid; ++mt) lo_tiles += ((tile0(mg) + mt + 1) * 128 > p.lo_row0) ? 1 : 0;
-        const uint32_t bytes = (mt_valid + lo_tiles) * C::A_BYTES + C::B_BYTES;
-        for (int kb = kb0; kb < kb1; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns)) {
-            record_error(p.err, DEV_WAIT_TIMEOUT_PRODUCER);
-            *abort_flag = 1;
-            break;
+        const uint32_t bytes = stage_bytes(mg);
+        for (int kb = kb0; kb < kb1; ++kb, ++it) {
+          const bool b_done = it < pre;  // B already issued before the wait (first use of the stage)
+          if (!b_done) {
+            if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns)) {
+              record_error(p.err, DEV_WAIT_TIMEOUT_PRODUCER);
+              *abort_flag = 1;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[stage], bytes);
           }
-          mbar_arrive_expect_tx(&full[stage], bytes);
           uint8_t* base = smem + stage * C::STAGE_BYTES;
           for (int mt = 0; mt < mt_valid; ++mt) {
             tma_load_2d(base + mt * C::A_BYTES, &tmA, &full[stage], kb * 64, (tile0(mg) + mt) * 128);
@@ -304,13 +338,7 @@ __global__ void __launch_bounds__(192, 1)
               if ((tile0(mg) + mt + 1) * 128 > p.lo_row0)
                 tma_load_2d(base + (MT + mt) * C::A_BYTES, &tmA2, &full[stage], kb * 64, (tile0(mg) + mt) * 128);
           }
-          uint8_t* bdst = base + C::A_PARTS * MT * C::A_BYTES;
-          if constexpr (CS == 1) {
-            tma_load_2d_hint(bdst, &tmB, &full[stage], kb * 64, nt * BN, pol_b);
-          } else {
-            tma_load_2d_mc(bdst + rank * B_SLICE * 128, &tmB, &full[stage], kb * 64, nt * BN + rank * B_SLICE, MASK,
-                           pol_b);
-          }
+          if (!b_done) load_b(stage, kb, nt);
           issued[stage] = true;
           last_phase[stage] = phase;
           if (++stage == C::STAGES) {
@@ -528,6 +556,34 @@ static bool encode_map(CUtensorMap* m, const void* ptr, int rows, int cols, int 
   return r == CUDA_SUCCESS;
 }
 
+bool make_kv_map(CUtensorMap* m, const void* base, int dh, int n_rows, int n_heads, int64_t head_rows, int n_layers,
+                 int64_t layer_elems) {
+  static std::mutex mu;
+  static std::map<std::tuple<uintptr_t, int, int, int, int64_t, int, int64_t>, CUtensorMap> cache;
+  const auto key = std::make_tuple(reinterpret_cast<uintptr_t>(base), dh, n_rows, n_heads, head_rows, n_layers,
+                                   layer_elems);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) {
+    *m = it->second;
+    return true;
+  }
+  if (!tma_init() || n_rows < 1 || dh % 64 || (reinterpret_cast<uintptr_t>(base) & 15)) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(dh), static_cast<cuuint64_t>(n_rows), static_cast<cuuint64_t>(n_heads),
+                        static_cast<cuuint64_t>(n_layers)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(dh) * 2, static_cast<cuuint64_t>(head_rows) * dh * 2,
+                           static_cast<cuuint64_t>(layer_elems) * 2};
+  cuuint32_t box[4] = {64, 64, 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  if (cache.size() > 1024) cache.clear();
+  cache.emplace(key, *m);
+  return true;
+}
+
 template <int MT, int BN, int EPI, int CS, bool ALO = false>
 static int launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ma2, const GemmParams& p,
                     const EpiArgs& e, cudaStream_t st, int sms) {
@@ -625,6 +681,7 @@ int launch_gemm(const GemmShape& s, int epi, const EpiArgs& e, const GemmTiling&
   p.err = dev_err;
   p.b_evict_first = (p.n_mgroups == 1 && t.mt * t.cs * 128 >= M) ? 1 : 0;
   p.lo_row0 = s.lo_row0;
+  p.b_const = s.b_const ? 1 : 0;
   CUtensorMap ma, mb, ma2;
   if (!make_map(&ma, s.a, M, K, s.a_ld, 128)) return -1;
   if (s.a_lo && !make_map(&ma2, s.a_lo, M, K, s.a_ld, 128)) return -1;

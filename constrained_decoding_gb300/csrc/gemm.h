@@ -2,6 +2,7 @@
 // 16-bit, both K-contiguous, fp32 accumulation in tensor memory, and one of a
 // few fused epilogues.
 #pragma once
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -27,6 +28,8 @@ struct GemmShape {
   int K;
   const void* a_lo = nullptr;            // optional low half of A (same layout): D = (A + A_lo) . B^T
   int lo_row0 = 0;                       // 128-row tiles entirely below this row skip the low half
+  bool b_const = false;                  // B is never written by an earlier kernel in the stream (weights):
+                                         // its first tiles may load before the programmatic dependency wait
 };
 
 struct EpiArgs {
@@ -40,7 +43,7 @@ struct EpiArgs {
   // EPI_QKV_ROPE: D columns are Hq query heads, then Hkv key heads, then Hkv value heads of 128
   act_t_storage* q_out = nullptr;  // [M][Hq * 128]
   int n_q_heads = 0, n_kv_heads = 0;
-  const float2* rope_cs = nullptr;  // [max_pos][64] (cos, sin)
+  const float2* rope_cs = nullptr;  // [64][max_pos] (cos, sin) of pair i at position pos: rope_cs[i * max_pos + pos]
   int max_pos = 0;
   int split_row = 0;              // rows < split_row use destination 0, the rest destination 1
   act_t_storage* kv_k[2] = {nullptr, nullptr};  // key of (head h, row r') at kv_k[d] + (h * kv_stride[d] + kv_row0[d] + r') * 128
@@ -73,5 +76,11 @@ int launch_gemm(const GemmShape& s, int epi, const EpiArgs& e, const GemmTiling&
 
 // Loads cuTensorMapEncodeTiled from the driver; false if it is unavailable.
 bool tma_init();
+// Tensor map over a 16-bit KV cache laid out [layer][head][row][dh] (head
+// stride head_rows rows, layer stride layer_elems elements): dimensions
+// {dh, n_rows, n_heads, n_layers}, so rows at or past n_rows read as zero;
+// box {64, 64, 1, 1} with 128-byte swizzling.  Cached by its arguments.
+bool make_kv_map(CUtensorMap* m, const void* base, int dh, int n_rows, int n_heads, int64_t head_rows, int n_layers,
+                 int64_t layer_elems);
 
 }  // namespace pcd

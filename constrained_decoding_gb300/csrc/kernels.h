@@ -1,5 +1,6 @@
 // Host launchers of the non-GEMM device steps of the PCD hot path.
 #pragma once
+#include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -102,12 +103,19 @@ struct TreeAttnArgs {
   const int32_t* tile_keys;                 // [chunks][64] branch key index, -1 past the union's end
   const unsigned long long* tile_mask;      // [chunks][tpt] bit i: key i of the chunk is visible to the token
   float scale_log2;                         // log2(e) / sqrt(DH)
-  int csk;                                  // CTAs (cluster size) per (tile, KV head): 1, 2, 4 or 8
+  int csk;                                  // CTAs (cluster size) per (tile, KV head): 1 .. 8
 };
 int launch_tree_attention(const TreeAttnArgs& a, cudaStream_t s);
-// CTAs per (tile, KV head) so that a launch fills the GPU: key blocks of the
-// heaviest tile (max_blocks) bound it.
-int tree_attention_csk(int tiles, int Hkv, int max_blocks, int sms);
+// The same on the tcgen05 tensor cores, head dim 128, tiles of tpt x G <= 128
+// rows.  tmK / tmV map the prefix cache (make_kv_map: rows past n_keys read
+// as zero); `layer` selects its layer.  Pipeline waits give up after wait_ns
+// and record an error code in *err.
+int launch_tree_attention_tc(const TreeAttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, int layer,
+                             uint64_t wait_ns, int* err, cudaStream_t s);
+// CTAs per (tile, KV head) for the warp-MMA (tc = false) or tensor-core
+// kernel: the key blocks of the heaviest tile (max_blocks) against the waves
+// of CTAs the cluster split adds.
+int tree_attention_csk(int tiles, int Hkv, int max_blocks, int sms, bool tc);
 
 // lse[r] = log sum_tiles sum exp(z) from per-tile (max, sum exp(z - max)).
 int launch_lse_combine(const float2* part, int n_tiles, int R, float* lse, cudaStream_t s);

@@ -28,25 +28,6 @@ struct TreeSmem {
   static_assert(64 * RED_LD * 4 <= KV_BYTES, "the partial output reuses the K/V buffers");
 };
 
-__device__ __forceinline__ uint32_t dsmem_addr(const void* p, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
-  return r;
-}
-__device__ __forceinline__ float2 dsmem_ld_f2(uint32_t addr) {
-  float2 v;
-  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
-  return v;
-}
-__device__ __forceinline__ float4 dsmem_ld_f4(uint32_t addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(addr)
-               : "memory");
-  return v;
-}
-
 // Grid: x = (branch tiles + prefix tiles) * csk, y = KV heads; the csk CTAs of
 // one (tile, head) form a cluster.  Branch tiles come first, then prefix tiles
 // from the last (most keys) to the first.  A CTA runs 4 warps x 16 query rows
@@ -375,7 +356,7 @@ static int launch_tree_t(const TreeAttnArgs& a, cudaStream_t s) {
 
 int launch_tree_attention(const TreeAttnArgs& a, cudaStream_t s) {
   if (a.n_br_tiles + a.n_pf_tiles <= 0) return 0;
-  if (a.csk != 1 && a.csk != 2 && a.csk != 4 && a.csk != 8) return cudaErrorInvalidValue;
+  if (a.csk < 1 || a.csk > 8) return cudaErrorInvalidValue;
   if (a.tpt < 1 || a.tpt * (a.Hq / a.Hkv) > 64) return cudaErrorInvalidValue;
   switch (a.DH) {
     case 16: return launch_tree_t<16>(a, s);
@@ -385,17 +366,29 @@ int launch_tree_attention(const TreeAttnArgs& a, cudaStream_t s) {
   return cudaErrorInvalidValue;
 }
 
-int tree_attention_csk(int tiles, int Hkv, int max_blocks, int sms) {
+int tree_attention_csk(int tiles, int Hkv, int max_blocks, int sms, bool tc) {
   static const int forced = [] {
     const char* e = std::getenv("PCD_TREE_CSK");
     return e ? std::atoi(e) : 0;
   }();
-  if (forced == 1 || forced == 2 || forced == 4 || forced == 8) return forced;
-  // two CTAs of this size fit an SM; stop once every SM has two, or a CTA
-  // would get fewer than two key blocks
-  int csk = 1;
-  while (csk < 8 && static_cast<long long>(tiles) * Hkv * csk < 2LL * sms && 2 * csk * 2 <= max_blocks) csk *= 2;
-  return csk;
+  if (forced >= 1 && forced <= 8) return forced;
+  // Time model in microseconds: a CTA costs a fixed part, its share of the
+  // tile's key blocks and, in a cluster, the combine; two CTAs fit an SM and
+  // CTAs past that run in a later wave.
+  const double fixed = 3.0, per_block = tc ? 0.7 : 1.5, combine = 6.0;  // measured: the combine waits on peers
+  int best = 1;
+  double best_t = 1e30;
+  for (int csk = 1; csk <= 8 && csk <= max_blocks; ++csk) {
+    const long long ctas = static_cast<long long>(tiles) * Hkv * csk;
+    const long long waves = (ctas + 2LL * sms - 1) / (2LL * sms);
+    const int blocks = (max_blocks + csk - 1) / csk;
+    const double t = static_cast<double>(waves) * (fixed + blocks * per_block + (csk > 1 ? combine : 0.0));
+    if (t < best_t - 1e-9) {
+      best_t = t;
+      best = csk;
+    }
+  }
+  return best;
 }
 
 }  // namespace pcd

@@ -1,0 +1,467 @@
+// Tree attention on the 5th-generation tensor cores (head dim 128).
+//
+// Same queries, keys and visibility as the warp-MMA tree attention: prefix
+// queries causal over the prefix, branch queries over the whole prefix plus
+// their own ancestors (the per-field branch mask of parallel constrained
+// decoding).  A CTA owns 128 query rows (whole tokens of one GQA group) and
+// walks 64-key blocks:
+//   S = Q K^T            tcgen05.mma, Q and K from shared memory, S in TMEM
+//   P = exp2(S - m)      one thread per row reads its S row from TMEM
+//   O += P V             tcgen05.mma, P (fp16) from TMEM, V as an
+//                        MN-major operand, O accumulated in TMEM
+// The running maximum m is only moved (and O, l rescaled) when a block's
+// maximum exceeds it by more than 2^8, which keeps every P <= 256 in fp16
+// and the result exact up to rounding.  Warp 0 loads K/V (TMA for prefix
+// blocks, gathered cp.async for ancestor chunks), warp 1 issues the MMAs,
+// warps 2-5 run the softmax and the epilogue; P goes back into TMEM over its
+// own S columns and is the A operand of the P V MMA.  A (csk, 1, 1) cluster splits
+// a tile's key blocks and combines the partial softmax states through
+// distributed shared memory.
+#include <climits>
+#include <cstdint>
+
+#include "common.cuh"
+#include "gemm.h"
+#include "kernels.h"
+#include "ptx.cuh"
+#include "warp_mma.cuh"
+
+namespace pcd {
+namespace {
+
+constexpr int kRows = 128;                   // query rows per CTA (MMA M)
+constexpr int kDH = 128;
+constexpr int kKeys = 64;                    // keys per block
+constexpr int kQBytes = kRows * kDH * 2;     // two 64-column halves of 16 KB
+constexpr int kKVBytes = kKeys * kDH * 2;    // two 64-column halves of 8 KB
+constexpr int kOffQ = 0;
+constexpr int kOffK = kQBytes;               // 2 stages
+constexpr int kOffV = kOffK + 2 * kKVBytes;  // 2 stages
+constexpr int kOffBar = kOffV + 2 * kKVBytes;
+constexpr int kOffML = kOffBar + 256;
+constexpr int kSmem = kOffML + 2048 + 1024;  // + alignment slack
+constexpr int kRedLd = kDH + 4;              // fp32 partial-O row stride for the cluster combine
+// a CTA receives ceil(128 / csk) rows from each of csk CTAs (csk <= 8)
+static_assert((kRows + 8) * kRedLd * 4 <= kOffBar, "received partial rows fit the Q/K/V region");
+static_assert((kRows + 8) * 8 <= 2048, "received (m, l) pairs fit their region");
+constexpr uint32_t kTmemCols = 256;          // S: 2 x 64 columns, O: 128
+constexpr uint32_t kColS = 0, kColO = 128;
+constexpr float kRescale = 8.f;              // log2 headroom before m moves
+
+__device__ __forceinline__ uint32_t swz(int row, int chunk) {  // 128-byte swizzled row of 8 16-byte chunks
+  return static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+__global__ void __launch_bounds__(192, 2)
+    tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                        const TreeAttnArgs a, int layer, uint64_t wait_ns, int* err) {
+  extern __shared__ uint8_t tta_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tta_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* k_full = bars;        // [2] producer -> MMA
+  uint64_t* v_full = bars + 2;    // [2]
+  uint64_t* s_full = bars + 4;    // [2] MMA: S ready (and the K stage read) -> softmax, producer
+  uint64_t* p_full = bars + 6;    // [2] softmax: P in TMEM -> MMA
+  uint64_t* pv_done = bars + 8;   // [2] MMA: O += P V done (S/P columns and V stage free)
+  uint64_t* drain = bars + 10;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float2* sML = reinterpret_cast<float2*>(smem + kOffML);
+  float* sRed = reinterpret_cast<float*>(smem);  // received partial rows, after the key loop
+
+  const int csk = a.csk;
+  const int item = blockIdx.x / csk;
+  const int rank = blockIdx.x - item * csk;
+  const int hk = blockIdx.y;
+  const int G = a.Hq / a.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  const bool branch = item < a.n_br_tiles;
+  const int tile = branch ? item : a.n_pf_tiles - 1 - (item - a.n_br_tiles);
+  const int t0 = tile * a.tpt;
+  const int ntok = min(a.tpt, (branch ? a.n_br : a.n_pf) - t0);
+  const int qrow0 = branch ? a.br_row0 + t0 : t0;
+  const int rows = ntok * G;
+  const int pf_keys = branch ? a.n_keys : min(a.n_keys, t0 + ntok);
+  const int nbp = (pf_keys + kKeys - 1) / kKeys;
+  const int ch0 = branch ? a.tile_chunk_off[tile] : 0;
+  const int nb = nbp + (branch ? a.tile_chunk_off[tile + 1] - ch0 : 0);
+  const int my_n = rank < nb ? (nb - 1 - rank) / csk + 1 : 0;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&k_full[s], 1);
+      mbar_init(&v_full[s], 1);
+      mbar_init(&s_full[s], 1);
+      mbar_init(&p_full[s], 128);
+      mbar_init(&pv_done[s], 1);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tbase = *tmem_slot;
+  griddep_launch_dependents();
+  griddep_wait();  // q, K and V come from the projection that ran just before
+
+  auto fail = [&](int code) {
+    record_error(err, code);
+    *abort_flag = 1;
+  };
+  const int r = 32 * (warp & 3) + lane;  // query row (TMEM lane) of a softmax thread (warps 2-5)
+  int kissued[2] = {0, 0}, vissued[2] = {0, 0};  // loads put into each K / V stage (producer warp)
+  float m_ref = -INFINITY, l = 0.f;              // softmax state of row r
+  bool have_o = false;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ K/V loads
+    const act_t* kbp = a.kb + static_cast<size_t>(hk) * a.n_br * kDH;
+    const act_t* vbp = a.vb + static_cast<size_t>(hk) * a.n_br * kDH;
+    // an ancestor chunk: rows of the branch K or V gathered by index, zero past the union's end
+    auto gather = [&](uint8_t* dst, const act_t* src, const int32_t* keys, uint64_t* bar) {
+      for (int e = lane; e < kKeys * 16; e += 32) {
+        const int kr = e >> 4, c = e & 15;
+        const int j = keys[kr];
+        const bool ok = j >= 0 && j < a.n_br;
+        cp_async16(dst + (c >> 3) * (kKVBytes / 2) + swz(kr, c & 7), src + static_cast<size_t>(ok ? j : 0) * kDH + c * 8,
+                   ok);
+      }
+      cp_async_commit();
+      cp_async_wait<0>();
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar);
+    };
+    for (int i = 0; i < my_n; ++i) {
+      if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+      const int s = i & 1, b = rank + i * csk;
+      const int32_t* keys = b >= nbp ? a.tile_keys + static_cast<size_t>(ch0 + b - nbp) * kKeys : nullptr;
+      // the K stage is free once the S of block i - 2 is computed
+      if (!__all_sync(0xffffffffu, i < 2 || mbar_wait(&s_full[s], ((i - 2) >> 1) & 1, wait_ns))) {
+        if (lane == 0) fail(DEV_WAIT_TIMEOUT_PRODUCER);
+        break;
+      }
+      uint8_t* kd = smem + kOffK + s * kKVBytes;
+      if (!keys) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&k_full[s], kKVBytes);
+          tma_load_4d(kd, &tmK, &k_full[s], 0, b * kKeys, hk, layer);
+          tma_load_4d(kd + kKVBytes / 2, &tmK, &k_full[s], 64, b * kKeys, hk, layer);
+        }
+      } else {
+        gather(kd, kbp, keys, &k_full[s]);
+      }
+      ++kissued[s];
+      // the V stage is free once the P V of block i - 2 is done
+      if (!__all_sync(0xffffffffu, i < 2 || mbar_wait(&pv_done[s], ((i - 2) >> 1) & 1, wait_ns))) {
+        if (lane == 0) fail(DEV_WAIT_TIMEOUT_PRODUCER);
+        break;
+      }
+      uint8_t* vd = smem + kOffV + s * kKVBytes;
+      if (!keys) {
+        if (lane == 0) {
+          mbar_arrive_expect_tx(&v_full[s], kKVBytes);
+          tma_load_4d(vd, &tmV, &v_full[s], 0, b * kKeys, hk, layer);
+          tma_load_4d(vd + kKVBytes / 2, &tmV, &v_full[s], 64, b * kKeys, hk, layer);
+        }
+      } else {
+        gather(vd, vbp, keys, &v_full[s]);
+      }
+      ++vissued[s];
+      __syncwarp();
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    named_barrier_sync(1, 160);  // Q is staged
+    if (lane == 0) {
+      tc_fence_after_sync();
+      constexpr uint32_t kIdescS = idesc_f16_f32(kRows, kKeys);
+      constexpr uint32_t kIdescO = idesc_f16_f32(kRows, kDH) | (1u << 16);  // B (V) is MN-major
+      const uint32_t qa = smem_u32(smem + kOffQ);
+      for (int i = 0; i <= my_n && !*abort_flag; ++i) {
+        if (i < my_n) {
+          const int s = i & 1;
+          // S/P columns s are free once the P V of block i - 2 is done
+          if (!mbar_wait(&k_full[s], (i >> 1) & 1, wait_ns) ||
+              (i >= 2 && !mbar_wait(&pv_done[s], ((i - 2) >> 1) & 1, wait_ns))) {
+            fail(DEV_WAIT_TIMEOUT_MMA);
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t ka = smem_u32(smem + kOffK + s * kKVBytes);
+#pragma unroll
+          for (int k = 0; k < kDH / 16; ++k)
+            umma_f16(tbase + kColS + s * kKeys, sdesc_kmajor_sw128(qa + (k >> 2) * (kQBytes / 2) + (k & 3) * 32),
+                     sdesc_kmajor_sw128(ka + (k >> 2) * (kKVBytes / 2) + (k & 3) * 32), kIdescS, k > 0 ? 1u : 0u);
+          umma_commit(&s_full[s]);
+        }
+        if (i > 0) {
+          const int ip = i - 1, sp = ip & 1;
+          if (!mbar_wait(&p_full[sp], (ip >> 1) & 1, wait_ns) || !mbar_wait(&v_full[sp], (ip >> 1) & 1, wait_ns)) {
+            fail(DEV_WAIT_TIMEOUT_MMA);
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t va = smem_u32(smem + kOffV + sp * kKVBytes);
+#pragma unroll
+          for (int k = 0; k < kKeys / 16; ++k)  // P: 16 keys = 8 packed columns per step
+            umma_f16_ts(tbase + kColO, tbase + kColS + sp * kKeys + k * 8,
+                        sdesc_mnmajor_sw128(va + k * 16 * 128, kKVBytes / 2, 1024), kIdescO, (ip > 0 || k > 0) ? 1u : 0u);
+          umma_commit(&pv_done[sp]);
+        }
+      }
+      // every MMA issued above has finished before TMEM is released
+      umma_commit(drain);
+      if (!mbar_wait(drain, 0, wait_ns)) record_error(err, DEV_WAIT_TIMEOUT_MMA);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax rows
+    {  // Q tile: the thread of row r stages it, swizzled
+      const bool ok = r < rows;
+      const uint4* src = reinterpret_cast<const uint4*>(
+          a.q + (static_cast<size_t>(qrow0 + (ok ? r / G : 0)) * a.Hq + hk * G + (ok ? r % G : 0)) * kDH);
+      uint4 v[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) v[c] = ok ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        *reinterpret_cast<uint4*>(smem + kOffQ + (c >> 3) * (kQBytes / 2) + swz(r, c & 7)) = v[c];
+      fence_proxy_async_smem();
+    }
+    named_barrier_sync(1, 160);
+    const uint32_t trow = tbase + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+    const bool valid = r < rows;
+    const int pos = branch ? INT_MAX : t0 + (valid ? r / G : 0);
+    const int tt = valid ? r / G : 0;
+    for (int i = 0; i < my_n; ++i) {
+      const int s = i & 1, b = rank + i * csk;
+      const bool ok = __all_sync(0xffffffffu, !*abort_flag && mbar_wait(&s_full[s], (i >> 1) & 1, wait_ns));
+      if (!ok) {
+        if (lane == 0) fail(DEV_WAIT_TIMEOUT_MMA);
+        break;
+      }
+      tc_fence_after_sync();
+      float sv[kKeys];
+      tmem_ld_32cols(trow + kColS + s * kKeys, sv);
+      tmem_ld_32cols(trow + kColS + s * kKeys + 32, sv + 32);
+
+      const bool local = b >= nbp;
+      const int j0 = b * kKeys;
+      // a prefix block wholly below the causal edge needs no per-key test
+      const bool all_vis = valid && !local && j0 + kKeys <= pf_keys && j0 + kKeys - 1 <= pos;
+      float mb = -INFINITY;
+      if (all_vis) {
+#pragma unroll
+        for (int c = 0; c < kKeys; ++c) mb = fmaxf(mb, sv[c]);
+      } else {
+        unsigned long long mk = 0ull;
+        if (local && valid) mk = a.tile_mask[static_cast<size_t>(ch0 + b - nbp) * a.tpt + tt];
+#pragma unroll
+        for (int c = 0; c < kKeys; ++c) {
+          const bool vis = valid && (local ? ((mk >> c) & 1ull) != 0ull : (j0 + c < pf_keys && j0 + c <= pos));
+          sv[c] = vis ? sv[c] : -INFINITY;
+          mb = fmaxf(mb, sv[c]);
+        }
+      }
+      mb *= a.scale_log2;  // log2 units; -inf stays -inf
+      if (__any_sync(0xffffffffu, mb > m_ref + kRescale)) {
+        const float m_new = fmaxf(m_ref, mb);
+        const float f = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_new);
+        if (i > 0) {  // O holds blocks 0 .. i-1 once their last P V is done
+          if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, wait_ns))) {
+            if (lane == 0) fail(DEV_WAIT_TIMEOUT_MMA);
+            break;
+          }
+          tc_fence_after_sync();
+#pragma unroll 1
+          for (int q = 0; q < kDH / 32; ++q) {
+            float ov[32];
+            tmem_ld_32cols(trow + kColO + q * 32, ov);
+#pragma unroll
+            for (int x = 0; x < 32; ++x) ov[x] *= f;
+            tmem_st_32cols(trow + kColO + q * 32, ov);
+          }
+        }
+        l *= f;
+        m_ref = m_new;
+      }
+      // P (fp16, two keys per column) over the first half of this block's S columns
+      const float mo = (m_ref == -INFINITY) ? 0.f : m_ref;  // nothing visible yet: every score is -inf
+      float ps = 0.f;
+      uint32_t pw[kKeys / 2];
+#pragma unroll
+      for (int c2 = 0; c2 < kKeys / 2; ++c2) {
+        const float p0 = ex2_approx(fmaf(sv[2 * c2], a.scale_log2, -mo));  // 2^-inf = 0
+        const float p1 = ex2_approx(fmaf(sv[2 * c2 + 1], a.scale_log2, -mo));
+        ps += p0 + p1;
+        pw[c2] = pack2(p0, p1);
+      }
+      tmem_st_32cols_u32(trow + kColS + s * kKeys, pw);
+      l += ps;
+      tc_fence_before_sync();
+      mbar_arrive(&p_full[s]);
+    }
+    have_o = my_n > 0 && !*abort_flag;
+    if (have_o && !mbar_wait(&pv_done[(my_n - 1) & 1], ((my_n - 1) >> 1) & 1, wait_ns)) {
+      if (lane == 0) fail(DEV_WAIT_TIMEOUT_MMA);
+      have_o = false;
+    }
+    have_o = __all_sync(0xffffffffu, have_o);
+    tc_fence_after_sync();
+    if (csk == 1) {
+      const float il = l > 0.f ? 1.f / l : 0.f;
+      const size_t base = static_cast<size_t>(qrow0 + tt) * a.ld_out + (hk * G + (valid ? r % G : 0)) * kDH;
+#pragma unroll 1
+      for (int q = 0; q < kDH / 32 && have_o; ++q) {
+        float ov[32];
+        tmem_ld_32cols(trow + kColO + q * 32, ov);
+        if (!valid) continue;
+#pragma unroll
+        for (int c8 = 0; c8 < 4; ++c8) {
+          uint32_t w[4], wl[4];
+#pragma unroll
+          for (int x = 0; x < 4; ++x) {
+            const float y0 = ov[c8 * 8 + 2 * x] * il, y1 = ov[c8 * 8 + 2 * x + 1] * il;
+            w[x] = pack2(y0, y1);
+            const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&w[x]));
+            wl[x] = pack2(y0 - h.x, y1 - h.y);
+          }
+          const size_t o = base + q * 32 + c8 * 8;
+          *reinterpret_cast<uint4*>(a.out + o) = make_uint4(w[0], w[1], w[2], w[3]);
+          if (a.out_lo) *reinterpret_cast<uint4*>(a.out_lo + o) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    // nothing of this CTA's copies may still be landing when it exits
+    for (int s = 0; s < 2; ++s) {
+      if (kissued[s] > 0) mbar_wait(&k_full[s], static_cast<uint32_t>((kissued[s] - 1) & 1), wait_ns);
+      if (vissued[s] > 0) mbar_wait(&v_full[s], static_cast<uint32_t>((vissued[s] - 1) & 1), wait_ns);
+    }
+  }
+  if (csk > 1) {
+    // rank q owns rows [q * per, (q + 1) * per) of the tile: every CTA pushes
+    // its partial state of those rows (unnormalised O relative to its m, and
+    // its l) into slot `rank` of the owner's shared memory, then the owner
+    // combines them locally
+    const int per = (kRows + csk - 1) / csk;
+    cluster_sync_all();  // every CTA of the cluster is done with its Q/K/V/P buffers
+    if (warp >= 2) {
+      const uint32_t trow = tbase + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
+      const int owner = r / per, lr = r - owner * per;
+      const uint32_t dst = dsmem_addr(sRed + (rank * per + lr) * kRedLd, owner);
+#pragma unroll 1
+      for (int q = 0; q < kDH / 32; ++q) {
+        float ov[32];
+        if (have_o) {
+          tc_fence_after_sync();
+          tmem_ld_32cols(trow + kColO + q * 32, ov);
+        } else {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) ov[x] = 0.f;
+        }
+        if (r < rows)
+#pragma unroll
+          for (int x = 0; x < 8; ++x)
+            dsmem_st_f4(dst + (q * 32 + 4 * x) * 4, make_float4(ov[4 * x], ov[4 * x + 1], ov[4 * x + 2], ov[4 * x + 3]));
+      }
+      if (r < rows)
+        dsmem_st_f2(dsmem_addr(sML + rank * per + lr, owner),
+                    make_float2(have_o ? m_ref : -INFINITY, have_o ? l : 0.f));
+    }
+    tc_fence_before_sync();
+    cluster_sync_all();  // the pushed states are visible to their owners
+    const int rb = rank * per, re = min(rows, rb + per);
+    constexpr int C4 = kDH / 4;
+    for (int idx = threadIdx.x; idx < (re - rb) * C4; idx += blockDim.x) {
+      const int lr = idx / C4, rr = rb + lr, d = (idx % C4) * 4;
+      float M = -INFINITY;
+      for (int pr = 0; pr < csk; ++pr) {
+        const float2 ml = sML[pr * per + lr];
+        if (ml.y > 0.f) M = fmaxf(M, ml.x);
+      }
+      float L = 0.f;
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int pr = 0; pr < csk; ++pr) {
+        const float2 ml = sML[pr * per + lr];
+        if (!(ml.y > 0.f)) continue;
+        const float w = ex2_approx(ml.x - M);
+        const float4 v = *reinterpret_cast<const float4*>(sRed + (pr * per + lr) * kRedLd + d);
+        L += w * ml.y;
+        acc.x += w * v.x;
+        acc.y += w * v.y;
+        acc.z += w * v.z;
+        acc.w += w * v.w;
+      }
+      const float il = L > 0.f ? 1.f / L : 0.f;
+      const float y0 = acc.x * il, y1 = acc.y * il, y2 = acc.z * il, y3 = acc.w * il;
+      const size_t o = static_cast<size_t>(qrow0 + rr / G) * a.ld_out + (hk * G + rr % G) * kDH + d;
+      const uint2 hv = make_uint2(pack2(y0, y1), pack2(y2, y3));
+      *reinterpret_cast<uint2*>(a.out + o) = hv;
+      if (a.out_lo) {
+        const float2 h01 = __half22float2(*reinterpret_cast<const __half2*>(&hv.x));
+        const float2 h23 = __half22float2(*reinterpret_cast<const __half2*>(&hv.y));
+        *reinterpret_cast<uint2*>(a.out_lo + o) = make_uint2(pack2(y0 - h01.x, y1 - h01.y), pack2(y2 - h23.x, y3 - h23.y));
+      }
+    }
+  }
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tbase, kTmemCols);
+  }
+}
+
+}  // namespace
+
+int launch_tree_attention_tc(const TreeAttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, int layer,
+                             uint64_t wait_ns, int* err, cudaStream_t s) {
+  if (a.n_br_tiles + a.n_pf_tiles <= 0) return 0;
+  if (a.DH != kDH || a.csk < 1 || a.csk > 8) return cudaErrorInvalidValue;
+  if (a.tpt < 1 || a.tpt * (a.Hq / a.Hkv) > kRows) return cudaErrorInvalidValue;
+  static bool attr = false;
+  if (!attr) {
+    cudaError_t r = cudaFuncSetAttribute(tree_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (r != cudaSuccess) return r;
+    attr = true;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>((a.n_br_tiles + a.n_pf_tiles) * a.csk), static_cast<unsigned>(a.Hkv), 1);
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = kSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[2];
+  int na = 0;
+  if (a.csk > 1) {
+    at[na].id = cudaLaunchAttributeClusterDimension;
+    at[na].val.clusterDim.x = static_cast<unsigned>(a.csk);
+    at[na].val.clusterDim.y = 1;
+    at[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  if (pdl_enabled()) {
+    at[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[na].val.programmaticStreamSerializationAllowed = 1;
+    ++na;
+  }
+  cfg.attrs = at;
+  cfg.numAttrs = na;
+  return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel, tmK, tmV, a, layer, wait_ns, err);
+}
+
+}  // namespace pcd
