@@ -35,6 +35,10 @@ class ModelConfig:
 _SHAPES = {
     # 2 layers, d=64, 4 query / 2 KV heads of dim 16, SwiGLU 172, vocab 512, fp32.
     "tiny": ModelConfig("tiny", 2, 64, 4, 2, 16, 172, 512, 1e-6, 1e4, True, "f32"),
+    # 2 layers, d=768, 6 query / 2 KV heads of dim 128 (the production head
+    # size), SwiGLU 1024, vocab 512, fp32: small enough for exhaustive oracle
+    # checks of the head-dim-128 kernels.
+    "tiny-h128": ModelConfig("tiny-h128", 2, 768, 6, 2, 128, 1024, 512, 1e-6, 1e4, True, "f32"),
     # Qwen2.5-1.5B shape, bf16, tied embedding.
     "1.5b": ModelConfig("1.5b", 28, 1536, 12, 2, 128, 8960, 151936, 1e-6, 1e6, True, "bf16"),
     # Qwen2.5-7B shape, bf16, untied LM head.

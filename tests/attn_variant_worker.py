@@ -1,8 +1,9 @@
-"""Child process of test_attention_variants: runs the CUDA path on the tiny
-decoder under the attention settings its environment selects (one tree-
-attention launch per layer with a forced cluster size, or the split
-attention + merge launches) and saves every field's results to an .npz.
-The settings are read once per process, hence a process per variant."""
+"""Child process of test_attention_variants: runs the CUDA path on a small
+decoder (argv: output .npz, shape name) under the attention settings its
+environment selects (tree attention on the tensor cores or on warp MMA, a
+forced cluster size, or the split attention + merge launches) and saves
+every field's results.  The settings are read once per process, hence a
+process per variant."""
 import os
 import sys
 
@@ -27,9 +28,9 @@ def requests():
     return [synth.make_request(1)] + [make_custom(s, 512, n, sp) for s, n, sp in VARIANT_REQUESTS]
 
 
-def main(out_path):
+def main(out_path, shape="tiny"):
     import constrained_decoding_gb300.pcd as pcd
-    w = synth.make_weights(synth.model_config("tiny"), seed=0)
+    w = synth.make_weights(synth.model_config(shape), seed=0)
     m = pcd.pcd_load_weights_host(w)
     arrays = {}
     for i, req in enumerate(requests()):
@@ -45,4 +46,4 @@ def main(out_path):
 
 
 if __name__ == "__main__":
-    main(sys.argv[1])
+    main(*sys.argv[1:])

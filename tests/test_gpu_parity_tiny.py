@@ -177,28 +177,3 @@ def test_single_pass_matches_oracle(pcd, model, tiny_oracle, request1, seed, pre
         assert a.label == b.label
         np.testing.assert_allclose(a.logprobs, b.logprobs, atol=2e-3)
 
-
-@pytest.mark.parametrize("env", [
-    {"PCD_TREE_CSK": "1"}, {"PCD_TREE_CSK": "2"}, {"PCD_TREE_CSK": "4"}, {"PCD_TREE_CSK": "8"},
-    {"PCD_TREE_ATTN": "0"},
-])
-def test_attention_variants(tiny_oracle, tmp_path, env):
-    """Tree attention at every cluster size, and the split attention + merge
-    launches, on multi-chunk ancestor sets, both passes, against the oracle."""
-    import os
-    import subprocess
-    import sys
-    from types import SimpleNamespace
-    import attn_variant_worker as wk
-    out = tmp_path / "res.npz"
-    subprocess.run([sys.executable, wk.__file__, str(out)], env={**os.environ, **env}, check=True, timeout=600)
-    got = np.load(out)
-    for i, req in enumerate(wk.requests()):
-        ref = _oracle_results(tiny_oracle, req)
-        for mode in ("single", "two"):
-            for f, r in enumerate(ref):
-                sc = got[f"{mode}_{i}_{f}_scalars"]
-                g = SimpleNamespace(logprobs=got[f"{mode}_{i}_{f}_logprobs"], probs=got[f"{mode}_{i}_{f}_probs"],
-                                    label=int(sc[0]), mass=float(sc[1]), log_mass=float(sc[2]),
-                                    first_mass=float(sc[3]))
-                compare_field(g, r, f"{env} {mode} request {i} field {f}")

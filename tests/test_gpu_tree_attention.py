@@ -1,0 +1,51 @@
+"""Tree attention variants against the oracle: every cluster size, the
+tensor-core kernel (head dim 128) and the warp-MMA one, and the split
+attention + merge launches, on requests whose ancestor sets span several
+64-key chunks, in both the single pass and the prefill + branch passes."""
+import os
+import subprocess
+import sys
+from types import SimpleNamespace
+
+import numpy as np
+import pytest
+
+import synth
+from parity import compare_field
+
+pytestmark = pytest.mark.gpu
+
+VARIANTS = {
+    "tiny": [{"PCD_TREE_CSK": "1"}, {"PCD_TREE_CSK": "2"}, {"PCD_TREE_CSK": "3"}, {"PCD_TREE_CSK": "8"},
+             {"PCD_TREE_ATTN": "0"}],
+    "tiny-h128": [{}, {"PCD_TREE_CSK": "2"}, {"PCD_TREE_CSK": "3"}, {"PCD_TREE_CSK": "5"}, {"PCD_TREE_CSK": "8"},
+                  {"PCD_ATTN_TC": "0"}, {"PCD_TREE_ATTN": "0"}],
+}
+CASES = [(shape, env) for shape, envs in VARIANTS.items() for env in envs]
+
+
+@pytest.fixture(scope="module")
+def oracles():
+    from oracle import Oracle
+    return {shape: Oracle(synth.make_weights(synth.model_config(shape), seed=0), np.float32) for shape in VARIANTS}
+
+
+@pytest.mark.parametrize("shape,env", CASES, ids=[f"{s}-{'-'.join(f'{k}={v}' for k, v in e.items()) or 'default'}"
+                                                 for s, e in CASES])
+def test_attention_variants(oracles, tmp_path, shape, env):
+    import attn_variant_worker as wk
+    out = tmp_path / "res.npz"
+    subprocess.run([sys.executable, wk.__file__, str(out), shape], env={**os.environ, **env}, check=True,
+                   timeout=600)
+    got = np.load(out)
+    orc = oracles[shape]
+    for i, req in enumerate(wk.requests()):
+        cache = orc.prefill(req.prefix)
+        ref = [orc.score_field(f, cache=cache) for f in req.fields]
+        for mode in ("single", "two"):
+            for f, r in enumerate(ref):
+                sc = got[f"{mode}_{i}_{f}_scalars"]
+                g = SimpleNamespace(logprobs=got[f"{mode}_{i}_{f}_logprobs"], probs=got[f"{mode}_{i}_{f}_probs"],
+                                    label=int(sc[0]), mass=float(sc[1]), log_mass=float(sc[2]),
+                                    first_mass=float(sc[3]))
+                compare_field(g, r, f"{shape} {env} {mode} request {i} field {f}")
