@@ -373,14 +373,15 @@ int tree_attention_csk(int tiles, int Hkv, int max_blocks, int sms, bool tc) {
   }();
   if (forced >= 1 && forced <= 8) return forced;
   // Time model in microseconds: a CTA costs a fixed part, its share of the
-  // tile's key blocks and, in a cluster, the combine; two CTAs fit an SM and
-  // CTAs past that run in a later wave.
+  // tile's key blocks and, in a cluster, the combine; CTAs past what the SMs
+  // hold at once run in a later wave.
   const double fixed = 3.0, per_block = tc ? 0.7 : 1.5, combine = 6.0;  // measured: the combine waits on peers
   int best = 1;
   double best_t = 1e30;
   for (int csk = 1; csk <= 8 && csk <= max_blocks; ++csk) {
     const long long ctas = static_cast<long long>(tiles) * Hkv * csk;
-    const long long waves = (ctas + 2LL * sms - 1) / (2LL * sms);
+    const long long slots = static_cast<long long>(tc ? 1 : 2) * sms;  // resident CTAs per SM: 1 (tensor-core), 2
+    const long long waves = (ctas + slots - 1) / slots;
     const int blocks = (max_blocks + csk - 1) / csk;
     const double t = static_cast<double>(waves) * (fixed + blocks * per_block + (csk > 1 ? combine : 0.0));
     if (t < best_t - 1e-9) {

@@ -10,8 +10,9 @@
 //   O += P V             tcgen05.mma, P (fp16) from TMEM, V as an
 //                        MN-major operand, O accumulated in TMEM
 // The running maximum m is only moved (and O, l rescaled) when a block's
-// maximum exceeds it by more than 2^8, which keeps every P <= 256 in fp16
-// and the result exact up to rounding.  Warp 0 loads K/V (TMA for prefix
+// maximum exceeds it by more than 14 (log2 units): every P stays <= 2^14, a
+// finite fp16, and the result is exact up to rounding, while the rescale
+// (which waits for the previous P V) is rare.  Warp 0 loads K/V (TMA for prefix
 // blocks, gathered cp.async for ancestor chunks), warp 1 issues the MMAs,
 // warps 2-5 run the softmax and the epilogue; P goes back into TMEM over its
 // own S columns and is the A operand of the P V MMA.  A (csk, 1, 1) cluster splits
@@ -35,36 +36,42 @@ constexpr int kKeys = 64;                    // keys per block
 constexpr int kQBytes = kRows * kDH * 2;     // two 64-column halves of 16 KB
 constexpr int kKVBytes = kKeys * kDH * 2;    // two 64-column halves of 8 KB
 constexpr int kOffQ = 0;
-constexpr int kOffK = kQBytes;               // 2 stages
-constexpr int kOffV = kOffK + 2 * kKVBytes;  // 2 stages
-constexpr int kOffBar = kOffV + 2 * kKVBytes;
+constexpr int kStages = 4;                   // K and V stages: the loads run ahead of the MMAs
+constexpr int kOffK = kQBytes;
+constexpr int kOffV = kOffK + kStages * kKVBytes;
+constexpr int kOffBar = kOffV + kStages * kKVBytes;
+constexpr int kOutLd = kDH * 2 + 16;         // staged output row (bytes): padded against bank conflicts
+static_assert(2 * kRows * kOutLd <= kOffBar, "staged hi and lo output rows fit the Q/K/V region");
 constexpr int kOffML = kOffBar + 256;
 constexpr int kSmem = kOffML + 2048 + 1024;  // + alignment slack
 constexpr int kRedLd = kDH + 4;              // fp32 partial-O row stride for the cluster combine
 // a CTA receives ceil(128 / csk) rows from each of csk CTAs (csk <= 8)
 static_assert((kRows + 8) * kRedLd * 4 <= kOffBar, "received partial rows fit the Q/K/V region");
 static_assert((kRows + 8) * 8 <= 2048, "received (m, l) pairs fit their region");
-constexpr uint32_t kTmemCols = 256;          // S: 2 x 64 columns, O: 128
-constexpr uint32_t kColS = 0, kColO = 128;
-constexpr float kRescale = 8.f;              // log2 headroom before m moves
+constexpr uint32_t kTmemCols = 512;          // S (then P): kStages x 64 columns, O: 128
+constexpr uint32_t kColS = 0, kColO = kStages * kKeys;
+constexpr bool kLoadsByCpAsync = false;      // prefix K/V blocks by cp.async instead of TMA
+constexpr float kRescale = 14.f;             // log2 headroom before m moves: P <= 2^14 stays finite in fp16
 
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {  // 128-byte swizzled row of 8 16-byte chunks
   return static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-__global__ void __launch_bounds__(192, 2)
+__global__ void __launch_bounds__(192, 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const TreeAttnArgs a, int layer, uint64_t wait_ns, int* err) {
   extern __shared__ uint8_t tta_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tta_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
-  uint64_t* k_full = bars;        // [2] producer -> MMA
-  uint64_t* v_full = bars + 2;    // [2]
-  uint64_t* s_full = bars + 4;    // [2] MMA: S ready (and the K stage read) -> softmax, producer
-  uint64_t* p_full = bars + 6;    // [2] softmax: P in TMEM -> MMA
-  uint64_t* pv_done = bars + 8;   // [2] MMA: O += P V done (S/P columns and V stage free)
-  uint64_t* drain = bars + 10;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 11);
+  uint64_t* k_full = bars;        // [kStages] producer -> MMA
+  uint64_t* v_full = bars + 4;    // [kStages]
+  uint64_t* k_free = bars + 8;    // [kStages] MMA: the S that read the K stage is done -> producer
+  uint64_t* v_free = bars + 12;   // [kStages] MMA: the P V that read the V stage is done -> producer
+  uint64_t* s_full = bars + 16;   // [kStages] MMA: S ready -> softmax
+  uint64_t* p_full = bars + 20;   // [kStages] softmax: P in TMEM -> MMA
+  uint64_t* pv_done = bars + 24;  // [kStages] MMA: O += P V done (S/P columns free, O current)
+  uint64_t* drain = bars + 28;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 29);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float2* sML = reinterpret_cast<float2*>(smem + kOffML);
   float* sRed = reinterpret_cast<float*>(smem);  // received partial rows, after the key loop
@@ -87,11 +94,17 @@ __global__ void __launch_bounds__(192, 2)
   const int ch0 = branch ? a.tile_chunk_off[tile] : 0;
   const int nb = nbp + (branch ? a.tile_chunk_off[tile + 1] - ch0 : 0);
   const int my_n = rank < nb ? (nb - 1 - rank) / csk + 1 : 0;
+  // CTAs of one KV head start at different key blocks (the online softmax
+  // takes them in any order), so they do not all read the same block at once
+  const int rot = my_n > 0 ? static_cast<int>((item * 5u + hk * 3u) % static_cast<unsigned>(my_n)) : 0;
+  auto block_of = [&](int i) { int j = i + rot; j -= j >= my_n ? my_n : 0; return rank + j * csk; };
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       mbar_init(&k_full[s], 1);
       mbar_init(&v_full[s], 1);
+      mbar_init(&k_free[s], 1);
+      mbar_init(&v_free[s], 1);
       mbar_init(&s_full[s], 1);
       mbar_init(&p_full[s], 128);
       mbar_init(&pv_done[s], 1);
@@ -120,7 +133,7 @@ __global__ void __launch_bounds__(192, 2)
     *abort_flag = 1;
   };
   const int r = 32 * (warp & 3) + lane;  // query row (TMEM lane) of a softmax thread (warps 2-5)
-  int kissued[2] = {0, 0}, vissued[2] = {0, 0};  // loads put into each K / V stage (producer warp)
+  int kissued[kStages] = {0, 0, 0, 0}, vissued[kStages] = {0, 0, 0, 0};  // loads per K / V stage (producer warp)
   float m_ref = -INFINITY, l = 0.f;              // softmax state of row r
   bool have_o = false;
 
@@ -143,12 +156,70 @@ __global__ void __launch_bounds__(192, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar);
     };
+    if constexpr (kLoadsByCpAsync) {
+      // every block by cp.async, K and V of a block in one commit group, up to
+      // kStages groups in flight; a block is signalled once its group is done
+      const act_t* kp = a.k + static_cast<size_t>(hk) * a.kv_head_stride * kDH;
+      const act_t* vp = a.v + static_cast<size_t>(hk) * a.kv_head_stride * kDH;
+      int sig = 0, pending = 0;
+      auto retire = [&]() {
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&k_full[sig % kStages]);
+          mbar_arrive(&v_full[sig % kStages]);
+        }
+        ++sig;
+        --pending;
+      };
+      for (int i = 0; i < my_n; ++i) {
+        if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
+        const int s = i % kStages, b = block_of(i);
+        const uint32_t fpar = static_cast<uint32_t>(((i - kStages) / kStages) & 1);
+        const int32_t* keys = b >= nbp ? a.tile_keys + static_cast<size_t>(ch0 + b - nbp) * kKeys : nullptr;
+        if (!__all_sync(0xffffffffu, i < kStages || (mbar_wait(&k_free[s], fpar, wait_ns) &&
+                                                      mbar_wait(&v_free[s], fpar, wait_ns)))) {
+          if (lane == 0) fail(DEV_WAIT_TIMEOUT_PRODUCER);
+          break;
+        }
+        uint8_t* kd = smem + kOffK + s * kKVBytes;
+        uint8_t* vd = smem + kOffV + s * kKVBytes;
+        const act_t* ksrc = keys ? kbp : kp;
+        const act_t* vsrc = keys ? vbp : vp;
+        for (int e = lane; e < kKeys * 16; e += 32) {
+          const int kr = e >> 4, c = e & 15;
+          const int j = keys ? keys[kr] : b * kKeys + kr;
+          const bool ok = keys ? (j >= 0 && j < a.n_br) : j < pf_keys;
+          const size_t off = static_cast<size_t>(ok ? j : 0) * kDH + c * 8;
+          const uint32_t so = (c >> 3) * (kKVBytes / 2) + swz(kr, c & 7);
+          cp_async16(kd + so, ksrc + off, ok);
+          cp_async16(vd + so, vsrc + off, ok);
+        }
+        cp_async_commit();
+        ++pending;
+        ++kissued[s];
+        ++vissued[s];
+        // a block is signalled before the producer waits on the stage it
+        // frees (the MMA issues S of block j before P V of block j - 1)
+        if (pending == kStages - 1) {
+          cp_async_wait<kStages - 2>();
+          retire();
+        }
+      }
+      while (pending > 0) {
+        if (pending >= 3) cp_async_wait<2>();
+        else if (pending == 2) cp_async_wait<1>();
+        else cp_async_wait<0>();
+        retire();
+      }
+    } else {
     for (int i = 0; i < my_n; ++i) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-      const int s = i & 1, b = rank + i * csk;
+      const int s = i % kStages, b = block_of(i);
+      const uint32_t fpar = static_cast<uint32_t>(((i - kStages) / kStages) & 1);  // phase of block i - kStages
       const int32_t* keys = b >= nbp ? a.tile_keys + static_cast<size_t>(ch0 + b - nbp) * kKeys : nullptr;
-      // the K stage is free once the S of block i - 2 is computed
-      if (!__all_sync(0xffffffffu, i < 2 || mbar_wait(&s_full[s], ((i - 2) >> 1) & 1, wait_ns))) {
+      // the K stage is free once the S of block i - kStages is computed
+      if (!__all_sync(0xffffffffu, i < kStages || mbar_wait(&k_free[s], fpar, wait_ns))) {
         if (lane == 0) fail(DEV_WAIT_TIMEOUT_PRODUCER);
         break;
       }
@@ -163,8 +234,8 @@ __global__ void __launch_bounds__(192, 2)
         gather(kd, kbp, keys, &k_full[s]);
       }
       ++kissued[s];
-      // the V stage is free once the P V of block i - 2 is done
-      if (!__all_sync(0xffffffffu, i < 2 || mbar_wait(&pv_done[s], ((i - 2) >> 1) & 1, wait_ns))) {
+      // the V stage is free once the P V of block i - kStages is done
+      if (!__all_sync(0xffffffffu, i < kStages || mbar_wait(&v_free[s], fpar, wait_ns))) {
         if (lane == 0) fail(DEV_WAIT_TIMEOUT_PRODUCER);
         break;
       }
@@ -181,6 +252,7 @@ __global__ void __launch_bounds__(192, 2)
       ++vissued[s];
       __syncwarp();
     }
+    }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     named_barrier_sync(1, 160);  // Q is staged
@@ -191,34 +263,37 @@ __global__ void __launch_bounds__(192, 2)
       const uint32_t qa = smem_u32(smem + kOffQ);
       for (int i = 0; i <= my_n && !*abort_flag; ++i) {
         if (i < my_n) {
-          const int s = i & 1;
-          // S/P columns s are free once the P V of block i - 2 is done
-          if (!mbar_wait(&k_full[s], (i >> 1) & 1, wait_ns) ||
-              (i >= 2 && !mbar_wait(&pv_done[s], ((i - 2) >> 1) & 1, wait_ns))) {
+          const int s = i % kStages, ks = s;
+          // S/P columns s are free once the P V of block i - kStages is done
+          if (!mbar_wait(&k_full[ks], static_cast<uint32_t>((i / kStages) & 1), wait_ns) ||
+              (i >= kStages && !mbar_wait(&pv_done[s], static_cast<uint32_t>(((i - kStages) / kStages) & 1), wait_ns))) {
             fail(DEV_WAIT_TIMEOUT_MMA);
             break;
           }
           tc_fence_after_sync();
-          const uint32_t ka = smem_u32(smem + kOffK + s * kKVBytes);
+          const uint32_t ka = smem_u32(smem + kOffK + ks * kKVBytes);
 #pragma unroll
           for (int k = 0; k < kDH / 16; ++k)
             umma_f16(tbase + kColS + s * kKeys, sdesc_kmajor_sw128(qa + (k >> 2) * (kQBytes / 2) + (k & 3) * 32),
                      sdesc_kmajor_sw128(ka + (k >> 2) * (kKVBytes / 2) + (k & 3) * 32), kIdescS, k > 0 ? 1u : 0u);
           umma_commit(&s_full[s]);
+          umma_commit(&k_free[ks]);
         }
         if (i > 0) {
-          const int ip = i - 1, sp = ip & 1;
-          if (!mbar_wait(&p_full[sp], (ip >> 1) & 1, wait_ns) || !mbar_wait(&v_full[sp], (ip >> 1) & 1, wait_ns)) {
+          const int ip = i - 1, sp = ip % kStages, vs = sp;
+          if (!mbar_wait(&p_full[sp], static_cast<uint32_t>((ip / kStages) & 1), wait_ns) ||
+              !mbar_wait(&v_full[vs], static_cast<uint32_t>((ip / kStages) & 1), wait_ns)) {
             fail(DEV_WAIT_TIMEOUT_MMA);
             break;
           }
           tc_fence_after_sync();
-          const uint32_t va = smem_u32(smem + kOffV + sp * kKVBytes);
+          const uint32_t va = smem_u32(smem + kOffV + vs * kKVBytes);
 #pragma unroll
           for (int k = 0; k < kKeys / 16; ++k)  // P: 16 keys = 8 packed columns per step
             umma_f16_ts(tbase + kColO, tbase + kColS + sp * kKeys + k * 8,
                         sdesc_mnmajor_sw128(va + k * 16 * 128, kKVBytes / 2, 1024), kIdescO, (ip > 0 || k > 0) ? 1u : 0u);
           umma_commit(&pv_done[sp]);
+          umma_commit(&v_free[vs]);
         }
       }
       // every MMA issued above has finished before TMEM is released
@@ -243,11 +318,14 @@ __global__ void __launch_bounds__(192, 2)
     named_barrier_sync(1, 160);
     const uint32_t trow = tbase + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
     const bool valid = r < rows;
-    const int pos = branch ? INT_MAX : t0 + (valid ? r / G : 0);
+    // padding rows (r >= rows) take the same path as the tile's last token: their Q is zero and
+    // their output is never written, and keeping the warp on one path keeps it in step
+    const int pos = branch ? INT_MAX : t0 + r / G;
     const int tt = valid ? r / G : 0;
     for (int i = 0; i < my_n; ++i) {
-      const int s = i & 1, b = rank + i * csk;
-      const bool ok = __all_sync(0xffffffffu, !*abort_flag && mbar_wait(&s_full[s], (i >> 1) & 1, wait_ns));
+      const int s = i % kStages, b = block_of(i);
+      const bool ok = __all_sync(0xffffffffu, !*abort_flag &&
+                                                  mbar_wait(&s_full[s], static_cast<uint32_t>((i / kStages) & 1), wait_ns));
       if (!ok) {
         if (lane == 0) fail(DEV_WAIT_TIMEOUT_MMA);
         break;
@@ -260,7 +338,7 @@ __global__ void __launch_bounds__(192, 2)
       const bool local = b >= nbp;
       const int j0 = b * kKeys;
       // a prefix block wholly below the causal edge needs no per-key test
-      const bool all_vis = valid && !local && j0 + kKeys <= pf_keys && j0 + kKeys - 1 <= pos;
+      const bool all_vis = !local && j0 + kKeys <= pf_keys && j0 + kKeys - 1 <= pos;
       float mb = -INFINITY;
       if (all_vis) {
 #pragma unroll
@@ -270,7 +348,7 @@ __global__ void __launch_bounds__(192, 2)
         if (local && valid) mk = a.tile_mask[static_cast<size_t>(ch0 + b - nbp) * a.tpt + tt];
 #pragma unroll
         for (int c = 0; c < kKeys; ++c) {
-          const bool vis = valid && (local ? ((mk >> c) & 1ull) != 0ull : (j0 + c < pf_keys && j0 + c <= pos));
+          const bool vis = local ? ((mk >> c) & 1ull) != 0ull : (j0 + c < pf_keys && j0 + c <= pos);
           sv[c] = vis ? sv[c] : -INFINITY;
           mb = fmaxf(mb, sv[c]);
         }
@@ -280,7 +358,8 @@ __global__ void __launch_bounds__(192, 2)
         const float m_new = fmaxf(m_ref, mb);
         const float f = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_new);
         if (i > 0) {  // O holds blocks 0 .. i-1 once their last P V is done
-          if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[(i - 1) & 1], ((i - 1) >> 1) & 1, wait_ns))) {
+          if (!__all_sync(0xffffffffu, mbar_wait(&pv_done[(i - 1) % kStages],
+                                                 static_cast<uint32_t>(((i - 1) / kStages) & 1), wait_ns))) {
             if (lane == 0) fail(DEV_WAIT_TIMEOUT_MMA);
             break;
           }
@@ -314,20 +393,23 @@ __global__ void __launch_bounds__(192, 2)
       mbar_arrive(&p_full[s]);
     }
     have_o = my_n > 0 && !*abort_flag;
-    if (have_o && !mbar_wait(&pv_done[(my_n - 1) & 1], ((my_n - 1) >> 1) & 1, wait_ns)) {
+    if (have_o && !mbar_wait(&pv_done[(my_n - 1) % kStages], static_cast<uint32_t>(((my_n - 1) / kStages) & 1),
+                             wait_ns)) {
       if (lane == 0) fail(DEV_WAIT_TIMEOUT_MMA);
       have_o = false;
     }
     have_o = __all_sync(0xffffffffu, have_o);
     tc_fence_after_sync();
     if (csk == 1) {
+      // normalised rows staged in shared memory (every MMA is done: Q, K and V
+      // are free), then one bulk copy per 256-byte output row
       const float il = l > 0.f ? 1.f / l : 0.f;
-      const size_t base = static_cast<size_t>(qrow0 + tt) * a.ld_out + (hk * G + (valid ? r % G : 0)) * kDH;
+      uint8_t* shi = smem + r * kOutLd;
+      uint8_t* slo = smem + (kRows + r) * kOutLd;
 #pragma unroll 1
       for (int q = 0; q < kDH / 32 && have_o; ++q) {
         float ov[32];
         tmem_ld_32cols(trow + kColO + q * 32, ov);
-        if (!valid) continue;
 #pragma unroll
         for (int c8 = 0; c8 < 4; ++c8) {
           uint32_t w[4], wl[4];
@@ -338,10 +420,17 @@ __global__ void __launch_bounds__(192, 2)
             const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&w[x]));
             wl[x] = pack2(y0 - h.x, y1 - h.y);
           }
-          const size_t o = base + q * 32 + c8 * 8;
-          *reinterpret_cast<uint4*>(a.out + o) = make_uint4(w[0], w[1], w[2], w[3]);
-          if (a.out_lo) *reinterpret_cast<uint4*>(a.out_lo + o) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
+          *reinterpret_cast<uint4*>(shi + q * 64 + c8 * 16) = make_uint4(w[0], w[1], w[2], w[3]);
+          *reinterpret_cast<uint4*>(slo + q * 64 + c8 * 16) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
         }
+      }
+      if (have_o && valid) {
+        fence_proxy_async_smem();
+        const size_t base = static_cast<size_t>(qrow0 + tt) * a.ld_out + (hk * G + r % G) * kDH;
+        bulk_store_s2g(a.out + base, shi, kDH * 2);
+        if (a.out_lo) bulk_store_s2g(a.out_lo + base, slo, kDH * 2);
+        bulk_commit();
+        bulk_wait_read_all();  // the staging rows stay valid until read
       }
     }
   }
@@ -350,7 +439,7 @@ __global__ void __launch_bounds__(192, 2)
   __syncthreads();
   if (warp == 0) {
     // nothing of this CTA's copies may still be landing when it exits
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < kStages; ++s) {
       if (kissued[s] > 0) mbar_wait(&k_full[s], static_cast<uint32_t>((kissued[s] - 1) & 1), wait_ns);
       if (vissued[s] > 0) mbar_wait(&v_full[s], static_cast<uint32_t>((vissued[s] - 1) & 1), wait_ns);
     }
