@@ -261,39 +261,58 @@ __global__ void __launch_bounds__(192, 1)
       constexpr uint32_t kIdescS = idesc_f16_f32(kRows, kKeys);
       constexpr uint32_t kIdescO = idesc_f16_f32(kRows, kDH) | (1u << 16);  // B (V) is MN-major
       const uint32_t qa = smem_u32(smem + kOffQ);
-      for (int i = 0; i <= my_n && !*abort_flag; ++i) {
-        if (i < my_n) {
-          const int s = i % kStages, ks = s;
-          // S/P columns s are free once the P V of block i - kStages is done
-          if (!mbar_wait(&k_full[ks], static_cast<uint32_t>((i / kStages) & 1), wait_ns) ||
-              (i >= kStages && !mbar_wait(&pv_done[s], static_cast<uint32_t>(((i - kStages) / kStages) & 1), wait_ns))) {
-            fail(DEV_WAIT_TIMEOUT_MMA);
-            break;
-          }
-          tc_fence_after_sync();
-          const uint32_t ka = smem_u32(smem + kOffK + ks * kKVBytes);
+      // S of block ns and P V of block npv are issued as soon as their inputs
+      // are ready, in block order each: neither waits behind the other
+      int ns = 0, npv = 0;
+      uint64_t t_last = globaltimer_ns();
+      uint32_t spins = 0;
+      while (npv < my_n) {
+        bool progressed = false;
+        if (ns < my_n) {
+          const int s = ns % kStages;
+          // S/P columns s are free once the P V of block ns - kStages is done
+          if (mbar_test(&k_full[s], static_cast<uint32_t>((ns / kStages) & 1)) &&
+              (ns < kStages || mbar_test(&pv_done[s], static_cast<uint32_t>(((ns - kStages) / kStages) & 1)))) {
+            tc_fence_after_sync();
+            const uint32_t ka = smem_u32(smem + kOffK + s * kKVBytes);
 #pragma unroll
-          for (int k = 0; k < kDH / 16; ++k)
-            umma_f16(tbase + kColS + s * kKeys, sdesc_kmajor_sw128(qa + (k >> 2) * (kQBytes / 2) + (k & 3) * 32),
-                     sdesc_kmajor_sw128(ka + (k >> 2) * (kKVBytes / 2) + (k & 3) * 32), kIdescS, k > 0 ? 1u : 0u);
-          umma_commit(&s_full[s]);
-          umma_commit(&k_free[ks]);
+            for (int k = 0; k < kDH / 16; ++k)
+              umma_f16(tbase + kColS + s * kKeys, sdesc_kmajor_sw128(qa + (k >> 2) * (kQBytes / 2) + (k & 3) * 32),
+                       sdesc_kmajor_sw128(ka + (k >> 2) * (kKVBytes / 2) + (k & 3) * 32), kIdescS, k > 0 ? 1u : 0u);
+            umma_commit(&s_full[s]);
+            umma_commit(&k_free[s]);
+            ++ns;
+            progressed = true;
+          }
         }
-        if (i > 0) {
-          const int ip = i - 1, sp = ip % kStages, vs = sp;
-          if (!mbar_wait(&p_full[sp], static_cast<uint32_t>((ip / kStages) & 1), wait_ns) ||
-              !mbar_wait(&v_full[vs], static_cast<uint32_t>((ip / kStages) & 1), wait_ns)) {
+        if (npv < ns) {
+          const int sp = npv % kStages;
+          const uint32_t par = static_cast<uint32_t>((npv / kStages) & 1);
+          if (mbar_test(&p_full[sp], par) && mbar_test(&v_full[sp], par)) {
+            tc_fence_after_sync();
+            const uint32_t va = smem_u32(smem + kOffV + sp * kKVBytes);
+#pragma unroll
+            for (int k = 0; k < kKeys / 16; ++k)  // P: 16 keys = 8 packed columns per step
+              umma_f16_ts(tbase + kColO, tbase + kColS + sp * kKeys + k * 8,
+                          sdesc_mnmajor_sw128(va + k * 16 * 128, kKVBytes / 2, 1024), kIdescO,
+                          (npv > 0 || k > 0) ? 1u : 0u);
+            umma_commit(&pv_done[sp]);
+            umma_commit(&v_free[sp]);
+            ++npv;
+            progressed = true;
+          }
+        }
+        if (progressed) {
+          t_last = globaltimer_ns();
+          continue;
+        }
+        __nanosleep(32);  // leave the issue slots to the softmax warp that shares this scheduler
+        if ((++spins & 63) == 0) {
+          if (*abort_flag) break;
+          if (globaltimer_ns() - t_last > wait_ns) {
             fail(DEV_WAIT_TIMEOUT_MMA);
             break;
           }
-          tc_fence_after_sync();
-          const uint32_t va = smem_u32(smem + kOffV + vs * kKVBytes);
-#pragma unroll
-          for (int k = 0; k < kKeys / 16; ++k)  // P: 16 keys = 8 packed columns per step
-            umma_f16_ts(tbase + kColO, tbase + kColS + sp * kKeys + k * 8,
-                        sdesc_mnmajor_sw128(va + k * 16 * 128, kKVBytes / 2, 1024), kIdescO, (ip > 0 || k > 0) ? 1u : 0u);
-          umma_commit(&pv_done[sp]);
-          umma_commit(&v_free[vs]);
         }
       }
       // every MMA issued above has finished before TMEM is released
@@ -322,6 +341,8 @@ __global__ void __launch_bounds__(192, 1)
     // their output is never written, and keeping the warp on one path keeps it in step
     const int pos = branch ? INT_MAX : t0 + r / G;
     const int tt = valid ? r / G : 0;
+    // the visibility mask of the tile's first ancestor chunk, loaded ahead
+    const unsigned long long mk0 = (valid && nb > nbp) ? a.tile_mask[static_cast<size_t>(ch0) * a.tpt + tt] : 0ull;
     for (int i = 0; i < my_n; ++i) {
       const int s = i % kStages, b = block_of(i);
       const bool ok = __all_sync(0xffffffffu, !*abort_flag &&
@@ -345,7 +366,7 @@ __global__ void __launch_bounds__(192, 1)
         for (int c = 0; c < kKeys; ++c) mb = fmaxf(mb, sv[c]);
       } else {
         unsigned long long mk = 0ull;
-        if (local && valid) mk = a.tile_mask[static_cast<size_t>(ch0 + b - nbp) * a.tpt + tt];
+        if (local && valid) mk = b == nbp ? mk0 : a.tile_mask[static_cast<size_t>(ch0 + b - nbp) * a.tpt + tt];
 #pragma unroll
         for (int c = 0; c < kKeys; ++c) {
           const bool vis = local ? ((mk >> c) & 1ull) != 0ull : (j0 + c < pf_keys && j0 + c <= pos);
