@@ -711,9 +711,12 @@ int launch_gemm(const GemmShape& s, int epi, const EpiArgs& e, const GemmTiling&
 GemmTiling choose_tiling(int M, int N, int K, int epi, int sms) {
   const int nkb = K / 64;
   const int mtiles = ceil_div(M, 128);
+  // clusters share B through L2 multicast, but every SM still takes the whole
+  // tile into its shared memory; measured on 825-row shapes they never beat
+  // single CTAs, so they are off unless PCD_GEMM_MAX_CS allows them
   static const int max_cs = [] {
     const char* e = std::getenv("PCD_GEMM_MAX_CS");
-    return e ? std::max(1, std::atoi(e)) : 4;
+    return e ? std::max(1, std::atoi(e)) : 1;
   }();
   GemmTiling best;
   best.mt = 1;
@@ -724,14 +727,18 @@ GemmTiling choose_tiling(int M, int N, int K, int epi, int sms) {
     for (int bn : {128, 256}) {
       const int nt = ceil_div(N, bn);
       const int groups = ceil_div(mtiles, cs);
-      const int max_split = (epi == EPI_F32_ATOMIC) ? std::max(1, nkb / 3) : 1;
-      for (int sp = 1; sp <= max_split; sp *= 2) {
-        const int units = groups * nt * sp;         // each unit occupies cs SMs
-        const int slots = std::max(1, sms / cs);    // units running at once
+      const int max_split = (epi == EPI_F32_ATOMIC) ? std::max(1, std::min(16, nkb / 3)) : 1;
+      for (int sp = 1; sp <= max_split; ++sp) {
+        const int units = groups * nt * sp;       // each unit occupies cs SMs
+        const int slots = std::max(1, sms / cs);  // units running at once
         const int kbs = ceil_div(nkb, sp);
+        // cycles per 64-deep k block: the MMA, or filling shared memory with
+        // the A and B tiles at ~55 B/clk per SM (measured with every SM loading)
         const double mma = 128.0 * bn * 128.0 / 8192.0;
-        const double fill = (128.0 + static_cast<double>(bn) / cs) * 128.0 / 60.0;
-        const double per_unit = kbs * std::max(mma, fill) + 2500.0 + (cs > 1 ? 500.0 : 0.0);
+        const double fill = (128.0 + bn) * 128.0 / 55.0;
+        // a unit's fixed cost: pipeline ramp, plus the fp32 atomics of a split-K epilogue
+        const double fixed = (epi == EPI_F32_ATOMIC) ? 7000.0 : 2500.0;
+        const double per_unit = kbs * std::max(mma, fill) + fixed + (cs > 1 ? 500.0 : 0.0);
         const double tt = ceil_div(units, slots) * per_unit + (sp > 1 ? 400.0 : 0.0);
         if (tt < best_t * 0.97) {
           best_t = tt;
