@@ -120,7 +120,7 @@ struct pcd_model {
   float2* rope = nullptr;
   int* d_err = nullptr;
   uint64_t wait_ns = 2000000000ull;
-  DevBuf x32, xn, xn_lo, qkv, q, kb, vb, att, att_lo, hb, hb_lo, hr_lo, part_o, part_ml, hr, ro_part, z, lse, plan_buf,
+  DevBuf x32, xn, xn_lo, qkv, q, q_lo, kb, vb, kb_lo, vb_lo, att, att_lo, hb, hb_lo, hr_lo, part_o, part_ml, hr, ro_part, z, lse, plan_buf,
       result, ids;
   // pinned staging: `up` feeds host->device copies (reused only once the last
   // copy from it has completed: up_ev), `down` receives results
@@ -140,12 +140,14 @@ struct pcd_model {
   // CUDA graphs of whole passes, keyed by everything a pass's launches bake in
   bool graphs = true;
   bool own_stream = false;
-  // which fp16 GEMM inputs also carry their rounding remainder (hi + lo):
+  // which fp16 operands also carry their rounding remainder (hi + lo):
   // 1 branch rows' QKV input, 64 prefix rows' QKV input, 128 every attention
   // output (the O projection's input), 32 branch rows' gate/up input, 2
   // prefill normalised inputs, 4 branch attention and SwiGLU outputs, 8
-  // prefill attention and SwiGLU outputs, 16 the readout rows
-  int split_act = 1 | 16 | 64 | 128;
+  // prefill attention and SwiGLU outputs, 16 the readout rows, 256 q, k, v
+  // and the attention weights inside the head-dim-128 tensor-core attention
+  // (the KV cache then keeps the remainders of k and v as well)
+  int split_act = 1 | 16 | 64 | 128 | 256;
   // one tree-attention launch per layer (else split attention + merge launches),
   // on the tcgen05 tensor cores at head dim 128 (else warp-level MMA)
   bool tree_attn = true;
@@ -160,6 +162,8 @@ struct pcd_cache {
   int len = 0, cap = 0;
   act_t* k = nullptr;  // [L][Hkv][cap][dh]
   act_t* v = nullptr;
+  act_t* k_lo = nullptr;  // fp16 rounding remainders of k and v (same layout), when the model keeps them
+  act_t* v_lo = nullptr;
 };
 
 struct pcd_plan {
@@ -169,6 +173,12 @@ struct pcd_plan {
 };
 
 namespace {
+
+int tree_tile_rows(const pcd_model* m);
+// q, k, v and P carry their fp16 remainders through the tensor-core attention
+bool kv_lo(const pcd_model* m);
+// a remainder workspace when the model keeps remainders, else nullptr
+inline act_t* lo_buf(const pcd_model* m, const DevBuf& b) { return kv_lo(m) ? static_cast<act_t*>(b.p) : nullptr; }
 
 // ----------------------------------------------------------------- helpers
 int ensure_pinned(void*& buf, size_t& cap, size_t bytes) {
@@ -313,9 +323,11 @@ struct KVDest {
   int row0;
   int pos_base;
   const int32_t* rel;
+  act_t* k_lo = nullptr;  // remainders of k and v, or nullptr
+  act_t* v_lo = nullptr;
 };
 int gemm_qkv_rope(pcd_model* m, int cls, const act_t* A, int M, const act_t* W, const act_t* A_lo, int lo_row0,
-                  act_t* q, int split_row, const KVDest& d0, const KVDest& d1) {
+                  act_t* q, int split_row, const KVDest& d0, const KVDest& d1, act_t* q_lo = nullptr) {
   if (M <= 0) return PCD_OK;
   auto key = std::make_tuple(M, m->Nqkv, m->d, pcd::EPI_QKV_ROPE + (A_lo ? 100 : 0));
   auto it = m->tilings.find(key);
@@ -343,11 +355,14 @@ int gemm_qkv_rope(pcd_model* m, int cls, const act_t* A, int M, const act_t* W, 
   for (int i = 0; i < 2; ++i) {
     e.kv_k[i] = ds[i]->k;
     e.kv_v[i] = ds[i]->v;
+    e.kv_k_lo[i] = ds[i]->k_lo;
+    e.kv_v_lo[i] = ds[i]->v_lo;
     e.kv_stride[i] = ds[i]->stride;
     e.kv_row0[i] = ds[i]->row0;
     e.pos_base[i] = ds[i]->pos_base;
     e.pos_rel[i] = ds[i]->rel;
   }
+  e.q_lo = q_lo;
   e.err = m->d_err;
   PCD_LAUNCH(timed(m, cls, [&] {
     return pcd::launch_gemm(s, pcd::EPI_QKV_ROPE, e, t, m->stream, m->d_err, m->wait_ns, m->sms);
@@ -363,6 +378,7 @@ int ensure_workspace(pcd_model* m, int T) {
   PCD_TRY(ensure(m->qkv, t * m->Nqkv * 4));
   if (m->qkv.p != old_qkv) PCD_CUDA(cudaMemsetAsync(m->qkv.p, 0, m->qkv.n, m->stream));
   PCD_TRY(ensure(m->q, t * m->qdim * 2));
+  if (kv_lo(m)) PCD_TRY(ensure(m->q_lo, t * m->qdim * 2));
   PCD_TRY(ensure(m->att, t * m->qdim * 2));
   PCD_TRY(ensure(m->hb, t * m->Fp * 2));
   PCD_TRY(ensure(m->xn_lo, t * m->d * 2));
@@ -419,7 +435,8 @@ int record_prefill(pcd_model* m, const int32_t* d_ids, int n, pcd_cache* c, int 
       return pcd::launch_rmsnorm(x, m->d, nullptr, n, m->d, W.attn_norm, m->cfg.rms_eps, xn, m->d, m->stream, xlo);
     }));
     if (m->dh == 128) {
-      const KVDest d0{c->k + l * layer_kv, c->v + l * layer_kv, c->cap, p0, p0, nullptr};
+      const KVDest d0{c->k + l * layer_kv, c->v + l * layer_kv, c->cap, p0, p0, nullptr,
+                      c->k_lo ? c->k_lo + l * layer_kv : nullptr, c->v_lo ? c->v_lo + l * layer_kv : nullptr};
       PCD_TRY(gemm_qkv_rope(m, PROF_GEMM_PREFILL, xn, n, W.wqkv, xlo, 0, q, n, d0, d0));
     } else {
     PCD_TRY(gemm(m, PROF_GEMM_PREFILL, xn, n, m->d, W.wqkv, m->Nqkv, m->d, m->d, pcd::EPI_F32_STORE, qkv, m->Nqkv, xlo));
@@ -505,7 +522,6 @@ struct Segment {
   int t0, t1;  // branch tokens of this request
 };
 
-int tree_tile_rows(const pcd_model* m);
 int launch_tree(pcd_model* m, const pcd::TreeAttnArgs& ta, const pcd_cache* c, int l);
 
 int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_seg, float* d_result, int splits,
@@ -517,6 +533,10 @@ int run_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_seg, 
   PCD_TRY(ensure_workspace(m, T));
   PCD_TRY(ensure(m->kb, static_cast<size_t>(m->Hkv) * T * m->dh * 2));
   PCD_TRY(ensure(m->vb, static_cast<size_t>(m->Hkv) * T * m->dh * 2));
+  if (kv_lo(m)) {
+    PCD_TRY(ensure(m->kb_lo, static_cast<size_t>(m->Hkv) * T * m->dh * 2));
+    PCD_TRY(ensure(m->vb_lo, static_cast<size_t>(m->Hkv) * T * m->dh * 2));
+  }
   PCD_TRY(ensure(m->xn_lo, static_cast<size_t>(T) * m->d * 2));
   int max_lp = 0;
   for (int s = 0; s < n_seg; ++s) max_lp = std::max(max_lp, segs[s].c->len);
@@ -597,8 +617,8 @@ int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_se
       return pcd::launch_rmsnorm(x, m->d, nullptr, T, m->d, W.attn_norm, m->cfg.rms_eps, xn, m->d, m->stream, xlo);
     }));
     if (m->dh == 128 && n_seg == 1) {
-      const KVDest d1{kb, vb, T, 0, segs[0].c->len, p.rel};
-      PCD_TRY(gemm_qkv_rope(m, PROF_GEMM_BRANCH, xn, T, W.wqkv, xlo, 0, q, 0, d1, d1));
+      const KVDest d1{kb, vb, T, 0, segs[0].c->len, p.rel, lo_buf(m, m->kb_lo), lo_buf(m, m->vb_lo)};
+      PCD_TRY(gemm_qkv_rope(m, PROF_GEMM_BRANCH, xn, T, W.wqkv, xlo, 0, q, 0, d1, d1, lo_buf(m, m->q_lo)));
     } else {
     PCD_TRY(gemm(m, PROF_GEMM_BRANCH, xn, T, m->d, W.wqkv, m->Nqkv, m->d, m->d, pcd::EPI_F32_STORE, qkv, m->Nqkv, xlo));
     for (int s = 0; s < n_seg; ++s) {
@@ -755,6 +775,10 @@ int run_single(pcd_model* m, const PlanView& p, const int32_t* d_ids, int n, pcd
   PCD_TRY(ensure_workspace(m, N));
   PCD_TRY(ensure(m->kb, static_cast<size_t>(m->Hkv) * T * m->dh * 2));
   PCD_TRY(ensure(m->vb, static_cast<size_t>(m->Hkv) * T * m->dh * 2));
+  if (kv_lo(m)) {
+    PCD_TRY(ensure(m->kb_lo, static_cast<size_t>(m->Hkv) * T * m->dh * 2));
+    PCD_TRY(ensure(m->vb_lo, static_cast<size_t>(m->Hkv) * T * m->dh * 2));
+  }
   PCD_TRY(ensure(m->ids, static_cast<size_t>(n) * 4));
   if (d_ids != m->ids.p)
     PCD_CUDA(cudaMemcpyAsync(m->ids.p, d_ids, static_cast<size_t>(n) * 4, cudaMemcpyDeviceToDevice, m->stream));
@@ -812,9 +836,10 @@ int record_single(pcd_model* m, const PlanView& p, const int32_t* ids, int n, pc
     }));
     if (m->dh == 128) {
       // RoPE in the projection's epilogue: prefix rows -> the cache, branch rows -> the branch scratch
-      const KVDest d0{c->k + l * layer_kv, c->v + l * layer_kv, c->cap, 0, 0, nullptr};
-      const KVDest d1{kb, vb, T, 0, n, p.rel};
-      PCD_TRY(gemm_qkv_rope(m, PROF_GEMM_SINGLE, xn, N, W.wqkv, xlo, qkv_lo_row0, q, n, d0, d1));
+      const KVDest d0{c->k + l * layer_kv, c->v + l * layer_kv, c->cap, 0, 0, nullptr,
+                      c->k_lo ? c->k_lo + l * layer_kv : nullptr, c->v_lo ? c->v_lo + l * layer_kv : nullptr};
+      const KVDest d1{kb, vb, T, 0, n, p.rel, lo_buf(m, m->kb_lo), lo_buf(m, m->vb_lo)};
+      PCD_TRY(gemm_qkv_rope(m, PROF_GEMM_SINGLE, xn, N, W.wqkv, xlo, qkv_lo_row0, q, n, d0, d1, lo_buf(m, m->q_lo)));
     } else {
     PCD_TRY(gemm(m, PROF_GEMM_SINGLE, xn, N, m->d, W.wqkv, m->Nqkv, m->d, m->d, pcd::EPI_F32_STORE, qkv, m->Nqkv, xlo,
                  nullptr, qkv_lo_row0));
@@ -1011,6 +1036,7 @@ int record_single(pcd_model* m, const PlanView& p, const int32_t* ids, int n, pc
 // Query rows per tree-attention tile: 128 for the tensor-core kernel, 64 for
 // the warp-MMA one.
 int tree_tile_rows(const pcd_model* m) { return (m->tree_attn && m->attn_tc && m->dh == 128) ? 128 : 64; }
+bool kv_lo(const pcd_model* m) { return tree_tile_rows(m) == 128 && (m->split_act & 256) != 0; }
 
 // One tree-attention launch over the prefix cache `c` at layer l.
 int launch_tree(pcd_model* m, const pcd::TreeAttnArgs& ta, const pcd_cache* c, int l) {
@@ -1020,7 +1046,19 @@ int launch_tree(pcd_model* m, const pcd::TreeAttnArgs& ta, const pcd_cache* c, i
     if (!pcd::make_kv_map(&mk, c->k, m->dh, ta.n_keys, m->Hkv, c->cap, m->L, layer_elems) ||
         !pcd::make_kv_map(&mv, c->v, m->dh, ta.n_keys, m->Hkv, c->cap, m->L, layer_elems))
       return cudaErrorInvalidValue;
-    return pcd::launch_tree_attention_tc(ta, mk, mv, l, m->wait_ns, m->d_err, m->stream);
+    if (kv_lo(m) && c->k_lo && c->v_lo) {
+      // q, k, v and P with their remainders: q and the branch keys' from this pass's projection
+      CUtensorMap mkl, mvl;
+      if (!pcd::make_kv_map(&mkl, c->k_lo, m->dh, ta.n_keys, m->Hkv, c->cap, m->L, layer_elems) ||
+          !pcd::make_kv_map(&mvl, c->v_lo, m->dh, ta.n_keys, m->Hkv, c->cap, m->L, layer_elems))
+        return cudaErrorInvalidValue;
+      pcd::TreeAttnArgs t2 = ta;
+      t2.q_lo = static_cast<const act_t*>(m->q_lo.p);
+      t2.kb_lo = static_cast<const act_t*>(m->kb_lo.p);
+      t2.vb_lo = static_cast<const act_t*>(m->vb_lo.p);
+      return pcd::launch_tree_attention_tc(t2, mk, mv, &mkl, &mvl, l, m->wait_ns, m->d_err, m->stream);
+    }
+    return pcd::launch_tree_attention_tc(ta, mk, mv, nullptr, nullptr, l, m->wait_ns, m->d_err, m->stream);
   }
   return pcd::launch_tree_attention(ta, m->stream);
 }
@@ -1395,7 +1433,8 @@ const void* file_tensor(void* ctx, int, size_t bytes) {
 
 // ------------------------------------------------------------ caches
 int new_cache(pcd_model* m, int cap, pcd_cache** out) {
-  const size_t bytes = static_cast<size_t>(m->L) * m->Hkv * cap * m->dh * 2 * 2;
+  const size_t one = static_cast<size_t>(m->L) * m->Hkv * cap * m->dh;  // elements of k (or v)
+  const size_t bytes = one * 2 * (kv_lo(m) ? 4 : 2);
   void* mem = nullptr;
   size_t got = 0;
   for (size_t i = 0; i < m->cache_pool.size(); ++i) {
@@ -1421,7 +1460,11 @@ int new_cache(pcd_model* m, int cap, pcd_cache** out) {
   c->cap = cap;
   c->len = 0;
   c->k = static_cast<act_t*>(mem);
-  c->v = c->k + static_cast<size_t>(m->L) * m->Hkv * cap * m->dh;
+  c->v = c->k + one;
+  if (kv_lo(m)) {
+    c->k_lo = c->v + one;
+    c->v_lo = c->k_lo + one;
+  }
   *out = c;
   return PCD_OK;
 }
@@ -1622,7 +1665,8 @@ void pcd_model_free(pcd_model* m) {
 
 int64_t pcd_kv_bytes_per_token(const pcd_model* m) {
   if (!m) return 0;
-  return static_cast<int64_t>(m->L) * 2 * m->Hkv * m->dh * 2;
+  // k and v in fp16, and their fp16 remainders when the model keeps them
+  return static_cast<int64_t>(m->L) * 2 * m->Hkv * m->dh * 2 * (kv_lo(m) ? 2 : 1);
 }
 
 int pcd_prefill_device(pcd_model* m, const int32_t* ids_device, int n, pcd_cache** out) {
@@ -1662,9 +1706,11 @@ int pcd_prefill_extend(pcd_model* m, const pcd_cache* head, const int32_t* ids, 
   PCD_TRY(new_cache(m, total, &c));
   // copy the head's keys and values: per (layer, KV head) a block of head->len rows
   const size_t row = static_cast<size_t>(m->dh) * 2;
-  for (act_t* const* pair : {&c->k, &c->v}) {
-    const act_t* src = (pair == &c->k) ? head->k : head->v;
-    const cudaError_t e = cudaMemcpy2DAsync(*pair, static_cast<size_t>(c->cap) * row, src,
+  const std::pair<act_t*, const act_t*> parts[4] = {{c->k, head->k}, {c->v, head->v}, {c->k_lo, head->k_lo},
+                                                     {c->v_lo, head->v_lo}};
+  for (const auto& pr : parts) {
+    if (!pr.first || !pr.second) continue;
+    const cudaError_t e = cudaMemcpy2DAsync(pr.first, static_cast<size_t>(c->cap) * row, pr.second,
                                             static_cast<size_t>(head->cap) * row, head->len * row,
                                             static_cast<size_t>(m->L) * m->Hkv, cudaMemcpyDeviceToDevice, m->stream);
     if (e != cudaSuccess) {

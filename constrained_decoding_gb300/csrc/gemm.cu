@@ -171,12 +171,17 @@ __device__ __forceinline__ void epi_qkv_rope(const GemmParams& p, const EpiArgs&
     if (head * 128 >= p.N) break;  // uniform across the warp
     const bool is_v = head >= e.n_q_heads + e.n_kv_heads;
     act_t* out;
+    act_t* out_lo;  // the remainder's row, or nullptr
     if (head < e.n_q_heads) {
-      out = e.q_out + static_cast<size_t>(row) * e.n_q_heads * 128 + head * 128;
+      const size_t o = static_cast<size_t>(row) * e.n_q_heads * 128 + head * 128;
+      out = e.q_out + o;
+      out_lo = e.q_lo ? e.q_lo + o : nullptr;
     } else {
       const int kh = is_v ? head - e.n_q_heads - e.n_kv_heads : head - e.n_q_heads;
-      act_t* base = is_v ? e.kv_v[dst] : e.kv_k[dst];
-      out = base + (static_cast<size_t>(kh) * e.kv_stride[dst] + e.kv_row0[dst] + r2) * 128;
+      const size_t o = (static_cast<size_t>(kh) * e.kv_stride[dst] + e.kv_row0[dst] + r2) * 128;
+      out = (is_v ? e.kv_v[dst] : e.kv_k[dst]) + o;
+      act_t* lb = is_v ? e.kv_v_lo[dst] : e.kv_k_lo[dst];
+      out_lo = lb ? lb + o : nullptr;
     }
 #pragma unroll 1
     for (int half = 0; half < 2; ++half) {
@@ -201,6 +206,22 @@ __device__ __forceinline__ void epi_qkv_rope(const GemmParams& p, const EpiArgs&
                            pack2(a[8 * j + 6], a[8 * j + 7]));
         o2[j] = make_uint4(pack2(b[8 * j], b[8 * j + 1]), pack2(b[8 * j + 2], b[8 * j + 3]), pack2(b[8 * j + 4], b[8 * j + 5]),
                            pack2(b[8 * j + 6], b[8 * j + 7]));
+      }
+      if (out_lo) {  // value - fp16(value), itself rounded to fp16
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          a[j] -= a2f(f2a(a[j]));
+          b[j] -= a2f(f2a(b[j]));
+        }
+        uint4* l1 = reinterpret_cast<uint4*>(out_lo + half * 32);
+        uint4* l2 = reinterpret_cast<uint4*>(out_lo + 64 + half * 32);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          l1[j] = make_uint4(pack2(a[8 * j], a[8 * j + 1]), pack2(a[8 * j + 2], a[8 * j + 3]),
+                             pack2(a[8 * j + 4], a[8 * j + 5]), pack2(a[8 * j + 6], a[8 * j + 7]));
+          l2[j] = make_uint4(pack2(b[8 * j], b[8 * j + 1]), pack2(b[8 * j + 2], b[8 * j + 3]),
+                             pack2(b[8 * j + 4], b[8 * j + 5]), pack2(b[8 * j + 6], b[8 * j + 7]));
+        }
       }
     }
   }

@@ -48,6 +48,10 @@ struct EpiArgs {
   int split_row = 0;              // rows < split_row use destination 0, the rest destination 1
   act_t_storage* kv_k[2] = {nullptr, nullptr};  // key of (head h, row r') at kv_k[d] + (h * kv_stride[d] + kv_row0[d] + r') * 128
   act_t_storage* kv_v[2] = {nullptr, nullptr};
+  // optional fp16 rounding remainders of q, k and v (same layouts as q_out, kv_k, kv_v)
+  act_t_storage* q_lo = nullptr;
+  act_t_storage* kv_k_lo[2] = {nullptr, nullptr};
+  act_t_storage* kv_v_lo[2] = {nullptr, nullptr};
   int64_t kv_stride[2] = {0, 0};
   int kv_row0[2] = {0, 0};
   int pos_base[2] = {0, 0};       // position = pos_base[d] + (pos_rel[d] ? pos_rel[d][r'] : r'), r' = row - (d ? split_row : 0)

@@ -99,6 +99,9 @@ struct TreeAttnArgs {
   int n_keys;
   const act_t* kb;              // branch keys/values [Hkv][n_br][DH]
   const act_t* vb;
+  const act_t* q_lo = nullptr;   // fp16 remainders of q, kb, vb (tensor-core kernel only), or nullptr
+  const act_t* kb_lo = nullptr;
+  const act_t* vb_lo = nullptr;
   const int32_t* tile_chunk_off;            // [n_br_tiles + 1] ancestor chunks of each branch tile
   const int32_t* tile_keys;                 // [chunks][64] branch key index, -1 past the union's end
   const unsigned long long* tile_mask;      // [chunks][tpt] bit i: key i of the chunk is visible to the token
@@ -108,10 +111,13 @@ struct TreeAttnArgs {
 int launch_tree_attention(const TreeAttnArgs& a, cudaStream_t s);
 // The same on the tcgen05 tensor cores, head dim 128, tiles of tpt x G <= 128
 // rows.  tmK / tmV map the prefix cache (make_kv_map: rows past n_keys read
-// as zero); `layer` selects its layer.  Pipeline waits give up after wait_ns
-// and record an error code in *err.
-int launch_tree_attention_tc(const TreeAttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, int layer,
-                             uint64_t wait_ns, int* err, cudaStream_t s);
+// as zero); `layer` selects its layer.  With q_lo set, q, k, v and the
+// attention weights carry their fp16 remainders (tmKlo / tmVlo map the
+// cache's, kb_lo / vb_lo hold the branch keys').  Pipeline waits give up
+// after wait_ns and record an error code in *err.
+int launch_tree_attention_tc(const TreeAttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                             const CUtensorMap* tmKlo, const CUtensorMap* tmVlo, int layer, uint64_t wait_ns, int* err,
+                             cudaStream_t s);
 // CTAs per (tile, KV head) for the warp-MMA (tc = false) or tensor-core
 // kernel: the key blocks of the heaviest tile (max_blocks) against the waves
 // of CTAs the cluster split adds.

@@ -36,30 +36,47 @@ constexpr int kKeys = 64;                    // keys per block
 constexpr int kQBytes = kRows * kDH * 2;     // two 64-column halves of 16 KB
 constexpr int kKVBytes = kKeys * kDH * 2;    // two 64-column halves of 8 KB
 constexpr int kOffQ = 0;
-constexpr int kStages = 4;                   // K and V stages: the loads run ahead of the MMAs
-constexpr int kOffK = kQBytes;
-constexpr int kOffV = kOffK + kStages * kKVBytes;
-constexpr int kOffBar = kOffV + kStages * kKVBytes;
 constexpr int kOutLd = kDH * 2 + 16;         // staged output row (bytes): padded against bank conflicts
-static_assert(2 * kRows * kOutLd <= kOffBar, "staged hi and lo output rows fit the Q/K/V region");
-constexpr int kOffML = kOffBar + 256;
-constexpr int kSmem = kOffML + 2048 + 1024;  // + alignment slack
 constexpr int kRedLd = kDH + 4;              // fp32 partial-O row stride for the cluster combine
-// a CTA receives ceil(128 / csk) rows from each of csk CTAs (csk <= 8)
-static_assert((kRows + 8) * kRedLd * 4 <= kOffBar, "received partial rows fit the Q/K/V region");
-static_assert((kRows + 8) * 8 <= 2048, "received (m, l) pairs fit their region");
-constexpr uint32_t kTmemCols = 512;          // S (then P): kStages x 64 columns, O: 128
-constexpr uint32_t kColS = 0, kColO = kStages * kKeys;
-constexpr bool kLoadsByCpAsync = false;      // prefix K/V blocks by cp.async instead of TMA
+constexpr uint32_t kColS = 0;
+
+// Shared and tensor memory layout.  LO: q, k, v and P also carry their fp16
+// rounding remainders (a second tile next to each), with 2 K/V stages to fit;
+// otherwise 4 stages.
+template <bool LO>
+struct TcCfg {
+  static constexpr int kStages = LO ? 2 : 4;               // K and V stages: loads run ahead of the MMAs
+  static constexpr int kQAll = kQBytes * (LO ? 2 : 1);     // Q (then Q's remainder)
+  static constexpr int kKVSt = kKVBytes * (LO ? 2 : 1);    // one K (or V) stage: hi, then lo
+  static constexpr int kOffK = kQAll;
+  static constexpr int kOffV = kOffK + kStages * kKVSt;
+  static constexpr int kOffBar = kOffV + kStages * kKVSt;
+  static constexpr int kOffML = kOffBar + 256;
+  static constexpr int kSmem = kOffML + 2048 + 1024;      // + alignment slack
+  // S (then P: hi in the first 32 columns, lo in the next 32) per stage, then O
+  static constexpr uint32_t kColO = kStages * kKeys;
+  static constexpr uint32_t kTmemCols = LO ? 256 : 512;
+  static_assert(kColO + kDH <= kTmemCols, "S stages and O fit the TMEM allocation");
+  static_assert(2 * kRows * kOutLd <= kOffBar, "staged hi and lo output rows fit the Q/K/V region");
+  static_assert((kRows + 8) * kRedLd * 4 <= kOffBar, "received partial rows fit the Q/K/V region");
+  static_assert((kRows + 8) * 8 <= 2048, "received (m, l) pairs fit their region");
+  static_assert(kSmem <= 227 * 1024, "shared memory per CTA");
+};
 constexpr float kRescale = 14.f;             // log2 headroom before m moves: P <= 2^14 stays finite in fp16
 
 __device__ __forceinline__ uint32_t swz(int row, int chunk) {  // 128-byte swizzled row of 8 16-byte chunks
   return static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
+template <bool LO>
 __global__ void __launch_bounds__(192, 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                        const __grid_constant__ CUtensorMap tmKlo, const __grid_constant__ CUtensorMap tmVlo,
                         const TreeAttnArgs a, int layer, uint64_t wait_ns, int* err) {
+  using C = TcCfg<LO>;
+  constexpr int kStages = C::kStages, kKVSt = C::kKVSt, kOffK = C::kOffK, kOffV = C::kOffV, kOffBar = C::kOffBar;
+  constexpr int kOffML = C::kOffML;
+  constexpr uint32_t kColO = C::kColO, kTmemCols = C::kTmemCols;
   extern __shared__ uint8_t tta_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(tta_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -116,6 +133,10 @@ __global__ void __launch_bounds__(192, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
+    if constexpr (LO) {
+      tma_prefetch_desc(&tmKlo);
+      tma_prefetch_desc(&tmVlo);
+    }
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -133,7 +154,7 @@ __global__ void __launch_bounds__(192, 1)
     *abort_flag = 1;
   };
   const int r = 32 * (warp & 3) + lane;  // query row (TMEM lane) of a softmax thread (warps 2-5)
-  int kissued[kStages] = {0, 0, 0, 0}, vissued[kStages] = {0, 0, 0, 0};  // loads per K / V stage (producer warp)
+  int kissued[kStages] = {}, vissued[kStages] = {};  // loads per K / V stage (producer warp)
   float m_ref = -INFINITY, l = 0.f;              // softmax state of row r
   bool have_o = false;
 
@@ -141,14 +162,19 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ K/V loads
     const act_t* kbp = a.kb + static_cast<size_t>(hk) * a.n_br * kDH;
     const act_t* vbp = a.vb + static_cast<size_t>(hk) * a.n_br * kDH;
-    // an ancestor chunk: rows of the branch K or V gathered by index, zero past the union's end
-    auto gather = [&](uint8_t* dst, const act_t* src, const int32_t* keys, uint64_t* bar) {
+    const act_t* kblp = LO ? a.kb_lo + static_cast<size_t>(hk) * a.n_br * kDH : nullptr;
+    const act_t* vblp = LO ? a.vb_lo + static_cast<size_t>(hk) * a.n_br * kDH : nullptr;
+    // an ancestor chunk: rows of the branch K or V (and remainder) gathered by
+    // index, zero past the union's end
+    auto gather = [&](uint8_t* dst, const act_t* src, const act_t* src_lo, const int32_t* keys, uint64_t* bar) {
       for (int e = lane; e < kKeys * 16; e += 32) {
         const int kr = e >> 4, c = e & 15;
         const int j = keys[kr];
         const bool ok = j >= 0 && j < a.n_br;
-        cp_async16(dst + (c >> 3) * (kKVBytes / 2) + swz(kr, c & 7), src + static_cast<size_t>(ok ? j : 0) * kDH + c * 8,
-                   ok);
+        const size_t off = static_cast<size_t>(ok ? j : 0) * kDH + c * 8;
+        const uint32_t so = (c >> 3) * (kKVBytes / 2) + swz(kr, c & 7);
+        cp_async16(dst + so, src + off, ok);
+        if constexpr (LO) cp_async16(dst + kKVBytes + so, src_lo + off, ok);
       }
       cp_async_commit();
       cp_async_wait<0>();
@@ -156,63 +182,16 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar);
     };
-    if constexpr (kLoadsByCpAsync) {
-      // every block by cp.async, K and V of a block in one commit group, up to
-      // kStages groups in flight; a block is signalled once its group is done
-      const act_t* kp = a.k + static_cast<size_t>(hk) * a.kv_head_stride * kDH;
-      const act_t* vp = a.v + static_cast<size_t>(hk) * a.kv_head_stride * kDH;
-      int sig = 0, pending = 0;
-      auto retire = [&]() {
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&k_full[sig % kStages]);
-          mbar_arrive(&v_full[sig % kStages]);
-        }
-        ++sig;
-        --pending;
-      };
-      for (int i = 0; i < my_n; ++i) {
-        if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
-        const int s = i % kStages, b = block_of(i);
-        const uint32_t fpar = static_cast<uint32_t>(((i - kStages) / kStages) & 1);
-        const int32_t* keys = b >= nbp ? a.tile_keys + static_cast<size_t>(ch0 + b - nbp) * kKeys : nullptr;
-        if (!__all_sync(0xffffffffu, i < kStages || (mbar_wait(&k_free[s], fpar, wait_ns) &&
-                                                      mbar_wait(&v_free[s], fpar, wait_ns)))) {
-          if (lane == 0) fail(DEV_WAIT_TIMEOUT_PRODUCER);
-          break;
-        }
-        uint8_t* kd = smem + kOffK + s * kKVBytes;
-        uint8_t* vd = smem + kOffV + s * kKVBytes;
-        const act_t* ksrc = keys ? kbp : kp;
-        const act_t* vsrc = keys ? vbp : vp;
-        for (int e = lane; e < kKeys * 16; e += 32) {
-          const int kr = e >> 4, c = e & 15;
-          const int j = keys ? keys[kr] : b * kKeys + kr;
-          const bool ok = keys ? (j >= 0 && j < a.n_br) : j < pf_keys;
-          const size_t off = static_cast<size_t>(ok ? j : 0) * kDH + c * 8;
-          const uint32_t so = (c >> 3) * (kKVBytes / 2) + swz(kr, c & 7);
-          cp_async16(kd + so, ksrc + off, ok);
-          cp_async16(vd + so, vsrc + off, ok);
-        }
-        cp_async_commit();
-        ++pending;
-        ++kissued[s];
-        ++vissued[s];
-        // a block is signalled before the producer waits on the stage it
-        // frees (the MMA issues S of block j before P V of block j - 1)
-        if (pending == kStages - 1) {
-          cp_async_wait<kStages - 2>();
-          retire();
-        }
+    // a prefix block by TMA: both 64-column halves, and the remainder's
+    auto tma_block = [&](uint8_t* dst, const CUtensorMap* hi, const CUtensorMap* lo, int b, uint64_t* bar) {
+      mbar_arrive_expect_tx(bar, kKVSt);
+      tma_load_4d(dst, hi, bar, 0, b * kKeys, hk, layer);
+      tma_load_4d(dst + kKVBytes / 2, hi, bar, 64, b * kKeys, hk, layer);
+      if constexpr (LO) {
+        tma_load_4d(dst + kKVBytes, lo, bar, 0, b * kKeys, hk, layer);
+        tma_load_4d(dst + kKVBytes + kKVBytes / 2, lo, bar, 64, b * kKeys, hk, layer);
       }
-      while (pending > 0) {
-        if (pending >= 3) cp_async_wait<2>();
-        else if (pending == 2) cp_async_wait<1>();
-        else cp_async_wait<0>();
-        retire();
-      }
-    } else {
+    };
     for (int i = 0; i < my_n; ++i) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
       const int s = i % kStages, b = block_of(i);
@@ -223,15 +202,11 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) fail(DEV_WAIT_TIMEOUT_PRODUCER);
         break;
       }
-      uint8_t* kd = smem + kOffK + s * kKVBytes;
+      uint8_t* kd = smem + kOffK + s * kKVSt;
       if (!keys) {
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&k_full[s], kKVBytes);
-          tma_load_4d(kd, &tmK, &k_full[s], 0, b * kKeys, hk, layer);
-          tma_load_4d(kd + kKVBytes / 2, &tmK, &k_full[s], 64, b * kKeys, hk, layer);
-        }
+        if (lane == 0) tma_block(kd, &tmK, &tmKlo, b, &k_full[s]);
       } else {
-        gather(kd, kbp, keys, &k_full[s]);
+        gather(kd, kbp, kblp, keys, &k_full[s]);
       }
       ++kissued[s];
       // the V stage is free once the P V of block i - kStages is done
@@ -239,19 +214,14 @@ __global__ void __launch_bounds__(192, 1)
         if (lane == 0) fail(DEV_WAIT_TIMEOUT_PRODUCER);
         break;
       }
-      uint8_t* vd = smem + kOffV + s * kKVBytes;
+      uint8_t* vd = smem + kOffV + s * kKVSt;
       if (!keys) {
-        if (lane == 0) {
-          mbar_arrive_expect_tx(&v_full[s], kKVBytes);
-          tma_load_4d(vd, &tmV, &v_full[s], 0, b * kKeys, hk, layer);
-          tma_load_4d(vd + kKVBytes / 2, &tmV, &v_full[s], 64, b * kKeys, hk, layer);
-        }
+        if (lane == 0) tma_block(vd, &tmV, &tmVlo, b, &v_full[s]);
       } else {
-        gather(vd, vbp, keys, &v_full[s]);
+        gather(vd, vbp, vblp, keys, &v_full[s]);
       }
       ++vissued[s];
       __syncwarp();
-    }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
@@ -274,11 +244,17 @@ __global__ void __launch_bounds__(192, 1)
           if (mbar_test(&k_full[s], static_cast<uint32_t>((ns / kStages) & 1)) &&
               (ns < kStages || mbar_test(&pv_done[s], static_cast<uint32_t>(((ns - kStages) / kStages) & 1)))) {
             tc_fence_after_sync();
-            const uint32_t ka = smem_u32(smem + kOffK + s * kKVBytes);
+            const uint32_t ka = smem_u32(smem + kOffK + s * kKVSt);
+            const uint32_t dS = tbase + kColS + s * kKeys;
 #pragma unroll
-            for (int k = 0; k < kDH / 16; ++k)
-              umma_f16(tbase + kColS + s * kKeys, sdesc_kmajor_sw128(qa + (k >> 2) * (kQBytes / 2) + (k & 3) * 32),
-                       sdesc_kmajor_sw128(ka + (k >> 2) * (kKVBytes / 2) + (k & 3) * 32), kIdescS, k > 0 ? 1u : 0u);
+            for (int k = 0; k < kDH / 16; ++k) {
+              const uint32_t qo = (k >> 2) * (kQBytes / 2) + (k & 3) * 32, ko = (k >> 2) * (kKVBytes / 2) + (k & 3) * 32;
+              umma_f16(dS, sdesc_kmajor_sw128(qa + qo), sdesc_kmajor_sw128(ka + ko), kIdescS, k > 0 ? 1u : 0u);
+              if constexpr (LO) {  // + Q K_lo + Q_lo K (the lo x lo term is below fp32 resolution of S)
+                umma_f16(dS, sdesc_kmajor_sw128(qa + qo), sdesc_kmajor_sw128(ka + kKVBytes + ko), kIdescS, 1u);
+                umma_f16(dS, sdesc_kmajor_sw128(qa + kQBytes + qo), sdesc_kmajor_sw128(ka + ko), kIdescS, 1u);
+              }
+            }
             umma_commit(&s_full[s]);
             umma_commit(&k_free[s]);
             ++ns;
@@ -290,12 +266,19 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t par = static_cast<uint32_t>((npv / kStages) & 1);
           if (mbar_test(&p_full[sp], par) && mbar_test(&v_full[sp], par)) {
             tc_fence_after_sync();
-            const uint32_t va = smem_u32(smem + kOffV + sp * kKVBytes);
+            const uint32_t va = smem_u32(smem + kOffV + sp * kKVSt);
+            const uint32_t pcol = tbase + kColS + sp * kKeys;
 #pragma unroll
-            for (int k = 0; k < kKeys / 16; ++k)  // P: 16 keys = 8 packed columns per step
-              umma_f16_ts(tbase + kColO, tbase + kColS + sp * kKeys + k * 8,
-                          sdesc_mnmajor_sw128(va + k * 16 * 128, kKVBytes / 2, 1024), kIdescO,
+            for (int k = 0; k < kKeys / 16; ++k) {  // P: 16 keys = 8 packed columns per step
+              umma_f16_ts(tbase + kColO, pcol + k * 8, sdesc_mnmajor_sw128(va + k * 16 * 128, kKVBytes / 2, 1024), kIdescO,
                           (npv > 0 || k > 0) ? 1u : 0u);
+              if constexpr (LO) {  // + P V_lo + P_lo V
+                umma_f16_ts(tbase + kColO, pcol + k * 8,
+                            sdesc_mnmajor_sw128(va + kKVBytes + k * 16 * 128, kKVBytes / 2, 1024), kIdescO, 1u);
+                umma_f16_ts(tbase + kColO, pcol + 32 + k * 8,
+                            sdesc_mnmajor_sw128(va + k * 16 * 128, kKVBytes / 2, 1024), kIdescO, 1u);
+              }
+            }
             umma_commit(&pv_done[sp]);
             umma_commit(&v_free[sp]);
             ++npv;
@@ -322,16 +305,19 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax rows
-    {  // Q tile: the thread of row r stages it, swizzled
+    {  // Q tile (and its remainder): the thread of row r stages it, swizzled
       const bool ok = r < rows;
-      const uint4* src = reinterpret_cast<const uint4*>(
-          a.q + (static_cast<size_t>(qrow0 + (ok ? r / G : 0)) * a.Hq + hk * G + (ok ? r % G : 0)) * kDH);
-      uint4 v[16];
+      const size_t qo = (static_cast<size_t>(qrow0 + (ok ? r / G : 0)) * a.Hq + hk * G + (ok ? r % G : 0)) * kDH;
+#pragma unroll 1
+      for (int part = 0; part < (LO ? 2 : 1); ++part) {
+        const uint4* src = reinterpret_cast<const uint4*>((part ? a.q_lo : a.q) + qo);
+        uint4 v[16];
 #pragma unroll
-      for (int c = 0; c < 16; ++c) v[c] = ok ? src[c] : make_uint4(0u, 0u, 0u, 0u);
+        for (int c = 0; c < 16; ++c) v[c] = ok ? src[c] : make_uint4(0u, 0u, 0u, 0u);
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
-        *reinterpret_cast<uint4*>(smem + kOffQ + (c >> 3) * (kQBytes / 2) + swz(r, c & 7)) = v[c];
+        for (int c = 0; c < 16; ++c)
+          *reinterpret_cast<uint4*>(smem + kOffQ + part * kQBytes + (c >> 3) * (kQBytes / 2) + swz(r, c & 7)) = v[c];
+      }
       fence_proxy_async_smem();
     }
     named_barrier_sync(1, 160);
@@ -407,8 +393,18 @@ __global__ void __launch_bounds__(192, 1)
         const float p1 = ex2_approx(fmaf(sv[2 * c2 + 1], a.scale_log2, -mo));
         ps += p0 + p1;
         pw[c2] = pack2(p0, p1);
+        if constexpr (LO) {  // the remainders, kept in sv for the second store
+          const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&pw[c2]));
+          sv[2 * c2] = p0 - h.x;
+          sv[2 * c2 + 1] = p1 - h.y;
+        }
       }
       tmem_st_32cols_u32(trow + kColS + s * kKeys, pw);
+      if constexpr (LO) {
+#pragma unroll
+        for (int c2 = 0; c2 < kKeys / 2; ++c2) pw[c2] = pack2(sv[2 * c2], sv[2 * c2 + 1]);
+        tmem_st_32cols_u32(trow + kColS + s * kKeys + 32, pw);
+      }
       l += ps;
       tc_fence_before_sync();
       mbar_arrive(&p_full[s]);
@@ -539,21 +535,20 @@ __global__ void __launch_bounds__(192, 1)
 
 }  // namespace
 
-int launch_tree_attention_tc(const TreeAttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, int layer,
-                             uint64_t wait_ns, int* err, cudaStream_t s) {
-  if (a.n_br_tiles + a.n_pf_tiles <= 0) return 0;
-  if (a.DH != kDH || a.csk < 1 || a.csk > 8) return cudaErrorInvalidValue;
-  if (a.tpt < 1 || a.tpt * (a.Hq / a.Hkv) > kRows) return cudaErrorInvalidValue;
+template <bool LO>
+static int launch_tc_t(const TreeAttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmKlo,
+                       const CUtensorMap& tmVlo, int layer, uint64_t wait_ns, int* err, cudaStream_t s) {
+  using C = TcCfg<LO>;
   static bool attr = false;
   if (!attr) {
-    cudaError_t r = cudaFuncSetAttribute(tree_attn_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    cudaError_t r = cudaFuncSetAttribute(tree_attn_tc_kernel<LO>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (r != cudaSuccess) return r;
     attr = true;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((a.n_br_tiles + a.n_pf_tiles) * a.csk), static_cast<unsigned>(a.Hkv), 1);
   cfg.blockDim = dim3(192, 1, 1);
-  cfg.dynamicSmemBytes = kSmem;
+  cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = s;
   cudaLaunchAttribute at[2];
   int na = 0;
@@ -571,7 +566,19 @@ int launch_tree_attention_tc(const TreeAttnArgs& a, const CUtensorMap& tmK, cons
   }
   cfg.attrs = at;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel, tmK, tmV, a, layer, wait_ns, err);
+  return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<LO>, tmK, tmV, tmKlo, tmVlo, a, layer, wait_ns, err);
+}
+
+int launch_tree_attention_tc(const TreeAttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                             const CUtensorMap* tmKlo, const CUtensorMap* tmVlo, int layer, uint64_t wait_ns, int* err,
+                             cudaStream_t s) {
+  if (a.n_br_tiles + a.n_pf_tiles <= 0) return 0;
+  if (a.DH != kDH || a.csk < 1 || a.csk > 8) return cudaErrorInvalidValue;
+  if (a.tpt < 1 || a.tpt * (a.Hq / a.Hkv) > kRows) return cudaErrorInvalidValue;
+  const bool lo = a.q_lo != nullptr;
+  if (lo && (!tmKlo || !tmVlo || !a.kb_lo || !a.vb_lo)) return cudaErrorInvalidValue;
+  if (lo) return launch_tc_t<true>(a, tmK, tmV, *tmKlo, *tmVlo, layer, wait_ns, err, s);
+  return launch_tc_t<false>(a, tmK, tmV, tmK, tmV, layer, wait_ns, err, s);
 }
 
 }  // namespace pcd

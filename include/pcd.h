@@ -144,9 +144,11 @@ int pcd_load_weights_host(const pcd_model_config* cfg, const void* const* tensor
 
 void pcd_model_free(pcd_model* m);
 
-/* Device bytes of one token's K and V over all layers (bf16): layers x 2 x
- * KV heads x head dim x 2 ("The piece of plumbing you need: the KV cache",
- * How TypeSafe's Jev Might Work). */
+/* Device bytes of one token's K and V over all layers: layers x 2 x KV heads
+ * x head dim x 2 for 16-bit k and v ("The piece of plumbing you need: the KV
+ * cache", How TypeSafe's Jev Might Work), twice that when the cache also
+ * keeps their fp16 rounding remainders (head dim 128 with the default
+ * precision: PCD_SPLIT_ACT bit 256). */
 int64_t pcd_kv_bytes_per_token(const pcd_model* m);
 
 /* ------------------------------------------------------------------ prefill */
