@@ -101,7 +101,7 @@ struct PlanView {
 };
 
 enum ProfClass { PROF_GEMM_PREFILL = 0, PROF_GEMM_BRANCH = 1, PROF_ATTN_PREFILL = 2, PROF_ATTN_BRANCH = 3,
-                 PROF_READOUT = 4, PROF_OTHER = 5, PROF_GEMM_SINGLE = 6 };
+                 PROF_READOUT = 4, PROF_OTHER = 5, PROF_GEMM_SINGLE = 6, PROF_GEMM_GU = 7 };
 
 }  // namespace
 
@@ -986,7 +986,7 @@ int record_single(pcd_model* m, const PlanView& p, const int32_t* ids, int n, pc
       return pcd::launch_rmsnorm(off(x, r0, m->d), m->d, nullptr, M, m->d, W.mlp_norm, m->cfg.rms_eps, xn, m->d,
                                  m->stream, xlo_m);
     }));
-    PCD_TRY(gemm(m, PROF_GEMM_SINGLE, xn, M, m->d, W.wgu, 2 * m->Fp, m->d, m->d, pcd::EPI_SWIGLU, hb, m->Fp, xlo_m, hb_lo,
+    PCD_TRY(gemm(m, PROF_GEMM_GU, xn, M, m->d, W.wgu, 2 * m->Fp, m->d, m->d, pcd::EPI_SWIGLU, hb, m->Fp, xlo_m, hb_lo,
                  n - r0));
     PCD_TRY(gemm(m, PROF_GEMM_SINGLE, hb, M, m->Fp, W.wd, m->d, m->Fp, m->Fp, pcd::EPI_F32_ADD, off(x, r0, m->d), m->d,
                  hb_lo));

@@ -323,12 +323,13 @@ def pcd_profile_enable(model: Model, on: bool = True) -> None:
     _check(load().pcd_profile_enable(model.handle, 1 if on else 0), "pcd_profile_enable")
 
 
-PROFILE_CLASSES = ("gemm_prefill", "gemm_branch", "attn_prefill", "attn_branch", "readout", "other", "gemm_single")
+PROFILE_CLASSES = ("gemm_prefill", "gemm_branch", "attn_prefill", "attn_branch", "readout", "other", "gemm_single",
+                   "gemm_gate_up")
 
 
 def pcd_profile_read(model: Model) -> dict:
-    n = (ctypes.c_int * 7)()
-    ms = (ctypes.c_float * 7)()
+    n = (ctypes.c_int * len(PROFILE_CLASSES))()
+    ms = (ctypes.c_float * len(PROFILE_CLASSES))()
     _check(load().pcd_profile_read(model.handle, n, ms), "pcd_profile_read")
     return {k: (int(n[i]), float(ms[i])) for i, k in enumerate(PROFILE_CLASSES)}
 

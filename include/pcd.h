@@ -221,10 +221,11 @@ int pcd_sync(pcd_model* m);
 /* Per-kernel-class timing: when enabled, every launch is bracketed by CUDA
  * events on the model stream (and passes run as direct launches, not
  * graphs).  Classes: 0 prefill GEMMs, 1 branch GEMMs, 2 prefill attention,
- * 3 branch attention, 4 fused readout, 5 other, 6 single-pass GEMMs.
- * pcd_profile_read synchronises, returns per class the launch count and the
- * summed milliseconds, and resets the counters. */
-#define PCD_PROF_CLASSES 7
+ * 3 branch attention, 4 fused readout, 5 other, 6 single-pass GEMMs other
+ * than the gate/up projection, 7 the single-pass gate/up projection (with
+ * its SwiGLU epilogue).  pcd_profile_read synchronises, returns per class the
+ * launch count and the summed milliseconds, and resets the counters. */
+#define PCD_PROF_CLASSES 8
 int pcd_profile_enable(pcd_model* m, int on);
 int pcd_profile_read(pcd_model* m, int* launches, float* ms);
 
