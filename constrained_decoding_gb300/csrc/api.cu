@@ -92,8 +92,11 @@ struct PlanView {
       *gather_off;
   const float* temp;
   const int4* gather;
-  // tree-attention tiles over the branch tokens (tpt whole tokens each)
+  // tree-attention tiles over the branch tokens (up to tpt whole tokens of one request each)
   int tpt = 1, n_br_tiles = 0, max_tile_chunks = 0;
+  const int32_t* tile_tok;          // [n_br_tiles][3] first token, tokens, request
+  const pcd::SegKV* segs = nullptr;  // a batch's prefix caches, one per request (else nullptr)
+  const int32_t* abs_pos = nullptr;  // a batch's absolute position of every branch token (else nullptr)
   const int32_t* tile_chunk_off;
   const int32_t* tile_keys;
   const unsigned long long* tile_mask;
@@ -179,6 +182,8 @@ int tree_tile_rows(const pcd_model* m);
 bool kv_lo(const pcd_model* m);
 // a remainder workspace when the model keeps remainders, else nullptr
 inline act_t* lo_buf(const pcd_model* m, const DevBuf& b) { return kv_lo(m) ? static_cast<act_t*>(b.p) : nullptr; }
+// one tree-attention launch over the prefix cache `c` at layer l
+int launch_tree(pcd_model* m, const pcd::TreeAttnArgs& ta, const pcd_cache* c, int l);
 
 // ----------------------------------------------------------------- helpers
 int ensure_pinned(void*& buf, size_t& cap, size_t bytes) {
@@ -437,7 +442,7 @@ int record_prefill(pcd_model* m, const int32_t* d_ids, int n, pcd_cache* c, int 
     if (m->dh == 128) {
       const KVDest d0{c->k + l * layer_kv, c->v + l * layer_kv, c->cap, p0, p0, nullptr,
                       c->k_lo ? c->k_lo + l * layer_kv : nullptr, c->v_lo ? c->v_lo + l * layer_kv : nullptr};
-      PCD_TRY(gemm_qkv_rope(m, PROF_GEMM_PREFILL, xn, n, W.wqkv, xlo, 0, q, n, d0, d0));
+      PCD_TRY(gemm_qkv_rope(m, PROF_GEMM_PREFILL, xn, n, W.wqkv, xlo, 0, q, n, d0, d0, lo_buf(m, m->q_lo)));
     } else {
     PCD_TRY(gemm(m, PROF_GEMM_PREFILL, xn, n, m->d, W.wqkv, m->Nqkv, m->d, m->d, pcd::EPI_F32_STORE, qkv, m->Nqkv, xlo));
     pcd::RopeArgs ra;
@@ -462,6 +467,29 @@ int record_prefill(pcd_model* m, const int32_t* d_ids, int n, pcd_cache* c, int 
     }
     // The last layer's attention output and MLP change no cached key or value.
     if (l == m->L - 1) break;
+    if (tree_tile_rows(m) == 128) {
+      // tensor-core tree attention with prefix queries only, at positions p0..
+      pcd::TreeAttnArgs ta{};
+      ta.q = q;
+      ta.out = att;
+      ta.out_lo = att_lo;
+      ta.ld_out = m->qdim;
+      ta.Hq = m->Hq;
+      ta.Hkv = m->Hkv;
+      ta.DH = m->dh;
+      ta.tpt = std::max(1, 128 / m->G);
+      ta.n_pf = n;
+      ta.n_pf_tiles = (n + ta.tpt - 1) / ta.tpt;
+      ta.pf_pos0 = p0;
+      ta.k = c->k + l * layer_kv;
+      ta.v = c->v + l * layer_kv;
+      ta.kv_head_stride = c->cap;
+      ta.n_keys = p0 + n;
+      ta.kb = ta.vb = q;  // no branch queries: unused
+      ta.scale_log2 = 1.4426950408889634f / std::sqrt(static_cast<float>(m->dh));
+      ta.csk = pcd::tree_attention_csk(ta.n_pf_tiles, m->Hkv, (p0 + n + 63) / 64, m->sms, true);
+      PCD_LAUNCH(timed(m, PROF_ATTN_PREFILL, [&] { return launch_tree(m, ta, c, l); }));
+    } else {
     pcd::AttnArgs aa{};
     aa.q = q;
     aa.n_tok = n;
@@ -504,6 +532,7 @@ int record_prefill(pcd_model* m, const int32_t* d_ids, int n, pcd_cache* c, int 
       ma.out_lo = att_lo;
       PCD_LAUNCH(timed(m, PROF_ATTN_PREFILL, [&] { return pcd::launch_branch_merge(ma, m->stream); }));
     }
+    }
     PCD_TRY(gemm(m, PROF_GEMM_PREFILL, att, n, m->qdim, W.wo, m->d, m->qdim, m->qdim, pcd::EPI_F32_ADD, x, m->d,
                  att_lo));
     PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
@@ -522,7 +551,6 @@ struct Segment {
   int t0, t1;  // branch tokens of this request
 };
 
-int launch_tree(pcd_model* m, const pcd::TreeAttnArgs& ta, const pcd_cache* c, int l);
 
 int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_seg, float* d_result, int splits,
                   cudaEvent_t ev_mid);
@@ -578,6 +606,7 @@ pcd::TreeAttnArgs tree_args(const pcd_model* m, const PlanView& p, const act_t* 
   ta.tpt = p.tpt;
   ta.n_br = p.T;
   ta.n_br_tiles = p.n_br_tiles;
+  ta.tile_tok = p.tile_tok;
   ta.tile_chunk_off = p.tile_chunk_off;
   ta.tile_keys = p.tile_keys;
   ta.tile_mask = p.tile_mask;
@@ -616,8 +645,10 @@ int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_se
     PCD_LAUNCH(timed(m, PROF_OTHER, [&] {
       return pcd::launch_rmsnorm(x, m->d, nullptr, T, m->d, W.attn_norm, m->cfg.rms_eps, xn, m->d, m->stream, xlo);
     }));
-    if (m->dh == 128 && n_seg == 1) {
-      const KVDest d1{kb, vb, T, 0, segs[0].c->len, p.rel, lo_buf(m, m->kb_lo), lo_buf(m, m->vb_lo)};
+    if (m->dh == 128 && (n_seg == 1 || p.abs_pos)) {
+      // one request: positions len + rel; a batch: each token's absolute position
+      const KVDest d1{kb, vb, T, 0, n_seg == 1 ? segs[0].c->len : 0, n_seg == 1 ? p.rel : p.abs_pos,
+                      lo_buf(m, m->kb_lo), lo_buf(m, m->vb_lo)};
       PCD_TRY(gemm_qkv_rope(m, PROF_GEMM_BRANCH, xn, T, W.wqkv, xlo, 0, q, 0, d1, d1, lo_buf(m, m->q_lo)));
     } else {
     PCD_TRY(gemm(m, PROF_GEMM_BRANCH, xn, T, m->d, W.wqkv, m->Nqkv, m->d, m->d, pcd::EPI_F32_STORE, qkv, m->Nqkv, xlo));
@@ -646,9 +677,12 @@ int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_se
       PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_rope_kv(ra, m->stream); }));
     }
     }
-    if (m->tree_attn && n_seg == 1) {
+    if (m->tree_attn && (n_seg == 1 || (p.segs && p.abs_pos && tree_tile_rows(m) == 128))) {
+      // one request, or a batch whose tiles each read their own request's cache
       const pcd_cache* c = segs[0].c;
       const size_t layer_kv = static_cast<size_t>(m->Hkv) * c->cap * m->dh;
+      int max_len = 0;
+      for (int s2 = 0; s2 < n_seg; ++s2) max_len = std::max(max_len, segs[s2].c->len);
       pcd::TreeAttnArgs ta = tree_args(m, p, q, att, att_lo, scale_log2);
       ta.k = c->k + l * layer_kv;
       ta.v = c->v + l * layer_kv;
@@ -656,7 +690,9 @@ int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_se
       ta.n_keys = c->len;
       ta.kb = kb;
       ta.vb = vb;
-      ta.csk = pcd::tree_attention_csk(ta.n_br_tiles, m->Hkv, (c->len + 63) / 64 + p.max_tile_chunks, m->sms,
+      ta.segs = n_seg > 1 ? p.segs : nullptr;
+      ta.layer = l;
+      ta.csk = pcd::tree_attention_csk(ta.n_br_tiles, m->Hkv, (max_len + 63) / 64 + p.max_tile_chunks, m->sms,
                                        tree_tile_rows(m) == 128);
       PCD_LAUNCH(timed(m, PROF_ATTN_BRANCH, [&] { return launch_tree(m, ta, c, l); }));
     } else {
@@ -1067,7 +1103,8 @@ int launch_tree(pcd_model* m, const pcd::TreeAttnArgs& ta, const pcd_cache* c, i
 // Serialises a host plan into an int32 blob; `view` gets pointers relative to
 // `dev` (the blob's device address).
 size_t plan_blob(const pcd_model* m, const pcd::HostPlan& hp, std::vector<int32_t>& blob, PlanView& v,
-                 const int32_t* dev) {
+                 const int32_t* dev, const std::vector<pcd::SegKV>* segs = nullptr,
+                 const std::vector<int32_t>* abs_pos = nullptr) {
   v.n_fields = hp.n_fields;
   v.T = hp.T;
   v.R = hp.R;
@@ -1096,11 +1133,21 @@ size_t plan_blob(const pcd_model* m, const pcd::HostPlan& hp, std::vector<int32_
   // a tile's ancestor keys are the ascending union of its tokens' ancestor
   // lists, in chunks of 64, with one visibility bit per (chunk key, token)
   v.tpt = std::max(1, tree_tile_rows(m) / std::max(1, m->G));
-  v.n_br_tiles = (hp.T + v.tpt - 1) / v.tpt;
+  // tiles never straddle two requests of a batch (their prefix caches differ)
+  std::vector<int32_t> seg_off = hp.seg_off;
+  if (seg_off.size() < 2) seg_off = {0, hp.T};
+  std::vector<int32_t> ttok;
+  for (size_t sg = 0; sg + 1 < seg_off.size(); ++sg)
+    for (int a0 = seg_off[sg]; a0 < seg_off[sg + 1]; a0 += v.tpt) {
+      ttok.push_back(a0);
+      ttok.push_back(std::min(v.tpt, seg_off[sg + 1] - a0));
+      ttok.push_back(static_cast<int32_t>(sg));
+    }
+  v.n_br_tiles = static_cast<int>(ttok.size() / 3);
   v.max_tile_chunks = 0;
   std::vector<int32_t> tco(v.n_br_tiles + 1, 0), tkeys, tmask;
   for (int ti = 0; ti < v.n_br_tiles; ++ti) {
-    const int a0 = ti * v.tpt, a1 = std::min(hp.T, a0 + v.tpt);
+    const int a0 = ttok[3 * ti], a1 = a0 + ttok[3 * ti + 1];
     std::vector<int32_t> u;
     for (int t = a0; t < a1; ++t)
       u.insert(u.end(), hp.anc_idx.begin() + hp.anc_off[t], hp.anc_idx.begin() + hp.anc_off[t + 1]);
@@ -1147,9 +1194,18 @@ size_t plan_blob(const pcd_model* m, const pcd::HostPlan& hp, std::vector<int32_
   v.temp = reinterpret_cast<const float*>(put(reinterpret_cast<const int32_t*>(hp.temp.data()), hp.temp.size()));
   v.gather_off = put(goff.data(), goff.size());
   v.gather = reinterpret_cast<const int4*>(put(g4.data(), g4.size()));
+  v.tile_tok = put(ttok.data(), ttok.size());
   v.tile_chunk_off = put(tco.data(), tco.size());
   v.tile_keys = put(tkeys.data(), tkeys.size());
   v.tile_mask = reinterpret_cast<const unsigned long long*>(put(tmask.data(), tmask.size()));
+  v.segs = nullptr;
+  v.abs_pos = nullptr;
+  if (segs && !segs->empty()) {
+    static_assert(sizeof(pcd::SegKV) % 4 == 0, "SegKV packs into the int32 blob");
+    v.segs = reinterpret_cast<const pcd::SegKV*>(
+        put(reinterpret_cast<const int32_t*>(segs->data()), segs->size() * sizeof(pcd::SegKV) / 4));
+  }
+  if (abs_pos && !abs_pos->empty()) v.abs_pos = put(abs_pos->data(), abs_pos->size());
   return blob.size() * sizeof(int32_t);
 }
 
@@ -1257,6 +1313,10 @@ int build_model(const pcd_model_config& cfg, TensorFn get, void* ctx, int dtype,
     m->own_stream = true;
   }
   if (const char* g = std::getenv("PCD_GRAPHS")) m->graphs = std::atoi(g) != 0;
+  // Wider decoders amplify fp16 rounding more: from the 7B width on every
+  // operand carries its remainder (measured: worst candidate-probability error
+  // 3e-3 -> 2e-4 at the Qwen2.5-7B shape; 1.5B holds 8e-4 with the default set).
+  if (m->cfg.d_model >= 3072) m->split_act = 511;
   if (const char* g = std::getenv("PCD_SPLIT_ACT")) m->split_act = std::atoi(g);
   if (const char* g = std::getenv("PCD_TREE_ATTN")) m->tree_attn = std::atoi(g) != 0;
   if (const char* g = std::getenv("PCD_ATTN_TC")) m->attn_tc = std::atoi(g) != 0;
@@ -1479,13 +1539,14 @@ int upload_ids(pcd_model* m, const int32_t* ids, int n, const int32_t** d_ids) {
 }
 
 // Uploads a host plan into the model's plan buffer; fills `v`.
-int upload_plan(pcd_model* m, const pcd::HostPlan& hp, PlanView& v, size_t* bytes_out) {
+int upload_plan(pcd_model* m, const pcd::HostPlan& hp, PlanView& v, size_t* bytes_out,
+                const std::vector<pcd::SegKV>* segs = nullptr, const std::vector<int32_t>* abs_pos = nullptr) {
   std::vector<int32_t> blob;
   // first pass for the size, second with the real device base
-  plan_blob(m, hp, blob, v, nullptr);
+  plan_blob(m, hp, blob, v, nullptr, segs, abs_pos);
   const size_t bytes = blob.size() * 4;
   PCD_TRY(ensure(m->plan_buf, bytes));
-  plan_blob(m, hp, blob, v, static_cast<const int32_t*>(m->plan_buf.p));
+  plan_blob(m, hp, blob, v, static_cast<const int32_t*>(m->plan_buf.p), segs, abs_pos);
   *bytes_out = bytes;
   return upload_async(m, m->plan_buf.p, blob.data(), bytes);
 }
@@ -1533,9 +1594,24 @@ int score_impl(pcd_model* m, const pcd_cache* const* caches, const pcd_field* co
     segs[r] = Segment{caches[r], t0, hp.T};
   }
   const auto t_comp = std::chrono::steady_clock::now();
+  // a batch: tree-attention tiles per request, each request's cache, and
+  // every branch token's absolute position (cache length + relative position)
+  std::vector<pcd::SegKV> seg_kv;
+  std::vector<int32_t> abs_pos;
+  if (n_req > 1) {
+    hp.seg_off.clear();
+    for (int r = 0; r < n_req; ++r) hp.seg_off.push_back(segs[r].t0);
+    hp.seg_off.push_back(hp.T);
+    abs_pos.resize(hp.T);
+    for (int r = 0; r < n_req; ++r) {
+      const pcd_cache* c = caches[r];
+      seg_kv.push_back(pcd::SegKV{c->k, c->v, c->k_lo, c->v_lo, c->cap, c->len, 0});
+      for (int t = segs[r].t0; t < segs[r].t1; ++t) abs_pos[t] = c->len + hp.rel[t];
+    }
+  }
   PlanView v;
   size_t plan_bytes = 0;
-  PCD_TRY(upload_plan(m, hp, v, &plan_bytes));
+  PCD_TRY(upload_plan(m, hp, v, &plan_bytes, &seg_kv, &abs_pos));
   PCD_TRY(ensure(m->result, static_cast<size_t>(v.result_floats()) * 4));
   if (stats) cudaEventRecord(m->ev_a, m->stream);
   // the mid-pass event splits branch and readout time; it forces direct

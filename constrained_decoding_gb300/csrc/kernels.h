@@ -84,6 +84,18 @@ int launch_branch_merge(const MergeArgs& a, cudaStream_t s);
 // (chunk, token of the tile).  csk CTAs (a thread-block cluster) share one
 // (tile, KV head) and split its key blocks; they combine their partial
 // softmax states through distributed shared memory.
+// The prefix cache of one request of a batch (tensor-core tree attention):
+// layer l's keys of KV head h at k + ((l * Hkv + h) * cap + j) * DH, j < n_keys.
+struct SegKV {
+  const act_t* k;
+  const act_t* v;
+  const act_t* k_lo;  // remainders, or nullptr
+  const act_t* v_lo;
+  int64_t cap;
+  int32_t n_keys;
+  int32_t pad;
+};
+
 struct TreeAttnArgs {
   const act_t* q;               // [rows][Hq][DH]: prefix queries at rows 0..n_pf-1, branch queries at br_row0..
   act_t* out;                   // out[row][h * DH + d]
@@ -91,7 +103,8 @@ struct TreeAttnArgs {
   int ld_out;
   int Hq, Hkv, DH;
   int tpt;                      // query tokens per tile
-  int n_pf, n_pf_tiles;         // causal prefix queries
+  int n_pf, n_pf_tiles;         // causal prefix queries: query i sits at position pf_pos0 + i, sees keys 0 .. that
+  int pf_pos0 = 0;
   int n_br, n_br_tiles, br_row0;
   const act_t* k;               // this layer's prefix keys: k + (h * kv_head_stride + j) * DH, j < n_keys
   const act_t* v;
@@ -102,6 +115,10 @@ struct TreeAttnArgs {
   const act_t* q_lo = nullptr;   // fp16 remainders of q, kb, vb (tensor-core kernel only), or nullptr
   const act_t* kb_lo = nullptr;
   const act_t* vb_lo = nullptr;
+  const int32_t* tile_tok;                  // [n_br_tiles][3]: first branch token, tokens, request of each tile
+  const SegKV* segs = nullptr;              // per request of a batch (branch tiles read their request's
+                                            // prefix keys by cp.async), or nullptr: k / v / n_keys above
+  int layer = 0;                            // layer of segs' caches
   const int32_t* tile_chunk_off;            // [n_br_tiles + 1] ancestor chunks of each branch tile
   const int32_t* tile_keys;                 // [chunks][64] branch key index, -1 past the union's end
   const unsigned long long* tile_mask;      // [chunks][tpt] bit i: key i of the chunk is visible to the token

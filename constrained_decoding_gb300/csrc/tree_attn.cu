@@ -60,11 +60,12 @@ __global__ void __launch_bounds__(128) tree_attn_kernel(TreeAttnArgs a) {
 
   const bool branch = item < a.n_br_tiles;
   const int tile = branch ? item : a.n_pf_tiles - 1 - (item - a.n_br_tiles);
-  const int t0 = tile * a.tpt;
-  const int ntok = min(a.tpt, (branch ? a.n_br : a.n_pf) - t0);
+  // a branch tile's tokens come from the plan (tiles end at request boundaries)
+  const int t0 = branch ? a.tile_tok[3 * tile] : tile * a.tpt;
+  const int ntok = branch ? a.tile_tok[3 * tile + 1] : min(a.tpt, a.n_pf - t0);
   const int qrow0 = branch ? a.br_row0 + t0 : t0;  // q / out row of the tile's first token
   const int rows = ntok * G;
-  const int pf_keys = branch ? a.n_keys : min(a.n_keys, t0 + ntok);
+  const int pf_keys = branch ? a.n_keys : min(a.n_keys, a.pf_pos0 + t0 + ntok);
   const int nbp = (pf_keys + 63) / 64;
   const int ch0 = branch ? a.tile_chunk_off[tile] : 0;
   const int nb = nbp + (branch ? a.tile_chunk_off[tile + 1] - ch0 : 0);
@@ -122,8 +123,8 @@ __global__ void __launch_bounds__(128) tree_attn_kernel(TreeAttnArgs a) {
 
   const int rlo = warp * 16 + gid, rhi = rlo + 8;
   // causal bound of prefix rows (branch rows see every prefix key)
-  const int pos_lo = branch ? INT_MAX : t0 + rlo / G;
-  const int pos_hi = branch ? INT_MAX : t0 + rhi / G;
+  const int pos_lo = branch ? INT_MAX : a.pf_pos0 + t0 + rlo / G;
+  const int pos_hi = branch ? INT_MAX : a.pf_pos0 + t0 + rhi / G;
   const int tlo = rlo / G, thi = rhi / G;  // token of the row within the tile (< 64)
   float o[ND][4];
 #pragma unroll

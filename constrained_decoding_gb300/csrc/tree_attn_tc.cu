@@ -102,11 +102,15 @@ __global__ void __launch_bounds__(192, 1)
 
   const bool branch = item < a.n_br_tiles;
   const int tile = branch ? item : a.n_pf_tiles - 1 - (item - a.n_br_tiles);
-  const int t0 = tile * a.tpt;
-  const int ntok = min(a.tpt, (branch ? a.n_br : a.n_pf) - t0);
+  // a branch tile's tokens come from the plan (tiles end at request boundaries)
+  const int t0 = branch ? a.tile_tok[3 * tile] : tile * a.tpt;
+  const int ntok = branch ? a.tile_tok[3 * tile + 1] : min(a.tpt, a.n_pf - t0);
   const int qrow0 = branch ? a.br_row0 + t0 : t0;
   const int rows = ntok * G;
-  const int pf_keys = branch ? a.n_keys : min(a.n_keys, t0 + ntok);
+  // a batch's branch tile reads its own request's prefix cache
+  const SegKV* sgk = (branch && a.segs) ? a.segs + a.tile_tok[3 * tile + 2] : nullptr;
+  const int n_keys = sgk ? sgk->n_keys : a.n_keys;
+  const int pf_keys = branch ? n_keys : min(n_keys, a.pf_pos0 + t0 + ntok);
   const int nbp = (pf_keys + kKeys - 1) / kKeys;
   const int ch0 = branch ? a.tile_chunk_off[tile] : 0;
   const int nb = nbp + (branch ? a.tile_chunk_off[tile + 1] - ch0 : 0);
@@ -162,15 +166,19 @@ __global__ void __launch_bounds__(192, 1)
     // ------------------------------------------------------------ K/V loads
     const act_t* kbp = a.kb + static_cast<size_t>(hk) * a.n_br * kDH;
     const act_t* vbp = a.vb + static_cast<size_t>(hk) * a.n_br * kDH;
+    // this (layer, KV head)'s rows in a batch request's cache
+    const size_t seg_off = sgk ? (static_cast<size_t>(a.layer) * a.Hkv + hk) * static_cast<size_t>(sgk->cap) * kDH : 0;
     const act_t* kblp = LO ? a.kb_lo + static_cast<size_t>(hk) * a.n_br * kDH : nullptr;
     const act_t* vblp = LO ? a.vb_lo + static_cast<size_t>(hk) * a.n_br * kDH : nullptr;
-    // an ancestor chunk: rows of the branch K or V (and remainder) gathered by
-    // index, zero past the union's end
-    auto gather = [&](uint8_t* dst, const act_t* src, const act_t* src_lo, const int32_t* keys, uint64_t* bar) {
+    // rows of K or V (and remainder) by cp.async: an ancestor chunk's rows of
+    // the branch K/V by index (keys), or a batch request's prefix rows j0.. of
+    // its own cache; zero past the end
+    auto gather = [&](uint8_t* dst, const act_t* src, const act_t* src_lo, const int32_t* keys, int j0, int n_valid,
+                      uint64_t* bar) {
       for (int e = lane; e < kKeys * 16; e += 32) {
         const int kr = e >> 4, c = e & 15;
-        const int j = keys[kr];
-        const bool ok = j >= 0 && j < a.n_br;
+        const int j = keys ? keys[kr] : j0 + kr;
+        const bool ok = keys ? (j >= 0 && j < a.n_br) : j < n_valid;
         const size_t off = static_cast<size_t>(ok ? j : 0) * kDH + c * 8;
         const uint32_t so = (c >> 3) * (kKVBytes / 2) + swz(kr, c & 7);
         cp_async16(dst + so, src + off, ok);
@@ -203,10 +211,12 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       uint8_t* kd = smem + kOffK + s * kKVSt;
-      if (!keys) {
-        if (lane == 0) tma_block(kd, &tmK, &tmKlo, b, &k_full[s]);
+      if (keys) {
+        gather(kd, kbp, kblp, keys, 0, 0, &k_full[s]);
+      } else if (sgk) {
+        gather(kd, sgk->k + seg_off, LO ? sgk->k_lo + seg_off : nullptr, nullptr, b * kKeys, pf_keys, &k_full[s]);
       } else {
-        gather(kd, kbp, kblp, keys, &k_full[s]);
+        if (lane == 0) tma_block(kd, &tmK, &tmKlo, b, &k_full[s]);
       }
       ++kissued[s];
       // the V stage is free once the P V of block i - kStages is done
@@ -215,10 +225,12 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       uint8_t* vd = smem + kOffV + s * kKVSt;
-      if (!keys) {
-        if (lane == 0) tma_block(vd, &tmV, &tmVlo, b, &v_full[s]);
+      if (keys) {
+        gather(vd, vbp, vblp, keys, 0, 0, &v_full[s]);
+      } else if (sgk) {
+        gather(vd, sgk->v + seg_off, LO ? sgk->v_lo + seg_off : nullptr, nullptr, b * kKeys, pf_keys, &v_full[s]);
       } else {
-        gather(vd, vbp, vblp, keys, &v_full[s]);
+        if (lane == 0) tma_block(vd, &tmV, &tmVlo, b, &v_full[s]);
       }
       ++vissued[s];
       __syncwarp();
@@ -325,7 +337,7 @@ __global__ void __launch_bounds__(192, 1)
     const bool valid = r < rows;
     // padding rows (r >= rows) take the same path as the tile's last token: their Q is zero and
     // their output is never written, and keeping the warp on one path keeps it in step
-    const int pos = branch ? INT_MAX : t0 + r / G;
+    const int pos = branch ? INT_MAX : a.pf_pos0 + t0 + r / G;
     const int tt = valid ? r / G : 0;
     // the visibility mask of the tile's first ancestor chunk, loaded ahead
     const unsigned long long mk0 = (valid && nb > nbp) ? a.tile_mask[static_cast<size_t>(ch0) * a.tpt + tt] : 0ull;
@@ -576,7 +588,7 @@ int launch_tree_attention_tc(const TreeAttnArgs& a, const CUtensorMap& tmK, cons
   if (a.DH != kDH || a.csk < 1 || a.csk > 8) return cudaErrorInvalidValue;
   if (a.tpt < 1 || a.tpt * (a.Hq / a.Hkv) > kRows) return cudaErrorInvalidValue;
   const bool lo = a.q_lo != nullptr;
-  if (lo && (!tmKlo || !tmVlo || !a.kb_lo || !a.vb_lo)) return cudaErrorInvalidValue;
+  if (lo && (!tmKlo || !tmVlo || (a.n_br_tiles > 0 && (!a.kb_lo || !a.vb_lo)))) return cudaErrorInvalidValue;
   if (lo) return launch_tc_t<true>(a, tmK, tmV, *tmKlo, *tmVlo, layer, wait_ns, err, s);
   return launch_tc_t<false>(a, tmK, tmV, tmK, tmV, layer, wait_ns, err, s);
 }

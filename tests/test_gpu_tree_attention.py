@@ -49,3 +49,35 @@ def test_attention_variants(oracles, tmp_path, shape, env):
                                     label=int(sc[0]), mass=float(sc[1]), log_mass=float(sc[2]),
                                     first_mass=float(sc[3]))
                 compare_field(g, r, f"{shape} {env} {mode} request {i} field {f}")
+
+
+def test_batch_and_extend_head_dim_128(oracles):
+    """A batch of requests with different prefix lengths in one branch pass
+    (each tile reads its own request's cache), and prefixes extended from a
+    cached head (prefill queries at positions past the head), against the
+    oracle on the head-dim-128 decoder."""
+    import constrained_decoding_gb300.pcd as pcd
+    from synth.requests import make_custom
+    orc = oracles["tiny-h128"]
+    w = synth.make_weights(synth.model_config("tiny-h128"), seed=0)
+    m = pcd.pcd_load_weights_host(w)
+    try:
+        specs = [("bool",), ("enum", 4, 1, 3), ("shared", 5, 2, 3), ("scaffold", 70), ("enum", 3, 2, 4)]
+        reqs = [make_custom(60 + i, 512, n, specs) for i, n in enumerate((40, 130, 257, 7, 333))]
+        caches = [pcd.pcd_prefill(m, r.prefix) for r in reqs]
+        batch = pcd.pcd_score_batch(m, caches, [r.fields for r in reqs])
+        head = pcd.pcd_prefill(m, reqs[4].prefix[:100])
+        ext = pcd.pcd_prefill_extend(m, head, reqs[4].prefix[100:])
+        warm = pcd.pcd_score(m, ext, reqs[4].fields)
+        for i, (r, got) in enumerate(zip(reqs, batch)):
+            oc = orc.prefill(r.prefix)
+            ref = [orc.score_field(f, cache=oc) for f in r.fields]
+            for f, (g, rf) in enumerate(zip(got, ref)):
+                compare_field(g, rf, f"batch request {i} field {f}")
+            if i == 4:
+                for f, (g, rf) in enumerate(zip(warm, ref)):
+                    compare_field(g, rf, f"extended prefix field {f}")
+        for c in caches + [head, ext]:
+            c.free()
+    finally:
+        m.free()
