@@ -512,6 +512,236 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+// ====================================================================== CTA pairs
+// The same GEMM on a pair of CTAs (a 2-CTA cluster) sharing one tcgen05 MMA of
+// M = 256: each CTA loads its own 128 rows of A and half of the B tile (BN/2
+// rows), so a k block brings 16 KB of A + BN/2 x 128 B of B into each SM
+// instead of 16 KB + BN x 128 B — the fill of each SM's shared memory is what
+// bounds the single-CTA mainloop at these sizes.  The leader (rank 0) issues
+// the MMAs; both CTAs run the epilogue on their own accumulator rows.
+template <int BN, bool ALO>
+struct PairCfg {
+  static constexpr int A_BYTES = 128 * 128;        // 128 rows x 64 fp16
+  static constexpr int B_BYTES = (BN / 2) * 128;   // this CTA's half of the B tile
+  static constexpr int A_PARTS = ALO ? 2 : 1;
+  static constexpr int STAGE_BYTES = A_PARTS * A_BYTES + B_BYTES;
+  static constexpr int SMEM_BUDGET = 227 * 1024 - 2048;
+  static constexpr int STAGES_RAW = SMEM_BUDGET / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
+  static constexpr int ACC_COLS = BN;
+  static constexpr int ACC_STAGES = (2 * ACC_COLS <= 512) ? 2 : 1;
+  static constexpr int TMEM_RAW = ACC_STAGES * ACC_COLS;
+  static constexpr int TMEM_COLS = TMEM_RAW <= 32 ? 32 : TMEM_RAW <= 64 ? 64 : TMEM_RAW <= 128 ? 128 : TMEM_RAW <= 256 ? 256 : 512;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 512;
+  static_assert(STAGES >= 2, "at least two stages");
+};
+
+template <int BN, int EPI, bool ALO>
+__global__ void __launch_bounds__(192, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                     const __grid_constant__ CUtensorMap tmA2, const GemmParams p, const EpiArgs e) {
+  using C = PairCfg<BN, ALO>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);  // used in the leader
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + C::ACC_STAGES;  // used in the leader
+  uint64_t* drain = tempty + C::ACC_STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int rank = static_cast<int>(cluster_ctarank());  // 0: leader
+  const int pair = static_cast<int>(cluster_id_x());
+  const int n_pairs = static_cast<int>(n_clusters_x());
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);  // the leader's producer expects both CTAs' bytes
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < C::ACC_STAGES; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 256);  // every epilogue thread of both CTAs
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    if constexpr (ALO) tma_prefetch_desc(&tmA2);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before_sync();
+  cluster_sync_all();  // the leader's barriers exist before the peer signals them
+  tc_fence_after_sync();
+  const uint32_t tbase = *tmem_slot;
+  griddep_launch_dependents();
+  griddep_wait();
+
+  auto row0 = [&](int mg) { return mg * 256 + rank * 128; };  // this CTA's first row of pair tile mg
+  // a pair tile carries the A remainder when any of its rows is at or past lo_row0 (both CTAs alike)
+  auto has_lo = [&](int mg) { return ALO && (mg + 1) * 256 > p.lo_row0; };
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer (both CTAs)
+    if (lane == 0) {
+      const uint64_t pol_b = p.b_evict_first ? l2_policy_evict_first() : l2_policy_evict_last();
+      (void)pol_b;
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int u = pair; u < p.n_units && !*abort_flag; u += n_pairs) {
+        int nt, mg, ks;
+        decode_unit(p, u, nt, mg, ks);
+        const int kb0 = ks * p.nkb / p.k_splits, kb1 = (ks + 1) * p.nkb / p.k_splits;
+        const bool lo = has_lo(mg);
+        const uint32_t bytes = (lo ? 2 : 1) * C::A_BYTES + C::B_BYTES;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.wait_ns)) {
+            record_error(p.err, DEV_WAIT_TIMEOUT_PRODUCER);
+            *abort_flag = 1;
+            break;
+          }
+          // the stage's bytes from both CTAs complete the leader's barrier; only
+          // the leader arrives on it (a remote arrive per stage from the peer
+          // measured twice as slow)
+          const uint32_t fb = cluster_addr(&full[stage], 0);
+          if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * bytes);
+          uint8_t* base = smem + stage * C::STAGE_BYTES;
+          tma_load_2d_pair(base, &tmA, fb, kb * 64, row0(mg));
+          if constexpr (ALO)
+            if (lo) tma_load_2d_pair(base + C::A_BYTES, &tmA2, fb, kb * 64, row0(mg));
+          tma_load_2d_pair(base + C::A_PARTS * C::A_BYTES, &tmB, fb, kb * 64, nt * BN + rank * (BN / 2));
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer (leader)
+    if (lane == 0 && rank == 0) {
+      constexpr uint32_t IDESC = idesc_f16_f32(256, BN);
+      int stage = 0, acc = 0;
+      uint32_t phase = 0, acc_phase = 0;
+      bool any = false;
+      for (int u = pair; u < p.n_units && !*abort_flag; u += n_pairs) {
+        int nt, mg, ks;
+        decode_unit(p, u, nt, mg, ks);
+        const int kb0 = ks * p.nkb / p.k_splits, kb1 = (ks + 1) * p.nkb / p.k_splits;
+        const bool lo = has_lo(mg);
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, p.wait_ns)) {
+          record_error(p.err, DEV_WAIT_TIMEOUT_MMA);
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d_base = tbase + acc * C::ACC_COLS;
+        bool ok = true;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&full[stage], phase, p.wait_ns)) {
+            record_error(p.err, DEV_WAIT_TIMEOUT_MMA);
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a_base = smem_u32(smem + stage * C::STAGE_BYTES);
+          const uint32_t b_base = a_base + C::A_PARTS * C::A_BYTES;
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            umma_f16_pair(d_base, sdesc_kmajor_sw128(a_base + k * 32), sdesc_kmajor_sw128(b_base + k * 32), IDESC,
+                          (kb > kb0 || k > 0) ? 1u : 0u);
+          if constexpr (ALO)
+            if (lo)
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                umma_f16_pair(d_base, sdesc_kmajor_sw128(a_base + C::A_BYTES + k * 32),
+                              sdesc_kmajor_sw128(b_base + k * 32), IDESC, 1u);
+          umma_commit_pair_mc(&empty[stage]);  // both CTAs' stage is free once these MMAs are done
+          any = true;
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        umma_commit_pair_mc(&tfull[acc]);
+        if (++acc == C::ACC_STAGES) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+      if (any) {
+        umma_commit_pair(drain);
+        if (!mbar_wait(drain, 0, p.wait_ns)) record_error(p.err, DEV_WAIT_TIMEOUT_DRAIN);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int q = warp & 3;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = pair; u < p.n_units && !*abort_flag; u += n_pairs) {
+      int nt, mg, ks;
+      decode_unit(p, u, nt, mg, ks);
+      if (!mbar_wait(&tfull[acc], acc_phase, p.wait_ns)) {
+        record_error(p.err, DEV_WAIT_TIMEOUT_EPILOGUE);
+        *abort_flag = 1;
+        break;
+      }
+      tc_fence_after_sync();
+      const int tile = mg * 2 + rank;  // this CTA's 128-row tile
+      const int row = tile * 128 + q * 32 + lane;
+      const uint32_t t_row = tbase + (static_cast<uint32_t>(q * 32) << 16) + acc * C::ACC_COLS;
+      float run_m = -INFINITY, run_s = 0.f;
+      if constexpr (EPI == EPI_QKV_ROPE) {
+        epi_qkv_rope<BN>(p, e, row, nt, t_row);
+      } else {
+        for (int c = 0; c < BN / 32; ++c) {
+          const int col0 = nt * BN + c * 32;
+          if (col0 >= p.N) break;  // uniform across the warp
+          float v[32];
+          tmem_ld_32cols(t_row + c * 32, v);
+          epi_chunk<EPI>(p, e, row, col0, v, run_m, run_s);
+        }
+      }
+      if constexpr (EPI == EPI_READOUT) {
+        if (row < p.M) e.part[static_cast<size_t>(nt) * p.M + row] = make_float2(run_m, run_s);
+        const int g0 = e.gather_off[nt], g1 = e.gather_off[nt + 1];
+        for (int g = g0; g < g1; ++g) {
+          const int4 en = e.gather[g];
+          const int r = en.y;
+          if (r / 128 != tile || ((r & 127) >> 5) != q) continue;
+          const float z = tmem_ld_1col(t_row + en.x);
+          if (lane == (r & 31)) e.z_out[en.z] = z;
+        }
+      }
+      tc_fence_before_sync();
+      mbar_arrive_cluster(cluster_addr(&tempty[acc], 0));  // the leader may reuse the accumulator
+      if (++acc == C::ACC_STAGES) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  cluster_sync_all();  // neither CTA's shared memory or barriers are touched by the other after this
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc_pair(tbase, C::TMEM_COLS);
+  }
+}
+
 // ====================================================================== host
 static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 static std::once_flag g_encode_once;
@@ -655,9 +885,63 @@ static int launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensor
   return cudaLaunchKernelEx(&cfg, kern, ma, mb, ma2, p, e);
 }
 
+template <int BN, int EPI, bool ALO>
+static int launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ma2, const GemmParams& p,
+                       const EpiArgs& e, cudaStream_t st, int sms) {
+  using C = PairCfg<BN, ALO>;
+  auto kern = gemm_pair_kernel<BN, EPI, ALO>;
+  static bool attr_set = false;  // per instantiation
+  static int max_pairs = 0;
+  if (!attr_set) {
+    cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (r != cudaSuccess) return r;
+    // how many pairs can be resident at once: the kernel is persistent
+    cudaLaunchConfig_t q = {};
+    q.gridDim = dim3(2 * (sms / 2), 1, 1);
+    q.blockDim = dim3(192, 1, 1);
+    q.dynamicSmemBytes = C::SMEM_BYTES;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = 2;
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    q.attrs = at;
+    q.numAttrs = 1;
+    int n = 0;
+    r = cudaOccupancyMaxActiveClusters(&n, kern, &q);
+    if (r != cudaSuccess) return r;
+    max_pairs = n > 0 ? n : 1;
+    attr_set = true;
+  }
+  const int pairs = std::min(p.n_units, max_pairs);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = 2;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, ma, mb, ma2, p, e);
+}
+
 template <int EPI>
 static int dispatch_tiling(const GemmTiling& t, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap* ma2,
                            const GemmParams& p, const EpiArgs& e, cudaStream_t st, int sms) {
+  if (t.pair) {
+    if (ma2) {
+      if (t.bn == 128) return launch_pair<128, EPI, true>(ma, mb, *ma2, p, e, st, sms);
+      if (t.bn == 256) return launch_pair<256, EPI, true>(ma, mb, *ma2, p, e, st, sms);
+    } else {
+      if (t.bn == 128) return launch_pair<128, EPI, false>(ma, mb, ma, p, e, st, sms);
+      if (t.bn == 256) return launch_pair<256, EPI, false>(ma, mb, ma, p, e, st, sms);
+    }
+    return -1;
+  }
   if (ma2) {  // hi + lo A: one 128-row tile per CTA, no cluster
     if constexpr (EPI == EPI_F32_STORE || EPI == EPI_F32_ADD || EPI == EPI_F32_ATOMIC || EPI == EPI_SWIGLU ||
                   EPI == EPI_READOUT || EPI == EPI_QKV_ROPE) {
@@ -694,20 +978,21 @@ int launch_gemm(const GemmShape& s, int epi, const EpiArgs& e, const GemmTiling&
   p.nkb = K / 64;
   if (t.cs != 1 && t.cs != 2 && t.cs != 4) return -1;
   if (t.cs > 1 && t.mt != 1) return -1;
-  p.n_mgroups = ceil_div(M, 128 * t.mt * t.cs);
+  if (t.pair && (t.mt != 1 || t.cs != 1)) return -1;
+  p.n_mgroups = ceil_div(M, t.pair ? 256 : 128 * t.mt * t.cs);
   p.n_ntiles = ceil_div(N, t.bn);
   p.k_splits = std::max(1, std::min(t.splits, p.nkb));
   p.n_units = p.n_mgroups * p.n_ntiles * p.k_splits;
   p.wait_ns = wait_ns;
   p.err = dev_err;
-  p.b_evict_first = (p.n_mgroups == 1 && t.mt * t.cs * 128 >= M) ? 1 : 0;
+  p.b_evict_first = (p.n_mgroups == 1 && (t.pair ? 256 : t.mt * t.cs * 128) >= M) ? 1 : 0;
   p.lo_row0 = s.lo_row0;
   p.b_const = s.b_const ? 1 : 0;
   CUtensorMap ma, mb, ma2;
   if (!make_map(&ma, s.a, M, K, s.a_ld, 128)) return -1;
   if (s.a_lo && !make_map(&ma2, s.a_lo, M, K, s.a_ld, 128)) return -1;
   const CUtensorMap* pa2 = s.a_lo ? &ma2 : nullptr;
-  if (!make_map(&mb, s.b, N, K, s.b_ld, t.bn / t.cs)) return -1;
+  if (!make_map(&mb, s.b, N, K, s.b_ld, t.pair ? t.bn / 2 : t.bn / t.cs)) return -1;
   switch (epi) {
     case EPI_BF16: return dispatch_tiling<EPI_BF16>(t, ma, mb, pa2, p, e, stream, sms);
     case EPI_F32_ADD: return dispatch_tiling<EPI_F32_ADD>(t, ma, mb, pa2, p, e, stream, sms);

@@ -25,11 +25,16 @@ int device_sms() {
 
 extern "C" int pcd_k_gemm(const void* a, int M, int lda, const void* b, int N, int ldb, int K, int epi, void* out,
                           int ldo, int mt, int bn, int splits, int* dev_err, void* stream) {
-  // mt = 10 * cs + 1 asks for a cluster of cs CTAs sharing each B tile (see the header)
+  // mt = 10 * cs + 1 asks for a cluster of cs CTAs sharing each B tile, mt = 3
+  // for a CTA pair sharing one MMA (see the header)
   int cs = 1;
+  bool pair = false;
   if (mt >= 10) {
     cs = mt / 10;
     mt = mt % 10;
+  } else if (mt == 3) {
+    pair = true;
+    mt = 1;
   }
   if (!a || !b || !out || M < 0 || N <= 0 || K <= 0) return -1;
   if (epi < PCD_EPI_BF16 || epi > PCD_EPI_SWIGLU) return -1;
@@ -42,6 +47,7 @@ extern "C" int pcd_k_gemm(const void* a, int M, int lda, const void* b, int N, i
     t.bn = bn;
     t.splits = splits < 1 ? 1 : splits;
     t.cs = cs;
+    t.pair = pair;
   }
   pcd::GemmShape s{a, M, lda, b, N, ldb, K};
   pcd::EpiArgs e;

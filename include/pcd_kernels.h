@@ -28,7 +28,9 @@ extern "C" {
  * K must be a multiple of 64, N a multiple of 32.  mt/bn/splits force a
  * tiling (mt in {1,2,4}, bn in {128,256}); mt = 0 lets the library choose;
  * mt = 21 or 41 runs clusters of 2 or 4 CTAs along M (one 128-row tile each)
- * that share every B tile through TMA multicast.
+ * that share every B tile through TMA multicast; mt = 3 runs CTA pairs that
+ * share one tensor-core MMA of 256 rows (each CTA loads its 128 rows of A and
+ * half of the B tile).
  * `dev_err` (device int, may be NULL) receives a nonzero code if a pipeline
  * wait times out. */
 int pcd_k_gemm(const void* a, int M, int lda, const void* b, int N, int ldb, int K, int epi, void* out, int ldo,

@@ -135,3 +135,19 @@ def test_gemm_split_activation(epi, bn, splits):
         e_split = (got - ref).abs().max().item()
         e_hi = (hi_only - ref).abs().max().item()
         assert e_split < 2e-4 and e_split < e_hi / 4, (e_split, e_hi)
+
+
+@pytest.mark.parametrize("M,N,K,epi,bn,splits", [
+    (128, 256, 256, 0, 128, 1),     # one pair tile, the peer's rows all past M
+    (300, 512, 512, 0, 128, 1),     # ragged M: the last pair tile half empty
+    (825, 2048, 1536, 0, 256, 1),
+    (825, 1536, 8960, 2, 256, 3),   # split-K with atomics
+    (825, 4096, 1536, 3, 128, 1),   # SwiGLU epilogue
+    (57, 512, 512, 1, 256, 1),      # fp32 add, fewer rows than one CTA
+])
+def test_gemm_cta_pair(M, N, K, epi, bn, splits):
+    """CTA pairs sharing one 256-row tcgen05 MMA (each CTA: its 128 rows of
+    A, half of the B tile, half of the accumulator rows)."""
+    out, ref, tol = _run(M, N, K, epi, 3, bn, splits)
+    err = (out - ref).abs().max().item()
+    assert err < tol * max(1.0, ref.abs().max().item()), err
