@@ -8,5 +8,6 @@ from .pcd_oracle import (  # noqa: F401
     Oracle, KVCache, FieldResult,
     rms_norm, rope_cos_sin, apply_rope, attention, silu, swiglu,
     logsumexp64, scores_to_result, combine_spellings, first_token_result,
+    length_normalised_scores, per_level_scores, field_scores, SCORINGS,
     kv_bytes_per_token,
 )

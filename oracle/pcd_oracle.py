@@ -41,6 +41,10 @@ Readings where the pages are silent (each also listed in the design notes):
   1/sqrt(dh), SwiGLU MLP, final RMSNorm, logits = E h (tied) or W_lm h;
 * multi-token mass is the sequence-level sum_c P(l_c);
 * T divides the summed log-probs; mass ignores T; T <= 0 means 1;
+* under the alternative scorings (length-normalised mean, per-level
+  product) T divides that score instead, and the label, probabilities and
+  margin follow it, while mass, log-mass and first-token mass keep their
+  full-vocabulary definitions;
 * the label's last token is a leaf: a label that is a strict prefix of
   another is not a valid schema (the caller appends its terminator token).
 
@@ -164,6 +168,61 @@ def scores_to_result(scores: Sequence[float], temperature: float = 1.0) -> Field
     srt = np.sort(s)[::-1]
     margin = float(srt[0] - srt[1]) if len(s) > 1 else float("inf")
     return FieldResult(s, p, label, float(np.exp(lm)), lm, margin)
+
+
+def length_normalised_scores(token_logprobs: Sequence[np.ndarray]) -> np.ndarray:
+    """Alternative label score: the MEAN of the label's token log-probs,
+    s_c = (sum_j lp_cj) / n_c, so that a label is not marked down merely for
+    having more tokens to get right (PCD From First Principles, "Multi-token
+    candidates": teacher-force, then sum or length-normalise; beam search's
+    reason for dividing by the length)."""
+    return np.array([float(np.sum(np.asarray(lp, np.float64))) / len(lp) for lp in token_logprobs])
+
+
+def per_level_scores(labels: Sequence[Sequence[int]], token_logprobs: Sequence[np.ndarray]) -> np.ndarray:
+    """Alternative label score: resolve shared prefixes one level at a time.
+    At every node of the label trie the decision is the distribution over the
+    node's allowed next tokens alone (renormalised), and a label's probability
+    is the product of those per-level probabilities along its path ("Resolve
+    shared prefixes level by level" and "Multi-level fields", PCD: A Technical
+    Reference).  Returns log of that product per label.
+
+    The full-vocabulary normaliser of a node cancels in the renormalisation,
+    so the per-level log-probability of token t at the node reached by the
+    prefix u is  lp(t | u) - log sum_{t' allowed after u} exp(lp(t' | u)),
+    with lp the full-vocabulary token log-probs of the teacher-forced labels
+    (a label passing through u carries lp(next token | u) at that step).
+    A node with one allowed continuation contributes probability 1."""
+    labs = [tuple(int(t) for t in l) for l in labels]
+    lps = [np.asarray(lp, np.float64) for lp in token_logprobs]
+    out = np.zeros(len(labs))
+    for c, lab in enumerate(labs):
+        for j in range(len(lab)):
+            prefix = lab[:j]
+            allowed = {}
+            for d, other in enumerate(labs):
+                if len(other) > j and other[:j] == prefix:
+                    allowed.setdefault(other[j], lps[d][j])
+            v = np.array(list(allowed.values()))
+            m = v.max()
+            out[c] += lps[c][j] - (m + np.log(np.exp(v - m).sum()))
+    return out
+
+
+SCORINGS = ("sum", "mean", "level")
+
+
+def field_scores(scoring: str, labels, token_logprobs) -> np.ndarray:
+    """The label scores a field's scoring rule asks for: "sum" (the summed
+    log-probs s_c), "mean" (length-normalised) or "level" (per-level
+    product)."""
+    if scoring == "sum":
+        return np.array([float(np.sum(np.asarray(lp, np.float64))) for lp in token_logprobs])
+    if scoring == "mean":
+        return length_normalised_scores(token_logprobs)
+    if scoring == "level":
+        return per_level_scores(labels, token_logprobs)
+    raise ValueError(scoring)
 
 
 def combine_spellings(path_scores: Sequence[float], label_of_path: Sequence[int]) -> np.ndarray:
@@ -339,7 +398,15 @@ class Oracle:
                 lps.append(self.label_logprobs_independent(np.asarray(prefix), np.asarray(field.scaffold), lab))
             else:
                 raise ValueError(mode)
-        res = scores_to_result([lp.sum() for lp in lps], getattr(field, "temperature", 1.0))
+        # the scoring rule decides label, probabilities and margin; the mass
+        # stays the full-vocabulary probability of the allowed labels
+        scoring = getattr(field, "scoring", "sum") or "sum"
+        sums = field_scores("sum", field.labels, lps)
+        res = scores_to_result(field_scores(scoring, field.labels, lps), getattr(field, "temperature", 1.0))
+        if scoring != "sum":
+            m = sums.max()
+            res.log_mass = float(m + np.log(np.exp(sums - m).sum()))
+            res.mass = float(np.exp(res.log_mass))
         res.token_logprobs = lps
         # candidate mass at the first decision: first-token probabilities of
         # the distinct first tokens; the first log-prob of every label is

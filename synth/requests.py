@@ -29,6 +29,7 @@ class Field:
     labels: List[np.ndarray]             # one int32 token path per label
     temperature: float = 1.0
     kind: str = "enum"
+    scoring: str = "sum"                 # "sum", "mean" (length-normalised) or "level" (per-level product)
 
 
 @dataclass

@@ -15,8 +15,9 @@ import pytest
 import torch
 
 import synth
-from oracle import (Oracle, apply_rope, attention, combine_spellings, first_token_result,
-                    kv_bytes_per_token, logsumexp64, rms_norm, rope_cos_sin, scores_to_result, silu)
+from oracle import (Oracle, apply_rope, attention, combine_spellings, field_scores, first_token_result,
+                    kv_bytes_per_token, length_normalised_scores, logsumexp64, per_level_scores, rms_norm,
+                    rope_cos_sin, scores_to_result, silu)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -348,6 +349,109 @@ def test_field_order_and_subset_invariance(tiny_oracle, request1):
     part = tiny_oracle.score(cache, [request1.fields[i] for i in perm])
     for j, i in enumerate(perm):
         np.testing.assert_array_equal(part[j].scores, full[i].scores)
+
+
+# --------------------------------------------------------------------------
+# Alternative scorers: per-level product and length-normalised mean
+# --------------------------------------------------------------------------
+def test_per_level_hand_example():
+    """Labels (5,1), (5,3), (7).  Root: P(5) = 0.3, P(7) = 0.1, so the first
+    level gives 0.75 / 0.25; after token 5: P(1) = 0.2, P(3) = 0.6, so the
+    second level gives 0.25 / 0.75.  Products: 0.1875, 0.5625, 0.25.
+    Counting token 5 once per label at the root (0.3 + 0.3 + 0.1) or leaving
+    the second level unrenormalised gives other numbers."""
+    labels = [[5, 1], [5, 3], [7]]
+    lps = [np.log([0.3, 0.2]), np.log([0.3, 0.6]), np.log([0.1])]
+    np.testing.assert_allclose(np.exp(per_level_scores(labels, lps)), [0.1875, 0.5625, 0.25], atol=1e-15)
+    # the summed-log-prob score of the same labels: 0.06, 0.18, 0.1
+    np.testing.assert_allclose(np.exp(field_scores("sum", labels, lps)), [0.06, 0.18, 0.1], atol=1e-15)
+
+
+def test_per_level_single_token_is_subset_softmax():
+    """With one-token labels there is a single level, and its renormalised
+    distribution is torch's softmax over the candidate logits."""
+    rng = np.random.default_rng(7)
+    z = rng.normal(0, 3, 64)
+    cands = [3, 17, 40, 41, 63]
+    lp = z - logsumexp64(z[None, :])[0]
+    got = np.exp(per_level_scores([[c] for c in cands], [lp[[c]] for c in cands]))
+    want = torch.softmax(torch.tensor(z[cands], dtype=torch.float64), 0).numpy()
+    np.testing.assert_allclose(got, want, atol=1e-14)
+
+
+def _random_trie_model(seed, vocab=6, depth=3, n_labels=9):
+    """A toy model: every prefix u has its own next-token distribution over
+    a 6-token vocabulary; the labels are distinct random paths of length
+    1..depth with no label a prefix of another."""
+    rng = np.random.default_rng(seed)
+    dist = {}
+
+    def p(u):
+        if u not in dist:
+            w = rng.gamma(0.7, 1.0, vocab)
+            dist[u] = w / w.sum()
+        return dist[u]
+
+    labels = []
+    while len(labels) < n_labels:
+        lab = tuple(int(t) for t in rng.integers(0, vocab, rng.integers(1, depth + 1)))
+        if any(lab == o[:len(lab)] or o == lab[:len(o)] for o in labels):
+            continue
+        labels.append(lab)
+    lps = [np.array([np.log(p(lab[:j])[lab[j]]) for j in range(len(lab))]) for lab in labels]
+    return labels, lps, p
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_per_level_by_brute_force(seed):
+    """Product over the label's levels of P_u(t) / sum of P_u over the
+    tokens that some label continues with after u, taken straight from the
+    toy model's node distributions.  The result is a distribution over the
+    labels, and a multi-level label never beats its first-level share."""
+    labels, lps, p = _random_trie_model(seed)
+    got = np.exp(per_level_scores(labels, lps))
+    for c, lab in enumerate(labels):
+        prob = 1.0
+        for j in range(len(lab)):
+            u = lab[:j]
+            allowed = {o[j] for o in labels if len(o) > j and o[:j] == u}
+            prob *= p(u)[lab[j]] / sum(p(u)[t] for t in allowed)
+        assert abs(got[c] - prob) < 1e-13
+        firsts = {o[0] for o in labels}
+        assert got[c] <= p(())[lab[0]] / sum(p(())[t] for t in firsts) + 1e-15
+    assert abs(got.sum() - 1.0) < 1e-13
+
+
+def test_length_normalised_mean():
+    """HIGH is one token at log-prob -0.5, MEDIUM two tokens at -0.3 each:
+    summing favours HIGH (-0.5 > -0.6), the per-token mean favours MEDIUM
+    (-0.3 > -0.5), the length bias the mean is there to remove."""
+    lps = [np.array([-0.5]), np.array([-0.3, -0.3])]
+    np.testing.assert_allclose(length_normalised_scores(lps), [-0.5, -0.3], atol=1e-15)
+    assert scores_to_result(field_scores("sum", [[1], [2, 3]], lps)).label == 0
+    assert scores_to_result(field_scores("mean", [[1], [2, 3]], lps)).label == 1
+    # one-token labels: the mean is the sum
+    one = [np.array([-1.25]), np.array([-0.75])]
+    np.testing.assert_array_equal(field_scores("mean", [[1], [2]], one), field_scores("sum", [[1], [2]], one))
+
+
+def test_scoring_rules_keep_the_mass(tiny_oracle64, request1):
+    """The scoring rule changes label, probabilities and margin, never the
+    full-vocabulary candidate mass or the first-token mass; the per-level
+    rule at T = 1 is already normalised, so its probabilities are exp(s)."""
+    orc = tiny_oracle64
+    cache = orc.prefill(request1.prefix)
+    for f in request1.fields:
+        base = orc.score_field(f, cache=cache)
+        for rule in ("mean", "level"):
+            g = synth.Field(f.scaffold, f.labels, f.temperature, f.kind, rule)
+            r = orc.score_field(g, cache=cache)
+            assert r.mass == base.mass and r.log_mass == base.log_mass and r.first_mass == base.first_mass
+            if rule == "level":
+                np.testing.assert_allclose(r.probs, np.exp(r.scores), atol=1e-12)
+            else:
+                lens = np.array([len(l) for l in f.labels])
+                np.testing.assert_allclose(r.scores * lens, base.scores, atol=1e-12)
 
 
 def test_workload_shapes():
