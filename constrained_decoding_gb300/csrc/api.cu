@@ -91,6 +91,7 @@ struct PlanView {
   const int32_t *tok, *rel, *anc_off, *anc_idx, *ro_tok, *row_ch, *child_row, *lab_off, *path, *fld_lab, *fld_root,
       *gather_off;
   const float* temp;
+  const int32_t* scoring;           // [n_fields] PCD_SCORE_* rule of each field
   const int4* gather;
   // tree-attention tiles over the branch tokens (up to tpt whole tokens of one request each)
   int tpt = 1, n_br_tiles = 0, max_tile_chunks = 0;
@@ -101,6 +102,27 @@ struct PlanView {
   const int32_t* tile_keys;
   const unsigned long long* tile_mask;
   int result_floats() const { return n_fields * 8 + 2 * n_labels; }
+  // Everything a captured pass bakes in from this view: the counts and the
+  // device address of every array (their offsets in the reused plan buffer
+  // depend on the lengths of the arrays before them).
+  void key_into(std::vector<int64_t>& k) const {
+    for (int x : {n_fields, T, R, n_children, n_labels, max_rel, n_vtiles, tpt, n_br_tiles, max_tile_chunks})
+      k.push_back(x);
+    for (const void* q : {static_cast<const void*>(tok), static_cast<const void*>(rel),
+                          static_cast<const void*>(anc_off), static_cast<const void*>(anc_idx),
+                          static_cast<const void*>(ro_tok), static_cast<const void*>(row_ch),
+                          static_cast<const void*>(child_row), static_cast<const void*>(lab_off),
+                          static_cast<const void*>(path), static_cast<const void*>(fld_lab),
+                          static_cast<const void*>(fld_root), static_cast<const void*>(gather_off),
+                          static_cast<const void*>(temp), static_cast<const void*>(scoring),
+                          static_cast<const void*>(gather), static_cast<const void*>(tile_tok),
+                          static_cast<const void*>(segs), static_cast<const void*>(abs_pos),
+                          static_cast<const void*>(tile_chunk_off), static_cast<const void*>(tile_keys),
+                          static_cast<const void*>(tile_mask)})
+      k.push_back(reinterpret_cast<int64_t>(q));
+    for (int x : {ro_tiling.mt, ro_tiling.bn, ro_tiling.splits, ro_tiling.cs, static_cast<int>(ro_tiling.pair)})
+      k.push_back(x);
+  }
 };
 
 enum ProfClass { PROF_GEMM_PREFILL = 0, PROF_GEMM_BRANCH = 1, PROF_ATTN_PREFILL = 2, PROF_ATTN_BRANCH = 3,
@@ -579,8 +601,8 @@ int run_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_seg, 
   PCD_TRY(ensure(m->z, static_cast<size_t>(std::max(p.n_children, 1)) * 4));
   PCD_TRY(ensure(m->lse, static_cast<size_t>(std::max(R, 1)) * 4));
   if (ev_mid) return record_branch(m, p, segs, n_seg, d_result, splits, ev_mid);
-  std::vector<int64_t> key{2, reinterpret_cast<int64_t>(p.tok), T, R, p.n_children, p.n_labels, p.n_fields,
-                           reinterpret_cast<int64_t>(d_result), splits, n_seg};
+  std::vector<int64_t> key{2, reinterpret_cast<int64_t>(d_result), splits, n_seg};
+  p.key_into(key);
   for (int s = 0; s < n_seg; ++s) {
     key.push_back(reinterpret_cast<int64_t>(segs[s].c->k));
     key.push_back(segs[s].c->cap);
@@ -787,6 +809,7 @@ int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_se
   sa.fld_root = p.fld_root;
   sa.row_ch = p.row_ch;
   sa.temp = p.temp;
+  sa.scoring = p.scoring;
   sa.n_fields = p.n_fields;
   sa.out_field = d_result;
   sa.out_probs = d_result + p.n_fields * 8;
@@ -830,9 +853,9 @@ int run_single(pcd_model* m, const PlanView& p, const int32_t* d_ids, int n, pcd
   PCD_TRY(ensure(m->z, static_cast<size_t>(std::max(p.n_children, 1)) * 4));
   PCD_TRY(ensure(m->lse, static_cast<size_t>(std::max(R, 1)) * 4));
   const int32_t* ids = static_cast<const int32_t*>(m->ids.p);
-  const std::vector<int64_t> key{3, n, reinterpret_cast<int64_t>(p.tok), T, R, p.n_children, p.n_labels, p.n_fields,
-                                 reinterpret_cast<int64_t>(d_result), reinterpret_cast<int64_t>(c->k), c->cap,
-                                 pf_splits, br_splits};
+  std::vector<int64_t> key{3, n, reinterpret_cast<int64_t>(d_result), reinterpret_cast<int64_t>(c->k), c->cap,
+                           pf_splits, br_splits};
+  p.key_into(key);
   return with_graph(m, key, [&] { return record_single(m, p, ids, n, c, d_result, pf_splits, br_splits); });
 }
 
@@ -1061,6 +1084,7 @@ int record_single(pcd_model* m, const PlanView& p, const int32_t* ids, int n, pc
   sa.fld_root = p.fld_root;
   sa.row_ch = p.row_ch;
   sa.temp = p.temp;
+  sa.scoring = p.scoring;
   sa.n_fields = p.n_fields;
   sa.out_field = d_result;
   sa.out_probs = d_result + p.n_fields * 8;
@@ -1192,6 +1216,7 @@ size_t plan_blob(const pcd_model* m, const pcd::HostPlan& hp, std::vector<int32_
   v.fld_lab = put(hp.fld_lab.data(), hp.fld_lab.size());
   v.fld_root = put(hp.fld_root.data(), hp.fld_root.size());
   v.temp = reinterpret_cast<const float*>(put(reinterpret_cast<const int32_t*>(hp.temp.data()), hp.temp.size()));
+  v.scoring = put(hp.scoring.data(), hp.scoring.size());
   v.gather_off = put(goff.data(), goff.size());
   v.gather = reinterpret_cast<const int4*>(put(g4.data(), g4.size()));
   v.tile_tok = put(ttok.data(), ttok.size());

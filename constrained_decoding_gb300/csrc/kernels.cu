@@ -6,6 +6,7 @@
 
 #include "common.cuh"
 #include "kernels.h"
+#include "pcd.h"
 #include "warp_mma.cuh"
 
 namespace pcd {
@@ -562,9 +563,13 @@ int launch_lse_combine(const float2* part, int n_tiles, int R, float* lse, cudaS
 }
 
 // ====================================================================== score
-// One CTA per field.  Label score s_c = sum over its path of (z - lse); then
-// the candidate-only softmax at temperature T, the argmax (lowest index on
-// ties), the candidate mass sum_c exp(s_c), the top-2 margin of s and the
+// One CTA per field.  The full-vocabulary log-probability of a label is
+// ss_c = sum over its path of (z - lse).  The field's rule makes its score:
+// s_c = ss_c (sum), ss_c / path length (length-normalised mean), or the sum
+// over its path of (z - log-sum-exp of the logits of the tokens allowed at
+// that trie node) (per-level product of renormalised decisions).  Then the
+// candidate-only softmax of s at temperature T, the argmax (lowest index on
+// ties), the top-2 margin of s, the candidate mass sum_c exp(ss_c) and the
 // first-decision mass (distinct first tokens at the root readout row).
 __global__ void __launch_bounds__(256) score_kernel(ScoreArgs a) {
   griddep_launch_dependents();
@@ -573,22 +578,34 @@ __global__ void __launch_bounds__(256) score_kernel(ScoreArgs a) {
   const int c0 = a.fld_lab[f], c1 = a.fld_lab[f + 1];
   const int nl = c1 - c0;
   const float T = a.temp[f];
-  __shared__ float s_sc[256];
+  const int rule = a.scoring[f];
   __shared__ float red[32];
   __shared__ int redi[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
 
   // scores (labels beyond 256 per field are rejected by the host)
-  float sc = -INFINITY;
+  float sc = -INFINITY, ss = -INFINITY;
   if (tid < nl) {
     const int c = c0 + tid;
-    float acc = 0.f;
-    for (int i = a.lab_off[c]; i < a.lab_off[c + 1]; ++i) {
+    const int i0 = a.lab_off[c], i1 = a.lab_off[c + 1];
+    float acc = 0.f, lvl = 0.f;
+    for (int i = i0; i < i1; ++i) {
       const int e = a.path[i];
-      acc += a.z[e] - a.lse[a.child_row[e]];
+      const int r = a.child_row[e];
+      const float ze = a.z[e];
+      acc += ze - a.lse[r];
+      if (rule == PCD_SCORE_LEVEL) {
+        // the node's allowed next tokens are its readout row's child entries
+        const int e0 = a.row_ch[r], e1 = a.row_ch[r + 1];
+        float m = -INFINITY;
+        for (int x = e0; x < e1; ++x) m = fmaxf(m, a.z[x]);
+        float sum = 0.f;
+        for (int x = e0; x < e1; ++x) sum += __expf(a.z[x] - m);
+        lvl += ze - (m + __logf(sum));
+      }
     }
-    sc = acc;
-    s_sc[tid] = acc;
+    ss = acc;
+    sc = rule == PCD_SCORE_MEAN ? acc / static_cast<float>(i1 - i0) : (rule == PCD_SCORE_LEVEL ? lvl : acc);
   }
   // block max of s (and its first index), block max of s/T
   auto block_max_idx = [&](float v, int idx, float& out_v, int& out_i) {
@@ -639,7 +656,11 @@ __global__ void __launch_bounds__(256) score_kernel(ScoreArgs a) {
   float s2;
   int i2;
   block_max_idx((tid < nl && tid != top) ? sc : -INFINITY, tid, s2, i2);
-  const float es = tid < nl ? __expf(sc - smax) : 0.f;
+  // candidate mass from the full-vocabulary log-probs
+  float ssmax;
+  int ssi;
+  block_max_idx(ss, tid, ssmax, ssi);
+  const float es = tid < nl ? __expf(ss - ssmax) : 0.f;
   const float sum_es = block_sum(es);
   const float ea = tid < nl ? __expf((sc - smax) / T) : 0.f;
   const float sum_ea = block_sum(ea);
@@ -654,7 +675,7 @@ __global__ void __launch_bounds__(256) score_kernel(ScoreArgs a) {
     a.out_logprobs[c0 + tid] = sc;
   }
   if (tid == 0) {
-    const float lm = smax + __logf(sum_es);
+    const float lm = ssmax + __logf(sum_es);
     float* o = a.out_field + static_cast<size_t>(f) * 8;
     o[0] = static_cast<float>(top);
     o[1] = __expf(lm);

@@ -153,6 +153,7 @@ struct ScoreArgs {
   const int32_t* fld_root;  // root readout row of each field
   const int32_t* row_ch;    // [R + 1] child entries of each readout row
   const float* temp;        // [n_fields]
+  const int32_t* scoring;   // [n_fields] PCD_SCORE_SUM / _MEAN / _LEVEL
   int n_fields;
   float* out_field;         // [n_fields][8]: label, mass, log_mass, margin, first_mass, n_labels, 0, 0
   float* out_probs;         // [n_labels_total]

@@ -53,6 +53,10 @@ int compile_fields(const pcd_field* fields, int n_fields, int vocab, HostPlan* p
       *msg = where + "temperature must be finite and >= 0";
       return PCD_ERR_INVALID_ARG;
     }
+    if (F.scoring != PCD_SCORE_SUM && F.scoring != PCD_SCORE_MEAN && F.scoring != PCD_SCORE_LEVEL) {
+      *msg = where + "unknown scoring rule " + std::to_string(F.scoring);
+      return PCD_ERR_INVALID_ARG;
+    }
     for (int k = 0; k < F.n_scaffold; ++k)
       if (F.scaffold[k] < 0 || F.scaffold[k] >= vocab) {
         *msg = where + "scaffold token out of range";
@@ -167,6 +171,7 @@ int compile_fields(const pcd_field* fields, int n_fields, int vocab, HostPlan* p
     }
     p->fld_lab.push_back(p->n_labels);
     p->temp.push_back(F.temperature > 0.f ? F.temperature : 1.f);
+    p->scoring.push_back(F.scoring);
     p->n_fields++;
   }
   return PCD_OK;

@@ -33,6 +33,7 @@ struct HostPlan {
   std::vector<int32_t> fld_lab;    // [n_fields + 1] labels of each field
   std::vector<int32_t> fld_root;   // [n_fields] readout row of the field's scaffold end
   std::vector<float> temp;         // [n_fields]
+  std::vector<int32_t> scoring;    // [n_fields] PCD_SCORE_* rule
   std::vector<int32_t> seg_off;    // [requests + 1] branch tokens of each request (empty: one request)
 };
 

@@ -199,6 +199,21 @@ def pcd_cache_free(cache: Cache) -> None:
 
 
 # ------------------------------------------------------------------- score
+SCORING = {"sum": 0, "mean": 1, "level": 2}
+
+
+def scoring_code(rule) -> int:
+    """PCD_SCORE_* code of a field's scoring rule, given by name ("sum",
+    "mean", "level") or code; None means "sum"."""
+    if rule is None:
+        return 0
+    if isinstance(rule, str):
+        if rule not in SCORING:
+            raise ValueError(f"unknown scoring rule {rule!r}")
+        return SCORING[rule]
+    return int(rule)
+
+
 class _Fields:
     """Keeps the int32 arrays of a list of fields alive for one call."""
 
@@ -213,7 +228,8 @@ class _Fields:
             offs = _i32(np.concatenate([[0], np.cumsum([len(l) for l in labels])]))
             self.keep += [sc, toks, offs]
             self.arr[i] = D.pcd_field(_ptr_i32(sc), len(sc), _ptr_i32(toks), _ptr_i32(offs), len(labels),
-                                      float(getattr(f, "temperature", 1.0) or 0.0))
+                                      float(getattr(f, "temperature", 1.0) or 0.0),
+                                      scoring_code(getattr(f, "scoring", "sum")))
             self.n_cands.append(len(labels))
 
 

@@ -89,7 +89,20 @@ typedef struct {
  *    may share prefixes (scored through the trie) but no label may be a
  *    strict prefix of another: append the terminator token the tokenizer
  *    writes after a value.
- *  temperature: T > 0 divides the summed log-probs; 0 means 1. */
+ *  temperature: T > 0 divides the label scores before the softmax; 0 means 1.
+ *  scoring: how a label's token log-probs make its score s_c
+ *    PCD_SCORE_SUM   their sum, log P(label) (default, zero-initialised);
+ *    PCD_SCORE_MEAN  their mean, sum / n_tokens (PCD From First Principles,
+ *                    "Multi-token candidates": length-normalised);
+ *    PCD_SCORE_LEVEL the log of the product, over the trie levels on the
+ *                    label's path, of the next token's probability
+ *                    renormalised over the tokens the field allows there
+ *                    (PCD: A Technical Reference, "Resolve shared prefixes
+ *                    level by level").
+ *    Any other value is PCD_ERR_INVALID_ARG. */
+#define PCD_SCORE_SUM 0
+#define PCD_SCORE_MEAN 1
+#define PCD_SCORE_LEVEL 2
 typedef struct {
   const int32_t* scaffold;
   int n_scaffold;
@@ -97,13 +110,16 @@ typedef struct {
   const int32_t* cand_offsets;
   int n_cands;
   float temperature;
+  int scoring;
 } pcd_field;
 
 /* Per-field result.  probs / logprobs are caller-owned arrays of n_cands
- * floats (may be NULL to skip).  logprobs[c] = s_c, the sum of the label's
- * full-vocabulary token log-probs; probs[c] = softmax(s / T)[c];
- * label = argmax (lowest index on exact ties); mass = sum_c exp(s_c),
- * log_mass = log(mass); margin = s_top1 - s_top2; first_mass = probability
+ * floats (may be NULL to skip).  logprobs[c] = s_c, the label's score under
+ * the field's scoring rule (PCD_SCORE_SUM: the sum of its full-vocabulary
+ * token log-probs); probs[c] = softmax(s / T)[c]; label = argmax (lowest
+ * index on exact ties); margin = s_top1 - s_top2.  Whatever the rule,
+ * mass = sum_c P(label c) with P the full-vocabulary product of the label's
+ * token probabilities, log_mass = log(mass), and first_mass = probability
  * that the next token after the scaffold starts any allowed label. */
 typedef struct {
   float* probs;

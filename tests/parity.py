@@ -51,3 +51,23 @@ def compare_request(gpu_results, ref_results, where="", prob_tol=PROB_TOL):
         for k, v in e.items():
             worst[k] = max(worst.get(k, 0.0), v)
     return worst
+
+
+def with_rule(fields, rule):
+    """Copies of `fields` scored under `rule` ("sum", "mean", "level"); a list
+    of rules is applied field by field, cycling."""
+    import dataclasses
+    rules = [rule] if isinstance(rule, str) else list(rule)
+    return [dataclasses.replace(f, scoring=rules[i % len(rules)]) for i, f in enumerate(fields)]
+
+
+def rescore(ref, field):
+    """The oracle's result for `field` under its scoring rule, from an oracle
+    result `ref` of the same labels (its token log-probs; the decoder does
+    not run again)."""
+    from oracle import field_scores, scores_to_result
+    rule = getattr(field, "scoring", "sum") or "sum"
+    out = scores_to_result(field_scores(rule, field.labels, ref.token_logprobs), field.temperature)
+    out.mass, out.log_mass, out.first_mass = ref.mass, ref.log_mass, ref.first_mass
+    out.token_logprobs = ref.token_logprobs
+    return out

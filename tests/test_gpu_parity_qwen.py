@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 
 import synth
-from parity import compare_request, compare_field
+from parity import compare_request, compare_field, rescore, with_rule
 
 pytestmark = pytest.mark.gpu
 
@@ -59,6 +59,13 @@ def test_config2_triage_full(qwen):
     assert c3.length == len(req.prefix)
     compare_request(pcd.unpack_plan_result(out.cpu().numpy(), [len(f.labels) for f in req.fields]), ref,
                     "config 2, single pass device plan")
+    # the alternative scoring rules on the same cache (the oracle rescores its
+    # token log-probs; the decoder does not run again)
+    for rule in ("mean", "level"):
+        fs = with_rule(req.fields, rule)
+        print(f"config 2 rule {rule} worst errors",
+              compare_request(pcd.pcd_score(model, cache, fs), [rescore(r, f) for r, f in zip(ref, fs)],
+                              f"config 2, rule {rule}"))
 
 
 def test_config3_router(qwen):

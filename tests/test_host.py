@@ -130,6 +130,16 @@ def test_branch_compiler_validation(lib):
     bad_T = F(np.array([1]), [np.array([5]), np.array([6])], temperature=-1.0)
     with pytest.raises(pcd.PCDError):
         pcd.pcd_plan_inspect([bad_T], 512)
+    # scoring rules: the three known ones compile to the same plan, others are rejected
+    for rule in ("sum", "mean", "level", 0, 1, 2):
+        ok = F(np.array([1]), [np.array([5, 7]), np.array([6])], scoring=rule)
+        assert pcd.pcd_plan_inspect([ok], 512)["NL"] == 2
+    for rule in (3, -1):
+        with pytest.raises(pcd.PCDError) as ei:
+            pcd.pcd_plan_inspect([F(np.array([1]), [np.array([5]), np.array([6])], scoring=rule)], 512)
+        assert ei.value.code == -1
+    with pytest.raises(ValueError):
+        pcd.pcd_plan_inspect([F(np.array([1]), [np.array([5]), np.array([6])], scoring="max")], 512)
 
 
 def _replica_worker(rank, world, port, out):
