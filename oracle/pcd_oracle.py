@@ -45,6 +45,10 @@ Readings where the pages are silent (each also listed in the design notes):
   product) T divides that score instead, and the label, probabilities and
   margin follow it, while mass, log-mass and first-token mass keep their
   full-vocabulary definitions;
+* a label with several spellings (token paths) scores each path by the
+  field's rule and takes the log-sum-exp of those path scores (for the
+  summed rule: the probability of writing any of its spellings); the mass
+  counts every allowed path;
 * the label's last token is a leaf: a label that is a strict prefix of
   another is not a valid schema (the caller appends its terminator token).
 
@@ -399,11 +403,18 @@ class Oracle:
             else:
                 raise ValueError(mode)
         # the scoring rule decides label, probabilities and margin; the mass
-        # stays the full-vocabulary probability of the allowed labels
+        # stays the full-vocabulary probability of the allowed labels.  With
+        # several spellings per label (``field.label_of``) every token path
+        # is scored by the rule and a label gets the log-sum-exp of its
+        # paths' scores.
         scoring = getattr(field, "scoring", "sum") or "sum"
+        label_of = getattr(field, "label_of", None)
         sums = field_scores("sum", field.labels, lps)
-        res = scores_to_result(field_scores(scoring, field.labels, lps), getattr(field, "temperature", 1.0))
-        if scoring != "sum":
+        scores = field_scores(scoring, field.labels, lps)
+        if label_of is not None:
+            scores = combine_spellings(scores, label_of)
+        res = scores_to_result(scores, getattr(field, "temperature", 1.0))
+        if scoring != "sum" or label_of is not None:
             m = sums.max()
             res.log_mass = float(m + np.log(np.exp(sums - m).sum()))
             res.mass = float(np.exp(res.log_mass))

@@ -30,6 +30,8 @@ class Field:
     temperature: float = 1.0
     kind: str = "enum"
     scoring: str = "sum"                 # "sum", "mean" (length-normalised) or "level" (per-level product)
+    label_of: Optional[np.ndarray] = None  # label of each token path in `labels` (several spellings
+                                           # of one label); None: one path per label
 
 
 @dataclass
@@ -97,6 +99,27 @@ def _line_id_field(rng, V, S, n_labels=218) -> Field:
     return Field(_i32(scaffold), labels, kind="line_id")
 
 
+def _spelled_field(rng, V, S, n_labels=2, n_spell=2) -> Field:
+    """Labels with several spellings: label i is written bare (its own ids,
+    1-2 tokens), quoted (a quote id, the same ids, the quote id again) and,
+    with n_spell = 3, as one more id of its own (another capitalisation)."""
+    scaffold = rng.integers(0, V, S)
+    lens = rng.integers(1, 3, n_labels)
+    ids = rng.choice(V, 1 + int(lens.sum()) + n_labels, replace=False)
+    quote, o = ids[0], 1
+    paths, label_of = [], []
+    for i, n in enumerate(lens):
+        base = list(ids[o:o + n])
+        o += n
+        spellings = [base, [quote, *base, quote]]
+        if n_spell >= 3:
+            spellings.append([ids[1 + int(lens.sum()) + i]])
+        for sp in spellings:
+            paths.append(_i32(sp))
+            label_of.append(i)
+    return Field(_i32(scaffold), paths, kind="spelled", label_of=_i32(label_of))
+
+
 def _triage_schema(rng, V, S=8) -> List[Field]:
     """28 fields: 10 booleans and 18 four-way enums of 1-4 token labels."""
     kinds = np.array(["bool"] * 10 + ["enum"] * 18)
@@ -148,7 +171,8 @@ def make_custom(seed: int, vocab: int, prefix_len: int, specs, scaffold_len: int
     """A request with an explicit list of field shapes, for edge-case tests.
 
     ``specs`` items: ("bool",), ("enum", n_labels, lo, hi), ("shared", n_labels,
-    lo, hi), ("router", n_labels) or ("line_id", n_labels); an optional
+    lo, hi), ("router", n_labels), ("line_id", n_labels) or ("spelled", n_labels,
+    n_spell); an optional
     ("scaffold", S) item before a field sets that field's scaffold length.
     """
     rng = np.random.default_rng(seed)
@@ -169,6 +193,8 @@ def make_custom(seed: int, vocab: int, prefix_len: int, specs, scaffold_len: int
             fields.append(_router_field(rng, vocab, S, *sp[1:]))
         elif kind == "line_id":
             fields.append(_line_id_field(rng, vocab, S, *sp[1:]))
+        elif kind == "spelled":
+            fields.append(_spelled_field(rng, vocab, S, *sp[1:]))
         else:
             raise ValueError(kind)
     return Request(_i32(prefix), fields)

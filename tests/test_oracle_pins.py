@@ -454,6 +454,42 @@ def test_scoring_rules_keep_the_mass(tiny_oracle64, request1):
                 np.testing.assert_allclose(r.scores * lens, base.scores, atol=1e-12)
 
 
+def test_spelled_labels_by_brute_force(tiny_oracle64):
+    """Labels with several spellings: at T = 1 a label's probability is the
+    sum over its spellings of the product of the spelling's token
+    probabilities, each token's probability written out from the logits of
+    the complete sequence, divided by that sum over every spelling; the mass
+    is the latter sum.  Under the per-level rule the label probabilities
+    (the sums of their paths' per-level products) add up to 1."""
+    from synth.requests import make_custom
+    orc = tiny_oracle64
+    req = make_custom(3, 512, 20, [("spelled", 2, 2), ("spelled", 3, 3)])
+    cache = orc.prefill(req.prefix)
+    P = req.prefix
+    for f in req.fields:
+        res = orc.score_field(f, cache=cache)
+        path_p = []
+        for lab in f.labels:
+            seq = np.concatenate([P, f.scaffold, lab])
+            h, _ = orc.forward(seq, np.arange(len(seq)))
+            z = orc.logits(h)
+            prob = 1.0
+            for j, t in enumerate(lab):
+                row = z[len(P) + len(f.scaffold) - 1 + j]
+                prob *= np.exp(row[t]) / np.exp(row).sum()
+            path_p.append(prob)
+        path_p = np.array(path_p)
+        n_lab = int(f.label_of.max()) + 1
+        lab_p = np.array([path_p[f.label_of == i].sum() for i in range(n_lab)])
+        np.testing.assert_allclose(res.probs, lab_p / path_p.sum(), atol=1e-10)
+        np.testing.assert_allclose(np.exp(res.scores), lab_p, rtol=1e-9)
+        assert abs(res.mass - path_p.sum()) < 1e-10 * max(1.0, path_p.sum()) + 1e-15
+        assert res.label == int(np.argmax(lab_p))
+        lvl = orc.score_field(synth.Field(f.scaffold, f.labels, 1.0, f.kind, "level", f.label_of), cache=cache)
+        assert abs(np.exp(lvl.scores).sum() - 1.0) < 1e-12
+        assert lvl.mass == res.mass
+
+
 def test_workload_shapes():
     """The generators give the branch sizes the workloads are described with."""
     r2 = synth.make_request(2)
