@@ -15,7 +15,7 @@ class pcd_model_config(ctypes.Structure):
 class pcd_field(ctypes.Structure):
     _fields_ = [("scaffold", P(c_int32)), ("n_scaffold", c_int), ("cand_tokens", P(c_int32)),
                 ("cand_offsets", P(c_int32)), ("n_cands", c_int), ("temperature", c_float),
-                ("scoring", c_int)]
+                ("scoring", c_int), ("cand_label", P(c_int32)), ("n_labels", c_int)]
 
 
 class pcd_field_result(ctypes.Structure):

@@ -86,12 +86,15 @@ struct Layer {
 // Device view of a compiled branch batch (all pointers into one int32 blob).
 struct PlanView {
   int n_fields = 0, T = 0, R = 0, n_children = 0, n_labels = 0, max_rel = 0;
+  int n_out = 0;  // labels of all fields (n_labels counts their candidate paths)
   int n_vtiles = 0;
   pcd::GemmTiling ro_tiling;
   const int32_t *tok, *rel, *anc_off, *anc_idx, *ro_tok, *row_ch, *child_row, *lab_off, *path, *fld_lab, *fld_root,
       *gather_off;
   const float* temp;
   const int32_t* scoring;           // [n_fields] PCD_SCORE_* rule of each field
+  const int32_t* cand_label;        // [n_labels] label (within its field) of each candidate path
+  const int32_t* fld_out;           // [n_fields + 1] outputs of each field
   const int4* gather;
   // tree-attention tiles over the branch tokens (up to tpt whole tokens of one request each)
   int tpt = 1, n_br_tiles = 0, max_tile_chunks = 0;
@@ -101,12 +104,12 @@ struct PlanView {
   const int32_t* tile_chunk_off;
   const int32_t* tile_keys;
   const unsigned long long* tile_mask;
-  int result_floats() const { return n_fields * 8 + 2 * n_labels; }
+  int result_floats() const { return n_fields * 8 + 2 * n_out; }
   // Everything a captured pass bakes in from this view: the counts and the
   // device address of every array (their offsets in the reused plan buffer
   // depend on the lengths of the arrays before them).
   void key_into(std::vector<int64_t>& k) const {
-    for (int x : {n_fields, T, R, n_children, n_labels, max_rel, n_vtiles, tpt, n_br_tiles, max_tile_chunks})
+    for (int x : {n_fields, T, R, n_children, n_labels, n_out, max_rel, n_vtiles, tpt, n_br_tiles, max_tile_chunks})
       k.push_back(x);
     for (const void* q : {static_cast<const void*>(tok), static_cast<const void*>(rel),
                           static_cast<const void*>(anc_off), static_cast<const void*>(anc_idx),
@@ -115,6 +118,7 @@ struct PlanView {
                           static_cast<const void*>(path), static_cast<const void*>(fld_lab),
                           static_cast<const void*>(fld_root), static_cast<const void*>(gather_off),
                           static_cast<const void*>(temp), static_cast<const void*>(scoring),
+                          static_cast<const void*>(cand_label), static_cast<const void*>(fld_out),
                           static_cast<const void*>(gather), static_cast<const void*>(tile_tok),
                           static_cast<const void*>(segs), static_cast<const void*>(abs_pos),
                           static_cast<const void*>(tile_chunk_off), static_cast<const void*>(tile_keys),
@@ -810,10 +814,12 @@ int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_se
   sa.row_ch = p.row_ch;
   sa.temp = p.temp;
   sa.scoring = p.scoring;
+  sa.cand_label = p.cand_label;
+  sa.fld_out = p.fld_out;
   sa.n_fields = p.n_fields;
   sa.out_field = d_result;
   sa.out_probs = d_result + p.n_fields * 8;
-  sa.out_logprobs = d_result + p.n_fields * 8 + p.n_labels;
+  sa.out_logprobs = d_result + p.n_fields * 8 + p.n_out;
   PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_score(sa, m->stream); }));
   return PCD_OK;
 }
@@ -1085,10 +1091,12 @@ int record_single(pcd_model* m, const PlanView& p, const int32_t* ids, int n, pc
   sa.row_ch = p.row_ch;
   sa.temp = p.temp;
   sa.scoring = p.scoring;
+  sa.cand_label = p.cand_label;
+  sa.fld_out = p.fld_out;
   sa.n_fields = p.n_fields;
   sa.out_field = d_result;
   sa.out_probs = d_result + p.n_fields * 8;
-  sa.out_logprobs = d_result + p.n_fields * 8 + p.n_labels;
+  sa.out_logprobs = d_result + p.n_fields * 8 + p.n_out;
   PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_score(sa, m->stream); }));
   return PCD_OK;
 }
@@ -1134,6 +1142,7 @@ size_t plan_blob(const pcd_model* m, const pcd::HostPlan& hp, std::vector<int32_
   v.R = hp.R;
   v.n_children = hp.n_children;
   v.n_labels = hp.n_labels;
+  v.n_out = hp.n_out;
   v.max_rel = hp.max_rel;
   v.ro_tiling = pcd::choose_tiling(hp.R, m->V, m->d, pcd::EPI_READOUT, m->sms);
   v.ro_tiling.splits = 1;
@@ -1217,6 +1226,8 @@ size_t plan_blob(const pcd_model* m, const pcd::HostPlan& hp, std::vector<int32_
   v.fld_root = put(hp.fld_root.data(), hp.fld_root.size());
   v.temp = reinterpret_cast<const float*>(put(reinterpret_cast<const int32_t*>(hp.temp.data()), hp.temp.size()));
   v.scoring = put(hp.scoring.data(), hp.scoring.size());
+  v.cand_label = put(hp.cand_label.data(), hp.cand_label.size());
+  v.fld_out = put(hp.fld_out.data(), hp.fld_out.size());
   v.gather_off = put(goff.data(), goff.size());
   v.gather = reinterpret_cast<const int4*>(put(g4.data(), g4.size()));
   v.tile_tok = put(ttok.data(), ttok.size());
@@ -1579,7 +1590,7 @@ int upload_plan(pcd_model* m, const pcd::HostPlan& hp, PlanView& v, size_t* byte
 void unpack_results(const float* res, const PlanView& v, int f0, int l0, int n_fields, pcd_field_result* out) {
   const float* fl = res;
   const float* probs = res + v.n_fields * 8;
-  const float* lps = probs + v.n_labels;
+  const float* lps = probs + v.n_out;
   int lab = l0;
   for (int f = 0; f < n_fields; ++f) {
     const float* o = fl + (f0 + f) * 8;
@@ -1608,7 +1619,7 @@ int score_impl(pcd_model* m, const pcd_cache* const* caches, const pcd_field* co
     if (!caches[r] || caches[r]->m != m) return fail(PCD_ERR_SHAPE_MISMATCH, "cache belongs to another model");
     if (n_fields[r] < 1 || !fields[r] || !out[r]) return fail(PCD_ERR_INVALID_ARG, "request without fields");
     field0[r] = hp.n_fields;
-    label0[r] = hp.n_labels;
+    label0[r] = hp.n_out;
     const int t0 = hp.T;
     const int rel0 = hp.max_rel;
     hp.max_rel = 0;

@@ -201,10 +201,12 @@ extern "C" int pcd_plan_inspect(const void* fields, int n_fields, int vocab, int
   sizes[4] = p.n_path;
   sizes[5] = static_cast<int32_t>(p.anc_idx.size());
   sizes[6] = p.n_fields;
+  sizes[7] = p.n_out;
   if (arrays) {
-    const std::vector<int32_t>* src[12] = {&p.tok,     &p.rel,       &p.anc_off, &p.anc_idx, &p.ro_tok,  &p.row_ch,
-                                          &p.ch_tok,  &p.child_row, &p.lab_off, &p.path,    &p.fld_lab, &p.fld_root};
-    for (int i = 0; i < 12; ++i)
+    const std::vector<int32_t>* src[15] = {&p.tok,     &p.rel,       &p.anc_off,    &p.anc_idx, &p.ro_tok,
+                                          &p.row_ch,  &p.ch_tok,    &p.child_row,  &p.lab_off, &p.path,
+                                          &p.fld_lab, &p.fld_root,  &p.cand_label, &p.fld_out, &p.scoring};
+    for (int i = 0; i < 15; ++i)
       if (arrays[i] && !src[i]->empty()) std::memcpy(arrays[i], src[i]->data(), src[i]->size() * sizeof(int32_t));
   }
   return PCD_OK;

@@ -563,28 +563,33 @@ int launch_lse_combine(const float2* part, int n_tiles, int R, float* lse, cudaS
 }
 
 // ====================================================================== score
-// One CTA per field.  The full-vocabulary log-probability of a label is
-// ss_c = sum over its path of (z - lse).  The field's rule makes its score:
-// s_c = ss_c (sum), ss_c / path length (length-normalised mean), or the sum
-// over its path of (z - log-sum-exp of the logits of the tokens allowed at
-// that trie node) (per-level product of renormalised decisions).  Then the
+// One CTA per field.  The full-vocabulary log-probability of a candidate path
+// is ss_p = sum over the path of (z - lse).  The field's rule makes the path's
+// score: sp_p = ss_p (sum), ss_p / path length (length-normalised mean), or
+// the sum over the path of (z - log-sum-exp of the logits of the tokens
+// allowed at that trie node) (per-level product of renormalised decisions).
+// A label's score s_c is the log-sum-exp of the scores of the paths that
+// spell it (one path per label unless the field lists spellings).  Then the
 // candidate-only softmax of s at temperature T, the argmax (lowest index on
-// ties), the top-2 margin of s, the candidate mass sum_c exp(ss_c) and the
+// ties), the top-2 margin of s, the candidate mass sum_p exp(ss_p) and the
 // first-decision mass (distinct first tokens at the root readout row).
 __global__ void __launch_bounds__(256) score_kernel(ScoreArgs a) {
   griddep_launch_dependents();
   griddep_wait();
   const int f = blockIdx.x;
   const int c0 = a.fld_lab[f], c1 = a.fld_lab[f + 1];
-  const int nl = c1 - c0;
+  const int nl = c1 - c0;                                 // candidate paths
+  const int o0 = a.fld_out[f], no = a.fld_out[f + 1] - o0;  // labels
   const float T = a.temp[f];
   const int rule = a.scoring[f];
+  __shared__ float s_path[256];
+  __shared__ int s_lab[256];
   __shared__ float red[32];
   __shared__ int redi[32];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
 
-  // scores (labels beyond 256 per field are rejected by the host)
-  float sc = -INFINITY, ss = -INFINITY;
+  // path scores (more than 255 paths per field are rejected by the host)
+  float sp = -INFINITY, ss = -INFINITY;
   if (tid < nl) {
     const int c = c0 + tid;
     const int i0 = a.lab_off[c], i1 = a.lab_off[c + 1];
@@ -605,7 +610,22 @@ __global__ void __launch_bounds__(256) score_kernel(ScoreArgs a) {
       }
     }
     ss = acc;
-    sc = rule == PCD_SCORE_MEAN ? acc / static_cast<float>(i1 - i0) : (rule == PCD_SCORE_LEVEL ? lvl : acc);
+    sp = rule == PCD_SCORE_MEAN ? acc / static_cast<float>(i1 - i0) : (rule == PCD_SCORE_LEVEL ? lvl : acc);
+    s_path[tid] = sp;
+    s_lab[tid] = a.cand_label[c];
+  }
+  __syncthreads();
+  // label scores: log-sum-exp over the label's spellings (exactly the path's
+  // score when it has one)
+  float sc = -INFINITY;
+  if (tid < no) {
+    float m = -INFINITY;
+    for (int q = 0; q < nl; ++q)
+      if (s_lab[q] == tid) m = fmaxf(m, s_path[q]);
+    float sum = 0.f;
+    for (int q = 0; q < nl; ++q)
+      if (s_lab[q] == tid) sum += __expf(s_path[q] - m);
+    sc = m + __logf(sum);
   }
   // block max of s (and its first index), block max of s/T
   auto block_max_idx = [&](float v, int idx, float& out_v, int& out_i) {
@@ -651,18 +671,18 @@ __global__ void __launch_bounds__(256) score_kernel(ScoreArgs a) {
   };
   float smax;
   int top;
-  block_max_idx(sc, tid < nl ? tid : 0x7fffffff, smax, top);
+  block_max_idx(sc, tid < no ? tid : 0x7fffffff, smax, top);
   // second best score: max over everything but the argmax
   float s2;
   int i2;
-  block_max_idx((tid < nl && tid != top) ? sc : -INFINITY, tid, s2, i2);
+  block_max_idx((tid < no && tid != top) ? sc : -INFINITY, tid, s2, i2);
   // candidate mass from the full-vocabulary log-probs
   float ssmax;
   int ssi;
   block_max_idx(ss, tid, ssmax, ssi);
   const float es = tid < nl ? __expf(ss - ssmax) : 0.f;
   const float sum_es = block_sum(es);
-  const float ea = tid < nl ? __expf((sc - smax) / T) : 0.f;
+  const float ea = tid < no ? __expf((sc - smax) / T) : 0.f;
   const float sum_ea = block_sum(ea);
   // first-decision mass at the field's root readout row
   const int root = a.fld_root[f];
@@ -670,9 +690,9 @@ __global__ void __launch_bounds__(256) score_kernel(ScoreArgs a) {
   for (int e = a.row_ch[root] + tid; e < a.row_ch[root + 1]; e += blockDim.x) fm += __expf(a.z[e] - a.lse[root]);
   fm = block_sum(fm);
 
-  if (tid < nl) {
-    a.out_probs[c0 + tid] = ea / sum_ea;
-    a.out_logprobs[c0 + tid] = sc;
+  if (tid < no) {
+    a.out_probs[o0 + tid] = ea / sum_ea;
+    a.out_logprobs[o0 + tid] = sc;
   }
   if (tid == 0) {
     const float lm = ssmax + __logf(sum_es);
@@ -680,9 +700,9 @@ __global__ void __launch_bounds__(256) score_kernel(ScoreArgs a) {
     o[0] = static_cast<float>(top);
     o[1] = __expf(lm);
     o[2] = lm;
-    o[3] = nl > 1 ? smax - s2 : INFINITY;
+    o[3] = no > 1 ? smax - s2 : INFINITY;
     o[4] = fm;
-    o[5] = static_cast<float>(nl);
+    o[5] = static_cast<float>(no);
     o[6] = 0.f;
     o[7] = 0.f;
   }

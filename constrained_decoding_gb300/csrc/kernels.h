@@ -147,13 +147,15 @@ struct ScoreArgs {
   const float* z;           // gathered candidate logits, one per child entry
   const float* lse;         // [R]
   const int32_t* child_row; // readout row of each child entry
-  const int32_t* lab_off;   // [n_labels_total + 1] CSR into path_entries
+  const int32_t* lab_off;   // [n_paths_total + 1] CSR into path_entries
   const int32_t* path;      // child entry of every step of every label path
-  const int32_t* fld_lab;   // [n_fields + 1] labels of each field
+  const int32_t* fld_lab;   // [n_fields + 1] candidate paths of each field
   const int32_t* fld_root;  // root readout row of each field
   const int32_t* row_ch;    // [R + 1] child entries of each readout row
   const float* temp;        // [n_fields]
   const int32_t* scoring;   // [n_fields] PCD_SCORE_SUM / _MEAN / _LEVEL
+  const int32_t* cand_label;  // [n_paths_total] label (within its field) each candidate path spells
+  const int32_t* fld_out;   // [n_fields + 1] outputs (labels) of each field
   int n_fields;
   float* out_field;         // [n_fields][8]: label, mass, log_mass, margin, first_mass, n_labels, 0, 0
   float* out_probs;         // [n_labels_total]

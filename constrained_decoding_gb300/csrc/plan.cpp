@@ -29,6 +29,7 @@ int compile_fields(const pcd_field* fields, int n_fields, int vocab, HostPlan* p
   if (p->row_ch.empty()) p->row_ch.push_back(0);
   if (p->lab_off.empty()) p->lab_off.push_back(0);
   if (p->fld_lab.empty()) p->fld_lab.push_back(0);
+  if (p->fld_out.empty()) p->fld_out.push_back(0);
 
   for (int f = 0; f < n_fields; ++f) {
     const pcd_field& F = fields[f];
@@ -52,6 +53,32 @@ int compile_fields(const pcd_field* fields, int n_fields, int vocab, HostPlan* p
     if (!(F.temperature >= 0.f) || std::isinf(F.temperature)) {
       *msg = where + "temperature must be finite and >= 0";
       return PCD_ERR_INVALID_ARG;
+    }
+    // spellings: the label each candidate path spells
+    int n_out = F.n_cands;
+    if (F.cand_label) {
+      n_out = F.n_labels;
+      if (n_out < 2) {
+        *msg = where + "fewer than 2 labels";
+        return PCD_ERR_TOO_FEW_CANDIDATES;
+      }
+      if (n_out > F.n_cands) {
+        *msg = where + "more labels than candidate paths";
+        return PCD_ERR_INVALID_ARG;
+      }
+      std::vector<int> paths(n_out, 0);
+      for (int c = 0; c < F.n_cands; ++c) {
+        if (F.cand_label[c] < 0 || F.cand_label[c] >= n_out) {
+          *msg = where + "cand_label out of range";
+          return PCD_ERR_INVALID_ARG;
+        }
+        paths[F.cand_label[c]]++;
+      }
+      for (int l = 0; l < n_out; ++l)
+        if (!paths[l]) {
+          *msg = where + "label " + std::to_string(l) + " has no spelling";
+          return PCD_ERR_INVALID_ARG;
+        }
     }
     if (F.scoring != PCD_SCORE_SUM && F.scoring != PCD_SCORE_MEAN && F.scoring != PCD_SCORE_LEVEL) {
       *msg = where + "unknown scoring rule " + std::to_string(F.scoring);
@@ -172,6 +199,9 @@ int compile_fields(const pcd_field* fields, int n_fields, int vocab, HostPlan* p
     p->fld_lab.push_back(p->n_labels);
     p->temp.push_back(F.temperature > 0.f ? F.temperature : 1.f);
     p->scoring.push_back(F.scoring);
+    for (int c = 0; c < F.n_cands; ++c) p->cand_label.push_back(F.cand_label ? F.cand_label[c] : c);
+    p->n_out += n_out;
+    p->fld_out.push_back(p->n_out);
     p->n_fields++;
   }
   return PCD_OK;

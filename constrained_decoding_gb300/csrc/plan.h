@@ -28,12 +28,16 @@ struct HostPlan {
   std::vector<int32_t> row_ch;     // [R + 1] child entries of each readout row
   std::vector<int32_t> ch_tok;     // [n_children] candidate token id of each child entry
   std::vector<int32_t> child_row;  // [n_children] its readout row
-  std::vector<int32_t> lab_off;    // [n_labels + 1] path steps of each label
+  std::vector<int32_t> lab_off;    // [n_labels + 1] path steps of each candidate path
+                                   // (n_labels counts candidate paths, n_out the labels they spell)
   std::vector<int32_t> path;       // [n_path] child entry of each step
   std::vector<int32_t> fld_lab;    // [n_fields + 1] labels of each field
   std::vector<int32_t> fld_root;   // [n_fields] readout row of the field's scaffold end
   std::vector<float> temp;         // [n_fields]
   std::vector<int32_t> scoring;    // [n_fields] PCD_SCORE_* rule
+  int n_out = 0;                   // labels (outputs) of all fields
+  std::vector<int32_t> cand_label; // [n_labels] label (within its field) each candidate path spells
+  std::vector<int32_t> fld_out;    // [n_fields + 1] outputs of each field
   std::vector<int32_t> seg_off;    // [requests + 1] branch tokens of each request (empty: one request)
 };
 

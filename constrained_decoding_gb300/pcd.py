@@ -227,10 +227,19 @@ class _Fields:
             toks = _i32(np.concatenate(labels)) if labels else _i32([])
             offs = _i32(np.concatenate([[0], np.cumsum([len(l) for l in labels])]))
             self.keep += [sc, toks, offs]
+            label_of = getattr(f, "label_of", None)
+            if label_of is None:
+                lab_ptr, n_out = None, len(labels)
+            else:
+                lab = _i32(label_of)
+                if len(lab) != len(labels):
+                    raise ValueError("label_of needs one entry per token path")
+                self.keep.append(lab)
+                lab_ptr, n_out = _ptr_i32(lab), (int(lab.max()) + 1 if len(lab) else 0)
             self.arr[i] = D.pcd_field(_ptr_i32(sc), len(sc), _ptr_i32(toks), _ptr_i32(offs), len(labels),
                                       float(getattr(f, "temperature", 1.0) or 0.0),
-                                      scoring_code(getattr(f, "scoring", "sum")))
-            self.n_cands.append(len(labels))
+                                      scoring_code(getattr(f, "scoring", "sum")), lab_ptr, n_out)
+            self.n_cands.append(n_out)
 
 
 class _Results:
@@ -317,8 +326,15 @@ def pcd_score_plan_device(model: Model, cache: Cache, plan: Plan, result_device)
     _check(load().pcd_score_plan_device(model.handle, cache.handle, plan.handle, ptr), "pcd_score_plan_device")
 
 
+def n_outputs(fields: Sequence) -> List[int]:
+    """Labels of each field: its token paths, or the labels they spell."""
+    return [len(f.labels) if getattr(f, "label_of", None) is None else int(np.max(f.label_of)) + 1
+            for f in fields]
+
+
 def unpack_plan_result(blob: np.ndarray, n_cands: Sequence[int]) -> List[FieldResult]:
-    """Splits a plan's result blob (layout in include/pcd.h) into per-field results."""
+    """Splits a plan's result blob (layout in include/pcd.h) into per-field
+    results; n_cands[f] is field f's number of labels (``n_outputs``)."""
     nf = len(n_cands)
     nl = int(sum(n_cands))
     probs, lps = blob[nf * 8:nf * 8 + nl], blob[nf * 8 + nl:nf * 8 + 2 * nl]
@@ -351,22 +367,22 @@ def pcd_profile_read(model: Model) -> dict:
 
 
 PLAN_ARRAYS = ("tok", "rel", "anc_off", "anc_idx", "ro_tok", "row_ch", "ch_tok", "child_row", "lab_off", "path",
-               "fld_lab", "fld_root")
+               "fld_lab", "fld_root", "cand_label", "fld_out", "scoring")
 
 
 def pcd_plan_inspect(fields: Sequence, vocab: int) -> dict:
     """Host-only compile of `fields` (no GPU): the packed branch batch as numpy arrays."""
     lib = load()
     f = _Fields(fields)
-    sizes = np.zeros(7, np.int32)
+    sizes = np.zeros(8, np.int32)
     _check(lib.pcd_plan_inspect(ctypes.cast(f.arr, ctypes.c_void_p), len(fields), vocab, _ptr_i32(sizes), None),
            "pcd_plan_inspect")
-    T, R, C, NL, NP, NA, NF = (int(x) for x in sizes)
-    lens = [T, T, T + 1, NA, R, R + 1, C, C, NL + 1, NP, NF + 1, NF]
+    T, R, C, NL, NP, NA, NF, NO = (int(x) for x in sizes)
+    lens = [T, T, T + 1, NA, R, R + 1, C, C, NL + 1, NP, NF + 1, NF, NL, NF + 1, NF]
     bufs = [np.zeros(max(n, 1), np.int32) for n in lens]
-    ptrs = (ctypes.POINTER(ctypes.c_int32) * 12)(*[_ptr_i32(b) for b in bufs])
+    ptrs = (ctypes.POINTER(ctypes.c_int32) * len(bufs))(*[_ptr_i32(b) for b in bufs])
     _check(lib.pcd_plan_inspect(ctypes.cast(f.arr, ctypes.c_void_p), len(fields), vocab, _ptr_i32(sizes), ptrs),
            "pcd_plan_inspect")
     out = {k: b[:n] for k, b, n in zip(PLAN_ARRAYS, bufs, lens)}
-    out.update(T=T, R=R, C=C, NL=NL, NP=NP, NA=NA, NF=NF)
+    out.update(T=T, R=R, C=C, NL=NL, NP=NP, NA=NA, NF=NF, NO=NO)
     return out

@@ -99,7 +99,14 @@ typedef struct {
  *                    renormalised over the tokens the field allows there
  *                    (PCD: A Technical Reference, "Resolve shared prefixes
  *                    level by level").
- *    Any other value is PCD_ERR_INVALID_ARG. */
+ *    Any other value is PCD_ERR_INVALID_ARG.
+ *  cand_label / n_labels: NULL / ignored when every candidate path is its
+ *    own label.  Otherwise cand_label[c] in [0, n_labels) names the label
+ *    that path c spells, so one label may have several spellings ("Small
+ *    models quote their booleans", How TypeSafe's Jev Might Work: a bare and
+ *    a quoted value are one answer); every label needs at least one path,
+ *    2 <= n_labels <= n_cands.  Each path is scored by the rule above and a
+ *    label's score is the log-sum-exp of its paths' scores. */
 #define PCD_SCORE_SUM 0
 #define PCD_SCORE_MEAN 1
 #define PCD_SCORE_LEVEL 2
@@ -111,16 +118,19 @@ typedef struct {
   int n_cands;
   float temperature;
   int scoring;
+  const int32_t* cand_label;
+  int n_labels;
 } pcd_field;
 
-/* Per-field result.  probs / logprobs are caller-owned arrays of n_cands
- * floats (may be NULL to skip).  logprobs[c] = s_c, the label's score under
- * the field's scoring rule (PCD_SCORE_SUM: the sum of its full-vocabulary
+/* Per-field result.  probs / logprobs are caller-owned arrays of one float
+ * per label (n_cands, or n_labels with cand_label; may be NULL to skip).
+ * logprobs[c] = s_c, the label's score under the field's scoring rule (PCD_SCORE_SUM: the sum of its full-vocabulary
  * token log-probs); probs[c] = softmax(s / T)[c]; label = argmax (lowest
  * index on exact ties); margin = s_top1 - s_top2.  Whatever the rule,
- * mass = sum_c P(label c) with P the full-vocabulary product of the label's
- * token probabilities, log_mass = log(mass), and first_mass = probability
- * that the next token after the scaffold starts any allowed label. */
+ * mass = sum over the candidate paths of the full-vocabulary product of the
+ * path's token probabilities, log_mass = log(mass), and first_mass =
+ * probability that the next token after the scaffold starts any allowed
+ * path. */
 typedef struct {
   float* probs;
   float* logprobs;
@@ -208,7 +218,7 @@ int pcd_score_batch(pcd_model* m, const pcd_cache* const* caches, const pcd_fiel
 int pcd_plan_create(pcd_model* m, const pcd_field* fields, int n_fields, pcd_plan** out);
 void pcd_plan_free(pcd_plan* p);
 /* Floats of the device result blob of a plan: n_fields * 8 (label, mass,
- * log_mass, margin, first_mass, n_cands, 0, 0), then probs[total labels],
+ * log_mass, margin, first_mass, labels of the field, 0, 0), then probs[total labels],
  * then logprobs[total labels], labels in field order. */
 int pcd_plan_result_floats(const pcd_plan* p);
 /* Scores a compiled plan against a cache; results go to a device buffer of

@@ -88,16 +88,19 @@ int pcd_k_readout_noalloc(const void* h, int R, const void* w, int V, int d, con
  * (pcd.h) for a vocabulary of `vocab` tokens into the packed branch batch the
  * branch pass runs (How TypeSafe's Jev Might Work, "When one token is not
  * enough": scaffold tokens plus every internal node of the label trie).
- * sizes[0..6] receives T (branch tokens), R (readout rows), C (child
- * entries), NL (labels), NP (label path steps), NA (ancestor entries),
- * NF (fields).  When `arrays` is non-NULL, arrays[i] (caller-allocated,
- * sized from a first call with arrays == NULL) receives:
+ * sizes[0..7] receives T (branch tokens), R (readout rows), C (child
+ * entries), NL (candidate paths), NP (path steps), NA (ancestor entries),
+ * NF (fields), NO (labels the paths spell).  When `arrays` is non-NULL,
+ * arrays[i] (caller-allocated, sized from a first call with arrays == NULL;
+ * a NULL entry is skipped) receives:
  *  0 tok[T], 1 rel[T] (position after the prefix end), 2 anc_off[T+1],
  *  3 anc_idx[NA] (ancestors of each token, itself included, same field),
  *  4 ro_tok[R] (branch token read at each readout row), 5 row_ch[R+1],
  *  6 ch_tok[C] (candidate next token of each child entry), 7 child_row[C],
  *  8 lab_off[NL+1], 9 path[NP] (child entry of each step of each label),
- *  10 fld_lab[NF+1], 11 fld_root[NF] (readout row of each scaffold end).
+ *  10 fld_lab[NF+1], 11 fld_root[NF] (readout row of each scaffold end),
+ *  12 cand_label[NL] (label, within its field, each path spells),
+ *  13 fld_out[NF+1] (labels of each field), 14 scoring[NF] (PCD_SCORE_*).
  * Returns 0 or the PCD_ERR_* validation code pcd_score would return. */
 int pcd_plan_inspect(const void* fields, int n_fields, int vocab, int32_t* sizes, int32_t* const* arrays);
 

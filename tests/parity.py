@@ -65,9 +65,12 @@ def rescore(ref, field):
     """The oracle's result for `field` under its scoring rule, from an oracle
     result `ref` of the same labels (its token log-probs; the decoder does
     not run again)."""
-    from oracle import field_scores, scores_to_result
+    from oracle import combine_spellings, field_scores, scores_to_result
     rule = getattr(field, "scoring", "sum") or "sum"
-    out = scores_to_result(field_scores(rule, field.labels, ref.token_logprobs), field.temperature)
+    scores = field_scores(rule, field.labels, ref.token_logprobs)
+    if getattr(field, "label_of", None) is not None:
+        scores = combine_spellings(scores, field.label_of)
+    out = scores_to_result(scores, field.temperature)
     out.mass, out.log_mass, out.first_mass = ref.mass, ref.log_mass, ref.first_mass
     out.token_logprobs = ref.token_logprobs
     return out

@@ -1,8 +1,10 @@
-"""The alternative scoring rules on the CUDA path against the oracle: the
-length-normalised mean of a label's token log-probs and the per-level product
-of renormalised trie decisions, field by field and mixed within one call, on
-every execution path (two-pass, batched requests, single pass), with the
-deep, wide and one-level tries of the edge workloads."""
+"""The alternative scoring rules and spelling sets on the CUDA path against
+the oracle: the length-normalised mean of a label's token log-probs, the
+per-level product of renormalised trie decisions, and labels written several
+ways (bare, quoted, another capitalisation) whose paths add up; field by
+field and mixed within one call, on every execution path (two-pass, batched
+requests, single pass, device-resident plan), with the deep, wide and
+one-level tries of the edge workloads."""
 import numpy as np
 import pytest
 
@@ -76,3 +78,47 @@ def test_rule_does_not_change_the_mass(pcd, model, request1):
         got = pcd.pcd_score(model, cache, with_rule(request1.fields, rule))
         for a, b in zip(base, got):
             assert abs(a.log_mass - b.log_mass) < 1e-5 and abs(a.first_mass - b.first_mass) < 1e-6
+
+
+SPELLED = [("spelled", 2, 2), ("bool",), ("spelled", 3, 3), ("scaffold", 9), ("spelled", 4, 2), ("enum", 3, 1, 2)]
+
+
+@pytest.mark.parametrize("rule", ["sum", "mean", "level"])
+def test_spellings(pcd, model, tiny_oracle, rule):
+    req = make_custom(31, 512, 90, SPELLED)
+    fields = with_rule(req.fields, rule)
+    ref = _ref(tiny_oracle, req, fields)
+    cache = pcd.pcd_prefill(model, req.prefix)
+    got = pcd.pcd_score(model, cache, fields)
+    assert [len(g.probs) for g in got] == pcd.n_outputs(fields) == [2, 2, 3, 4, 3]
+    compare_request(got, ref, f"spellings, rule {rule}")
+    compare_request(pcd.pcd_prefill_score(model, req.prefix, fields), ref, f"spellings single pass, rule {rule}")
+
+
+def test_spellings_batch_and_device_plan(pcd, model, tiny_oracle):
+    import torch
+    reqs = [make_custom(50 + i, 512, 40 + 23 * i, SPELLED) for i in range(3)]
+    fields = [with_rule(r.fields, ["sum", "level", "mean"]) for r in reqs]
+    caches = [pcd.pcd_prefill(model, r.prefix) for r in reqs]
+    refs = [_ref(tiny_oracle, r, fs) for r, fs in zip(reqs, fields)]
+    for b, ref in zip(pcd.pcd_score_batch(model, caches, fields), refs):
+        compare_request(b, ref, "spellings batch")
+    plan = pcd.pcd_plan_create(model, fields[0])
+    assert plan.result_floats == 8 * len(fields[0]) + 2 * sum(pcd.n_outputs(fields[0]))
+    out = torch.zeros(plan.result_floats, dtype=torch.float32, device="cuda")
+    pcd.pcd_score_plan_device(model, caches[0], plan, out)
+    pcd.pcd_sync(model)
+    compare_request(pcd.unpack_plan_result(out.cpu().numpy(), pcd.n_outputs(fields[0])), refs[0],
+                    "spellings device plan")
+
+
+def test_one_spelling_per_label_is_unchanged(pcd, model, request1):
+    """An explicit identity label map gives bit-identical results."""
+    import dataclasses
+    cache = pcd.pcd_prefill(model, request1.prefix)
+    base = pcd.pcd_score(model, cache, request1.fields)
+    ident = [dataclasses.replace(f, label_of=np.arange(len(f.labels), dtype=np.int32)) for f in request1.fields]
+    for a, b in zip(base, pcd.pcd_score(model, cache, ident)):
+        np.testing.assert_array_equal(a.probs, b.probs)
+        np.testing.assert_array_equal(a.logprobs, b.logprobs)
+        assert a.label == b.label and a.mass == b.mass

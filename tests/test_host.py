@@ -142,6 +142,29 @@ def test_branch_compiler_validation(lib):
         pcd.pcd_plan_inspect([F(np.array([1]), [np.array([5]), np.array([6])], scoring="max")], 512)
 
 
+def test_branch_compiler_spellings(lib):
+    """Candidate paths that spell one label: the plan records each path's
+    label and each field's label count; bad label maps are rejected."""
+    import constrained_decoding_gb300.pcd as pcd
+    F = synth.Field
+    req = make_custom(5, 512, 10, [("spelled", 2, 2), ("bool",), ("spelled", 3, 3)])
+    plan = pcd.pcd_plan_inspect(req.fields, 512)
+    want = np.concatenate([req.fields[0].label_of, [0, 1], req.fields[2].label_of])
+    np.testing.assert_array_equal(plan["cand_label"], want)
+    np.testing.assert_array_equal(plan["fld_out"], [0, 2, 4, 7])
+    assert plan["NO"] == 7 and plan["NL"] == 4 + 2 + 9
+    np.testing.assert_array_equal(pcd.n_outputs(req.fields), [2, 2, 3])
+    paths = [np.array([5]), np.array([6]), np.array([7, 8])]
+    for code, label_of in ((-1, [0, 0, 2]),       # label 1 has no spelling
+                           (-1, [0, 3, 1]),       # out of range
+                           (-3, [0, 0, 0])):      # one label
+        with pytest.raises(pcd.PCDError) as ei:
+            pcd.pcd_plan_inspect([F(np.array([1]), paths, label_of=np.array(label_of))], 512)
+        assert ei.value.code == code, label_of
+    with pytest.raises(ValueError):
+        pcd.pcd_plan_inspect([F(np.array([1]), paths, label_of=np.array([0, 1]))], 512)
+
+
 def _replica_worker(rank, world, port, out):
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank), WORLD_SIZE=str(world),
                       LOCAL_RANK=str(rank))
