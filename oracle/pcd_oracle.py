@@ -430,3 +430,29 @@ class Oracle:
 
     def score(self, cache: KVCache, fields) -> List[FieldResult]:
         return [self.score_field(f, cache=cache) for f in fields]
+
+    def answer_line(self, field, res: FieldResult, sep) -> np.ndarray:
+        """The tokens that write a decided field into the prompt: its
+        scaffold, the first listed spelling of the winning label, then the
+        separator tokens (e.g. the closing quote, comma and newline)."""
+        label_of = getattr(field, "label_of", None)
+        if label_of is None:
+            path = field.labels[res.label]
+        else:
+            path = field.labels[int(np.flatnonzero(np.asarray(label_of) == res.label)[0])]
+        return np.concatenate([np.asarray(field.scaffold), np.asarray(path),
+                               np.asarray(sep, dtype=np.int64)]).astype(np.int64)
+
+    def score_first_field_first(self, cache: KVCache, fields, sep) -> List[FieldResult]:
+        """Decide the schema's first field on its own, write its answer into
+        the prompt, then decide every other field after that line ("The
+        first key of a JSON object is a special position", How TypeSafe's
+        Jev Might Work: asked as the first key of the object, later fields
+        sit where the model rarely is; a warm request then costs four
+        passes)."""
+        first = self.score_field(fields[0], cache=cache)
+        if len(fields) == 1:
+            return [first]
+        line = self.answer_line(fields[0], first, sep)
+        cache2 = self.extend(cache, line)
+        return [first] + [self.score_field(f, cache=cache2) for f in fields[1:]]

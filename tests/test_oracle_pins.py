@@ -490,6 +490,41 @@ def test_spelled_labels_by_brute_force(tiny_oracle64):
         assert lvl.mass == res.mass
 
 
+def test_first_field_first_by_brute_force(tiny_oracle64, request1):
+    """First field first: field 0 is scored right after the prefix; every
+    other label's probability is the product of its tokens' probabilities
+    written out from the logits of the complete sequence prefix || field 0's
+    scaffold || field 0's winning label || separator || scaffold || label."""
+    orc = tiny_oracle64
+    P = request1.prefix
+    sep = np.array([7, 11])
+    cache = orc.prefill(P)
+    res = orc.score_first_field_first(cache, request1.fields, sep)
+    plain = orc.score_field(request1.fields[0], cache=cache)
+    np.testing.assert_array_equal(res[0].scores, plain.scores)
+    f0 = request1.fields[0]
+    line = np.concatenate([f0.scaffold, f0.labels[plain.label], sep])
+    for f, r in zip(request1.fields[1:], res[1:]):
+        for c, lab in enumerate(f.labels):
+            seq = np.concatenate([P, line, f.scaffold, lab])
+            h, _ = orc.forward(seq, np.arange(len(seq)))
+            z = orc.logits(h)
+            prob = 1.0
+            for j, t in enumerate(lab):
+                row = z[len(P) + len(line) + len(f.scaffold) - 1 + j]
+                prob *= np.exp(row[t]) / np.exp(row).sum()
+            assert abs(np.log(prob) - r.scores[c]) < 1e-10
+    # the written spelling of a label with several is its first listed path
+    from synth.requests import make_custom
+    sp = make_custom(9, 512, 12, [("spelled", 3, 3)]).fields[0]
+    fake = scores_to_result([0.0, -1.0, -2.0])   # label 0 wins
+    for want in range(3):
+        fake.label = want
+        first_path = sp.labels[int(np.flatnonzero(sp.label_of == want)[0])]
+        np.testing.assert_array_equal(orc.answer_line(sp, fake, sep),
+                                      np.concatenate([sp.scaffold, first_path, sep]))
+
+
 def test_workload_shapes():
     """The generators give the branch sizes the workloads are described with."""
     r2 = synth.make_request(2)
