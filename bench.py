@@ -334,6 +334,30 @@ def run_ours(args):
     e2e_s = max_over_ranks(dist, time.perf_counter() - t_e2e0)
     barrier(dist)
 
+    # ---- first field first through the same host-pointer ABI: prefill the
+    # prefix, decide field 1, write its answer line, decide the other 27
+    sep = np.array([1, 2, 3], np.int32)        # the tokens closing a written value
+
+    def fff_step(i):
+        c = pcd.pcd_prefill(model, prefixes[i % n_pref])
+        res, st = pcd.pcd_score_first_field_first(model, c, fields, sep, with_stats=True)
+        c.free()
+        return st
+
+    for i in range(2):
+        fff_step(i)
+    torch.cuda.synchronize()
+    fff_ms = []
+    for i in range(K):
+        t0 = time.perf_counter()
+        fst = fff_step(i)
+        fff_ms.append((time.perf_counter() - t0) * 1e3)
+    fff_p50 = statistics.median(fff_ms)
+    first_field_first = {"value": round(1e3 * K / sum(fff_ms), 3), "unit": "req/s", "p50_latency_ms": round(fff_p50, 4),
+                         "forward_passes": 1 + fst["forward_passes"],
+                         "extra_latency_vs_e2e": round(fff_p50 / statistics.median(e2e_ms) - 1.0, 4),
+                         "note": "host-pointer ABI per request: prefill + field 1 + answer line + 27 fields"}
+
     # ---- roofline of the dominant kernel class
     T, R = st["branch_tokens"], st["readout_rows"]
     wm = work_model(cfg, len(req.prefix), T, R)
@@ -418,6 +442,7 @@ def run_ours(args):
                        "req_per_s": round(1e3 / other_ms, 3)},
         "e2e": {"value": round(n_total / e2e_s, 3), "unit": "req/s", "p50_latency_ms": round(statistics.median(e2e_ms), 4),
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)},
+        "first_field_first": first_field_first,
         "gpu_launches": int(round(launches_per_step * K)),
         "clocks": clocks,
     }

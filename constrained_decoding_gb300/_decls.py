@@ -50,6 +50,8 @@ SIGNATURES = [
     ("pcd_prefill_score", c_int, [c_void_p, P(c_int32), c_int, P(pcd_field), c_int, P(pcd_field_result),
                                   P(pcd_stats), P(c_void_p)]),
     ("pcd_prefill_score_plan_device", c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p, P(c_void_p)]),
+    ("pcd_score_first_field_first", c_int, [c_void_p, c_void_p, P(pcd_field), c_int, P(c_int32), c_int,
+                                            P(pcd_field_result), P(pcd_stats), P(c_void_p)]),
     ("pcd_sync", c_int, [c_void_p]),
     ("pcd_profile_enable", c_int, [c_void_p, c_int]),
     ("pcd_profile_read", c_int, [c_void_p, P(c_int), P(c_float)]),

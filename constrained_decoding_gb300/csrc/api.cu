@@ -1862,6 +1862,69 @@ int pcd_score_batch(pcd_model* m, const pcd_cache* const* caches, const pcd_fiel
   return score_impl(m, caches, fields, n_fields, n_requests, out, stats);
 }
 
+int pcd_score_first_field_first(pcd_model* m, const pcd_cache* cache, const pcd_field* fields, int n_fields,
+                                const int32_t* sep, int n_sep, pcd_field_result* out, pcd_stats* stats,
+                                pcd_cache** cache_out) {
+  if (cache_out) *cache_out = nullptr;
+  if (!m || !cache || !fields || !out || n_fields < 1) return fail(PCD_ERR_INVALID_ARG, "NULL argument or no fields");
+  if (n_sep < 0 || (n_sep > 0 && !sep)) return fail(PCD_ERR_INVALID_ARG, "bad separator");
+  for (int i = 0; i < n_sep; ++i)
+    if (sep[i] < 0 || sep[i] >= m->V) return fail(PCD_ERR_TOKEN_RANGE, "separator token out of range");
+  const auto t_start = std::chrono::steady_clock::now();
+  {
+    // validate every field before the first pass
+    pcd::HostPlan hp;
+    std::string msg;
+    const int rc = pcd::compile_fields(fields, n_fields, m->V, &hp, &msg);
+    if (rc != PCD_OK) return fail(rc, msg);
+  }
+  pcd_stats s1{}, s2{};
+  PCD_TRY(pcd_score(m, cache, fields, 1, out, stats ? &s1 : nullptr));
+  if (n_fields == 1) {
+    if (stats) {
+      *stats = s1;
+      stats->total_ms = std::chrono::duration<float, std::milli>(std::chrono::steady_clock::now() - t_start).count();
+    }
+    return PCD_OK;
+  }
+  // the answer line: scaffold, the winning label's first listed path, separator
+  const pcd_field& F = fields[0];
+  const int win = out[0].label;
+  int path = win;
+  if (F.cand_label)
+    for (path = 0; path < F.n_cands && F.cand_label[path] != win; ++path) {
+    }
+  if (win < 0 || path >= F.n_cands) return fail(PCD_ERR_CUDA, "first field: no decided label");
+  std::vector<int32_t> line(F.scaffold, F.scaffold + F.n_scaffold);
+  line.insert(line.end(), F.cand_tokens + F.cand_offsets[path], F.cand_tokens + F.cand_offsets[path + 1]);
+  line.insert(line.end(), sep, sep + n_sep);
+  const auto t_ext = std::chrono::steady_clock::now();
+  pcd_cache* ext = nullptr;
+  PCD_TRY(pcd_prefill_extend(m, cache, line.data(), static_cast<int>(line.size()), &ext));
+  int rc = pcd_sync(m);
+  const auto t_ext_end = std::chrono::steady_clock::now();
+  if (rc == PCD_OK) rc = pcd_score(m, ext, fields + 1, n_fields - 1, out + 1, stats ? &s2 : nullptr);
+  if (rc != PCD_OK || !cache_out)
+    pcd_cache_free(ext);
+  else
+    *cache_out = ext;
+  if (rc != PCD_OK) return rc;
+  if (stats) {
+    *stats = s1;
+    stats->prefill_ms = std::chrono::duration<float, std::milli>(t_ext_end - t_ext).count();
+    stats->compile_ms += s2.compile_ms;
+    stats->branch_ms += s2.branch_ms;
+    stats->readout_ms += s2.readout_ms;
+    stats->forward_passes = 3;
+    stats->branch_tokens += s2.branch_tokens;
+    stats->readout_rows += s2.readout_rows;
+    stats->h2d_bytes += s2.h2d_bytes + static_cast<int64_t>(line.size()) * 4;
+    stats->d2h_bytes += s2.d2h_bytes;
+    stats->total_ms = std::chrono::duration<float, std::milli>(std::chrono::steady_clock::now() - t_start).count();
+  }
+  return PCD_OK;
+}
+
 int pcd_plan_create(pcd_model* m, const pcd_field* fields, int n_fields, pcd_plan** out) {
   if (!m || !fields || !out || n_fields < 1) return fail(PCD_ERR_INVALID_ARG, "NULL argument or no fields");
   pcd::HostPlan hp;

@@ -303,6 +303,29 @@ def pcd_prefill_score(model: Model, ids, fields: Sequence, with_stats: bool = Fa
     return out[0] if len(out) == 1 else tuple(out)
 
 
+def pcd_score_first_field_first(model: Model, cache: Cache, fields: Sequence, sep=(), with_stats: bool = False,
+                                keep_cache: bool = False):
+    """Decide fields[0] alone, write its answer line (scaffold, winning
+    label's first spelling, ``sep`` tokens) into a copy of the prefix, then
+    decide the other fields after it.  Returns results (and stats, and the
+    extended prefix Cache when keep_cache)."""
+    f = _Fields(fields)
+    r = _Results(f.n_cands)
+    sp = _i32(sep)
+    st = D.pcd_stats()
+    ext = ctypes.c_void_p()
+    _check(load().pcd_score_first_field_first(model.handle, cache.handle, f.arr, len(fields),
+                                              _ptr_i32(sp) if len(sp) else None, len(sp), r.arr, ctypes.byref(st),
+                                              ctypes.byref(ext) if keep_cache else None),
+           "pcd_score_first_field_first")
+    out = [r.results()]
+    if with_stats:
+        out.append(_stats_dict(st))
+    if keep_cache:
+        out.append(Cache(model, ext.value) if ext.value else None)
+    return out[0] if len(out) == 1 else tuple(out)
+
+
 def pcd_prefill_score_plan_device(model: Model, ids_device, plan: Plan, result_device, keep_cache: bool = False):
     """Single-pass request from device-resident ids (CUDA int32 tensor) and a plan; only enqueues."""
     cache = ctypes.c_void_p()
