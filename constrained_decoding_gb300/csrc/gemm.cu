@@ -1051,6 +1051,36 @@ GemmTiling choose_tiling(int M, int N, int K, int epi, int sms) {
           best.bn = bn;
           best.splits = sp;
           best.cs = cs;
+          best.pair = false;
+        }
+      }
+    }
+  }
+  // CTA pairs: 256-row tiles on two SMs, each SM filling its 128 A rows and
+  // half of the B tile per k block (off unless PCD_GEMM_PAIR allows them)
+  static const bool allow_pair = [] {
+    const char* e = std::getenv("PCD_GEMM_PAIR");
+    return e && std::atoi(e) != 0;
+  }();
+  if (allow_pair) {
+    const int pgroups = ceil_div(M, 256);
+    for (int bn : {128, 256}) {
+      const int nt = ceil_div(N, bn);
+      const int max_split = (epi == EPI_F32_ATOMIC) ? std::max(1, std::min(16, nkb / 3)) : 1;
+      for (int sp = 1; sp <= max_split; ++sp) {
+        const int units = pgroups * nt * sp;
+        const int slots = std::max(1, sms / 2);
+        const int kbs = ceil_div(nkb, sp);
+        const double mma = 128.0 * bn * 128.0 / 8192.0;
+        const double fill = (128.0 + bn / 2) * 128.0 / 55.0;
+        const double fixed = (epi == EPI_F32_ATOMIC) ? 7000.0 : 2500.0;
+        const double tt = ceil_div(units, slots) * (kbs * std::max(mma, fill) + fixed) + (sp > 1 ? 400.0 : 0.0);
+        if (tt < best_t * 0.97) {
+          best_t = tt;
+          best.bn = bn;
+          best.splits = sp;
+          best.cs = 1;
+          best.pair = true;
         }
       }
     }
