@@ -52,6 +52,8 @@ SIGNATURES = [
     ("pcd_prefill_score_plan_device", c_int, [c_void_p, c_void_p, c_int, c_void_p, c_void_p, P(c_void_p)]),
     ("pcd_score_first_field_first", c_int, [c_void_p, c_void_p, P(pcd_field), c_int, P(c_int32), c_int,
                                             P(pcd_field_result), P(pcd_stats), P(c_void_p)]),
+    ("pcd_prefill_score_first_field_first", c_int, [c_void_p, P(c_int32), c_int, P(pcd_field), c_int, P(c_int32),
+                                                    c_int, P(pcd_field_result), P(pcd_stats), P(c_void_p)]),
     ("pcd_sync", c_int, [c_void_p]),
     ("pcd_profile_enable", c_int, [c_void_p, c_int]),
     ("pcd_profile_read", c_int, [c_void_p, P(c_int), P(c_float)]),
@@ -64,7 +66,7 @@ SIGNATURES = [
                               c_void_p, c_void_p, c_int64, c_void_p, c_void_p]),
     ("pcd_k_readout_noalloc", c_int, [c_void_p, c_int, c_void_p, c_int, c_int, P(c_int32), P(c_int32), c_int,
                                       c_void_p, c_void_p, c_void_p, c_void_p]),
-    ("pcd_plan_inspect", c_int, [c_void_p, c_int, c_int, P(c_int32), P(P(c_int32))]),
+    ("pcd_plan_inspect", c_int, [c_void_p, c_int, c_int, P(c_int32), P(P(c_int32)), P(c_int32), c_int]),
     ("pcd_k_gemm", c_int, [c_void_p, c_int, c_int, c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_int,
                            c_int, c_int, c_int, c_void_p, c_void_p]),
 ]

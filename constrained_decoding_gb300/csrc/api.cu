@@ -1607,8 +1607,12 @@ void unpack_results(const float* res, const PlanView& v, int f0, int l0, int n_f
   }
 }
 
+// ctx / n_ctx (may be NULL): per request, tokens written after its prefix
+// and before all its fields (first field first's answer line), run as branch
+// tokens in the same pass.
 int score_impl(pcd_model* m, const pcd_cache* const* caches, const pcd_field* const* fields, const int* n_fields,
-               int n_req, pcd_field_result* const* out, pcd_stats* stats) {
+               int n_req, pcd_field_result* const* out, pcd_stats* stats, const int32_t* const* ctx = nullptr,
+               const int* n_ctx = nullptr) {
   if (!m || !caches || !fields || !n_fields || !out || n_req < 1) return fail(PCD_ERR_INVALID_ARG, "NULL argument");
   const auto t_start = std::chrono::steady_clock::now();
   pcd::HostPlan hp;
@@ -1623,7 +1627,8 @@ int score_impl(pcd_model* m, const pcd_cache* const* caches, const pcd_field* co
     const int t0 = hp.T;
     const int rel0 = hp.max_rel;
     hp.max_rel = 0;
-    int rc = pcd::compile_fields(fields[r], n_fields[r], m->V, &hp, &msg);
+    int rc = pcd::compile_fields(fields[r], n_fields[r], m->V, &hp, &msg, ctx ? ctx[r] : nullptr,
+                                 n_ctx ? n_ctx[r] : 0);
     if (rc != PCD_OK) return fail(rc, "request " + std::to_string(r) + ", " + msg);
     PCD_TRY(check_positions(m, caches[r]->len, hp.max_rel));
     hp.max_rel = std::max(hp.max_rel, rel0);
@@ -1684,6 +1689,88 @@ int score_impl(pcd_model* m, const pcd_cache* const* caches, const pcd_field* co
 }
 
 }  // namespace
+
+// First field first: `decide` runs the pass that decides fields[0] (writing
+// out[0]) and names the prefix it ran against; the answer line (scaffold,
+// the winning label's first listed path, sep) is then either written after
+// a copy of that prefix by an extension pass (when the caller keeps the
+// extended prefix: three passes) or run as context tokens ahead of the other
+// fields in their branch pass (two passes; the same attention and positions).
+template <typename Decide>
+int first_field_first(pcd_model* m, const pcd_field* fields, int n_fields, const int32_t* sep, int n_sep,
+                      pcd_field_result* out, pcd_stats* stats, pcd_cache** cache_out, Decide&& decide) {
+  if (!m || !fields || !out || n_fields < 1) return fail(PCD_ERR_INVALID_ARG, "NULL argument or no fields");
+  if (n_sep < 0 || (n_sep > 0 && !sep)) return fail(PCD_ERR_INVALID_ARG, "bad separator");
+  for (int i = 0; i < n_sep; ++i)
+    if (sep[i] < 0 || sep[i] >= m->V) return fail(PCD_ERR_TOKEN_RANGE, "separator token out of range");
+  const auto t_start = std::chrono::steady_clock::now();
+  {
+    // validate every field before the first pass
+    pcd::HostPlan hp;
+    std::string msg;
+    const int rc = pcd::compile_fields(fields, n_fields, m->V, &hp, &msg);
+    if (rc != PCD_OK) return fail(rc, msg);
+  }
+  pcd_stats s1{}, s2{};
+  const pcd_cache* prefix = nullptr;
+  PCD_TRY(decide(&s1, &prefix));
+  const int passes1 = s1.forward_passes;
+  if (n_fields == 1) {
+    if (stats) {
+      *stats = s1;
+      stats->total_ms = std::chrono::duration<float, std::milli>(std::chrono::steady_clock::now() - t_start).count();
+    }
+    return PCD_OK;
+  }
+  // the answer line: scaffold, the winning label's first listed path, separator
+  const pcd_field& F = fields[0];
+  const int win = out[0].label;
+  int path = win;
+  if (F.cand_label)
+    for (path = 0; path < F.n_cands && F.cand_label[path] != win; ++path) {
+    }
+  if (win < 0 || path >= F.n_cands) return fail(PCD_ERR_CUDA, "first field: no decided label");
+  std::vector<int32_t> line(F.scaffold, F.scaffold + F.n_scaffold);
+  line.insert(line.end(), F.cand_tokens + F.cand_offsets[path], F.cand_tokens + F.cand_offsets[path + 1]);
+  line.insert(line.end(), sep, sep + n_sep);
+  const int n_line = static_cast<int>(line.size());
+  int passes = passes1 + 1;
+  float ext_ms = 0.f;
+  if (cache_out) {
+    const auto t_ext = std::chrono::steady_clock::now();
+    pcd_cache* ext = nullptr;
+    PCD_TRY(pcd_prefill_extend(m, prefix, line.data(), n_line, &ext));
+    int rc = pcd_sync(m);
+    ext_ms = std::chrono::duration<float, std::milli>(std::chrono::steady_clock::now() - t_ext).count();
+    if (rc == PCD_OK) rc = pcd_score(m, ext, fields + 1, n_fields - 1, out + 1, stats ? &s2 : nullptr);
+    if (rc != PCD_OK) {
+      pcd_cache_free(ext);
+      return rc;
+    }
+    *cache_out = ext;
+    passes += 1;
+  } else {
+    const pcd_field* fs[1] = {fields + 1};
+    const int nf[1] = {n_fields - 1};
+    pcd_field_result* os[1] = {out + 1};
+    const int32_t* cx[1] = {line.data()};
+    PCD_TRY(score_impl(m, &prefix, fs, nf, 1, os, stats ? &s2 : nullptr, cx, &n_line));
+  }
+  if (stats) {
+    *stats = s1;
+    stats->prefill_ms += ext_ms;
+    stats->compile_ms += s2.compile_ms;
+    stats->branch_ms += s2.branch_ms;
+    stats->readout_ms += s2.readout_ms;
+    stats->forward_passes = passes;
+    stats->branch_tokens += s2.branch_tokens;
+    stats->readout_rows += s2.readout_rows;
+    stats->h2d_bytes += s2.h2d_bytes + (cache_out ? static_cast<int64_t>(n_line) * 4 : 0);
+    stats->d2h_bytes += s2.d2h_bytes;
+    stats->total_ms = std::chrono::duration<float, std::milli>(std::chrono::steady_clock::now() - t_start).count();
+  }
+  return PCD_OK;
+}
 
 // ===================================================================== C ABI
 extern "C" {
@@ -1866,63 +1953,31 @@ int pcd_score_first_field_first(pcd_model* m, const pcd_cache* cache, const pcd_
                                 const int32_t* sep, int n_sep, pcd_field_result* out, pcd_stats* stats,
                                 pcd_cache** cache_out) {
   if (cache_out) *cache_out = nullptr;
-  if (!m || !cache || !fields || !out || n_fields < 1) return fail(PCD_ERR_INVALID_ARG, "NULL argument or no fields");
-  if (n_sep < 0 || (n_sep > 0 && !sep)) return fail(PCD_ERR_INVALID_ARG, "bad separator");
-  for (int i = 0; i < n_sep; ++i)
-    if (sep[i] < 0 || sep[i] >= m->V) return fail(PCD_ERR_TOKEN_RANGE, "separator token out of range");
-  const auto t_start = std::chrono::steady_clock::now();
-  {
-    // validate every field before the first pass
-    pcd::HostPlan hp;
-    std::string msg;
-    const int rc = pcd::compile_fields(fields, n_fields, m->V, &hp, &msg);
-    if (rc != PCD_OK) return fail(rc, msg);
-  }
-  pcd_stats s1{}, s2{};
-  PCD_TRY(pcd_score(m, cache, fields, 1, out, stats ? &s1 : nullptr));
-  if (n_fields == 1) {
-    if (stats) {
-      *stats = s1;
-      stats->total_ms = std::chrono::duration<float, std::milli>(std::chrono::steady_clock::now() - t_start).count();
-    }
-    return PCD_OK;
-  }
-  // the answer line: scaffold, the winning label's first listed path, separator
-  const pcd_field& F = fields[0];
-  const int win = out[0].label;
-  int path = win;
-  if (F.cand_label)
-    for (path = 0; path < F.n_cands && F.cand_label[path] != win; ++path) {
-    }
-  if (win < 0 || path >= F.n_cands) return fail(PCD_ERR_CUDA, "first field: no decided label");
-  std::vector<int32_t> line(F.scaffold, F.scaffold + F.n_scaffold);
-  line.insert(line.end(), F.cand_tokens + F.cand_offsets[path], F.cand_tokens + F.cand_offsets[path + 1]);
-  line.insert(line.end(), sep, sep + n_sep);
-  const auto t_ext = std::chrono::steady_clock::now();
-  pcd_cache* ext = nullptr;
-  PCD_TRY(pcd_prefill_extend(m, cache, line.data(), static_cast<int>(line.size()), &ext));
-  int rc = pcd_sync(m);
-  const auto t_ext_end = std::chrono::steady_clock::now();
-  if (rc == PCD_OK) rc = pcd_score(m, ext, fields + 1, n_fields - 1, out + 1, stats ? &s2 : nullptr);
-  if (rc != PCD_OK || !cache_out)
-    pcd_cache_free(ext);
-  else
-    *cache_out = ext;
-  if (rc != PCD_OK) return rc;
-  if (stats) {
-    *stats = s1;
-    stats->prefill_ms = std::chrono::duration<float, std::milli>(t_ext_end - t_ext).count();
-    stats->compile_ms += s2.compile_ms;
-    stats->branch_ms += s2.branch_ms;
-    stats->readout_ms += s2.readout_ms;
-    stats->forward_passes = 3;
-    stats->branch_tokens += s2.branch_tokens;
-    stats->readout_rows += s2.readout_rows;
-    stats->h2d_bytes += s2.h2d_bytes + static_cast<int64_t>(line.size()) * 4;
-    stats->d2h_bytes += s2.d2h_bytes;
-    stats->total_ms = std::chrono::duration<float, std::milli>(std::chrono::steady_clock::now() - t_start).count();
-  }
-  return PCD_OK;
+  if (!cache) return fail(PCD_ERR_INVALID_ARG, "NULL cache");
+  return first_field_first(
+      m, fields, n_fields, sep, n_sep, out, stats, cache_out,
+      [&](pcd_stats* s1, const pcd_cache** c) {
+        *c = cache;
+        return pcd_score(m, cache, fields, 1, out, s1);
+      });
+}
+
+int pcd_prefill_score_first_field_first(pcd_model* m, const int32_t* ids, int n, const pcd_field* fields,
+                                        int n_fields, const int32_t* sep, int n_sep, pcd_field_result* out,
+                                        pcd_stats* stats, pcd_cache** cache_out) {
+  if (cache_out) *cache_out = nullptr;
+  pcd_cache* prefix = nullptr;
+  const int rc = first_field_first(
+      m, fields, n_fields, sep, n_sep, out, stats, nullptr, [&](pcd_stats* s1, const pcd_cache** c) {
+        const int r = pcd_prefill_score(m, ids, n, fields, 1, out, s1, &prefix);
+        *c = prefix;
+        return r;
+      });
+  if (rc == PCD_OK && cache_out)
+    *cache_out = prefix;
+  else if (prefix)
+    pcd_cache_free(prefix);
+  return rc;
 }
 
 int pcd_plan_create(pcd_model* m, const pcd_field* fields, int n_fields, pcd_plan** out) {

@@ -188,11 +188,12 @@ extern "C" int pcd_k_readout_noalloc(const void* h, int R, const void* w, int V,
                       static_cast<int64_t>(PCD_K_READOUT_NOALLOC_MAX_BYTES), dev_err, static_cast<cudaStream_t>(stream));
 }
 
-extern "C" int pcd_plan_inspect(const void* fields, int n_fields, int vocab, int32_t* sizes, int32_t* const* arrays) {
+extern "C" int pcd_plan_inspect(const void* fields, int n_fields, int vocab, int32_t* sizes, int32_t* const* arrays,
+                                const int32_t* ctx, int n_ctx) {
   if (!sizes || vocab < 1) return PCD_ERR_INVALID_ARG;
   pcd::HostPlan p;
   std::string msg;
-  const int rc = pcd::compile_fields(static_cast<const pcd_field*>(fields), n_fields, vocab, &p, &msg);
+  const int rc = pcd::compile_fields(static_cast<const pcd_field*>(fields), n_fields, vocab, &p, &msg, ctx, n_ctx);
   if (rc != PCD_OK) return rc;
   sizes[0] = p.T;
   sizes[1] = p.R;

@@ -20,16 +20,37 @@ struct Node {
 };
 }  // namespace
 
-int compile_fields(const pcd_field* fields, int n_fields, int vocab, HostPlan* p, std::string* msg) {
+int compile_fields(const pcd_field* fields, int n_fields, int vocab, HostPlan* p, std::string* msg,
+                   const int32_t* ctx, int n_ctx) {
   if (n_fields < 0 || (n_fields > 0 && !fields)) {
     *msg = "fields is NULL or n_fields < 0";
     return PCD_ERR_INVALID_ARG;
   }
+  if (n_ctx < 0 || (n_ctx > 0 && !ctx)) {
+    *msg = "context tokens NULL or n_ctx < 0";
+    return PCD_ERR_INVALID_ARG;
+  }
+  for (int k = 0; k < n_ctx; ++k)
+    if (ctx[k] < 0 || ctx[k] >= vocab) {
+      *msg = "context token out of range";
+      return PCD_ERR_TOKEN_RANGE;
+    }
   if (p->anc_off.empty()) p->anc_off.push_back(0);
   if (p->row_ch.empty()) p->row_ch.push_back(0);
   if (p->lab_off.empty()) p->lab_off.push_back(0);
   if (p->fld_lab.empty()) p->fld_lab.push_back(0);
   if (p->fld_out.empty()) p->fld_out.push_back(0);
+
+  // ---- context tokens: a chain right after the prefix, ancestors of every field
+  const int c0 = p->T;
+  for (int k = 0; k < n_ctx; ++k) {
+    p->tok.push_back(ctx[k]);
+    p->rel.push_back(k);
+    for (int a = 0; a <= k; ++a) p->anc_idx.push_back(c0 + a);
+    p->anc_off.push_back(static_cast<int32_t>(p->anc_idx.size()));
+    p->T++;
+  }
+  if (n_ctx - 1 > p->max_rel) p->max_rel = n_ctx - 1;
 
   for (int f = 0; f < n_fields; ++f) {
     const pcd_field& F = fields[f];
@@ -143,7 +164,8 @@ int compile_fields(const pcd_field* fields, int n_fields, int vocab, HostPlan* p
     const int t0 = p->T;
     for (int k = 0; k < S; ++k) {
       p->tok.push_back(F.scaffold[k]);
-      p->rel.push_back(k);
+      p->rel.push_back(n_ctx + k);
+      for (int a = 0; a < n_ctx; ++a) p->anc_idx.push_back(c0 + a);
       for (int a = 0; a <= k; ++a) p->anc_idx.push_back(t0 + a);
       p->anc_off.push_back(static_cast<int32_t>(p->anc_idx.size()));
       p->T++;
@@ -157,9 +179,10 @@ int compile_fields(const pcd_field* fields, int n_fields, int vocab, HostPlan* p
       Node& n = nodes[id];
       n.branch = p->T;
       p->tok.push_back(n.token);
-      const int rel = S + n.depth - 1;
+      const int rel = n_ctx + S + n.depth - 1;
       p->rel.push_back(rel);
       if (rel > p->max_rel) p->max_rel = rel;
+      for (int a = 0; a < n_ctx; ++a) p->anc_idx.push_back(c0 + a);
       for (int a = 0; a < S; ++a) p->anc_idx.push_back(t0 + a);
       std::vector<int> chain;
       for (int x = id; x != 0; x = nodes[x].parent) chain.push_back(nodes[x].branch);
@@ -167,7 +190,7 @@ int compile_fields(const pcd_field* fields, int n_fields, int vocab, HostPlan* p
       p->anc_off.push_back(static_cast<int32_t>(p->anc_idx.size()));
       p->T++;
     }
-    if (S - 1 > p->max_rel) p->max_rel = S - 1;
+    if (n_ctx + S - 1 > p->max_rel) p->max_rel = n_ctx + S - 1;
 
     // ---- readout rows and their child entries
     std::map<std::pair<int, int>, int> entry_of;  // (node, child token) -> child entry

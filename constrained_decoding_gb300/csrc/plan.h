@@ -20,8 +20,9 @@ struct HostPlan {
   int n_fields = 0, T = 0, R = 0, n_children = 0, n_labels = 0, n_path = 0;
   int max_rel = 0;                 // largest relative position
   std::vector<int32_t> tok;        // [T] token id of each branch token
-  std::vector<int32_t> rel;        // [T] position after the prefix end: k for scaffold token k,
-                                   //     S + depth - 1 for a trie node at depth >= 1
+  std::vector<int32_t> rel;        // [T] position after the prefix end: C + k for scaffold token k,
+                                   //     C + S + depth - 1 for a trie node at depth >= 1, with C
+                                   //     context tokens before the fields (k for context token k)
   std::vector<int32_t> anc_off;    // [T + 1] ancestors of each token (same field, itself included)
   std::vector<int32_t> anc_idx;
   std::vector<int32_t> ro_tok;     // [R] branch token whose output is read
@@ -41,8 +42,13 @@ struct HostPlan {
   std::vector<int32_t> seg_off;    // [requests + 1] branch tokens of each request (empty: one request)
 };
 
-// Appends `fields` to `p` (so several requests can share one batch).  On
-// error returns a PCD_ERR_* code and sets *msg; `p` is then unspecified.
-int compile_fields(const pcd_field* fields, int n_fields, int vocab, HostPlan* p, std::string* msg);
+// Appends `fields` to `p` (so several requests can share one batch).  With
+// n_ctx > 0 the context tokens ctx[0..n_ctx) come first: branch tokens right
+// after the prefix (each an ancestor of the ones after it, no readout), and
+// every field's scaffold follows them (an answer line written before the
+// fields: first field first).  On error returns a PCD_ERR_* code and sets
+// *msg; `p` is then unspecified.
+int compile_fields(const pcd_field* fields, int n_fields, int vocab, HostPlan* p, std::string* msg,
+                   const int32_t* ctx = nullptr, int n_ctx = 0);
 
 }  // namespace pcd

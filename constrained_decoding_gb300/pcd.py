@@ -305,10 +305,10 @@ def pcd_prefill_score(model: Model, ids, fields: Sequence, with_stats: bool = Fa
 
 def pcd_score_first_field_first(model: Model, cache: Cache, fields: Sequence, sep=(), with_stats: bool = False,
                                 keep_cache: bool = False):
-    """Decide fields[0] alone, write its answer line (scaffold, winning
-    label's first spelling, ``sep`` tokens) into a copy of the prefix, then
-    decide the other fields after it.  Returns results (and stats, and the
-    extended prefix Cache when keep_cache)."""
+    """Decide fields[0] alone, then the other fields after its answer line
+    (scaffold, winning label's first spelling, ``sep`` tokens).  With
+    keep_cache the line is first written after a copy of the prefix and that
+    extended prefix Cache is returned too.  Returns results (and stats)."""
     f = _Fields(fields)
     r = _Results(f.n_cands)
     sp = _i32(sep)
@@ -323,6 +323,29 @@ def pcd_score_first_field_first(model: Model, cache: Cache, fields: Sequence, se
         out.append(_stats_dict(st))
     if keep_cache:
         out.append(Cache(model, ext.value) if ext.value else None)
+    return out[0] if len(out) == 1 else tuple(out)
+
+
+def pcd_prefill_score_first_field_first(model: Model, ids, fields: Sequence, sep=(), with_stats: bool = False,
+                                        keep_cache: bool = False):
+    """First field first from the prefix ids in two passes (prefix with
+    fields[0]; answer line with the other fields).  Returns results (and
+    stats, and the prefix Cache when keep_cache)."""
+    ids = _i32(ids)
+    f = _Fields(fields)
+    r = _Results(f.n_cands)
+    sp = _i32(sep)
+    st = D.pcd_stats()
+    cache = ctypes.c_void_p()
+    _check(load().pcd_prefill_score_first_field_first(model.handle, _ptr_i32(ids), len(ids), f.arr, len(fields),
+                                                      _ptr_i32(sp) if len(sp) else None, len(sp), r.arr,
+                                                      ctypes.byref(st), ctypes.byref(cache) if keep_cache else None),
+           "pcd_prefill_score_first_field_first")
+    out = [r.results()]
+    if with_stats:
+        out.append(_stats_dict(st))
+    if keep_cache:
+        out.append(Cache(model, cache.value) if cache.value else None)
     return out[0] if len(out) == 1 else tuple(out)
 
 
@@ -393,19 +416,22 @@ PLAN_ARRAYS = ("tok", "rel", "anc_off", "anc_idx", "ro_tok", "row_ch", "ch_tok",
                "fld_lab", "fld_root", "cand_label", "fld_out", "scoring")
 
 
-def pcd_plan_inspect(fields: Sequence, vocab: int) -> dict:
-    """Host-only compile of `fields` (no GPU): the packed branch batch as numpy arrays."""
+def pcd_plan_inspect(fields: Sequence, vocab: int, ctx=()) -> dict:
+    """Host-only compile of `fields` (no GPU), after the context tokens `ctx`
+    if any: the packed branch batch as numpy arrays."""
     lib = load()
     f = _Fields(fields)
+    cx = _i32(ctx)
+    cxp = _ptr_i32(cx) if len(cx) else None
     sizes = np.zeros(8, np.int32)
-    _check(lib.pcd_plan_inspect(ctypes.cast(f.arr, ctypes.c_void_p), len(fields), vocab, _ptr_i32(sizes), None),
-           "pcd_plan_inspect")
+    _check(lib.pcd_plan_inspect(ctypes.cast(f.arr, ctypes.c_void_p), len(fields), vocab, _ptr_i32(sizes), None,
+                                cxp, len(cx)), "pcd_plan_inspect")
     T, R, C, NL, NP, NA, NF, NO = (int(x) for x in sizes)
     lens = [T, T, T + 1, NA, R, R + 1, C, C, NL + 1, NP, NF + 1, NF, NL, NF + 1, NF]
     bufs = [np.zeros(max(n, 1), np.int32) for n in lens]
     ptrs = (ctypes.POINTER(ctypes.c_int32) * len(bufs))(*[_ptr_i32(b) for b in bufs])
-    _check(lib.pcd_plan_inspect(ctypes.cast(f.arr, ctypes.c_void_p), len(fields), vocab, _ptr_i32(sizes), ptrs),
-           "pcd_plan_inspect")
+    _check(lib.pcd_plan_inspect(ctypes.cast(f.arr, ctypes.c_void_p), len(fields), vocab, _ptr_i32(sizes), ptrs,
+                                cxp, len(cx)), "pcd_plan_inspect")
     out = {k: b[:n] for k, b, n in zip(PLAN_ARRAYS, bufs, lens)}
     out.update(T=T, R=R, C=C, NL=NL, NP=NP, NA=NA, NF=NF, NO=NO)
     return out

@@ -242,23 +242,34 @@ int pcd_prefill_score_plan_device(pcd_model* m, const int32_t* ids_device, int n
 /* First field first (How TypeSafe's Jev Might Work, "The first key of a JSON
  * object is a special position": every row of the batched pass otherwise
  * asks its field as if it were the object's first key).  Scores fields[0]
- * alone against `cache`; writes its answer line -- fields[0].scaffold, the
- * first listed path of its winning label, then sep[0..n_sep) (the tokens
- * that close the value, e.g. quote, comma, newline) -- after a copy of the
- * prefix with one extension pass; then scores fields[1..n_fields) after
- * that line in one batched branch pass.  out[f] is written for every field.
- * `cache` is not modified; cache_out (may be NULL) receives the extended
- * prefix, owned by the caller (NULL is stored with a single field, where no
- * line is written).  stats (may be NULL) adds up the passes of this call:
- * forward_passes = 3 (1 with a single field), branch_tokens and
- * readout_rows summed, prefill_ms the extension pass, total_ms the call.
- * All fields are validated before the first pass.  Synchronises the model
- * stream between passes (the line depends on the first decision).
- * Errors: as pcd_score and pcd_prefill_extend; sep tokens out of range are
- * PCD_ERR_TOKEN_RANGE, n_sep < 0 or sep NULL with n_sep > 0 INVALID_ARG. */
+ * alone against `cache`; its answer line -- fields[0].scaffold, the first
+ * listed path of its winning label, then sep[0..n_sep) (the tokens that
+ * close the value, e.g. quote, comma, newline) -- then stands between the
+ * prefix and every other field, and fields[1..n_fields) are scored after it
+ * in one batched branch pass.  out[f] is written for every field.
+ * With cache_out == NULL the line runs as branch tokens ahead of the other
+ * fields inside that pass (two passes in all).  With cache_out the line is
+ * written after a copy of the prefix by an extension pass first (three
+ * passes) and *cache_out receives that extended prefix, owned by the caller
+ * (NULL is stored with a single field, where no line is written).  `cache`
+ * is not modified.  stats (may be NULL) adds up the passes of this call:
+ * forward_passes counted, branch_tokens and readout_rows summed, prefill_ms
+ * the extension pass, total_ms the call.  All fields are validated before
+ * the first pass.  Synchronises the model stream after the first decision
+ * (the line depends on it).  Errors: as pcd_score and pcd_prefill_extend;
+ * sep tokens out of range are PCD_ERR_TOKEN_RANGE, n_sep < 0 or sep NULL
+ * with n_sep > 0 INVALID_ARG. */
 int pcd_score_first_field_first(pcd_model* m, const pcd_cache* cache, const pcd_field* fields, int n_fields,
                                 const int32_t* sep, int n_sep, pcd_field_result* out, pcd_stats* stats,
                                 pcd_cache** cache_out);
+/* The same from the prefix ids: one pass runs the prefix with fields[0]'s
+ * rows (as pcd_prefill_score), the second runs the answer line and the
+ * other fields as branch tokens on that prefix -- the four sequential passes
+ * of a warm request (prefill, first field, line, the rest) in two.
+ * cache_out (may be NULL) receives the prefix's cache (without the line). */
+int pcd_prefill_score_first_field_first(pcd_model* m, const int32_t* ids, int n, const pcd_field* fields,
+                                        int n_fields, const int32_t* sep, int n_sep, pcd_field_result* out,
+                                        pcd_stats* stats, pcd_cache** cache_out);
 
 /* Waits for the model stream; reports a device-side failure recorded since
  * the last pcd_sync (PCD_ERR_DEVICE_TIMEOUT, PCD_ERR_TOKEN_RANGE). */

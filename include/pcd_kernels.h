@@ -101,8 +101,11 @@ int pcd_k_readout_noalloc(const void* h, int R, const void* w, int V, int d, con
  *  10 fld_lab[NF+1], 11 fld_root[NF] (readout row of each scaffold end),
  *  12 cand_label[NL] (label, within its field, each path spells),
  *  13 fld_out[NF+1] (labels of each field), 14 scoring[NF] (PCD_SCORE_*).
- * Returns 0 or the PCD_ERR_* validation code pcd_score would return. */
-int pcd_plan_inspect(const void* fields, int n_fields, int vocab, int32_t* sizes, int32_t* const* arrays);
+ * ctx[0..n_ctx) (NULL / 0 for none): context tokens written before every
+ * field (first field first's answer line), compiled as the first branch
+ * tokens.  Returns 0 or the PCD_ERR_* validation code pcd_score would return. */
+int pcd_plan_inspect(const void* fields, int n_fields, int vocab, int32_t* sizes, int32_t* const* arrays,
+                     const int32_t* ctx, int n_ctx);
 
 #ifdef __cplusplus
 }

@@ -34,12 +34,23 @@ def model(pcd, tiny_weights):
 def test_tiny(pcd, model, tiny_oracle, request1):
     cache = pcd.pcd_prefill(model, request1.prefix)
     before = pcd.pcd_score(model, cache, request1.fields)
-    got, st, ext = pcd.pcd_score_first_field_first(model, cache, request1.fields, SEP, with_stats=True,
-                                                   keep_cache=True)
     oc = tiny_oracle.prefill(request1.prefix)
     ref = tiny_oracle.score_first_field_first(oc, request1.fields, SEP)
+    # the answer line as branch tokens ahead of the other fields: two passes
+    two, st2 = pcd.pcd_score_first_field_first(model, cache, request1.fields, SEP, with_stats=True)
+    compare_request(two, ref, "first field first, line in the branch pass")
+    assert st2["forward_passes"] == 2
+    # from the ids: prefix with field 1, then line and the rest
+    pf, st3 = pcd.pcd_prefill_score_first_field_first(model, request1.prefix, request1.fields, SEP, with_stats=True)
+    compare_request(pf, ref, "first field first from the ids")
+    assert st3["forward_passes"] == 2
+    # the line written into an extended prefix first: three passes
+    got, st, ext = pcd.pcd_score_first_field_first(model, cache, request1.fields, SEP, with_stats=True,
+                                                   keep_cache=True)
     compare_request(got, ref, "first field first")
     assert st["forward_passes"] == 3
+    for a, b in zip(got, two):
+        np.testing.assert_allclose(a.logprobs, b.logprobs, atol=2e-3)
     line = tiny_oracle.answer_line(request1.fields[0], ref[0], SEP)
     assert ext.length == len(request1.prefix) + len(line)
     # the extended prefix is the prefix followed by the line: scoring the
@@ -56,12 +67,16 @@ def test_tiny(pcd, model, tiny_oracle, request1):
 def test_spellings_and_rules(pcd, model, tiny_oracle, rules):
     req = make_custom(61, 512, 70, [("spelled", 3, 3), ("bool",), ("shared", 4, 2, 3), ("spelled", 2, 2)])
     fields = with_rule(req.fields, rules)
-    got = pcd.pcd_score_first_field_first(model, pcd.pcd_prefill(model, req.prefix), fields, SEP)
+    cache = pcd.pcd_prefill(model, req.prefix)
     oc = tiny_oracle.prefill(req.prefix)
     ref = tiny_oracle.score_first_field_first(oc, fields, SEP)
     # the written line follows field 1's decision, so the comparison of the
     # later fields covers it too
-    compare_request(got, ref, f"first field first {rules}")
+    compare_request(pcd.pcd_score_first_field_first(model, cache, fields, SEP), ref, f"first field first {rules}")
+    compare_request(pcd.pcd_score_first_field_first(model, cache, fields, SEP, keep_cache=True)[0], ref,
+                    f"first field first {rules}, extended prefix")
+    compare_request(pcd.pcd_prefill_score_first_field_first(model, req.prefix, fields, SEP), ref,
+                    f"first field first {rules}, from the ids")
 
 
 def test_single_field_and_errors(pcd, model, request1):
@@ -91,11 +106,17 @@ def test_config2_triage(pcd):
         sep = np.array([1, 2], np.int32)
         cache = pcd.pcd_prefill(model, req.prefix)
         got, st = pcd.pcd_score_first_field_first(model, cache, req.fields, sep, with_stats=True)
-        assert st["forward_passes"] == 3
+        assert st["forward_passes"] == 2
+        pf, st2 = pcd.pcd_prefill_score_first_field_first(model, req.prefix, req.fields, sep, with_stats=True)
+        assert st2["forward_passes"] == 2
+        ext = pcd.pcd_score_first_field_first(model, cache, req.fields, sep, keep_cache=True)[0]
         orc = Oracle(w, np.float32)
         t = time.time()
         ref = orc.score_first_field_first(orc.prefill(req.prefix), req.fields, sep)
         print(f"oracle: {time.time() - t:.1f} s")
         print("config 2 first field first worst errors", compare_request(got, ref, "config 2 first field first"))
+        print("config 2 first field first from the ids",
+              compare_request(pf, ref, "config 2 first field first from the ids"))
+        compare_request(ext, ref, "config 2 first field first, extended prefix")
     finally:
         model.free()

@@ -142,6 +142,37 @@ def test_branch_compiler_validation(lib):
         pcd.pcd_plan_inspect([F(np.array([1]), [np.array([5]), np.array([6])], scoring="max")], 512)
 
 
+def test_branch_compiler_context_tokens(lib):
+    """Context tokens (an answer line written before the fields) come first,
+    chained; every field token has them as its first ancestors and its
+    position moves past them; nothing else changes."""
+    import constrained_decoding_gb300.pcd as pcd
+    req = make_custom(6, 512, 10, [("bool",), ("shared", 3, 2, 3), ("spelled", 2, 2)])
+    ctx = np.array([9, 8, 7, 6], np.int32)
+    base = pcd.pcd_plan_inspect(req.fields, 512)
+    plan = pcd.pcd_plan_inspect(req.fields, 512, ctx)
+    C = len(ctx)
+    assert plan["T"] == base["T"] + C and plan["NP"] == base["NP"] and plan["R"] == base["R"]
+    np.testing.assert_array_equal(plan["tok"][:C], ctx)
+    np.testing.assert_array_equal(plan["tok"][C:], base["tok"])
+    np.testing.assert_array_equal(plan["rel"][:C], np.arange(C))
+    np.testing.assert_array_equal(plan["rel"][C:], base["rel"] + C)
+    for t in range(plan["T"]):
+        anc = plan["anc_idx"][plan["anc_off"][t]:plan["anc_off"][t + 1]]
+        if t < C:
+            np.testing.assert_array_equal(anc, np.arange(t + 1))
+        else:
+            b = t - C
+            np.testing.assert_array_equal(anc, np.concatenate(
+                [np.arange(C), base["anc_idx"][base["anc_off"][b]:base["anc_off"][b + 1]] + C]))
+    np.testing.assert_array_equal(plan["ro_tok"], base["ro_tok"] + C)
+    for k in ("row_ch", "ch_tok", "child_row", "lab_off", "path", "fld_lab", "fld_root", "cand_label", "fld_out"):
+        np.testing.assert_array_equal(plan[k], base[k])
+    with pytest.raises(pcd.PCDError) as ei:
+        pcd.pcd_plan_inspect(req.fields, 512, [3, 512])
+    assert ei.value.code == -7
+
+
 def test_branch_compiler_spellings(lib):
     """Candidate paths that spell one label: the plan records each path's
     label and each field's label count; bad label maps are rejected."""
