@@ -38,6 +38,8 @@ struct GemmParams {
   int b_evict_first;  // B is read by one M group only: stream it past L2
   int lo_row0;        // ALO: tiles entirely below this row have no low half
   int b_const;        // B tiles may load before the programmatic dependency wait
+  int n_wide;         // units of the full N tile width; units past it are 64-column slices of
+  int nw_col0;        //   the last N tiles, from column nw_col0 (the last wave's tail, split finer)
 };
 
 template <int MT, int BN, bool ALO = false>
@@ -233,8 +235,13 @@ __device__ __forceinline__ void epi_qkv_rope(const GemmParams& p, const EpiArgs&
 template <int MT, int BN, int EPI, int CS, bool ALO>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmA2, const GemmParams p, const EpiArgs e) {
+                   const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
+                   const GemmParams p, const EpiArgs e) {
   using C = GemmCfg<MT, BN, ALO>;
+  // narrow tail units (tmB2: 64-row B boxes) exist only for single-tile CTAs
+  // with an elementwise epilogue
+  constexpr int NW = 64;
+  constexpr bool kTail = MT == 1 && CS == 1 && EPI == EPI_SWIGLU && BN > NW;
   static_assert(CS == 1 || MT == 1, "clusters share B across single-tile CTAs");
   constexpr uint16_t MASK = static_cast<uint16_t>((1u << CS) - 1u);
   constexpr int B_SLICE = BN / CS;  // B rows each CTA of a cluster loads and multicasts
@@ -289,23 +296,38 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after_sync();
   const uint32_t tbase = *tmem_slot;
 
+  // unit u: its N tile (full width) or -1, M group, K split, first column and width
+  auto unit = [&](int u, int& nt, int& mg, int& ks, int& col0, int& width) {
+    if (!kTail || u < p.n_wide) {
+      decode_unit(p, u, nt, mg, ks);
+      col0 = nt * BN;
+      width = BN;
+    } else {
+      const int v = u - p.n_wide;
+      mg = v % p.n_mgroups;
+      ks = 0;
+      nt = -1;
+      col0 = p.nw_col0 + (v / p.n_mgroups) * NW;
+      width = NW;
+    }
+  };
   auto tile0 = [&](int mg) { return mg * MT * CS + rank * MT; };  // this CTA's first M tile of group mg
   auto valid_tiles = [&](int mg) { return max(0, min(MT, mtiles - tile0(mg))); };
   // bytes one stage of unit (mg) receives: its A tiles (and lo halves), then B
-  auto stage_bytes = [&](int mg) {
+  auto stage_bytes = [&](int mg, int width) {
     const int mt_valid = valid_tiles(mg);
     int lo_tiles = 0;
     if constexpr (ALO)
       for (int mt = 0; mt < mt_valid; ++mt) lo_tiles += ((tile0(mg) + mt + 1) * 128 > p.lo_row0) ? 1 : 0;
-    return static_cast<uint32_t>((mt_valid + lo_tiles) * C::A_BYTES + C::B_BYTES);
+    return static_cast<uint32_t>((mt_valid + lo_tiles) * C::A_BYTES + width * 128);
   };
   const uint64_t pol_b = p.b_evict_first ? l2_policy_evict_first() : l2_policy_evict_last();
-  auto load_b = [&](int stage, int kb, int nt) {
+  auto load_b = [&](int stage, int kb, int col0, int width) {
     uint8_t* bdst = smem + stage * C::STAGE_BYTES + C::A_PARTS * MT * C::A_BYTES;
     if constexpr (CS == 1) {
-      tma_load_2d_hint(bdst, &tmB, &full[stage], kb * 64, nt * BN, pol_b);
+      tma_load_2d_hint(bdst, (kTail && width != BN) ? &tmB2 : &tmB, &full[stage], kb * 64, col0, pol_b);
     } else {
-      tma_load_2d_mc(bdst + rank * B_SLICE * 128, &tmB, &full[stage], kb * 64, nt * BN + rank * B_SLICE, MASK, pol_b);
+      tma_load_2d_mc(bdst + rank * B_SLICE * 128, &tmB, &full[stage], kb * 64, col0 + rank * B_SLICE, MASK, pol_b);
     }
   };
   // The weights do not depend on the previous kernel: the first STAGES
@@ -314,13 +336,13 @@ __global__ void __launch_bounds__(192, 1)
   int pre = 0;
   if (p.b_const && warp == 0 && lane == 0) {
     for (int u = slot; u < p.n_units && pre < C::STAGES; u += stride) {
-      int nt, mg, ks;
-      decode_unit(p, u, nt, mg, ks);
+      int nt, mg, ks, col0, width;
+      unit(u, nt, mg, ks, col0, width);
       const int kb0 = ks * p.nkb / p.k_splits, kb1 = (ks + 1) * p.nkb / p.k_splits;
-      const uint32_t bytes = stage_bytes(mg);
+      const uint32_t bytes = stage_bytes(mg, width);
       for (int kb = kb0; kb < kb1 && pre < C::STAGES; ++kb, ++pre) {
         mbar_arrive_expect_tx(&full[pre], bytes);
-        load_b(pre, kb, nt);
+        load_b(pre, kb, col0, width);
       }
     }
   }
@@ -337,11 +359,11 @@ __global__ void __launch_bounds__(192, 1)
       bool issued[8];
       for (int s = 0; s < 8; ++s) issued[s] = s < pre, last_phase[s] = 0;
       for (int u = slot; u < p.n_units && !*abort_flag; u += stride) {
-        int nt, mg, ks;
-        decode_unit(p, u, nt, mg, ks);
+        int nt, mg, ks, col0, width;
+        unit(u, nt, mg, ks, col0, width);
         const int kb0 = ks * p.nkb / p.k_splits, kb1 = (ks + 1) * p.nkb / p.k_splits;
         const int mt_valid = valid_tiles(mg);
-        const uint32_t bytes = stage_bytes(mg);
+        const uint32_t bytes = stage_bytes(mg, width);
         for (int kb = kb0; kb < kb1; ++kb, ++it) {
           const bool b_done = it < pre;  // B already issued before the wait (first use of the stage)
           if (!b_done) {
@@ -359,7 +381,7 @@ __global__ void __launch_bounds__(192, 1)
               if ((tile0(mg) + mt + 1) * 128 > p.lo_row0)
                 tma_load_2d(base + (MT + mt) * C::A_BYTES, &tmA2, &full[stage], kb * 64, (tile0(mg) + mt) * 128);
           }
-          if (!b_done) load_b(stage, kb, nt);
+          if (!b_done) load_b(stage, kb, col0, width);
           issued[stage] = true;
           last_phase[stage] = phase;
           if (++stage == C::STAGES) {
@@ -382,13 +404,15 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      constexpr uint32_t IDESC = idesc_f16_f32(128, BN);
+      constexpr uint32_t IDESC_W = idesc_f16_f32(128, BN);
+      constexpr uint32_t IDESC_N = idesc_f16_f32(128, NW);
       int stage = 0, acc = 0;
       uint32_t phase = 0, acc_phase = 0;
       bool any = false;
       for (int u = slot; u < p.n_units && !*abort_flag; u += stride) {
-        int nt, mg, ks;
-        decode_unit(p, u, nt, mg, ks);
+        int nt, mg, ks, col0, width;
+        unit(u, nt, mg, ks, col0, width);
+        const uint32_t IDESC = (kTail && width != BN) ? IDESC_N : IDESC_W;
         const int kb0 = ks * p.nkb / p.k_splits, kb1 = (ks + 1) * p.nkb / p.k_splits;
         const int mt_valid = valid_tiles(mg);
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, p.wait_ns)) {
@@ -453,8 +477,8 @@ __global__ void __launch_bounds__(192, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int u = slot; u < p.n_units && !*abort_flag; u += stride) {
-      int nt, mg, ks;
-      decode_unit(p, u, nt, mg, ks);
+      int nt, mg, ks, ucol0, width;
+      unit(u, nt, mg, ks, ucol0, width);
       const int mt_valid = valid_tiles(mg);
       if (!mbar_wait(&tfull[acc], acc_phase, p.wait_ns)) {
         record_error(p.err, DEV_WAIT_TIMEOUT_EPILOGUE);
@@ -470,8 +494,8 @@ __global__ void __launch_bounds__(192, 1)
         if constexpr (EPI == EPI_QKV_ROPE) {
           epi_qkv_rope<BN>(p, e, row, nt, t_row);
         } else {
-          for (int c = 0; c < BN / 32; ++c) {
-            const int col0 = nt * BN + c * 32;
+          for (int c = 0; c < width / 32; ++c) {
+            const int col0 = ucol0 + c * 32;
             if (col0 >= p.N) break;  // uniform across the warp
             float v[32];
             tmem_ld_32cols(t_row + c * 32, v);
@@ -836,8 +860,8 @@ bool make_kv_map(CUtensorMap* m, const void* base, int dh, int n_rows, int n_hea
 }
 
 template <int MT, int BN, int EPI, int CS, bool ALO = false>
-static int launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ma2, const GemmParams& p,
-                    const EpiArgs& e, cudaStream_t st, int sms) {
+static int launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ma2, const CUtensorMap& mb2,
+                    const GemmParams& p, const EpiArgs& e, cudaStream_t st, int sms) {
   using C = GemmCfg<MT, BN, ALO>;
   auto kern = gemm_tc_kernel<MT, BN, EPI, CS, ALO>;
   static bool attr_set = false;  // per instantiation
@@ -867,7 +891,7 @@ static int launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensor
   }
   if (CS == 1) {
     const int grid = std::min(p.n_units, sms);
-    return launch_k(kern, dim3(grid), dim3(192), C::SMEM_BYTES, st, ma, mb, ma2, p, e);
+    return launch_k(kern, dim3(grid), dim3(192), C::SMEM_BYTES, st, ma, mb, ma2, mb2, p, e);
   }
   const int clusters = std::min(p.n_units, max_clusters);
   cudaLaunchConfig_t cfg = {};
@@ -882,7 +906,7 @@ static int launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensor
   at[0].val.clusterDim.z = 1;
   cfg.attrs = at;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, ma, mb, ma2, p, e);
+  return cudaLaunchKernelEx(&cfg, kern, ma, mb, ma2, mb2, p, e);
 }
 
 template <int BN, int EPI, bool ALO>
@@ -931,7 +955,7 @@ static int launch_pair(const CUtensorMap& ma, const CUtensorMap& mb, const CUten
 
 template <int EPI>
 static int dispatch_tiling(const GemmTiling& t, const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap* ma2,
-                           const GemmParams& p, const EpiArgs& e, cudaStream_t st, int sms) {
+                           const CUtensorMap& mb2, const GemmParams& p, const EpiArgs& e, cudaStream_t st, int sms) {
   if (t.pair) {
     if (ma2) {
       if (t.bn == 128) return launch_pair<128, EPI, true>(ma, mb, *ma2, p, e, st, sms);
@@ -945,22 +969,22 @@ static int dispatch_tiling(const GemmTiling& t, const CUtensorMap& ma, const CUt
   if (ma2) {  // hi + lo A: one 128-row tile per CTA, no cluster
     if constexpr (EPI == EPI_F32_STORE || EPI == EPI_F32_ADD || EPI == EPI_F32_ATOMIC || EPI == EPI_SWIGLU ||
                   EPI == EPI_READOUT || EPI == EPI_QKV_ROPE) {
-      if (t.mt == 1 && t.cs == 1 && t.bn == 128) return launch_t<1, 128, EPI, 1, true>(ma, mb, *ma2, p, e, st, sms);
-      if (t.mt == 1 && t.cs == 1 && t.bn == 256) return launch_t<1, 256, EPI, 1, true>(ma, mb, *ma2, p, e, st, sms);
+      if (t.mt == 1 && t.cs == 1 && t.bn == 128) return launch_t<1, 128, EPI, 1, true>(ma, mb, *ma2, mb2, p, e, st, sms);
+      if (t.mt == 1 && t.cs == 1 && t.bn == 256) return launch_t<1, 256, EPI, 1, true>(ma, mb, *ma2, mb2, p, e, st, sms);
     }
     return -1;
   }
   if (t.cs == 1) {
-    if (t.mt == 1 && t.bn == 128) return launch_t<1, 128, EPI, 1>(ma, mb, ma, p, e, st, sms);
-    if (t.mt == 1 && t.bn == 256) return launch_t<1, 256, EPI, 1>(ma, mb, ma, p, e, st, sms);
-    if (t.mt == 2 && t.bn == 128) return launch_t<2, 128, EPI, 1>(ma, mb, ma, p, e, st, sms);
-    if (t.mt == 2 && t.bn == 256) return launch_t<2, 256, EPI, 1>(ma, mb, ma, p, e, st, sms);
-    if (t.mt == 4 && t.bn == 128) return launch_t<4, 128, EPI, 1>(ma, mb, ma, p, e, st, sms);
+    if (t.mt == 1 && t.bn == 128) return launch_t<1, 128, EPI, 1>(ma, mb, ma, mb2, p, e, st, sms);
+    if (t.mt == 1 && t.bn == 256) return launch_t<1, 256, EPI, 1>(ma, mb, ma, mb2, p, e, st, sms);
+    if (t.mt == 2 && t.bn == 128) return launch_t<2, 128, EPI, 1>(ma, mb, ma, mb2, p, e, st, sms);
+    if (t.mt == 2 && t.bn == 256) return launch_t<2, 256, EPI, 1>(ma, mb, ma, mb2, p, e, st, sms);
+    if (t.mt == 4 && t.bn == 128) return launch_t<4, 128, EPI, 1>(ma, mb, ma, mb2, p, e, st, sms);
   } else if (t.mt == 1) {
-    if (t.cs == 2 && t.bn == 128) return launch_t<1, 128, EPI, 2>(ma, mb, ma, p, e, st, sms);
-    if (t.cs == 2 && t.bn == 256) return launch_t<1, 256, EPI, 2>(ma, mb, ma, p, e, st, sms);
-    if (t.cs == 4 && t.bn == 128) return launch_t<1, 128, EPI, 4>(ma, mb, ma, p, e, st, sms);
-    if (t.cs == 4 && t.bn == 256) return launch_t<1, 256, EPI, 4>(ma, mb, ma, p, e, st, sms);
+    if (t.cs == 2 && t.bn == 128) return launch_t<1, 128, EPI, 2>(ma, mb, ma, mb2, p, e, st, sms);
+    if (t.cs == 2 && t.bn == 256) return launch_t<1, 256, EPI, 2>(ma, mb, ma, mb2, p, e, st, sms);
+    if (t.cs == 4 && t.bn == 128) return launch_t<1, 128, EPI, 4>(ma, mb, ma, mb2, p, e, st, sms);
+    if (t.cs == 4 && t.bn == 256) return launch_t<1, 256, EPI, 4>(ma, mb, ma, mb2, p, e, st, sms);
   }
   return -1;
 }
@@ -988,21 +1012,49 @@ int launch_gemm(const GemmShape& s, int epi, const EpiArgs& e, const GemmTiling&
   p.b_evict_first = (p.n_mgroups == 1 && (t.pair ? 256 : t.mt * t.cs * 128) >= M) ? 1 : 0;
   p.lo_row0 = s.lo_row0;
   p.b_const = s.b_const ? 1 : 0;
-  CUtensorMap ma, mb, ma2;
+  // the last wave's tail: when the units leave the final wave part-filled,
+  // the last N tiles run as 64-column units instead, filling that wave with
+  // shorter work (elementwise SwiGLU epilogue, single-tile CTAs)
+  p.n_wide = p.n_units;
+  p.nw_col0 = 0;
+  static const bool tail_on = [] {
+    const char* v = std::getenv("PCD_GEMM_TAIL");
+    return !v || std::atoi(v) != 0;
+  }();
+  if (tail_on && epi == EPI_SWIGLU && t.mt == 1 && t.cs == 1 && !t.pair && p.k_splits == 1 && t.bn > 64 &&
+      N % t.bn == 0) {
+    const int grid = std::min(p.n_units, sms);
+    const int waves = p.n_units / grid, rest = p.n_units - waves * grid;
+    if (waves >= 1 && rest > 0) {
+      const int tt = ceil_div(rest, p.n_mgroups);  // N tiles turned into 64-column units
+      const int narrow = tt * (t.bn / 64) * p.n_mgroups;
+      if (tt < p.n_ntiles && narrow <= grid) {
+        p.n_wide = (p.n_ntiles - tt) * p.n_mgroups;
+        p.nw_col0 = (p.n_ntiles - tt) * t.bn;
+        p.n_units = p.n_wide + narrow;
+      }
+    }
+  }
+  CUtensorMap ma, mb, ma2, mb2;
   if (!make_map(&ma, s.a, M, K, s.a_ld, 128)) return -1;
   if (s.a_lo && !make_map(&ma2, s.a_lo, M, K, s.a_ld, 128)) return -1;
   const CUtensorMap* pa2 = s.a_lo ? &ma2 : nullptr;
   if (!make_map(&mb, s.b, N, K, s.b_ld, t.pair ? t.bn / 2 : t.bn / t.cs)) return -1;
+  if (p.n_wide < p.n_units) {
+    if (!make_map(&mb2, s.b, N, K, s.b_ld, 64)) return -1;
+  } else {
+    mb2 = mb;
+  }
   switch (epi) {
-    case EPI_BF16: return dispatch_tiling<EPI_BF16>(t, ma, mb, pa2, p, e, stream, sms);
-    case EPI_F32_ADD: return dispatch_tiling<EPI_F32_ADD>(t, ma, mb, pa2, p, e, stream, sms);
-    case EPI_F32_ATOMIC: return dispatch_tiling<EPI_F32_ATOMIC>(t, ma, mb, pa2, p, e, stream, sms);
-    case EPI_SWIGLU: return dispatch_tiling<EPI_SWIGLU>(t, ma, mb, pa2, p, e, stream, sms);
-    case EPI_READOUT: return dispatch_tiling<EPI_READOUT>(t, ma, mb, pa2, p, e, stream, sms);
-    case EPI_F32_STORE: return dispatch_tiling<EPI_F32_STORE>(t, ma, mb, pa2, p, e, stream, sms);
+    case EPI_BF16: return dispatch_tiling<EPI_BF16>(t, ma, mb, pa2, mb2, p, e, stream, sms);
+    case EPI_F32_ADD: return dispatch_tiling<EPI_F32_ADD>(t, ma, mb, pa2, mb2, p, e, stream, sms);
+    case EPI_F32_ATOMIC: return dispatch_tiling<EPI_F32_ATOMIC>(t, ma, mb, pa2, mb2, p, e, stream, sms);
+    case EPI_SWIGLU: return dispatch_tiling<EPI_SWIGLU>(t, ma, mb, pa2, mb2, p, e, stream, sms);
+    case EPI_READOUT: return dispatch_tiling<EPI_READOUT>(t, ma, mb, pa2, mb2, p, e, stream, sms);
+    case EPI_F32_STORE: return dispatch_tiling<EPI_F32_STORE>(t, ma, mb, pa2, mb2, p, e, stream, sms);
     case EPI_QKV_ROPE:
       if (t.splits != 1 || t.bn % 128 || N % 128) return -1;
-      return dispatch_tiling<EPI_QKV_ROPE>(t, ma, mb, pa2, p, e, stream, sms);
+      return dispatch_tiling<EPI_QKV_ROPE>(t, ma, mb, pa2, mb2, p, e, stream, sms);
   }
   return -1;
 }

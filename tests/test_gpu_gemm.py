@@ -70,6 +70,18 @@ def test_gemm_swiglu():
     assert (out - ref).abs().max().item() < tol
 
 
+@pytest.mark.parametrize("M,N,K,bn", [
+    (825, 17920, 1536, 256),     # the gate/up projection: 490 units, the last 5 N tiles as 140 narrow units
+    (640, 8192, 256, 256),       # 160 units: 2 N tiles become 40 narrow units
+    (512, 5120, 192, 128),       # 128-wide tiles: 2 N tiles become 16 narrow units
+])
+def test_gemm_swiglu_narrow_tail(M, N, K, bn):
+    """More units than SMs with a part-filled last wave: the last N tiles run
+    as 64-column units (another B box, MMA width and epilogue width)."""
+    out, ref, tol = _run(M, N, K, 3, 1, bn, 1, seed=9)
+    assert (out - ref).abs().max().item() < tol
+
+
 def test_gemm_auto_tiling_large():
     out, ref, tol = _run(332, 2048, 1536, 2, 0, 0, 0, seed=3)
     assert (out - ref).abs().max().item() < 1e-3
