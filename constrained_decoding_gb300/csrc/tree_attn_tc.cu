@@ -453,13 +453,23 @@ __global__ void __launch_bounds__(192, 1)
           *reinterpret_cast<uint4*>(slo + q * 64 + c8 * 16) = make_uint4(wl[0], wl[1], wl[2], wl[3]);
         }
       }
-      if (have_o && valid) {
-        fence_proxy_async_smem();
-        const size_t base = static_cast<size_t>(qrow0 + tt) * a.ld_out + (hk * G + r % G) * kDH;
-        bulk_store_s2g(a.out + base, shi, kDH * 2);
-        if (a.out_lo) bulk_store_s2g(a.out_lo + base, slo, kDH * 2);
-        bulk_commit();
-        bulk_wait_read_all();  // the staging rows stay valid until read
+      // the four softmax warps copy the staged rows out together: a token's G
+      // rows are adjacent in the output, so 16 lanes write one 256-byte row
+      // and a warp two rows per store
+      named_barrier_sync(2, 128);
+      if (my_n > 0 && !*abort_flag) {
+        const int tid = threadIdx.x - 64;  // softmax threads: warps 2-5
+        const int per_part = rows * 16;
+        const int n_idx = (a.out_lo ? 2 : 1) * per_part;
+        for (int idx = tid; idx < n_idx; idx += 128) {
+          const int part = idx >= per_part ? 1 : 0;
+          const int rem = idx - part * per_part;
+          const int rr = rem >> 4, c = rem & 15;
+          const uint4 v = *reinterpret_cast<const uint4*>(smem + (part * kRows + rr) * kOutLd + c * 16);
+          act_t* dst = (part ? a.out_lo : a.out) + static_cast<size_t>(qrow0 + rr / G) * a.ld_out +
+                       (hk * G + rr % G) * kDH;
+          *reinterpret_cast<uint4*>(dst + c * 8) = v;
+        }
       }
     }
   }
