@@ -859,6 +859,32 @@ bool make_kv_map(CUtensorMap* m, const void* base, int dh, int n_rows, int n_hea
   return true;
 }
 
+bool make_q_map(CUtensorMap* m, const void* base, int dh, int n_heads, int n_rows, int box_heads, int box_rows) {
+  static std::mutex mu;
+  static std::map<std::tuple<uintptr_t, int, int, int, int, int>, CUtensorMap> cache;
+  const auto key = std::make_tuple(reinterpret_cast<uintptr_t>(base), dh, n_heads, n_rows, box_heads, box_rows);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) {
+    *m = it->second;
+    return true;
+  }
+  if (!tma_init() || n_rows < 1 || dh % 64 || box_heads < 1 || box_heads > 256 || box_rows < 1 || box_rows > 256 ||
+      (reinterpret_cast<uintptr_t>(base) & 15))
+    return false;
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(dh), static_cast<cuuint64_t>(n_heads), static_cast<cuuint64_t>(n_rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(dh) * 2, static_cast<cuuint64_t>(n_heads) * dh * 2};
+  cuuint32_t box[3] = {64, static_cast<cuuint32_t>(box_heads), static_cast<cuuint32_t>(box_rows)};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return false;
+  if (cache.size() > 1024) cache.clear();
+  cache.emplace(key, *m);
+  return true;
+}
+
 template <int MT, int BN, int EPI, int CS, bool ALO = false>
 static int launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ma2, const CUtensorMap& mb2,
                     const GemmParams& p, const EpiArgs& e, cudaStream_t st, int sms) {

@@ -87,5 +87,10 @@ bool tma_init();
 // box {64, 64, 1, 1} with 128-byte swizzling.  Cached by its arguments.
 bool make_kv_map(CUtensorMap* m, const void* base, int dh, int n_rows, int n_heads, int64_t head_rows, int n_layers,
                  int64_t layer_elems);
+// 3-D map of a row-major [n_rows][n_heads][dh] fp16 tensor (q: a token's
+// heads side by side) with boxes of 64 x box_heads x box_rows, 128-byte
+// swizzle: the rows land as box_rows x box_heads consecutive 128-byte rows of
+// one 64-column half.  Cached by its arguments.
+bool make_q_map(CUtensorMap* m, const void* base, int dh, int n_heads, int n_rows, int box_heads, int box_rows);
 
 }  // namespace pcd

@@ -72,6 +72,7 @@ template <bool LO>
 __global__ void __launch_bounds__(192, 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const __grid_constant__ CUtensorMap tmKlo, const __grid_constant__ CUtensorMap tmVlo,
+                        const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQlo,
                         const TreeAttnArgs a, int layer, uint64_t wait_ns, int* err) {
   using C = TcCfg<LO>;
   constexpr int kStages = C::kStages, kKVSt = C::kKVSt, kOffK = C::kOffK, kOffV = C::kOffV, kOffBar = C::kOffBar;
@@ -89,6 +90,7 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* pv_done = bars + 24;  // [kStages] MMA: O += P V done (S/P columns free, O current)
   uint64_t* drain = bars + 28;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 29);
+  uint64_t* q_full = bars + 30;   // producer: the Q tile (and remainder) landed -> MMA
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float2* sML = reinterpret_cast<float2*>(smem + kOffML);
   float* sRed = reinterpret_cast<float*>(smem);  // received partial rows, after the key loop
@@ -131,13 +133,16 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&pv_done[s], 1);
     }
     mbar_init(drain, 1);
+    mbar_init(q_full, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     if constexpr (LO) {
+      tma_prefetch_desc(&tmQlo);
       tma_prefetch_desc(&tmKlo);
       tma_prefetch_desc(&tmVlo);
     }
@@ -200,6 +205,20 @@ __global__ void __launch_bounds__(192, 1)
         tma_load_4d(dst + kKVBytes + kKVBytes / 2, lo, bar, 64, b * kKeys, hk, layer);
       }
     };
+    if (lane == 0) {
+      // the Q tile: tpt tokens x G heads of this KV head, both 64-column
+      // halves (and the remainder's), one box each; rows past tpt x G are
+      // zeroed by the softmax warps
+      const uint32_t box = 64u * static_cast<uint32_t>(G * a.tpt) * 2u;
+      mbar_arrive_expect_tx(q_full, (LO ? 4u : 2u) * box);
+      tma_load_3d(smem + kOffQ, &tmQ, q_full, 0, hk * G, qrow0);
+      tma_load_3d(smem + kOffQ + kQBytes / 2, &tmQ, q_full, 64, hk * G, qrow0);
+      if constexpr (LO) {
+        tma_load_3d(smem + kOffQ + kQBytes, &tmQlo, q_full, 0, hk * G, qrow0);
+        tma_load_3d(smem + kOffQ + kQBytes + kQBytes / 2, &tmQlo, q_full, 64, hk * G, qrow0);
+      }
+    }
+    __syncwarp();
     for (int i = 0; i < my_n; ++i) {
       if (__any_sync(0xffffffffu, *abort_flag != 0)) break;
       const int s = i % kStages, b = block_of(i);
@@ -237,8 +256,10 @@ __global__ void __launch_bounds__(192, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    named_barrier_sync(1, 160);  // Q is staged
+    named_barrier_sync(1, 160);  // the rows past the Q box are zeroed
     if (lane == 0) {
+      const bool q_ok = mbar_wait(q_full, 0, wait_ns);
+      if (!q_ok) fail(DEV_WAIT_TIMEOUT_MMA);
       tc_fence_after_sync();
       constexpr uint32_t kIdescS = idesc_f16_f32(kRows, kKeys);
       constexpr uint32_t kIdescO = idesc_f16_f32(kRows, kDH) | (1u << 16);  // B (V) is MN-major
@@ -248,7 +269,7 @@ __global__ void __launch_bounds__(192, 1)
       int ns = 0, npv = 0;
       uint64_t t_last = globaltimer_ns();
       uint32_t spins = 0;
-      while (npv < my_n) {
+      while (q_ok && npv < my_n) {
         bool progressed = false;
         if (ns < my_n) {
           const int s = ns % kStages;
@@ -317,18 +338,14 @@ __global__ void __launch_bounds__(192, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax rows
-    {  // Q tile (and its remainder): the thread of row r stages it, swizzled
-      const bool ok = r < rows;
-      const size_t qo = (static_cast<size_t>(qrow0 + (ok ? r / G : 0)) * a.Hq + hk * G + (ok ? r % G : 0)) * kDH;
+    {  // the Q tile arrives by TMA (rows tt * G + g); the rows past it are zero
+      if (r >= a.tpt * G) {
 #pragma unroll 1
-      for (int part = 0; part < (LO ? 2 : 1); ++part) {
-        const uint4* src = reinterpret_cast<const uint4*>((part ? a.q_lo : a.q) + qo);
-        uint4 v[16];
+        for (int part = 0; part < (LO ? 2 : 1); ++part)
 #pragma unroll
-        for (int c = 0; c < 16; ++c) v[c] = ok ? src[c] : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int c = 0; c < 16; ++c)
-          *reinterpret_cast<uint4*>(smem + kOffQ + part * kQBytes + (c >> 3) * (kQBytes / 2) + swz(r, c & 7)) = v[c];
+          for (int c = 0; c < 16; ++c)
+            *reinterpret_cast<uint4*>(smem + kOffQ + part * kQBytes + (c >> 3) * (kQBytes / 2) + swz(r, c & 7)) =
+                make_uint4(0u, 0u, 0u, 0u);
       }
       fence_proxy_async_smem();
     }
@@ -478,6 +495,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   if (warp == 0) {
     // nothing of this CTA's copies may still be landing when it exits
+    mbar_wait(q_full, 0, wait_ns);
     for (int s = 0; s < kStages; ++s) {
       if (kissued[s] > 0) mbar_wait(&k_full[s], static_cast<uint32_t>((kissued[s] - 1) & 1), wait_ns);
       if (vissued[s] > 0) mbar_wait(&v_full[s], static_cast<uint32_t>((vissued[s] - 1) & 1), wait_ns);
@@ -559,7 +577,8 @@ __global__ void __launch_bounds__(192, 1)
 
 template <bool LO>
 static int launch_tc_t(const TreeAttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmKlo,
-                       const CUtensorMap& tmVlo, int layer, uint64_t wait_ns, int* err, cudaStream_t s) {
+                       const CUtensorMap& tmVlo, const CUtensorMap& tmQ, const CUtensorMap& tmQlo, int layer,
+                       uint64_t wait_ns, int* err, cudaStream_t s) {
   using C = TcCfg<LO>;
   static bool attr = false;
   if (!attr) {
@@ -588,7 +607,7 @@ static int launch_tc_t(const TreeAttnArgs& a, const CUtensorMap& tmK, const CUte
   }
   cfg.attrs = at;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<LO>, tmK, tmV, tmKlo, tmVlo, a, layer, wait_ns, err);
+  return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<LO>, tmK, tmV, tmKlo, tmVlo, tmQ, tmQlo, a, layer, wait_ns, err);
 }
 
 int launch_tree_attention_tc(const TreeAttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,
@@ -599,8 +618,16 @@ int launch_tree_attention_tc(const TreeAttnArgs& a, const CUtensorMap& tmK, cons
   if (a.tpt < 1 || a.tpt * (a.Hq / a.Hkv) > kRows) return cudaErrorInvalidValue;
   const bool lo = a.q_lo != nullptr;
   if (lo && (!tmKlo || !tmVlo || (a.n_br_tiles > 0 && (!a.kb_lo || !a.vb_lo)))) return cudaErrorInvalidValue;
-  if (lo) return launch_tc_t<true>(a, tmK, tmV, *tmKlo, *tmVlo, layer, wait_ns, err, s);
-  return launch_tc_t<false>(a, tmK, tmV, tmK, tmV, layer, wait_ns, err, s);
+  // the Q tiles by TMA: the q rows hold every head of a token side by side
+  const int G = a.Hq / a.Hkv;
+  const int q_rows = std::max(a.n_pf, a.n_br_tiles > 0 ? a.br_row0 + a.n_br : 0);
+  CUtensorMap mq, mql;
+  if (!make_q_map(&mq, a.q, kDH, a.Hq, std::max(q_rows, 1), G, a.tpt)) return cudaErrorInvalidValue;
+  if (lo) {
+    if (!make_q_map(&mql, a.q_lo, kDH, a.Hq, std::max(q_rows, 1), G, a.tpt)) return cudaErrorInvalidValue;
+    return launch_tc_t<true>(a, tmK, tmV, *tmKlo, *tmVlo, mq, mql, layer, wait_ns, err, s);
+  }
+  return launch_tc_t<false>(a, tmK, tmV, tmK, tmV, mq, mq, layer, wait_ns, err, s);
 }
 
 }  // namespace pcd
