@@ -214,48 +214,124 @@ def scoring_code(rule) -> int:
     return int(rule)
 
 
-class _Fields:
-    """Keeps the int32 arrays of a list of fields alive for one call."""
+def _struct_dtype(cstruct) -> np.dtype:
+    """numpy record type with the byte layout of a ctypes structure (pointers
+    as uint64), so an array of structs is filled column by column."""
+    names, formats, offsets = [], [], []
+    for name, ct in cstruct._fields_:
+        names.append(name)
+        offsets.append(getattr(cstruct, name).offset)
+        if ct is ctypes.c_float:
+            formats.append(np.float32)
+        elif ct in (ctypes.c_int, ctypes.c_int32):
+            formats.append(np.int32)
+        else:  # a pointer
+            formats.append(np.uint64)
+    return np.dtype({"names": names, "formats": formats, "offsets": offsets, "itemsize": ctypes.sizeof(cstruct)})
+
+
+_FIELD_DT = _struct_dtype(D.pcd_field)
+_RESULT_DT = _struct_dtype(D.pcd_field_result)
+
+
+def _ints(a) -> list:
+    return a.tolist() if isinstance(a, np.ndarray) else [int(x) for x in a]
+
+
+class Schema:
+    """A list of fields packed once into the C layout (one int32 buffer and an
+    array of pcd_field), for callers that score the same schema many times:
+    every call that takes `fields` also takes a Schema.  Each field needs
+    `scaffold` and `labels` (token paths), and may set `temperature`,
+    `scoring` ("sum", "mean", "level" or a PCD_SCORE_* code) and `label_of`
+    (the label each path spells)."""
 
     def __init__(self, fields: Sequence):
-        self.keep = []
-        self.arr = (D.pcd_field * len(fields))()
-        self.n_cands = []
-        for i, f in enumerate(fields):
-            sc = _i32(f.scaffold)
-            labels = [_i32(l) for l in f.labels]
-            toks = _i32(np.concatenate(labels)) if labels else _i32([])
-            offs = _i32(np.concatenate([[0], np.cumsum([len(l) for l in labels])]))
-            self.keep += [sc, toks, offs]
+        fields = list(fields)
+        ints: list = []
+        cols = {k: [] for k in ("o_sc", "n_sc", "o_tok", "o_off", "n_c", "temp", "rule", "o_lab", "n_lab")}
+        self.n_cands: List[int] = []
+        for f in fields:
+            sc = _ints(f.scaffold)
+            labels = [_ints(l) for l in f.labels]
+            cols["o_sc"].append(len(ints))
+            cols["n_sc"].append(len(sc))
+            ints.extend(sc)
+            cols["o_tok"].append(len(ints))
+            for l in labels:
+                ints.extend(l)
+            cols["o_off"].append(len(ints))
+            acc = 0
+            ints.append(0)
+            for l in labels:
+                acc += len(l)
+                ints.append(acc)
             label_of = getattr(f, "label_of", None)
             if label_of is None:
-                lab_ptr, n_out = None, len(labels)
+                cols["o_lab"].append(-1)
+                n_out = len(labels)
             else:
-                lab = _i32(label_of)
+                lab = _ints(label_of)
                 if len(lab) != len(labels):
                     raise ValueError("label_of needs one entry per token path")
-                self.keep.append(lab)
-                lab_ptr, n_out = _ptr_i32(lab), (int(lab.max()) + 1 if len(lab) else 0)
-            self.arr[i] = D.pcd_field(_ptr_i32(sc), len(sc), _ptr_i32(toks), _ptr_i32(offs), len(labels),
-                                      float(getattr(f, "temperature", 1.0) or 0.0),
-                                      scoring_code(getattr(f, "scoring", "sum")), lab_ptr, n_out)
+                cols["o_lab"].append(len(ints))
+                ints.extend(lab)
+                n_out = max(lab) + 1 if lab else 0
+            cols["n_c"].append(len(labels))
+            cols["temp"].append(float(getattr(f, "temperature", 1.0) or 0.0))
+            cols["rule"].append(scoring_code(getattr(f, "scoring", "sum")))
+            cols["n_lab"].append(n_out)
             self.n_cands.append(n_out)
+        self.data = np.array(ints if ints else [0], dtype=np.int32)
+        base = np.uint64(self.data.ctypes.data)
+        a = np.zeros(len(fields), _FIELD_DT)
+        if fields:
+            four = np.uint64(4)
+            a["scaffold"] = base + four * np.array(cols["o_sc"], np.uint64)
+            a["n_scaffold"] = cols["n_sc"]
+            a["cand_tokens"] = base + four * np.array(cols["o_tok"], np.uint64)
+            a["cand_offsets"] = base + four * np.array(cols["o_off"], np.uint64)
+            a["n_cands"] = cols["n_c"]
+            a["temperature"] = cols["temp"]
+            a["scoring"] = cols["rule"]
+            o_lab = np.array(cols["o_lab"], np.int64)
+            a["cand_label"] = np.where(o_lab >= 0, base + four * np.maximum(o_lab, 0).astype(np.uint64), np.uint64(0))
+            a["n_labels"] = cols["n_lab"]
+        self.structs = a
+        self.arr = ctypes.cast(a.ctypes.data, ctypes.POINTER(D.pcd_field))
+
+    def __len__(self) -> int:
+        return len(self.n_cands)
+
+
+def _Fields(fields) -> Schema:
+    """The packed form of `fields` (a Schema is used as it is)."""
+    return fields if isinstance(fields, Schema) else Schema(fields)
 
 
 class _Results:
+    """Result structs and one float buffer (probs, then logprobs) for a call."""
+
     def __init__(self, n_cands: List[int]):
-        self.arr = (D.pcd_field_result * len(n_cands))()
-        self.buf = []
-        for i, n in enumerate(n_cands):
-            p = np.zeros(n, np.float32)
-            lp = np.zeros(n, np.float32)
-            self.buf.append((p, lp))
-            self.arr[i].probs = p.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
-            self.arr[i].logprobs = lp.ctypes.data_as(ctypes.POINTER(ctypes.c_float))
+        self.n_cands = list(n_cands)
+        self.total = int(sum(self.n_cands))
+        self.buf = np.zeros(2 * max(self.total, 1), np.float32)
+        self.offs = np.concatenate([[0], np.cumsum(self.n_cands, dtype=np.int64)])[:-1].astype(np.uint64)
+        a = np.zeros(len(self.n_cands), _RESULT_DT)
+        base = np.uint64(self.buf.ctypes.data)
+        four = np.uint64(4)
+        a["probs"] = base + four * self.offs
+        a["logprobs"] = base + four * (np.uint64(self.total) + self.offs)
+        self.structs = a
+        self.arr = ctypes.cast(a.ctypes.data, ctypes.POINTER(D.pcd_field_result))
 
     def results(self) -> List[FieldResult]:
-        return [FieldResult(p, lp, int(r.label), float(r.mass), float(r.log_mass), float(r.margin),
-                            float(r.first_mass)) for r, (p, lp) in zip(self.arr, self.buf)]
+        a = self.structs
+        t = self.total
+        return [FieldResult(self.buf[o:o + n], self.buf[t + o:t + o + n], lab, m, lm, mg, fm)
+                for o, n, lab, m, lm, mg, fm in zip(self.offs.tolist(), self.n_cands, a["label"].tolist(),
+                                                    a["mass"].tolist(), a["log_mass"].tolist(),
+                                                    a["margin"].tolist(), a["first_mass"].tolist())]
 
 
 def _stats_dict(s: D.pcd_stats) -> dict:

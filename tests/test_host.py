@@ -173,6 +173,25 @@ def test_branch_compiler_context_tokens(lib):
     assert ei.value.code == -7
 
 
+def test_schema_packing(lib):
+    """A Schema (fields packed once into the C layout) compiles to the same
+    plan as the list of fields, scoring rules and label maps included."""
+    import dataclasses
+    import constrained_decoding_gb300.pcd as pcd
+    req = make_custom(8, 512, 10, [("spelled", 3, 3), ("bool",), ("shared", 4, 2, 3), ("enum", 5, 1, 4)])
+    fields = [dataclasses.replace(f, scoring=r, temperature=t)
+              for f, r, t in zip(req.fields, ("level", "sum", "mean", 2), (1.0, 0.5, 0.0, 3.0))]
+    a = pcd.pcd_plan_inspect(fields, 512)
+    sch = pcd.Schema(fields)
+    b = pcd.pcd_plan_inspect(sch, 512)
+    for k in pcd.PLAN_ARRAYS:
+        np.testing.assert_array_equal(a[k], b[k], err_msg=k)
+    np.testing.assert_array_equal(b["scoring"], [2, 0, 1, 2])
+    assert len(sch) == 4 and sch.n_cands == [3, 2, 4, 5]
+    np.testing.assert_allclose(sch.structs["temperature"], [1.0, 0.5, 0.0, 3.0])
+    assert sch.structs["cand_label"][1] == 0 and sch.structs["cand_label"][0] != 0
+
+
 def test_branch_compiler_spellings(lib):
     """Candidate paths that spell one label: the plan records each path's
     label and each field's label count; bad label maps are rejected."""
