@@ -122,3 +122,22 @@ def test_one_spelling_per_label_is_unchanged(pcd, model, request1):
         np.testing.assert_array_equal(a.probs, b.probs)
         np.testing.assert_array_equal(a.logprobs, b.logprobs)
         assert a.label == b.label and a.mass == b.mass
+
+
+def test_schema_gives_the_same_results(pcd, model, request1):
+    """A Schema packed once gives bit-identical results to the field list, on
+    every path that takes fields."""
+    sch = pcd.Schema(request1.fields)
+    cache = pcd.pcd_prefill(model, request1.prefix)
+    pairs = [(pcd.pcd_score(model, cache, request1.fields), pcd.pcd_score(model, cache, sch)),
+             (pcd.pcd_prefill_score(model, request1.prefix, request1.fields),
+              pcd.pcd_prefill_score(model, request1.prefix, sch)),
+             (pcd.pcd_score_batch(model, [cache, cache], [request1.fields, request1.fields])[1],
+              pcd.pcd_score_batch(model, [cache, cache], [sch, sch])[1]),
+             (pcd.pcd_prefill_score_first_field_first(model, request1.prefix, request1.fields, [3]),
+              pcd.pcd_prefill_score_first_field_first(model, request1.prefix, sch, [3]))]
+    for a, b in pairs:
+        for x, y in zip(a, b):
+            np.testing.assert_array_equal(x.probs, y.probs)
+            np.testing.assert_array_equal(x.logprobs, y.logprobs)
+            assert x.label == y.label and x.mass == y.mass and x.first_mass == y.first_mass
