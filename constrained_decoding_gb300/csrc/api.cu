@@ -1688,8 +1688,6 @@ int score_impl(pcd_model* m, const pcd_cache* const* caches, const pcd_field* co
   return PCD_OK;
 }
 
-}  // namespace
-
 // First field first: `decide` runs the pass that decides fields[0] (writing
 // out[0]) and names the prefix it ran against; the answer line (scaffold,
 // the winning label's first listed path, sep) is then either written after
@@ -1771,6 +1769,8 @@ int first_field_first(pcd_model* m, const pcd_field* fields, int n_fields, const
   }
   return PCD_OK;
 }
+
+}  // namespace
 
 // ===================================================================== C ABI
 extern "C" {
