@@ -109,84 +109,10 @@ __global__ void __launch_bounds__(kNormThreads) rmsnorm_kernel(const float* __re
   }
 }
 
-// One warp per row: the row's float4s stay in registers (NV per lane), the
-// sum of squares is reduced by shuffles alone, eight rows per CTA.
-template <int NV>
-__global__ void __launch_bounds__(256) rmsnorm_warp_kernel(const float* __restrict__ x, int ldx,
-                                                           const int32_t* __restrict__ rows, int n, int d,
-                                                           const float* __restrict__ gain, float eps,
-                                                           act_t* __restrict__ out, int ldo,
-                                                           act_t* __restrict__ out_lo) {
-  griddep_launch_dependents();
-  griddep_wait();
-  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (r >= n) return;
-  const int src = rows ? rows[r] : r;
-  const float4* xr = reinterpret_cast<const float4*>(x + static_cast<size_t>(src) * ldx);
-  const int nv = d / 4;
-  float4 v[NV];
-  float ss = 0.f;
-#pragma unroll
-  for (int j = 0; j < NV; ++j) {
-    const int i = lane + 32 * j;
-    if (i < nv) {
-      v[j] = xr[i];
-      ss += v[j].x * v[j].x + v[j].y * v[j].y + v[j].z * v[j].z + v[j].w * v[j].w;
-    }
-  }
-#pragma unroll
-  for (int o = 16; o; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  const float inv = rsqrtf(ss / static_cast<float>(d) + eps);
-  const float4* g4 = reinterpret_cast<const float4*>(gain);
-  uint2* o2 = reinterpret_cast<uint2*>(out + static_cast<size_t>(r) * ldo);
-  uint2* l2 = out_lo ? reinterpret_cast<uint2*>(out_lo + static_cast<size_t>(r) * ldo) : nullptr;
-#pragma unroll
-  for (int j = 0; j < NV; ++j) {
-    const int i = lane + 32 * j;
-    if (i < nv) {
-      const float4 g = g4[i];
-      const float y0 = v[j].x * inv * g.x, y1 = v[j].y * inv * g.y, y2 = v[j].z * inv * g.z, y3 = v[j].w * inv * g.w;
-      uint2 w;
-      w.x = pack2(y0, y1);
-      w.y = pack2(y2, y3);
-      o2[i] = w;
-      if (l2) {  // the rounding remainder, so hi + lo carries the fp32 value
-        const __half2* h = reinterpret_cast<const __half2*>(&w);
-        const float2 a = __half22float2(h[0]), b = __half22float2(h[1]);
-        uint2 lo;
-        lo.x = pack2(y0 - a.x, y1 - a.y);
-        lo.y = pack2(y2 - b.x, y3 - b.y);
-        l2[i] = lo;
-      }
-    }
-  }
-}
-
-template <int NV>
-static int launch_norm_warp(const float* x, int ldx, const int32_t* rows, int n, int d, const float* gain, float eps,
-                            act_t* out, int ldo, cudaStream_t s, act_t* out_lo) {
-  return launch_k(rmsnorm_warp_kernel<NV>, dim3((n + 7) / 8), dim3(256), 0, s, x, ldx, rows, n, d, gain, eps, out, ldo,
-                  out_lo);
-}
-
 int launch_rmsnorm(const float* x, int ldx, const int32_t* rows, int n, int d, const float* gain, float eps, act_t* out,
                    int ldo, cudaStream_t s, act_t* out_lo) {
   if (n <= 0) return 0;
   if (d % 4 || d > 4 * kNormThreads * kNormMaxVec) return -1;
-  static const bool warp_rows = [] {
-    const char* e = std::getenv("PCD_NORM_WARP");
-    return !e || std::atoi(e) != 0;
-  }();
-  if (warp_rows) {
-    const int per_lane = (d / 4 + 31) / 32;
-    if (per_lane <= 1) return launch_norm_warp<1>(x, ldx, rows, n, d, gain, eps, out, ldo, s, out_lo);
-    if (per_lane <= 4) return launch_norm_warp<4>(x, ldx, rows, n, d, gain, eps, out, ldo, s, out_lo);
-    if (per_lane <= 8) return launch_norm_warp<8>(x, ldx, rows, n, d, gain, eps, out, ldo, s, out_lo);
-    if (per_lane <= 12) return launch_norm_warp<12>(x, ldx, rows, n, d, gain, eps, out, ldo, s, out_lo);
-    if (per_lane <= 16) return launch_norm_warp<16>(x, ldx, rows, n, d, gain, eps, out, ldo, s, out_lo);
-    if (per_lane <= 28) return launch_norm_warp<28>(x, ldx, rows, n, d, gain, eps, out, ldo, s, out_lo);
-  }
   return launch_k(rmsnorm_kernel, dim3(n), dim3(kNormThreads), 0, s, x, ldx, rows, n, d, gain, eps, out, ldo, out_lo);
 }
 
