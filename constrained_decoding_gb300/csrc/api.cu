@@ -148,12 +148,6 @@ struct pcd_model {
   float* final_norm = nullptr;
   float2* rope = nullptr;
   int* d_err = nullptr;
-  // split long tree-attention tiles over two CTAs: partial states and ticket
-  // counters for at most `sms` (tile, KV head) slots
-  bool tree_split = true;
-  float* split_o = nullptr;
-  float2* split_ml = nullptr;
-  int* split_cnt = nullptr;
   uint64_t wait_ns = 2000000000ull;
   DevBuf x32, xn, xn_lo, qkv, q, q_lo, kb, vb, kb_lo, vb_lo, att, att_lo, hb, hb_lo, hr_lo, part_o, part_ml, hr, ro_part, z, lse, plan_buf,
       result, ids;
@@ -1113,18 +1107,8 @@ int tree_tile_rows(const pcd_model* m) { return (m->tree_attn && m->attn_tc && m
 bool kv_lo(const pcd_model* m) { return tree_tile_rows(m) == 128 && (m->split_act & 256) != 0; }
 
 // One tree-attention launch over the prefix cache `c` at layer l.
-int launch_tree(pcd_model* m, const pcd::TreeAttnArgs& ta_in, const pcd_cache* c, int l) {
+int launch_tree(pcd_model* m, const pcd::TreeAttnArgs& ta, const pcd_cache* c, int l) {
   if (tree_tile_rows(m) == 128) {
-    // split the longest tiles over a second CTA while every CTA still fits
-    // one wave of the SMs (the kernel orders tiles longest first)
-    pcd::TreeAttnArgs ta = ta_in;
-    const int items = ta.n_br_tiles + ta.n_pf_tiles;
-    if (ta.csk == 1 && m->tree_split && m->split_cnt && m->Hkv > 0) {
-      ta.n_split = std::max(0, std::min(items, m->sms / m->Hkv - items));
-      ta.split_o = m->split_o;
-      ta.split_ml = m->split_ml;
-      ta.split_cnt = m->split_cnt;
-    }
     CUtensorMap mk, mv;
     const int64_t layer_elems = static_cast<int64_t>(m->Hkv) * c->cap * m->dh;
     if (!pcd::make_kv_map(&mk, c->k, m->dh, ta.n_keys, m->Hkv, c->cap, m->L, layer_elems) ||
@@ -1144,7 +1128,7 @@ int launch_tree(pcd_model* m, const pcd::TreeAttnArgs& ta_in, const pcd_cache* c
     }
     return pcd::launch_tree_attention_tc(ta, mk, mv, nullptr, nullptr, l, m->wait_ns, m->d_err, m->stream);
   }
-  return pcd::launch_tree_attention(ta_in, m->stream);
+  return pcd::launch_tree_attention(ta, m->stream);
 }
 
 // ------------------------------------------------------------ plan upload
@@ -1372,7 +1356,6 @@ int build_model(const pcd_model_config& cfg, TensorFn get, void* ctx, int dtype,
   if (const char* g = std::getenv("PCD_SPLIT_ACT")) m->split_act = std::atoi(g);
   if (const char* g = std::getenv("PCD_TREE_ATTN")) m->tree_attn = std::atoi(g) != 0;
   if (const char* g = std::getenv("PCD_ATTN_TC")) m->attn_tc = std::atoi(g) != 0;
-  if (const char* g = std::getenv("PCD_TREE_SPLIT")) m->tree_split = std::atoi(g) != 0;
   m->sms = prop.multiProcessorCount;
   if (const char* w = std::getenv("PCD_WAIT_LIMIT_MS")) m->wait_ns = static_cast<uint64_t>(std::atof(w) * 1e6);
 
@@ -1515,17 +1498,6 @@ int build_model(const pcd_model_config& cfg, TensorFn get, void* ctx, int dtype,
     return cleanup(fail(PCD_ERR_OOM, "error word"));
   }
   cudaMemset(m->d_err, 0, sizeof(int));
-  if (m->dh == 128) {  // the tensor-core tree attention's split tiles (left off if this fails)
-    const size_t slots = static_cast<size_t>(m->sms);
-    if (cudaMalloc(&m->split_o, slots * 2 * 128 * 128 * sizeof(float)) != cudaSuccess ||
-        cudaMalloc(&m->split_ml, slots * 2 * 128 * sizeof(float2)) != cudaSuccess ||
-        cudaMalloc(&m->split_cnt, slots * sizeof(int)) != cudaSuccess) {
-      cudaGetLastError();
-      m->tree_split = false;
-    } else {
-      cudaMemset(m->split_cnt, 0, slots * sizeof(int));
-    }
-  }
   cudaEventCreateWithFlags(&m->up_ev, cudaEventDisableTiming);
   cudaEventCreate(&m->ev_a);
   cudaEventCreate(&m->ev_b);
@@ -1879,8 +1851,6 @@ void pcd_model_free(pcd_model* m) {
   if (m->fblob) cudaFree(m->fblob);
   if (m->rope) cudaFree(m->rope);
   if (m->d_err) cudaFree(m->d_err);
-  for (void* b : {static_cast<void*>(m->split_o), static_cast<void*>(m->split_ml), static_cast<void*>(m->split_cnt)})
-    if (b) cudaFree(b);
   if (m->up) cudaFreeHost(m->up);
   if (m->down) cudaFreeHost(m->down);
   if (m->up_ev) cudaEventDestroy(m->up_ev);

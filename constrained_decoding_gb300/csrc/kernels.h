@@ -124,14 +124,6 @@ struct TreeAttnArgs {
   const unsigned long long* tile_mask;      // [chunks][tpt] bit i: key i of the chunk is visible to the token
   float scale_log2;                         // log2(e) / sqrt(DH)
   int csk;                                  // CTAs (cluster size) per (tile, KV head): 1 .. 8
-  // csk = 1 only: the first n_split tiles run as two CTAs each (half of the
-  // key blocks each), merged through split_o / split_ml (per (tile, KV head,
-  // part) 128 rows of fp32 O and (m, l)); split_cnt holds one zeroed ticket
-  // counter per (tile, KV head), left zero again by each launch
-  int n_split = 0;
-  float* split_o = nullptr;
-  float2* split_ml = nullptr;
-  int* split_cnt = nullptr;
 };
 int launch_tree_attention(const TreeAttnArgs& a, cudaStream_t s);
 // The same on the tcgen05 tensor cores, head dim 128, tiles of tpt x G <= 128

@@ -96,23 +96,8 @@ __global__ void __launch_bounds__(192, 1)
   float* sRed = reinterpret_cast<float*>(smem);  // received partial rows, after the key loop
 
   const int csk = a.csk;
-  // CTAs of one (tile, KV head): a cluster of csk, or (csk = 1) two parts for
-  // each of the first n_split tiles (the longest: branch tiles, then prefix
-  // tiles from the last), merged through global memory, else one
-  int item, rank, parts;
-  if (csk > 1) {
-    item = blockIdx.x / csk;
-    rank = blockIdx.x - item * csk;
-    parts = csk;
-  } else if (static_cast<int>(blockIdx.x) < 2 * a.n_split) {
-    item = blockIdx.x >> 1;
-    rank = blockIdx.x & 1;
-    parts = 2;
-  } else {
-    item = blockIdx.x - a.n_split;
-    rank = 0;
-    parts = 1;
-  }
+  const int item = blockIdx.x / csk;
+  const int rank = blockIdx.x - item * csk;
   const int hk = blockIdx.y;
   const int G = a.Hq / a.Hkv;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -131,11 +116,11 @@ __global__ void __launch_bounds__(192, 1)
   const int nbp = (pf_keys + kKeys - 1) / kKeys;
   const int ch0 = branch ? a.tile_chunk_off[tile] : 0;
   const int nb = nbp + (branch ? a.tile_chunk_off[tile + 1] - ch0 : 0);
-  const int my_n = rank < nb ? (nb - 1 - rank) / parts + 1 : 0;
+  const int my_n = rank < nb ? (nb - 1 - rank) / csk + 1 : 0;
   // CTAs of one KV head start at different key blocks (the online softmax
   // takes them in any order), so they do not all read the same block at once
   const int rot = my_n > 0 ? static_cast<int>((item * 5u + hk * 3u) % static_cast<unsigned>(my_n)) : 0;
-  auto block_of = [&](int i) { int j = i + rot; j -= j >= my_n ? my_n : 0; return rank + j * parts; };
+  auto block_of = [&](int i) { int j = i + rot; j -= j >= my_n ? my_n : 0; return rank + j * csk; };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -461,75 +446,9 @@ __global__ void __launch_bounds__(192, 1)
     }
     have_o = __all_sync(0xffffffffu, have_o);
     tc_fence_after_sync();
-    // a split tile's two parts: each leaves its partial state (unnormalised O,
-    // m, l of every row) in global memory and takes a ticket; the second one
-    // folds the other's state into its own O (TMEM) and l and writes the
-    // output as a whole tile does.  Nothing waits on the other part.
-    bool emit = my_n > 0;
-    if (csk == 1 && parts == 2) {
-      const size_t slot = static_cast<size_t>(item) * a.Hkv + hk;
-      const size_t mine = (slot * 2 + rank) * kRows + r, other = (slot * 2 + (rank ^ 1)) * kRows + r;
-      const float m1 = have_o ? m_ref : -INFINITY, l1 = have_o ? l : 0.f;
-      float4* po = reinterpret_cast<float4*>(a.split_o + mine * kDH);
-#pragma unroll 1
-      for (int q = 0; q < kDH / 32; ++q) {
-        float ov[32];
-        if (have_o) {
-          tmem_ld_32cols(trow + kColO + q * 32, ov);
-        } else {
-#pragma unroll
-          for (int x = 0; x < 32; ++x) ov[x] = 0.f;
-        }
-#pragma unroll
-        for (int x = 0; x < 8; ++x) po[q * 8 + x] = make_float4(ov[4 * x], ov[4 * x + 1], ov[4 * x + 2], ov[4 * x + 3]);
-      }
-      a.split_ml[mine] = make_float2(m1, l1);
-      __threadfence();
-      named_barrier_sync(2, 128);
-      volatile int* ticket = reinterpret_cast<volatile int*>(bars + 31);
-      if (threadIdx.x == 64) {
-        const int t = atomicAdd(a.split_cnt + slot, 1);
-        if (t == 1) atomicExch(a.split_cnt + slot, 0);  // the next launch starts from zero
-        *ticket = t;
-      }
-      named_barrier_sync(2, 128);
-      emit = *ticket == 1;
-      if (emit) {
-        __threadfence();
-        const float2 ml2 = __ldcg(a.split_ml + other);
-        const float m2 = ml2.x, l2 = ml2.y;
-        float M = -INFINITY;
-        if (l1 > 0.f) M = m1;
-        if (l2 > 0.f) M = fmaxf(M, m2);
-        const float w1 = l1 > 0.f ? ex2_approx(m1 - M) : 0.f;
-        const float w2 = l2 > 0.f ? ex2_approx(m2 - M) : 0.f;
-        const float4* p2 = reinterpret_cast<const float4*>(a.split_o + other * kDH);
-#pragma unroll 1
-        for (int q = 0; q < kDH / 32; ++q) {
-          float ov[32];
-          if (have_o) {
-            tmem_ld_32cols(trow + kColO + q * 32, ov);
-          } else {
-#pragma unroll
-            for (int x = 0; x < 32; ++x) ov[x] = 0.f;
-          }
-#pragma unroll
-          for (int x = 0; x < 8; ++x) {
-            const float4 o2 = __ldcg(p2 + q * 8 + x);
-            ov[4 * x] = w1 * ov[4 * x] + w2 * o2.x;
-            ov[4 * x + 1] = w1 * ov[4 * x + 1] + w2 * o2.y;
-            ov[4 * x + 2] = w1 * ov[4 * x + 2] + w2 * o2.z;
-            ov[4 * x + 3] = w1 * ov[4 * x + 3] + w2 * o2.w;
-          }
-          tmem_st_32cols(trow + kColO + q * 32, ov);
-        }
-        l = w1 * l1 + w2 * l2;
-        have_o = true;
-      }
-    }
-    if (csk == 1 && emit) {
+    if (csk == 1) {
       // normalised rows staged in shared memory (every MMA is done: Q, K and V
-      // are free), then copied out by the four softmax warps
+      // are free), then one bulk copy per 256-byte output row
       const float il = l > 0.f ? 1.f / l : 0.f;
       uint8_t* shi = smem + r * kOutLd;
       uint8_t* slo = smem + (kRows + r) * kOutLd;
@@ -555,7 +474,7 @@ __global__ void __launch_bounds__(192, 1)
       // rows are adjacent in the output, so 16 lanes write one 256-byte row
       // and a warp two rows per store
       named_barrier_sync(2, 128);
-      if (!*abort_flag) {
+      if (my_n > 0 && !*abort_flag) {
         const int tid = threadIdx.x - 64;  // softmax threads: warps 2-5
         const int per_part = rows * 16;
         const int n_idx = (a.out_lo ? 2 : 1) * per_part;
@@ -668,8 +587,7 @@ static int launch_tc_t(const TreeAttnArgs& a, const CUtensorMap& tmK, const CUte
     attr = true;
   }
   cudaLaunchConfig_t cfg = {};
-  const int items = a.n_br_tiles + a.n_pf_tiles;
-  cfg.gridDim = dim3(static_cast<unsigned>(a.csk > 1 ? items * a.csk : items + a.n_split), static_cast<unsigned>(a.Hkv), 1);
+  cfg.gridDim = dim3(static_cast<unsigned>((a.n_br_tiles + a.n_pf_tiles) * a.csk), static_cast<unsigned>(a.Hkv), 1);
   cfg.blockDim = dim3(192, 1, 1);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = s;
@@ -697,9 +615,6 @@ int launch_tree_attention_tc(const TreeAttnArgs& a, const CUtensorMap& tmK, cons
                              cudaStream_t s) {
   if (a.n_br_tiles + a.n_pf_tiles <= 0) return 0;
   if (a.DH != kDH || a.csk < 1 || a.csk > 8) return cudaErrorInvalidValue;
-  if (a.n_split < 0 || a.n_split > a.n_br_tiles + a.n_pf_tiles || (a.n_split > 0 && (a.csk > 1 || !a.split_o ||
-                                                                                    !a.split_ml || !a.split_cnt)))
-    return cudaErrorInvalidValue;
   if (a.tpt < 1 || a.tpt * (a.Hq / a.Hkv) > kRows) return cudaErrorInvalidValue;
   const bool lo = a.q_lo != nullptr;
   if (lo && (!tmKlo || !tmVlo || (a.n_br_tiles > 0 && (!a.kb_lo || !a.vb_lo)))) return cudaErrorInvalidValue;
