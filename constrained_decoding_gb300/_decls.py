@@ -57,6 +57,7 @@ SIGNATURES = [
     ("pcd_sync", c_int, [c_void_p]),
     ("pcd_profile_enable", c_int, [c_void_p, c_int]),
     ("pcd_profile_read", c_int, [c_void_p, P(c_int), P(c_float)]),
+    ("pcd_abi_layout", c_int, [P(c_int32), c_int]),
     ("pcd_strerror", c_char_p, [c_int]),
     ("pcd_last_error", c_char_p, []),
     ("pcd_k_gemm_split", c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, c_int, c_int, c_int, c_int, c_void_p,

@@ -5,6 +5,7 @@
 #include <algorithm>
 #include <chrono>
 #include <cmath>
+#include <cstddef>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -2126,6 +2127,29 @@ int pcd_profile_read(pcd_model* m, int* launches, float* ms) {
   m->prof_rec.clear();
   m->ev_next = 0;
   return PCD_OK;
+}
+
+int pcd_abi_layout(int32_t* out, int n) {
+  const int32_t v[] = {
+      static_cast<int32_t>(sizeof(pcd_model_config)), offsetof(pcd_model_config, n_layers),
+      offsetof(pcd_model_config, d_model), offsetof(pcd_model_config, n_q_heads),
+      offsetof(pcd_model_config, n_kv_heads), offsetof(pcd_model_config, head_dim), offsetof(pcd_model_config, d_ff),
+      offsetof(pcd_model_config, vocab), offsetof(pcd_model_config, rms_eps), offsetof(pcd_model_config, rope_theta),
+      offsetof(pcd_model_config, tied_embedding), offsetof(pcd_model_config, max_positions),
+      static_cast<int32_t>(sizeof(pcd_field)), offsetof(pcd_field, scaffold), offsetof(pcd_field, n_scaffold),
+      offsetof(pcd_field, cand_tokens), offsetof(pcd_field, cand_offsets), offsetof(pcd_field, n_cands),
+      offsetof(pcd_field, temperature), offsetof(pcd_field, scoring), offsetof(pcd_field, cand_label),
+      offsetof(pcd_field, n_labels),
+      static_cast<int32_t>(sizeof(pcd_field_result)), offsetof(pcd_field_result, probs),
+      offsetof(pcd_field_result, logprobs), offsetof(pcd_field_result, label), offsetof(pcd_field_result, mass),
+      offsetof(pcd_field_result, log_mass), offsetof(pcd_field_result, margin), offsetof(pcd_field_result, first_mass),
+      static_cast<int32_t>(sizeof(pcd_stats)), offsetof(pcd_stats, prefill_ms), offsetof(pcd_stats, compile_ms),
+      offsetof(pcd_stats, branch_ms), offsetof(pcd_stats, readout_ms), offsetof(pcd_stats, total_ms),
+      offsetof(pcd_stats, forward_passes), offsetof(pcd_stats, branch_tokens), offsetof(pcd_stats, readout_rows),
+      offsetof(pcd_stats, h2d_bytes), offsetof(pcd_stats, d2h_bytes)};
+  const int total = static_cast<int>(sizeof(v) / sizeof(v[0]));
+  for (int i = 0; out && i < n && i < total; ++i) out[i] = v[i];
+  return total;
 }
 
 const char* pcd_strerror(int code) {

@@ -290,6 +290,14 @@ int pcd_profile_read(pcd_model* m, int* launches, float* ms);
 const char* pcd_strerror(int code);
 const char* pcd_last_error(void);
 
+/* The byte layout of the ABI structs as this library was compiled, for a
+ * binding to check its own copy of the declarations: for pcd_model_config,
+ * pcd_field, pcd_field_result and pcd_stats in that order, the struct's size
+ * and then the offset of each member in declaration order.  Writes at most n
+ * values to out (out may be NULL with n = 0) and returns how many the full
+ * layout has.  Host only. */
+int pcd_abi_layout(int32_t* out, int n);
+
 #ifdef __cplusplus
 }
 #endif

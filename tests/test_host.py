@@ -173,6 +173,21 @@ def test_branch_compiler_context_tokens(lib):
     assert ei.value.code == -7
 
 
+def test_struct_layout_matches_the_library(lib):
+    """The binding's ctypes copies of the ABI structs have the sizes and
+    member offsets the compiled library reports."""
+    import ctypes
+    from constrained_decoding_gb300 import _decls as D
+    n = lib.pcd_abi_layout(None, 0)
+    got = (ctypes.c_int32 * n)()
+    assert lib.pcd_abi_layout(got, n) == n
+    want = []
+    for S in (D.pcd_model_config, D.pcd_field, D.pcd_field_result, D.pcd_stats):
+        want.append(ctypes.sizeof(S))
+        want += [getattr(S, name).offset for name, _ in S._fields_]
+    assert list(got) == want
+
+
 def test_schema_packing(lib):
     """A Schema (fields packed once into the C layout) compiles to the same
     plan as the list of fields, scoring rules and label maps included."""
