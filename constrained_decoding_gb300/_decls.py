@@ -68,6 +68,7 @@ SIGNATURES = [
     ("pcd_k_readout_noalloc", c_int, [c_void_p, c_int, c_void_p, c_int, c_int, P(c_int32), P(c_int32), c_int,
                                       c_void_p, c_void_p, c_void_p, c_void_p]),
     ("pcd_plan_inspect", c_int, [c_void_p, c_int, c_int, P(c_int32), P(P(c_int32)), P(c_int32), c_int]),
+    ("pcd_answer_line", c_int, [c_void_p, c_int, P(c_int32), c_int, P(c_int32), c_int]),
     ("pcd_k_gemm", c_int, [c_void_p, c_int, c_int, c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_int,
                            c_int, c_int, c_int, c_void_p, c_void_p]),
 ]

@@ -1722,16 +1722,9 @@ int first_field_first(pcd_model* m, const pcd_field* fields, int n_fields, const
     return PCD_OK;
   }
   // the answer line: scaffold, the winning label's first listed path, separator
-  const pcd_field& F = fields[0];
-  const int win = out[0].label;
-  int path = win;
-  if (F.cand_label)
-    for (path = 0; path < F.n_cands && F.cand_label[path] != win; ++path) {
-    }
-  if (win < 0 || path >= F.n_cands) return fail(PCD_ERR_CUDA, "first field: no decided label");
-  std::vector<int32_t> line(F.scaffold, F.scaffold + F.n_scaffold);
-  line.insert(line.end(), F.cand_tokens + F.cand_offsets[path], F.cand_tokens + F.cand_offsets[path + 1]);
-  line.insert(line.end(), sep, sep + n_sep);
+  std::vector<int32_t> line;
+  if (pcd::answer_line(fields[0], out[0].label, sep, n_sep, &line) != PCD_OK)
+    return fail(PCD_ERR_CUDA, "first field: no decided label");
   const int n_line = static_cast<int>(line.size());
   int passes = passes1 + 1;
   float ext_ms = 0.f;

@@ -188,6 +188,15 @@ extern "C" int pcd_k_readout_noalloc(const void* h, int R, const void* w, int V,
                       static_cast<int64_t>(PCD_K_READOUT_NOALLOC_MAX_BYTES), dev_err, static_cast<cudaStream_t>(stream));
 }
 
+extern "C" int pcd_answer_line(const void* field, int label, const int32_t* sep, int n_sep, int32_t* out, int cap) {
+  if (!field || cap < 0) return PCD_ERR_INVALID_ARG;
+  std::vector<int32_t> line;
+  const int rc = pcd::answer_line(*static_cast<const pcd_field*>(field), label, sep, n_sep, &line);
+  if (rc != PCD_OK) return rc;
+  for (int i = 0; out && i < cap && i < static_cast<int>(line.size()); ++i) out[i] = line[i];
+  return static_cast<int>(line.size());
+}
+
 extern "C" int pcd_plan_inspect(const void* fields, int n_fields, int vocab, int32_t* sizes, int32_t* const* arrays,
                                 const int32_t* ctx, int n_ctx) {
   if (!sizes || vocab < 1) return PCD_ERR_INVALID_ARG;

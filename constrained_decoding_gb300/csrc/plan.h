@@ -51,4 +51,9 @@ struct HostPlan {
 int compile_fields(const pcd_field* fields, int n_fields, int vocab, HostPlan* p, std::string* msg,
                    const int32_t* ctx = nullptr, int n_ctx = 0);
 
+// The tokens that write a decided field into the prompt (first field first):
+// its scaffold, the first listed path that spells `label`, then sep.  Returns
+// PCD_ERR_INVALID_ARG when no path spells the label.
+int answer_line(const pcd_field& f, int label, const int32_t* sep, int n_sep, std::vector<int32_t>* line);
+
 }  // namespace pcd

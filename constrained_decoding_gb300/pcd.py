@@ -492,6 +492,21 @@ PLAN_ARRAYS = ("tok", "rel", "anc_off", "anc_idx", "ro_tok", "row_ch", "ch_tok",
                "fld_lab", "fld_root", "cand_label", "fld_out", "scoring")
 
 
+def pcd_answer_line(field, label: int, sep=()) -> np.ndarray:
+    """Host-only: the tokens first field first writes for `field` decided as
+    `label` (scaffold, the label's first listed spelling, `sep`)."""
+    lib = load()
+    f = _Fields([field])
+    sp = _i32(sep)
+    sp_ptr = _ptr_i32(sp) if len(sp) else None
+    n = lib.pcd_answer_line(ctypes.cast(f.arr, ctypes.c_void_p), int(label), sp_ptr, len(sp), None, 0)
+    if n < 0:
+        _check(n, "pcd_answer_line")
+    out = np.zeros(max(n, 1), np.int32)
+    lib.pcd_answer_line(ctypes.cast(f.arr, ctypes.c_void_p), int(label), sp_ptr, len(sp), _ptr_i32(out), n)
+    return out[:n]
+
+
 def pcd_plan_inspect(fields: Sequence, vocab: int, ctx=()) -> dict:
     """Host-only compile of `fields` (no GPU), after the context tokens `ctx`
     if any: the packed branch batch as numpy arrays."""

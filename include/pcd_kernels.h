@@ -107,6 +107,14 @@ int pcd_k_readout_noalloc(const void* h, int R, const void* w, int V, int d, con
 int pcd_plan_inspect(const void* fields, int n_fields, int vocab, int32_t* sizes, int32_t* const* arrays,
                      const int32_t* ctx, int n_ctx);
 
+/* Host only, no GPU: the answer line first field first writes for `field`
+ * (a pcd_field, pcd.h) decided as `label`: its scaffold, the first listed
+ * candidate path that spells the label, then sep[0..n_sep) (How TypeSafe's
+ * Jev Might Work, "The first key of a JSON object is a special position").
+ * Writes at most cap tokens to out (may be NULL with cap = 0) and returns the
+ * line's length, or PCD_ERR_INVALID_ARG when no path spells the label. */
+int pcd_answer_line(const void* field, int label, const int32_t* sep, int n_sep, int32_t* out, int cap);
+
 #ifdef __cplusplus
 }
 #endif

@@ -188,6 +188,27 @@ def test_struct_layout_matches_the_library(lib):
     assert list(got) == want
 
 
+def test_answer_line_matches_the_oracle(lib):
+    """The line first field first writes (scaffold, the winning label's first
+    listed spelling, separator) is the oracle's, for plain, shared-prefix and
+    spelled fields; a label no path spells is an error."""
+    import constrained_decoding_gb300.pcd as pcd
+    from oracle import Oracle, scores_to_result
+    req = make_custom(12, 512, 10, [("enum", 4, 1, 3), ("shared", 3, 2, 3), ("spelled", 3, 3), ("spelled", 2, 2)])
+    orc = Oracle.__new__(Oracle)  # answer_line needs no weights
+    sep = np.array([4, 9, 2], np.int32)
+    for f in req.fields:
+        n_lab = len(f.labels) if f.label_of is None else int(f.label_of.max()) + 1
+        for lab in range(n_lab):
+            res = scores_to_result(np.zeros(n_lab))
+            res.label = lab
+            np.testing.assert_array_equal(pcd.pcd_answer_line(f, lab, sep), orc.answer_line(f, res, sep))
+        np.testing.assert_array_equal(pcd.pcd_answer_line(f, 0, []), orc.answer_line(f, scores_to_result([0.0, 0.0]), []))
+    with pytest.raises(pcd.PCDError) as ei:
+        pcd.pcd_answer_line(req.fields[2], 3, sep)
+    assert ei.value.code == -1
+
+
 def test_schema_packing(lib):
     """A Schema (fields packed once into the C layout) compiles to the same
     plan as the list of fields, scoring rules and label maps included."""
