@@ -437,7 +437,9 @@ def run_ours(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "bf16",
+        "dtype": "f16",
+        "dtype_note": "bf16 weights held exactly as fp16 tensor-core operands (values >= 2^-17), fp32 accumulation; "
+                      "activations fp16 with fp16 remainders at the rounding points that need them",
         "data": "synthetic (seeded random-init weights and token ids)",
         "config": {"workload": WORKLOAD, "prefix_len": len(req.prefix), "fields": len(req.fields),
                    "branch_tokens": T, "readout_rows": R, "requests_per_step": 1, "mode": args.mode,
