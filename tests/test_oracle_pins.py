@@ -205,6 +205,36 @@ def test_causality(tiny_oracle64):
     assert np.abs(h1[12:] - h2[12:]).max() > 1e-3
 
 
+def test_rope_enters_relatively_on_q_and_k(tiny_oracle64):
+    """Where RoPE enters the decoder.  Rotating q and k by their positions
+    makes every attention score depend on the positions' difference only, so
+    moving a whole sequence by one offset leaves the logits unchanged (1e-10,
+    fp64) -- with or without a cached prefix.  A rotation of q alone, of k
+    alone, or of v as well breaks that.  Positions still matter: opening a gap
+    inside the sequence changes every row after it and none before it, which
+    a decoder without RoPE would not do."""
+    o = tiny_oracle64
+    rng = np.random.default_rng(21)
+    ids = rng.integers(0, 512, 24)
+    pos = np.arange(24)
+    base = o.logits(o.forward(ids, pos)[0])
+    for off in (1, 37, 1000):
+        moved = o.logits(o.forward(ids, pos + off)[0])
+        np.testing.assert_allclose(moved, base, atol=1e-10, rtol=0)
+    # a cached prefix at shifted positions, extended at the matching ones
+    k = 10
+    for off in (0, 300):
+        hp, (kk, vv) = o.forward(ids[:k], pos[:k] + off)
+        from oracle.pcd_oracle import KVCache
+        cache = KVCache(kk, vv, pos[:k] + off)
+        ht, _ = o.forward(ids[k:], pos[k:] + off, cache)
+        np.testing.assert_allclose(o.logits(ht), base[k:], atol=1e-10, rtol=0)
+    gap = np.concatenate([pos[:12], pos[12:] + 5])
+    opened = o.logits(o.forward(ids, gap)[0])
+    np.testing.assert_allclose(opened[:12], base[:12], atol=1e-10, rtol=0)
+    assert np.abs(opened[12:] - base[12:]).max(axis=1).min() > 1e-4
+
+
 def test_gqa_equals_mha_with_repeated_kv_heads(tiny_weights):
     """GQA with group G equals MHA whose KV head h is KV head h // G."""
     import copy
