@@ -23,6 +23,12 @@ __device__ __forceinline__ void record_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }
 
+// Bound on the waits of an abort path for copies and MMAs that were already
+// issued.  Those complete on their own, so their drain does not take the
+// configurable pipeline limit (which a caller may shrink far below a copy's
+// latency); it only guards against a lost completion.
+constexpr uint64_t kDrainWaitNs = 4000000000ull;
+
 // Element type of every tensor-core operand and stored activation: fp16.
 // The model's weights are bf16 numbers; they are carried as fp16 (every bf16
 // value of magnitude >= 2^-17 is exact in fp16, smaller ones land on the

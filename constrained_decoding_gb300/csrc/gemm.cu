@@ -232,7 +232,7 @@ __device__ __forceinline__ void epi_qkv_rope(const GemmParams& p, const EpiArgs&
 // ALO: A is given as two fp16 matrices, hi and lo (hi + lo carries ~22 bits of
 // the activation); both are multiplied by the same B tile into one
 // accumulator, so the weights are read once.
-template <int MT, int BN, int EPI, int CS, bool ALO>
+template <int MT, int BN, int EPI, bool ALO>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB2,
@@ -241,10 +241,7 @@ __global__ void __launch_bounds__(192, 1)
   // narrow tail units (tmB2: 64-row B boxes) exist only for single-tile CTAs
   // with an elementwise epilogue
   constexpr int NW = 64;
-  constexpr bool kTail = MT == 1 && CS == 1 && EPI == EPI_SWIGLU && BN > NW;
-  static_assert(CS == 1 || MT == 1, "clusters share B across single-tile CTAs");
-  constexpr uint16_t MASK = static_cast<uint16_t>((1u << CS) - 1u);
-  constexpr int B_SLICE = BN / CS;  // B rows each CTA of a cluster loads and multicasts
+  constexpr bool kTail = MT == 1 && EPI == EPI_SWIGLU && BN > NW;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::STAGES * C::STAGE_BYTES);
@@ -257,18 +254,15 @@ __global__ void __launch_bounds__(192, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  // work distribution: a CTA (CS = 1) or a cluster (CS > 1) takes units slot,
-  // slot + stride, ...; in a cluster every CTA runs the same units, on its own
-  // M tile, and they share the B tile
-  const int rank = CS > 1 ? static_cast<int>(cluster_ctarank()) : 0;
-  const int slot = CS > 1 ? static_cast<int>(cluster_id_x()) : static_cast<int>(blockIdx.x);
-  const int stride = CS > 1 ? static_cast<int>(n_clusters_x()) : static_cast<int>(gridDim.x);
+  // work distribution: CTA b takes units b, b + gridDim.x, ...
+  const int slot = static_cast<int>(blockIdx.x);
+  const int stride = static_cast<int>(gridDim.x);
   const int mtiles = (p.M + 127) / 128;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], CS);
+      mbar_init(&empty[s], 1);
     }
     for (int a = 0; a < C::ACC_STAGES; ++a) {
       mbar_init(&tfull[a], 1);
@@ -288,11 +282,7 @@ __global__ void __launch_bounds__(192, 1)
     tmem_relinquish();
   }
   tc_fence_before_sync();
-  if constexpr (CS > 1) {
-    cluster_sync_all();  // peers multicast into this CTA only once its barriers exist
-  } else {
-    __syncthreads();
-  }
+  __syncthreads();
   tc_fence_after_sync();
   const uint32_t tbase = *tmem_slot;
 
@@ -311,7 +301,7 @@ __global__ void __launch_bounds__(192, 1)
       width = NW;
     }
   };
-  auto tile0 = [&](int mg) { return mg * MT * CS + rank * MT; };  // this CTA's first M tile of group mg
+  auto tile0 = [&](int mg) { return mg * MT; };  // this CTA's first M tile of group mg
   auto valid_tiles = [&](int mg) { return max(0, min(MT, mtiles - tile0(mg))); };
   // bytes one stage of unit (mg) receives: its A tiles (and lo halves), then B
   auto stage_bytes = [&](int mg, int width) {
@@ -324,11 +314,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint64_t pol_b = p.b_evict_first ? l2_policy_evict_first() : l2_policy_evict_last();
   auto load_b = [&](int stage, int kb, int col0, int width) {
     uint8_t* bdst = smem + stage * C::STAGE_BYTES + C::A_PARTS * MT * C::A_BYTES;
-    if constexpr (CS == 1) {
-      tma_load_2d_hint(bdst, (kTail && width != BN) ? &tmB2 : &tmB, &full[stage], kb * 64, col0, pol_b);
-    } else {
-      tma_load_2d_mc(bdst + rank * B_SLICE * 128, &tmB, &full[stage], kb * 64, col0 + rank * B_SLICE, MASK, pol_b);
-    }
+    tma_load_2d_hint(bdst, (kTail && width != BN) ? &tmB2 : &tmB, &full[stage], kb * 64, col0, pol_b);
   };
   // The weights do not depend on the previous kernel: the first STAGES
   // stages (all empty now) get their B tiles before the wait below, in the
@@ -393,12 +379,7 @@ __global__ void __launch_bounds__(192, 1)
       if (*abort_flag) {
         // let every copy still in flight land before the CTA exits
         for (int s = 0; s < C::STAGES; ++s)
-          if (issued[s]) mbar_wait(&full[s], last_phase[s], p.wait_ns);
-      }
-      if constexpr (CS > 1) {
-        // every peer's release of the last fill of each stage has arrived here
-        for (int s = 0; s < C::STAGES; ++s)
-          if (issued[s] && !mbar_wait(&empty[s], last_phase[s], p.wait_ns)) record_error(p.err, DEV_WAIT_TIMEOUT_PRODUCER);
+          if (issued[s]) mbar_wait(&full[s], last_phase[s], kDrainWaitNs);
       }
     }
   } else if (warp == 1) {
@@ -447,11 +428,7 @@ __global__ void __launch_bounds__(192, 1)
                          sdesc_kmajor_sw128(b_base + k * 32), IDESC, 1u);
             }
           }
-          if constexpr (CS == 1) {
-            umma_commit(&empty[stage]);
-          } else {
-            umma_commit_mc(&empty[stage], MASK);  // the stage is free once every CTA of the cluster is done
-          }
+          umma_commit(&empty[stage]);
           any = true;
           if (++stage == C::STAGES) {
             stage = 0;
@@ -468,7 +445,7 @@ __global__ void __launch_bounds__(192, 1)
       // every MMA must be finished before TMEM is released
       if (any) {
         umma_commit(drain);
-        if (!mbar_wait(drain, 0, p.wait_ns)) record_error(p.err, DEV_WAIT_TIMEOUT_DRAIN);
+        if (!mbar_wait(drain, 0, kDrainWaitNs)) record_error(p.err, DEV_WAIT_TIMEOUT_DRAIN);
       }
     }
   } else {
@@ -525,11 +502,7 @@ __global__ void __launch_bounds__(192, 1)
   }
 
   tc_fence_before_sync();
-  if constexpr (CS > 1) {
-    cluster_sync_all();  // no peer touches this CTA's shared memory after this point
-  } else {
-    __syncthreads();
-  }
+  __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tbase, C::TMEM_COLS);
@@ -706,7 +679,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       if (any) {
         umma_commit_pair(drain);
-        if (!mbar_wait(drain, 0, p.wait_ns)) record_error(p.err, DEV_WAIT_TIMEOUT_DRAIN);
+        if (!mbar_wait(drain, 0, kDrainWaitNs)) record_error(p.err, DEV_WAIT_TIMEOUT_DRAIN);
       }
     }
   } else {
@@ -885,54 +858,19 @@ bool make_q_map(CUtensorMap* m, const void* base, int dh, int n_heads, int n_row
   return true;
 }
 
-template <int MT, int BN, int EPI, int CS, bool ALO = false>
+template <int MT, int BN, int EPI, bool ALO = false>
 static int launch_t(const CUtensorMap& ma, const CUtensorMap& mb, const CUtensorMap& ma2, const CUtensorMap& mb2,
                     const GemmParams& p, const EpiArgs& e, cudaStream_t st, int sms) {
   using C = GemmCfg<MT, BN, ALO>;
-  auto kern = gemm_tc_kernel<MT, BN, EPI, CS, ALO>;
+  auto kern = gemm_tc_kernel<MT, BN, EPI, ALO>;
   static bool attr_set = false;  // per instantiation
-  static int max_clusters = 0;
   if (!attr_set) {
     cudaError_t r = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (r != cudaSuccess) return r;
-    if (CS > 1) {
-      // how many clusters can be resident at once: the kernel is persistent
-      cudaLaunchConfig_t q = {};
-      q.gridDim = dim3(CS * (sms / CS), 1, 1);
-      q.blockDim = dim3(192, 1, 1);
-      q.dynamicSmemBytes = C::SMEM_BYTES;
-      cudaLaunchAttribute at[1];
-      at[0].id = cudaLaunchAttributeClusterDimension;
-      at[0].val.clusterDim.x = CS;
-      at[0].val.clusterDim.y = 1;
-      at[0].val.clusterDim.z = 1;
-      q.attrs = at;
-      q.numAttrs = 1;
-      int n = 0;
-      r = cudaOccupancyMaxActiveClusters(&n, kern, &q);
-      if (r != cudaSuccess) return r;
-      max_clusters = n > 0 ? n : 1;
-    }
     attr_set = true;
   }
-  if (CS == 1) {
-    const int grid = std::min(p.n_units, sms);
-    return launch_k(kern, dim3(grid), dim3(192), C::SMEM_BYTES, st, ma, mb, ma2, mb2, p, e);
-  }
-  const int clusters = std::min(p.n_units, max_clusters);
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(clusters * CS, 1, 1);
-  cfg.blockDim = dim3(192, 1, 1);
-  cfg.dynamicSmemBytes = C::SMEM_BYTES;
-  cfg.stream = st;
-  cudaLaunchAttribute at[1];
-  at[0].id = cudaLaunchAttributeClusterDimension;
-  at[0].val.clusterDim.x = CS;
-  at[0].val.clusterDim.y = 1;
-  at[0].val.clusterDim.z = 1;
-  cfg.attrs = at;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, ma, mb, ma2, mb2, p, e);
+  const int grid = std::min(p.n_units, sms);
+  return launch_k(kern, dim3(grid), dim3(192), C::SMEM_BYTES, st, ma, mb, ma2, mb2, p, e);
 }
 
 template <int BN, int EPI, bool ALO>
@@ -992,26 +930,19 @@ static int dispatch_tiling(const GemmTiling& t, const CUtensorMap& ma, const CUt
     }
     return -1;
   }
-  if (ma2) {  // hi + lo A: one 128-row tile per CTA, no cluster
+  if (ma2) {  // hi + lo A: one 128-row tile per CTA
     if constexpr (EPI == EPI_F32_STORE || EPI == EPI_F32_ADD || EPI == EPI_F32_ATOMIC || EPI == EPI_SWIGLU ||
                   EPI == EPI_READOUT || EPI == EPI_QKV_ROPE) {
-      if (t.mt == 1 && t.cs == 1 && t.bn == 128) return launch_t<1, 128, EPI, 1, true>(ma, mb, *ma2, mb2, p, e, st, sms);
-      if (t.mt == 1 && t.cs == 1 && t.bn == 256) return launch_t<1, 256, EPI, 1, true>(ma, mb, *ma2, mb2, p, e, st, sms);
+      if (t.mt == 1 && t.bn == 128) return launch_t<1, 128, EPI, true>(ma, mb, *ma2, mb2, p, e, st, sms);
+      if (t.mt == 1 && t.bn == 256) return launch_t<1, 256, EPI, true>(ma, mb, *ma2, mb2, p, e, st, sms);
     }
     return -1;
   }
-  if (t.cs == 1) {
-    if (t.mt == 1 && t.bn == 128) return launch_t<1, 128, EPI, 1>(ma, mb, ma, mb2, p, e, st, sms);
-    if (t.mt == 1 && t.bn == 256) return launch_t<1, 256, EPI, 1>(ma, mb, ma, mb2, p, e, st, sms);
-    if (t.mt == 2 && t.bn == 128) return launch_t<2, 128, EPI, 1>(ma, mb, ma, mb2, p, e, st, sms);
-    if (t.mt == 2 && t.bn == 256) return launch_t<2, 256, EPI, 1>(ma, mb, ma, mb2, p, e, st, sms);
-    if (t.mt == 4 && t.bn == 128) return launch_t<4, 128, EPI, 1>(ma, mb, ma, mb2, p, e, st, sms);
-  } else if (t.mt == 1) {
-    if (t.cs == 2 && t.bn == 128) return launch_t<1, 128, EPI, 2>(ma, mb, ma, mb2, p, e, st, sms);
-    if (t.cs == 2 && t.bn == 256) return launch_t<1, 256, EPI, 2>(ma, mb, ma, mb2, p, e, st, sms);
-    if (t.cs == 4 && t.bn == 128) return launch_t<1, 128, EPI, 4>(ma, mb, ma, mb2, p, e, st, sms);
-    if (t.cs == 4 && t.bn == 256) return launch_t<1, 256, EPI, 4>(ma, mb, ma, mb2, p, e, st, sms);
-  }
+  if (t.mt == 1 && t.bn == 128) return launch_t<1, 128, EPI>(ma, mb, ma, mb2, p, e, st, sms);
+  if (t.mt == 1 && t.bn == 256) return launch_t<1, 256, EPI>(ma, mb, ma, mb2, p, e, st, sms);
+  if (t.mt == 2 && t.bn == 128) return launch_t<2, 128, EPI>(ma, mb, ma, mb2, p, e, st, sms);
+  if (t.mt == 2 && t.bn == 256) return launch_t<2, 256, EPI>(ma, mb, ma, mb2, p, e, st, sms);
+  if (t.mt == 4 && t.bn == 128) return launch_t<4, 128, EPI>(ma, mb, ma, mb2, p, e, st, sms);
   return -1;
 }
 
@@ -1026,16 +957,14 @@ int launch_gemm(const GemmShape& s, int epi, const EpiArgs& e, const GemmTiling&
   p.N = N;
   p.K = K;
   p.nkb = K / 64;
-  if (t.cs != 1 && t.cs != 2 && t.cs != 4) return -1;
-  if (t.cs > 1 && t.mt != 1) return -1;
-  if (t.pair && (t.mt != 1 || t.cs != 1)) return -1;
-  p.n_mgroups = ceil_div(M, t.pair ? 256 : 128 * t.mt * t.cs);
+  if (t.pair && t.mt != 1) return -1;
+  p.n_mgroups = ceil_div(M, t.pair ? 256 : 128 * t.mt);
   p.n_ntiles = ceil_div(N, t.bn);
   p.k_splits = std::max(1, std::min(t.splits, p.nkb));
   p.n_units = p.n_mgroups * p.n_ntiles * p.k_splits;
   p.wait_ns = wait_ns;
   p.err = dev_err;
-  p.b_evict_first = (p.n_mgroups == 1 && (t.pair ? 256 : t.mt * t.cs * 128) >= M) ? 1 : 0;
+  p.b_evict_first = (p.n_mgroups == 1 && (t.pair ? 256 : t.mt * 128) >= M) ? 1 : 0;
   p.lo_row0 = s.lo_row0;
   p.b_const = s.b_const ? 1 : 0;
   // the last wave's tail: when the units leave the final wave part-filled,
@@ -1047,7 +976,7 @@ int launch_gemm(const GemmShape& s, int epi, const EpiArgs& e, const GemmTiling&
     const char* v = std::getenv("PCD_GEMM_TAIL");
     return !v || std::atoi(v) != 0;
   }();
-  if (tail_on && epi == EPI_SWIGLU && t.mt == 1 && t.cs == 1 && !t.pair && p.k_splits == 1 && t.bn > 64 &&
+  if (tail_on && epi == EPI_SWIGLU && t.mt == 1 && !t.pair && p.k_splits == 1 && t.bn > 64 &&
       N % t.bn == 0) {
     const int grid = std::min(p.n_units, sms);
     const int waves = p.n_units / grid, rest = p.n_units - waves * grid;
@@ -1065,7 +994,7 @@ int launch_gemm(const GemmShape& s, int epi, const EpiArgs& e, const GemmTiling&
   if (!make_map(&ma, s.a, M, K, s.a_ld, 128)) return -1;
   if (s.a_lo && !make_map(&ma2, s.a_lo, M, K, s.a_ld, 128)) return -1;
   const CUtensorMap* pa2 = s.a_lo ? &ma2 : nullptr;
-  if (!make_map(&mb, s.b, N, K, s.b_ld, t.pair ? t.bn / 2 : t.bn / t.cs)) return -1;
+  if (!make_map(&mb, s.b, N, K, s.b_ld, t.pair ? t.bn / 2 : t.bn)) return -1;
   if (p.n_wide < p.n_units) {
     if (!make_map(&mb2, s.b, N, K, s.b_ld, 64)) return -1;
   } else {
@@ -1095,42 +1024,28 @@ int launch_gemm(const GemmShape& s, int epi, const EpiArgs& e, const GemmTiling&
 GemmTiling choose_tiling(int M, int N, int K, int epi, int sms) {
   const int nkb = K / 64;
   const int mtiles = ceil_div(M, 128);
-  // clusters share B through L2 multicast, but every SM still takes the whole
-  // tile into its shared memory; measured on 825-row shapes they never beat
-  // single CTAs, so they are off unless PCD_GEMM_MAX_CS allows them
-  static const int max_cs = [] {
-    const char* e = std::getenv("PCD_GEMM_MAX_CS");
-    return e ? std::max(1, std::atoi(e)) : 1;
-  }();
   GemmTiling best;
   best.mt = 1;
   double best_t = 1e30;
-  for (int cs : {1, 2, 4}) {
-    if (cs > max_cs) continue;
-    if (cs > 1 && mtiles < cs) continue;  // a cluster needs that many M tiles to share B
-    for (int bn : {128, 256}) {
-      const int nt = ceil_div(N, bn);
-      const int groups = ceil_div(mtiles, cs);
-      const int max_split = (epi == EPI_F32_ATOMIC) ? std::max(1, std::min(16, nkb / 3)) : 1;
-      for (int sp = 1; sp <= max_split; ++sp) {
-        const int units = groups * nt * sp;       // each unit occupies cs SMs
-        const int slots = std::max(1, sms / cs);  // units running at once
-        const int kbs = ceil_div(nkb, sp);
-        // cycles per 64-deep k block: the MMA, or filling shared memory with
-        // the A and B tiles at ~55 B/clk per SM (measured with every SM loading)
-        const double mma = 128.0 * bn * 128.0 / 8192.0;
-        const double fill = (128.0 + bn) * 128.0 / 55.0;
-        // a unit's fixed cost: pipeline ramp, plus the fp32 atomics of a split-K epilogue
-        const double fixed = (epi == EPI_F32_ATOMIC) ? 7000.0 : 2500.0;
-        const double per_unit = kbs * std::max(mma, fill) + fixed + (cs > 1 ? 500.0 : 0.0);
-        const double tt = ceil_div(units, slots) * per_unit + (sp > 1 ? 400.0 : 0.0);
-        if (tt < best_t * 0.97) {
-          best_t = tt;
-          best.bn = bn;
-          best.splits = sp;
-          best.cs = cs;
-          best.pair = false;
-        }
+  for (int bn : {128, 256}) {
+    const int nt = ceil_div(N, bn);
+    const int max_split = (epi == EPI_F32_ATOMIC) ? std::max(1, std::min(16, nkb / 3)) : 1;
+    for (int sp = 1; sp <= max_split; ++sp) {
+      const int units = mtiles * nt * sp;
+      const int kbs = ceil_div(nkb, sp);
+      // cycles per 64-deep k block: the MMA, or filling shared memory with
+      // the A and B tiles at ~55 B/clk per SM (measured with every SM loading)
+      const double mma = 128.0 * bn * 128.0 / 8192.0;
+      const double fill = (128.0 + bn) * 128.0 / 55.0;
+      // a unit's fixed cost: pipeline ramp, plus the fp32 atomics of a split-K epilogue
+      const double fixed = (epi == EPI_F32_ATOMIC) ? 7000.0 : 2500.0;
+      const double per_unit = kbs * std::max(mma, fill) + fixed;
+      const double tt = ceil_div(units, std::max(1, sms)) * per_unit + (sp > 1 ? 400.0 : 0.0);
+      if (tt < best_t * 0.97) {
+        best_t = tt;
+        best.bn = bn;
+        best.splits = sp;
+        best.pair = false;
       }
     }
   }
@@ -1157,7 +1072,6 @@ GemmTiling choose_tiling(int M, int N, int K, int epi, int sms) {
           best_t = tt;
           best.bn = bn;
           best.splits = sp;
-          best.cs = 1;
           best.pair = true;
         }
       }

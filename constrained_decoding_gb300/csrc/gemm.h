@@ -63,9 +63,7 @@ struct GemmTiling {
   int mt = 1;       // 128-row M tiles per CTA work unit (1, 2 or 4)
   int bn = 256;     // N tile (128 or 256)
   int splits = 1;   // K splits (EPI_F32_ATOMIC only when > 1)
-  int cs = 1;       // cluster size along M (1, 2 or 4; mt must be 1): the CTAs of a
-                    // cluster share each B tile through TMA multicast
-  bool pair = false;  // a CTA pair (cta_group::2 MMA, M = 256) per work unit; mt = 1, cs = 1
+  bool pair = false;  // a CTA pair (cta_group::2 MMA, M = 256) per work unit; mt = 1
 };
 
 // Picks a tiling for the shape and epilogue on an `sms`-SM device.

@@ -5,7 +5,6 @@
 #include <string>
 
 #include <algorithm>
-#include <mutex>
 #include <vector>
 
 #include "gemm.h"
@@ -25,14 +24,9 @@ int device_sms() {
 
 extern "C" int pcd_k_gemm(const void* a, int M, int lda, const void* b, int N, int ldb, int K, int epi, void* out,
                           int ldo, int mt, int bn, int splits, int* dev_err, void* stream) {
-  // mt = 10 * cs + 1 asks for a cluster of cs CTAs sharing each B tile, mt = 3
-  // for a CTA pair sharing one MMA (see the header)
-  int cs = 1;
+  // mt = 3 asks for a CTA pair sharing one MMA (see the header)
   bool pair = false;
-  if (mt >= 10) {
-    cs = mt / 10;
-    mt = mt % 10;
-  } else if (mt == 3) {
+  if (mt == 3) {
     pair = true;
     mt = 1;
   }
@@ -46,7 +40,6 @@ extern "C" int pcd_k_gemm(const void* a, int M, int lda, const void* b, int N, i
     t.mt = mt;
     t.bn = bn;
     t.splits = splits < 1 ? 1 : splits;
-    t.cs = cs;
     t.pair = pair;
   }
   pcd::GemmShape s{a, M, lda, b, N, ldb, K};
@@ -65,7 +58,6 @@ extern "C" int pcd_k_gemm_split(const void* a_hi, const void* a_lo, int M, int l
   t.mt = 1;
   t.bn = bn;
   t.splits = splits < 1 ? 1 : splits;
-  t.cs = 1;
   pcd::GemmShape s{a_hi, M, lda, b, N, ldb, K, a_lo};
   pcd::EpiArgs e;
   e.out = out;
@@ -91,6 +83,14 @@ int readout_into(const void* h, int R, const void* w, int V, int d, const int32_
   if (!h || !w || !lse || R < 1 || V < 32 || V % 32 || d < 64 || d % 64 || n_cand < 0) return PCD_ERR_INVALID_ARG;
   if (n_cand > 0 && (!cand_row || !cand_tok || !z_out)) return PCD_ERR_INVALID_ARG;
   if (!scratch || scratch_bytes < readout_scratch_bytes(R, V, n_cand)) return PCD_ERR_INVALID_ARG;
+  // the gather list is copied from a host vector that lives only until this
+  // call returns, so a stream being captured into a graph is refused
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    return PCD_ERR_INVALID_ARG;
+  }
+  if (cap != cudaStreamCaptureStatusNone) return PCD_ERR_INVALID_ARG;
   for (int i = 0; i < n_cand; ++i)
     if (cand_row[i] < 0 || cand_row[i] >= R || cand_tok[i] < 0 || cand_tok[i] >= V) return PCD_ERR_TOKEN_RANGE;
   const int sms = device_sms();
@@ -148,29 +148,20 @@ extern "C" int pcd_k_readout(const void* h, int R, const void* w, int V, int d, 
 // The readout's scratch for callers that cannot allocate: a fixed array in
 // device global memory, shared by every call on a device.  Host code may not
 // use the symbol's address directly (in host code it names a host-side
-// stand-in), so its device address is looked up once per device.
+// stand-in), so every call looks up its device address with the caller's
+// device current.  Looking it up each time (a host-side table lookup that
+// allocates nothing) keeps the address right after cudaDeviceReset or a
+// re-created primary context, when the module is loaded again elsewhere.
 static __device__ __align__(256) unsigned char g_readout_scratch[PCD_K_READOUT_NOALLOC_MAX_BYTES];
 
 namespace {
-constexpr int kMaxDevices = 64;
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of g_readout_scratch on the current device (looked up on the
-// first call per device, with that device current).
 int noalloc_scratch(void** out) {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PCD_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_readout_scratch) != cudaSuccess || !p) {
-      cudaGetLastError();
-      return PCD_ERR_CUDA;
-    }
-    g_scratch_ptr[dev] = p;
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_readout_scratch) != cudaSuccess || !p) {
+    cudaGetLastError();
+    return PCD_ERR_CUDA;
   }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return PCD_OK;
 }
 }  // namespace

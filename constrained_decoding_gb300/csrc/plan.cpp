@@ -232,10 +232,15 @@ int compile_fields(const pcd_field* fields, int n_fields, int vocab, HostPlan* p
 
 int answer_line(const pcd_field& f, int label, const int32_t* sep, int n_sep, std::vector<int32_t>* line) {
   if (label < 0 || n_sep < 0 || (n_sep > 0 && !sep) || !f.cand_offsets || !f.cand_tokens) return PCD_ERR_INVALID_ARG;
+  if (f.n_scaffold < 0 || (f.n_scaffold > 0 && !f.scaffold) || f.n_cands < 0) return PCD_ERR_INVALID_ARG;
   int path = -1;
   for (int c = 0; c < f.n_cands && path < 0; ++c)
     if ((f.cand_label ? f.cand_label[c] : c) == label) path = c;
   if (path < 0) return PCD_ERR_INVALID_ARG;
+  // the chosen path's token range must be well formed before it is read
+  if (f.cand_offsets[0] != 0 || f.cand_offsets[path] < 0 || f.cand_offsets[path] > f.cand_offsets[path + 1] ||
+      f.cand_offsets[path + 1] > f.cand_offsets[f.n_cands])
+    return PCD_ERR_INVALID_ARG;
   line->assign(f.scaffold, f.scaffold + f.n_scaffold);
   line->insert(line->end(), f.cand_tokens + f.cand_offsets[path], f.cand_tokens + f.cand_offsets[path + 1]);
   line->insert(line->end(), sep, sep + n_sep);

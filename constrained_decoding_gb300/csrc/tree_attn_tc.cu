@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(192, 1)
       }
       // every MMA issued above has finished before TMEM is released
       umma_commit(drain);
-      if (!mbar_wait(drain, 0, wait_ns)) record_error(err, DEV_WAIT_TIMEOUT_MMA);
+      if (!mbar_wait(drain, 0, kDrainWaitNs)) record_error(err, DEV_WAIT_TIMEOUT_DRAIN);
     }
     __syncwarp();
   } else {
@@ -495,10 +495,10 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   if (warp == 0) {
     // nothing of this CTA's copies may still be landing when it exits
-    mbar_wait(q_full, 0, wait_ns);
+    mbar_wait(q_full, 0, kDrainWaitNs);
     for (int s = 0; s < kStages; ++s) {
-      if (kissued[s] > 0) mbar_wait(&k_full[s], static_cast<uint32_t>((kissued[s] - 1) & 1), wait_ns);
-      if (vissued[s] > 0) mbar_wait(&v_full[s], static_cast<uint32_t>((vissued[s] - 1) & 1), wait_ns);
+      if (kissued[s] > 0) mbar_wait(&k_full[s], static_cast<uint32_t>((kissued[s] - 1) & 1), kDrainWaitNs);
+      if (vissued[s] > 0) mbar_wait(&v_full[s], static_cast<uint32_t>((vissued[s] - 1) & 1), kDrainWaitNs);
     }
   }
   if (csk > 1) {

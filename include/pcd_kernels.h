@@ -27,10 +27,8 @@ extern "C" {
  * (configs: nn.Linear weights [out][in] as B, activations [tokens][in] as A).
  * K must be a multiple of 64, N a multiple of 32.  mt/bn/splits force a
  * tiling (mt in {1,2,4}, bn in {128,256}); mt = 0 lets the library choose;
- * mt = 21 or 41 runs clusters of 2 or 4 CTAs along M (one 128-row tile each)
- * that share every B tile through TMA multicast; mt = 3 runs CTA pairs that
- * share one tensor-core MMA of 256 rows (each CTA loads its 128 rows of A and
- * half of the B tile).
+ * mt = 3 runs CTA pairs that share one tensor-core MMA of 256 rows (each CTA
+ * loads its 128 rows of A and half of the B tile).
  * `dev_err` (device int, may be NULL) receives a nonzero code if a pipeline
  * wait times out. */
 int pcd_k_gemm(const void* a, int M, int lda, const void* b, int N, int ldb, int K, int epi, void* out, int ldo,
@@ -56,7 +54,10 @@ int pcd_k_gemm_split(const void* a_hi, const void* a_lo, int M, int lda, const v
  * z[cand_row][cand_tok], fp32.  `scratch` is a device buffer of at least
  * pcd_k_readout_scratch_bytes(R, V, n_cand) bytes that the call overwrites
  * (per-tile partial maxima and sums, the tile-sorted gather list).  Enqueued
- * on `stream`; the gather list is copied from host memory first. */
+ * on `stream`; the gather list is copied from host memory first, from a
+ * buffer that lives only until the call returns, so a call made while
+ * `stream` is being captured into a CUDA graph returns PCD_ERR_INVALID_ARG
+ * without enqueueing anything. */
 int64_t pcd_k_readout_scratch_bytes(int R, int V, int n_cand);
 int pcd_k_readout(const void* h, int R, const void* w, int V, int d, const int32_t* cand_row, const int32_t* cand_tok,
                   int n_cand, float* lse, float* z_out, void* scratch, int64_t scratch_bytes, int* dev_err,
@@ -72,10 +73,11 @@ int pcd_k_readout(const void* h, int R, const void* w, int V, int d, const int32
  * PCD_K_READOUT_NOALLOC_MAX_BYTES bytes that every GPU loading the library
  * holds until the process exits.  Inputs, outputs and errors are those of
  * pcd_k_readout; a problem whose pcd_k_readout_scratch_bytes(R, V, n_cand)
- * exceeds the array returns PCD_ERR_OOM without launching anything.  The
- * first call on a device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current; make that first call
- * before any stream capture.  No call allocates or frees memory.  Every call
+ * exceeds the array returns PCD_ERR_OOM without launching anything.  Every
+ * call looks up the array's device address (cudaGetSymbolAddress) with the
+ * caller's device current; the first call on a device also loads the
+ * library's device code there, so make that first call before any stream
+ * capture.  No call allocates or frees memory.  Every call
  * shares the one array and leaves its contents behind; each call writes every
  * scratch element it reads before reading it, so nothing needs clearing, but
  * calls that overlap on the GPU (other streams, other threads) race on the

@@ -87,31 +87,6 @@ def test_gemm_auto_tiling_large():
     assert (out - ref).abs().max().item() < 1e-3
 
 
-@pytest.mark.parametrize("M,N,K,cs,bn", [
-    (256, 256, 128, 2, 128),     # two full tiles sharing B
-    (313, 512, 1536, 4, 256),    # the branch shape: the 4th CTA of the cluster has no rows
-    (512, 1024, 512, 4, 128),
-    (77, 256, 192, 2, 256),      # second CTA idle
-    (1000, 768, 320, 2, 256),    # several cluster groups
-])
-def test_gemm_cluster_multicast(M, N, K, cs, bn):
-    out, ref, tol = _run(M, N, K, 0, 10 * cs + 1, bn, 1, seed=M)
-    err = (out - ref).abs().max().item()
-    assert err < tol * max(1.0, ref.abs().max().item()), err
-
-
-@pytest.mark.parametrize("cs,splits", [(2, 1), (4, 3)])
-def test_gemm_cluster_multicast_f32(cs, splits):
-    epi = 1 if splits == 1 else 2
-    out, ref, tol = _run(300, 512, 1024, epi, 10 * cs + 1, 256, splits, seed=5)
-    assert (out - ref).abs().max().item() < tol
-
-
-def test_gemm_cluster_swiglu():
-    out, ref, tol = _run(313, 1024, 256, 3, 41, 256, 1, seed=6)
-    assert (out - ref).abs().max().item() < tol
-
-
 @pytest.mark.parametrize("epi,bn,splits", [(1, 128, 1), (2, 256, 4), (3, 256, 1), (3, 128, 1)])
 def test_gemm_split_activation(epi, bn, splits):
     """A carried as fp16 hi + lo: the product matches the fp32 activation's

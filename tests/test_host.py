@@ -209,6 +209,66 @@ def test_answer_line_matches_the_oracle(lib):
     assert ei.value.code == -1
 
 
+def test_answer_line_rejects_malformed_fields(lib):
+    """A caller's malformed field is an error code, never a read out of
+    bounds: a NULL scaffold with a nonzero length, and candidate offsets that
+    run backwards or past the last candidate."""
+    import ctypes
+    from constrained_decoding_gb300 import _decls as D
+    toks = (ctypes.c_int32 * 4)(5, 6, 7, 8)
+    scaf = (ctypes.c_int32 * 2)(1, 2)
+
+    def field(scaffold, n_scaffold, offsets):
+        offs = (ctypes.c_int32 * len(offsets))(*offsets)
+        f = D.pcd_field(scaffold=scaffold, n_scaffold=n_scaffold, cand_tokens=toks, cand_offsets=offs,
+                        n_cands=len(offsets) - 1)
+        return f, offs
+
+    out = (ctypes.c_int32 * 16)()
+    good, k0 = field(scaf, 2, [0, 2, 4])
+    assert lib.pcd_answer_line(ctypes.byref(good), 1, None, 0, out, 16) == 4
+    assert list(out[:4]) == [1, 2, 7, 8]
+    for f, keep in (field(None, 2, [0, 2, 4]),        # no scaffold, two tokens claimed
+                    field(scaf, -1, [0, 2, 4]),       # negative scaffold length
+                    field(scaf, 2, [0, 3, 2]),        # path 1 runs backwards
+                    field(scaf, 2, [1, 2, 4])):       # offsets do not start at 0
+        assert lib.pcd_answer_line(ctypes.byref(f), 1, None, 0, out, 16) == -1
+    bad, k1 = field(scaf, 2, [0, 2, 4])
+    k1[1] = 9                                         # path 0 ends past the last candidate's end
+    assert lib.pcd_answer_line(ctypes.byref(bad), 0, None, 0, out, 16) == -1
+
+
+def test_weight_file_errors(lib, tmp_path):
+    """The .pcdw loader refuses a missing, truncated, padded, foreign or
+    differently shaped file with its error code before it touches a GPU."""
+    import dataclasses
+    import constrained_decoding_gb300.pcd as pcd
+    w = synth.make_weights(synth.model_config("tiny"), seed=0)
+    good = tmp_path / "tiny.pcdw"
+    synth.write_pcdw(w, str(good))
+    raw = good.read_bytes()
+
+    def code(data=None, cfg=None, path=None):
+        p = path or tmp_path / "case.pcdw"
+        if data is not None:
+            p.write_bytes(data)
+        with pytest.raises(pcd.PCDError) as ei:
+            pcd.pcd_load_weights(str(p), cfg)
+        return ei.value.code
+
+    assert code(path=tmp_path / "absent.pcdw") == -12
+    assert code(raw[:-4]) == -12                       # truncated
+    assert code(raw + b"\0" * 8) == -12                # trailing bytes
+    assert code(raw[:40]) == -12                       # shorter than the header
+    assert code(b"PCDX" + raw[4:]) == -12              # wrong magic
+    assert code(raw[:4] + (2).to_bytes(4, "little") + raw[8:]) == -12   # unknown version
+    assert code(raw[:8] + (3).to_bytes(4, "little") + raw[12:]) == -12  # unknown dtype
+    wider = dataclasses.replace(w.cfg, d_ff=w.cfg.d_ff + 8)
+    assert code(raw, cfg=wider) == -8                   # config does not match the header
+    untied = dataclasses.replace(w.cfg, tied_embedding=False)
+    assert code(raw, cfg=untied) == -8
+
+
 def test_schema_packing(lib):
     """A Schema (fields packed once into the C layout) compiles to the same
     plan as the list of fields, scoring rules and label maps included."""
