@@ -1,22 +1,26 @@
 #!/usr/bin/env python
 """Benchmark of the parallel constrained decoding (PCD) hot path on GB300.
 
-One step = one request of the 28-field triage workload: a Qwen2.5-1.5B-shaped
-random decoder (bf16), a 512-token prefix (uniform ids), 28 fields (10
-booleans, 18 four-way enums of 1-4 token labels, 8 scaffold tokens each):
-prefill the prefix into a KV cache, then one batched branch pass scores every
-field.  Inputs are seeded and synthetic; the weights (3.1 GB) are larger than
-L2, so every step streams them from HBM.
+Headline step = one request of the 28-field triage workload: a
+Qwen2.5-1.5B-shaped random decoder (bf16), a 512-token prefix (uniform ids),
+28 fields (10 booleans, 18 four-way enums of 1-4 token labels, 8 scaffold
+tokens each), prefix and branch rows in one forward pass.  Inputs are seeded
+and synthetic; the weights (3.1 GB) are larger than L2, so every step streams
+them from HBM.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
 `value` is requests/s with the prefix ids and the compiled schema resident in
 HBM; `e2e` is the same metric through the host-pointer C ABI (ids and fields
 from host memory, results back to host memory, copies inside the timed
-region).  With N > 1 (torchrun) every rank runs an independent replica on
-its own GPU (requests are independent: weak scaling, no collective on the
-data path).  `--impl reference` times the CPU oracle on the host cores on a
-bounded sample of the same workload.
+region).  `branch_pass` is the branch pass alone on a cached prefix (the pass
+a warm request runs), replayed as a graph and timed as a whole.  `configs`
+holds the other workloads: the 255-choice router (prefix 1024), the long
+document (prefix 8192, 29 fields) and batched serving of 64 requests at the
+Qwen2.5-7B shape, cold and warm.  With N > 1 (torchrun) every rank runs an
+independent replica on its own GPU (requests are independent: weak scaling,
+no collective on the data path).  `--impl reference` times the CPU oracle
+on the host cores on a bounded sample of the same workload.
 """
 from __future__ import annotations
 
@@ -35,7 +39,14 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "28-field requests/sec & p50 latency (ms); branch-pass HBM GB/s vs peak"
-WORKLOAD = "28-field triage request: Qwen2.5-1.5B-shaped decoder (bf16, random init), prefix 512, 28 fields"
+WORKLOADS = {
+    2: "28-field triage request: Qwen2.5-1.5B-shaped decoder (bf16, random init), prefix 512, 28 fields",
+    3: "255-choice router: Qwen2.5-1.5B-shaped decoder, prefix 1024, 1 field of 255 three-token labels "
+       "sharing a first token + 3 booleans",
+    4: "long document: Qwen2.5-1.5B-shaped decoder, prefix 8192, 28 triage fields + a 218-label line-ID field",
+    5: "batched serving: Qwen2.5-7B-shaped decoder (bf16, untied head), 64 requests, prefixes uniform in "
+       "[512, 4096], the 28-field schema each",
+}
 
 
 def parse_args():
@@ -44,8 +55,8 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", type=int, default=2, help="workload number (2: 28-field triage)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the router, long-document and 7B workloads")
     ap.add_argument("--only-timed", action="store_true",
                     help="run only the warm-up and timed steps (for a clean profiler launch list)")
     ap.add_argument("--mode", default="single", choices=["single", "two-pass"],
@@ -102,6 +113,10 @@ def read_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
 
 
+def host_cores():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+
+
 class ClockSampler:
     """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -151,10 +166,11 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# DRAM traffic (read + write bytes) of one launch of the dominant kernel, from
-# one ncu capture (profiles/gemm_gate_up_28field_1p5b.md: the 825-row launch
-# of the gate/up projection); reported only while the GEMM sources are the ones
-# that capture ran, else null.
+# DRAM traffic (read + write bytes) of one launch of a kernel, from one ncu
+# capture of it (the gate/up projection with its SwiGLU epilogue at 825 rows,
+# the single-pass 28-field request: dram__bytes_read.sum + dram__bytes_write.sum);
+# reported only while the GEMM sources hash to the ones that capture ran on,
+# else null.
 PROFILED_TRAFFIC = {
     "gemm_gate_up": {"bytes_per_launch": 57.631488e6 + 0.714752e6,
                      "sources": ("gemm.cu", "gemm.h", "ptx.cuh", "common.cuh"),
@@ -167,7 +183,7 @@ def profiled_traffic(kernel: str):
     if ent is None:
         return None
     import hashlib
-    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "constrained_decoding_gb300", "csrc")
+    csrc = os.path.join(ROOT, "constrained_decoding_gb300", "csrc")
     # same digest as `sha1sum <files> | sha1sum`
     lines = "".join(f"{hashlib.sha1(open(os.path.join(csrc, f), 'rb').read()).hexdigest()}  "
                     f"constrained_decoding_gb300/csrc/{f}\n" for f in ent["sources"])
@@ -176,34 +192,73 @@ def profiled_traffic(kernel: str):
     return ent["bytes_per_launch"]
 
 
-def work_model(cfg, Lp: int, T: int, R: int):
-    """Algorithmic work of one request (units counted once, no padding)."""
-    d, L, F, V = cfg.d_model, cfg.n_layers, cfg.d_ff, cfg.vocab
+# ------------------------------------------------------------ work models
+def layer_params(cfg):
+    d, F = cfg.d_model, cfg.d_ff
+    return dict(qkv=d * (cfg.q_dim + 2 * cfg.kv_dim), o=cfg.q_dim * d, mlp=3 * F * d)
+
+
+def request_work(cfg, Lp: int, T: int, R: int, n_anc: int, mode: str):
+    """Algorithmic work of one request (units counted once, no padding).
+
+    flops: every projection of every row (in the single pass the prefix rows
+    of the last layer need only their keys and values), causal prefix
+    attention, each branch token against the whole prefix plus its ancestors
+    (n_anc entries, itself included), and the readout rows against the
+    vocabulary.  bytes: the layer weights and the LM head once per pass, and
+    the prefix keys/values written once and read once."""
+    L, d, V = cfg.n_layers, cfg.d_model, cfg.vocab
+    lp = layer_params(cfg)
+    P = lp["qkv"] + lp["o"] + lp["mlp"]
     qd, kd = cfg.q_dim, cfg.kv_dim
-    w_qkv, w_o, w_mlp = d * (qd + 2 * kd), qd * d, 3 * F * d
-    layer_params = w_qkv + w_o + w_mlp
-    # prefill GEMMs: the last layer only needs its keys and values (QKV)
-    prefill_gemm_flops = 2.0 * Lp * (L * w_qkv + (L - 1) * (w_o + w_mlp))
-    prefill_attn_flops = 2.0 * 2 * (Lp * (Lp + 1) / 2) * qd * (L - 1)
-    branch_weight_bytes = 2.0 * L * layer_params
-    branch_gemm_flops = 2.0 * T * L * layer_params
-    branch_attn_bytes = 2.0 * Lp * L * 2 * kd           # prefix K and V, read once per request
-    readout_bytes = 2.0 * V * d
-    readout_flops = 2.0 * R * V * d
-    # single pass: every row through every layer, except the prefix rows of
-    # the last layer, which only need their keys and values
-    single_gemm_flops = 2.0 * (Lp + T) * L * layer_params - 2.0 * Lp * (w_o + w_mlp)
-    # the single pass's gate/up projection (with its SwiGLU epilogue): every row
-    # in all but the last layer, the branch rows there
-    single_gu_flops = 2.0 * d * 2 * F * ((L - 1) * (Lp + T) + T)
-    return dict(single_gu_flops=single_gu_flops, prefill_gemm_flops=prefill_gemm_flops, prefill_attn_flops=prefill_attn_flops,
-                branch_weight_bytes=branch_weight_bytes, branch_gemm_flops=branch_gemm_flops,
-                branch_attn_bytes=branch_attn_bytes, readout_bytes=readout_bytes, readout_flops=readout_flops,
-                single_gemm_flops=single_gemm_flops)
+    passes = 1 if mode == "single" else 2
+    gemm = 2.0 * (Lp + T) * L * P - 2.0 * Lp * (lp["o"] + lp["mlp"])
+    attn_prefix = 4.0 * qd * (Lp * (Lp + 1) / 2) * (L - 1)
+    attn_branch = 4.0 * qd * (T * Lp + n_anc) * L
+    readout = 2.0 * R * V * d
+    flops = gemm + attn_prefix + attn_branch + readout
+    weight_bytes = 2.0 * L * P
+    head_bytes = 2.0 * V * d
+    kv_bytes = 2.0 * Lp * L * 2 * kd
+    bytes_ = passes * weight_bytes + head_bytes + 2 * kv_bytes
+    # the gate/up projection of the single pass: every row in all but the last
+    # layer, the branch rows there (the dominant kernel's work)
+    gu_flops = 2.0 * d * 2 * cfg.d_ff * ((L - 1) * (Lp + T) + T)
+    # the branch pass alone on a cached prefix
+    branch_flops = 2.0 * T * L * P + attn_branch + readout
+    branch_bytes = weight_bytes + head_bytes + kv_bytes
+    return dict(flops=flops, bytes=bytes_, gu_flops=gu_flops, branch_flops=branch_flops, branch_bytes=branch_bytes,
+                weight_bytes=weight_bytes, head_bytes=head_bytes, kv_bytes=kv_bytes)
+
+
+def roofline_frac(flops, bytes_, seconds, peaks):
+    """max(bytes / HBM, flops / tensor peak) over the measured time."""
+    t_hbm = bytes_ / (peaks["hbm_gbs"] * 1e9)
+    t_tc = flops / (peaks["bf16_tflops"] * 1e12)
+    bound = "hbm" if t_hbm >= t_tc else "tensor"
+    return {"bound": bound, "roofline_ms": round(max(t_hbm, t_tc) * 1e3, 4), "frac": round(max(t_hbm, t_tc) / seconds, 4),
+            "hbm_ms": round(t_hbm * 1e3, 4), "tensor_ms": round(t_tc * 1e3, 4)}
+
+
+def oracle_flops(cfg, req):
+    """Work of the oracle's incremental mode on one request: the prefix once,
+    then each label's row (scaffold + all but its last token) on top of the
+    cache, one label at a time, with the full-vocabulary head at each of the
+    label's positions."""
+    L, d, V = cfg.n_layers, cfg.d_model, cfg.vocab
+    lp = layer_params(cfg)
+    P = lp["qkv"] + lp["o"] + lp["mlp"]
+    Lp = len(req.prefix)
+    fl = 2.0 * Lp * L * P + 4.0 * cfg.q_dim * Lp * (Lp + 1) / 2 * L
+    for f in req.fields:
+        for lab in f.labels:
+            n = len(f.scaffold) + len(lab) - 1
+            fl += 2.0 * n * L * P + 4.0 * cfg.q_dim * n * (Lp + n / 2) * L + 2.0 * len(lab) * V * d
+    return fl
 
 
 # --------------------------------------------------------- CPU oracle timing
-def time_oracle(weights, req, n_field_steps: int, warm_prefill: bool = True):
+def time_oracle(weights, req, n_field_steps: int):
     """The oracle as it stands on the host cores.  Sample: one prefill of the
     request's prefix plus `n_field_steps` fields (cycling through the schema);
     a request's time = prefill + sum over its fields of the measured mean time
@@ -214,20 +269,158 @@ def time_oracle(weights, req, n_field_steps: int, warm_prefill: bool = True):
     cache = orc.prefill(req.prefix)
     t_prefill = time.perf_counter() - t0
     per_kind = {}
-    order = list(range(len(req.fields)))
     for i in range(n_field_steps):
-        f = req.fields[order[i % len(order)]]
+        f = req.fields[i % len(req.fields)]
         t0 = time.perf_counter()
         orc.score_field(f, cache=cache)
         per_kind.setdefault(f.kind, []).append(time.perf_counter() - t0)
     mean_kind = {k: float(np.mean(v)) for k, v in per_kind.items()}
     fallback = float(np.mean([x for v in per_kind.values() for x in v]))
     t_req = t_prefill + sum(mean_kind.get(f.kind, fallback) for f in req.fields)
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
-    return t_req, t_prefill, per_kind, cores
+    return t_req, t_prefill, per_kind, host_cores()
 
 
 # ------------------------------------------------------------------- ours
+def event_times(stream, fn, n):
+    """Runs fn(i) n times on `stream` with a CUDA event after each; returns
+    the per-call milliseconds and the total."""
+    import torch
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n + 1)]
+    torch.cuda.synchronize()
+    evs[0].record(stream)
+    for i in range(n):
+        fn(i)
+        evs[i + 1].record(stream)
+    torch.cuda.synchronize()
+    return [evs[i].elapsed_time(evs[i + 1]) for i in range(n)], evs[0].elapsed_time(evs[n])
+
+
+def plan_sizes(pcd, fields, vocab):
+    s = pcd.pcd_plan_inspect(fields, vocab)
+    return s["T"], s["R"], s["NA"]
+
+
+def measure_single_request(pcd, model, cfg, req, stream, K, W, peaks, oracle_rate, n_pref=4, seed=11):
+    """One single-request workload: the single pass from device-resident ids
+    (req/s, p50, max-roofline fraction), the branch pass alone on a cached
+    prefix, and the oracle's time extrapolated from its measured rate."""
+    import torch
+    plan = pcd.pcd_plan_create(model, req.fields)
+    rng = np.random.default_rng(seed)
+    prefixes = [req.prefix] + [rng.integers(0, cfg.vocab, len(req.prefix)).astype(np.int32) for _ in range(n_pref - 1)]
+    ids = [torch.tensor(p, dtype=torch.int32, device="cuda") for p in prefixes]
+    out = torch.zeros(plan.result_floats, dtype=torch.float32, device="cuda")
+    step = lambda i: pcd.pcd_prefill_score_plan_device(model, ids[i % n_pref], plan, out)
+    for i in range(W):
+        step(i)
+    pcd.pcd_sync(model)
+    ms, total = event_times(stream, step, K)
+    pcd.pcd_sync(model)
+    T, R, NA = plan_sizes(pcd, req.fields, cfg.vocab)
+    wk = request_work(cfg, len(req.prefix), T, R, NA, "single")
+    per_req_s = total / K / 1e3
+    cache = pcd.pcd_prefill_device(model, ids[0])
+    bp = lambda i: pcd.pcd_score_plan_device(model, cache, plan, out)
+    for i in range(W):
+        bp(i)
+    bms, btotal = event_times(stream, bp, K)
+    pcd.pcd_sync(model)
+    cache.free()
+    plan.free()
+    b_s = btotal / K / 1e3
+    ofl = oracle_flops(cfg, req)
+    return {
+        "req_per_s": round(1.0 / per_req_s, 3), "p50_latency_ms": round(statistics.median(ms), 4),
+        "fields_per_s": round(len(req.fields) / per_req_s, 1), "ms_per_request": round(per_req_s * 1e3, 4),
+        "prefix_len": len(req.prefix), "fields": len(req.fields), "branch_tokens": T, "readout_rows": R,
+        "roofline": {**roofline_frac(wk["flops"], wk["bytes"], per_req_s, peaks),
+                     "flops": wk["flops"], "bytes": wk["bytes"]},
+        "branch_pass": {"ms": round(b_s * 1e3, 4), "hbm_gbs": round(wk["branch_bytes"] / b_s / 1e9, 1),
+                        "frac_of_measured_hbm": round(wk["branch_bytes"] / b_s / 1e9 / peaks["hbm_gbs"], 4),
+                        "max_roofline": roofline_frac(wk["branch_flops"], wk["branch_bytes"], b_s, peaks)},
+        "cpu_baseline": {"value": round(oracle_rate / ofl, 6), "unit": "req/s", "kind": "oracle", "cores": host_cores(),
+                         "sample": f"extrapolated: {ofl / 1e12:.2f} TFLOP of the oracle's incremental mode at its "
+                                   f"measured {oracle_rate / 1e9:.1f} GFLOP/s on the 28-field sample"},
+    }
+
+
+def measure_batched(pcd, K, W, peaks, oracle_rate):
+    """64 requests at the Qwen2.5-7B shape through the host-pointer ABI, all
+    submitted at t = 0: cold (a full prefill per request, then one batched
+    branch pass) and warm (the shared 512-token schema head cached once, each
+    request's tail extending it, then the batched branch pass).  Every request
+    completes when the batched pass does, so p50 = the batch's wall time."""
+    import torch
+    import synth
+    cfg = synth.model_config("7b")
+    t0 = time.time()
+    w = synth.make_weights(cfg, seed=0)
+    t_draw = time.time() - t0
+    model = pcd.pcd_load_weights_host(w)
+    del w
+    reqs = synth.make_requests(5)
+    schema = pcd.Schema(reqs[0].fields)
+    n = len(reqs)
+
+    def cold(_):
+        caches = [pcd.pcd_prefill(model, r.prefix) for r in reqs]
+        pcd.pcd_score_batch(model, caches, [schema] * n)
+        for c in caches:
+            c.free()
+
+    head = pcd.pcd_prefill(model, reqs[0].prefix[:reqs[0].head_len])
+
+    def warm(_):
+        caches = [pcd.pcd_prefill_extend(model, head, r.prefix[r.head_len:]) for r in reqs]
+        pcd.pcd_score_batch(model, caches, [schema] * n)
+        for c in caches:
+            c.free()
+
+    out = {}
+    T, R, NA = plan_sizes(pcd, reqs[0].fields, cfg.vocab)
+    for name, fn in (("cold", cold), ("warm", warm)):
+        for i in range(W):
+            fn(i)
+        torch.cuda.synchronize()
+        wall = []
+        for i in range(K):
+            t = time.perf_counter()
+            fn(i)
+            wall.append(time.perf_counter() - t)
+        flops = bytes_ = 0.0
+        for r in reqs:
+            Lp = len(r.prefix) if name == "cold" else len(r.prefix) - r.head_len
+            base = 0 if name == "cold" else r.head_len
+            wk = request_work(cfg, len(r.prefix), T, R, NA, "two-pass")
+            # the prefill of this request's rows (attending to the cached head when warm)
+            lp = layer_params(cfg)
+            P = lp["qkv"] + lp["o"] + lp["mlp"]
+            flops += 2.0 * Lp * cfg.n_layers * P + 4.0 * cfg.q_dim * Lp * (base + (Lp + 1) / 2) * cfg.n_layers
+            flops += wk["branch_flops"]
+            bytes_ += wk["kv_bytes"] * 2
+        # algorithmic minimum: the weights once for all prefill rows and once
+        # for the branch rows, the LM head once, every request's K/V written and read
+        bytes_ += 2 * wk["weight_bytes"] + wk["head_bytes"]
+        sec = statistics.median(wall)
+        out[name] = {"req_per_s": round(n / sec, 3), "p50_latency_ms": round(sec * 1e3, 2),
+                     "fields_per_s": round(n * len(reqs[0].fields) / sec, 1), "batch_wall_ms": round(sec * 1e3, 2),
+                     "roofline": {**roofline_frac(flops, bytes_, sec, peaks), "flops": flops}}
+    head.free()
+    model.free()
+    ofl = sum(oracle_flops(cfg, r) for r in reqs) / n
+    out.update({"requests": n, "prefix_len_range": [int(min(len(r.prefix) for r in reqs)),
+                                                     int(max(len(r.prefix) for r in reqs))],
+                "head_len": reqs[0].head_len, "branch_tokens_per_request": T, "weights_drawn_s": round(t_draw, 1),
+                "note": "host-pointer ABI (pcd_prefill / pcd_prefill_extend per request, one pcd_score_batch); "
+                        "wall clock per batch of 64",
+                "cpu_baseline": {"value": round(oracle_rate / ofl, 7), "unit": "req/s", "kind": "oracle",
+                                 "cores": host_cores(),
+                                 "sample": f"extrapolated: {ofl / 1e12:.1f} TFLOP per request (oracle incremental "
+                                           f"mode, cold) at the rate measured on the 1.5B 28-field sample "
+                                           f"({oracle_rate / 1e9:.1f} GFLOP/s)"}})
+    return out
+
+
 def run_ours(args):
     import torch
     import synth
@@ -236,10 +429,9 @@ def run_ours(args):
     ws, rank, local = dist_info()
     dist = dist_init(ws)
     torch.cuda.set_device(local)
-    from synth.shapes import CONFIG_MODEL
-    cfg = synth.model_config(CONFIG_MODEL[args.config])
+    cfg = synth.model_config("1.5b")
     weights = synth.make_weights(cfg, seed=0)
-    req = synth.make_request(args.config)
+    req = synth.make_request(2)
     stream = torch.cuda.Stream()          # a non-default stream: passes run as CUDA graphs
     torch.cuda.set_stream(stream)
     model = pcd.pcd_load_weights_host(weights, stream=stream)
@@ -260,8 +452,8 @@ def run_ours(args):
         pcd.pcd_prefill_score_plan_device(model, ids_dev[i % n_pref], plan, out)
 
     step = step_single if args.mode == "single" else step_two_pass
-
-    for i in range(max(args.warmup, 3)):
+    W = max(args.warmup, 3)
+    for i in range(W):
         step(i)
     pcd.pcd_sync(model)
 
@@ -287,36 +479,56 @@ def run_ours(args):
     total_s = evs[0].elapsed_time(evs[K]) / 1e3
     total_s = max_over_ranks(dist, total_s)
     clocks = clk.summary()
+    ms_per_step = total_s * 1e3 / K
+    T, R, NA = plan_sizes(pcd, req.fields, cfg.vocab)
+    peaks = read_peaks()
+
     # the other execution mode, same workload, for context
     other = step_two_pass if step is step_single else step_single
     for i in range(3):
         other(i)
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(K):
-        other(i)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    other_ms = e0.elapsed_time(e1) / K
+    other_ms = event_times(stream, other, K)[1] / K
 
-    # ---- per-kernel-class times over the same workload (profiled pass)
+    # ---- per-kernel-class times: the same passes replayed as graphs that also
+    # hold an event record around every launch (each replay synchronised)
     pcd.pcd_profile_enable(model, True)
+    step(0)
+    pcd.pcd_profile_read(model)            # the first call captures the profiled graph
     for i in range(K):
         step(i)
     prof = pcd.pcd_profile_read(model)
     pcd.pcd_profile_enable(model, False)
     launches_per_step = sum(n for n, _ in prof.values()) / K
-    # the same for the other mode (its branch pass, for the HBM figure below)
+    cls_ms = {k: v[1] / K for k, v in prof.items()}
+    classes_sum = sum(cls_ms.values())
+
+    # ---- the branch pass alone on a cached 512-token prefix (what a warm
+    # request and first field first's second round run): graph replays timed
+    # as a whole, no per-launch events
+    wk = request_work(cfg, len(req.prefix), T, R, NA, args.mode)
+    cache = pcd.pcd_prefill_device(model, ids_dev[0])
+    bp = lambda i: pcd.pcd_score_plan_device(model, cache, plan, out)
+    for i in range(3):
+        bp(i)
+    b_ms, b_total = event_times(stream, bp, K)
+    pcd.pcd_sync(model)
+    b_s = b_total / K / 1e3
+    branch_gbs = wk["branch_bytes"] / b_s / 1e9
+    # and its kernel classes, profiled the same way as the step
     pcd.pcd_profile_enable(model, True)
+    bp(0)
+    pcd.pcd_profile_read(model)
     for i in range(K):
-        other(i)
-    prof_other = pcd.pcd_profile_read(model)
+        bp(i)
+    bprof = pcd.pcd_profile_read(model)
     pcd.pcd_profile_enable(model, False)
+    cache.free()
+    b_cls = {k: round(v[1] / K, 4) for k, v in bprof.items() if v[0]}
 
     # ---- end to end through the host-pointer C ABI; the schema is packed
     # once (pcd.Schema), as a server scoring one schema per request does
     fields = pcd.Schema(req.fields)
+
     def e2e_step(i):
         if args.mode == "single":
             res, st = pcd.pcd_prefill_score(model, prefixes[i % n_pref], fields, with_stats=True)
@@ -363,12 +575,7 @@ def run_ours(args):
                          "extra_latency_vs_e2e": round(fff_p50 / statistics.median(e2e_ms) - 1.0, 4),
                          "note": "host-pointer ABI per request: prefix + field 1, then answer line + 27 fields"}
 
-    # ---- roofline of the dominant kernel class
-    T, R = st["branch_tokens"], st["readout_rows"]
-    wm = work_model(cfg, len(req.prefix), T, R)
-    peaks = read_peaks()
-    cls_ms = {k: v[1] / K for k, v in prof.items()}       # per request
-    # the kernel with the largest share of the step (classes that are one kernel each)
+    # ---- roofline of the dominant kernel class (the largest share of the step)
     candidates = (("gemm_gate_up", "attn_branch", "readout") if args.mode == "single" else
                   ("gemm_prefill", "gemm_branch", "attn_prefill", "attn_branch", "readout"))
     dominant = max(candidates, key=lambda k: cls_ms[k])
@@ -377,50 +584,32 @@ def run_ours(args):
         ms = cls_ms[cls]
         n_launch = prof[cls][0] / K
         if cls == "gemm_prefill":
-            work, bound = wm["prefill_gemm_flops"], "tensor"
+            L = cfg.n_layers
+            lp = layer_params(cfg)
+            work = 2.0 * len(req.prefix) * (L * lp["qkv"] + (L - 1) * (lp["o"] + lp["mlp"]))
+            bound = "tensor"
         elif cls == "gemm_gate_up":
-            work, bound = wm["single_gu_flops"], "tensor"
-        elif cls == "gemm_single":
-            t_hbm = wm["branch_weight_bytes"] / (peaks["hbm_gbs"] * 1e9)
-            t_tc = wm["single_gemm_flops"] / (peaks["bf16_tflops"] * 1e12)
-            work, bound = (wm["branch_weight_bytes"], "hbm") if t_hbm >= t_tc else (wm["single_gemm_flops"], "tensor")
+            work, bound = wk["gu_flops"], "tensor"
         elif cls == "gemm_branch":
-            # at the ridge: report the bound with the larger roofline time
-            t_hbm = wm["branch_weight_bytes"] / (peaks["hbm_gbs"] * 1e9)
-            t_tc = wm["branch_gemm_flops"] / (peaks["bf16_tflops"] * 1e12)
-            work, bound = (wm["branch_weight_bytes"], "hbm") if t_hbm >= t_tc else (wm["branch_gemm_flops"], "tensor")
-        elif cls == "attn_prefill":
-            work, bound = wm["prefill_attn_flops"], "tensor"
-        elif cls == "attn_branch":
-            work, bound = wm["branch_attn_bytes"], "hbm"
+            work, bound = 2.0 * T * wk["weight_bytes"] / 2, "tensor"
+        elif cls in ("attn_prefill", "attn_branch"):
+            work, bound = wk["kv_bytes"], "hbm"
         else:
-            work, bound = wm["readout_bytes"], "hbm"
+            work, bound = wk["head_bytes"], "hbm"
         if bound == "hbm":
             achieved = work / (ms / 1e3) / 1e9
             peak, unit = peaks["hbm_gbs"], "GB/s"
         else:
             achieved = work / (ms / 1e3) / 1e12
             peak, unit = peaks["bf16_tflops"], "TFLOP/s"
+        traffic = profiled_traffic(cls)
         return {"kernel": cls, "bound": bound, "achieved": round(achieved, 2), "peak": peak, "unit": unit,
-                "frac": round(achieved / peak, 4), "traffic": profiled_traffic(cls), "launches_per_step": n_launch,
-                "ms_per_step": round(ms, 4), "algorithmic_per_step": work,
-                "peak_source": peaks["source"] + (" (burst)" if unit == "TFLOP/s" else "")}
+                "frac": round(achieved / peak, 4), "traffic": traffic, "launches_per_step": n_launch,
+                "ms_per_launch": round(ms / n_launch, 5), "ms_per_step": round(ms, 4),
+                "algorithmic_per_step": work, "algorithmic_per_launch": work / n_launch,
+                "peak_source": peaks["source"] + (" (burst)" if unit == "TFLOP/s" else " (copy)")}
 
     roofline = roof(dominant)
-    # HBM GB/s of the pass that streams the weights for the branch rows (the
-    # metric's second half): weights + prefix KV + E over that pass's kernels
-    # (in single-pass mode the prefix rows share the same weight stream)
-    branch_ms = (cls_ms["gemm_branch"] + cls_ms["gemm_single"] + cls_ms["gemm_gate_up"] + cls_ms["attn_branch"] +
-                 cls_ms["readout"])
-    if args.mode == "single":
-        branch_ms += cls_ms["attn_prefill"]
-    branch_bytes = wm["branch_weight_bytes"] + wm["branch_attn_bytes"] + wm["readout_bytes"]
-    branch_gbs = branch_bytes / (branch_ms / 1e3) / 1e9
-    # the two-pass branch pass alone: weights + prefix KV + E over its kernels
-    two = prof if args.mode == "two-pass" else prof_other
-    two_ms = {k: v[1] / K for k, v in two.items()}
-    two_branch_ms = two_ms["gemm_branch"] + two_ms["attn_branch"] + two_ms["readout"]
-    two_branch_gbs = branch_bytes / (two_branch_ms / 1e3) / 1e9 if two_branch_ms > 0 else None
 
     n_total = sum_over_ranks(dist, K)
     value = n_total / total_s
@@ -430,8 +619,8 @@ def run_ours(args):
         "unit": "req/s",
         "n_gpus": ws,
         "steps": K,
-        "warmup": max(args.warmup, 3),
-        "ms_per_step": round(total_s * 1e3 / K, 4),
+        "warmup": W,
+        "ms_per_step": round(ms_per_step, 4),
         "p50_latency_ms": round(statistics.median(step_ms), 4),
         "fields_per_s": round(value * len(req.fields), 1),
         "higher_is_better": True,
@@ -441,21 +630,25 @@ def run_ours(args):
         "dtype_note": "bf16 weights held exactly as fp16 tensor-core operands (values >= 2^-17), fp32 accumulation; "
                       "activations fp16 with fp16 remainders at the rounding points that need them",
         "data": "synthetic (seeded random-init weights and token ids)",
-        "config": {"workload": WORKLOAD, "prefix_len": len(req.prefix), "fields": len(req.fields),
+        "config": {"workload": WORKLOADS[2], "prefix_len": len(req.prefix), "fields": len(req.fields),
                    "branch_tokens": T, "readout_rows": R, "requests_per_step": 1, "mode": args.mode,
                    "l2": "inputs larger than L2 (3.1 GB of weights streamed every step)",
                    "parallelism": f"replicas x{ws}"},
         "roofline": roofline,
+        "request_roofline": {**roofline_frac(wk["flops"], wk["bytes"], ms_per_step / 1e3, peaks),
+                             "flops": wk["flops"], "bytes": wk["bytes"]},
         "branch_pass": {"hbm_gbs": round(branch_gbs, 1), "frac_of_measured": round(branch_gbs / peaks["hbm_gbs"], 4),
-                        "frac_of_8tbs_spec": round(branch_gbs / 8000.0, 4), "ms_per_request": round(branch_ms, 4),
-                        "algorithmic_bytes": branch_bytes},
+                        "frac_of_8tbs_spec": round(branch_gbs / 8000.0, 4), "ms_per_pass": round(b_s * 1e3, 4),
+                        "p50_ms": round(statistics.median(b_ms), 4), "algorithmic_bytes": wk["branch_bytes"],
+                        "max_roofline": roofline_frac(wk["branch_flops"], wk["branch_bytes"], b_s, peaks),
+                        "kernel_ms_per_pass": b_cls,
+                        "note": f"{T} branch rows scored on a cached {len(req.prefix)}-token prefix "
+                                "(pcd_score_plan_device), graph replays timed as a whole; bytes = layer weights + "
+                                "LM head + prefix K/V, each read once"},
         "kernel_ms_per_step": {k: round(v, 4) for k, v in cls_ms.items()},
+        "kernel_classes_vs_step": round(classes_sum / ms_per_step, 4),
         "other_mode": {"mode": "two-pass" if args.mode == "single" else "single", "ms_per_step": round(other_ms, 4),
                        "req_per_s": round(1e3 / other_ms, 3)},
-        "two_pass_branch_pass": {"hbm_gbs": round(two_branch_gbs, 1) if two_branch_gbs else None,
-                                 "frac_of_measured": round(two_branch_gbs / peaks["hbm_gbs"], 4) if two_branch_gbs else None,
-                                 "ms_per_request": round(two_branch_ms, 4), "algorithmic_bytes": branch_bytes,
-                                 "note": "the branch pass of two-pass mode (313 rows on the cached prefix), kernels timed one by one"},
         "e2e": {"value": round(n_total / e2e_s, 3), "unit": "req/s", "p50_latency_ms": round(statistics.median(e2e_ms), 4),
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
                 "note": "host ids in, host results out, per request; the schema packed once (pcd.Schema)"},
@@ -463,16 +656,43 @@ def run_ours(args):
         "gpu_launches": int(round(launches_per_step * K)),
         "clocks": clocks,
     }
+    # a kernel class is a subset of a step's launches and the branch pass's
+    # classes a subset of its launches: neither may exceed the time it is part of
+    assert max(cls_ms.values()) <= ms_per_step, (cls_ms, ms_per_step)
+    assert max(b_cls.values()) <= b_s * 1e3, (b_cls, b_s)
+
+    oracle_rate = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         t_req, t_pf, per_kind, cores = time_oracle(weights, req, n_field_steps=2)
         line["cpu_baseline"] = {"value": round(1.0 / t_req, 5), "unit": "req/s", "cores": cores, "kind": "oracle",
                                 "sample": f"oracle (numpy fp32) prefill of the 512-token prefix ({t_pf:.2f} s) + "
                                           f"2 fields ({', '.join(f'{k}: {np.mean(v):.2f} s' for k, v in per_kind.items())}); "
                                           "request time = prefill + 28 fields at the measured per-kind mean"}
+        oracle_rate = oracle_flops(cfg, req) / t_req
+    for x in (plan,):
+        x.free()
+
+    if not args.no_configs and ws == 1:
+        rate = oracle_rate or 0.0
+        confs = {}
+        for c in (3, 4):
+            r = synth.make_request(c)
+            confs[str(c)] = {"workload": WORKLOADS[c],
+                             **measure_single_request(pcd, model, cfg, r, stream, min(K, 10), 3, peaks, rate or 1.0)}
+            if not rate:
+                confs[str(c)].pop("cpu_baseline")
+        model.free()
+        model = None
+        del weights
+        c5 = measure_batched(pcd, 3, 1, peaks, rate or 1.0)
+        if not rate:
+            c5.pop("cpu_baseline")
+        confs["5"] = {"workload": WORKLOADS[5], **c5}
+        line["configs"] = confs
     if rank == 0:
         print(json.dumps(line), flush=True)
-    for x in (plan, model):
-        x.free()
+    if model is not None:
+        model.free()
 
 
 # -------------------------------------------------------------- reference
@@ -481,10 +701,9 @@ def run_reference(args):
     if rank != 0:
         return
     import synth
-    from synth.shapes import CONFIG_MODEL
-    cfg = synth.model_config(CONFIG_MODEL[args.config])
+    cfg = synth.model_config("1.5b")
     weights = synth.make_weights(cfg, seed=0)
-    req = synth.make_request(args.config)
+    req = synth.make_request(2)
     from oracle import Oracle
     orc = Oracle(weights, np.float32)
     t0 = time.perf_counter()
@@ -507,7 +726,6 @@ def run_reference(args):
     fb = float(np.mean(step_s))
     t_req = t_prefill + sum(mean_kind.get(f.kind, fb) for f in fields)
     value = 1.0 / t_req
-    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     sample = (f"each step scores one field of the request with the oracle (numpy fp32) on the prefix cache; the "
               f"prefix prefill ({t_prefill:.2f} s) is timed once; request time = prefill + 28 fields at the "
               f"measured per-kind mean")
@@ -516,9 +734,10 @@ def run_reference(args):
         "warmup": args.warmup, "ms_per_step": round(wall * 1e3 / args.steps, 3),
         "p50_latency_ms": round(t_req * 1e3, 1), "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "f32", "data": "synthetic (seeded random-init weights and token ids)",
-        "config": {"workload": WORKLOAD, "prefix_len": len(req.prefix), "fields": len(fields)},
+        "config": {"workload": WORKLOADS[2], "prefix_len": len(req.prefix), "fields": len(fields)},
         "impl": "reference",
-        "cpu_baseline": {"value": round(value, 5), "unit": "req/s", "kind": "oracle", "cores": cores, "sample": sample},
+        "cpu_baseline": {"value": round(value, 5), "unit": "req/s", "kind": "oracle", "cores": host_cores(),
+                         "sample": sample},
         "e2e": {"value": round(value, 5), "unit": "req/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)

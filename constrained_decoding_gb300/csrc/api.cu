@@ -125,7 +125,7 @@ struct PlanView {
                           static_cast<const void*>(tile_chunk_off), static_cast<const void*>(tile_keys),
                           static_cast<const void*>(tile_mask)})
       k.push_back(reinterpret_cast<int64_t>(q));
-    for (int x : {ro_tiling.mt, ro_tiling.bn, ro_tiling.splits, ro_tiling.cs, static_cast<int>(ro_tiling.pair)})
+    for (int x : {ro_tiling.mt, ro_tiling.bn, ro_tiling.splits, static_cast<int>(ro_tiling.pair)})
       k.push_back(x);
   }
 };
@@ -166,6 +166,12 @@ struct pcd_model {
   std::vector<cudaEvent_t> ev_pool;
   size_t ev_next = 0;
   std::vector<std::tuple<int, cudaEvent_t, cudaEvent_t>> prof_rec;
+  // profiled graphs: the (class, start, end) event pairs each one records;
+  // after every replay of one the stream is synchronised and its pairs are
+  // added to prof_n / prof_ms
+  std::map<std::vector<int64_t>, std::vector<std::tuple<int, cudaEvent_t, cudaEvent_t>>> graph_prof;
+  int prof_n[PCD_PROF_CLASSES] = {};
+  double prof_ms[PCD_PROF_CLASSES] = {};
   cudaEvent_t ev_a = nullptr, ev_b = nullptr, ev_c = nullptr;
   // CUDA graphs of whole passes, keyed by everything a pass's launches bake in
   bool graphs = true;
@@ -271,28 +277,51 @@ int timed(pcd_model* m, int cls, Fn&& launch) {
 void drop_graphs(pcd_model* m) {
   for (auto& kv : m->graph_cache) cudaGraphExecDestroy(kv.second.second);
   m->graph_cache.clear();
+  m->graph_prof.clear();
+}
+
+// After a replay of a profiled graph: waits for it and adds its event pairs.
+int collect_graph_prof(pcd_model* m, const std::vector<std::tuple<int, cudaEvent_t, cudaEvent_t>>& rec) {
+  PCD_CUDA(cudaStreamSynchronize(m->stream));
+  for (const auto& r : rec) {
+    float t = 0.f;
+    PCD_CUDA(cudaEventElapsedTime(&t, std::get<1>(r), std::get<2>(r)));
+    m->prof_n[std::get<0>(r)]++;
+    m->prof_ms[std::get<0>(r)] += t;
+  }
+  return PCD_OK;
 }
 
 // Runs `record` (a sequence of launches on the model stream) as a CUDA graph:
 // captured on first use of `key`, replayed afterwards.  `record` must not
-// allocate.  Without graphs (disabled, or profiling) the launches run directly.
+// allocate.  Without graphs the launches run directly.  When profiling, the
+// graph also holds the event records that bracket each launch (a separate
+// graph per key); it is replayed like any other and synchronised after each
+// replay, so its launches keep the graph's launch path and are timed in it.
 template <class Fn>
-int with_graph(pcd_model* m, const std::vector<int64_t>& key, Fn&& record) {
-  if (!m->graphs || m->prof) return record();
+int with_graph(pcd_model* m, const std::vector<int64_t>& key0, Fn&& record) {
+  if (!m->graphs) return record();
+  std::vector<int64_t> key = key0;
+  if (m->prof) key.push_back(-1);  // profiled variant
   auto it = m->graph_cache.find(key);
   if (it != m->graph_cache.end()) {
     if (it->second.first == g_alloc_epoch) {
       PCD_CUDA(cudaGraphLaunch(it->second.second, m->stream));
+      if (m->prof) return collect_graph_prof(m, m->graph_prof[key]);
       return PCD_OK;
     }
     cudaGraphExecDestroy(it->second.second);
     m->graph_cache.erase(it);
+    m->graph_prof.erase(key);
   }
   if (m->graph_cache.size() >= 64) drop_graphs(m);
+  const size_t rec0 = m->prof_rec.size();
   PCD_CUDA(cudaStreamBeginCapture(m->stream, cudaStreamCaptureModeThreadLocal));
   const int rc = record();
   cudaGraph_t graph = nullptr;
   const cudaError_t ec = cudaStreamEndCapture(m->stream, &graph);
+  std::vector<std::tuple<int, cudaEvent_t, cudaEvent_t>> rec(m->prof_rec.begin() + rec0, m->prof_rec.end());
+  m->prof_rec.resize(rec0);
   if (rc != PCD_OK) {
     if (graph) cudaGraphDestroy(graph);
     cudaGetLastError();
@@ -305,6 +334,10 @@ int with_graph(pcd_model* m, const std::vector<int64_t>& key, Fn&& record) {
   if (ei != cudaSuccess) return fail(PCD_ERR_CUDA, std::string("graph instantiate: ") + cudaGetErrorString(ei));
   m->graph_cache[key] = {g_alloc_epoch, exec};
   PCD_CUDA(cudaGraphLaunch(exec, m->stream));
+  if (m->prof) {
+    m->graph_prof[key] = rec;
+    return collect_graph_prof(m, m->graph_prof[key]);
+  }
   return PCD_OK;
 }
 
@@ -322,9 +355,8 @@ int gemm(pcd_model* m, int cls, const void* A, int M, int lda, const act_t* B, i
   pcd::GemmTiling t;
   if (it == m->tilings.end()) {
     t = pcd::choose_tiling(M, N, K, key_epi, m->sms);
-    if (A_lo) {  // the hi + lo form runs one 128-row tile per CTA, no cluster
+    if (A_lo) {  // the hi + lo form runs one 128-row tile per CTA
       t.mt = 1;
-      t.cs = 1;
     }
     m->tilings[key] = t;
   } else {
@@ -369,7 +401,6 @@ int gemm_qkv_rope(pcd_model* m, int cls, const act_t* A, int M, const act_t* W, 
     t.splits = 1;
     if (A_lo) {
       t.mt = 1;
-      t.cs = 1;
     }
     m->tilings[key] = t;
   } else {
@@ -790,7 +821,6 @@ int record_branch(pcd_model* m, const PlanView& p, const Segment* segs, int n_se
   pcd::GemmTiling ro_t = p.ro_tiling;
   if (hr_lo) {
     ro_t.mt = 1;
-    ro_t.cs = 1;
   }
   pcd::EpiArgs re;
   re.part = static_cast<float2*>(m->ro_part.p);
@@ -1067,7 +1097,6 @@ int record_single(pcd_model* m, const PlanView& p, const int32_t* ids, int n, pc
   pcd::GemmTiling ro_t = p.ro_tiling;
   if (hr_lo) {
     ro_t.mt = 1;
-    ro_t.cs = 1;
   }
   pcd::EpiArgs re;
   re.part = static_cast<float2*>(m->ro_part.p);
@@ -2101,16 +2130,17 @@ int pcd_sync(pcd_model* m) {
 
 int pcd_profile_enable(pcd_model* m, int on) {
   if (!m) return fail(PCD_ERR_INVALID_ARG, "NULL model");
+  PCD_CUDA(cudaStreamSynchronize(m->stream));
   m->prof = on != 0;
   m->prof_rec.clear();
-  m->ev_next = 0;
+  for (int i = 0; i < PCD_PROF_CLASSES; ++i) m->prof_n[i] = 0, m->prof_ms[i] = 0.0;
   return PCD_OK;
 }
 
 int pcd_profile_read(pcd_model* m, int* launches, float* ms) {
   if (!m || !launches || !ms) return fail(PCD_ERR_INVALID_ARG, "NULL argument");
   PCD_CUDA(cudaStreamSynchronize(m->stream));
-  for (int i = 0; i < PCD_PROF_CLASSES; ++i) launches[i] = 0, ms[i] = 0.f;
+  for (int i = 0; i < PCD_PROF_CLASSES; ++i) launches[i] = m->prof_n[i], ms[i] = static_cast<float>(m->prof_ms[i]);
   for (auto& r : m->prof_rec) {
     float t = 0.f;
     cudaEventElapsedTime(&t, std::get<1>(r), std::get<2>(r));
@@ -2118,7 +2148,8 @@ int pcd_profile_read(pcd_model* m, int* launches, float* ms) {
     ms[std::get<0>(r)] += t;
   }
   m->prof_rec.clear();
-  m->ev_next = 0;
+  for (int i = 0; i < PCD_PROF_CLASSES; ++i) m->prof_n[i] = 0, m->prof_ms[i] = 0.0;
+  if (m->graph_prof.empty()) m->ev_next = 0;  // no cached graph records into the pool's events
   return PCD_OK;
 }
 

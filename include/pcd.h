@@ -277,8 +277,11 @@ int pcd_sync(pcd_model* m);
 
 /* ---------------------------------------------------------- instrumentation */
 /* Per-kernel-class timing: when enabled, every launch is bracketed by CUDA
- * events on the model stream (and passes run as direct launches, not
- * graphs).  Classes: 0 prefill GEMMs, 1 branch GEMMs, 2 prefill attention,
+ * events on the model stream.  A pass still runs as a CUDA graph (a separate
+ * graph that holds the event records), and the call that replays it
+ * synchronises the stream and adds up its events before returning, so
+ * profiled calls are synchronous; the event records between launches cost
+ * the overlap of one launch's start with the previous one's tail.  Classes: 0 prefill GEMMs, 1 branch GEMMs, 2 prefill attention,
  * 3 branch attention, 4 fused readout, 5 other, 6 single-pass GEMMs other
  * than the gate/up projection, 7 the single-pass gate/up projection (with
  * its SwiGLU epilogue).  pcd_profile_read synchronises, returns per class the
