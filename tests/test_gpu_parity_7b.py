@@ -1,8 +1,9 @@
 """Batched serving at the Qwen2.5-7B shape (untied LM head, GQA group 7):
 64 requests with prefixes of 512-4096 tokens and the 28-field schema, scored
 in one branch pass, cold and warm (a cached 512-token schema head extended by
-each request's tail).  The oracle checks the two shortest requests, cold and
-warm, at the same bounds as every other workload."""
+each request's tail).  Warm equals cold on all 64 requests; the oracle checks
+eight seeded requests, the longest prefixes among them, cold and warm, at the
+same bounds as every other workload."""
 import time
 
 import numpy as np
@@ -28,6 +29,23 @@ def big():
     model.free()
 
 
+def _oracle_sample(reqs, seed=5):
+    """The seeded requests the oracle checks: the two shortest prefixes (every
+    field), the two longest (3,500+ tokens: tree attention over up to 4,096
+    prefix keys at GQA group 7) and four drawn from the rest; the last six
+    on a seeded 7-field subset (the 7B prefill dominates the oracle's time)."""
+    order = [int(i) for i in np.argsort([len(r.prefix) for r in reqs], kind="stable")]
+    short, long_ = order[:2], order[-2:]
+    rng = np.random.default_rng(seed)
+    rest = [i for i in order if i not in short + long_]
+    mid = [int(i) for i in rng.choice(rest, 4, replace=False)]
+    n_f = len(reqs[0].fields)
+    out = [(i, list(range(n_f))) for i in short]
+    for i in long_ + mid:
+        out.append((i, sorted(int(f) for f in rng.choice(n_f, 7, replace=False))))
+    return out
+
+
 def test_config5_cold_parity_and_warm_equals_cold(big):
     pcd, model, w = big
     reqs = synth.make_requests(5)
@@ -42,22 +60,31 @@ def test_config5_cold_parity_and_warm_equals_cold(big):
     head = pcd.pcd_prefill(model, reqs[0].prefix[:512])
     warm_caches = [pcd.pcd_prefill_extend(model, head, r.prefix[512:]) for r in reqs]
     warm = pcd.pcd_score_batch(model, warm_caches, [r.fields for r in reqs])
-    # warm and cold are two valid rounding orders of the same numbers; the
-    # oracle judges both on the two shortest requests
-    gaps = [max(float(np.max(np.abs(a.probs - b.probs))) for a, b in zip(ra, rb)) for ra, rb in zip(cold, warm)]
-    print("warm/cold largest prob gap", max(gaps), "at request", int(np.argmax(gaps)))
     for c in warm_caches:
         c.free()
     head.free()
+    # warm and cold are two rounding orders of the same numbers: on every one
+    # of the 64 requests they agree within the parity bounds, and on the same
+    # label wherever the cold result is not a near tie
+    gaps = []
+    for i, (ra, rb) in enumerate(zip(cold, warm)):
+        for f, (a, b) in enumerate(zip(ra, rb)):
+            gp = float(np.max(np.abs(a.probs - b.probs)))
+            gl = float(np.max(np.abs(a.logprobs - b.logprobs)))
+            gaps.append(gp)
+            assert gp <= 2e-3 and gl <= 3e-2, (i, f, gp, gl)
+            assert abs(a.log_mass - b.log_mass) <= 3e-2, (i, f)
+            if a.margin > 0.05 + 3e-2:
+                assert a.label == b.label, (i, f, a.margin)
+    print("warm/cold largest prob gap", max(gaps))
     from oracle import Oracle
     orc = Oracle(w, np.float32)
-    pick = [int(i) for i in np.argsort([len(r.prefix) for r in reqs])[:2]]
-    for i in pick:
+    for i, fsel in _oracle_sample(reqs):
         t = time.time()
         oc = orc.prefill(reqs[i].prefix)
-        ref = [orc.score_field(f, cache=oc) for f in reqs[i].fields]
-        print(f"oracle request {i} (prefix {len(reqs[i].prefix)}): {time.time() - t:.1f} s")
-        worst = compare_request(cold[i], ref, f"config 5 request {i} cold")
+        ref = [orc.score_field(reqs[i].fields[f], cache=oc) for f in fsel]
+        print(f"oracle request {i} (prefix {len(reqs[i].prefix)}, {len(fsel)} fields): {time.time() - t:.1f} s")
+        worst = compare_request([cold[i][f] for f in fsel], ref, f"config 5 request {i} cold")
         print("config 5 cold worst errors", worst)
-        worst = compare_request(warm[i], ref, f"config 5 request {i} warm")
+        worst = compare_request([warm[i][f] for f in fsel], ref, f"config 5 request {i} warm")
         print("config 5 warm worst errors", worst)

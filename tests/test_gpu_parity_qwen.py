@@ -1,6 +1,6 @@
 """CUDA path vs the oracle at the Qwen2.5-1.5B shape (bf16 weights, V=151936):
-the 28-field triage request in full, the 255-choice router, and the
-long-document request (8192-token prefix) on sampled fields.  The launch
+the 28-field triage request, the 255-choice router and the long-document
+request (8192-token prefix), every field of each.  The launch
 configuration is the benchmark's: one prefill, one branch pass."""
 import time
 
@@ -94,23 +94,24 @@ def test_warm_equals_cold_at_scale(qwen):
         np.testing.assert_allclose(a.logprobs, b.logprobs, atol=3e-2)
 
 
-def test_config4_long_document_sampled(qwen):
-    """8192-token prefix, 29 fields; the oracle checks a boolean, an enum and
-    the 218-label line-ID field (all its labels)."""
+def test_config4_long_document(qwen):
+    """8192-token prefix, 29 fields: every field against the oracle (the 28
+    triage fields and the 218-label line-ID field), in the two-pass form and
+    in the single pass the benchmark times."""
     pcd, model, orc = qwen
     req = synth.make_request(4)
     cache = pcd.pcd_prefill(model, req.prefix)
     got, st = pcd.pcd_score(model, cache, req.fields, with_stats=True)
+    cache.free()
+    single = pcd.pcd_prefill_score(model, req.prefix, req.fields)
     t = time.time()
     oc = orc.prefill(req.prefix)
     print(f"oracle prefill 8192: {time.time() - t:.1f} s")
-    pick = [next(i for i, f in enumerate(req.fields) if f.kind == "bool"),
-            next(i for i, f in enumerate(req.fields) if f.kind == "enum"), len(req.fields) - 1]
     t = time.time()
-    ref = [orc.score_field(req.fields[i], cache=oc) for i in pick]
+    ref = [orc.score_field(f, cache=oc) for f in req.fields]
     print(f"oracle fields: {time.time() - t:.1f} s")
-    worst = compare_request([got[i] for i in pick], ref, "config 4")
+    worst = compare_request(got, ref, "config 4")
     print("config 4 worst errors", worst, "T", st["branch_tokens"], "R", st["readout_rows"])
-    # properties on every field
+    print("config 4 single pass worst errors", compare_request(single, ref, "config 4, single pass"))
     for g in got:
-        assert abs(g.probs.sum() - 1) < 1e-4 and 0 <= g.mass <= g.first_mass + 1e-6 <= 1 + 1e-6
+        assert 0 <= g.mass <= g.first_mass + 1e-6 <= 1 + 1e-6
