@@ -71,6 +71,7 @@ SIGNATURES = [
     ("pcd_answer_line", c_int, [c_void_p, c_int, P(c_int32), c_int, P(c_int32), c_int]),
     ("pcd_k_gemm", c_int, [c_void_p, c_int, c_int, c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_int,
                            c_int, c_int, c_int, c_void_p, c_void_p]),
+    ("pcd_k_wait_probe", c_int, [c_int64, c_void_p, c_void_p, c_void_p]),
 ]
 
 

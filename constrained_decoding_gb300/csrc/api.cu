@@ -261,14 +261,20 @@ cudaEvent_t next_event(pcd_model* m) {
 template <class Fn>
 int timed(pcd_model* m, int cls, Fn&& launch) {
   cudaEvent_t a = nullptr, b = nullptr;
+  // under stream capture the records become event-record nodes of the graph
+  // (external events), so every replay records them
+  unsigned flags = cudaEventRecordDefault;
   if (m->prof) {
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(m->stream, &cs) == cudaSuccess && cs == cudaStreamCaptureStatusActive)
+      flags = cudaEventRecordExternal;
     a = next_event(m);
     b = next_event(m);
-    cudaEventRecord(a, m->stream);
+    cudaEventRecordWithFlags(a, m->stream, flags);
   }
   const int r = launch();
   if (m->prof) {
-    cudaEventRecord(b, m->stream);
+    cudaEventRecordWithFlags(b, m->stream, flags);
     m->prof_rec.emplace_back(cls, a, b);
   }
   return r;

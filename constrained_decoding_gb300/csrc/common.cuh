@@ -17,6 +17,7 @@ enum DeviceError : int {
   DEV_WAIT_TIMEOUT_EPILOGUE = 3,
   DEV_WAIT_TIMEOUT_DRAIN = 4,
   DEV_BAD_INDEX = 5,
+  DEV_WAIT_TIMEOUT_PROBE = 6,
 };
 
 __device__ __forceinline__ void record_error(int* err, int code) {

@@ -320,6 +320,8 @@ __global__ void __launch_bounds__(192, 1)
   // stages (all empty now) get their B tiles before the wait below, in the
   // producer's own (unit, k block) order; their A tiles follow after it.
   int pre = 0;
+  uint32_t a_owed[8];  // A bytes a prologue stage still expects (its A loads not yet issued)
+  for (int s = 0; s < 8; ++s) a_owed[s] = 0;
   if (p.b_const && warp == 0 && lane == 0) {
     for (int u = slot; u < p.n_units && pre < C::STAGES; u += stride) {
       int nt, mg, ks, col0, width;
@@ -329,6 +331,7 @@ __global__ void __launch_bounds__(192, 1)
       for (int kb = kb0; kb < kb1 && pre < C::STAGES; ++kb, ++pre) {
         mbar_arrive_expect_tx(&full[pre], bytes);
         load_b(pre, kb, col0, width);
+        a_owed[pre] = bytes - static_cast<uint32_t>(width) * 128u;
       }
     }
   }
@@ -368,6 +371,7 @@ __global__ void __launch_bounds__(192, 1)
                 tma_load_2d(base + (MT + mt) * C::A_BYTES, &tmA2, &full[stage], kb * 64, (tile0(mg) + mt) * 128);
           }
           if (!b_done) load_b(stage, kb, col0, width);
+          a_owed[stage] = 0;
           issued[stage] = true;
           last_phase[stage] = phase;
           if (++stage == C::STAGES) {
@@ -376,10 +380,14 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
-      if (*abort_flag) {
-        // let every copy still in flight land before the CTA exits
-        for (int s = 0; s < C::STAGES; ++s)
-          if (issued[s]) mbar_wait(&full[s], last_phase[s], kDrainWaitNs);
+      // let every copy still in flight land before the CTA exits: another warp
+      // may have given up after this loop issued its last load (in a normal
+      // run these phases are complete and the waits return at once)
+      // (a prologue stage left without its A tiles by an abort is owed their
+      // bytes, so that its phase completes once its B tile has landed)
+      for (int s = 0; s < C::STAGES; ++s) {
+        if (a_owed[s]) mbar_complete_tx(&full[s], a_owed[s]);
+        if (issued[s]) mbar_wait(&full[s], last_phase[s], kDrainWaitNs);
       }
     }
   } else if (warp == 1) {

@@ -7,13 +7,29 @@
 #include <algorithm>
 #include <vector>
 
+#include "common.cuh"
 #include "gemm.h"
 #include "kernels.h"
 #include "pcd.h"
 #include "pcd_kernels.h"
 #include "plan.h"
+#include "ptx.cuh"
 
 namespace {
+// One thread waits, with the pipelines' bounded wait, on a shared-memory
+// mbarrier whose single expected arrival never comes.
+__global__ void wait_probe_kernel(uint64_t limit_ns, int* err, int64_t* elapsed_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x != 0) return;
+  pcd::mbar_init(&bar, 1);
+  pcd::fence_mbar_init();
+  const uint64_t t0 = pcd::globaltimer_ns();
+  const bool done = pcd::mbar_wait(&bar, 0, limit_ns);
+  const uint64_t t1 = pcd::globaltimer_ns();
+  if (!done) pcd::record_error(err, pcd::DEV_WAIT_TIMEOUT_PROBE);
+  if (elapsed_ns) *elapsed_ns = static_cast<int64_t>(t1 - t0);
+}
+
 int device_sms() {
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
@@ -211,4 +227,11 @@ extern "C" int pcd_plan_inspect(const void* fields, int n_fields, int vocab, int
       if (arrays[i] && !src[i]->empty()) std::memcpy(arrays[i], src[i]->data(), src[i]->size() * sizeof(int32_t));
   }
   return PCD_OK;
+}
+
+extern "C" int pcd_k_wait_probe(int64_t limit_ns, int* dev_err, int64_t* elapsed_ns, void* stream) {
+  if (limit_ns < 0 || limit_ns > 10000000000ll || !dev_err) return -1;
+  wait_probe_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(static_cast<uint64_t>(limit_ns), dev_err,
+                                                                    elapsed_ns);
+  return cudaGetLastError() == cudaSuccess ? 0 : -10;
 }

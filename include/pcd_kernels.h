@@ -86,6 +86,18 @@ int pcd_k_readout(const void* h, int R, const void* w, int V, int d, const int32
 int pcd_k_readout_noalloc(const void* h, int R, const void* w, int V, int d, const int32_t* cand_row,
                           const int32_t* cand_tok, int n_cand, float* lse, float* z_out, int* dev_err, void* stream);
 
+/* Bounded-wait check (the pages have no counterpart: it exercises this
+ * library's failure path, a pipeline partner that never arrives, without
+ * faulting or hanging the GPU).  One thread waits on a shared-memory mbarrier
+ * that nothing ever arrives on, with the bounded wait every pipeline of the
+ * library uses, and gives up once `limit_ns` (0 .. 10^10) has passed: it
+ * then records a nonzero code in `dev_err` (a device int, which it never
+ * clears) and writes the wait's duration in ns, by the device's global timer,
+ * to `elapsed_ns` (a device int64, may be NULL).  Enqueued on `stream`;
+ * returns 0, -1 for a bad argument (nothing enqueued) or -10 for a launch
+ * error. */
+int pcd_k_wait_probe(int64_t limit_ns, int* dev_err, int64_t* elapsed_ns, void* stream);
+
 /* Host-only view of the branch compiler (no GPU needed): compiles `fields`
  * (pcd.h) for a vocabulary of `vocab` tokens into the packed branch batch the
  * branch pass runs (How TypeSafe's Jev Might Work, "When one token is not

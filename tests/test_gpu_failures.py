@@ -15,8 +15,10 @@ pytestmark = pytest.mark.gpu
 
 @pytest.mark.parametrize("shape", ["tiny", "tiny-h128"])
 def test_weight_file_loads_like_host_arrays(tmp_path, shape):
-    """A model loaded from a .pcdw file gives bit-identical results to the
-    same weights passed as host arrays."""
+    """A model loaded from a .pcdw file scores like the same weights passed
+    as host arrays.  At head dim 128 the projections run split-K with fp32
+    atomic adds, whose order varies from run to run, so the two agree to
+    that run-to-run spread (~1e-6), not bit for bit."""
     import constrained_decoding_gb300.pcd as pcd
     w = synth.make_weights(synth.model_config(shape), seed=0)
     path = tmp_path / f"{shape}.pcdw"
@@ -29,9 +31,10 @@ def test_weight_file_loads_like_host_arrays(tmp_path, shape):
         c.free()
         m.free()
     for a, b in zip(*results):
-        np.testing.assert_array_equal(a.probs, b.probs)
-        np.testing.assert_array_equal(a.logprobs, b.logprobs)
-        assert a.label == b.label and a.mass == b.mass
+        np.testing.assert_allclose(a.probs, b.probs, rtol=0, atol=2e-5)
+        np.testing.assert_allclose(a.logprobs, b.logprobs, rtol=0, atol=1e-4)
+        assert a.label == b.label
+        assert abs(a.mass - b.mass) <= 1e-4 * max(1.0, abs(b.mass))
 
 
 def test_cache_of_another_model_is_refused(tiny_weights):
@@ -49,6 +52,32 @@ def test_cache_of_another_model_is_refused(tiny_weights):
     ca.free()
     a.free()
     b.free()
+
+
+def test_bounded_wait_gives_up():
+    """A wait on an mbarrier that nothing arrives on ends after its limit with
+    an error code in the device error word, and the stream stays usable."""
+    import torch
+    from constrained_decoding_gb300 import load
+    lib = load()
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    el = torch.zeros(1, dtype=torch.int64, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    for limit in (1_000, 2_000_000):
+        err.zero_()
+        assert lib.pcd_k_wait_probe(limit, err.data_ptr(), el.data_ptr(), st) == 0
+        torch.cuda.synchronize()
+        assert int(err.item()) == 6
+        assert limit <= int(el.item()) < limit + 50_000_000, (limit, int(el.item()))
+    assert lib.pcd_k_wait_probe(-1, err.data_ptr(), el.data_ptr(), st) == -1
+    assert lib.pcd_k_wait_probe(10, 0, 0, st) == -1
+    # the context still runs work after the abandoned waits
+    a = torch.randn(256, 128, device="cuda").half()
+    b = torch.randn(256, 128, device="cuda").half()
+    out = torch.zeros(256, 256, device="cuda")
+    assert lib.pcd_k_gemm(a.data_ptr(), 256, 128, b.data_ptr(), 256, 128, 128, 1, out.data_ptr(), 256, 0, 0, 1,
+                          None, st) == 0
+    torch.testing.assert_close(out, a.float() @ b.float().T, atol=1e-2, rtol=1e-3)
 
 
 def test_device_wait_timeout():
