@@ -61,6 +61,9 @@ def parse_args():
                     help="run only the warm-up and timed steps (for a clean profiler launch list)")
     ap.add_argument("--mode", default="single", choices=["single", "two-pass"],
                     help="single: prefix and branches in one forward pass; two-pass: prefill, then the branch pass")
+    ap.add_argument("--workload", type=int, default=2, choices=[2, 3, 4],
+                    help="the request of the timed steps (2: 28-field triage, the headline; 3: router; "
+                         "4: long document) -- for profiling one workload's launches")
     return ap.parse_args()
 
 
@@ -431,7 +434,7 @@ def run_ours(args):
     torch.cuda.set_device(local)
     cfg = synth.model_config("1.5b")
     weights = synth.make_weights(cfg, seed=0)
-    req = synth.make_request(2)
+    req = synth.make_request(args.workload)
     stream = torch.cuda.Stream()          # a non-default stream: passes run as CUDA graphs
     torch.cuda.set_stream(stream)
     model = pcd.pcd_load_weights_host(weights, stream=stream)
@@ -630,7 +633,7 @@ def run_ours(args):
         "dtype_note": "bf16 weights held exactly as fp16 tensor-core operands (values >= 2^-17), fp32 accumulation; "
                       "activations fp16 with fp16 remainders at the rounding points that need them",
         "data": "synthetic (seeded random-init weights and token ids)",
-        "config": {"workload": WORKLOADS[2], "prefix_len": len(req.prefix), "fields": len(req.fields),
+        "config": {"workload": WORKLOADS[args.workload], "prefix_len": len(req.prefix), "fields": len(req.fields),
                    "branch_tokens": T, "readout_rows": R, "requests_per_step": 1, "mode": args.mode,
                    "l2": "inputs larger than L2 (3.1 GB of weights streamed every step)",
                    "parallelism": f"replicas x{ws}"},

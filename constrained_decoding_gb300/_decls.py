@@ -72,6 +72,8 @@ SIGNATURES = [
     ("pcd_k_gemm", c_int, [c_void_p, c_int, c_int, c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_int,
                            c_int, c_int, c_int, c_void_p, c_void_p]),
     ("pcd_k_wait_probe", c_int, [c_int64, c_void_p, c_void_p, c_void_p]),
+    ("pcd_k_gemm_swap", c_int, [c_void_p, c_void_p, c_int, c_int, c_void_p, c_int, c_int, c_int, c_int, c_void_p,
+                                c_int, c_int, c_void_p, c_void_p]),
 ]
 
 

@@ -188,6 +188,10 @@ struct pcd_model {
   // on the tcgen05 tensor cores at head dim 128 (else warp-level MMA)
   bool tree_attn = true;
   bool attn_tc = true;
+  // projections of at most pcd::kSwapMaxRows rows stream the weights as the
+  // 256-row side of a CTA-pair MMA (head dim 128 models); off unless
+  // PCD_GEMM_SWAP=1: measured slower than the 128-row tiles on GB300
+  bool swap_gemm = false;
   std::map<std::vector<int64_t>, std::pair<uint64_t, cudaGraphExec_t>> graph_cache;
 };
 
@@ -351,9 +355,35 @@ int with_graph(pcd_model* m, const std::vector<int64_t>& key0, Fn&& record) {
 //   EPI_F32_ADD    residual += (split-K with atomics when the tiling splits K)
 //   EPI_F32_STORE  out = (zeroed + atomics when split)
 //   EPI_SWIGLU / EPI_BF16: one K split
+bool use_swap(const pcd_model* m, int M, int N, int K, int epi, int lo_row0) {
+  return m->swap_gemm && m->dh == 128 && M <= pcd::kSwapMaxRows && lo_row0 == 0 && K % 64 == 0 && N % 32 == 0 &&
+         (epi == pcd::EPI_F32_ADD || epi == pcd::EPI_F32_STORE || epi == pcd::EPI_SWIGLU);
+}
+
+// The weight-streaming form of gemm() (M <= kSwapMaxRows token rows).
+int gemm_swap(pcd_model* m, int cls, const void* A, int M, int lda, const act_t* B, int N, int ldb, int K, int epi,
+              void* out, int ldo, const void* A_lo, void* out_lo) {
+  int run_epi = epi, splits = 1;
+  if (epi == pcd::EPI_F32_ADD || epi == pcd::EPI_F32_STORE) {
+    // EPI_F32_STORE outputs are kept zeroed by their consumer: both add
+    splits = pcd::swap_splits(N, K, pcd::EPI_F32_ATOMIC, m->sms);
+    run_epi = splits > 1 ? pcd::EPI_F32_ATOMIC : pcd::EPI_F32_ADD;
+  }
+  pcd::SwapShape s{B, N, ldb, A, M, lda, K, A_lo, true};
+  pcd::EpiArgs e;
+  e.out = out;
+  e.ldo = ldo;
+  e.out_lo = out_lo;
+  PCD_LAUNCH(timed(m, cls, [&] {
+    return pcd::launch_gemm_swap(s, run_epi, e, splits, m->stream, m->d_err, m->wait_ns, m->sms);
+  }));
+  return PCD_OK;
+}
+
 int gemm(pcd_model* m, int cls, const void* A, int M, int lda, const act_t* B, int N, int ldb, int K, int epi, void* out,
          int ldo, const void* A_lo = nullptr, void* out_lo = nullptr, int lo_row0 = 0) {
   if (M <= 0) return PCD_OK;
+  if (use_swap(m, M, N, K, epi, lo_row0)) return gemm_swap(m, cls, A, M, lda, B, N, ldb, K, epi, out, ldo, A_lo, out_lo);
   const bool splittable = (epi == pcd::EPI_F32_ADD || epi == pcd::EPI_F32_STORE);
   const int key_epi = splittable ? pcd::EPI_F32_ATOMIC : epi;
   auto key = std::make_tuple(M, N, K, key_epi + (A_lo ? 100 : 0));
@@ -399,6 +429,36 @@ struct KVDest {
 int gemm_qkv_rope(pcd_model* m, int cls, const act_t* A, int M, const act_t* W, const act_t* A_lo, int lo_row0,
                   act_t* q, int split_row, const KVDest& d0, const KVDest& d1, act_t* q_lo = nullptr) {
   if (M <= 0) return PCD_OK;
+  if (use_swap(m, M, m->Nqkv, m->d, pcd::EPI_F32_STORE, lo_row0) && (split_row <= 0 || split_row >= M)) {
+    // weight-streaming projection into the (zeroed) fp32 q/k/v buffer, split
+    // over K with atomics, then the rotary embedding and the K/V writes
+    float* qkv = static_cast<float*>(m->qkv.p);
+    PCD_TRY(gemm_swap(m, cls, A, M, m->d, W, m->Nqkv, m->d, m->d, pcd::EPI_F32_STORE, qkv, m->Nqkv, A_lo, nullptr));
+    const KVDest& dd = split_row <= 0 ? d1 : d0;
+    pcd::RopeArgs ra;
+    ra.qkv = qkv;
+    ra.ldqkv = m->Nqkv;
+    ra.n = M;
+    ra.Hq = m->Hq;
+    ra.Hkv = m->Hkv;
+    ra.DH = m->dh;
+    ra.cs = m->rope;
+    ra.max_pos = m->max_pos;
+    ra.rel = dd.rel;
+    ra.base = dd.pos_base;
+    ra.q = q;
+    ra.k_dst = dd.k;
+    ra.v_dst = dd.v;
+    ra.kv_head_stride = dd.stride;
+    ra.kv_row0 = dd.row0;
+    ra.err = m->d_err;
+    ra.clear_qkv = 1;
+    ra.q_lo = q_lo;
+    ra.k_lo = dd.k_lo;
+    ra.v_lo = dd.v_lo;
+    PCD_LAUNCH(timed(m, PROF_OTHER, [&] { return pcd::launch_rope_kv(ra, m->stream); }));
+    return PCD_OK;
+  }
   auto key = std::make_tuple(M, m->Nqkv, m->d, pcd::EPI_QKV_ROPE + (A_lo ? 100 : 0));
   auto it = m->tilings.find(key);
   pcd::GemmTiling t;
@@ -1394,6 +1454,7 @@ int build_model(const pcd_model_config& cfg, TensorFn get, void* ctx, int dtype,
   if (const char* g = std::getenv("PCD_ATTN_TC")) m->attn_tc = std::atoi(g) != 0;
   m->sms = prop.multiProcessorCount;
   if (const char* w = std::getenv("PCD_WAIT_LIMIT_MS")) m->wait_ns = static_cast<uint64_t>(std::atof(w) * 1e6);
+  if (const char* g = std::getenv("PCD_GEMM_SWAP")) m->swap_gemm = std::atoi(g) != 0;
 
   auto cleanup = [&](int code) {
     pcd_model_free(m);

@@ -539,6 +539,7 @@ struct PairCfg {
   static constexpr int TMEM_COLS = TMEM_RAW <= 32 ? 32 : TMEM_RAW <= 64 ? 64 : TMEM_RAW <= 128 ? 128 : TMEM_RAW <= 256 ? 256 : 512;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + 512;
   static_assert(STAGES >= 2, "at least two stages");
+  static_assert((2 * STAGES + 2 * ACC_STAGES + 1) * 8 + 8 + 8 * STAGES <= 512, "barriers and drain counts fit");
 };
 
 template <int BN, int EPI, bool ALO>
@@ -595,11 +596,17 @@ __global__ void __launch_bounds__(192, 1)
   // a pair tile carries the A remainder when any of its rows is at or past lo_row0 (both CTAs alike)
   auto has_lo = [&](int mg) { return ALO && (mg + 1) * 256 > p.lo_row0; };
 
+  // phases this CTA's producer issued into each stage and the bytes of the
+  // last one; the peer reports its counts to the leader, which completes the
+  // drain (see the end of the kernel)
+  uint32_t* peer_cnt = tmem_slot + 2;  // [C::STAGES], after the TMEM slot and the abort flag
+  uint32_t* peer_last = peer_cnt + C::STAGES;
+  uint32_t cnt[C::STAGES], last[C::STAGES];
+  for (int s2 = 0; s2 < C::STAGES; ++s2) cnt[s2] = 0, last[s2] = 0;
+
   if (warp == 0) {
     // ------------------------------------------------------------ producer (both CTAs)
     if (lane == 0) {
-      const uint64_t pol_b = p.b_evict_first ? l2_policy_evict_first() : l2_policy_evict_last();
-      (void)pol_b;
       int stage = 0;
       uint32_t phase = 0;
       for (int u = pair; u < p.n_units && !*abort_flag; u += n_pairs) {
@@ -624,12 +631,20 @@ __global__ void __launch_bounds__(192, 1)
           if constexpr (ALO)
             if (lo) tma_load_2d_pair(base + C::A_BYTES, &tmA2, fb, kb * 64, row0(mg));
           tma_load_2d_pair(base + C::A_PARTS * C::A_BYTES, &tmB, fb, kb * 64, nt * BN + rank * (BN / 2));
+          cnt[stage] += 1;
+          last[stage] = bytes;
           if (++stage == C::STAGES) {
             stage = 0;
             phase ^= 1;
           }
         }
       }
+      if (rank == 1)
+        for (int s2 = 0; s2 < C::STAGES; ++s2) {
+          asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr(&peer_cnt[s2], 0)), "r"(cnt[s2]) : "memory");
+          asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(cluster_addr(&peer_last[s2], 0)), "r"(last[s2])
+                       : "memory");
+        }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer (leader)
@@ -740,6 +755,32 @@ __global__ void __launch_bounds__(192, 1)
   }
 
   tc_fence_before_sync();
+  cluster_sync_all();  // no copy is issued after this; the peer's counts are visible to the leader
+  if (warp == 0 && lane == 0 && rank == 0) {
+    // every phase either CTA issued into completes before either exits: a
+    // phase this CTA armed that the peer never loaded is owed the peer's bytes;
+    // one the peer loaded ahead of this CTA's arming is armed with them (each
+    // CTA's ring waits on the previous phase of the other, so the counts
+    // differ by at most one)
+    for (int s2 = 0; s2 < C::STAGES; ++s2) {
+      const uint32_t a = cnt[s2], n = peer_cnt[s2], pb = peer_last[s2];
+      if (a == 0 && n == 0) continue;
+      if (n > a + 1 || n + 1 < a) {
+        record_error(p.err, DEV_WAIT_TIMEOUT_DRAIN);
+        continue;
+      }
+      uint32_t ph;
+      if (n == a + 1) {
+        mbar_arrive_expect_tx(&full[s2], pb);
+        ph = n - 1;
+      } else {
+        if (n + 1 == a) mbar_complete_tx(&full[s2], last[s2]);
+        ph = a - 1;
+      }
+      if (!mbar_wait(&full[s2], ph & 1u, kDrainWaitNs)) record_error(p.err, DEV_WAIT_TIMEOUT_DRAIN);
+    }
+  }
+  tc_fence_before_sync();
   cluster_sync_all();  // neither CTA's shared memory or barriers are touched by the other after this
   if (warp == 1) {
     tc_fence_after_sync();
@@ -797,6 +838,10 @@ static bool make_map(CUtensorMap* m, const void* ptr, int rows, int cols, int ld
   if (g_maps.size() > 4096) g_maps.clear();
   g_maps.emplace(k, *m);
   return true;
+}
+
+bool make_tile_map(CUtensorMap* m, const void* ptr, int rows, int cols, int ld, int box_rows) {
+  return make_map(m, ptr, rows, cols, ld, box_rows);
 }
 
 static bool encode_map(CUtensorMap* m, const void* ptr, int rows, int cols, int ld, int box_rows) {

@@ -77,8 +77,32 @@ inline int gemm_n_tiles(int N, const GemmTiling& t) { return (N + t.bn - 1) / t.
 int launch_gemm(const GemmShape& s, int epi, const EpiArgs& e, const GemmTiling& t, cudaStream_t stream,
                 int* dev_err, uint64_t wait_ns, int sms);
 
+// ---------------------------------------------------------------- weight-streaming form
+// D^T = W . X^T for at most kSwapMaxRows token rows: the weights are the
+// 256-row side of a CTA-pair MMA and the tokens its N side, so every weight
+// tile is read once (instead of once per 128-token tile).
+constexpr int kSwapMaxRows = 512;
+struct SwapShape {
+  const void* w; int w_rows; int w_ld;   // weights [w_rows][K] (output features), leading dim in elements
+  const void* x; int x_rows; int x_ld;   // activations [x_rows][K]
+  int K;
+  const void* x_lo = nullptr;            // optional activation remainder (same layout): D = W . (X + X_lo)^T
+  bool w_const = false;                  // W is never written by an earlier kernel in the stream
+};
+// K splits for the shape (1 unless epi is EPI_F32_ATOMIC).
+int swap_splits(int w_rows, int K, int epi, int sms);
+// Launches the weight-streaming GEMM; epi is EPI_F32_ADD (splits 1),
+// EPI_F32_ATOMIC or EPI_SWIGLU (splits 1), writing out[t][n] (n a weight row;
+// SwiGLU: out[t][f] from rows 2f, 2f+1).  Returns a cudaError_t value, -1 for
+// an invalid shape.
+int launch_gemm_swap(const SwapShape& s, int epi, const EpiArgs& e, int splits, cudaStream_t stream, int* dev_err,
+                     uint64_t wait_ns, int sms);
+
 // Loads cuTensorMapEncodeTiled from the driver; false if it is unavailable.
 bool tma_init();
+// 2-D tensor map of a 16-bit row-major matrix [rows][>= cols] (leading dim
+// `ld` elements), box 64 columns x box_rows rows, 128-byte swizzle; cached.
+bool make_tile_map(CUtensorMap* m, const void* ptr, int rows, int cols, int ld, int box_rows);
 // Tensor map over a 16-bit KV cache laid out [layer][head][row][dh] (head
 // stride head_rows rows, layer stride layer_elems elements): dimensions
 // {dh, n_rows, n_heads, n_layers}, so rows at or past n_rows read as zero;

@@ -235,3 +235,17 @@ extern "C" int pcd_k_wait_probe(int64_t limit_ns, int* dev_err, int64_t* elapsed
                                                                     elapsed_ns);
   return cudaGetLastError() == cudaSuccess ? 0 : -10;
 }
+
+extern "C" int pcd_k_gemm_swap(const void* a, const void* a_lo, int M, int lda, const void* b, int N, int ldb, int K,
+                               int epi, void* out, int ldo, int splits, int* dev_err, void* stream) {
+  if (!a || !b || !out || M < 0 || N <= 0 || K <= 0) return -1;
+  if (epi != PCD_EPI_F32_ADD && epi != PCD_EPI_F32_ATOMIC && epi != PCD_EPI_SWIGLU) return -1;
+  const int sms = device_sms();
+  if (splits < 1) splits = pcd::swap_splits(N, K, epi, sms);
+  pcd::SwapShape s{b, N, ldb, a, M, lda, K, a_lo, false};
+  pcd::EpiArgs e;
+  e.out = out;
+  e.ldo = ldo;
+  const int r = pcd::launch_gemm_swap(s, epi, e, splits, static_cast<cudaStream_t>(stream), dev_err, 2000000000ull, sms);
+  return r == 0 ? 0 : (r < 0 ? -1 : -10);
+}

@@ -145,18 +145,33 @@ __global__ void rope_kv_kernel(RopeArgs a) {
     const float2 cs = a.cs[static_cast<size_t>(pos) * half + i];
     const float y1 = x1 * cs.x - x2 * cs.y;
     const float y2 = x2 * cs.x + x1 * cs.y;
-    act_t* dst;
+    size_t o;
+    act_t *dst, *lo;
     if (h < a.Hq) {
-      dst = a.q + (static_cast<size_t>(t) * a.Hq + h) * a.DH;
+      o = (static_cast<size_t>(t) * a.Hq + h) * a.DH;
+      dst = a.q + o;
+      lo = a.q_lo ? a.q_lo + o : nullptr;
     } else {
-      dst = a.k_dst + (static_cast<size_t>(h - a.Hq) * a.kv_head_stride + a.kv_row0 + t) * a.DH;
+      o = (static_cast<size_t>(h - a.Hq) * a.kv_head_stride + a.kv_row0 + t) * a.DH;
+      dst = a.k_dst + o;
+      lo = a.k_lo ? a.k_lo + o : nullptr;
     }
-    dst[i] = f2a(y1);
-    dst[i + half] = f2a(y2);
+    const act_t h1 = f2a(y1), h2 = f2a(y2);
+    dst[i] = h1;
+    dst[i + half] = h2;
+    if (lo) {
+      lo[i] = f2a(y1 - a2f(h1));
+      lo[i + half] = f2a(y2 - a2f(h2));
+    }
   } else {
-    act_t* dst = a.v_dst + (static_cast<size_t>(h - a.Hq - a.Hkv) * a.kv_head_stride + a.kv_row0 + t) * a.DH;
-    dst[i] = f2a(x1);
-    dst[i + half] = f2a(x2);
+    const size_t o = (static_cast<size_t>(h - a.Hq - a.Hkv) * a.kv_head_stride + a.kv_row0 + t) * a.DH;
+    const act_t h1 = f2a(x1), h2 = f2a(x2);
+    a.v_dst[o + i] = h1;
+    a.v_dst[o + i + half] = h2;
+    if (a.v_lo) {
+      a.v_lo[o + i] = f2a(x1 - a2f(h1));
+      a.v_lo[o + i + half] = f2a(x2 - a2f(h2));
+    }
   }
 }
 

@@ -31,6 +31,9 @@ struct RopeArgs {
   int kv_row0;
   int* err;
   int clear_qkv = 0;      // zero the consumed qkv values (the next split-K projection accumulates into them)
+  act_t* q_lo = nullptr;  // optional fp16 rounding remainders of q, k and v (same layouts)
+  act_t* k_lo = nullptr;
+  act_t* v_lo = nullptr;
 };
 int launch_rope_kv(const RopeArgs& a, cudaStream_t s);
 
@@ -139,6 +142,9 @@ int launch_tree_attention_tc(const TreeAttnArgs& a, const CUtensorMap& tmK, cons
 // kernel: the key blocks of the heaviest tile (max_blocks) against the waves
 // of CTAs the cluster split adds.
 int tree_attention_csk(int tiles, int Hkv, int max_blocks, int sms, bool tc);
+// CTAs of the tensor-core tree attention that can be resident at once when
+// launched in clusters of csk (1..8); 0 if the query fails.
+int tree_attention_tc_slots(int csk);
 
 // lse[r] = log sum_tiles sum exp(z) from per-tile (max, sum exp(z - max)).
 int launch_lse_combine(const float2* part, int n_tiles, int R, float* lse, cudaStream_t s);

@@ -376,12 +376,20 @@ int tree_attention_csk(int tiles, int Hkv, int max_blocks, int sms, bool tc) {
   // Time model in microseconds: a CTA costs a fixed part, its share of the
   // tile's key blocks and, in a cluster, the combine; CTAs past what the SMs
   // hold at once run in a later wave.
-  const double fixed = 3.0, per_block = tc ? 0.7 : 1.5, combine = 6.0;  // measured: the combine waits on peers
+  // fitted to per-phase timings of the tensor-core kernel on GB300 (start and
+  // epilogue ~6.6 us, ~2.0 us per 64-key block with the remainder MMAs, the
+  // cluster combine ~12 us); the warp-MMA kernel's figures from whole-launch times
+  const double fixed = tc ? 6.6 : 3.0, per_block = tc ? 2.0 : 1.5, combine = tc ? 12.0 : 6.0;
   int best = 1;
   double best_t = 1e30;
   for (int csk = 1; csk <= 8 && csk <= max_blocks; ++csk) {
     const long long ctas = static_cast<long long>(tiles) * Hkv * csk;
-    const long long slots = static_cast<long long>(tc ? 1 : 2) * sms;  // resident CTAs per SM: 1 (tensor-core), 2
+    // resident CTAs: the tensor-core kernel runs one per SM, its clusters within a GPC each
+    long long slots = static_cast<long long>(tc ? 1 : 2) * sms;
+    if (tc) {
+      const int q = tree_attention_tc_slots(csk);
+      if (q > 0) slots = q;
+    }
     const long long waves = (ctas + slots - 1) / slots;
     const int blocks = (max_blocks + csk - 1) / csk;
     const double t = static_cast<double>(waves) * (fixed + blocks * per_block + (csk > 1 ? combine : 0.0));

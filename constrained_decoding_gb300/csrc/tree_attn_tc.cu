@@ -18,6 +18,7 @@
 // own S columns and is the A operand of the P V MMA.  A (csk, 1, 1) cluster splits
 // a tile's key blocks and combines the partial softmax states through
 // distributed shared memory.
+#include <algorithm>
 #include <climits>
 #include <cstdint>
 
@@ -608,6 +609,46 @@ static int launch_tc_t(const TreeAttnArgs& a, const CUtensorMap& tmK, const CUte
   cfg.attrs = at;
   cfg.numAttrs = na;
   return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<LO>, tmK, tmV, tmKlo, tmVlo, tmQ, tmQlo, a, layer, wait_ns, err);
+}
+
+int tree_attention_tc_slots(int csk) {
+  // clusters must fit inside one GPC, so fewer CTAs than SMs may be resident
+  // at once for csk > 1 (e.g. clusters of 5 on GPCs of 19 SMs)
+  static int cache[9] = {};
+  if (csk < 1 || csk > 8) return 0;
+  if (cache[csk]) return cache[csk];
+  using C = TcCfg<true>;
+  auto kern = tree_attn_tc_kernel<true>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess) return 0;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int slots = 0;
+  if (csk == 1) {
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 192, C::kSmem) != cudaSuccess) return 0;
+    slots = per_sm * sms;
+  } else {
+    cudaLaunchConfig_t q = {};
+    q.gridDim = dim3(static_cast<unsigned>(csk * std::max(1, sms / csk)), 1, 1);
+    q.blockDim = dim3(192, 1, 1);
+    q.dynamicSmemBytes = C::kSmem;
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeClusterDimension;
+    at[0].val.clusterDim.x = static_cast<unsigned>(csk);
+    at[0].val.clusterDim.y = 1;
+    at[0].val.clusterDim.z = 1;
+    q.attrs = at;
+    q.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess) {
+      cudaGetLastError();
+      return 0;
+    }
+    slots = n * csk;
+  }
+  cache[csk] = slots;
+  return slots;
 }
 
 int launch_tree_attention_tc(const TreeAttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV,

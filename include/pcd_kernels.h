@@ -42,6 +42,20 @@ int pcd_k_gemm(const void* a, int M, int lda, const void* b, int N, int ldb, int
 int pcd_k_gemm_split(const void* a_hi, const void* a_lo, int M, int lda, const void* b, int N, int ldb, int K, int epi,
                      void* out, int ldo, int bn, int splits, int* dev_err, void* stream);
 
+/* pcd_k_gemm in the weight-streaming form for short activations (M <= 512
+ * token rows: the branch rows of one request, How TypeSafe's Jev Might Work,
+ * "One forward pass for all fields"): the same D[M][N] = (A + A_lo)[M][K] .
+ * B[N][K]^T, computed with B (the weights) as the 256-row side of a tensor-core
+ * MMA shared by a pair of CTAs and A as its N side, so every weight tile is
+ * read from HBM once.  a_lo (may be NULL) is A's fp16 rounding remainder.
+ * epi PCD_EPI_F32_ADD (splits 1), PCD_EPI_F32_ATOMIC (splits >= 1; 0 lets the
+ * library choose) or PCD_EPI_SWIGLU (splits 1; B rows 2f, 2f+1 are gate f and
+ * up f, out[M][ldo] fp16).  K a multiple of 64, N a multiple of 32, lda/ldb
+ * multiples of 8.  Returns 0, -1 for an invalid shape, -10 for a launch
+ * error; `dev_err` as in pcd_k_gemm. */
+int pcd_k_gemm_swap(const void* a, const void* a_lo, int M, int lda, const void* b, int N, int ldb, int K, int epi,
+                    void* out, int ldo, int splits, int* dev_err, void* stream);
+
 /* Fused vocabulary readout: the LM-head contraction z = h . W^T run tile by
  * tile on the tensor cores with an online log-sum-exp over the whole
  * vocabulary and a gather of selected logits, so the [R][V] logits are never
