@@ -429,11 +429,13 @@ struct KVDest {
 int gemm_qkv_rope(pcd_model* m, int cls, const act_t* A, int M, const act_t* W, const act_t* A_lo, int lo_row0,
                   act_t* q, int split_row, const KVDest& d0, const KVDest& d1, act_t* q_lo = nullptr) {
   if (M <= 0) return PCD_OK;
-  if (use_swap(m, M, m->Nqkv, m->d, pcd::EPI_F32_STORE, lo_row0) && (split_row <= 0 || split_row >= M)) {
-    // weight-streaming projection into the (zeroed) fp32 q/k/v buffer, split
-    // over K with atomics, then the rotary embedding and the K/V writes
+  if (M <= pcd::kSwapMaxRows && lo_row0 == 0 && (split_row <= 0 || split_row >= M)) {
+    // a short projection with one destination: into the (zeroed) fp32 q/k/v
+    // buffer, split over K with atomics to fill the SMs (the fused RoPE
+    // epilogue allows no K split: 48 CTAs at 313 rows), then the rotary
+    // embedding and the K/V writes in one elementwise pass
     float* qkv = static_cast<float*>(m->qkv.p);
-    PCD_TRY(gemm_swap(m, cls, A, M, m->d, W, m->Nqkv, m->d, m->d, pcd::EPI_F32_STORE, qkv, m->Nqkv, A_lo, nullptr));
+    PCD_TRY(gemm(m, cls, A, M, m->d, W, m->Nqkv, m->d, m->d, pcd::EPI_F32_STORE, qkv, m->Nqkv, A_lo));
     const KVDest& dd = split_row <= 0 ? d1 : d0;
     pcd::RopeArgs ra;
     ra.qkv = qkv;

@@ -122,14 +122,16 @@ int launch_rmsnorm(const float* x, int ldx, const int32_t* rows, int n, int d, c
 __global__ void rope_kv_kernel(RopeArgs a) {
   griddep_launch_dependents();
   griddep_wait();
-  const int half = a.DH / 2;
-  const int heads = a.Hq + 2 * a.Hkv;
-  const long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long total = static_cast<long long>(a.n) * heads * half;
-  if (idx >= total) return;
-  const int i = static_cast<int>(idx % half);
-  const int h = static_cast<int>((idx / half) % heads);
-  const int t = static_cast<int>(idx / (static_cast<long long>(half) * heads));
+  // 32-bit index arithmetic (the launcher checks that every index fits):
+  // 64-bit divisions cost ten times as much and made this kernel slow
+  const unsigned half = static_cast<unsigned>(a.DH / 2);
+  const unsigned heads = static_cast<unsigned>(a.Hq + 2 * a.Hkv);
+  const unsigned idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= static_cast<unsigned>(a.n) * heads * half) return;
+  const unsigned th = idx / half;
+  const int i = static_cast<int>(idx - th * half);
+  const int t = static_cast<int>(th / heads);
+  const int h = static_cast<int>(th - static_cast<unsigned>(t) * heads);
   int pos = a.base + (a.rel ? a.rel[t] : t);
   if (pos < 0 || pos >= a.max_pos) {
     record_error(a.err, DEV_BAD_INDEX);
@@ -178,6 +180,7 @@ __global__ void rope_kv_kernel(RopeArgs a) {
 int launch_rope_kv(const RopeArgs& a, cudaStream_t s) {
   if (a.n <= 0) return 0;
   const long long total = static_cast<long long>(a.n) * (a.Hq + 2 * a.Hkv) * (a.DH / 2);
+  if (total >= (1ll << 31)) return cudaErrorInvalidValue;
   return launch_k(rope_kv_kernel, dim3(static_cast<unsigned>((total + 255) / 256)), dim3(256), 0, s, a);
 }
 

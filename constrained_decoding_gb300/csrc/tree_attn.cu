@@ -376,10 +376,12 @@ int tree_attention_csk(int tiles, int Hkv, int max_blocks, int sms, bool tc) {
   // Time model in microseconds: a CTA costs a fixed part, its share of the
   // tile's key blocks and, in a cluster, the combine; CTAs past what the SMs
   // hold at once run in a later wave.
-  // fitted to per-phase timings of the tensor-core kernel on GB300 (start and
-  // epilogue ~6.6 us, ~2.0 us per 64-key block with the remainder MMAs, the
-  // cluster combine ~12 us); the warp-MMA kernel's figures from whole-launch times
-  const double fixed = tc ? 6.6 : 3.0, per_block = tc ? 2.0 : 1.5, combine = tc ? 12.0 : 6.0;
+  // fitted on GB300: the tensor-core kernel's start and epilogue ~6.6 us
+  // (per-phase timer trace), ~2.4 us per 64-key block with the remainder MMAs
+  // and gathered ancestor chunks, the cluster combine ~11 us (branch-pass
+  // launches at key splits 1-4); the warp-MMA kernel's figures from
+  // whole-launch times
+  const double fixed = tc ? 6.6 : 3.0, per_block = tc ? 2.4 : 1.5, combine = tc ? 11.0 : 6.0;
   int best = 1;
   double best_t = 1e30;
   for (int csk = 1; csk <= 8 && csk <= max_blocks; ++csk) {

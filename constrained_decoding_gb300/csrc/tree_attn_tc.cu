@@ -13,7 +13,8 @@
 // maximum exceeds it by more than 14 (log2 units): every P stays <= 2^14, a
 // finite fp16, and the result is exact up to rounding, while the rescale
 // (which waits for the previous P V) is rare.  Warp 0 loads K/V (TMA for prefix
-// blocks, gathered cp.async for ancestor chunks), warp 1 issues the MMAs,
+// blocks, gathered cp.async for ancestor chunks), warp 1 issues the S MMAs and
+// warp 6 the P V MMAs,
 // warps 2-5 run the softmax and the epilogue; P goes back into TMEM over its
 // own S columns and is the A operand of the P V MMA.  A (csk, 1, 1) cluster splits
 // a tile's key blocks and combines the partial softmax states through
@@ -70,7 +71,7 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {  // 128-byte swizz
 }
 
 template <bool LO>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(224, 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const __grid_constant__ CUtensorMap tmKlo, const __grid_constant__ CUtensorMap tmVlo,
                         const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQlo,
@@ -92,6 +93,7 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* drain = bars + 28;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 29);
   uint64_t* q_full = bars + 30;   // producer: the Q tile (and remainder) landed -> MMA
+  uint64_t* drain2 = bars + 31;   // the P V issuer's MMAs are done
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float2* sML = reinterpret_cast<float2*>(smem + kOffML);
   float* sRed = reinterpret_cast<float*>(smem);  // received partial rows, after the key loop
@@ -134,6 +136,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&pv_done[s], 1);
     }
     mbar_init(drain, 1);
+    mbar_init(drain2, 1);
     mbar_init(q_full, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -255,28 +258,37 @@ __global__ void __launch_bounds__(192, 1)
       ++vissued[s];
       __syncwarp();
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    named_barrier_sync(1, 160);  // the rows past the Q box are zeroed
+  } else if (warp == 1 || warp == 6) {
+    // ------------------------------------------------------------ MMA issuers
+    // Warp 1 issues S = Q K^T, warp 6 O += P V, each in block order as soon as
+    // its inputs are ready (the barriers order the two as a single issuer
+    // would).  A tcgen05.mma holds its issuing thread for tens of cycles, so
+    // one thread issuing both kept the next block's S waiting behind this
+    // block's P V.
+    const bool is_s = warp == 1;
+    if (is_s) named_barrier_sync(1, 160);  // the rows past the Q box are zeroed
     if (lane == 0) {
-      const bool q_ok = mbar_wait(q_full, 0, wait_ns);
-      if (!q_ok) fail(DEV_WAIT_TIMEOUT_MMA);
+      bool ok = true;
+      if (is_s) {
+        ok = mbar_wait(q_full, 0, wait_ns);
+        if (!ok) fail(DEV_WAIT_TIMEOUT_MMA);
+      }
       tc_fence_after_sync();
       constexpr uint32_t kIdescS = idesc_f16_f32(kRows, kKeys);
       constexpr uint32_t kIdescO = idesc_f16_f32(kRows, kDH) | (1u << 16);  // B (V) is MN-major
       const uint32_t qa = smem_u32(smem + kOffQ);
-      // S of block ns and P V of block npv are issued as soon as their inputs
-      // are ready, in block order each: neither waits behind the other
-      int ns = 0, npv = 0;
+      int n = 0;
       uint64_t t_last = globaltimer_ns();
       uint32_t spins = 0;
-      while (q_ok && npv < my_n) {
-        bool progressed = false;
-        if (ns < my_n) {
-          const int s = ns % kStages;
-          // S/P columns s are free once the P V of block ns - kStages is done
-          if (mbar_test(&k_full[s], static_cast<uint32_t>((ns / kStages) & 1)) &&
-              (ns < kStages || mbar_test(&pv_done[s], static_cast<uint32_t>(((ns - kStages) / kStages) & 1)))) {
+      while (ok && n < my_n) {
+        const int s = n % kStages;
+        const uint32_t par = static_cast<uint32_t>((n / kStages) & 1);
+        bool ready;
+        if (is_s) {
+          // S/P columns s are free once the P V of block n - kStages is done
+          ready = mbar_test(&k_full[s], par) &&
+                  (n < kStages || mbar_test(&pv_done[s], static_cast<uint32_t>(((n - kStages) / kStages) & 1)));
+          if (ready) {
             tc_fence_after_sync();
             const uint32_t ka = smem_u32(smem + kOffK + s * kKVSt);
             const uint32_t dS = tbase + kColS + s * kKeys;
@@ -291,21 +303,17 @@ __global__ void __launch_bounds__(192, 1)
             }
             umma_commit(&s_full[s]);
             umma_commit(&k_free[s]);
-            ++ns;
-            progressed = true;
           }
-        }
-        if (npv < ns) {
-          const int sp = npv % kStages;
-          const uint32_t par = static_cast<uint32_t>((npv / kStages) & 1);
-          if (mbar_test(&p_full[sp], par) && mbar_test(&v_full[sp], par)) {
+        } else {
+          ready = mbar_test(&p_full[s], par) && mbar_test(&v_full[s], par);
+          if (ready) {
             tc_fence_after_sync();
-            const uint32_t va = smem_u32(smem + kOffV + sp * kKVSt);
-            const uint32_t pcol = tbase + kColS + sp * kKeys;
+            const uint32_t va = smem_u32(smem + kOffV + s * kKVSt);
+            const uint32_t pcol = tbase + kColS + s * kKeys;
 #pragma unroll
             for (int k = 0; k < kKeys / 16; ++k) {  // P: 16 keys = 8 packed columns per step
               umma_f16_ts(tbase + kColO, pcol + k * 8, sdesc_mnmajor_sw128(va + k * 16 * 128, kKVBytes / 2, 1024), kIdescO,
-                          (npv > 0 || k > 0) ? 1u : 0u);
+                          (n > 0 || k > 0) ? 1u : 0u);
               if constexpr (LO) {  // + P V_lo + P_lo V
                 umma_f16_ts(tbase + kColO, pcol + k * 8,
                             sdesc_mnmajor_sw128(va + kKVBytes + k * 16 * 128, kKVBytes / 2, 1024), kIdescO, 1u);
@@ -313,13 +321,12 @@ __global__ void __launch_bounds__(192, 1)
                             sdesc_mnmajor_sw128(va + k * 16 * 128, kKVBytes / 2, 1024), kIdescO, 1u);
               }
             }
-            umma_commit(&pv_done[sp]);
-            umma_commit(&v_free[sp]);
-            ++npv;
-            progressed = true;
+            umma_commit(&pv_done[s]);
+            umma_commit(&v_free[s]);
           }
         }
-        if (progressed) {
+        if (ready) {
+          ++n;
           t_last = globaltimer_ns();
           continue;
         }
@@ -332,12 +339,13 @@ __global__ void __launch_bounds__(192, 1)
           }
         }
       }
-      // every MMA issued above has finished before TMEM is released
-      umma_commit(drain);
-      if (!mbar_wait(drain, 0, kDrainWaitNs)) record_error(err, DEV_WAIT_TIMEOUT_DRAIN);
+      // every MMA this thread issued has finished before TMEM is released
+      uint64_t* dr = is_s ? drain : drain2;
+      umma_commit(dr);
+      if (!mbar_wait(dr, 0, kDrainWaitNs)) record_error(err, DEV_WAIT_TIMEOUT_DRAIN);
     }
     __syncwarp();
-  } else {
+  } else if (warp <= 5) {
     // ------------------------------------------------------------ softmax rows
     {  // the Q tile arrives by TMA (rows tt * G + g); the rows past it are zero
       if (r >= a.tpt * G) {
@@ -509,7 +517,7 @@ __global__ void __launch_bounds__(192, 1)
     // combines them locally
     const int per = (kRows + csk - 1) / csk;
     cluster_sync_all();  // every CTA of the cluster is done with its Q/K/V/P buffers
-    if (warp >= 2) {
+    if (warp >= 2 && warp <= 5) {
       const uint32_t trow = tbase + (static_cast<uint32_t>(32 * (warp & 3)) << 16);
       const int owner = r / per, lr = r - owner * per;
       const uint32_t dst = dsmem_addr(sRed + (rank * per + lr) * kRedLd, owner);
@@ -589,7 +597,7 @@ static int launch_tc_t(const TreeAttnArgs& a, const CUtensorMap& tmK, const CUte
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>((a.n_br_tiles + a.n_pf_tiles) * a.csk), static_cast<unsigned>(a.Hkv), 1);
-  cfg.blockDim = dim3(192, 1, 1);
+  cfg.blockDim = dim3(224, 1, 1);
   cfg.dynamicSmemBytes = C::kSmem;
   cfg.stream = s;
   cudaLaunchAttribute at[2];
@@ -626,12 +634,12 @@ int tree_attention_tc_slots(int csk) {
   int slots = 0;
   if (csk == 1) {
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 192, C::kSmem) != cudaSuccess) return 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, 224, C::kSmem) != cudaSuccess) return 0;
     slots = per_sm * sms;
   } else {
     cudaLaunchConfig_t q = {};
     q.gridDim = dim3(static_cast<unsigned>(csk * std::max(1, sms / csk)), 1, 1);
-    q.blockDim = dim3(192, 1, 1);
+    q.blockDim = dim3(224, 1, 1);
     q.dynamicSmemBytes = C::kSmem;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;

@@ -18,7 +18,8 @@ def test_weight_file_loads_like_host_arrays(tmp_path, shape):
     """A model loaded from a .pcdw file scores like the same weights passed
     as host arrays.  At head dim 128 the projections run split-K with fp32
     atomic adds, whose order varies from run to run, so the two agree to
-    that run-to-run spread (~1e-6), not bit for bit."""
+    that run-to-run spread (~1e-6 in probabilities, ~1e-5 relative in
+    log-probs near -20), not bit for bit."""
     import constrained_decoding_gb300.pcd as pcd
     w = synth.make_weights(synth.model_config(shape), seed=0)
     path = tmp_path / f"{shape}.pcdw"
@@ -32,7 +33,7 @@ def test_weight_file_loads_like_host_arrays(tmp_path, shape):
         m.free()
     for a, b in zip(*results):
         np.testing.assert_allclose(a.probs, b.probs, rtol=0, atol=2e-5)
-        np.testing.assert_allclose(a.logprobs, b.logprobs, rtol=0, atol=1e-4)
+        np.testing.assert_allclose(a.logprobs, b.logprobs, rtol=1e-4, atol=1e-4)
         assert a.label == b.label
         assert abs(a.mass - b.mass) <= 1e-4 * max(1.0, abs(b.mass))
 
