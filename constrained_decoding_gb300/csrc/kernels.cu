@@ -122,14 +122,17 @@ int launch_rmsnorm(const float* x, int ldx, const int32_t* rows, int n, int d, c
 __global__ void rope_kv_kernel(RopeArgs a) {
   griddep_launch_dependents();
   griddep_wait();
-  // 32-bit index arithmetic (the launcher checks that every index fits):
-  // 64-bit divisions cost ten times as much and made this kernel slow
+  // a thread takes four consecutive rotation pairs (i0 .. i0+3, i0+h .. i0+h+3
+  // with h = DH/2) of one (token, head): 16-byte loads of q/k/v and of the
+  // (cos, sin) table, 8-byte stores.  32-bit index arithmetic (the launcher
+  // checks that every index fits).
   const unsigned half = static_cast<unsigned>(a.DH / 2);
+  const unsigned quads = half / 4;
   const unsigned heads = static_cast<unsigned>(a.Hq + 2 * a.Hkv);
   const unsigned idx = blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= static_cast<unsigned>(a.n) * heads * half) return;
-  const unsigned th = idx / half;
-  const int i = static_cast<int>(idx - th * half);
+  if (idx >= static_cast<unsigned>(a.n) * heads * quads) return;
+  const unsigned th = idx / quads;
+  const int i0 = static_cast<int>(idx - th * quads) * 4;
   const int t = static_cast<int>(th / heads);
   const int h = static_cast<int>(th - static_cast<unsigned>(t) * heads);
   int pos = a.base + (a.rel ? a.rel[t] : t);
@@ -137,49 +140,58 @@ __global__ void rope_kv_kernel(RopeArgs a) {
     record_error(a.err, DEV_BAD_INDEX);
     pos = 0;
   }
-  float* src = const_cast<float*>(a.qkv) + static_cast<size_t>(t) * a.ldqkv + h * a.DH;
-  const float x1 = src[i], x2 = src[i + half];
+  float4* src = reinterpret_cast<float4*>(const_cast<float*>(a.qkv) + static_cast<size_t>(t) * a.ldqkv + h * a.DH + i0);
+  float4* src2 = src + half / 4;
+  const float4 x1 = *src, x2 = *src2;
   if (a.clear_qkv) {  // leave the accumulation buffer zeroed for the next split-K projection
-    src[i] = 0.f;
-    src[i + half] = 0.f;
+    *src = make_float4(0.f, 0.f, 0.f, 0.f);
+    *src2 = make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  float y1[4] = {x1.x, x1.y, x1.z, x1.w}, y2[4] = {x2.x, x2.y, x2.z, x2.w};
+  act_t *dst, *lo;
+  size_t o;
   if (h < a.Hq + a.Hkv) {
-    const float2 cs = a.cs[static_cast<size_t>(pos) * half + i];
-    const float y1 = x1 * cs.x - x2 * cs.y;
-    const float y2 = x2 * cs.x + x1 * cs.y;
-    size_t o;
-    act_t *dst, *lo;
+    const float4* cp = reinterpret_cast<const float4*>(a.cs + static_cast<size_t>(pos) * half + i0);
+    const float4 c01 = cp[0], c23 = cp[1];
+    const float cs_c[4] = {c01.x, c01.z, c23.x, c23.z}, cs_s[4] = {c01.y, c01.w, c23.y, c23.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const float u = y1[k], w = y2[k];
+      y1[k] = u * cs_c[k] - w * cs_s[k];
+      y2[k] = w * cs_c[k] + u * cs_s[k];
+    }
     if (h < a.Hq) {
       o = (static_cast<size_t>(t) * a.Hq + h) * a.DH;
-      dst = a.q + o;
-      lo = a.q_lo ? a.q_lo + o : nullptr;
+      dst = a.q;
+      lo = a.q_lo;
     } else {
       o = (static_cast<size_t>(h - a.Hq) * a.kv_head_stride + a.kv_row0 + t) * a.DH;
-      dst = a.k_dst + o;
-      lo = a.k_lo ? a.k_lo + o : nullptr;
-    }
-    const act_t h1 = f2a(y1), h2 = f2a(y2);
-    dst[i] = h1;
-    dst[i + half] = h2;
-    if (lo) {
-      lo[i] = f2a(y1 - a2f(h1));
-      lo[i + half] = f2a(y2 - a2f(h2));
+      dst = a.k_dst;
+      lo = a.k_lo;
     }
   } else {
-    const size_t o = (static_cast<size_t>(h - a.Hq - a.Hkv) * a.kv_head_stride + a.kv_row0 + t) * a.DH;
-    const act_t h1 = f2a(x1), h2 = f2a(x2);
-    a.v_dst[o + i] = h1;
-    a.v_dst[o + i + half] = h2;
-    if (a.v_lo) {
-      a.v_lo[o + i] = f2a(x1 - a2f(h1));
-      a.v_lo[o + i + half] = f2a(x2 - a2f(h2));
-    }
+    o = (static_cast<size_t>(h - a.Hq - a.Hkv) * a.kv_head_stride + a.kv_row0 + t) * a.DH;
+    dst = a.v_dst;
+    lo = a.v_lo;
+  }
+  const uint2 hv1 = make_uint2(pack2(y1[0], y1[1]), pack2(y1[2], y1[3]));
+  const uint2 hv2 = make_uint2(pack2(y2[0], y2[1]), pack2(y2[2], y2[3]));
+  *reinterpret_cast<uint2*>(dst + o + i0) = hv1;
+  *reinterpret_cast<uint2*>(dst + o + half + i0) = hv2;
+  if (lo) {  // value - fp16(value), itself rounded to fp16
+    const __half* e1 = reinterpret_cast<const __half*>(&hv1);
+    const __half* e2 = reinterpret_cast<const __half*>(&hv2);
+    *reinterpret_cast<uint2*>(lo + o + i0) =
+        make_uint2(pack2(y1[0] - a2f(e1[0]), y1[1] - a2f(e1[1])), pack2(y1[2] - a2f(e1[2]), y1[3] - a2f(e1[3])));
+    *reinterpret_cast<uint2*>(lo + o + half + i0) =
+        make_uint2(pack2(y2[0] - a2f(e2[0]), y2[1] - a2f(e2[1])), pack2(y2[2] - a2f(e2[2]), y2[3] - a2f(e2[3])));
   }
 }
 
 int launch_rope_kv(const RopeArgs& a, cudaStream_t s) {
   if (a.n <= 0) return 0;
-  const long long total = static_cast<long long>(a.n) * (a.Hq + 2 * a.Hkv) * (a.DH / 2);
+  if (a.DH % 8 || a.ldqkv % 4) return cudaErrorInvalidValue;  // four pairs per thread, 16-byte rows
+  const long long total = static_cast<long long>(a.n) * (a.Hq + 2 * a.Hkv) * (a.DH / 8);
   if (total >= (1ll << 31)) return cudaErrorInvalidValue;
   return launch_k(rope_kv_kernel, dim3(static_cast<unsigned>((total + 255) / 256)), dim3(256), 0, s, a);
 }
