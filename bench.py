@@ -171,13 +171,13 @@ class ClockSampler:
 
 # DRAM traffic (read + write bytes) of one launch of a kernel, from one ncu
 # capture of it (the gate/up projection with its SwiGLU epilogue at 825 rows,
-# the single-pass 28-field request: dram__bytes_read.sum + dram__bytes_write.sum);
-# reported only while the GEMM sources hash to the ones that capture ran on,
-# else null.
+# two 128-row tiles per unit, in the single-pass 28-field request:
+# dram__bytes_read.sum + dram__bytes_write.sum); reported only while the GEMM
+# sources hash to the ones that capture ran on, else null.
 PROFILED_TRAFFIC = {
-    "gemm_gate_up": {"bytes_per_launch": 57.631488e6 + 0.714752e6,
+    "gemm_gate_up": {"bytes_per_launch": 57.636608e6 + 0.883712e6,
                      "sources": ("gemm.cu", "gemm.h", "ptx.cuh", "common.cuh"),
-                     "sha1": "a6574d53ae1aff6a57488180073420d5de777da5"},
+                     "sha1": "6488782f4433beece3585cb8e4ead732ba593186"},
 }
 
 
