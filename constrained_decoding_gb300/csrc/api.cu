@@ -12,6 +12,7 @@
 #include <map>
 #include <string>
 #include <tuple>
+#include <unordered_set>
 #include <vector>
 
 #include "common.cuh"
@@ -192,6 +193,11 @@ struct pcd_model {
   // 256-row side of a CTA-pair MMA (head dim 128 models); off unless
   // PCD_GEMM_SWAP=1: measured slower than the 128-row tiles on GB300
   bool swap_gemm = false;
+  // caches and plans created on this model and not yet freed: freeing the
+  // model releases their device memory and detaches them, so a later
+  // pcd_cache_free / pcd_plan_free only deletes the handle
+  std::unordered_set<pcd_cache*> live_caches;
+  std::unordered_set<pcd_plan*> live_plans;
   std::map<std::vector<int64_t>, std::pair<uint64_t, cudaGraphExec_t>> graph_cache;
 };
 
@@ -1659,6 +1665,7 @@ int new_cache(pcd_model* m, int cap, pcd_cache** out) {
   }
   pcd_cache* c = new pcd_cache();
   c->m = m;
+  m->live_caches.insert(c);
   c->mem = mem;
   c->bytes = got;
   c->cap = cap;
@@ -1948,6 +1955,17 @@ void pcd_model_free(pcd_model* m) {
                     &m->hr_lo})
     if (b->p) cudaFree(b->p);
   for (auto& e : m->cache_pool) cudaFree(e.second);
+  for (pcd_cache* c : m->live_caches) {
+    if (c->mem) cudaFree(c->mem);
+    c->mem = nullptr;
+    c->k = c->v = c->k_lo = c->v_lo = nullptr;
+    c->m = nullptr;
+  }
+  for (pcd_plan* p : m->live_plans) {
+    if (p->mem) cudaFree(p->mem);
+    p->mem = nullptr;
+    p->m = nullptr;
+  }
   if (m->wblob) cudaFree(m->wblob);
   if (m->fblob) cudaFree(m->fblob);
   if (m->rope) cudaFree(m->rope);
@@ -2032,7 +2050,10 @@ int pcd_cache_length(const pcd_cache* c) { return c ? c->len : 0; }
 
 void pcd_cache_free(pcd_cache* c) {
   if (!c) return;
-  if (c->m && c->mem) c->m->cache_pool.emplace_back(c->bytes, c->mem);
+  if (c->m) {  // else its model was freed first and released the memory
+    c->m->live_caches.erase(c);
+    if (c->mem) c->m->cache_pool.emplace_back(c->bytes, c->mem);
+  }
   delete c;
 }
 
@@ -2102,14 +2123,18 @@ int pcd_plan_create(pcd_model* m, const pcd_field* fields, int n_fields, pcd_pla
     delete p;
     return fail(PCD_ERR_CUDA, "plan upload");
   }
+  m->live_plans.insert(p);
   *out = p;
   return PCD_OK;
 }
 
 void pcd_plan_free(pcd_plan* p) {
   if (!p) return;
-  if (p->m && p->m->stream) cudaStreamSynchronize(p->m->stream);
-  if (p->mem) cudaFree(p->mem);
+  if (p->m) {  // else its model was freed first and released the memory
+    if (p->m->stream) cudaStreamSynchronize(p->m->stream);
+    p->m->live_plans.erase(p);
+    if (p->mem) cudaFree(p->mem);
+  }
   delete p;
 }
 

@@ -117,8 +117,8 @@ int launch_rmsnorm(const float* x, int ldx, const int32_t* rows, int n, int d, c
 }
 
 // ====================================================================== rope_kv
-// Thread per (token, head, rotation pair).  Rotate-half pairing (i, i + DH/2),
-// angle pos * theta^(-2i/DH) from a (cos, sin) table built in double precision.
+// Rotate-half pairing (i, i + DH/2), angle pos * theta^(-2i/DH) from a
+// (cos, sin) table built in double precision; four pairs per thread.
 __global__ void rope_kv_kernel(RopeArgs a) {
   griddep_launch_dependents();
   griddep_wait();

@@ -55,6 +55,36 @@ def test_cache_of_another_model_is_refused(tiny_weights):
     b.free()
 
 
+def test_handles_outliving_their_model():
+    """Freeing a model releases the device memory of its caches and plans and
+    detaches them: freeing them afterwards only deletes the handles, and a
+    detached cache or plan is refused by another model."""
+    import constrained_decoding_gb300.pcd as pcd
+    from constrained_decoding_gb300 import load
+    lib = load()
+    w = synth.make_weights(synth.model_config("tiny"), seed=0)
+    req = synth.make_request(1)
+    a = pcd.pcd_load_weights_host(w)
+    cache = pcd.pcd_prefill(a, req.prefix)
+    plan = pcd.pcd_plan_create(a, req.fields)
+    handles = (cache.handle, plan.handle)
+    lib.pcd_model_free(a.handle)        # through the C ABI: the binding's handles stay live
+    a.handle = None
+    b = pcd.pcd_load_weights_host(w)
+    with pytest.raises(pcd.PCDError) as ei:
+        pcd.pcd_score(b, cache, req.fields)
+    assert ei.value.code == -8
+    lib.pcd_cache_free(handles[0])
+    lib.pcd_plan_free(handles[1])
+    cache.handle = plan.handle = None
+    # the process is intact: the second model scores as usual
+    c2 = pcd.pcd_prefill(b, req.prefix)
+    got = pcd.pcd_score(b, c2, req.fields)
+    assert all(abs(float(np.sum(g.probs)) - 1.0) < 1e-4 for g in got)
+    c2.free()
+    b.free()
+
+
 def test_bounded_wait_gives_up():
     """A wait on an mbarrier that nothing arrives on ends after its limit with
     an error code in the device error word, and the stream stays usable."""
