@@ -231,7 +231,8 @@ def request_work(cfg, Lp: int, T: int, R: int, n_anc: int, mode: str):
     branch_flops = 2.0 * T * L * P + attn_branch + readout
     branch_bytes = weight_bytes + head_bytes + kv_bytes
     return dict(flops=flops, bytes=bytes_, gu_flops=gu_flops, branch_flops=branch_flops, branch_bytes=branch_bytes,
-                weight_bytes=weight_bytes, head_bytes=head_bytes, kv_bytes=kv_bytes)
+                weight_bytes=weight_bytes, head_bytes=head_bytes, kv_bytes=kv_bytes,
+                attn_prefix_flops=attn_prefix, attn_branch_flops=attn_branch)
 
 
 def roofline_frac(flops, bytes_, seconds, peaks):
@@ -595,8 +596,12 @@ def run_ours(args):
             work, bound = wk["gu_flops"], "tensor"
         elif cls == "gemm_branch":
             work, bound = 2.0 * T * wk["weight_bytes"] / 2, "tensor"
-        elif cls in ("attn_prefill", "attn_branch"):
-            work, bound = wk["kv_bytes"], "hbm"
+        elif cls == "attn_prefill":
+            work, bound = wk["attn_prefix_flops"], "tensor"
+        elif cls == "attn_branch":
+            # the single pass's tree attention also runs the causal prefix queries
+            work = wk["attn_branch_flops"] + (wk["attn_prefix_flops"] if args.mode == "single" else 0.0)
+            bound = "tensor"
         else:
             work, bound = wk["head_bytes"], "hbm"
         if bound == "hbm":

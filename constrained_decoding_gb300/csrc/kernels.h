@@ -127,6 +127,8 @@ struct TreeAttnArgs {
   const unsigned long long* tile_mask;      // [chunks][tpt] bit i: key i of the chunk is visible to the token
   float scale_log2;                         // log2(e) / sqrt(DH)
   int csk;                                  // CTAs (cluster size) per (tile, KV head): 1 .. 8
+  int lo_terms = 3;                         // with remainders: 1 = S takes Q K_lo + Q_lo K, 2 = O takes
+                                            // P V_lo + P_lo V
 };
 int launch_tree_attention(const TreeAttnArgs& a, cudaStream_t s);
 // The same on the tcgen05 tensor cores, head dim 128, tiles of tpt x G <= 128

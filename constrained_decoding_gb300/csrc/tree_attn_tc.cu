@@ -297,8 +297,10 @@ __global__ void __launch_bounds__(224, 1)
               const uint32_t qo = (k >> 2) * (kQBytes / 2) + (k & 3) * 32, ko = (k >> 2) * (kKVBytes / 2) + (k & 3) * 32;
               umma_f16(dS, sdesc_kmajor_sw128(qa + qo), sdesc_kmajor_sw128(ka + ko), kIdescS, k > 0 ? 1u : 0u);
               if constexpr (LO) {  // + Q K_lo + Q_lo K (the lo x lo term is below fp32 resolution of S)
-                umma_f16(dS, sdesc_kmajor_sw128(qa + qo), sdesc_kmajor_sw128(ka + kKVBytes + ko), kIdescS, 1u);
-                umma_f16(dS, sdesc_kmajor_sw128(qa + kQBytes + qo), sdesc_kmajor_sw128(ka + ko), kIdescS, 1u);
+                if (a.lo_terms & 1) {
+                  umma_f16(dS, sdesc_kmajor_sw128(qa + qo), sdesc_kmajor_sw128(ka + kKVBytes + ko), kIdescS, 1u);
+                  umma_f16(dS, sdesc_kmajor_sw128(qa + kQBytes + qo), sdesc_kmajor_sw128(ka + ko), kIdescS, 1u);
+                }
               }
             }
             umma_commit(&s_full[s]);
@@ -315,10 +317,12 @@ __global__ void __launch_bounds__(224, 1)
               umma_f16_ts(tbase + kColO, pcol + k * 8, sdesc_mnmajor_sw128(va + k * 16 * 128, kKVBytes / 2, 1024), kIdescO,
                           (n > 0 || k > 0) ? 1u : 0u);
               if constexpr (LO) {  // + P V_lo + P_lo V
-                umma_f16_ts(tbase + kColO, pcol + k * 8,
-                            sdesc_mnmajor_sw128(va + kKVBytes + k * 16 * 128, kKVBytes / 2, 1024), kIdescO, 1u);
-                umma_f16_ts(tbase + kColO, pcol + 32 + k * 8,
-                            sdesc_mnmajor_sw128(va + k * 16 * 128, kKVBytes / 2, 1024), kIdescO, 1u);
+                if (a.lo_terms & 2) {
+                  umma_f16_ts(tbase + kColO, pcol + k * 8,
+                              sdesc_mnmajor_sw128(va + kKVBytes + k * 16 * 128, kKVBytes / 2, 1024), kIdescO, 1u);
+                  umma_f16_ts(tbase + kColO, pcol + 32 + k * 8,
+                              sdesc_mnmajor_sw128(va + k * 16 * 128, kKVBytes / 2, 1024), kIdescO, 1u);
+                }
               }
             }
             umma_commit(&pv_done[s]);
