@@ -19,7 +19,9 @@ VARIANTS = {
     "tiny": [{"PCD_TREE_CSK": "1"}, {"PCD_TREE_CSK": "2"}, {"PCD_TREE_CSK": "3"}, {"PCD_TREE_CSK": "8"},
              {"PCD_TREE_ATTN": "0"}],
     "tiny-h128": [{}, {"PCD_TREE_CSK": "2"}, {"PCD_TREE_CSK": "3"}, {"PCD_TREE_CSK": "5"}, {"PCD_TREE_CSK": "8"},
-                  {"PCD_ATTN_TC": "0"}, {"PCD_TREE_ATTN": "0"}],
+                  {"PCD_ATTN_TC": "0"}, {"PCD_TREE_ATTN": "0"},
+                  # every remainder term of the attention (the 7B width's default), and none in P.V
+                  {"PCD_ATTN_LO_TERMS": "3"}, {"PCD_ATTN_LO_TERMS": "1"}, {"PCD_ATTN_LO_TERMS": "3", "PCD_TREE_CSK": "3"}],
 }
 CASES = [(shape, env) for shape, envs in VARIANTS.items() for env in envs]
 
