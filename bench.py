@@ -547,12 +547,14 @@ def run_ours(args):
     barrier(dist)
     torch.cuda.synchronize()
     e2e_ms = []
+    e2e_st = []
     h2d = d2h = 0
     t_e2e0 = time.perf_counter()
     for i in range(K):
         t0 = time.perf_counter()
         st, h2d = e2e_step(i)
         e2e_ms.append((time.perf_counter() - t0) * 1e3)
+        e2e_st.append(st)
         d2h = st["d2h_bytes"]
     e2e_s = max_over_ranks(dist, time.perf_counter() - t_e2e0)
     barrier(dist)
@@ -659,6 +661,11 @@ def run_ours(args):
                        "req_per_s": round(1e3 / other_ms, 3)},
         "e2e": {"value": round(n_total / e2e_s, 3), "unit": "req/s", "p50_latency_ms": round(statistics.median(e2e_ms), 4),
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                # where a request's time goes: inside the C call (plan compile,
+                # uploads, the pass, the result copy and sync) and its device part
+                "c_call_ms_p50": round(statistics.median(x["total_ms"] for x in e2e_st), 4),
+                "compile_ms_p50": round(statistics.median(x["compile_ms"] for x in e2e_st), 4),
+                "device_ms_p50": round(statistics.median(x["branch_ms"] for x in e2e_st), 4),
                 "note": "host ids in, host results out, per request; the schema packed once (pcd.Schema)"},
         "first_field_first": first_field_first,
         "gpu_launches": int(round(launches_per_step * K)),

@@ -42,22 +42,24 @@ constexpr int kOutLd = kDH * 2 + 16;         // staged output row (bytes): padde
 constexpr int kRedLd = kDH + 4;              // fp32 partial-O row stride for the cluster combine
 constexpr uint32_t kColS = 0;
 
-// Shared and tensor memory layout.  LO: q, k, v and P also carry their fp16
-// rounding remainders (a second tile next to each), with 2 K/V stages to fit;
-// otherwise 4 stages.
-template <bool LO>
+// Shared and tensor memory layout.  QLO: q and k also carry their fp16
+// rounding remainders (a second tile next to each) for the S cross terms;
+// VLO: v and P carry theirs for the P V cross terms.  Stages: 2 with both
+// sets of remainders, 3 with one, 4 without any.
+template <bool QLO, bool VLO>
 struct TcCfg {
-  static constexpr int kStages = LO ? 2 : 4;               // K and V stages: loads run ahead of the MMAs
-  static constexpr int kQAll = kQBytes * (LO ? 2 : 1);     // Q (then Q's remainder)
-  static constexpr int kKVSt = kKVBytes * (LO ? 2 : 1);    // one K (or V) stage: hi, then lo
+  static constexpr int kStages = (QLO && VLO) ? 2 : (QLO || VLO) ? 3 : 4;  // K and V stages: loads run ahead
+  static constexpr int kQAll = kQBytes * (QLO ? 2 : 1);     // Q (then Q's remainder)
+  static constexpr int kKSt = kKVBytes * (QLO ? 2 : 1);     // one K stage: hi, then lo
+  static constexpr int kVSt = kKVBytes * (VLO ? 2 : 1);     // one V stage: hi, then lo
   static constexpr int kOffK = kQAll;
-  static constexpr int kOffV = kOffK + kStages * kKVSt;
-  static constexpr int kOffBar = kOffV + kStages * kKVSt;
+  static constexpr int kOffV = kOffK + kStages * kKSt;
+  static constexpr int kOffBar = kOffV + kStages * kVSt;
   static constexpr int kOffML = kOffBar + 256;
   static constexpr int kSmem = kOffML + 2048 + 1024;      // + alignment slack
   // S (then P: hi in the first 32 columns, lo in the next 32) per stage, then O
   static constexpr uint32_t kColO = kStages * kKeys;
-  static constexpr uint32_t kTmemCols = LO ? 256 : 512;
+  static constexpr uint32_t kTmemCols = kColO + kDH <= 256 ? 256 : 512;
   static_assert(kColO + kDH <= kTmemCols, "S stages and O fit the TMEM allocation");
   static_assert(2 * kRows * kOutLd <= kOffBar, "staged hi and lo output rows fit the Q/K/V region");
   static_assert((kRows + 8) * kRedLd * 4 <= kOffBar, "received partial rows fit the Q/K/V region");
@@ -70,14 +72,15 @@ __device__ __forceinline__ uint32_t swz(int row, int chunk) {  // 128-byte swizz
   return static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128 + ((chunk ^ (row & 7)) << 4));
 }
 
-template <bool LO>
+template <bool QLO, bool VLO>
 __global__ void __launch_bounds__(224, 1)
     tree_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                         const __grid_constant__ CUtensorMap tmKlo, const __grid_constant__ CUtensorMap tmVlo,
                         const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmQlo,
                         const TreeAttnArgs a, int layer, uint64_t wait_ns, int* err) {
-  using C = TcCfg<LO>;
-  constexpr int kStages = C::kStages, kKVSt = C::kKVSt, kOffK = C::kOffK, kOffV = C::kOffV, kOffBar = C::kOffBar;
+  using C = TcCfg<QLO, VLO>;
+  constexpr int kStages = C::kStages, kKSt = C::kKSt, kVSt = C::kVSt, kOffK = C::kOffK, kOffV = C::kOffV,
+                kOffBar = C::kOffBar;
   constexpr int kOffML = C::kOffML;
   constexpr uint32_t kColO = C::kColO, kTmemCols = C::kTmemCols;
   extern __shared__ uint8_t tta_raw[];
@@ -145,11 +148,11 @@ __global__ void __launch_bounds__(224, 1)
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
-    if constexpr (LO) {
+    if constexpr (QLO) {
       tma_prefetch_desc(&tmQlo);
       tma_prefetch_desc(&tmKlo);
-      tma_prefetch_desc(&tmVlo);
     }
+    if constexpr (VLO) tma_prefetch_desc(&tmVlo);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -177,8 +180,8 @@ __global__ void __launch_bounds__(224, 1)
     const act_t* vbp = a.vb + static_cast<size_t>(hk) * a.n_br * kDH;
     // this (layer, KV head)'s rows in a batch request's cache
     const size_t seg_off = sgk ? (static_cast<size_t>(a.layer) * a.Hkv + hk) * static_cast<size_t>(sgk->cap) * kDH : 0;
-    const act_t* kblp = LO ? a.kb_lo + static_cast<size_t>(hk) * a.n_br * kDH : nullptr;
-    const act_t* vblp = LO ? a.vb_lo + static_cast<size_t>(hk) * a.n_br * kDH : nullptr;
+    const act_t* kblp = QLO ? a.kb_lo + static_cast<size_t>(hk) * a.n_br * kDH : nullptr;
+    const act_t* vblp = VLO ? a.vb_lo + static_cast<size_t>(hk) * a.n_br * kDH : nullptr;
     // rows of K or V (and remainder) by cp.async: an ancestor chunk's rows of
     // the branch K/V by index (keys), or a batch request's prefix rows j0.. of
     // its own cache; zero past the end
@@ -191,7 +194,7 @@ __global__ void __launch_bounds__(224, 1)
         const size_t off = static_cast<size_t>(ok ? j : 0) * kDH + c * 8;
         const uint32_t so = (c >> 3) * (kKVBytes / 2) + swz(kr, c & 7);
         cp_async16(dst + so, src + off, ok);
-        if constexpr (LO) cp_async16(dst + kKVBytes + so, src_lo + off, ok);
+        if (src_lo) cp_async16(dst + kKVBytes + so, src_lo + off, ok);
       }
       cp_async_commit();
       cp_async_wait<0>();
@@ -199,12 +202,12 @@ __global__ void __launch_bounds__(224, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar);
     };
-    // a prefix block by TMA: both 64-column halves, and the remainder's
+    // a prefix block by TMA: both 64-column halves, and the remainder's (lo)
     auto tma_block = [&](uint8_t* dst, const CUtensorMap* hi, const CUtensorMap* lo, int b, uint64_t* bar) {
-      mbar_arrive_expect_tx(bar, kKVSt);
+      mbar_arrive_expect_tx(bar, lo ? 2u * kKVBytes : static_cast<uint32_t>(kKVBytes));
       tma_load_4d(dst, hi, bar, 0, b * kKeys, hk, layer);
       tma_load_4d(dst + kKVBytes / 2, hi, bar, 64, b * kKeys, hk, layer);
-      if constexpr (LO) {
+      if (lo) {
         tma_load_4d(dst + kKVBytes, lo, bar, 0, b * kKeys, hk, layer);
         tma_load_4d(dst + kKVBytes + kKVBytes / 2, lo, bar, 64, b * kKeys, hk, layer);
       }
@@ -214,10 +217,10 @@ __global__ void __launch_bounds__(224, 1)
       // halves (and the remainder's), one box each; rows past tpt x G are
       // zeroed by the softmax warps
       const uint32_t box = 64u * static_cast<uint32_t>(G * a.tpt) * 2u;
-      mbar_arrive_expect_tx(q_full, (LO ? 4u : 2u) * box);
+      mbar_arrive_expect_tx(q_full, (QLO ? 4u : 2u) * box);
       tma_load_3d(smem + kOffQ, &tmQ, q_full, 0, hk * G, qrow0);
       tma_load_3d(smem + kOffQ + kQBytes / 2, &tmQ, q_full, 64, hk * G, qrow0);
-      if constexpr (LO) {
+      if constexpr (QLO) {
         tma_load_3d(smem + kOffQ + kQBytes, &tmQlo, q_full, 0, hk * G, qrow0);
         tma_load_3d(smem + kOffQ + kQBytes + kQBytes / 2, &tmQlo, q_full, 64, hk * G, qrow0);
       }
@@ -233,13 +236,13 @@ __global__ void __launch_bounds__(224, 1)
         if (lane == 0) fail(DEV_WAIT_TIMEOUT_PRODUCER);
         break;
       }
-      uint8_t* kd = smem + kOffK + s * kKVSt;
+      uint8_t* kd = smem + kOffK + s * kKSt;
       if (keys) {
         gather(kd, kbp, kblp, keys, 0, 0, &k_full[s]);
       } else if (sgk) {
-        gather(kd, sgk->k + seg_off, LO ? sgk->k_lo + seg_off : nullptr, nullptr, b * kKeys, pf_keys, &k_full[s]);
+        gather(kd, sgk->k + seg_off, QLO ? sgk->k_lo + seg_off : nullptr, nullptr, b * kKeys, pf_keys, &k_full[s]);
       } else {
-        if (lane == 0) tma_block(kd, &tmK, &tmKlo, b, &k_full[s]);
+        if (lane == 0) tma_block(kd, &tmK, QLO ? &tmKlo : nullptr, b, &k_full[s]);
       }
       ++kissued[s];
       // the V stage is free once the P V of block i - kStages is done
@@ -247,13 +250,13 @@ __global__ void __launch_bounds__(224, 1)
         if (lane == 0) fail(DEV_WAIT_TIMEOUT_PRODUCER);
         break;
       }
-      uint8_t* vd = smem + kOffV + s * kKVSt;
+      uint8_t* vd = smem + kOffV + s * kVSt;
       if (keys) {
         gather(vd, vbp, vblp, keys, 0, 0, &v_full[s]);
       } else if (sgk) {
-        gather(vd, sgk->v + seg_off, LO ? sgk->v_lo + seg_off : nullptr, nullptr, b * kKeys, pf_keys, &v_full[s]);
+        gather(vd, sgk->v + seg_off, VLO ? sgk->v_lo + seg_off : nullptr, nullptr, b * kKeys, pf_keys, &v_full[s]);
       } else {
-        if (lane == 0) tma_block(vd, &tmV, &tmVlo, b, &v_full[s]);
+        if (lane == 0) tma_block(vd, &tmV, VLO ? &tmVlo : nullptr, b, &v_full[s]);
       }
       ++vissued[s];
       __syncwarp();
@@ -290,17 +293,15 @@ __global__ void __launch_bounds__(224, 1)
                   (n < kStages || mbar_test(&pv_done[s], static_cast<uint32_t>(((n - kStages) / kStages) & 1)));
           if (ready) {
             tc_fence_after_sync();
-            const uint32_t ka = smem_u32(smem + kOffK + s * kKVSt);
+            const uint32_t ka = smem_u32(smem + kOffK + s * kKSt);
             const uint32_t dS = tbase + kColS + s * kKeys;
 #pragma unroll
             for (int k = 0; k < kDH / 16; ++k) {
               const uint32_t qo = (k >> 2) * (kQBytes / 2) + (k & 3) * 32, ko = (k >> 2) * (kKVBytes / 2) + (k & 3) * 32;
               umma_f16(dS, sdesc_kmajor_sw128(qa + qo), sdesc_kmajor_sw128(ka + ko), kIdescS, k > 0 ? 1u : 0u);
-              if constexpr (LO) {  // + Q K_lo + Q_lo K (the lo x lo term is below fp32 resolution of S)
-                if (a.lo_terms & 1) {
-                  umma_f16(dS, sdesc_kmajor_sw128(qa + qo), sdesc_kmajor_sw128(ka + kKVBytes + ko), kIdescS, 1u);
-                  umma_f16(dS, sdesc_kmajor_sw128(qa + kQBytes + qo), sdesc_kmajor_sw128(ka + ko), kIdescS, 1u);
-                }
+              if constexpr (QLO) {  // + Q K_lo + Q_lo K (the lo x lo term is below fp32 resolution of S)
+                umma_f16(dS, sdesc_kmajor_sw128(qa + qo), sdesc_kmajor_sw128(ka + kKVBytes + ko), kIdescS, 1u);
+                umma_f16(dS, sdesc_kmajor_sw128(qa + kQBytes + qo), sdesc_kmajor_sw128(ka + ko), kIdescS, 1u);
               }
             }
             umma_commit(&s_full[s]);
@@ -310,19 +311,17 @@ __global__ void __launch_bounds__(224, 1)
           ready = mbar_test(&p_full[s], par) && mbar_test(&v_full[s], par);
           if (ready) {
             tc_fence_after_sync();
-            const uint32_t va = smem_u32(smem + kOffV + s * kKVSt);
+            const uint32_t va = smem_u32(smem + kOffV + s * kVSt);
             const uint32_t pcol = tbase + kColS + s * kKeys;
 #pragma unroll
             for (int k = 0; k < kKeys / 16; ++k) {  // P: 16 keys = 8 packed columns per step
               umma_f16_ts(tbase + kColO, pcol + k * 8, sdesc_mnmajor_sw128(va + k * 16 * 128, kKVBytes / 2, 1024), kIdescO,
                           (n > 0 || k > 0) ? 1u : 0u);
-              if constexpr (LO) {  // + P V_lo + P_lo V
-                if (a.lo_terms & 2) {
-                  umma_f16_ts(tbase + kColO, pcol + k * 8,
-                              sdesc_mnmajor_sw128(va + kKVBytes + k * 16 * 128, kKVBytes / 2, 1024), kIdescO, 1u);
-                  umma_f16_ts(tbase + kColO, pcol + 32 + k * 8,
-                              sdesc_mnmajor_sw128(va + k * 16 * 128, kKVBytes / 2, 1024), kIdescO, 1u);
-                }
+              if constexpr (VLO) {  // + P V_lo + P_lo V
+                umma_f16_ts(tbase + kColO, pcol + k * 8,
+                            sdesc_mnmajor_sw128(va + kKVBytes + k * 16 * 128, kKVBytes / 2, 1024), kIdescO, 1u);
+                umma_f16_ts(tbase + kColO, pcol + 32 + k * 8, sdesc_mnmajor_sw128(va + k * 16 * 128, kKVBytes / 2, 1024),
+                            kIdescO, 1u);
               }
             }
             umma_commit(&pv_done[s]);
@@ -354,7 +353,7 @@ __global__ void __launch_bounds__(224, 1)
     {  // the Q tile arrives by TMA (rows tt * G + g); the rows past it are zero
       if (r >= a.tpt * G) {
 #pragma unroll 1
-        for (int part = 0; part < (LO ? 2 : 1); ++part)
+        for (int part = 0; part < (QLO ? 2 : 1); ++part)
 #pragma unroll
           for (int c = 0; c < 16; ++c)
             *reinterpret_cast<uint4*>(smem + kOffQ + part * kQBytes + (c >> 3) * (kQBytes / 2) + swz(r, c & 7)) =
@@ -435,14 +434,14 @@ __global__ void __launch_bounds__(224, 1)
         const float p1 = ex2_approx(fmaf(sv[2 * c2 + 1], a.scale_log2, -mo));
         ps += p0 + p1;
         pw[c2] = pack2(p0, p1);
-        if constexpr (LO) {  // the remainders, kept in sv for the second store
+        if constexpr (VLO) {  // the remainders, kept in sv for the second store
           const float2 h = __half22float2(*reinterpret_cast<const __half2*>(&pw[c2]));
           sv[2 * c2] = p0 - h.x;
           sv[2 * c2 + 1] = p1 - h.y;
         }
       }
       tmem_st_32cols_u32(trow + kColS + s * kKeys, pw);
-      if constexpr (LO) {
+      if constexpr (VLO) {
 #pragma unroll
         for (int c2 = 0; c2 < kKeys / 2; ++c2) pw[c2] = pack2(sv[2 * c2], sv[2 * c2 + 1]);
         tmem_st_32cols_u32(trow + kColS + s * kKeys + 32, pw);
@@ -588,14 +587,15 @@ __global__ void __launch_bounds__(224, 1)
 
 }  // namespace
 
-template <bool LO>
+template <bool QLO, bool VLO>
 static int launch_tc_t(const TreeAttnArgs& a, const CUtensorMap& tmK, const CUtensorMap& tmV, const CUtensorMap& tmKlo,
                        const CUtensorMap& tmVlo, const CUtensorMap& tmQ, const CUtensorMap& tmQlo, int layer,
                        uint64_t wait_ns, int* err, cudaStream_t s) {
-  using C = TcCfg<LO>;
+  using C = TcCfg<QLO, VLO>;
   static bool attr = false;
   if (!attr) {
-    cudaError_t r = cudaFuncSetAttribute(tree_attn_tc_kernel<LO>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+    cudaError_t r =
+        cudaFuncSetAttribute(tree_attn_tc_kernel<QLO, VLO>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
     if (r != cudaSuccess) return r;
     attr = true;
   }
@@ -620,7 +620,7 @@ static int launch_tc_t(const TreeAttnArgs& a, const CUtensorMap& tmK, const CUte
   }
   cfg.attrs = at;
   cfg.numAttrs = na;
-  return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<LO>, tmK, tmV, tmKlo, tmVlo, tmQ, tmQlo, a, layer, wait_ns, err);
+  return cudaLaunchKernelEx(&cfg, tree_attn_tc_kernel<QLO, VLO>, tmK, tmV, tmKlo, tmVlo, tmQ, tmQlo, a, layer, wait_ns, err);
 }
 
 int tree_attention_tc_slots(int csk) {
@@ -629,8 +629,9 @@ int tree_attention_tc_slots(int csk) {
   static int cache[9] = {};
   if (csk < 1 || csk > 8) return 0;
   if (cache[csk]) return cache[csk];
-  using C = TcCfg<true>;
-  auto kern = tree_attn_tc_kernel<true>;
+  // every variant runs one CTA per SM; the largest one's footprint decides
+  using C = TcCfg<true, true>;
+  auto kern = tree_attn_tc_kernel<true, true>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem) != cudaSuccess) return 0;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
@@ -671,16 +672,19 @@ int launch_tree_attention_tc(const TreeAttnArgs& a, const CUtensorMap& tmK, cons
   if (a.tpt < 1 || a.tpt * (a.Hq / a.Hkv) > kRows) return cudaErrorInvalidValue;
   const bool lo = a.q_lo != nullptr;
   if (lo && (!tmKlo || !tmVlo || (a.n_br_tiles > 0 && (!a.kb_lo || !a.vb_lo)))) return cudaErrorInvalidValue;
+  const bool qlo = lo && (a.lo_terms & 1) != 0, vlo = lo && (a.lo_terms & 2) != 0;
   // the Q tiles by TMA: the q rows hold every head of a token side by side
   const int G = a.Hq / a.Hkv;
   const int q_rows = std::max(a.n_pf, a.n_br_tiles > 0 ? a.br_row0 + a.n_br : 0);
   CUtensorMap mq, mql;
   if (!make_q_map(&mq, a.q, kDH, a.Hq, std::max(q_rows, 1), G, a.tpt)) return cudaErrorInvalidValue;
-  if (lo) {
+  if (qlo) {
     if (!make_q_map(&mql, a.q_lo, kDH, a.Hq, std::max(q_rows, 1), G, a.tpt)) return cudaErrorInvalidValue;
-    return launch_tc_t<true>(a, tmK, tmV, *tmKlo, *tmVlo, mq, mql, layer, wait_ns, err, s);
+    if (vlo) return launch_tc_t<true, true>(a, tmK, tmV, *tmKlo, *tmVlo, mq, mql, layer, wait_ns, err, s);
+    return launch_tc_t<true, false>(a, tmK, tmV, *tmKlo, tmV, mq, mql, layer, wait_ns, err, s);
   }
-  return launch_tc_t<false>(a, tmK, tmV, tmK, tmV, mq, mq, layer, wait_ns, err, s);
+  if (vlo) return launch_tc_t<false, true>(a, tmK, tmV, tmK, *tmVlo, mq, mq, layer, wait_ns, err, s);
+  return launch_tc_t<false, false>(a, tmK, tmV, tmK, tmV, mq, mq, layer, wait_ns, err, s);
 }
 
 }  // namespace pcd
