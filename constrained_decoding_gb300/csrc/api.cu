@@ -153,10 +153,13 @@ struct pcd_model {
   uint64_t wait_ns = 2000000000ull;
   DevBuf x32, xn, xn_lo, qkv, q, q_lo, kb, vb, kb_lo, vb_lo, att, att_lo, hb, hb_lo, hr_lo, part_o, part_ml, hr, ro_part, z, lse, plan_buf,
       result, ids;
-  // pinned staging: `up` feeds host->device copies (reused only once the last
-  // copy from it has completed: up_ev), `down` receives results
+  // pinned staging: `up` feeds host->device copies, filled front to back
+  // (up_off) and rewound only once the last copy from it has completed
+  // (up_ev), so a call's several uploads never wait on one another; `down`
+  // receives results
   void* up = nullptr;
   size_t up_n = 0;
+  size_t up_off = 0;
   void* down = nullptr;
   size_t down_n = 0;
   cudaEvent_t up_ev = nullptr;
@@ -250,15 +253,23 @@ int ensure_pinned(void*& buf, size_t& cap, size_t bytes) {
 // Copies `bytes` of host data to `dst` on the model stream through the pinned
 // upload buffer.
 int upload_async(pcd_model* m, void* dst, const void* src, size_t bytes) {
-  if (m->up_pending) {
-    cudaEventSynchronize(m->up_ev);
-    m->up_pending = false;
+  const size_t need = (bytes + 255) & ~static_cast<size_t>(255);
+  if (!m->up_pending) m->up_off = 0;  // nothing in flight (the last call synchronised)
+  if (m->up_off + need > m->up_n) {
+    // full: wait for the copies in flight, then start over (growing if needed)
+    if (m->up_pending) {
+      cudaEventSynchronize(m->up_ev);
+      m->up_pending = false;
+    }
+    m->up_off = 0;
+    PCD_TRY(ensure_pinned(m->up, m->up_n, std::max(need, static_cast<size_t>(1) << 18)));
   }
-  PCD_TRY(ensure_pinned(m->up, m->up_n, bytes));
-  std::memcpy(m->up, src, bytes);
-  PCD_CUDA(cudaMemcpyAsync(dst, m->up, bytes, cudaMemcpyHostToDevice, m->stream));
+  uint8_t* stage = static_cast<uint8_t*>(m->up) + m->up_off;
+  std::memcpy(stage, src, bytes);
+  PCD_CUDA(cudaMemcpyAsync(dst, stage, bytes, cudaMemcpyHostToDevice, m->stream));
   cudaEventRecord(m->up_ev, m->stream);
   m->up_pending = true;
+  m->up_off += need;
   return PCD_OK;
 }
 
