@@ -150,6 +150,7 @@ struct pcd_model {
   float* final_norm = nullptr;
   float2* rope = nullptr;
   int* d_err = nullptr;
+  int* h_err = nullptr;  // pinned: where the error word is copied behind a call's work
   uint64_t wait_ns = 2000000000ull;
   DevBuf x32, xn, xn_lo, qkv, q, q_lo, kb, vb, kb_lo, vb_lo, att, att_lo, hb, hb_lo, hr_lo, part_o, part_ml, hr, ro_part, z, lse, plan_buf,
       result, ids;
@@ -1382,9 +1383,13 @@ int check_positions(const pcd_model* m, int prefix_len, int max_rel) {
   return PCD_OK;
 }
 
-int read_device_error(pcd_model* m) {
-  int h = 0;
-  PCD_CUDA(cudaMemcpy(&h, m->d_err, sizeof(int), cudaMemcpyDeviceToHost));
+// Waits for the model stream and maps the device error word to a status
+// (resetting it).  The word is copied into pinned memory behind the work
+// already queued (result copies included), so one wait collects both.
+int sync_read_error(pcd_model* m) {
+  PCD_CUDA(cudaMemcpyAsync(m->h_err, m->d_err, sizeof(int), cudaMemcpyDeviceToHost, m->stream));
+  PCD_CUDA(cudaStreamSynchronize(m->stream));
+  const int h = *m->h_err;
   if (h != 0) {
     cudaMemset(m->d_err, 0, sizeof(int));
     if (h == pcd::DEV_BAD_INDEX) return fail(PCD_ERR_TOKEN_RANGE, "a device kernel met a token id or position out of range");
@@ -1636,6 +1641,11 @@ int build_model(const pcd_model_config& cfg, TensorFn get, void* ctx, int dtype,
     return cleanup(fail(PCD_ERR_OOM, "error word"));
   }
   cudaMemset(m->d_err, 0, sizeof(int));
+  if (cudaMallocHost(&m->h_err, sizeof(int)) != cudaSuccess) {
+    cudaGetLastError();
+    m->h_err = nullptr;
+    return cleanup(fail(PCD_ERR_OOM, "pinned error word"));
+  }
   cudaEventCreateWithFlags(&m->up_ev, cudaEventDisableTiming);
   cudaEventCreate(&m->ev_a);
   cudaEventCreate(&m->ev_b);
@@ -1802,9 +1812,11 @@ int score_impl(pcd_model* m, const pcd_cache* const* caches, const pcd_field* co
   const size_t rbytes = static_cast<size_t>(v.result_floats()) * 4;
   PCD_TRY(ensure_pinned(m->down, m->down_n, rbytes));
   PCD_CUDA(cudaMemcpyAsync(m->down, m->result.p, rbytes, cudaMemcpyDeviceToHost, m->stream));
-  PCD_CUDA(cudaStreamSynchronize(m->stream));
-  m->up_pending = false;
-  PCD_TRY(read_device_error(m));
+  {
+    const int e = sync_read_error(m);
+    if (e == PCD_OK || e != PCD_ERR_CUDA) m->up_pending = false;  // the stream has drained
+    PCD_TRY(e);
+  }
   for (int r = 0; r < n_req; ++r)
     unpack_results(static_cast<const float*>(m->down), v, field0[r], label0[r], n_fields[r], out[r]);
   if (stats) {
@@ -1994,6 +2006,7 @@ void pcd_model_free(pcd_model* m) {
   if (m->fblob) cudaFree(m->fblob);
   if (m->rope) cudaFree(m->rope);
   if (m->d_err) cudaFree(m->d_err);
+  if (m->h_err) cudaFreeHost(m->h_err);
   if (m->up) cudaFreeHost(m->up);
   if (m->down) cudaFreeHost(m->down);
   if (m->up_ev) cudaEventDestroy(m->up_ev);
@@ -2202,9 +2215,10 @@ int pcd_prefill_score(pcd_model* m, const int32_t* ids, int n, const pcd_field* 
   r = ensure_pinned(m->down, m->down_n, rbytes);
   if (r == PCD_OK && cudaMemcpyAsync(m->down, m->result.p, rbytes, cudaMemcpyDeviceToHost, m->stream) != cudaSuccess)
     r = fail(PCD_ERR_CUDA, "result copy");
-  if (r == PCD_OK && cudaStreamSynchronize(m->stream) != cudaSuccess) r = fail(PCD_ERR_CUDA, "stream sync");
-  m->up_pending = false;
-  if (r == PCD_OK) r = read_device_error(m);
+  if (r == PCD_OK) {
+    r = sync_read_error(m);
+    if (r != PCD_ERR_CUDA) m->up_pending = false;  // the stream has drained
+  }
   if (r != PCD_OK) {
     pcd_cache_free(c);
     return r;
@@ -2251,8 +2265,9 @@ int pcd_prefill_score_plan_device(pcd_model* m, const int32_t* ids_device, int n
 
 int pcd_sync(pcd_model* m) {
   if (!m) return fail(PCD_ERR_INVALID_ARG, "NULL model");
-  PCD_CUDA(cudaStreamSynchronize(m->stream));
-  return read_device_error(m);
+  const int r = sync_read_error(m);
+  if (r != PCD_ERR_CUDA) m->up_pending = false;
+  return r;
 }
 
 int pcd_profile_enable(pcd_model* m, int on) {

@@ -6,6 +6,7 @@ the hot path runs in the library's CUDA kernels.
 from __future__ import annotations
 
 import ctypes
+import functools
 import weakref
 from dataclasses import dataclass
 from typing import List, Optional, Sequence
@@ -44,7 +45,7 @@ def _stream_handle(stream) -> Optional[int]:
     return int(getattr(stream, "cuda_stream", stream))
 
 
-@dataclass
+@dataclass(slots=True)
 class FieldResult:
     probs: np.ndarray
     logprobs: np.ndarray
@@ -309,27 +310,39 @@ def _Fields(fields) -> Schema:
     return fields if isinstance(fields, Schema) else Schema(fields)
 
 
+@functools.lru_cache(maxsize=256)
+def _result_layout(n_cands: tuple):
+    """Per field count list: the total, each field's offset into the float
+    buffer, and result structs whose probs/logprobs hold byte offsets."""
+    total = int(sum(n_cands))
+    offs = np.concatenate([[0], np.cumsum(n_cands, dtype=np.int64)])[:-1].astype(np.uint64)
+    a = np.zeros(len(n_cands), _RESULT_DT)
+    four = np.uint64(4)
+    a["probs"] = four * offs
+    a["logprobs"] = four * (np.uint64(total) + offs)
+    return total, offs.tolist(), a
+
+
 class _Results:
     """Result structs and one float buffer (probs, then logprobs) for a call."""
 
     def __init__(self, n_cands: List[int]):
         self.n_cands = list(n_cands)
-        self.total = int(sum(self.n_cands))
+        self.total, self.offs, tmpl = _result_layout(tuple(self.n_cands))
         self.buf = np.zeros(2 * max(self.total, 1), np.float32)
-        self.offs = np.concatenate([[0], np.cumsum(self.n_cands, dtype=np.int64)])[:-1].astype(np.uint64)
-        a = np.zeros(len(self.n_cands), _RESULT_DT)
+        a = tmpl.copy()
         base = np.uint64(self.buf.ctypes.data)
-        four = np.uint64(4)
-        a["probs"] = base + four * self.offs
-        a["logprobs"] = base + four * (np.uint64(self.total) + self.offs)
+        a["probs"] += base
+        a["logprobs"] += base
         self.structs = a
         self.arr = ctypes.cast(a.ctypes.data, ctypes.POINTER(D.pcd_field_result))
 
     def results(self) -> List[FieldResult]:
         a = self.structs
         t = self.total
-        return [FieldResult(self.buf[o:o + n], self.buf[t + o:t + o + n], lab, m, lm, mg, fm)
-                for o, n, lab, m, lm, mg, fm in zip(self.offs.tolist(), self.n_cands, a["label"].tolist(),
+        buf = self.buf
+        return [FieldResult(buf[o:o + n], buf[t + o:t + o + n], lab, m, lm, mg, fm)
+                for o, n, lab, m, lm, mg, fm in zip(self.offs, self.n_cands, a["label"].tolist(),
                                                     a["mass"].tolist(), a["log_mass"].tolist(),
                                                     a["margin"].tolist(), a["first_mass"].tolist())]
 

@@ -17,9 +17,11 @@ pytestmark = pytest.mark.gpu
 def test_weight_file_loads_like_host_arrays(tmp_path, shape):
     """A model loaded from a .pcdw file scores like the same weights passed
     as host arrays.  At head dim 128 the projections run split-K with fp32
-    atomic adds, whose order varies from run to run, so the two agree to
-    that run-to-run spread (~1e-6 in probabilities, ~1e-5 relative in
-    log-probs near -20), not bit for bit."""
+    atomic adds, whose order varies from run to run; a different order can
+    tip an fp16 rounding of an activation, so the two agree to that
+    run-to-run spread (seen up to 3e-5 in a probability), not bit for bit.
+    The bounds sit well above that spread and far below what a misread or
+    misconverted tensor gives (differences of order 0.1)."""
     import constrained_decoding_gb300.pcd as pcd
     w = synth.make_weights(synth.model_config(shape), seed=0)
     path = tmp_path / f"{shape}.pcdw"
@@ -32,10 +34,10 @@ def test_weight_file_loads_like_host_arrays(tmp_path, shape):
         c.free()
         m.free()
     for a, b in zip(*results):
-        np.testing.assert_allclose(a.probs, b.probs, rtol=0, atol=2e-5)
-        np.testing.assert_allclose(a.logprobs, b.logprobs, rtol=1e-4, atol=1e-4)
+        np.testing.assert_allclose(a.probs, b.probs, rtol=0, atol=2e-4)
+        np.testing.assert_allclose(a.logprobs, b.logprobs, rtol=1e-3, atol=1e-3)
         assert a.label == b.label
-        assert abs(a.mass - b.mass) <= 1e-4 * max(1.0, abs(b.mass))
+        assert abs(a.mass - b.mass) <= 1e-3 * max(1.0, abs(b.mass))
 
 
 def test_cache_of_another_model_is_refused(tiny_weights):

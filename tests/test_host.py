@@ -347,3 +347,24 @@ def test_reference_arm_other_ranks_exit_without_work():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
                         "--warmup", "0"], env=env, capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_result_buffers_are_per_call():
+    """Result structs point into their own call's float buffer (probs, then
+    logprobs, field by field), and a second call gets a fresh buffer even
+    though the layout is shared."""
+    from constrained_decoding_gb300 import pcd
+    n = [4, 2, 3]
+    r1, r2 = pcd._Results(n), pcd._Results(n)
+    for r in (r1, r2):
+        base = r.buf.ctypes.data
+        assert r.total == 9 and r.buf.size == 18
+        assert r.structs["probs"].tolist() == [base, base + 16, base + 24]
+        assert r.structs["logprobs"].tolist() == [base + 36, base + 52, base + 60]
+    assert r1.buf.ctypes.data != r2.buf.ctypes.data
+    r1.buf[:] = np.arange(18)
+    r1.structs["label"] = [3, 1, 0]
+    out = r1.results()
+    assert [x.label for x in out] == [3, 1, 0]
+    assert out[1].probs.tolist() == [4.0, 5.0] and out[2].logprobs.tolist() == [15.0, 16.0, 17.0]
+    assert r2.results()[0].probs.tolist() == [0.0] * 4
