@@ -12,13 +12,14 @@
 // The running maximum m is only moved (and O, l rescaled) when a block's
 // maximum exceeds it by more than 14 (log2 units): every P stays <= 2^14, a
 // finite fp16, and the result is exact up to rounding, while the rescale
-// (which waits for the previous P V) is rare.  Warp 0 loads K/V (TMA for prefix
-// blocks, gathered cp.async for ancestor chunks), warp 1 issues the S MMAs and
-// warp 6 the P V MMAs,
-// warps 2-5 run the softmax and the epilogue; P goes back into TMEM over its
-// own S columns and is the A operand of the P V MMA.  A (csk, 1, 1) cluster splits
-// a tile's key blocks and combines the partial softmax states through
-// distributed shared memory.
+// (which waits for the previous P V) is rare.  Warp 0 loads K/V (TMA for
+// prefix blocks, gathered cp.async for ancestor chunks), warp 1 issues the S
+// MMAs and warp 6 the P V MMAs, warps 2-5 run the softmax and the epilogue;
+// P goes back into TMEM over its own S columns and is the A operand of the
+// P V MMA.  With fp16 rounding remainders, S takes Q K_lo + Q_lo K and O
+// takes P V_lo + P_lo V (each set optional: a template variant per set).  A
+// (csk, 1, 1) cluster splits a tile's key blocks and combines the partial
+// softmax states through distributed shared memory.
 #include <algorithm>
 #include <climits>
 #include <cstdint>
