@@ -1,9 +1,11 @@
 // Branch compiler (see plan.h).
 #include "plan.h"
 
+#include <algorithm>
+#include <climits>
 #include <cmath>
-#include <map>
 #include <string>
+#include <utility>
 #include <vector>
 
 namespace pcd {
@@ -13,10 +15,11 @@ struct Node {
   int token = -1;
   int parent = -1;
   int depth = 0;
-  std::map<int, int> children;  // token -> node
   bool label_end = false;
-  int branch = -1;              // branch token index (internal nodes)
-  int row = -1;                 // readout row (root and internal nodes)
+  int branch = -1;  // branch token index (internal nodes)
+  int row = -1;     // readout row (root and internal nodes)
+  int entry = -1;   // child entry of the edge parent -> this node
+  std::vector<std::pair<int, int>> kids;  // (token, node), ascending token
 };
 }  // namespace
 
@@ -52,112 +55,81 @@ int compile_fields(const pcd_field* fields, int n_fields, int vocab, HostPlan* p
   }
   if (n_ctx - 1 > p->max_rel) p->max_rel = n_ctx - 1;
 
+  // reused across fields
+  std::vector<Node> nodes;
+  std::vector<int> lab_node, lab_start, order, chain, paths;
   for (int f = 0; f < n_fields; ++f) {
     const pcd_field& F = fields[f];
-    const std::string where = "field " + std::to_string(p->n_fields) + ": ";
-    if (F.n_scaffold < 1 || !F.scaffold) {
-      *msg = where + "the scaffold needs at least one token";
-      return PCD_ERR_INVALID_ARG;
-    }
-    if (F.n_cands > 255) {
-      *msg = where + std::to_string(F.n_cands) + " candidates (at most 255)";
-      return PCD_ERR_TOO_MANY_CANDIDATES;
-    }
-    if (F.n_cands < 2) {
-      *msg = where + "fewer than 2 candidates";
-      return PCD_ERR_TOO_FEW_CANDIDATES;
-    }
-    if (!F.cand_tokens || !F.cand_offsets || F.cand_offsets[0] != 0) {
-      *msg = where + "candidate arrays missing or cand_offsets[0] != 0";
-      return PCD_ERR_INVALID_ARG;
-    }
-    if (!(F.temperature >= 0.f) || std::isinf(F.temperature)) {
-      *msg = where + "temperature must be finite and >= 0";
-      return PCD_ERR_INVALID_ARG;
-    }
+    // the message names the field only when there is an error
+    auto bad = [&](int code, const std::string& text) {
+      *msg = "field " + std::to_string(p->n_fields) + ": " + text;
+      return code;
+    };
+    if (F.n_scaffold < 1 || !F.scaffold) return bad(PCD_ERR_INVALID_ARG, "the scaffold needs at least one token");
+    if (F.n_cands > 255)
+      return bad(PCD_ERR_TOO_MANY_CANDIDATES, std::to_string(F.n_cands) + " candidates (at most 255)");
+    if (F.n_cands < 2) return bad(PCD_ERR_TOO_FEW_CANDIDATES, "fewer than 2 candidates");
+    if (!F.cand_tokens || !F.cand_offsets || F.cand_offsets[0] != 0)
+      return bad(PCD_ERR_INVALID_ARG, "candidate arrays missing or cand_offsets[0] != 0");
+    if (!(F.temperature >= 0.f) || std::isinf(F.temperature))
+      return bad(PCD_ERR_INVALID_ARG, "temperature must be finite and >= 0");
     // spellings: the label each candidate path spells
     int n_out = F.n_cands;
     if (F.cand_label) {
       n_out = F.n_labels;
-      if (n_out < 2) {
-        *msg = where + "fewer than 2 labels";
-        return PCD_ERR_TOO_FEW_CANDIDATES;
-      }
-      if (n_out > F.n_cands) {
-        *msg = where + "more labels than candidate paths";
-        return PCD_ERR_INVALID_ARG;
-      }
-      std::vector<int> paths(n_out, 0);
+      if (n_out < 2) return bad(PCD_ERR_TOO_FEW_CANDIDATES, "fewer than 2 labels");
+      if (n_out > F.n_cands) return bad(PCD_ERR_INVALID_ARG, "more labels than candidate paths");
+      paths.assign(n_out, 0);
       for (int c = 0; c < F.n_cands; ++c) {
-        if (F.cand_label[c] < 0 || F.cand_label[c] >= n_out) {
-          *msg = where + "cand_label out of range";
-          return PCD_ERR_INVALID_ARG;
-        }
+        if (F.cand_label[c] < 0 || F.cand_label[c] >= n_out) return bad(PCD_ERR_INVALID_ARG, "cand_label out of range");
         paths[F.cand_label[c]]++;
       }
       for (int l = 0; l < n_out; ++l)
-        if (!paths[l]) {
-          *msg = where + "label " + std::to_string(l) + " has no spelling";
-          return PCD_ERR_INVALID_ARG;
-        }
+        if (!paths[l]) return bad(PCD_ERR_INVALID_ARG, "label " + std::to_string(l) + " has no spelling");
     }
-    if (F.scoring != PCD_SCORE_SUM && F.scoring != PCD_SCORE_MEAN && F.scoring != PCD_SCORE_LEVEL) {
-      *msg = where + "unknown scoring rule " + std::to_string(F.scoring);
-      return PCD_ERR_INVALID_ARG;
-    }
+    if (F.scoring != PCD_SCORE_SUM && F.scoring != PCD_SCORE_MEAN && F.scoring != PCD_SCORE_LEVEL)
+      return bad(PCD_ERR_INVALID_ARG, "unknown scoring rule " + std::to_string(F.scoring));
     for (int k = 0; k < F.n_scaffold; ++k)
-      if (F.scaffold[k] < 0 || F.scaffold[k] >= vocab) {
-        *msg = where + "scaffold token out of range";
-        return PCD_ERR_TOKEN_RANGE;
-      }
+      if (F.scaffold[k] < 0 || F.scaffold[k] >= vocab) return bad(PCD_ERR_TOKEN_RANGE, "scaffold token out of range");
 
-    // ---- trie of the label paths
-    std::vector<Node> nodes(1);  // node 0: the scaffold end
-    std::vector<std::vector<int>> label_nodes(F.n_cands);
+    // ---- trie of the label paths; node 0 is the scaffold end
+    nodes.assign(1, Node());
+    lab_node.clear();
+    lab_start.assign(1, 0);
     for (int c = 0; c < F.n_cands; ++c) {
       const int b = F.cand_offsets[c], e = F.cand_offsets[c + 1];
-      if (e < b) {
-        *msg = where + "cand_offsets not increasing";
-        return PCD_ERR_INVALID_ARG;
-      }
-      if (e == b) {
-        *msg = where + "label " + std::to_string(c) + " is empty";
-        return PCD_ERR_EMPTY_LABEL;
-      }
+      if (e < b) return bad(PCD_ERR_INVALID_ARG, "cand_offsets not increasing");
+      if (e == b) return bad(PCD_ERR_EMPTY_LABEL, "label " + std::to_string(c) + " is empty");
       int cur = 0;
       for (int j = b; j < e; ++j) {
         const int t = F.cand_tokens[j];
-        if (t < 0 || t >= vocab) {
-          *msg = where + "label token out of range";
-          return PCD_ERR_TOKEN_RANGE;
-        }
-        auto it = nodes[cur].children.find(t);
+        if (t < 0 || t >= vocab) return bad(PCD_ERR_TOKEN_RANGE, "label token out of range");
+        auto& kids = nodes[cur].kids;
+        const auto it = std::lower_bound(kids.begin(), kids.end(), std::make_pair(t, INT_MIN));
         int nx;
-        if (it == nodes[cur].children.end()) {
+        if (it != kids.end() && it->first == t) {
+          nx = it->second;
+        } else {
+          const auto at = it - kids.begin();
           nx = static_cast<int>(nodes.size());
           Node n;
           n.token = t;
           n.parent = cur;
           n.depth = nodes[cur].depth + 1;
-          nodes.push_back(n);
-          nodes[cur].children[t] = nx;
-        } else {
-          nx = it->second;
+          nodes.push_back(std::move(n));  // may move nodes: index, don't hold references across it
+          nodes[cur].kids.insert(nodes[cur].kids.begin() + at, std::make_pair(t, nx));
         }
-        label_nodes[c].push_back(nx);
+        lab_node.push_back(nx);
         cur = nx;
       }
-      if (nodes[cur].label_end) {
-        *msg = where + "label " + std::to_string(c) + " repeats an earlier label";
-        return PCD_ERR_DUPLICATE_LABEL;
-      }
+      lab_start.push_back(static_cast<int>(lab_node.size()));
+      if (nodes[cur].label_end)
+        return bad(PCD_ERR_DUPLICATE_LABEL, "label " + std::to_string(c) + " repeats an earlier label");
       nodes[cur].label_end = true;
     }
     for (const Node& n : nodes)
-      if (n.label_end && !n.children.empty()) {
-        *msg = where + "a label is a strict prefix of another (append its terminator token)";
-        return PCD_ERR_PREFIX_LABEL;
-      }
+      if (n.label_end && !n.kids.empty())
+        return bad(PCD_ERR_PREFIX_LABEL, "a label is a strict prefix of another (append its terminator token)");
 
     // ---- branch tokens: the scaffold, then internal nodes in breadth-first order
     const int S = F.n_scaffold;
@@ -171,11 +143,11 @@ int compile_fields(const pcd_field* fields, int n_fields, int vocab, HostPlan* p
       p->T++;
     }
     nodes[0].branch = t0 + S - 1;
-    std::vector<int> order(1, 0);
+    order.assign(1, 0);
     for (size_t i = 0; i < order.size(); ++i)
-      for (auto& kv : nodes[order[i]].children) order.push_back(kv.second);
+      for (const auto& kv : nodes[order[i]].kids) order.push_back(kv.second);
     for (int id : order) {
-      if (id == 0 || nodes[id].children.empty()) continue;
+      if (id == 0 || nodes[id].kids.empty()) continue;
       Node& n = nodes[id];
       n.branch = p->T;
       p->tok.push_back(n.token);
@@ -184,37 +156,34 @@ int compile_fields(const pcd_field* fields, int n_fields, int vocab, HostPlan* p
       if (rel > p->max_rel) p->max_rel = rel;
       for (int a = 0; a < n_ctx; ++a) p->anc_idx.push_back(c0 + a);
       for (int a = 0; a < S; ++a) p->anc_idx.push_back(t0 + a);
-      std::vector<int> chain;
+      chain.clear();
       for (int x = id; x != 0; x = nodes[x].parent) chain.push_back(nodes[x].branch);
-      for (auto it = chain.rbegin(); it != chain.rend(); ++it) p->anc_idx.push_back(*it);
+      p->anc_idx.insert(p->anc_idx.end(), chain.rbegin(), chain.rend());
       p->anc_off.push_back(static_cast<int32_t>(p->anc_idx.size()));
       p->T++;
     }
     if (n_ctx + S - 1 > p->max_rel) p->max_rel = n_ctx + S - 1;
 
     // ---- readout rows and their child entries
-    std::map<std::pair<int, int>, int> entry_of;  // (node, child token) -> child entry
     p->fld_root.push_back(p->R);
     for (int id : order) {
       Node& n = nodes[id];
-      if (n.children.empty()) continue;
+      if (n.kids.empty()) continue;
       n.row = p->R++;
       p->ro_tok.push_back(n.branch);
-      for (auto& kv : n.children) {
-        entry_of[{id, kv.first}] = p->n_children++;
+      for (const auto& kv : n.kids) {
+        nodes[kv.second].entry = p->n_children++;
         p->ch_tok.push_back(kv.first);
         p->child_row.push_back(n.row);
       }
       p->row_ch.push_back(p->n_children);
     }
 
-    // ---- label paths
+    // ---- label paths: the child entry of every step
     for (int c = 0; c < F.n_cands; ++c) {
-      int parent = 0;
-      for (int nid : label_nodes[c]) {
-        p->path.push_back(entry_of.at({parent, nodes[nid].token}));
+      for (int j = lab_start[c]; j < lab_start[c + 1]; ++j) {
+        p->path.push_back(nodes[lab_node[j]].entry);
         p->n_path++;
-        parent = nid;
       }
       p->lab_off.push_back(p->n_path);
       p->n_labels++;
