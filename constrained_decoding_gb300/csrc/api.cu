@@ -1814,7 +1814,7 @@ int score_impl(pcd_model* m, const pcd_cache* const* caches, const pcd_field* co
   PCD_CUDA(cudaMemcpyAsync(m->down, m->result.p, rbytes, cudaMemcpyDeviceToHost, m->stream));
   {
     const int e = sync_read_error(m);
-    if (e == PCD_OK || e != PCD_ERR_CUDA) m->up_pending = false;  // the stream has drained
+    if (e != PCD_ERR_CUDA) m->up_pending = false;  // the stream has drained
     PCD_TRY(e);
   }
   for (int r = 0; r < n_req; ++r)
